@@ -1,0 +1,426 @@
+/*
+ * tpmlp_oracle.c -- plain fp64 CPU oracle for the t-sharded Megatron MLP block.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA path and must never be used as a
+ * fallback for it.
+ *
+ * What it computes (row convention, every matrix row-major):
+ *   X  [T x d]      tokens x hidden
+ *   W1 [d x dff]    first linear (SwiGLU: the gate projection)
+ *   W3 [d x dff]    SwiGLU up projection (unused for GeLU)
+ *   W2 [dff x d]    second linear
+ *   GeLU  : A = X W1,          H = GeLU(A),            Y = H W2
+ *   SwiGLU: G = X W1, U = X W3, H = U * Swish(G),      Y = H W2
+ * Sources:
+ *   - "Parallelism" tag page of Jiang Yi's homepage, post "megatron-lm",
+ *     Method / FFN: the Linear-GeLU-Linear FFN Y = GeLU(X W1) W2 with
+ *     X in R^{bs x d}, W1 in R^{d x dff}, W2 in R^{dff x d}; the column split of
+ *     W1, the row split of W2 and the SwiGLU form Y = (X W3 . Swish(X W1)) W2.
+ *   - "Tensor parallelism" (brunomaga.github.io), section "Megatron-LM tensor
+ *     parallelism": Megatron_FeedForward calls F.gelu (the exact, erf-based
+ *     GeLU) and the f/g operators.
+ *   - "Parallelism" page, Implementation / SwiGLU listing: the gate is
+ *     silu(w1(x)) multiplied by w3(x), i.e. Swish with beta = 1.
+ * The backward pass is the chain rule applied to the definitions above;
+ * the backward of the seed is an input dY (no loss is formed).
+ *
+ * Unsharded functions compute the block directly.  The sharded functions
+ * follow the pages' per-shard formulation (column shard i owns columns
+ * [o_i, o_i + d_i) of W1/W3 and rows [o_i, o_i + d_i) of W2; forward partial
+ * outputs Z_i are summed by the g operator, backward partial input gradients
+ * dX_i are summed by the f operator) and exist so the tests can check the
+ * identities the pages state.
+ *
+ * Two extra activations, identity and ReLU, are test hooks: they keep
+ * small-integer inputs integral so sharded and unsharded results can be
+ * compared exactly.
+ *
+ * Every loop is a plain definition: no blocking, no reordering beyond the
+ * OpenMP split of independent output rows.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_ACT_GELU 0
+#define ORACLE_ACT_SWIGLU 1
+#define ORACLE_ACT_IDENTITY 2 /* test hook */
+#define ORACLE_ACT_RELU 3     /* test hook */
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG 1
+#define ORACLE_ERR_NOMEM 2
+
+/* ---- activations and their derivatives (scalar, fp64) ------------------ */
+
+/* Standard normal CDF and density. */
+static double norm_cdf(double a) { return 0.5 * (1.0 + erf(a / sqrt(2.0))); }
+static double norm_pdf(double a) { return exp(-0.5 * a * a) / sqrt(2.0 * M_PI); }
+
+/* GeLU(a) = a * Phi(a) (erf form). */
+static double gelu(double a) { return a * norm_cdf(a); }
+/* d/da GeLU(a) = Phi(a) + a * phi(a). */
+static double gelu_grad(double a) { return norm_cdf(a) + a * norm_pdf(a); }
+
+static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
+/* Swish_1(g) = g * sigmoid(g). */
+static double swish(double g) { return g * sigmoid(g); }
+/* d/dg Swish_1(g) = s + g s (1 - s), s = sigmoid(g). */
+static double swish_grad(double g) {
+  double s = sigmoid(g);
+  return s + g * s * (1.0 - s);
+}
+
+/* Elementwise act for the single-input activations (GeLU and the hooks). */
+static double act_value(int act, double a) {
+  switch (act) {
+    case ORACLE_ACT_GELU: return gelu(a);
+    case ORACLE_ACT_IDENTITY: return a;
+    case ORACLE_ACT_RELU: return a > 0.0 ? a : 0.0;
+    default: return NAN;
+  }
+}
+static double act_grad(int act, double a) {
+  switch (act) {
+    case ORACLE_ACT_GELU: return gelu_grad(a);
+    case ORACLE_ACT_IDENTITY: return 1.0;
+    case ORACLE_ACT_RELU: return a > 0.0 ? 1.0 : 0.0;
+    default: return NAN;
+  }
+}
+
+/* ---- plain matrix product ------------------------------------------------
+ * C[m][n] = sum_k A(m,k) * B(k,n) for m < M, n < N, k < K in increasing k.
+ * A(m,k) = A[m*sam + k*sak], B(k,n) = B[k*sbk + n*sbn], C[m*ldc + n].
+ * The strides express transposed operands without copies.                   */
+static void matmul(int64_t M, int64_t N, int64_t K,
+                   const double* A, int64_t sam, int64_t sak,
+                   const double* B, int64_t sbk, int64_t sbn,
+                   double* C, int64_t ldc) {
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t n = 0; n < N; ++n) {
+      double s = 0.0;
+      for (int64_t k = 0; k < K; ++k) s += A[m * sam + k * sak] * B[k * sbk + n * sbn];
+      C[m * ldc + n] = s;
+    }
+  }
+}
+
+static int valid_act(int act) {
+  return act == ORACLE_ACT_GELU || act == ORACLE_ACT_SWIGLU || act == ORACLE_ACT_IDENTITY ||
+         act == ORACLE_ACT_RELU;
+}
+
+/* ---- unsharded forward ----------------------------------------------------
+ * Outputs: A (SwiGLU: G) [T x dff], U [T x dff] (SwiGLU only, may be NULL
+ * otherwise), H [T x dff], Y [T x d].                                        */
+int oracle_forward(int64_t T, int64_t d, int64_t dff, int act, const double* X, const double* W1,
+                   const double* W3, const double* W2, double* A, double* U, double* H, double* Y) {
+  if (T < 0 || d < 1 || dff < 1 || !valid_act(act) || !X || !W1 || !W2 || !A || !H || !Y)
+    return ORACLE_ERR_ARG;
+  if (act == ORACLE_ACT_SWIGLU && (!W3 || !U)) return ORACLE_ERR_ARG;
+  /* A = X W1 */
+  matmul(T, dff, d, X, d, 1, W1, dff, 1, A, dff);
+  if (act == ORACLE_ACT_SWIGLU) {
+    /* U = X W3; H = U * Swish(G) */
+    matmul(T, dff, d, X, d, 1, W3, dff, 1, U, dff);
+    for (int64_t i = 0; i < T * dff; ++i) H[i] = U[i] * swish(A[i]);
+  } else {
+    for (int64_t i = 0; i < T * dff; ++i) H[i] = act_value(act, A[i]);
+  }
+  /* Y = H W2 */
+  matmul(T, d, dff, H, dff, 1, W2, d, 1, Y, d);
+  return ORACLE_OK;
+}
+
+/* ---- unsharded backward ---------------------------------------------------
+ * Given dY = dL/dY, returns dX, dW1, dW3 (SwiGLU only), dW2 and the
+ * activation gradient dA (SwiGLU: dG) / dU, recomputing the forward from X.
+ * Any of dAct/dUo may be NULL if not wanted.                                 */
+int oracle_backward(int64_t T, int64_t d, int64_t dff, int act, const double* X, const double* W1,
+                    const double* W3, const double* W2, const double* dY, double* dX, double* dW1,
+                    double* dW3, double* dW2, double* dAct, double* dUo) {
+  if (T < 0 || d < 1 || dff < 1 || !valid_act(act) || !X || !W1 || !W2 || !dY || !dX || !dW1 || !dW2)
+    return ORACLE_ERR_ARG;
+  int swiglu = act == ORACLE_ACT_SWIGLU;
+  if (swiglu && (!W3 || !dW3)) return ORACLE_ERR_ARG;
+  size_t n = (size_t)(T * dff);
+  size_t nb = n ? n : 1;
+  double* A = (double*)malloc(nb * sizeof(double));
+  double* U = swiglu ? (double*)malloc(nb * sizeof(double)) : NULL;
+  double* H = (double*)malloc(nb * sizeof(double));
+  double* dH = (double*)malloc(nb * sizeof(double));
+  double* dA = (double*)malloc(nb * sizeof(double));
+  double* dU = swiglu ? (double*)malloc(nb * sizeof(double)) : NULL;
+  double* Y = (double*)malloc((size_t)(T * d ? T * d : 1) * sizeof(double));
+  int rc = ORACLE_ERR_NOMEM;
+  if (!A || !H || !dH || !dA || !Y || (swiglu && (!U || !dU))) goto done;
+  rc = oracle_forward(T, d, dff, act, X, W1, W3, W2, A, U, H, Y);
+  if (rc) goto done;
+  /* dH = dY W2^T : dH[r][j] = sum_n dY[r][n] W2[j][n] */
+  matmul(T, dff, d, dY, d, 1, W2, 1, d, dH, dff);
+  if (swiglu) {
+    /* H = U * Swish(G): dU = dH * Swish(G), dG = dH * U * Swish'(G) */
+    for (size_t i = 0; i < n; ++i) {
+      dU[i] = dH[i] * swish(A[i]);
+      dA[i] = dH[i] * U[i] * swish_grad(A[i]);
+    }
+  } else {
+    for (size_t i = 0; i < n; ++i) dA[i] = dH[i] * act_grad(act, A[i]);
+  }
+  /* dW2 = H^T dY : dW2[j][n] = sum_r H[r][j] dY[r][n] */
+  matmul(dff, d, T, H, 1, dff, dY, d, 1, dW2, d);
+  /* dW1 = X^T dA : dW1[k][j] = sum_r X[r][k] dA[r][j] */
+  matmul(d, dff, T, X, 1, d, dA, dff, 1, dW1, dff);
+  /* dX = dA W1^T (+ dU W3^T) */
+  matmul(T, d, dff, dA, dff, 1, W1, 1, dff, dX, d);
+  if (swiglu) {
+    matmul(d, dff, T, X, 1, d, dU, dff, 1, dW3, dff);
+    double* dX3 = (double*)malloc((size_t)(T * d ? T * d : 1) * sizeof(double));
+    if (!dX3) { rc = ORACLE_ERR_NOMEM; goto done; }
+    matmul(T, d, dff, dU, dff, 1, W3, 1, dff, dX3, d);
+    for (int64_t i = 0; i < T * d; ++i) dX[i] += dX3[i];
+    free(dX3);
+  }
+  if (dAct) memcpy(dAct, dA, n * sizeof(double));
+  if (dUo && swiglu) memcpy(dUo, dU, n * sizeof(double));
+  rc = ORACLE_OK;
+done:
+  free(A); free(U); free(H); free(dH); free(dA); free(dU); free(Y);
+  return rc;
+}
+
+/* ---- sharded forward (the pages' per-shard formulation) ------------------
+ * Shard i: A_i = X W1_i, H_i = act(A_i) (SwiGLU: U_i * Swish(X W1_i) with
+ * U_i = X W3_i), Z_i = H_i W2_i; the g operator (forward all-reduce) gives
+ * Y = sum_i Z_i, summed in shard order.  W1_i, W3_i are [d x d_i], W2_i is
+ * [d_i x d], H_i is [T x d_i] (optional output; pass NULL to skip).          */
+int oracle_forward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i, int act,
+                           const double* X, const double* const* W1_i, const double* const* W3_i,
+                           const double* const* W2_i, double* Y, double* const* H_i) {
+  if (T < 0 || d < 1 || t < 1 || !d_i || !valid_act(act) || !X || !W1_i || !W2_i || !Y)
+    return ORACLE_ERR_ARG;
+  int swiglu = act == ORACLE_ACT_SWIGLU;
+  if (swiglu && !W3_i) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < T * d; ++i) Y[i] = 0.0;
+  for (int32_t s = 0; s < t; ++s) {
+    int64_t di = d_i[s];
+    if (di < 1) return ORACLE_ERR_ARG;
+    size_t n = (size_t)(T * di ? T * di : 1);
+    double* A = (double*)malloc(n * sizeof(double));
+    double* U = swiglu ? (double*)malloc(n * sizeof(double)) : NULL;
+    double* H = (double*)malloc(n * sizeof(double));
+    double* Z = (double*)malloc((size_t)(T * d ? T * d : 1) * sizeof(double));
+    if (!A || !H || !Z || (swiglu && !U)) {
+      free(A); free(U); free(H); free(Z);
+      return ORACLE_ERR_NOMEM;
+    }
+    matmul(T, di, d, X, d, 1, W1_i[s], di, 1, A, di);
+    if (swiglu) {
+      matmul(T, di, d, X, d, 1, W3_i[s], di, 1, U, di);
+      for (int64_t i = 0; i < T * di; ++i) H[i] = U[i] * swish(A[i]);
+    } else {
+      for (int64_t i = 0; i < T * di; ++i) H[i] = act_value(act, A[i]);
+    }
+    matmul(T, d, di, H, di, 1, W2_i[s], d, 1, Z, d);
+    for (int64_t i = 0; i < T * d; ++i) Y[i] += Z[i]; /* g: sum of partial outputs */
+    if (H_i && H_i[s]) memcpy(H_i[s], H, (size_t)(T * di) * sizeof(double));
+    free(A); free(U); free(H); free(Z);
+  }
+  return ORACLE_OK;
+}
+
+/* ---- sharded backward ------------------------------------------------------
+ * g backward is the identity (every shard receives the same dY); each shard
+ * forms dH_i = dY W2_i^T, dA_i, dW2_i = H_i^T dY, dW1_i = X^T dA_i
+ * (SwiGLU: dW3_i = X^T dU_i) and its partial input gradient
+ * dX_i = dA_i W1_i^T (+ dU_i W3_i^T); f backward (all-reduce) gives
+ * dX = sum_i dX_i, summed in shard order.                                    */
+int oracle_backward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i, int act,
+                            const double* X, const double* const* W1_i, const double* const* W3_i,
+                            const double* const* W2_i, const double* dY, double* dX,
+                            double* const* dW1_i, double* const* dW3_i, double* const* dW2_i) {
+  if (T < 0 || d < 1 || t < 1 || !d_i || !valid_act(act) || !X || !W1_i || !W2_i || !dY || !dX ||
+      !dW1_i || !dW2_i)
+    return ORACLE_ERR_ARG;
+  int swiglu = act == ORACLE_ACT_SWIGLU;
+  if (swiglu && (!W3_i || !dW3_i)) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < T * d; ++i) dX[i] = 0.0;
+  for (int32_t s = 0; s < t; ++s) {
+    int64_t di = d_i[s];
+    if (di < 1) return ORACLE_ERR_ARG;
+    size_t n = (size_t)(T * di ? T * di : 1);
+    size_t nx = (size_t)(T * d ? T * d : 1);
+    double* A = (double*)malloc(n * sizeof(double));
+    double* U = swiglu ? (double*)malloc(n * sizeof(double)) : NULL;
+    double* H = (double*)malloc(n * sizeof(double));
+    double* dH = (double*)malloc(n * sizeof(double));
+    double* dA = (double*)malloc(n * sizeof(double));
+    double* dU = swiglu ? (double*)malloc(n * sizeof(double)) : NULL;
+    double* dXs = (double*)malloc(nx * sizeof(double));
+    double* dX3 = swiglu ? (double*)malloc(nx * sizeof(double)) : NULL;
+    int bad = !A || !H || !dH || !dA || !dXs || (swiglu && (!U || !dU || !dX3));
+    if (!bad) {
+      matmul(T, di, d, X, d, 1, W1_i[s], di, 1, A, di);
+      if (swiglu) {
+        matmul(T, di, d, X, d, 1, W3_i[s], di, 1, U, di);
+        for (int64_t i = 0; i < T * di; ++i) H[i] = U[i] * swish(A[i]);
+      } else {
+        for (int64_t i = 0; i < T * di; ++i) H[i] = act_value(act, A[i]);
+      }
+      matmul(T, di, d, dY, d, 1, W2_i[s], 1, d, dH, di);
+      if (swiglu) {
+        for (int64_t i = 0; i < T * di; ++i) {
+          dU[i] = dH[i] * swish(A[i]);
+          dA[i] = dH[i] * U[i] * swish_grad(A[i]);
+        }
+      } else {
+        for (int64_t i = 0; i < T * di; ++i) dA[i] = dH[i] * act_grad(act, A[i]);
+      }
+      matmul(di, d, T, H, 1, di, dY, d, 1, dW2_i[s], d);
+      matmul(d, di, T, X, 1, d, dA, di, 1, dW1_i[s], di);
+      matmul(T, d, di, dA, di, 1, W1_i[s], 1, di, dXs, d);
+      if (swiglu) {
+        matmul(d, di, T, X, 1, d, dU, di, 1, dW3_i[s], di);
+        matmul(T, d, di, dU, di, 1, W3_i[s], 1, di, dX3, d);
+        for (int64_t i = 0; i < T * d; ++i) dXs[i] += dX3[i];
+      }
+      for (int64_t i = 0; i < T * d; ++i) dX[i] += dXs[i]; /* f: sum of partial dX */
+    }
+    free(A); free(U); free(H); free(dH); free(dA); free(dU); free(dXs); free(dX3);
+    if (bad) return ORACLE_ERR_NOMEM;
+  }
+  return ORACLE_OK;
+}
+
+/* ---- sampled outputs for large problems -----------------------------------
+ * oracle_rows: Y[r, :] and dX[r, :] for the listed token rows r, each from
+ * its own definition (a token's forward and input gradient depend only on
+ * that token's row of X and dY).  Y_rows and dX_rows are [nrows x d].       */
+int oracle_rows(int64_t T, int64_t d, int64_t dff, int act, const double* X, const double* W1,
+                const double* W3, const double* W2, const double* dY, int64_t nrows,
+                const int64_t* rows, double* Y_rows, double* dX_rows) {
+  if (T < 1 || d < 1 || dff < 1 || !valid_act(act) || nrows < 0 || !rows || !X || !W1 || !W2 ||
+      !dY || !Y_rows || !dX_rows)
+    return ORACLE_ERR_ARG;
+  int swiglu = act == ORACLE_ACT_SWIGLU;
+  if (swiglu && !W3) return ORACLE_ERR_ARG;
+  for (int64_t q = 0; q < nrows; ++q)
+    if (rows[q] < 0 || rows[q] >= T) return ORACLE_ERR_ARG;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t q = 0; q < nrows; ++q) {
+    const double* x = X + rows[q] * d;
+    const double* g = dY + rows[q] * d;
+    double* a = (double*)malloc((size_t)dff * 5 * sizeof(double));
+    if (!a) { err = 1; continue; }
+    double* u = a + dff;
+    double* h = a + 2 * dff;
+    double* dh = a + 3 * dff;
+    double* da = a + 4 * dff;
+    for (int64_t j = 0; j < dff; ++j) {
+      double s = 0.0, s3 = 0.0, sg = 0.0;
+      for (int64_t k = 0; k < d; ++k) {
+        s += x[k] * W1[k * dff + j];
+        if (swiglu) s3 += x[k] * W3[k * dff + j];
+      }
+      for (int64_t n = 0; n < d; ++n) sg += g[n] * W2[j * d + n];
+      a[j] = s;
+      u[j] = s3;
+      dh[j] = sg;
+      if (swiglu) {
+        h[j] = s3 * swish(s);
+        da[j] = sg * s3 * swish_grad(s);
+      } else {
+        h[j] = act_value(act, s);
+        da[j] = sg * act_grad(act, s);
+      }
+    }
+    for (int64_t n = 0; n < d; ++n) {
+      double y = 0.0, dx = 0.0;
+      for (int64_t j = 0; j < dff; ++j) {
+        y += h[j] * W2[j * d + n];
+        dx += da[j] * W1[n * dff + j];
+        if (swiglu) dx += dh[j] * swish(a[j]) * W3[n * dff + j];
+      }
+      Y_rows[q * d + n] = y;
+      dX_rows[q * d + n] = dx;
+    }
+    free(a);
+  }
+  return err ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* oracle_wgrad_units: for the listed hidden units j (columns of W1/W3, rows
+ * of W2), dW1[:, j], dW3[:, j] (SwiGLU) and dW2[j, :], each a sum over all T
+ * tokens of its definition.  Outputs are [nunits x d]: dW1_cols[q*d + k] =
+ * dW1[k][j_q], dW2_rows[q*d + n] = dW2[j_q][n].                              */
+int oracle_wgrad_units(int64_t T, int64_t d, int64_t dff, int act, const double* X, const double* W1,
+                       const double* W3, const double* W2, const double* dY, int64_t nunits,
+                       const int64_t* units, double* dW1_cols, double* dW3_cols, double* dW2_rows) {
+  if (T < 0 || d < 1 || dff < 1 || !valid_act(act) || nunits < 0 || !units || !X || !W1 || !W2 ||
+      !dY || !dW1_cols || !dW2_rows)
+    return ORACLE_ERR_ARG;
+  int swiglu = act == ORACLE_ACT_SWIGLU;
+  if (swiglu && (!W3 || !dW3_cols)) return ORACLE_ERR_ARG;
+  for (int64_t q = 0; q < nunits; ++q)
+    if (units[q] < 0 || units[q] >= dff) return ORACLE_ERR_ARG;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t q = 0; q < nunits; ++q) {
+    int64_t j = units[q];
+    size_t nt = (size_t)(T ? T : 1);
+    double* h = (double*)malloc(nt * 3 * sizeof(double));
+    if (!h) { err = 1; continue; }
+    double* da = h + nt;
+    double* du = h + 2 * nt;
+    for (int64_t r = 0; r < T; ++r) {
+      double a = 0.0, u = 0.0, dh = 0.0;
+      for (int64_t k = 0; k < d; ++k) {
+        a += X[r * d + k] * W1[k * dff + j];
+        if (swiglu) u += X[r * d + k] * W3[k * dff + j];
+      }
+      for (int64_t n = 0; n < d; ++n) dh += dY[r * d + n] * W2[j * d + n];
+      if (swiglu) {
+        h[r] = u * swish(a);
+        da[r] = dh * u * swish_grad(a);
+        du[r] = dh * swish(a);
+      } else {
+        h[r] = act_value(act, a);
+        da[r] = dh * act_grad(act, a);
+        du[r] = 0.0;
+      }
+    }
+    for (int64_t k = 0; k < d; ++k) {
+      double s1 = 0.0, s3 = 0.0, s2 = 0.0;
+      for (int64_t r = 0; r < T; ++r) {
+        s1 += X[r * d + k] * da[r];
+        if (swiglu) s3 += X[r * d + k] * du[r];
+        s2 += h[r] * dY[r * d + k];
+      }
+      dW1_cols[q * d + k] = s1;
+      if (swiglu) dW3_cols[q * d + k] = s3;
+      dW2_rows[q * d + k] = s2;
+    }
+    free(h);
+  }
+  return err ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* Scalar access for the closed-form pins (value of the activation, its
+ * derivative, for act in {GeLU, Swish-as-SwiGLU-gate, identity, ReLU}).      */
+double oracle_act_value(int act, double a) { return act == ORACLE_ACT_SWIGLU ? swish(a) : act_value(act, a); }
+double oracle_act_grad(int act, double a) { return act == ORACLE_ACT_SWIGLU ? swish_grad(a) : act_grad(act, a); }
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

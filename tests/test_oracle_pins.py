@@ -1,0 +1,358 @@
+"""Pins of the fp64 oracle to things other than itself (CPU only).
+
+Each test ties an oracle function to something the pages or the mathematics
+fix: tabulated values of the normal and logistic functions, hand-worked
+examples, the split identities the pages state (exact on small integers),
+central finite differences, an independent numpy implementation, and, last,
+planted mistakes compiled into copies of the oracle that these pins must
+catch.
+"""
+import os
+import re
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import np_oracle
+import synthetic_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _table(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append([float(v) for v in line.split()])
+    return rows
+
+
+def _fixture(name):
+    out = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.split("#")[0].strip()
+        if "=" not in line:
+            continue
+        k, v = (p.strip() for p in line.split("=", 1))
+        out[k] = np.array([[float(x) for x in row.split()] for row in v.split(";")])
+    return out
+
+
+# ---------------------------------------------------------------- closed forms
+
+def check_normal_table(o):
+    """max relative error of GeLU and GeLU' against the normal-table values."""
+    err = 0.0
+    for x, P, Z in _table("normal_table.txt"):
+        for xs, Ps in ((x, P), (-x, 1.0 - P)):
+            g = o.act_value("gelu", xs)
+            gp = o.act_grad("gelu", xs)
+            err = max(err, abs(g - xs * Ps) / max(1.0, abs(xs * Ps)))
+            err = max(err, abs(gp - (Ps + xs * Z)) / max(1.0, abs(Ps + xs * Z)))
+    return err
+
+
+def test_gelu_matches_normal_table():
+    assert check_normal_table(oracle.default()) < 2e-15
+
+
+def test_swish_matches_logistic_table():
+    for g, s in _table("logistic_table.txt"):
+        assert abs(oracle.act_value("swiglu", g) - g * s) < 2e-15
+        assert abs(oracle.act_grad("swiglu", g) - (s + g * s * (1 - s))) < 2e-15
+
+
+def test_activation_special_values():
+    assert oracle.act_value("gelu", 0.0) == 0.0
+    assert oracle.act_grad("gelu", 0.0) == 0.5
+    assert oracle.act_value("swiglu", 0.0) == 0.0
+    assert oracle.act_grad("swiglu", 0.0) == 0.5
+    rng = np.random.default_rng(3)
+    for x in rng.normal(0, 3, 50):
+        # GeLU(x) - GeLU(-x) = x (P(x) + P(-x) = 1); the same holds for Swish.
+        assert abs(oracle.act_value("gelu", x) - oracle.act_value("gelu", -x) - x) < 1e-14 * max(1, abs(x))
+        assert abs(oracle.act_value("swiglu", x) - oracle.act_value("swiglu", -x) - x) < 1e-14 * max(1, abs(x))
+    assert abs(oracle.act_value("gelu", 12.0) - 12.0) < 1e-15 * 12
+    assert abs(oracle.act_value("gelu", -12.0)) < 1e-30
+    assert oracle.act_value("relu", -2.0) == 0.0 and oracle.act_grad("relu", 3.0) == 1.0
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_hand_worked_identity_example_unsharded_and_sharded():
+    f = _fixture("tiny_mlp_identity_t2.txt")
+    fw = oracle.forward(f["X"], f["W1"], f["W2"], act="identity")
+    bw = oracle.backward(f["X"], f["W1"], f["W2"], f["dY"], act="identity")
+    assert np.array_equal(fw["Y"], f["Y"])
+    assert np.array_equal(bw["dX"], f["dX"])
+    assert np.array_equal(bw["dW1"], f["dW1"])
+    assert np.array_equal(bw["dW2"], f["dW2"])
+    W1_i = [f["W1"][:, 0:2], f["W1"][:, 2:4]]
+    W2_i = [f["W2"][0:2], f["W2"][2:4]]
+    Y, _ = oracle.forward_sharded(f["X"], W1_i, W2_i, act="identity")
+    b = oracle.backward_sharded(f["X"], W1_i, W2_i, f["dY"], act="identity")
+    assert np.array_equal(Y, f["Y"])
+    assert np.array_equal(b["dX"], f["dX"])
+    assert np.array_equal(np.concatenate(b["dW1_i"], 1), f["dW1"])
+    assert np.array_equal(np.concatenate(b["dW2_i"], 0), f["dW2"])
+
+
+def test_hand_worked_gelu_example():
+    f = _fixture("tiny_mlp_gelu.txt")
+    fw = oracle.forward(f["X"], f["W1"], f["W2"])
+    bw = oracle.backward(f["X"], f["W1"], f["W2"], f["dY"])
+    for got, want in ((fw["Y"], f["Y"]), (bw["dX"], f["dX"]), (bw["dW1"], f["dW1"]), (bw["dW2"], f["dW2"])):
+        np.testing.assert_allclose(got, want, rtol=0, atol=4e-16)
+
+
+# ---------------------------------------------------------------- split identities
+
+def test_column_identity_is_bitwise():
+    """[act(X W1_i)]_i equals act(X W1) bit for bit (same dot products, same order)."""
+    rng = np.random.default_rng(11)
+    T, d, d_i = 9, 13, [5, 8, 3]
+    X = rng.normal(size=(T, d)); W1 = rng.normal(size=(d, sum(d_i))); W2 = rng.normal(size=(sum(d_i), d))
+    W3 = rng.normal(size=(d, sum(d_i)))
+    for act in ("gelu", "swiglu"):
+        full = oracle.forward(X, W1, W2, act=act, W3=W3)
+        sl = si.shard_slices(d_i)
+        _, H_i = oracle.forward_sharded(X, [W1[:, a:b] for a, b in sl], [W2[a:b] for a, b in sl], act=act,
+                                        W3_i=[W3[:, a:b] for a, b in sl] if act == "swiglu" else None)
+        assert np.array_equal(np.concatenate(H_i, axis=1), full["H"])
+
+
+@pytest.mark.parametrize("t", [1, 2, 4, 8])
+@pytest.mark.parametrize("act", ["identity", "relu"])
+def test_row_identity_exact_on_small_integers(t, act):
+    """Sharded Y, dX, dW equal the unsharded ones exactly (integers below 2^53)."""
+    inp = si.small_int_inputs(4, 8, [16 // t] * t, act)
+    full_f = oracle.forward(inp.X, inp.W1, inp.W2, act=act)
+    full_b = oracle.backward(inp.X, inp.W1, inp.W2, inp.dY, act=act)
+    Y, _ = oracle.forward_sharded(inp.X, inp.W1_i, inp.W2_i, act=act)
+    b = oracle.backward_sharded(inp.X, inp.W1_i, inp.W2_i, inp.dY, act=act)
+    assert np.array_equal(Y, full_f["Y"])
+    assert np.array_equal(b["dX"], full_b["dX"])
+    assert np.array_equal(np.concatenate(b["dW1_i"], 1), full_b["dW1"])
+    assert np.array_equal(np.concatenate(b["dW2_i"], 0), full_b["dW2"])
+    assert np.all(full_f["Y"] == np.round(full_f["Y"]))  # the integers stayed integers
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("d_i", [[16], [8, 8], [3, 5, 8], [4, 4, 4, 4], [1, 2, 3, 4, 6]])
+def test_sharded_equals_unsharded_smooth_acts(act, d_i):
+    rng = np.random.default_rng(5)
+    T, d = 6, 7
+    dff = sum(d_i)
+    X = rng.normal(size=(T, d)); W1 = rng.normal(size=(d, dff)) * 0.3; W2 = rng.normal(size=(dff, d)) * 0.3
+    W3 = rng.normal(size=(d, dff)) * 0.3 if act == "swiglu" else None
+    dY = rng.normal(size=(T, d))
+    sl = si.shard_slices(d_i)
+    W1_i = [W1[:, a:b] for a, b in sl]; W2_i = [W2[a:b] for a, b in sl]
+    W3_i = [W3[:, a:b] for a, b in sl] if W3 is not None else None
+    full_f = oracle.forward(X, W1, W2, act=act, W3=W3)
+    full_b = oracle.backward(X, W1, W2, dY, act=act, W3=W3)
+    Y, _ = oracle.forward_sharded(X, W1_i, W2_i, act=act, W3_i=W3_i)
+    b = oracle.backward_sharded(X, W1_i, W2_i, dY, act=act, W3_i=W3_i)
+    np.testing.assert_allclose(Y, full_f["Y"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(b["dX"], full_b["dX"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(np.concatenate(b["dW1_i"], 1), full_b["dW1"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(np.concatenate(b["dW2_i"], 0), full_b["dW2"], rtol=1e-13, atol=1e-13)
+    if act == "swiglu":
+        np.testing.assert_allclose(np.concatenate(b["dW3_i"], 1), full_b["dW3"], rtol=1e-13, atol=1e-13)
+
+
+def test_t1_is_the_plain_mlp():
+    """t = 1: the sharded form is the textbook Linear-act-Linear block."""
+    rng = np.random.default_rng(9)
+    X = rng.normal(size=(5, 6)); W1 = rng.normal(size=(6, 10)); W2 = rng.normal(size=(10, 6))
+    Y, _ = oracle.forward_sharded(X, [W1], [W2])
+    assert np.array_equal(Y, oracle.forward(X, W1, W2)["Y"])
+
+
+# ---------------------------------------------------------------- finite differences
+
+def fd_check(o, act, seed=1, h=1e-6):
+    """max over X, W1, W3, W2 of |analytic - central difference| / max|analytic|,
+    for L = <dY, Y> at T=3, d=5, unequal shards d_i=[3,4]."""
+    rng = np.random.default_rng(seed)
+    T, d, dff = 3, 5, 7
+    P = {"X": rng.normal(size=(T, d)), "W1": rng.normal(size=(d, dff)) * 0.5,
+         "W2": rng.normal(size=(dff, d)) * 0.5}
+    if act == "swiglu":
+        P["W3"] = rng.normal(size=(d, dff)) * 0.5
+    dY = rng.normal(size=(T, d))
+
+    def loss(p):
+        return float(np.sum(dY * o.forward(p["X"], p["W1"], p["W2"], act=act, W3=p.get("W3"))["Y"]))
+
+    g = o.backward(P["X"], P["W1"], P["W2"], dY, act=act, W3=P.get("W3"))
+    grads = {"X": g["dX"], "W1": g["dW1"], "W2": g["dW2"], "W3": g["dW3"]}
+    worst = 0.0
+    for name, val in P.items():
+        num = np.zeros_like(val)
+        for idx in np.ndindex(val.shape):
+            p_plus = {k: v.copy() for k, v in P.items()}; p_plus[name][idx] += h
+            p_minus = {k: v.copy() for k, v in P.items()}; p_minus[name][idx] -= h
+            num[idx] = (loss(p_plus) - loss(p_minus)) / (2 * h)
+        worst = max(worst, float(np.max(np.abs(num - grads[name])) / np.max(np.abs(grads[name]))))
+    return worst
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_finite_differences(act):
+    assert fd_check(oracle.default(), act) < 1e-7
+
+
+def test_sharded_backward_finite_differences():
+    """The f-sum (backward of the identity f) gives the true input gradient."""
+    rng = np.random.default_rng(2)
+    X = rng.normal(size=(3, 5)); W1 = rng.normal(size=(5, 7)) * 0.5; W2 = rng.normal(size=(7, 5)) * 0.5
+    dY = rng.normal(size=(3, 5))
+    sl = si.shard_slices([3, 4])
+    W1_i = [W1[:, a:b] for a, b in sl]; W2_i = [W2[a:b] for a, b in sl]
+    b = oracle.backward_sharded(X, W1_i, W2_i, dY)
+    h = 1e-6
+    num = np.zeros_like(X)
+    for idx in np.ndindex(X.shape):
+        Xp = X.copy(); Xp[idx] += h
+        Xm = X.copy(); Xm[idx] -= h
+        yp, _ = oracle.forward_sharded(Xp, W1_i, W2_i)
+        ym, _ = oracle.forward_sharded(Xm, W1_i, W2_i)
+        num[idx] = np.sum(dY * (yp - ym)) / (2 * h)
+    assert np.max(np.abs(num - b["dX"])) / np.max(np.abs(b["dX"])) < 1e-7
+
+
+# ---------------------------------------------------------------- special inputs
+
+def test_zero_inputs():
+    rng = np.random.default_rng(4)
+    T, d, dff = 4, 6, 8
+    W1 = rng.normal(size=(d, dff)); W2 = rng.normal(size=(dff, d)); W3 = rng.normal(size=(d, dff))
+    for act in ("gelu", "swiglu"):
+        b = oracle.backward(np.zeros((T, d)), W1, W2, rng.normal(size=(T, d)), act=act, W3=W3)
+        assert np.all(oracle.forward(np.zeros((T, d)), W1, W2, act=act, W3=W3)["Y"] == 0)
+        assert np.all(b["dW2"] == 0) and np.all(b["dW1"] == 0)
+        b0 = oracle.backward(rng.normal(size=(T, d)), W1, W2, np.zeros((T, d)), act=act, W3=W3)
+        for k in ("dX", "dW1", "dW2"):
+            assert np.all(b0[k] == 0)
+
+
+def test_empty_token_batch():
+    rng = np.random.default_rng(4)
+    W1 = rng.normal(size=(6, 8)); W2 = rng.normal(size=(8, 6))
+    b = oracle.backward(np.zeros((0, 6)), W1, W2, np.zeros((0, 6)))
+    assert b["dX"].shape == (0, 6)
+    assert np.all(b["dW1"] == 0) and np.all(b["dW2"] == 0)
+
+
+def test_flop_count_matches_pages():
+    """Forward MLP FLOPs with dff = 4h are 16 T h^2, the MLP part of the pages'
+    24 h^2 per token (section 3.4 of the network primer); fwd+bwd is 3x."""
+    h, T = 3072, 16384
+    fwd = 2 * T * h * (4 * h) * 2  # two GEMMs of 2 T h dff
+    assert fwd == 16 * T * h * h
+    assert 3 * fwd == 12 * T * h * (4 * h)
+
+
+# ---------------------------------------------------------------- independent cross-check
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("shape", [(1, 1, 1), (5, 7, 9), (17, 12, 40), (33, 64, 96)])
+def test_c_oracle_matches_numpy_oracle(act, shape):
+    T, d, dff = shape
+    rng = np.random.default_rng(T * 100 + d)
+    X = rng.normal(size=(T, d)); W1 = rng.normal(size=(d, dff)) * 0.2; W2 = rng.normal(size=(dff, d)) * 0.2
+    W3 = rng.normal(size=(d, dff)) * 0.2
+    dY = rng.normal(size=(T, d))
+    c_f = oracle.forward(X, W1, W2, act=act, W3=W3)
+    c_b = oracle.backward(X, W1, W2, dY, act=act, W3=W3)
+    n_f = np_oracle.forward(X, W1, W2, act=act, W3=W3)
+    n_b = np_oracle.backward(X, W1, W2, dY, act=act, W3=W3)
+    for a, b in ((c_f["Y"], n_f["Y"]), (c_f["H"], n_f["H"]), (c_b["dX"], n_b["dX"]), (c_b["dW1"], n_b["dW1"]),
+                 (c_b["dW2"], n_b["dW2"]), (c_b["dA"], n_b["dA"])):
+        assert np.max(np.abs(a - b)) <= 1e-12 * max(1.0, np.max(np.abs(b)))
+    if act == "swiglu":
+        assert np.max(np.abs(c_b["dW3"] - n_b["dW3"])) <= 1e-12 * max(1.0, np.max(np.abs(n_b["dW3"])))
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_sampled_rows_and_units_match_full(act):
+    rng = np.random.default_rng(8)
+    T, d, dff = 37, 24, 40
+    X = rng.normal(size=(T, d)); W1 = rng.normal(size=(d, dff)) * 0.2; W2 = rng.normal(size=(dff, d)) * 0.2
+    W3 = rng.normal(size=(d, dff)) * 0.2 if act == "swiglu" else None
+    dY = rng.normal(size=(T, d))
+    full_f = np_oracle.forward(X, W1, W2, act=act, W3=W3)
+    full_b = np_oracle.backward(X, W1, W2, dY, act=act, W3=W3)
+    r = np.array([0, 5, 36, 17])
+    Yr, dXr = oracle.rows(X, W1, W2, dY, r, act=act, W3=W3)
+    np.testing.assert_allclose(Yr, full_f["Y"][r], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dXr, full_b["dX"][r], rtol=0, atol=1e-12)
+    u = np.array([0, 39, 13])
+    c1, c3, c2 = oracle.wgrad_units(X, W1, W2, dY, u, act=act, W3=W3)
+    np.testing.assert_allclose(c1, full_b["dW1"][:, u].T, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(c2, full_b["dW2"][u, :], rtol=0, atol=1e-11)
+    if act == "swiglu":
+        np.testing.assert_allclose(c3, full_b["dW3"][:, u].T, rtol=0, atol=1e-11)
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+_SRC = os.path.join(os.path.dirname(oracle.__file__), "tpmlp_oracle.c")
+
+# (name, text to find, replacement, pin that must fail)
+MUTANTS = [
+    ("gelu_grad_drops_x_phi", "return norm_cdf(a) + a * norm_pdf(a);", "return norm_cdf(a);", "fd_gelu"),
+    ("tanh_gelu", "static double gelu(double a) { return a * norm_cdf(a); }",
+     "static double gelu(double a) { return 0.5 * a * (1.0 + tanh(0.7978845608028654 * (a + 0.044715 * a * a * a))); }",
+     "table"),
+    ("dW1_uses_dH", "matmul(d, dff, T, X, 1, d, dA, dff, 1, dW1, dff);",
+     "matmul(d, dff, T, X, 1, d, dH, dff, 1, dW1, dff);", "fd_gelu"),
+    ("dH_untransposed_W2", "matmul(T, dff, d, dY, d, 1, W2, 1, d, dH, dff);",
+     "matmul(T, dff, d, dY, d, 1, W2, d, 1, dH, dff);", "fd_gelu"),
+    ("swiglu_gate_up_swapped", "dU[i] = dH[i] * swish(A[i]);\n      dA[i] = dH[i] * U[i] * swish_grad(A[i]);",
+     "dU[i] = dH[i] * swish(U[i]);\n      dA[i] = dH[i] * U[i] * swish_grad(A[i]);", "fd_swiglu"),
+    ("g_sum_drops_partials", "Y[i] += Z[i]; /* g: sum of partial outputs */", "Y[i] = Z[i];", "row_identity"),
+    ("f_sum_drops_partials", "dX[i] += dXs[i]; /* f: sum of partial dX */", "dX[i] = dXs[i];", "row_identity"),
+    ("swish_grad_sign", "return s + g * s * (1.0 - s);", "return s - g * s * (1.0 - s);", "fd_swiglu"),
+]
+
+
+def _row_identity_error(o):
+    inp = si.small_int_inputs(4, 8, [4, 4, 8], "relu")
+    Y, _ = o.forward_sharded(inp.X, inp.W1_i, inp.W2_i, act="relu")
+    b = o.backward_sharded(inp.X, inp.W1_i, inp.W2_i, inp.dY, act="relu")
+    ff = o.forward(inp.X, inp.W1, inp.W2, act="relu")
+    fb = o.backward(inp.X, inp.W1, inp.W2, inp.dY, act="relu")
+    return max(np.max(np.abs(Y - ff["Y"])), np.max(np.abs(b["dX"] - fb["dX"])))
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(mutant, tmp_path):
+    name, find, repl, pin = mutant
+    src = open(_SRC).read()
+    assert src.count(find) == 1, f"mutation site for {name} not found exactly once"
+    msrc = tmp_path / "mutant.c"
+    msrc.write_text(src.replace(find, repl))
+    lib = oracle.build(force=True, src=str(msrc), out=str(tmp_path / "libmutant.so"))
+    o = oracle.load_variant(lib)
+    if pin == "fd_gelu":
+        assert fd_check(o, "gelu") > 1e-4
+    elif pin == "fd_swiglu":
+        assert fd_check(o, "swiglu") > 1e-4
+    elif pin == "table":
+        assert check_normal_table(o) > 1e-6
+    elif pin == "row_identity":
+        assert _row_identity_error(o) >= 1.0
+    # and the unmodified oracle passes the same pin
+    clean = oracle.default()
+    if pin.startswith("fd"):
+        assert fd_check(clean, pin[3:]) < 1e-7
+    elif pin == "table":
+        assert check_normal_table(clean) < 2e-15
+    else:
+        assert _row_identity_error(clean) == 0.0
