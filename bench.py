@@ -1,0 +1,415 @@
+"""Benchmark: forward + backward of the t-sharded Megatron MLP block on GB300.
+
+One step = the whole hot path over one batch: the column-parallel GEMM with
+the fused activation, the row-parallel GEMM with the g-sum, the dgrad GEMM
+with act' fused (plus dW2), and the dX GEMM with the f-sum (plus dW1 / dW3).
+The default workload is the largest GeLU configuration, T = b*s = 16384
+tokens, d = 3072, d_ff = 12288 in t = 8 shards of 1536 (the north-star
+target names the largest configurations).
+
+Prints one JSON line (rank 0).  Multi-GPU: one process per GPU (torchrun),
+each GPU runs its own replica of the workload (the block's shards all live on
+one GPU; replicas only, no collective on the data path), barrier + max over
+ranks around the timed region, value = total FLOPs of all ranks / time.
+
+--impl reference times the fp64 CPU oracle instead (on the host cores, a
+bounded token sample of the same workload): there is no other implementation
+of this block to run.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic_inputs as si  # noqa: E402
+
+METRIC = "TP-sharded MLP fwd+bwd TFLOP/s on 1 GB300 (% of dense BF16 peak)"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1000 * 1000
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def flops_fwd_bwd(w: si.Workload, T: int | None = None) -> int:
+    """Algorithmic FLOPs: 12 T d dff (GeLU), 18 T d dff (SwiGLU); no padding, no recompute."""
+    per = 18 if w.act == "swiglu" else 12
+    return per * (w.T if T is None else T) * w.d * w.dff
+
+
+def phase_flops(w: si.Workload) -> dict:
+    """Algorithmic FLOPs of each of the four launches of a step."""
+    g = 2 * w.T * w.d * w.dff
+    if w.act == "swiglu":
+        return {"fwd_column": 2 * g, "fwd_row": g, "bwd_dgrad": 2 * g, "bwd_fsum": 4 * g}
+    return {"fwd_column": g, "fwd_row": g, "bwd_dgrad": 2 * g, "bwd_fsum": 2 * g}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(w: si.Workload, extra=None):
+    cfg = {"workload": w.name, "T": w.T, "b": w.b, "s": w.s, "d": w.d, "d_ff": w.dff, "t": w.t,
+           "d_i": list(w.d_i), "act": w.act,
+           "l2": "no flush: every launch reads more than the 129 MB L2 (inputs of one step ~1.9 GB)"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+class OracleLeg:
+    """The fp64 oracle timed on a bounded sample of the workload: the first
+    `tokens` tokens and the first `shards` shards (a sub-block of the same
+    weights; its FLOPs are 12 (SwiGLU: 18) * tokens * d * sum of those d_i).
+    Inputs are converted to fp64 once, outside the timed calls."""
+
+    def __init__(self, w: si.Workload, max_tokens: int, seed: int = si.BASE_SEED):
+        import numpy as np
+        self.w = w
+        inp = si.make_inputs(max_tokens, w.d, w.d_i, w.act, w.dtype, seed)
+        f64 = lambda t: None if t is None else np.ascontiguousarray(t.double().numpy())
+        self.X, self.dY = f64(inp.X), f64(inp.dY)
+        self.W1, self.W2, self.W3 = f64(inp.W1), f64(inp.W2), f64(inp.W3)
+
+    def flops(self, tokens: int, shards: int) -> int:
+        per = 18 if self.w.act == "swiglu" else 12
+        return per * tokens * self.w.d * sum(self.w.d_i[:shards])
+
+    def step(self, tokens: int, shards: int) -> float:
+        import oracle
+        n = sum(self.w.d_i[:shards])
+        W1, W2 = self.W1[:, :n], self.W2[:n]
+        W3 = self.W3[:, :n] if self.W3 is not None else None
+        t0 = time.perf_counter()
+        oracle.forward(self.X[:tokens], W1, W2, act=self.w.act, W3=W3)
+        oracle.backward(self.X[:tokens], W1, W2, self.dY[:tokens], act=self.w.act, W3=W3)
+        return time.perf_counter() - t0
+
+
+def oracle_threads() -> int:
+    import oracle
+    return oracle.num_threads()
+
+
+def cpu_baseline(w: si.Workload, tokens: int):
+    leg = OracleLeg(w, tokens)
+    dt = leg.step(tokens, w.t)
+    v = leg.flops(tokens, w.t) / dt / 1e12
+    return {"value": v, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle forward+backward on the first {tokens} of {w.T} tokens with all {w.t} shards "
+                      f"(full weights), one call of {dt:.1f} s; TFLOP/s = algorithmic FLOPs of that sample / time"}
+
+
+def run_reference(args, w: si.Workload):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    leg = OracleLeg(w, 64)
+    # size the per-step sample so the whole run stays within ~150 s
+    budget = 150.0 / (args.steps + args.warmup)
+    t11 = leg.step(1, 1)
+    t81 = leg.step(8, 1)
+    per_tok = max(0.0, (t81 - t11) / 7)
+    shards, tokens = 1, 1
+    for sh in range(w.t, 0, -1):
+        if sh * t11 <= budget:
+            shards = sh
+            break
+    for tk in (64, 32, 16, 8, 4, 2, 1):
+        if shards * (t11 + (tk - 1) * per_tok) <= budget:
+            tokens = tk
+            break
+    for _ in range(args.warmup):
+        leg.step(tokens, shards)
+    times = [leg.step(tokens, shards) for _ in range(args.steps)]
+    total = sum(times)
+    value = leg.flops(tokens, shards) * len(times) / total / 1e12
+    sample = (f"per step: fp64 oracle forward+backward on the first {tokens} of {w.T} tokens and the first "
+              f"{shards} of {w.t} shards (d_ff slice {sum(w.d_i[:shards])}); TFLOP/s = algorithmic FLOPs of the "
+              f"sample / time")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) X/dY, N(0,0.02) W)", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_ours(args, w: si.Workload):
+    import torch
+    import megatron_tensor_transformer_column_gb300 as tp
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tp.load()
+
+    inp = si.make_workload_inputs(w)
+    td = si.torch_dtype(w.dtype)
+    mlp = tp.ShardedMLP(w.T, w.d, w.d_i, w.act, w.dtype, device=dev)
+    sw = w.act == "swiglu"
+    X = inp.X.to(dev)
+    dY = inp.dY.to(dev)
+    W1 = [x.to(dev) for x in inp.W1_i]
+    W2 = [x.to(dev) for x in inp.W2_i]
+    W3 = [x.to(dev) for x in inp.W3_i] if sw else None
+    Y, saved, H = mlp.alloc_forward()
+    dact, dX, dW1, dW3, dW2 = mlp.alloc_backward()
+    stream = torch.cuda.current_stream(dev)
+    plan, wsp = mlp.plan, mlp.workspace
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        tp.tpmlp_forward_column(plan, X, W1, W3, saved, H, wsp, stream)
+        if ev:
+            ev[1].record(stream)
+        tp.tpmlp_forward_row(plan, W2, H, Y, wsp, stream)
+        if ev:
+            ev[2].record(stream)
+        tp.tpmlp_backward_dgrad(plan, W2, saved, H, dY, dact, dW2, wsp, stream)
+        if ev:
+            ev[3].record(stream)
+        tp.tpmlp_backward_fsum(plan, X, W1, W3, dact, dX, dW1, dW3, wsp, stream)
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    mlp.check(stream)
+
+    # ---- timed region: K steps, CUDA events on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
+    barrier(ws)
+    mlp.check(stream)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
+    ms_per_step = elapsed_ms / args.steps
+    names = ["fwd_column", "fwd_row", "bwd_dgrad", "bwd_fsum"]
+    per_phase = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
+                 for i, n in enumerate(names)}
+    total_flops = flops_fwd_bwd(w) * ws
+    value = total_flops * args.steps / (elapsed_ms / 1e3) / 1e12
+
+    # ---- end to end through the public API, host buffers (pinned), copies timed
+    e2e = run_e2e(args, w, tp, mlp, inp, dev, stream, ws)
+
+    peaks, peak_src = load_peaks()
+    pf = phase_flops(w)
+    dom = max(per_phase, key=per_phase.get)
+    achieved = pf[dom] / (per_phase[dom] / 1e3) / 1e12
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": achieved / peak_sus, "traffic": None,
+                "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); "
+                             f"frac of {peak_src} burst {peak_burst}: {achieved / peak_burst:.3f}"}
+    if rank != 0:
+        return 0
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.oracle_tokens)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) X/dY, N(0,0.02) W, rounded once to bf16)",
+        "config": workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)"}),
+        "pct_of_peak": {"sustained": value / ws / peak_sus, "burst": value / ws / peak_burst, "source": peak_src},
+        "tokens_per_s": w.T * ws * args.steps / (elapsed_ms / 1e3),
+        "phase_ms": per_phase,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, w, tp, mlp, inp, dev, stream, ws):
+    """Same metric through tpmlp_forward / tpmlp_backward with the inputs copied
+    from pinned host memory every step and the results (Y, dX, dW*) read back."""
+    import torch
+    sw = w.act == "swiglu"
+    pin = lambda t: t.contiguous().pin_memory()
+    hX, hdY = pin(inp.X), pin(inp.dY)
+    hW1 = [pin(x) for x in inp.W1_i]
+    hW2 = [pin(x) for x in inp.W2_i]
+    hW3 = [pin(x) for x in inp.W3_i] if sw else []
+    dX_in = torch.empty_like(hX, device=dev)
+    ddY = torch.empty_like(hdY, device=dev)
+    dW1_in = [torch.empty_like(x, device=dev) for x in hW1]
+    dW2_in = [torch.empty_like(x, device=dev) for x in hW2]
+    dW3_in = [torch.empty_like(x, device=dev) for x in hW3]
+    Y, saved, H = mlp.alloc_forward()
+    dact, dX, dW1, dW3, dW2 = mlp.alloc_backward()
+    outs_dev = [Y, dX, *dW1, *dW2, *(dW3 or [])]
+    outs_host = [torch.empty_like(o, device="cpu").pin_memory() for o in outs_dev]
+    h2d = sum(x.numel() * x.element_size() for x in [hX, hdY, *hW1, *hW2, *hW3])
+    d2h = sum(x.numel() * x.element_size() for x in outs_host)
+
+    def step():
+        dX_in.copy_(hX, non_blocking=True)
+        ddY.copy_(hdY, non_blocking=True)
+        for d_, h_ in zip(dW1_in + dW2_in + dW3_in, hW1 + hW2 + hW3):
+            d_.copy_(h_, non_blocking=True)
+        tp.tpmlp_forward(mlp.plan, dX_in, dW1_in, dW3_in if sw else None, dW2_in, Y, saved, H, mlp.workspace,
+                         stream)
+        tp.tpmlp_backward(mlp.plan, dX_in, dW1_in, dW3_in if sw else None, dW2_in, saved, H, ddY, dact, dX, dW1,
+                          dW3, dW2, mlp.workspace, stream)
+        for h_, d_ in zip(outs_host, outs_dev):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    n = max(3, min(args.steps, 20))
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    mlp.check(stream)
+    return {"value": flops_fwd_bwd(w) * ws * n / (ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
+            "api": "tpmlp_forward + tpmlp_backward, inputs from pinned host memory"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="C5", choices=sorted(si.WORKLOADS))
+    ap.add_argument("--oracle-tokens", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    w = si.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

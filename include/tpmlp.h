@@ -1,0 +1,171 @@
+/*
+ * tpmlp.h -- C ABI of the t-sharded Megatron tensor-parallel MLP block on one
+ * GB300 (sm_103a).
+ *
+ * The block (row convention, all matrices row-major):
+ *   GeLU  : A_i = X W1_i,  H_i = GeLU(A_i),                    Y = sum_i H_i W2_i
+ *   SwiGLU: G_i = X W1_i,  U_i = X W3_i,  H_i = U_i * Swish(G_i), Y = sum_i H_i W2_i
+ * with X [T x d], W1_i / W3_i [d x d_i] (column shard i of W1 / W3),
+ * W2_i [d_i x d] (row shard i of W2), H_i [T x d_i], Y [T x d] and
+ * sum_i d_i = d_ff.
+ *   - Column split of W1 and the identity GeLU(X [W11, W12]) =
+ *     [GeLU(X W11), GeLU(X W12)]; row split of W2 and the partial-sum identity
+ *     [H1, H2][W21; W22] = H1 W21 + H2 W22; the SwiGLU split: "Parallelism"
+ *     tag page of Jiang Yi's homepage, post "megatron-lm", Method / FFN.
+ *   - f is the identity forward and a sum (all-reduce) backward; g is a sum
+ *     forward and the identity backward: same page, the f/g operator table;
+ *     "Tensor parallelism" (brunomaga.github.io), Megatron_f / Megatron_g;
+ *     "AI Training Network Primer" ch. 3, section 3.4, Fig. 3.4 and 3.6.
+ * On one GPU the t shards sit side by side in HBM and both sums are
+ * accumulations in the kernels' fp32 accumulators: the g-sum inside the
+ * row-parallel GEMM's K loop, the f-sum inside the dX GEMM's K loop.  There
+ * is no collective.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named X, W*, H, Y, dY, dX, dW*, saved, dact, workspace are
+ *     DEVICE pointers owned by the caller; the library never allocates,
+ *     frees or retains them.  Arrays of pointers (const void* const* W1 ...)
+ *     are HOST arrays of t device pointers, read during the call only.
+ *   - Every tensor is a dense row-major 2-D array of the plan's dtype, its
+ *     start 16-byte aligned; with bf16, d and every d_i must be multiples of 8
+ *     (16-byte rows for the tensor-memory-access engine), with fp32 of 4.
+ *   - Calls are asynchronous on the given stream (0 = the legacy default
+ *     stream).  Argument errors are reported synchronously before anything
+ *     is launched.  A device-side watchdog (a bounded wait inside the
+ *     kernels) records TPMLP_ERR_DEVICE_TIMEOUT in the workspace's status
+ *     word instead of hanging; tpmlp_check() reads and clears it.
+ *   - Outputs are overwritten, never accumulated into.  Results are
+ *     deterministic: every reduction has a fixed order, with no atomics.
+ *   - Thread safety: a plan is immutable after creation and may be used from
+ *     several threads; calls that share a workspace must be ordered on the
+ *     device (same stream or events).
+ */
+#ifndef TPMLP_H_
+#define TPMLP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TPMLP_API __attribute__((visibility("default")))
+#else
+#define TPMLP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tpmlp_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  TPMLP_OK = 0,
+  TPMLP_ERR_INVALID_ARG = 1,     /* NULL pointer, bad enum value, NULL plan */
+  TPMLP_ERR_SHAPE = 2,           /* T < 0, d < 1, t < 1 or > TPMLP_MAX_SHARDS, some d_i < 1 */
+  TPMLP_ERR_ALIGNMENT = 3,       /* a pointer not 16-byte aligned, d or d_i not a multiple of 8 (bf16) / 4 (fp32) */
+  TPMLP_ERR_UNSUPPORTED = 4,     /* device is not sm_103 (GB300) or a size beyond the kernels' limits */
+  TPMLP_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed; see tpmlp_last_cuda_error() */
+  TPMLP_ERR_DEVICE_TIMEOUT = 6,  /* a kernel's bounded wait expired (reported by tpmlp_check) */
+  TPMLP_ERR_NOT_IMPLEMENTED = 7
+} tpmlp_status;
+
+typedef enum { TPMLP_ACT_GELU = 0, TPMLP_ACT_SWIGLU = 1 } tpmlp_act;
+typedef enum { TPMLP_BF16 = 0, TPMLP_FP32 = 1 } tpmlp_dtype;
+
+#define TPMLP_MAX_SHARDS 16
+
+/* Problem description.  d_i points to t shard widths (host memory, copied
+ * by tpmlp_plan_create).  Shard i covers hidden units [o_i, o_i + d_i) with
+ * o_i = d_0 + ... + d_{i-1}; widths may differ (the pages allow
+ * d_1 + d_2 = d_ff with d_1 != d_2).                                          */
+typedef struct {
+  int64_t T;           /* tokens (b * s); may be 0 */
+  int64_t d;           /* hidden size */
+  int32_t t;           /* number of shards, 1 .. TPMLP_MAX_SHARDS */
+  const int64_t* d_i;  /* t widths, sum = d_ff */
+  tpmlp_act act;
+  tpmlp_dtype dtype;   /* storage dtype of every tensor; accumulation is fp32 */
+} tpmlp_desc;
+
+typedef struct tpmlp_plan tpmlp_plan;
+
+/* Validate desc and build a plan (host memory only).  On error *out is NULL. */
+TPMLP_API tpmlp_status tpmlp_plan_create(const tpmlp_desc* desc, tpmlp_plan** out);
+/* Free a plan (NULL is a no-op). */
+TPMLP_API void tpmlp_plan_destroy(tpmlp_plan* plan);
+
+/* Bytes of device workspace every call needs: a 256-byte block holding the
+ * device status word.  The caller allocates it once, zero-filled, and passes
+ * it to every call of this plan.                                              */
+TPMLP_API size_t tpmlp_workspace_size(const tpmlp_plan* plan);
+
+/* Forward.  Inputs X [T x d]; W1[i], W3[i] (SwiGLU only; pass NULL for GeLU)
+ * [d x d_i]; W2[i] [d_i x d].  Outputs: Y [T x d]; H[i] [T x d_i]; saved =
+ * the pre-activations kept for backward: GeLU t pointers A_i [T x d_i];
+ * SwiGLU 2t pointers, G_0..G_{t-1} then U_0..U_{t-1}, each [T x d_i].
+ * Two kernels run: the column-parallel GEMM with the activation fused into
+ * its epilogue (f forward = identity: X is read by every shard), then the
+ * row-parallel GEMM whose K loop walks shard 0..t-1 into one fp32
+ * accumulator (the g-sum).                                                    */
+TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_plan* plan, const void* X, const void* const* W1,
+                           const void* const* W3, const void* const* W2, void* Y, void* const* saved,
+                           void* const* H, void* workspace, tpmlp_stream_t stream);
+
+/* Backward.  Inputs: X, W1, W3, W2 as in forward; saved and H as written by
+ * tpmlp_forward; dY [T x d].  Outputs: dact = per-shard activation gradients
+ * (GeLU t pointers dA_i; SwiGLU 2t pointers dG_0..dG_{t-1}, dU_0..dU_{t-1},
+ * each [T x d_i]), dX [T x d], dW1[i], dW3[i] (SwiGLU only, else NULL)
+ * [d x d_i], dW2[i] [d_i x d].
+ * g backward is the identity (every shard reads the same dY).  Two kernels
+ * run: (1) dH_i = dY W2_i^T with act' fused (writes dact) together with
+ * dW2_i = H_i^T dY; (2) dX = sum_i dA_i W1_i^T (SwiGLU: + dU_i W3_i^T) with
+ * the f-sum in one fp32 accumulator, together with dW1_i = X^T dA_i
+ * (dW3_i = X^T dU_i).  With T = 0 the weight gradients are zero-filled.       */
+TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_plan* plan, const void* X, const void* const* W1,
+                            const void* const* W3, const void* const* W2, const void* const* saved,
+                            const void* const* H, const void* dY, void* const* dact, void* dX,
+                            void* const* dW1, void* const* dW3, void* const* dW2, void* workspace,
+                            tpmlp_stream_t stream);
+
+/* The two launches of tpmlp_forward, callable one at a time (same arguments
+ * and layouts; each is exactly one kernel launch):
+ *   tpmlp_forward_column: saved and H from X, W1 (and W3).
+ *   tpmlp_forward_row:    Y = sum_i H_i W2_i (the g-sum in the accumulator). */
+TPMLP_API tpmlp_status tpmlp_forward_column(const tpmlp_plan* plan, const void* X, const void* const* W1,
+                                  const void* const* W3, void* const* saved, void* const* H, void* workspace,
+                                  tpmlp_stream_t stream);
+TPMLP_API tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* const* W2, void* const* H, void* Y,
+                               void* workspace, tpmlp_stream_t stream);
+
+/* The two launches of tpmlp_backward, callable one at a time:
+ *   tpmlp_backward_dgrad: dact from dY, W2 and saved (act' fused), and dW2
+ *                         from H and dY.
+ *   tpmlp_backward_fsum:  dX = sum_i dact_i W1_i^T (+ dU_i W3_i^T) (the
+ *                         f-sum in the accumulator), dW1 and dW3 from X and
+ *                         dact.  Must follow tpmlp_backward_dgrad.          */
+TPMLP_API tpmlp_status tpmlp_backward_dgrad(const tpmlp_plan* plan, const void* const* W2, const void* const* saved,
+                                  const void* const* H, const void* dY, void* const* dact, void* const* dW2,
+                                  void* workspace, tpmlp_stream_t stream);
+TPMLP_API tpmlp_status tpmlp_backward_fsum(const tpmlp_plan* plan, const void* X, const void* const* W1,
+                                 const void* const* W3, const void* const* dact, void* dX, void* const* dW1,
+                                 void* const* dW3, void* workspace, tpmlp_stream_t stream);
+
+/* Synchronise the stream, read the workspace's status word and clear it.
+ * Returns TPMLP_OK, TPMLP_ERR_DEVICE_TIMEOUT, or TPMLP_ERR_CUDA.               */
+TPMLP_API tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpmlp_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+TPMLP_API const char* tpmlp_status_string(tpmlp_status status);
+/* The last CUDA error code seen by this thread (0 if none), for TPMLP_ERR_CUDA. */
+TPMLP_API int tpmlp_last_cuda_error(void);
+/* ABI version: 100 * major + minor. */
+TPMLP_API int tpmlp_version(void);
+
+/* Kernel launches the last tpmlp_forward / tpmlp_backward call on this
+ * thread made (for accounting; 0 before the first call).                     */
+TPMLP_API int tpmlp_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TPMLP_H_ */

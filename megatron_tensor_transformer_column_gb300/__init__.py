@@ -1,0 +1,353 @@
+"""Python binding of libtpmlp: the t-sharded Megatron tensor-parallel MLP block
+on one GB300.
+
+The functions named ``tpmlp_*`` mirror the C ABI of ``include/tpmlp.h`` one to
+one: they only marshal arguments (torch CUDA tensors or raw device pointers,
+lists of per-shard tensors) and raise :class:`TpmlpError` on a non-OK status.
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback, and :func:`load` raises if the library is missing.
+
+``ShardedMLP`` is a small convenience layer that allocates the outputs with
+PyTorch (device memory and streams are all PyTorch provides here) and
+``TPMLPFunction`` wraps forward/backward as a ``torch.autograd.Function``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import List, Optional, Sequence
+
+from . import _build
+
+__all__ = [
+    "TpmlpError", "load", "Plan", "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size",
+    "tpmlp_forward", "tpmlp_backward", "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_backward_dgrad",
+    "tpmlp_backward_fsum", "tpmlp_check", "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version",
+    "tpmlp_last_launch_count", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
+]
+
+ACT = {"gelu": 0, "swiglu": 1}
+DTYPE = {"bf16": 0, "fp32": 1}
+STATUS = {0: "TPMLP_OK", 1: "TPMLP_ERR_INVALID_ARG", 2: "TPMLP_ERR_SHAPE", 3: "TPMLP_ERR_ALIGNMENT",
+          4: "TPMLP_ERR_UNSUPPORTED", 5: "TPMLP_ERR_CUDA", 6: "TPMLP_ERR_DEVICE_TIMEOUT",
+          7: "TPMLP_ERR_NOT_IMPLEMENTED"}
+MAX_SHARDS = 16
+
+EXPORTED_SYMBOLS = (
+    "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size", "tpmlp_forward", "tpmlp_backward",
+    "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_backward_dgrad", "tpmlp_backward_fsum", "tpmlp_check",
+    "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version", "tpmlp_last_launch_count",
+)
+
+
+class TpmlpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        name = STATUS.get(self.status, f"status {status}")
+        extra = ""
+        if self.status == 5 and _lib is not None:
+            extra = f" (cuda error {_lib.tpmlp_last_cuda_error()})"
+        super().__init__(f"{where}: {name}{extra}")
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int64), ("t", ctypes.c_int32),
+                ("d_i", ctypes.POINTER(ctypes.c_int64)), ("act", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libtpmlp.so (built by ``__graft_entry__.build()`` / ``_build.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built: {path} is missing (run __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        vp, pp, i32, st = ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_int
+        lib.tpmlp_plan_create.argtypes = [ctypes.POINTER(_Desc), ctypes.POINTER(vp)]
+        lib.tpmlp_plan_create.restype = st
+        lib.tpmlp_plan_destroy.argtypes = [vp]
+        lib.tpmlp_plan_destroy.restype = None
+        lib.tpmlp_workspace_size.argtypes = [vp]
+        lib.tpmlp_workspace_size.restype = ctypes.c_size_t
+        lib.tpmlp_forward.argtypes = [vp, vp, pp, pp, pp, vp, pp, pp, vp, vp]
+        lib.tpmlp_forward.restype = st
+        lib.tpmlp_backward.argtypes = [vp, vp, pp, pp, pp, pp, pp, vp, pp, vp, pp, pp, pp, vp, vp]
+        lib.tpmlp_backward.restype = st
+        lib.tpmlp_forward_column.argtypes = [vp, vp, pp, pp, pp, pp, vp, vp]
+        lib.tpmlp_forward_column.restype = st
+        lib.tpmlp_forward_row.argtypes = [vp, pp, pp, vp, vp, vp]
+        lib.tpmlp_forward_row.restype = st
+        lib.tpmlp_backward_dgrad.argtypes = [vp, pp, pp, pp, vp, pp, pp, vp, vp]
+        lib.tpmlp_backward_dgrad.restype = st
+        lib.tpmlp_backward_fsum.argtypes = [vp, vp, pp, pp, pp, vp, pp, pp, vp, vp]
+        lib.tpmlp_backward_fsum.restype = st
+        lib.tpmlp_check.argtypes = [vp, vp, vp]
+        lib.tpmlp_check.restype = st
+        lib.tpmlp_status_string.argtypes = [i32]
+        lib.tpmlp_status_string.restype = ctypes.c_char_p
+        lib.tpmlp_last_cuda_error.argtypes = []
+        lib.tpmlp_last_cuda_error.restype = i32
+        lib.tpmlp_version.argtypes = []
+        lib.tpmlp_version.restype = i32
+        lib.tpmlp_last_launch_count.argtypes = []
+        lib.tpmlp_last_launch_count.restype = i32
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------- marshalling
+
+def _addr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if x.numel() and not x.is_cuda:
+            raise ValueError("tensor must live on a CUDA device")
+        if x.numel() and not x.is_contiguous():
+            raise ValueError("tensor must be contiguous (row-major)")
+        return x.data_ptr() or None
+    raise TypeError(f"expected a tensor or an int device pointer, got {type(x)}")
+
+
+def _arr(xs) -> Optional[ctypes.Array]:
+    if xs is None:
+        return None
+    return (ctypes.c_void_p * len(xs))(*[_addr(x) for x in xs])
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        try:
+            import torch
+            return torch.cuda.current_stream().cuda_stream or None
+        except Exception:  # no torch CUDA: legacy default stream
+            return None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _ok(status: int, where: str):
+    if status != 0:
+        raise TpmlpError(status, where)
+
+
+class Plan:
+    """Owns a ``tpmlp_plan*`` (host memory only)."""
+
+    def __init__(self, T: int, d: int, d_i: Sequence[int], act: str = "gelu", dtype: str = "bf16"):
+        lib = load()
+        self.T, self.d, self.d_i = int(T), int(d), tuple(int(v) for v in d_i)
+        self.t = len(self.d_i)
+        self.act, self.dtype = act, dtype
+        self._d_i = (ctypes.c_int64 * max(1, self.t))(*self.d_i)
+        desc = _Desc(self.T, self.d, self.t, ctypes.cast(self._d_i, ctypes.POINTER(ctypes.c_int64)),
+                     ACT[act] if isinstance(act, str) else int(act),
+                     DTYPE[dtype] if isinstance(dtype, str) else int(dtype))
+        h = ctypes.c_void_p()
+        _ok(lib.tpmlp_plan_create(ctypes.byref(desc), ctypes.byref(h)), "tpmlp_plan_create")
+        self.handle = h
+
+    @property
+    def dff(self) -> int:
+        return sum(self.d_i)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.tpmlp_plan_destroy(h)
+            self.handle = None
+
+
+def tpmlp_plan_create(T, d, d_i, act="gelu", dtype="bf16") -> Plan:
+    return Plan(T, d, d_i, act, dtype)
+
+
+def tpmlp_plan_destroy(plan: Plan):
+    if plan.handle is not None and plan.handle.value:
+        load().tpmlp_plan_destroy(plan.handle)
+        plan.handle = None
+
+
+def tpmlp_workspace_size(plan: Plan) -> int:
+    return int(load().tpmlp_workspace_size(plan.handle))
+
+
+def tpmlp_forward(plan, X, W1, W3, W2, Y, saved, H, workspace, stream=None):
+    _ok(load().tpmlp_forward(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(W2), _addr(Y), _arr(saved), _arr(H),
+                             _addr(workspace), _stream(stream)), "tpmlp_forward")
+
+
+def tpmlp_backward(plan, X, W1, W3, W2, saved, H, dY, dact, dX, dW1, dW3, dW2, workspace, stream=None):
+    _ok(load().tpmlp_backward(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(W2), _arr(saved), _arr(H),
+                              _addr(dY), _arr(dact), _addr(dX), _arr(dW1), _arr(dW3), _arr(dW2), _addr(workspace),
+                              _stream(stream)), "tpmlp_backward")
+
+
+def tpmlp_forward_column(plan, X, W1, W3, saved, H, workspace, stream=None):
+    _ok(load().tpmlp_forward_column(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(saved), _arr(H),
+                                    _addr(workspace), _stream(stream)), "tpmlp_forward_column")
+
+
+def tpmlp_forward_row(plan, W2, H, Y, workspace, stream=None):
+    _ok(load().tpmlp_forward_row(plan.handle, _arr(W2), _arr(H), _addr(Y), _addr(workspace), _stream(stream)),
+        "tpmlp_forward_row")
+
+
+def tpmlp_backward_dgrad(plan, W2, saved, H, dY, dact, dW2, workspace, stream=None):
+    _ok(load().tpmlp_backward_dgrad(plan.handle, _arr(W2), _arr(saved), _arr(H), _addr(dY), _arr(dact), _arr(dW2),
+                                    _addr(workspace), _stream(stream)), "tpmlp_backward_dgrad")
+
+
+def tpmlp_backward_fsum(plan, X, W1, W3, dact, dX, dW1, dW3, workspace, stream=None):
+    _ok(load().tpmlp_backward_fsum(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(dact), _addr(dX), _arr(dW1),
+                                   _arr(dW3), _addr(workspace), _stream(stream)), "tpmlp_backward_fsum")
+
+
+def tpmlp_check(plan, workspace, stream=None):
+    _ok(load().tpmlp_check(plan.handle, _addr(workspace), _stream(stream)), "tpmlp_check")
+
+
+def tpmlp_status_string(status: int) -> str:
+    return load().tpmlp_status_string(int(status)).decode()
+
+
+def tpmlp_last_cuda_error() -> int:
+    return int(load().tpmlp_last_cuda_error())
+
+
+def tpmlp_version() -> int:
+    return int(load().tpmlp_version())
+
+
+def tpmlp_last_launch_count() -> int:
+    return int(load().tpmlp_last_launch_count())
+
+
+# ---------------------------------------------------------------- convenience layer
+
+class ShardedMLP:
+    """Plan + workspace + output allocation for one problem shape.
+
+    Tensors follow the C ABI: X [T, d]; W1_i, W3_i [d, d_i]; W2_i [d_i, d];
+    every tensor contiguous on the current CUDA device, in the plan's dtype.
+    """
+
+    def __init__(self, T: int, d: int, d_i: Sequence[int], act: str = "gelu", dtype: str = "bf16", device=None):
+        import torch
+        self.plan = Plan(T, d, d_i, act, dtype)
+        self.device = torch.device(device or "cuda")
+        self.tdtype = {"bf16": torch.bfloat16, "fp32": torch.float32}[dtype]
+        self.workspace = torch.zeros(tpmlp_workspace_size(self.plan), dtype=torch.uint8, device=self.device)
+
+    @property
+    def swiglu(self) -> bool:
+        return self.plan.act == "swiglu"
+
+    def _empty(self, *shape):
+        import torch
+        return torch.empty(*shape, dtype=self.tdtype, device=self.device)
+
+    def check_inputs(self, X, W1_i, W2_i, W3_i=None):
+        p = self.plan
+        assert tuple(X.shape) == (p.T, p.d), f"X shape {tuple(X.shape)} != {(p.T, p.d)}"
+        assert len(W1_i) == p.t and len(W2_i) == p.t
+        for i, w in enumerate(p.d_i):
+            assert tuple(W1_i[i].shape) == (p.d, w) and tuple(W2_i[i].shape) == (w, p.d)
+            if self.swiglu:
+                assert tuple(W3_i[i].shape) == (p.d, w)
+        for x in [X, *W1_i, *W2_i, *(W3_i or [])]:
+            assert x.dtype == self.tdtype and x.is_cuda
+
+    def alloc_forward(self):
+        p = self.plan
+        Y = self._empty(p.T, p.d)
+        H = [self._empty(p.T, w) for w in p.d_i]
+        saved = [self._empty(p.T, w) for w in p.d_i * (2 if self.swiglu else 1)]
+        return Y, saved, H
+
+    def alloc_backward(self):
+        p = self.plan
+        dX = self._empty(p.T, p.d)
+        dact = [self._empty(p.T, w) for w in p.d_i * (2 if self.swiglu else 1)]
+        dW1 = [self._empty(p.d, w) for w in p.d_i]
+        dW3 = [self._empty(p.d, w) for w in p.d_i] if self.swiglu else None
+        dW2 = [self._empty(w, p.d) for w in p.d_i]
+        return dact, dX, dW1, dW3, dW2
+
+    def forward(self, X, W1_i, W2_i, W3_i=None, out=None, stream=None):
+        self.check_inputs(X, W1_i, W2_i, W3_i)
+        Y, saved, H = out if out is not None else self.alloc_forward()
+        tpmlp_forward(self.plan, X, W1_i, W3_i, W2_i, Y, saved, H, self.workspace, stream)
+        return Y, saved, H
+
+    def backward(self, X, W1_i, W2_i, saved, H, dY, W3_i=None, out=None, stream=None):
+        dact, dX, dW1, dW3, dW2 = out if out is not None else self.alloc_backward()
+        tpmlp_backward(self.plan, X, W1_i, W3_i, W2_i, saved, H, dY, dact, dX, dW1, dW3, dW2, self.workspace,
+                       stream)
+        return {"dX": dX, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dact": dact}
+
+    def check(self, stream=None):
+        tpmlp_check(self.plan, self.workspace, stream)
+
+
+def _make_function():
+    import torch
+
+    class TPMLPFunction(torch.autograd.Function):
+        """Y = TPMLPFunction.apply(mlp, X, *W1_i, *W2_i[, *W3_i]) with the library's backward."""
+
+        @staticmethod
+        def forward(ctx, mlp: ShardedMLP, X, *weights):
+            t = mlp.plan.t
+            W1_i, W2_i = list(weights[:t]), list(weights[t:2 * t])
+            W3_i = list(weights[2 * t:3 * t]) if mlp.swiglu else None
+            Y, saved, H = mlp.forward(X.contiguous(), W1_i, W2_i, W3_i)
+            ctx.mlp = mlp
+            ctx.save_for_backward(X, *weights, *saved, *H)
+            return Y
+
+        @staticmethod
+        def backward(ctx, dY):
+            mlp = ctx.mlp
+            t = mlp.plan.t
+            ns = 2 * t if mlp.swiglu else t
+            tensors = ctx.saved_tensors
+            X = tensors[0]
+            nw = 3 * t if mlp.swiglu else 2 * t
+            weights = list(tensors[1:1 + nw])
+            saved = list(tensors[1 + nw:1 + nw + ns])
+            H = list(tensors[1 + nw + ns:])
+            W1_i, W2_i = weights[:t], weights[t:2 * t]
+            W3_i = weights[2 * t:] if mlp.swiglu else None
+            g = mlp.backward(X, W1_i, W2_i, saved, H, dY.contiguous(), W3_i)
+            grads = g["dW1"] + g["dW2"] + (g["dW3"] if mlp.swiglu else [])
+            return (None, g["dX"], *grads)
+
+    return TPMLPFunction
+
+
+class _LazyFunction:
+    _fn = None
+
+    def __getattr__(self, name):
+        if _LazyFunction._fn is None:
+            _LazyFunction._fn = _make_function()
+        return getattr(_LazyFunction._fn, name)
+
+
+TPMLPFunction = _LazyFunction()

@@ -1,0 +1,139 @@
+// simt_gemm.cu -- fp32 path of the t-sharded MLP block (exact fp32 FFMA,
+// fp32 accumulation), for problems stored in fp32.
+//
+// It runs the same problem lists as the tensor-core path (same segments, so
+// the g-sum and the f-sum are K loops into one register accumulator here
+// too, and the same epilogues), one 32x32 output tile per CTA.  The
+// tensor-core path is bf16-only; fp32 storage with a 1e-4 relative bound
+// rules out the tf32 tensor-core kind, whose per-product error is too close
+// to that bound.
+#include <cuda_runtime.h>
+
+#include "act.cuh"
+#include "tpmlp_internal.h"
+
+namespace tpmlp {
+namespace {
+
+constexpr int kT = 32;        // tile edge (M and N)
+constexpr int kK = 32;        // K chunk
+constexpr int kThreads = 256; // 32 columns x 8 row groups of 4 rows
+
+__device__ __forceinline__ float load_a(const Seg& S, int major, int64_t m, int64_t k) {
+  const float* a = static_cast<const float*>(S.a);
+  return major == MAJOR_MN ? a[k * S.lda + m] : a[m * S.lda + k];
+}
+
+__device__ __forceinline__ float load_b(const void* b, int64_t ldb, int major, int64_t k, int64_t n) {
+  const float* bp = static_cast<const float*>(b);
+  return major == MAJOR_MN ? bp[k * ldb + n] : bp[n * ldb + k];
+}
+
+__global__ void __launch_bounds__(kThreads) tpmlp_fp32_simt_gemm(const __grid_constant__ GemmParams p) {
+  __shared__ float As[kK][kT + 1];   // [k][m]
+  __shared__ float Bs[kK][kT + 1];   // [k][n]
+  __shared__ float B2s[kK][kT + 1];  // [k][n] (SwiGLU up projection)
+
+  // tile decode (same raster as the tensor-core path, tile_m = 32)
+  const int tile = blockIdx.x;
+  int g = 0;
+  while (g + 1 < p.num_groups && tile >= p.groups[g + 1].tile_start) ++g;
+  const Group& G = p.groups[g];
+  const int local = tile - G.tile_start;
+  const int full_band = G.band_m * G.tiles_per_row;
+  const int band = local / full_band;
+  const int m_first = band * G.band_m;
+  const int bm = min(G.band_m, G.tiles_m - m_first);
+  const int r = local - band * full_band;
+  int n_lin = r / bm;
+  const int mt = m_first + (r - n_lin * bm);
+  int pi = G.first_prob;
+  while (n_lin >= p.probs[pi].tiles_n) {
+    n_lin -= p.probs[pi].tiles_n;
+    ++pi;
+  }
+  const Prob& P = p.probs[pi];
+  const int64_t m0 = static_cast<int64_t>(mt) * kT;
+  const int64_t n0 = static_cast<int64_t>(n_lin) * P.tile_n;
+  const bool dual = P.epi == EPI_SWIGLU_FWD;
+
+  const int tx = threadIdx.x & 31;   // output column in tile
+  const int ty = threadIdx.x >> 5;   // rows 4*ty .. 4*ty+3
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+
+  for (int s = P.seg_begin; s < P.seg_begin + P.seg_count; ++s) {
+    const Seg& S = p.segs[s];
+    for (int k0 = 0; k0 < S.K; k0 += kK) {
+      for (int e = threadIdx.x; e < kT * kK; e += kThreads) {
+        // coalesce along the contiguous dimension of each operand
+        int mm, kk, nn, kb;
+        if (P.a_major == MAJOR_MN) { mm = e & 31; kk = e >> 5; } else { kk = e & 31; mm = e >> 5; }
+        if (P.b_major == MAJOR_MN) { nn = e & 31; kb = e >> 5; } else { kb = e & 31; nn = e >> 5; }
+        const int64_t gm = m0 + mm, gk = k0 + kk, gn = n0 + nn, gkb = k0 + kb;
+        As[kk][mm] = (gm < P.M && gk < S.K) ? load_a(S, P.a_major, gm, gk) : 0.f;
+        const bool bin = gn < P.N && gkb < S.K;
+        Bs[kb][nn] = bin ? load_b(S.b, S.ldb, P.b_major, gkb, gn) : 0.f;
+        if (dual) B2s[kb][nn] = bin ? load_b(S.b2, S.ldb, P.b_major, gkb, gn) : 0.f;
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < kK; ++kk) {
+        const float b = Bs[kk][tx];
+        const float b2 = dual ? B2s[kk][tx] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a = As[kk][4 * ty + i];
+          acc[i] = fmaf(a, b, acc[i]);
+          if (dual) acc2[i] = fmaf(a, b2, acc2[i]);
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  const int64_t col = n0 + tx;
+  if (col >= P.N) return;
+  for (int i = 0; i < 4; ++i) {
+    const int64_t row = m0 + 4 * ty + i;
+    if (row >= P.M) continue;
+    const int64_t o = row * P.ldo + col;
+    const float v = acc[i];
+    switch (P.epi) {
+      case EPI_STORE:
+        static_cast<float*>(P.out0)[o] = v;
+        break;
+      case EPI_GELU_FWD:
+        static_cast<float*>(P.out0)[o] = v;
+        static_cast<float*>(P.out1)[o] = act::gelu(v);
+        break;
+      case EPI_SWIGLU_FWD:
+        static_cast<float*>(P.out0)[o] = v;
+        static_cast<float*>(P.out1)[o] = acc2[i];
+        static_cast<float*>(P.out2)[o] = acc2[i] * act::swish(v);
+        break;
+      case EPI_GELU_BWD:
+        static_cast<float*>(P.out0)[o] = v * act::gelu_grad(static_cast<const float*>(P.aux0)[o]);
+        break;
+      case EPI_SWIGLU_BWD: {
+        float dg, du;
+        act::swiglu_grads(v, static_cast<const float*>(P.aux0)[o], static_cast<const float*>(P.aux1)[o], dg, du);
+        static_cast<float*>(P.out0)[o] = dg;
+        static_cast<float*>(P.out1)[o] = du;
+        break;
+      }
+      default:
+        break;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_simt_gemm(const GemmParams& p, cudaStream_t stream) {
+  if (p.total_tiles <= 0) return cudaSuccess;
+  tpmlp_fp32_simt_gemm<<<p.total_tiles, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace tpmlp

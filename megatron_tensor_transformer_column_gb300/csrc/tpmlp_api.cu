@@ -1,0 +1,565 @@
+// tpmlp_api.cu -- host side of the C ABI declared in include/tpmlp.h:
+// argument checks, the shard table, TMA tensor maps, the per-launch problem
+// lists and the launches.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "tpmlp.h"
+#include "tpmlp_internal.h"
+
+using namespace tpmlp;
+
+struct tpmlp_plan {
+  int64_t T, d;
+  int32_t t;
+  std::vector<int64_t> d_i;
+  std::vector<int64_t> o_i;
+  int64_t dff;
+  tpmlp_act act;
+  tpmlp_dtype dtype;
+  uint64_t timeout_ns;
+};
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+thread_local int g_last_launches = 0;
+
+constexpr int kTileM = 128;
+constexpr int kSimtTile = 32;
+constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000 * 1000;  // 2 s
+
+tpmlp_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return TPMLP_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ device
+struct DeviceInfo {
+  bool ok = false;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+};
+
+tpmlp_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 0 || dev >= 64) return TPMLP_ERR_UNSUPPORTED;
+  if (!cache[dev].ok) {
+    DeviceInfo di;
+    if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    di.ok = true;
+    cache[dev] = di;
+  }
+  *out = cache[dev];
+  // The kernels are built for sm_103a only (GB300).
+  if (out->cc_major != 10 || out->cc_minor != 3) return TPMLP_ERR_UNSUPPORTED;
+  return TPMLP_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major bf16 [rows x cols]; 64 x 64 boxes, 128-byte swizzle,
+// out-of-range elements read as zero.
+bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ problem lists
+struct Builder {
+  GemmParams* p;
+  bool tc;  // tensor-core path (tensor maps) or fp32 SIMT path
+  int tile_m;
+  std::vector<const void*> map_ptr;
+  bool map_error = false;
+  int cur_group = -1;
+
+  explicit Builder(GemmParams* params, bool tensor_cores) : p(params), tc(tensor_cores) {
+    std::memset(static_cast<void*>(p), 0, sizeof(GemmParams));
+    tile_m = tc ? kTileM : kSimtTile;
+    p->tile_m = tile_m;
+  }
+
+  int map(const void* ptr, int64_t rows, int64_t cols) {
+    if (!tc) return -1;
+    for (size_t i = 0; i < map_ptr.size(); ++i)
+      if (map_ptr[i] == ptr) return static_cast<int>(i);
+    if (p->num_maps >= kMaxMaps) {
+      map_error = true;
+      return 0;
+    }
+    const int idx = p->num_maps++;
+    if (!encode_map(&p->maps[idx], ptr, rows, cols)) map_error = true;
+    map_ptr.push_back(ptr);
+    return idx;
+  }
+
+  void begin_group(int64_t M, int band_m) {
+    Group& G = p->groups[p->num_groups];
+    cur_group = p->num_groups++;
+    G.first_prob = p->num_probs;
+    G.num_probs = 0;
+    G.tiles_m = static_cast<int32_t>((M + tile_m - 1) / tile_m);
+    G.tiles_per_row = 0;
+    G.band_m = std::max(1, std::min(band_m, G.tiles_m));
+    G.tile_start = p->total_tiles;
+  }
+
+  Prob& add_prob(int64_t M, int64_t N, int tile_n, int a_major, int b_major, int epi, int64_t ldo) {
+    Prob& P = p->probs[p->num_probs++];
+    P.M = static_cast<int32_t>(M);
+    P.N = static_cast<int32_t>(N);
+    P.tile_n = tc ? tile_n : kSimtTile;
+    P.tiles_n = static_cast<int32_t>((N + P.tile_n - 1) / P.tile_n);
+    P.seg_begin = p->num_segs;
+    P.seg_count = 0;
+    P.a_major = a_major;
+    P.b_major = b_major;
+    P.epi = epi;
+    P.ldo = ldo;
+    Group& G = p->groups[cur_group];
+    G.num_probs++;
+    G.tiles_per_row += P.tiles_n;
+    return P;
+  }
+
+  void add_seg(Prob& P, const void* a, int64_t a_rows, int64_t a_cols, const void* b, int64_t b_rows,
+               int64_t b_cols, const void* b2, int64_t K) {
+    Seg& S = p->segs[p->num_segs++];
+    S.a = a;
+    S.b = b;
+    S.b2 = b2;
+    S.lda = a_cols;
+    S.ldb = b_cols;
+    S.a_map = map(a, a_rows, a_cols);
+    S.b_map = map(b, b_rows, b_cols);
+    S.b2_map = b2 ? map(b2, b_rows, b_cols) : -1;
+    S.K = static_cast<int32_t>(K);
+    P.seg_count++;
+  }
+
+  void end_group() {
+    Group& G = p->groups[cur_group];
+    p->total_tiles += G.tiles_m * G.tiles_per_row;
+  }
+};
+
+GemmParams* scratch_params() {
+  thread_local GemmParams* params = nullptr;
+  if (!params) params = new (std::align_val_t(64)) GemmParams;
+  return params;
+}
+
+int band_for(int sms) {
+  // CTAs running at the same time cover about a square block of tiles.
+  int b = 1;
+  while ((b + 1) * (b + 1) <= sms) ++b;
+  return b;
+}
+
+tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan* plan, void* workspace,
+                    cudaStream_t stream) {
+  if (B.map_error) return TPMLP_ERR_INVALID_ARG;
+  GemmParams& p = *B.p;
+  if (p.total_tiles == 0) return TPMLP_OK;
+  p.status = static_cast<int32_t*>(workspace);
+  p.timeout_ns = plan->timeout_ns;
+  cudaError_t e;
+  if (B.tc) {
+    const int grid = std::min(p.total_tiles, di.sms);
+    e = launch_tc_gemm(p, tag, grid, stream);
+  } else {
+    e = launch_simt_gemm(p, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  ++g_last_launches;
+  return TPMLP_OK;
+}
+
+// ------------------------------------------------------------------ checks
+tpmlp_status check_ptrs(const tpmlp_plan* pl, std::initializer_list<const void*> must, bool t_rows_may_be_null) {
+  for (const void* q : must) {
+    if (!q) {
+      if (t_rows_may_be_null) continue;
+      return TPMLP_ERR_INVALID_ARG;
+    }
+    if (!aligned16(q)) return TPMLP_ERR_ALIGNMENT;
+  }
+  (void)pl;
+  return TPMLP_OK;
+}
+
+tpmlp_status check_array(const void* const* arr, int n, bool may_be_null_entries) {
+  if (!arr) return TPMLP_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    if (!arr[i]) {
+      if (may_be_null_entries) continue;
+      return TPMLP_ERR_INVALID_ARG;
+    }
+    if (!aligned16(arr[i])) return TPMLP_ERR_ALIGNMENT;
+  }
+  return TPMLP_OK;
+}
+
+#define TPMLP_TRY(expr)                   \
+  do {                                    \
+    tpmlp_status st_ = (expr);            \
+    if (st_ != TPMLP_OK) return st_;      \
+  } while (0)
+
+bool swiglu(const tpmlp_plan* pl) { return pl->act == TPMLP_ACT_SWIGLU; }
+int nsaved(const tpmlp_plan* pl) { return swiglu(pl) ? 2 * pl->t : pl->t; }
+
+tpmlp_status common_checks(const tpmlp_plan* pl, void* workspace, DeviceInfo* di) {
+  if (!pl) return TPMLP_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return workspace ? TPMLP_ERR_ALIGNMENT : TPMLP_ERR_INVALID_ARG;
+  return device_info(di);
+}
+
+// ------------------------------------------------------------------ phases
+tpmlp_status fwd_column(const tpmlp_plan* pl, const DeviceInfo& di, const void* X, const void* const* W1,
+                        const void* const* W3, void* const* saved, void* const* H, void* ws, cudaStream_t st) {
+  if (pl->T == 0) return TPMLP_OK;
+  const bool tc = pl->dtype == TPMLP_BF16;
+  const bool sw = swiglu(pl);
+  Builder B(scratch_params(), tc);
+  B.begin_group(pl->T, band_for(di.sms));
+  for (int i = 0; i < pl->t; ++i) {
+    const int64_t di_ = pl->d_i[i];
+    Prob& P = B.add_prob(pl->T, di_, sw ? 128 : 256, MAJOR_K, MAJOR_MN, sw ? EPI_SWIGLU_FWD : EPI_GELU_FWD, di_);
+    P.out0 = saved[i];
+    P.out1 = sw ? saved[pl->t + i] : H[i];
+    P.out2 = sw ? H[i] : nullptr;
+    B.add_seg(P, X, pl->T, pl->d, W1[i], pl->d, di_, sw ? W3[i] : nullptr, pl->d);
+  }
+  B.end_group();
+  return launch(B, TAG_FWD_COLUMN, di, pl, ws, st);
+}
+
+tpmlp_status fwd_row(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* W2, void* Y,
+                     void* const* H, void* ws, cudaStream_t st) {
+  if (pl->T == 0) return TPMLP_OK;
+  Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
+  B.begin_group(pl->T, band_for(di.sms));
+  Prob& P = B.add_prob(pl->T, pl->d, 256, MAJOR_K, MAJOR_MN, EPI_STORE, pl->d);
+  P.out0 = Y;
+  // g operator: every shard's H_i W2_i accumulates into the same tile.
+  for (int i = 0; i < pl->t; ++i) B.add_seg(P, H[i], pl->T, pl->d_i[i], W2[i], pl->d_i[i], pl->d, nullptr, pl->d_i[i]);
+  B.end_group();
+  return launch(B, TAG_FWD_ROW, di, pl, ws, st);
+}
+
+tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* W2,
+                       const void* const* saved, const void* const* H, const void* dY, void* const* dact,
+                       void* const* dW2, void* ws, cudaStream_t st) {
+  const bool sw = swiglu(pl);
+  if (pl->T == 0) {
+    const size_t es = pl->dtype == TPMLP_BF16 ? 2 : 4;
+    for (int i = 0; i < pl->t; ++i) {
+      cudaError_t e = cudaMemsetAsync(dW2[i], 0, static_cast<size_t>(pl->d_i[i] * pl->d) * es, st);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TPMLP_OK;
+  }
+  Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
+  const int band = band_for(di.sms);
+  // dW2_i = H_i^T dY (K = T: the long tiles go first)
+  for (int i = 0; i < pl->t; ++i) {
+    const int64_t di_ = pl->d_i[i];
+    B.begin_group(di_, band);
+    Prob& P = B.add_prob(di_, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
+    P.out0 = dW2[i];
+    B.add_seg(P, H[i], pl->T, di_, dY, pl->T, pl->d, nullptr, pl->T);
+    B.end_group();
+  }
+  // dH_i = dY W2_i^T with act' fused (g backward = identity: every shard reads dY)
+  B.begin_group(pl->T, band);
+  for (int i = 0; i < pl->t; ++i) {
+    const int64_t di_ = pl->d_i[i];
+    Prob& P = B.add_prob(pl->T, di_, 256, MAJOR_K, MAJOR_K, sw ? EPI_SWIGLU_BWD : EPI_GELU_BWD, di_);
+    P.aux0 = saved[i];
+    P.aux1 = sw ? saved[pl->t + i] : nullptr;
+    P.out0 = dact[i];
+    P.out1 = sw ? dact[pl->t + i] : nullptr;
+    B.add_seg(P, dY, pl->T, pl->d, W2[i], di_, pl->d, nullptr, pl->d);
+  }
+  B.end_group();
+  return launch(B, TAG_BWD_DGRAD, di, pl, ws, st);
+}
+
+tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X, const void* const* W1,
+                      const void* const* W3, const void* const* dact, void* dX, void* const* dW1,
+                      void* const* dW3, void* ws, cudaStream_t st) {
+  const bool sw = swiglu(pl);
+  if (pl->T == 0) {
+    const size_t es = pl->dtype == TPMLP_BF16 ? 2 : 4;
+    for (int i = 0; i < pl->t; ++i) {
+      const size_t n = static_cast<size_t>(pl->d * pl->d_i[i]) * es;
+      cudaError_t e = cudaMemsetAsync(dW1[i], 0, n, st);
+      if (e == cudaSuccess && sw) e = cudaMemsetAsync(dW3[i], 0, n, st);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TPMLP_OK;
+  }
+  Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
+  const int band = band_for(di.sms);
+  // dW1_i = X^T dA_i (SwiGLU: X^T dG_i) and dW3_i = X^T dU_i (K = T)
+  B.begin_group(pl->d, band);
+  for (int i = 0; i < pl->t; ++i) {
+    const int64_t di_ = pl->d_i[i];
+    Prob& P = B.add_prob(pl->d, di_, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, di_);
+    P.out0 = dW1[i];
+    B.add_seg(P, X, pl->T, pl->d, dact[i], pl->T, di_, nullptr, pl->T);
+  }
+  if (sw) {
+    for (int i = 0; i < pl->t; ++i) {
+      const int64_t di_ = pl->d_i[i];
+      Prob& P = B.add_prob(pl->d, di_, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, di_);
+      P.out0 = dW3[i];
+      B.add_seg(P, X, pl->T, pl->d, dact[pl->t + i], pl->T, di_, nullptr, pl->T);
+    }
+  }
+  B.end_group();
+  // dX = sum_i dA_i W1_i^T (+ dU_i W3_i^T): the f operator's backward sum.
+  B.begin_group(pl->T, band);
+  Prob& P = B.add_prob(pl->T, pl->d, 256, MAJOR_K, MAJOR_K, EPI_STORE, pl->d);
+  P.out0 = dX;
+  for (int i = 0; i < pl->t; ++i)
+    B.add_seg(P, dact[i], pl->T, pl->d_i[i], W1[i], pl->d, pl->d_i[i], nullptr, pl->d_i[i]);
+  if (sw)
+    for (int i = 0; i < pl->t; ++i)
+      B.add_seg(P, dact[pl->t + i], pl->T, pl->d_i[i], W3[i], pl->d, pl->d_i[i], nullptr, pl->d_i[i]);
+  B.end_group();
+  return launch(B, TAG_BWD_FSUM, di, pl, ws, st);
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+tpmlp_status tpmlp_plan_create(const tpmlp_desc* desc, tpmlp_plan** out) {
+  if (!out) return TPMLP_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!desc || !desc->d_i) return TPMLP_ERR_INVALID_ARG;
+  if (desc->act != TPMLP_ACT_GELU && desc->act != TPMLP_ACT_SWIGLU) return TPMLP_ERR_INVALID_ARG;
+  if (desc->dtype != TPMLP_BF16 && desc->dtype != TPMLP_FP32) return TPMLP_ERR_INVALID_ARG;
+  if (desc->T < 0 || desc->d < 1 || desc->t < 1 || desc->t > TPMLP_MAX_SHARDS) return TPMLP_ERR_SHAPE;
+  const int64_t mult = desc->dtype == TPMLP_BF16 ? 8 : 4;
+  const int64_t kMax32 = (int64_t(1) << 31) - 1;
+  int64_t dff = 0;
+  for (int i = 0; i < desc->t; ++i) {
+    if (desc->d_i[i] < 1) return TPMLP_ERR_SHAPE;
+    dff += desc->d_i[i];
+  }
+  if (desc->d % mult) return TPMLP_ERR_ALIGNMENT;
+  for (int i = 0; i < desc->t; ++i)
+    if (desc->d_i[i] % mult) return TPMLP_ERR_ALIGNMENT;
+  if (desc->T > kMax32 || desc->d > kMax32 || dff > kMax32) return TPMLP_ERR_UNSUPPORTED;
+  tpmlp_plan* pl = new (std::nothrow) tpmlp_plan;
+  if (!pl) return TPMLP_ERR_INVALID_ARG;
+  pl->T = desc->T;
+  pl->d = desc->d;
+  pl->t = desc->t;
+  pl->d_i.assign(desc->d_i, desc->d_i + desc->t);
+  pl->o_i.resize(desc->t);
+  int64_t o = 0;
+  for (int i = 0; i < desc->t; ++i) {
+    pl->o_i[i] = o;
+    o += pl->d_i[i];
+  }
+  pl->dff = dff;
+  pl->act = desc->act;
+  pl->dtype = desc->dtype;
+  pl->timeout_ns = kDefaultTimeoutNs;
+  if (const char* s = std::getenv("TPMLP_WAIT_TIMEOUT_MS")) {
+    const long long ms = std::atoll(s);
+    if (ms > 0) pl->timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
+  }
+  *out = pl;
+  return TPMLP_OK;
+}
+
+void tpmlp_plan_destroy(tpmlp_plan* plan) { delete plan; }
+
+size_t tpmlp_workspace_size(const tpmlp_plan* plan) { return plan ? 256 : 0; }
+
+tpmlp_status tpmlp_forward_column(const tpmlp_plan* plan, const void* X, const void* const* W1,
+                                  const void* const* W3, void* const* saved, void* const* H, void* workspace,
+                                  tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_ptrs(plan, {X}, tz));
+  TPMLP_TRY(check_array(W1, plan->t, false));
+  if (swiglu(plan)) TPMLP_TRY(check_array(W3, plan->t, false));
+  TPMLP_TRY(check_array(saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array(H, plan->t, tz));
+  return fwd_column(plan, di, X, W1, W3, saved, H, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* const* W2, void* const* H, void* Y,
+                               void* workspace, tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_array(W2, plan->t, false));
+  TPMLP_TRY(check_array(H, plan->t, tz));
+  TPMLP_TRY(check_ptrs(plan, {Y}, tz));
+  return fwd_row(plan, di, W2, Y, H, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_forward(const tpmlp_plan* plan, const void* X, const void* const* W1, const void* const* W3,
+                           const void* const* W2, void* Y, void* const* saved, void* const* H, void* workspace,
+                           tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_ptrs(plan, {X, Y}, tz));
+  TPMLP_TRY(check_array(W1, plan->t, false));
+  if (swiglu(plan)) TPMLP_TRY(check_array(W3, plan->t, false));
+  TPMLP_TRY(check_array(W2, plan->t, false));
+  TPMLP_TRY(check_array(saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array(H, plan->t, tz));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  TPMLP_TRY(fwd_column(plan, di, X, W1, W3, saved, H, workspace, st));
+  return fwd_row(plan, di, W2, Y, H, workspace, st);
+}
+
+tpmlp_status tpmlp_backward_dgrad(const tpmlp_plan* plan, const void* const* W2, const void* const* saved,
+                                  const void* const* H, const void* dY, void* const* dact, void* const* dW2,
+                                  void* workspace, tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_array(W2, plan->t, false));
+  TPMLP_TRY(check_array(saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array(H, plan->t, tz));
+  TPMLP_TRY(check_ptrs(plan, {dY}, tz));
+  TPMLP_TRY(check_array(dact, nsaved(plan), tz));
+  TPMLP_TRY(check_array(dW2, plan->t, false));
+  return bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_backward_fsum(const tpmlp_plan* plan, const void* X, const void* const* W1,
+                                 const void* const* W3, const void* const* dact, void* dX, void* const* dW1,
+                                 void* const* dW3, void* workspace, tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_ptrs(plan, {X, dX}, tz));
+  TPMLP_TRY(check_array(W1, plan->t, false));
+  if (swiglu(plan)) {
+    TPMLP_TRY(check_array(W3, plan->t, false));
+    TPMLP_TRY(check_array(dW3, plan->t, false));
+  }
+  TPMLP_TRY(check_array(dact, nsaved(plan), tz));
+  TPMLP_TRY(check_array(dW1, plan->t, false));
+  return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_backward(const tpmlp_plan* plan, const void* X, const void* const* W1, const void* const* W3,
+                            const void* const* W2, const void* const* saved, const void* const* H, const void* dY,
+                            void* const* dact, void* dX, void* const* dW1, void* const* dW3, void* const* dW2,
+                            void* workspace, tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_ptrs(plan, {X, dY, dX}, tz));
+  TPMLP_TRY(check_array(W1, plan->t, false));
+  TPMLP_TRY(check_array(W2, plan->t, false));
+  if (swiglu(plan)) {
+    TPMLP_TRY(check_array(W3, plan->t, false));
+    TPMLP_TRY(check_array(dW3, plan->t, false));
+  }
+  TPMLP_TRY(check_array(saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array(H, plan->t, tz));
+  TPMLP_TRY(check_array(dact, nsaved(plan), tz));
+  TPMLP_TRY(check_array(dW1, plan->t, false));
+  TPMLP_TRY(check_array(dW2, plan->t, false));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  TPMLP_TRY(bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, workspace, st));
+  return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, workspace, st);
+}
+
+tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpmlp_stream_t stream) {
+  if (!plan || !workspace) return TPMLP_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int32_t word = 0;
+  e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word != kDevOk) {
+    e = cudaMemset(workspace, 0, sizeof(word));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return TPMLP_ERR_DEVICE_TIMEOUT;
+  }
+  return TPMLP_OK;
+}
+
+const char* tpmlp_status_string(tpmlp_status s) {
+  switch (s) {
+    case TPMLP_OK: return "TPMLP_OK";
+    case TPMLP_ERR_INVALID_ARG: return "TPMLP_ERR_INVALID_ARG";
+    case TPMLP_ERR_SHAPE: return "TPMLP_ERR_SHAPE";
+    case TPMLP_ERR_ALIGNMENT: return "TPMLP_ERR_ALIGNMENT";
+    case TPMLP_ERR_UNSUPPORTED: return "TPMLP_ERR_UNSUPPORTED";
+    case TPMLP_ERR_CUDA: return "TPMLP_ERR_CUDA";
+    case TPMLP_ERR_DEVICE_TIMEOUT: return "TPMLP_ERR_DEVICE_TIMEOUT";
+    case TPMLP_ERR_NOT_IMPLEMENTED: return "TPMLP_ERR_NOT_IMPLEMENTED";
+  }
+  return "TPMLP_ERR_UNKNOWN";
+}
+
+int tpmlp_last_cuda_error(void) { return g_last_cuda_error; }
+int tpmlp_version(void) { return 100; }
+int tpmlp_last_launch_count(void) { return g_last_launches; }
+
+}  // extern "C"

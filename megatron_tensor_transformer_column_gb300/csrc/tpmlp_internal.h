@@ -1,0 +1,114 @@
+// tpmlp_internal.h -- work description shared by the host launcher and the
+// kernels of the t-sharded MLP library.
+//
+// Every launch of the library is a list of GEMM problems
+//     C[M x N] = sum over segments s of A_s[M x K_s] * B_s[K_s x N]
+// followed by a fused epilogue.  A segment list longer than one is how the
+// cross-shard sums are done on chip: the row-parallel forward GEMM has one
+// segment per shard (H_i, W2_i) and its K loop walks them into one fp32
+// accumulator (the g operator); the dX GEMM does the same with (dA_i, W1_i)
+// (the f operator's backward sum).  See tpmlp.h for the algebra and sources.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the driver entry point is fetched at run time)
+#include <stdint.h>
+
+namespace tpmlp {
+
+constexpr int kMaxShards = 16;
+constexpr int kMaxMaps = 4 * kMaxShards + 2;
+constexpr int kMaxProbs = 2 * kMaxShards + 2;
+constexpr int kMaxGroups = kMaxShards + 2;
+constexpr int kMaxSegs = 4 * kMaxShards + 2;
+
+// Fused epilogues.  acc is the fp32 accumulator tile.
+enum EpiKind : int32_t {
+  EPI_STORE = 0,       // out0 = acc
+  EPI_GELU_FWD = 1,    // out0 = A = acc (pre-activation, kept for backward), out1 = H = GeLU(acc)
+  EPI_SWIGLU_FWD = 2,  // two accumulators G (B = W1_i) and U (B2 = W3_i):
+                       // out0 = G, out1 = U, out2 = H = U * Swish(G)
+  EPI_GELU_BWD = 3,    // acc = dH; aux0 = A: out0 = dA = dH * GeLU'(A)
+  EPI_SWIGLU_BWD = 4,  // acc = dH; aux0 = G, aux1 = U:
+                       // out0 = dG = dH * U * Swish'(G), out1 = dU = dH * Swish(G)
+};
+
+// Operand majors.  A(m, k) is K-major when a[m][k] is contiguous in k,
+// MN-major when a[k][m] is contiguous in m; B(k, n) likewise.
+enum Major : int32_t { MAJOR_K = 0, MAJOR_MN = 1 };
+
+struct Seg {
+  const void* a;   // raw pointers (used by the SIMT path)
+  const void* b;
+  const void* b2;  // second B (SwiGLU up projection), else null
+  int64_t lda;     // row stride of the stored 2-D array behind A, in elements
+  int64_t ldb;
+  int32_t a_map;   // tensor-map indices (used by the tensor-core path)
+  int32_t b_map;
+  int32_t b2_map;
+  int32_t K;
+};
+
+struct Prob {
+  int32_t M, N;
+  int32_t tile_n;    // tile width along N for this problem
+  int32_t tiles_n;
+  int32_t seg_begin, seg_count;
+  int32_t a_major, b_major;
+  int32_t epi;
+  int32_t pad_;
+  int64_t ldo;       // row stride of out*/aux*, in elements
+  void* out0;
+  void* out1;
+  void* out2;
+  const void* aux0;
+  const void* aux1;
+};
+
+// Problems with the same M that are rastered together: tiles are ordered in
+// bands of band_m M-tiles; inside a band, N-tiles (across every problem of
+// the group, in order) are the slow index and M-tiles the fast one, so the
+// CTAs that run at the same time share operand panels in L2.
+struct Group {
+  int32_t first_prob, num_probs;
+  int32_t tiles_m;
+  int32_t tiles_per_row;  // sum of tiles_n over the group's problems
+  int32_t band_m;
+  int32_t tile_start;     // first global tile index of the group
+};
+
+struct GemmParams {
+  CUtensorMap maps[kMaxMaps];
+  Prob probs[kMaxProbs];
+  Group groups[kMaxGroups];
+  Seg segs[kMaxSegs];
+  int32_t num_maps, num_probs, num_groups, num_segs;
+  int32_t total_tiles;
+  int32_t tile_m;
+  int32_t* status;          // device status word (workspace)
+  uint64_t timeout_ns;      // bound on every wait inside the kernel
+};
+
+// Kernel parameters live in the 32 KB parameter space (__grid_constant__).
+static_assert(sizeof(GemmParams) <= 32000, "kernel parameter block too large");
+
+// Status codes written to the device status word.
+constexpr int32_t kDevOk = 0;
+constexpr int32_t kDevTimeoutProducer = 1;
+constexpr int32_t kDevTimeoutMma = 2;
+constexpr int32_t kDevTimeoutEpilogue = 3;
+
+// Launchers (defined next to their kernels).
+int tc_gemm_max_smem_bytes();
+cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int grid, cudaStream_t stream);
+cudaError_t launch_simt_gemm(const GemmParams& p, cudaStream_t stream);
+
+// Kernel tags: one kernel symbol per launch kind, so that profiles tell the
+// four launches of a training step apart.
+enum KernelTag : int {
+  TAG_FWD_COLUMN = 0,   // column-parallel GEMM + activation
+  TAG_FWD_ROW = 1,      // row-parallel GEMM with the g-sum
+  TAG_BWD_DGRAD = 2,    // dH_i -> dA_i (act') and dW2_i
+  TAG_BWD_FSUM = 3,     // dX with the f-sum, and dW1_i (dW3_i)
+};
+
+}  // namespace tpmlp

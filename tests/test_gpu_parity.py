@@ -1,0 +1,137 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bar: max|err| <= 2e-2 * max|ref| per output tensor for bf16 storage with fp32
+accumulation, 1e-4 * max|ref| for fp32 (the bounds stated for this block).
+Small cases are compared element by element on every output; the full-size
+workloads are compared on sampled token rows (Y, dX) and sampled hidden
+units (columns of dW1 / dW3, rows of dW2), each computed by the oracle from
+its own definition, in the launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic_inputs as si
+from gpu_helpers import cat_cols, cat_rows, rel_err, run_gpu, to_np, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_compare(tp, T, d, d_i, act, dtype, seed=1234, check_intermediates=True):
+    inp = si.make_inputs(T, d, d_i, act, dtype, seed)
+    g = run_gpu(tp, inp, act, dtype)
+    f = oracle.forward(inp.X, inp.W1, inp.W2, act=act, W3=inp.W3)
+    b = oracle.backward(inp.X, inp.W1, inp.W2, inp.dY, act=act, W3=inp.W3)
+    tol = tol_for(dtype)
+    errs = {
+        "Y": rel_err(to_np(g["Y"]), f["Y"]),
+        "dX": rel_err(to_np(g["dX"]), b["dX"]),
+        "dW1": rel_err(cat_cols(g["dW1"]), b["dW1"]),
+        "dW2": rel_err(cat_rows(g["dW2"]), b["dW2"]),
+    }
+    if act == "swiglu":
+        errs["dW3"] = rel_err(cat_cols(g["dW3"]), b["dW3"])
+    if check_intermediates:
+        t = len(d_i)
+        errs["H"] = rel_err(cat_cols(g["H"]), f["H"])
+        errs["A"] = rel_err(cat_cols(g["saved"][:t]), f["A"])
+        errs["dA"] = rel_err(cat_cols(g["dact"][:t]), b["dA"])
+        if act == "swiglu":
+            errs["U"] = rel_err(cat_cols(g["saved"][t:]), f["U"])
+            errs["dU"] = rel_err(cat_cols(g["dact"][t:]), b["dU"])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"over tolerance {tol}: {bad} (all: {errs})"
+    return errs
+
+
+# ------------------------------------------------------------- small, ragged, every tail
+
+SMALL_CASES = [
+    # T, d, d_i: tiles of 128 x 256 with ragged tails in M, N and K, unequal shards
+    (200, 72, (40, 136, 64)),
+    (128, 256, (256,)),
+    (333, 200, (8, 96, 264, 152)),
+    (64, 64, (64, 64)),
+    (257, 136, (120, 392)),
+    (1, 8, (8,)),
+    (37, 24, (8, 8, 8, 8, 8, 8, 8, 8, 8, 8, 8, 8, 8, 8, 8, 8)),  # 16 shards of width 8
+]
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("case", SMALL_CASES, ids=[f"T{c[0]}_d{c[1]}_t{len(c[2])}" for c in SMALL_CASES])
+def test_small_bf16_all_outputs(gpu_lib, act, case):
+    T, d, d_i = case
+    _full_compare(gpu_lib, T, d, d_i, act, "bf16")
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_multi_wave_bf16(gpu_lib, act):
+    # more tiles than SMs in every launch, several K blocks per shard
+    _full_compare(gpu_lib, 1024, 384, (512, 384, 640, 256), act, "bf16")
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("case", [(32, 64, (128, 128)), (45, 36, (20, 44)), (130, 100, (64, 36, 100))])
+def test_fp32_path(gpu_lib, act, case):
+    T, d, d_i = case
+    _full_compare(gpu_lib, T, d, d_i, act, "fp32")
+
+
+def test_config_C1_fp32(gpu_lib):
+    w = si.WORKLOADS["C1"]
+    _full_compare(gpu_lib, w.T, w.d, w.d_i, w.act, w.dtype)
+
+
+# ------------------------------------------------------------- full-size workloads (sampled)
+
+def _sampled_compare(tp, w: si.Workload, nrows=24, nunits=24, seed=1234):
+    inp = si.make_workload_inputs(w, seed)
+    g = run_gpu(tp, inp, w.act, w.dtype)
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, nrows, replace=False)]))
+    units = np.unique(np.concatenate([[0, w.dff - 1], rng.choice(w.dff, nunits, replace=False)]))
+    # include the first and last unit of every shard (shard boundaries)
+    for lo, hi in si.shard_slices(w.d_i):
+        units = np.union1d(units, [lo, hi - 1])
+    Yr, dXr = oracle.rows(inp.X, inp.W1, inp.W2, inp.dY, rows, act=w.act, W3=inp.W3)
+    c1, c3, c2 = oracle.wgrad_units(inp.X, inp.W1, inp.W2, inp.dY, units, act=w.act, W3=inp.W3)
+    Y = to_np(g["Y"])[rows]
+    dX = to_np(g["dX"])[rows]
+    dW1 = cat_cols(g["dW1"])[:, units].T
+    dW2 = cat_rows(g["dW2"])[units, :]
+    tol = tol_for(w.dtype)
+    errs = {"Y": rel_err(Y, Yr), "dX": rel_err(dX, dXr), "dW1": rel_err(dW1, c1), "dW2": rel_err(dW2, c2)}
+    if w.act == "swiglu":
+        errs["dW3"] = rel_err(cat_cols(g["dW3"])[:, units].T, c3)
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"{w.name}: over tolerance {tol}: {bad} (all: {errs})"
+    # properties that hold at any size: finite outputs everywhere
+    for k in ("Y", "dX"):
+        assert torch.isfinite(g[k]).all()
+    for k in ("dW1", "dW2"):
+        assert all(torch.isfinite(x).all() for x in g[k])
+    return g, errs
+
+
+@pytest.mark.parametrize("name", ["C2t1", "C2t2", "C2t4", "C3", "C4", "C5"])
+def test_workload_sampled_parity(gpu_lib, name):
+    _sampled_compare(gpu_lib, si.WORKLOADS[name])
+
+
+def test_C2_shard_count_invariance(gpu_lib):
+    """C2 at t = 1, 2, 4: the same full weights give the same outputs within the bound."""
+    w1 = si.WORKLOADS["C2t1"]
+    inp = si.make_workload_inputs(w1)
+    outs = {}
+    for t in (1, 2, 4):
+        d_i = tuple([w1.dff // t] * t)
+        g = run_gpu(gpu_lib, inp, "gelu", "bf16", d_i=d_i)
+        outs[t] = {"Y": to_np(g["Y"]), "dX": to_np(g["dX"]), "dW1": cat_cols(g["dW1"]), "dW2": cat_rows(g["dW2"])}
+        del g
+        torch.cuda.empty_cache()
+    for a, b in ((1, 2), (1, 4), (2, 4)):
+        for k in outs[1]:
+            e = rel_err(outs[b][k], outs[a][k])
+            assert e <= 2e-2, f"t={a} vs t={b}: {k} differs by {e}"
