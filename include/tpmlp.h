@@ -158,6 +158,10 @@ TPMLP_API tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpml
 TPMLP_API const char* tpmlp_status_string(tpmlp_status status);
 /* The last CUDA error code seen by this thread (0 if none), for TPMLP_ERR_CUDA. */
 TPMLP_API int tpmlp_last_cuda_error(void);
+/* Description of the last failure on this thread (argument, CUDA or tensor
+ * map error; empty string after a successful call).  Static storage per
+ * thread, valid until the next call on the same thread.                      */
+TPMLP_API const char* tpmlp_last_error(void);
 /* ABI version: 100 * major + minor. */
 TPMLP_API int tpmlp_version(void);
 

@@ -24,7 +24,7 @@ __all__ = [
     "TpmlpError", "load", "Plan", "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size",
     "tpmlp_forward", "tpmlp_backward", "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_backward_dgrad",
     "tpmlp_backward_fsum", "tpmlp_check", "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version",
-    "tpmlp_last_launch_count", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
+    "tpmlp_last_launch_count", "tpmlp_last_error", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
 ]
 
 ACT = {"gelu": 0, "swiglu": 1}
@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size", "tpmlp_forward", "tpmlp_backward",
     "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_backward_dgrad", "tpmlp_backward_fsum", "tpmlp_check",
     "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version", "tpmlp_last_launch_count",
+    "tpmlp_last_error",
 )
 
 
@@ -46,8 +47,10 @@ class TpmlpError(RuntimeError):
         self.status = int(status)
         name = STATUS.get(self.status, f"status {status}")
         extra = ""
-        if self.status == 5 and _lib is not None:
-            extra = f" (cuda error {_lib.tpmlp_last_cuda_error()})"
+        if _lib is not None:
+            msg = _lib.tpmlp_last_error()
+            if msg:
+                extra = f": {msg.decode(errors='replace')}"
         super().__init__(f"{where}: {name}{extra}")
 
 
@@ -97,6 +100,8 @@ def load():
         lib.tpmlp_check.restype = st
         lib.tpmlp_status_string.argtypes = [i32]
         lib.tpmlp_status_string.restype = ctypes.c_char_p
+        lib.tpmlp_last_error.argtypes = []
+        lib.tpmlp_last_error.restype = ctypes.c_char_p
         lib.tpmlp_last_cuda_error.argtypes = []
         lib.tpmlp_last_cuda_error.restype = i32
         lib.tpmlp_version.argtypes = []
@@ -228,6 +233,10 @@ def tpmlp_status_string(status: int) -> str:
 
 def tpmlp_last_cuda_error() -> int:
     return int(load().tpmlp_last_cuda_error())
+
+
+def tpmlp_last_error() -> str:
+    return load().tpmlp_last_error().decode(errors="replace")
 
 
 def tpmlp_version() -> int:

@@ -6,6 +6,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdarg>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -32,6 +34,16 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 thread_local int g_last_launches = 0;
+thread_local char g_last_error[256] = "";
+
+tpmlp_status fail(tpmlp_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+tpmlp_status fail(tpmlp_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
 
 constexpr int kTileM = 128;
 constexpr int kSimtTile = 32;
@@ -39,7 +51,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000 * 1000;  // 2 s
 
 tpmlp_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
-  return TPMLP_ERR_CUDA;
+  return fail(TPMLP_ERR_CUDA, "CUDA error %d (%s)", static_cast<int>(e), cudaGetErrorString(e));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -70,8 +82,14 @@ tpmlp_status device_info(DeviceInfo* out) {
     cache[dev] = di;
   }
   *out = cache[dev];
+  // Bind the device's primary context to this thread (threads that only ran
+  // runtime calls without a context, such as autograd's worker, have none
+  // current; the tensor-map encoder is a driver call and needs one).
+  if ((e = cudaSetDevice(dev)) != cudaSuccess) return cuda_fail(e);
   // The kernels are built for sm_103a only (GB300).
-  if (out->cc_major != 10 || out->cc_minor != 3) return TPMLP_ERR_UNSUPPORTED;
+  if (out->cc_major != 10 || out->cc_minor != 3)
+    return fail(TPMLP_ERR_UNSUPPORTED, "device %d is sm_%d%d; the kernels are built for sm_103a", dev, out->cc_major,
+                out->cc_minor);
   return TPMLP_OK;
 }
 
@@ -92,9 +110,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D row-major bf16 [rows x cols]; 64 x 64 boxes, 128-byte swizzle,
 // out-of-range elements read as zero.
-bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+// Returns 0 on success, the CUresult otherwise (-1: entry point unavailable).
+int encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn) return -1;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
   cuuint32_t box[2] = {64, 64};
@@ -102,7 +121,7 @@ bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return static_cast<int>(r);
 }
 
 // ------------------------------------------------------------------ problem lists
@@ -111,6 +130,7 @@ struct Builder {
   bool tc;  // tensor-core path (tensor maps) or fp32 SIMT path
   int tile_m;
   std::vector<const void*> map_ptr;
+  std::vector<int64_t> map_rows, map_cols;
   bool map_error = false;
   int cur_group = -1;
 
@@ -123,14 +143,22 @@ struct Builder {
   int map(const void* ptr, int64_t rows, int64_t cols) {
     if (!tc) return -1;
     for (size_t i = 0; i < map_ptr.size(); ++i)
-      if (map_ptr[i] == ptr) return static_cast<int>(i);
+      if (map_ptr[i] == ptr && map_rows[i] == rows && map_cols[i] == cols) return static_cast<int>(i);
     if (p->num_maps >= kMaxMaps) {
       map_error = true;
+      fail(TPMLP_ERR_INVALID_ARG, "more than %d tensor maps in one launch", kMaxMaps);
       return 0;
     }
     const int idx = p->num_maps++;
-    if (!encode_map(&p->maps[idx], ptr, rows, cols)) map_error = true;
+    const int r = encode_map(&p->maps[idx], ptr, rows, cols);
+    if (r != 0) {
+      map_error = true;
+      fail(TPMLP_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for %p [%lld x %lld]", r, ptr,
+           static_cast<long long>(rows), static_cast<long long>(cols));
+    }
     map_ptr.push_back(ptr);
+    map_rows.push_back(rows);
+    map_cols.push_back(cols);
     return idx;
   }
 
@@ -199,7 +227,7 @@ int band_for(int sms) {
 
 tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan* plan, void* workspace,
                     cudaStream_t stream) {
-  if (B.map_error) return TPMLP_ERR_INVALID_ARG;
+  if (B.map_error) return TPMLP_ERR_INVALID_ARG;  // message set by Builder::map
   GemmParams& p = *B.p;
   if (p.total_tiles == 0) return TPMLP_OK;
   p.status = static_cast<int32_t*>(workspace);
@@ -217,42 +245,37 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
 }
 
 // ------------------------------------------------------------------ checks
-tpmlp_status check_ptrs(const tpmlp_plan* pl, std::initializer_list<const void*> must, bool t_rows_may_be_null) {
-  for (const void* q : must) {
-    if (!q) {
-      if (t_rows_may_be_null) continue;
-      return TPMLP_ERR_INVALID_ARG;
-    }
-    if (!aligned16(q)) return TPMLP_ERR_ALIGNMENT;
-  }
-  (void)pl;
-  return TPMLP_OK;
-}
-
-tpmlp_status check_array(const void* const* arr, int n, bool may_be_null_entries) {
-  if (!arr) return TPMLP_ERR_INVALID_ARG;
-  for (int i = 0; i < n; ++i) {
-    if (!arr[i]) {
-      if (may_be_null_entries) continue;
-      return TPMLP_ERR_INVALID_ARG;
-    }
-    if (!aligned16(arr[i])) return TPMLP_ERR_ALIGNMENT;
-  }
-  return TPMLP_OK;
-}
-
 #define TPMLP_TRY(expr)                   \
   do {                                    \
     tpmlp_status st_ = (expr);            \
     if (st_ != TPMLP_OK) return st_;      \
   } while (0)
 
+tpmlp_status check_ptr(const char* name, const void* q, bool may_be_null) {
+  if (!q) return may_be_null ? TPMLP_OK : fail(TPMLP_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(q)) return fail(TPMLP_ERR_ALIGNMENT, "%s (%p) is not 16-byte aligned", name, q);
+  return TPMLP_OK;
+}
+
+tpmlp_status check_array(const char* name, const void* const* arr, int n, bool may_be_null_entries) {
+  if (!arr) return fail(TPMLP_ERR_INVALID_ARG, "pointer array %s is NULL", name);
+  for (int i = 0; i < n; ++i) {
+    if (!arr[i]) {
+      if (may_be_null_entries) continue;
+      return fail(TPMLP_ERR_INVALID_ARG, "%s[%d] is NULL", name, i);
+    }
+    if (!aligned16(arr[i])) return fail(TPMLP_ERR_ALIGNMENT, "%s[%d] (%p) is not 16-byte aligned", name, i, arr[i]);
+  }
+  return TPMLP_OK;
+}
+
 bool swiglu(const tpmlp_plan* pl) { return pl->act == TPMLP_ACT_SWIGLU; }
 int nsaved(const tpmlp_plan* pl) { return swiglu(pl) ? 2 * pl->t : pl->t; }
 
 tpmlp_status common_checks(const tpmlp_plan* pl, void* workspace, DeviceInfo* di) {
-  if (!pl) return TPMLP_ERR_INVALID_ARG;
-  if (!workspace || !aligned16(workspace)) return workspace ? TPMLP_ERR_ALIGNMENT : TPMLP_ERR_INVALID_ARG;
+  g_last_error[0] = 0;
+  if (!pl) return fail(TPMLP_ERR_INVALID_ARG, "plan is NULL");
+  TPMLP_TRY(check_ptr("workspace", workspace, false));
   return device_info(di);
 }
 
@@ -379,23 +402,33 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
 extern "C" {
 
 tpmlp_status tpmlp_plan_create(const tpmlp_desc* desc, tpmlp_plan** out) {
-  if (!out) return TPMLP_ERR_INVALID_ARG;
+  g_last_error[0] = 0;
+  if (!out) return fail(TPMLP_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
-  if (!desc || !desc->d_i) return TPMLP_ERR_INVALID_ARG;
-  if (desc->act != TPMLP_ACT_GELU && desc->act != TPMLP_ACT_SWIGLU) return TPMLP_ERR_INVALID_ARG;
-  if (desc->dtype != TPMLP_BF16 && desc->dtype != TPMLP_FP32) return TPMLP_ERR_INVALID_ARG;
-  if (desc->T < 0 || desc->d < 1 || desc->t < 1 || desc->t > TPMLP_MAX_SHARDS) return TPMLP_ERR_SHAPE;
+  if (!desc || !desc->d_i) return fail(TPMLP_ERR_INVALID_ARG, "desc or desc->d_i is NULL");
+  if (desc->act != TPMLP_ACT_GELU && desc->act != TPMLP_ACT_SWIGLU)
+    return fail(TPMLP_ERR_INVALID_ARG, "unknown act %d", static_cast<int>(desc->act));
+  if (desc->dtype != TPMLP_BF16 && desc->dtype != TPMLP_FP32)
+    return fail(TPMLP_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(desc->dtype));
+  if (desc->T < 0 || desc->d < 1 || desc->t < 1 || desc->t > TPMLP_MAX_SHARDS)
+    return fail(TPMLP_ERR_SHAPE, "need T >= 0, d >= 1, 1 <= t <= %d (got T=%lld d=%lld t=%d)", TPMLP_MAX_SHARDS,
+                static_cast<long long>(desc->T), static_cast<long long>(desc->d), desc->t);
   const int64_t mult = desc->dtype == TPMLP_BF16 ? 8 : 4;
   const int64_t kMax32 = (int64_t(1) << 31) - 1;
   int64_t dff = 0;
   for (int i = 0; i < desc->t; ++i) {
-    if (desc->d_i[i] < 1) return TPMLP_ERR_SHAPE;
+    if (desc->d_i[i] < 1) return fail(TPMLP_ERR_SHAPE, "d_i[%d] = %lld < 1", i, static_cast<long long>(desc->d_i[i]));
     dff += desc->d_i[i];
   }
-  if (desc->d % mult) return TPMLP_ERR_ALIGNMENT;
+  if (desc->d % mult)
+    return fail(TPMLP_ERR_ALIGNMENT, "d = %lld is not a multiple of %lld", static_cast<long long>(desc->d),
+                static_cast<long long>(mult));
   for (int i = 0; i < desc->t; ++i)
-    if (desc->d_i[i] % mult) return TPMLP_ERR_ALIGNMENT;
-  if (desc->T > kMax32 || desc->d > kMax32 || dff > kMax32) return TPMLP_ERR_UNSUPPORTED;
+    if (desc->d_i[i] % mult)
+      return fail(TPMLP_ERR_ALIGNMENT, "d_i[%d] = %lld is not a multiple of %lld", i,
+                  static_cast<long long>(desc->d_i[i]), static_cast<long long>(mult));
+  if (desc->T > kMax32 || desc->d > kMax32 || dff > kMax32)
+    return fail(TPMLP_ERR_UNSUPPORTED, "T, d and d_ff must each be below 2^31");
   tpmlp_plan* pl = new (std::nothrow) tpmlp_plan;
   if (!pl) return TPMLP_ERR_INVALID_ARG;
   pl->T = desc->T;
@@ -431,11 +464,11 @@ tpmlp_status tpmlp_forward_column(const tpmlp_plan* plan, const void* X, const v
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
   const bool tz = plan->T == 0;
-  TPMLP_TRY(check_ptrs(plan, {X}, tz));
-  TPMLP_TRY(check_array(W1, plan->t, false));
-  if (swiglu(plan)) TPMLP_TRY(check_array(W3, plan->t, false));
-  TPMLP_TRY(check_array(saved, nsaved(plan), tz));
-  TPMLP_TRY(check_array(H, plan->t, tz));
+  TPMLP_TRY(check_ptr("X", X, tz));
+  TPMLP_TRY(check_array("W1", W1, plan->t, false));
+  if (swiglu(plan)) TPMLP_TRY(check_array("W3", W3, plan->t, false));
+  TPMLP_TRY(check_array("saved", saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array("H", H, plan->t, tz));
   return fwd_column(plan, di, X, W1, W3, saved, H, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -445,9 +478,9 @@ tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* const* W2, vo
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
   const bool tz = plan->T == 0;
-  TPMLP_TRY(check_array(W2, plan->t, false));
-  TPMLP_TRY(check_array(H, plan->t, tz));
-  TPMLP_TRY(check_ptrs(plan, {Y}, tz));
+  TPMLP_TRY(check_array("W2", W2, plan->t, false));
+  TPMLP_TRY(check_array("H", H, plan->t, tz));
+  TPMLP_TRY(check_ptr("Y", Y, tz));
   return fwd_row(plan, di, W2, Y, H, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -458,12 +491,12 @@ tpmlp_status tpmlp_forward(const tpmlp_plan* plan, const void* X, const void* co
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
   const bool tz = plan->T == 0;
-  TPMLP_TRY(check_ptrs(plan, {X, Y}, tz));
-  TPMLP_TRY(check_array(W1, plan->t, false));
-  if (swiglu(plan)) TPMLP_TRY(check_array(W3, plan->t, false));
-  TPMLP_TRY(check_array(W2, plan->t, false));
-  TPMLP_TRY(check_array(saved, nsaved(plan), tz));
-  TPMLP_TRY(check_array(H, plan->t, tz));
+  TPMLP_TRY(check_ptr("X", X, tz)); TPMLP_TRY(check_ptr("Y", Y, tz));
+  TPMLP_TRY(check_array("W1", W1, plan->t, false));
+  if (swiglu(plan)) TPMLP_TRY(check_array("W3", W3, plan->t, false));
+  TPMLP_TRY(check_array("W2", W2, plan->t, false));
+  TPMLP_TRY(check_array("saved", saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array("H", H, plan->t, tz));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   TPMLP_TRY(fwd_column(plan, di, X, W1, W3, saved, H, workspace, st));
   return fwd_row(plan, di, W2, Y, H, workspace, st);
@@ -476,12 +509,12 @@ tpmlp_status tpmlp_backward_dgrad(const tpmlp_plan* plan, const void* const* W2,
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
   const bool tz = plan->T == 0;
-  TPMLP_TRY(check_array(W2, plan->t, false));
-  TPMLP_TRY(check_array(saved, nsaved(plan), tz));
-  TPMLP_TRY(check_array(H, plan->t, tz));
-  TPMLP_TRY(check_ptrs(plan, {dY}, tz));
-  TPMLP_TRY(check_array(dact, nsaved(plan), tz));
-  TPMLP_TRY(check_array(dW2, plan->t, false));
+  TPMLP_TRY(check_array("W2", W2, plan->t, false));
+  TPMLP_TRY(check_array("saved", saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array("H", H, plan->t, tz));
+  TPMLP_TRY(check_ptr("dY", dY, tz));
+  TPMLP_TRY(check_array("dact", dact, nsaved(plan), tz));
+  TPMLP_TRY(check_array("dW2", dW2, plan->t, false));
   return bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -492,14 +525,14 @@ tpmlp_status tpmlp_backward_fsum(const tpmlp_plan* plan, const void* X, const vo
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
   const bool tz = plan->T == 0;
-  TPMLP_TRY(check_ptrs(plan, {X, dX}, tz));
-  TPMLP_TRY(check_array(W1, plan->t, false));
+  TPMLP_TRY(check_ptr("X", X, tz)); TPMLP_TRY(check_ptr("dX", dX, tz));
+  TPMLP_TRY(check_array("W1", W1, plan->t, false));
   if (swiglu(plan)) {
-    TPMLP_TRY(check_array(W3, plan->t, false));
-    TPMLP_TRY(check_array(dW3, plan->t, false));
+    TPMLP_TRY(check_array("W3", W3, plan->t, false));
+    TPMLP_TRY(check_array("dW3", dW3, plan->t, false));
   }
-  TPMLP_TRY(check_array(dact, nsaved(plan), tz));
-  TPMLP_TRY(check_array(dW1, plan->t, false));
+  TPMLP_TRY(check_array("dact", dact, nsaved(plan), tz));
+  TPMLP_TRY(check_array("dW1", dW1, plan->t, false));
   return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -511,18 +544,18 @@ tpmlp_status tpmlp_backward(const tpmlp_plan* plan, const void* X, const void* c
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
   const bool tz = plan->T == 0;
-  TPMLP_TRY(check_ptrs(plan, {X, dY, dX}, tz));
-  TPMLP_TRY(check_array(W1, plan->t, false));
-  TPMLP_TRY(check_array(W2, plan->t, false));
+  TPMLP_TRY(check_ptr("X", X, tz)); TPMLP_TRY(check_ptr("dY", dY, tz)); TPMLP_TRY(check_ptr("dX", dX, tz));
+  TPMLP_TRY(check_array("W1", W1, plan->t, false));
+  TPMLP_TRY(check_array("W2", W2, plan->t, false));
   if (swiglu(plan)) {
-    TPMLP_TRY(check_array(W3, plan->t, false));
-    TPMLP_TRY(check_array(dW3, plan->t, false));
+    TPMLP_TRY(check_array("W3", W3, plan->t, false));
+    TPMLP_TRY(check_array("dW3", dW3, plan->t, false));
   }
-  TPMLP_TRY(check_array(saved, nsaved(plan), tz));
-  TPMLP_TRY(check_array(H, plan->t, tz));
-  TPMLP_TRY(check_array(dact, nsaved(plan), tz));
-  TPMLP_TRY(check_array(dW1, plan->t, false));
-  TPMLP_TRY(check_array(dW2, plan->t, false));
+  TPMLP_TRY(check_array("saved", saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array("H", H, plan->t, tz));
+  TPMLP_TRY(check_array("dact", dact, nsaved(plan), tz));
+  TPMLP_TRY(check_array("dW1", dW1, plan->t, false));
+  TPMLP_TRY(check_array("dW2", dW2, plan->t, false));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   TPMLP_TRY(bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, workspace, st));
   return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, workspace, st);
@@ -559,6 +592,7 @@ const char* tpmlp_status_string(tpmlp_status s) {
 }
 
 int tpmlp_last_cuda_error(void) { return g_last_cuda_error; }
+const char* tpmlp_last_error(void) { return g_last_error; }
 int tpmlp_version(void) { return 100; }
 int tpmlp_last_launch_count(void) { return g_last_launches; }
 
