@@ -1,13 +1,21 @@
-// tc_gemm.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a with
-// the MLP block's fused epilogues.
+// tc_gemm.cu -- persistent, warp-specialised 2-SM tcgen05 GEMM for sm_103a
+// with the MLP block's fused epilogues.
 //
-// One CTA per SM.  Warp 0 (one lane) streams 64x64 bf16 boxes of A and B
-// into a 4-stage shared-memory ring with TMA; warp 1 (one lane) allocates
-// 512 TMEM columns and issues tcgen05.mma into one of two 128x256 fp32
-// accumulators; warps 2..9 drain the other accumulator through tcgen05.ld,
-// apply the epilogue (store, GeLU / SwiGLU forward, GeLU' / SwiGLU'
-// backward) and write bf16 rows straight to HBM.  The two accumulators let
-// the epilogue of one tile run under the main loop of the next.
+// CTAs run in pairs (clusters of two, one CTA per SM).  A pair owns a
+// 256 x 256 output tile: each CTA holds 128 rows of A and half of B's columns
+// in its shared memory; the even CTA issues tcgen05.mma.cta_group::2, which
+// reads both CTAs' operands and writes each CTA's 128 rows of D into that
+// CTA's TMEM.  Per CTA:
+//   * warp 0 (one lane): TMA producer -- 2 A boxes and 2 B boxes of 64 x 64
+//     bf16 (32 KB) per 64-wide K block into a 7-stage ring; the completion of
+//     both CTAs' copies is counted on the even CTA's "full" barrier;
+//   * warp 1 (one lane, even CTA): allocates 512 TMEM columns in both CTAs,
+//     issues the MMAs into one of two 256-column accumulators and multicasts
+//     its commits (stage free, accumulator ready) to both CTAs;
+//   * warps 2..9: drain the other accumulator through tcgen05.ld, apply the
+//     epilogue (store, GeLU / SwiGLU forward, GeLU' / SwiGLU' backward) and
+//     write bf16 rows to HBM; the two accumulators let the epilogue of one
+//     tile run under the main loop of the next.
 //
 // The shard sums of the tensor-parallel MLP are K loops here: a problem
 // with several segments (one per shard) accumulates every segment's product
@@ -18,11 +26,13 @@
 // and the f/g table.)
 //
 // Every wait is bounded: after GemmParams::timeout_ns a waiting role records
-// a status code in the workspace, raises a shared abort flag that makes the
-// other roles leave their loops, waits (again bounded) for its own copies
-// and MMAs in flight, and the CTA frees its TMEM and exits.
+// a status code in the workspace, raises the abort flag of both CTAs, which
+// makes the other roles leave their loops, waits (again bounded) for its own
+// copies and MMAs in flight, and the pair frees its TMEM and exits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "act.cuh"
 #include "ptx.cuh"
@@ -31,11 +41,12 @@
 namespace tpmlp {
 namespace {
 
-constexpr int kBM = 128;                        // tile rows (MMA M)
+constexpr int kBM = 128;                        // rows of A / D per CTA
+constexpr int kPairM = 2 * kBM;                 // rows of a pair's tile
 constexpr int kBK = 64;                         // K per stage (one 128-byte swizzle row of bf16)
-constexpr int kStages = 4;
+constexpr int kStages = 7;
 constexpr int kBoxBytes = 64 * 64 * 2;          // one TMA box: 64 x 64 bf16
-constexpr int kStageBytes = 6 * kBoxBytes;      // 2 A boxes + 4 B boxes
+constexpr int kStageBytes = 4 * kBoxBytes;      // 2 A boxes + 2 B boxes
 constexpr int kNumEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kNumEpiWarps);
 constexpr int kTmemCols = 512;
@@ -44,6 +55,8 @@ constexpr int kNumAcc = 2;
 constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1;
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 8 * kNumBars + 16;
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
+constexpr uint64_t kPeerDrainNs = 2ull * 1000 * 1000;
+constexpr uint16_t kPairMask = 0x3;
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kNumAcc * kAccCols <= kTmemCols, "TMEM budget");
@@ -72,21 +85,28 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
   const Prob& P = p.probs[pi];
   TileInfo t;
   t.prob = pi;
-  t.m0 = mt * kBM;
+  t.m0 = mt * kPairM;
   t.n0 = n_lin * P.tile_n;
-  t.valid_m = min(kBM, P.M - t.m0);
+  t.valid_m = min(kPairM, P.M - t.m0);
   t.valid_n = min(P.tile_n, P.N - t.n0);
   return t;
 }
 
 struct Ctl {
   volatile int32_t* abort_flag;
+  uint32_t peer_abort;  // cluster address of the peer CTA's abort flag
   int32_t* status;
   uint64_t timeout_ns;
 };
 
+__device__ __forceinline__ void raise_abort(const Ctl& c, int32_t code) {
+  *c.abort_flag = 1;
+  ptx::st_cluster_u32(c.peer_abort, 1u);
+  if (c.status) atomicCAS(c.status, 0, code);
+}
+
 // Wait for the phase of `bar` with the given parity; false if the wait
-// timed out (status recorded) or another role aborted.
+// timed out (status recorded, both CTAs aborted) or an abort was raised.
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const Ctl& c, int32_t code) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -94,8 +114,7 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, cons
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*c.abort_flag) return false;
     if (ptx::globaltimer_ns() - t0 > c.timeout_ns) {
-      *c.abort_flag = 1;
-      if (c.status) atomicCAS(c.status, 0, code);
+      raise_abort(c, code);
       return false;
     }
   }
@@ -107,6 +126,36 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   while (!ptx::mbar_try_wait(bar, parity)) {
     if (ptx::globaltimer_ns() - t0 > kDrainTimeoutNs) return;
   }
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (ptx::globaltimer_ns() - t0 < ns) {
+  }
+}
+
+// What CTA `rank` of the pair loads and computes for one tile.
+struct PairShape {
+  int n_mma;   // MMA N (multiple of 32, covers the tile's valid columns)
+  int half;    // B columns held by each CTA (n_mma / 2)
+  int vm[2];   // valid A/D rows of each CTA
+  int nA[2];   // A boxes each CTA loads
+  int nB[2];   // B boxes (per B operand) each CTA loads
+};
+
+__device__ __forceinline__ PairShape pair_shape(const TileInfo& ti, bool dual) {
+  PairShape s;
+  const int cap = dual ? 128 : 256;
+  s.n_mma = min(cap, (ti.valid_n + 31) & ~31);
+  s.half = s.n_mma >> 1;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    s.vm[r] = max(0, min(kBM, ti.valid_m - kBM * r));
+    s.nA[r] = s.vm[r] > 64 ? 2 : (s.vm[r] > 0 ? 1 : 0);
+    const int vb = max(0, min(s.half, ti.valid_n - s.half * r));
+    s.nB[r] = (vb + 63) / 64;
+  }
+  return s;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -206,14 +255,18 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
 
   const uint32_t smem_base = ptx::smem_u32(smem);
   const uint32_t bar0 = ptx::smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kNumAcc + a); };
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };                        // even CTA: copies landed
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };           // both: stage consumed
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };       // both: accumulator ready
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kNumAcc + a); };  // even CTA: drained
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kNumAcc);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -222,7 +275,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
     }
     for (int a = 0; a < kNumAcc; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
-      ptx::mbar_init(tempty_bar(a), kNumEpiWarps);
+      ptx::mbar_init(tempty_bar(a), 2 * kNumEpiWarps);
     }
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -232,17 +285,18 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
     for (int i = 0; i < p.num_maps; ++i) ptx::prefetch_tmap(&p.maps[i]);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_holder), kTmemCols);
+    ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+  const Ctl ctl{abort_flag, ptx::map_to_cta(ptx::smem_u32(const_cast<int32_t*>(abort_flag)), rank ^ 1u), p.status,
+                p.timeout_ns};
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -250,13 +304,19 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
 #pragma unroll
       for (int s = 0; s < kStages; ++s) armed_parity[s] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+      bool issued = false;
+      for (int tile = pair; ok && tile < p.total_tiles; tile += npairs) {
         const TileInfo ti = decode_tile(p, tile);
         const Prob& P = p.probs[ti.prob];
         const bool dual = P.epi == EPI_SWIGLU_FWD;
-        const int nA = ti.valid_m > 64 ? 2 : 1;
-        const int nB = (ti.valid_n + 63) / 64;
-        const uint32_t bytes = static_cast<uint32_t>((nA + nB * (dual ? 2 : 1)) * kBoxBytes);
+        const PairShape ps = pair_shape(ti, dual);
+        const int nops = dual ? 2 : 1;
+        const uint32_t bytes_pair =
+            static_cast<uint32_t>((ps.nA[0] + ps.nA[1] + nops * (ps.nB[0] + ps.nB[1])) * kBoxBytes);
+        const int my_nA = leader ? ps.nA[0] : ps.nA[1];
+        const int my_nB = leader ? ps.nB[0] : ps.nB[1];
+        const int a_row = ti.m0 + kBM * static_cast<int>(rank);
+        const int b_col = ti.n0 + ps.half * static_cast<int>(rank);
         for (int s = P.seg_begin; ok && s < P.seg_begin + P.seg_count; ++s) {
           const Seg& S = p.segs[s];
           const void* ma = &p.maps[S.a_map];
@@ -268,26 +328,27 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
               ok = false;
               break;
             }
-            const uint32_t fb = full_bar(stage);
-            ptx::mbar_arrive_expect_tx(fb, bytes);
-            armed_parity[stage] = static_cast<int>(phase);
+            if (leader) {
+              ptx::mbar_arrive_expect_tx(full_bar(stage), bytes_pair);
+              armed_parity[stage] = static_cast<int>(phase);
+            }
+            const uint32_t fb = ptx::map_to_cta(full_bar(stage), 0);
             const uint32_t sb = smem_base + stage * kStageBytes;
             const int k0 = kb * kBK;
-            for (int b = 0; b < nA; ++b) {
+            for (int b = 0; b < my_nA; ++b) {
               if (P.a_major == MAJOR_MN)
-                ptx::tma_load_2d(sb + b * kBoxBytes, ma, ti.m0 + 64 * b, k0, fb);
+                ptx::tma_load_2d_pair(sb + b * kBoxBytes, ma, a_row + 64 * b, k0, fb);
               else
-                ptx::tma_load_2d(sb + b * kBoxBytes, ma, k0, ti.m0 + 64 * b, fb);
+                ptx::tma_load_2d_pair(sb + b * kBoxBytes, ma, k0, a_row + 64 * b, fb);
             }
-            for (int j = 0; j < nB; ++j) {
+            for (int j = 0; j < my_nB; ++j) {
               if (P.b_major == MAJOR_MN)
-                ptx::tma_load_2d(sb + (2 + j) * kBoxBytes, mb, ti.n0 + 64 * j, k0, fb);
+                ptx::tma_load_2d_pair(sb + (2 + j) * kBoxBytes, mb, b_col + 64 * j, k0, fb);
               else
-                ptx::tma_load_2d(sb + (2 + j) * kBoxBytes, mb, k0, ti.n0 + 64 * j, fb);
+                ptx::tma_load_2d_pair(sb + (2 + j) * kBoxBytes, mb, k0, b_col + 64 * j, fb);
             }
-            if (dual) {
-              for (int j = 0; j < nB; ++j) ptx::tma_load_2d(sb + (4 + j) * kBoxBytes, mb2, ti.n0 + 64 * j, k0, fb);
-            }
+            if (dual && my_nB > 0) ptx::tma_load_2d_pair(sb + 3 * kBoxBytes, mb2, b_col, k0, fb);
+            issued = true;
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -295,28 +356,30 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
           }
         }
       }
-      if (!ok) {
+      if (!ok && issued) {
         // Let every copy already issued land before the CTA can exit.
-        for (int s = 0; s < kStages; ++s)
-          if (armed_parity[s] >= 0) drain_wait(full_bar(s), static_cast<uint32_t>(armed_parity[s]));
+        if (leader) {
+          for (int s = 0; s < kStages; ++s)
+            if (armed_parity[s] >= 0) drain_wait(full_bar(s), static_cast<uint32_t>(armed_parity[s]));
+        }
+        spin_ns(kPeerDrainNs);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+      for (int tile = pair; ok && tile < p.total_tiles; tile += npairs) {
         const TileInfo ti = decode_tile(p, tile);
         const Prob& P = p.probs[ti.prob];
         const bool dual = P.epi == EPI_SWIGLU_FWD;
-        const int n_cap = dual ? 128 : 256;
-        const int n_mma = min(n_cap, (ti.valid_n + 15) & ~15);
-        const uint32_t idesc = ptx::make_idesc_bf16(kBM, n_mma, P.a_major, P.b_major);
+        const PairShape ps = pair_shape(ti, dual);
+        const uint32_t idesc = ptx::make_idesc_bf16(kPairM, ps.n_mma, P.a_major, P.b_major);
         if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, ctl, kDevTimeoutMma)) {
           ok = false;
           break;
@@ -342,15 +405,15 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
                                                         : ptx::make_sdesc_sw128(sa + 32u * j, 16, 1024);
               const uint64_t bd = P.b_major == MAJOR_MN ? ptx::make_sdesc_sw128(sb + 2048u * j, kBoxBytes, 1024)
                                                         : ptx::make_sdesc_sw128(sb + 32u * j, 16, 1024);
-              ptx::mma_bf16(d_tmem, ad, bd, idesc, accumulate);
+              ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
               if (dual) {
-                const uint64_t bd2 = ptx::make_sdesc_sw128(sb + 2 * kBoxBytes + 2048u * j, kBoxBytes, 1024);
-                ptx::mma_bf16(d_tmem + 128u, ad, bd2, idesc, accumulate);
+                const uint64_t bd2 = ptx::make_sdesc_sw128(sb + kBoxBytes + 2048u * j, kBoxBytes, 1024);
+                ptx::mma_bf16_pair(d_tmem + 128u, ad, bd2, idesc, accumulate);
               }
               accumulate = 1;
               issued = true;
             }
-            ptx::mma_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
+            ptx::mma_commit_pair_mc(empty_bar(stage), kPairMask);  // stage free in both CTAs
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -358,7 +421,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
           }
         }
         if (!ok) break;
-        ptx::mma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+        ptx::mma_commit_pair_mc(tfull_bar(acc), kPairMask);  // accumulator ready in both CTAs
         if (++acc == kNumAcc) {
           acc = 0;
           acc_phase ^= 1u;
@@ -366,62 +429,65 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       }
       if (!ok && issued) {
         // Every MMA issued so far must finish before TMEM is released.
-        ptx::mma_commit(drain_bar);
+        ptx::mma_commit_pair(drain_bar);
         drain_wait(drain_bar, 0);
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;              // TMEM lane quarter this warp may read
     const int half = (warp - 2) >> 2;    // which half of the tile's columns
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    for (int tile = pair; tile < p.total_tiles; tile += npairs) {
       const TileInfo ti = decode_tile(p, tile);
       const Prob& P = p.probs[ti.prob];
       if (!bounded_wait(tfull_bar(acc), acc_phase, ctl, kDevTimeoutEpilogue)) break;
       ptx::tc_fence_after();
       const int row = q * 32 + lane;
-      const bool row_ok = row < ti.valid_m;
-      const int64_t grow = static_cast<int64_t>(ti.m0) + row;
+      const int vm = max(0, min(kBM, ti.valid_m - kBM * static_cast<int>(rank)));
+      const bool row_ok = row < vm;
+      const int64_t grow = static_cast<int64_t>(ti.m0) + kBM * static_cast<int>(rank) + row;
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
-      if (P.epi == EPI_SWIGLU_FWD) {
+      if (vm > 0) {
+        if (P.epi == EPI_SWIGLU_FWD) {
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          const int col = half * 64 + c * 32;
-          if (col >= ti.valid_n) break;
-          uint32_t rg[32], ru[32];
-          ptx::tmem_ld_32x32b_x32(tacc + col, rg);
-          ptx::tmem_ld_32x32b_x32(tacc + 128u + col, ru);
-          ptx::tmem_wait_ld();
-          if (row_ok) {
-            const int nvalid = min(32, ti.valid_n - col);
-            float g[32], u[32], h[32];
+          for (int c = 0; c < 2; ++c) {
+            const int col = half * 64 + c * 32;
+            if (col >= ti.valid_n) break;
+            uint32_t rg[32], ru[32];
+            ptx::tmem_ld_32x32b_x32(tacc + col, rg);
+            ptx::tmem_ld_32x32b_x32(tacc + 128u + col, ru);
+            ptx::tmem_wait_ld();
+            if (row_ok) {
+              const int nvalid = min(32, ti.valid_n - col);
+              float g[32], u[32], h[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              g[j] = __uint_as_float(rg[j]);
-              u[j] = __uint_as_float(ru[j]);
-              h[j] = u[j] * act::swish(g[j]);
+              for (int j = 0; j < 32; ++j) {
+                g[j] = __uint_as_float(rg[j]);
+                u[j] = __uint_as_float(ru[j]);
+                h[j] = u[j] * act::swish(g[j]);
+              }
+              store_row32(P.out0, P.ldo, grow, ti.n0 + col, nvalid, g);
+              store_row32(P.out1, P.ldo, grow, ti.n0 + col, nvalid, u);
+              store_row32(P.out2, P.ldo, grow, ti.n0 + col, nvalid, h);
             }
-            store_row32(P.out0, P.ldo, grow, ti.n0 + col, nvalid, g);
-            store_row32(P.out1, P.ldo, grow, ti.n0 + col, nvalid, u);
-            store_row32(P.out2, P.ldo, grow, ti.n0 + col, nvalid, h);
           }
-        }
-      } else {
+        } else {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          const int col = half * 128 + c * 32;
-          if (col >= ti.valid_n) break;
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(tacc + col, r);
-          ptx::tmem_wait_ld();
-          if (row_ok) epilogue_chunk(P, grow, ti.n0 + col, min(32, ti.valid_n - col), r);
+          for (int c = 0; c < 4; ++c) {
+            const int col = half * 128 + c * 32;
+            if (col >= ti.valid_n) break;
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(tacc + col, r);
+            ptx::tmem_wait_ld();
+            if (row_ok) epilogue_chunk(P, grow, ti.n0 + col, min(32, ti.valid_n - col), r);
+          }
         }
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_to_cta(tempty_bar(acc), 0));
       if (++acc == kNumAcc) {
         acc = 0;
         acc_phase ^= 1u;
@@ -430,11 +496,11 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -454,19 +520,66 @@ TPMLP_TC_KERNEL(tpmlp_bwd_dx_fsum_wgrad1)
 
 int tc_gemm_max_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int grid, cudaStream_t stream) {
-  void (*k)(GemmParams) = nullptr;
-  switch (kernel_tag) {
-    case TAG_FWD_COLUMN: k = tpmlp_fwd_column_gemm_act; break;
-    case TAG_FWD_ROW: k = tpmlp_fwd_row_gemm_gsum; break;
-    case TAG_BWD_DGRAD: k = tpmlp_bwd_dgrad_act_wgrad2; break;
-    case TAG_BWD_FSUM: k = tpmlp_bwd_dx_fsum_wgrad1; break;
-    default: return cudaErrorInvalidValue;
+using KernelFn = void (*)(GemmParams);
+
+KernelFn kernel_for(int tag) {
+  switch (tag) {
+    case TAG_FWD_COLUMN: return tpmlp_fwd_column_gemm_act;
+    case TAG_FWD_ROW: return tpmlp_fwd_row_gemm_gsum;
+    case TAG_BWD_DGRAD: return tpmlp_bwd_dgrad_act_wgrad2;
+    case TAG_BWD_FSUM: return tpmlp_bwd_dx_fsum_wgrad1;
+    default: return nullptr;
   }
+}
+
+// Pairs (clusters of two CTAs) that can be resident at once on this device.
+int tc_gemm_max_pairs(int tag) {
+  static std::mutex mu;
+  static int cache[64][4] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || tag < 0 || tag > 3) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev][tag] > 0) return cache[dev][tag];
+  KernelFn k = kernel_for(tag);
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) return 0;
+  cache[dev][tag] = n;
+  return n;
+}
+
+cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int max_pairs_hint, cudaStream_t stream) {
+  KernelFn k = kernel_for(kernel_tag);
+  if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  int pairs = tc_gemm_max_pairs(kernel_tag);
+  if (pairs <= 0) pairs = max_pairs_hint > 0 ? max_pairs_hint : 1;
+  pairs = pairs < p.total_tiles ? pairs : p.total_tiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
 }
 
 }  // namespace tpmlp

@@ -45,7 +45,7 @@ tpmlp_status fail(tpmlp_status st, const char* fmt, ...) {
   return st;
 }
 
-constexpr int kTileM = 128;
+constexpr int kTileM = 256;  // rows of a CTA pair's tile
 constexpr int kSimtTile = 32;
 constexpr uint64_t kDefaultTimeoutNs = 2000ull * 1000 * 1000;  // 2 s
 
@@ -219,9 +219,10 @@ GemmParams* scratch_params() {
 }
 
 int band_for(int sms) {
-  // CTAs running at the same time cover about a square block of tiles.
+  // The pairs running at the same time cover about a square block of tiles.
+  const int pairs = sms / 2;
   int b = 1;
-  while ((b + 1) * (b + 1) <= sms) ++b;
+  while ((b + 1) * (b + 1) <= pairs) ++b;
   return b;
 }
 
@@ -234,8 +235,7 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
   p.timeout_ns = plan->timeout_ns;
   cudaError_t e;
   if (B.tc) {
-    const int grid = std::min(p.total_tiles, di.sms);
-    e = launch_tc_gemm(p, tag, grid, stream);
+    e = launch_tc_gemm(p, tag, di.sms / 2, stream);
   } else {
     e = launch_simt_gemm(p, stream);
   }

@@ -99,7 +99,9 @@ constexpr int32_t kDevTimeoutEpilogue = 3;
 
 // Launchers (defined next to their kernels).
 int tc_gemm_max_smem_bytes();
-cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int grid, cudaStream_t stream);
+// Launches clusters of two CTAs, as many pairs as fit on the device (at most
+// one per tile); max_pairs_hint is used if the occupancy query fails.
+cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int max_pairs_hint, cudaStream_t stream);
 cudaError_t launch_simt_gemm(const GemmParams& p, cudaStream_t stream);
 
 // Kernel tags: one kernel symbol per launch kind, so that profiles tell the
