@@ -137,6 +137,29 @@ TPMLP_API tpmlp_status tpmlp_forward_column(const tpmlp_plan* plan, const void* 
 TPMLP_API tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* const* W2, void* const* H, void* Y,
                                void* workspace, tpmlp_stream_t stream);
 
+/* tpmlp_forward_row without a workspace argument, for callers that cannot
+ * allocate device memory: code handed only its input and output buffers by a
+ * host framework that owns the device allocator (a plugin or an operator
+ * inside someone else's runtime), or a latency-bound caller that must not
+ * call cudaMalloc because it synchronises the whole device.  The pages have
+ * no counterpart: it is an interface variant, not a step of the method.
+ *
+ * Same arguments, layouts and result as tpmlp_forward_row (one launch of the
+ * row-parallel GEMM whose K loop carries the g-sum).  Its only scratch, the
+ * device status word, lives in a library-owned static device array of
+ * 256 bytes (held by every GPU that loads the library until the process
+ * exits); the call allocates and frees nothing.  The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress) with the device
+ * current; make that first call before any stream capture.  Each call clears
+ * the status word on the stream, launches, then waits for the stream and
+ * reports the kernel's status itself (TPMLP_ERR_DEVICE_TIMEOUT if a bounded
+ * wait expired), so it blocks until its kernel has finished.  All calls on a
+ * device share the array: calls that overlap on the GPU (other streams, other
+ * host threads) race on the status word.  A plan whose scratch would exceed
+ * the array is rejected with TPMLP_ERR_UNSUPPORTED.                          */
+TPMLP_API tpmlp_status tpmlp_forward_row_noalloc(const tpmlp_plan* plan, const void* const* W2, void* const* H,
+                                                 void* Y, tpmlp_stream_t stream);
+
 /* The two launches of tpmlp_backward, callable one at a time:
  *   tpmlp_backward_dgrad: dact from dY, W2 and saved (act' fused), and dW2
  *                         from H and dY.

@@ -22,7 +22,7 @@ from . import _build
 
 __all__ = [
     "TpmlpError", "load", "Plan", "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size",
-    "tpmlp_forward", "tpmlp_backward", "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_backward_dgrad",
+    "tpmlp_forward", "tpmlp_backward", "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad",
     "tpmlp_backward_fsum", "tpmlp_check", "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version",
     "tpmlp_last_launch_count", "tpmlp_last_error", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
 ]
@@ -36,9 +36,9 @@ MAX_SHARDS = 16
 
 EXPORTED_SYMBOLS = (
     "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size", "tpmlp_forward", "tpmlp_backward",
-    "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_backward_dgrad", "tpmlp_backward_fsum", "tpmlp_check",
+    "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad", "tpmlp_backward_fsum", "tpmlp_check",
     "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version", "tpmlp_last_launch_count",
-    "tpmlp_last_error",
+    "tpmlp_last_error", "tpmlp_forward_row_noalloc",
 )
 
 
@@ -92,6 +92,8 @@ def load():
         lib.tpmlp_forward_column.restype = st
         lib.tpmlp_forward_row.argtypes = [vp, pp, pp, vp, vp, vp]
         lib.tpmlp_forward_row.restype = st
+        lib.tpmlp_forward_row_noalloc.argtypes = [vp, pp, pp, vp, vp]
+        lib.tpmlp_forward_row_noalloc.restype = st
         lib.tpmlp_backward_dgrad.argtypes = [vp, pp, pp, pp, vp, pp, pp, vp, vp]
         lib.tpmlp_backward_dgrad.restype = st
         lib.tpmlp_backward_fsum.argtypes = [vp, vp, pp, pp, pp, vp, pp, pp, vp, vp]
@@ -211,6 +213,14 @@ def tpmlp_forward_column(plan, X, W1, W3, saved, H, workspace, stream=None):
 def tpmlp_forward_row(plan, W2, H, Y, workspace, stream=None):
     _ok(load().tpmlp_forward_row(plan.handle, _arr(W2), _arr(H), _addr(Y), _addr(workspace), _stream(stream)),
         "tpmlp_forward_row")
+
+
+def tpmlp_forward_row_noalloc(plan, W2, H, Y, stream=None):
+    """Row-parallel GEMM (g-sum) without a workspace: the scratch status word
+    is a library-owned static device array, for callers that cannot allocate
+    device memory.  Blocks until its kernel has finished."""
+    _ok(load().tpmlp_forward_row_noalloc(plan.handle, _arr(W2), _arr(H), _addr(Y), _stream(stream)),
+        "tpmlp_forward_row_noalloc")
 
 
 def tpmlp_backward_dgrad(plan, W2, saved, H, dY, dact, dW2, workspace, stream=None):

@@ -398,6 +398,33 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
 
 }  // namespace
 
+// ------------------------------------------------------------------ library-owned scratch
+// Scratch of tpmlp_forward_row_noalloc: a file-scope device array instead of
+// a caller workspace.  Every device that loads the library holds it until
+// the process exits; all calls on a device share it.
+constexpr size_t kStaticScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device (the host-side name is only a stand-in for the symbol).
+tpmlp_status static_scratch(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return fail(TPMLP_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  static std::mutex mu;
+  static void* addr[64] = {};
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    addr[dev] = ptr;
+  }
+  *out = static_cast<int32_t*>(addr[dev]);
+  return TPMLP_OK;
+}
+
 // ====================================================================== C ABI
 extern "C" {
 
@@ -482,6 +509,36 @@ tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* const* W2, vo
   TPMLP_TRY(check_array("H", H, plan->t, tz));
   TPMLP_TRY(check_ptr("Y", Y, tz));
   return fwd_row(plan, di, W2, Y, H, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_forward_row_noalloc(const tpmlp_plan* plan, const void* const* W2, void* const* H, void* Y,
+                                       tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  g_last_error[0] = 0;
+  if (!plan) return fail(TPMLP_ERR_INVALID_ARG, "plan is NULL");
+  DeviceInfo di;
+  TPMLP_TRY(device_info(&di));  // also makes the device's primary context current
+  const size_t need = tpmlp_workspace_size(plan);
+  if (need > kStaticScratchBytes)
+    return fail(TPMLP_ERR_UNSUPPORTED, "this plan needs %zu bytes of scratch; the static scratch holds %zu", need,
+                kStaticScratchBytes);
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_array("W2", W2, plan->t, false));
+  TPMLP_TRY(check_array("H", H, plan->t, tz));
+  TPMLP_TRY(check_ptr("Y", Y, tz));
+  int32_t* scratch = nullptr;
+  TPMLP_TRY(static_scratch(&scratch));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // The status word must start at zero; the array keeps the last call's contents.
+  cudaError_t e = cudaMemsetAsync(scratch, 0, need, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  TPMLP_TRY(fwd_row(plan, di, W2, Y, H, scratch, st));
+  int32_t word = 0;
+  e = cudaMemcpyAsync(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word != kDevOk) return fail(TPMLP_ERR_DEVICE_TIMEOUT, "device wait timed out (code %d)", word);
+  return TPMLP_OK;
 }
 
 tpmlp_status tpmlp_forward(const tpmlp_plan* plan, const void* X, const void* const* W1, const void* const* W3,
