@@ -32,5 +32,45 @@ __device__ __forceinline__ void swiglu_grads(float dh, float g, float u, float& 
   dg = dh * u * (s + g * s * (1.0f - s));
 }
 
+// Faster forms for the bf16 tensor-core epilogues, whose outputs are rounded
+// to bf16 (relative step 2^-8): Phi from the rational approximation of erf
+// by Hastings given as formula 7.1.26 in Abramowitz & Stegun (|error of erf|
+// <= 1.5e-7), with exp(-a^2/2) shared between Phi and the density in GeLU'.
+struct NormTerms {
+  float cdf;  // Phi(a)
+  float e;    // exp(-a^2 / 2)
+};
+
+__device__ __forceinline__ NormTerms norm_terms_fast(float a) {
+  constexpr float p = 0.3275911f * kInvSqrt2;  // t = 1 / (1 + p |a| / sqrt 2)
+  constexpr float a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f, a4 = -1.453152027f,
+                  a5 = 1.061405429f;
+  const float t = __fdividef(1.0f, fmaf(p, fabsf(a), 1.0f));
+  const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1);
+  const float e = __expf(-0.5f * a * a);
+  const float q = 0.5f * poly * e;  // Phi(-|a|)
+  NormTerms r;
+  r.cdf = a >= 0.0f ? 1.0f - q : q;
+  r.e = e;
+  return r;
+}
+
+__device__ __forceinline__ float gelu_fast(float a) { return a * norm_terms_fast(a).cdf; }
+
+__device__ __forceinline__ float gelu_grad_fast(float a) {
+  const NormTerms n = norm_terms_fast(a);
+  return fmaf(a * kInvSqrt2Pi, n.e, n.cdf);
+}
+
+__device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+
+__device__ __forceinline__ float swish_fast(float g) { return g * sigmoid_fast(g); }
+
+__device__ __forceinline__ void swiglu_grads_fast(float dh, float g, float u, float& dg, float& du) {
+  const float s = sigmoid_fast(g);
+  du = dh * (g * s);
+  dg = dh * u * (s + g * s * (1.0f - s));
+}
+
 }  // namespace act
 }  // namespace tpmlp

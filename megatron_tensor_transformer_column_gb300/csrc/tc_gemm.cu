@@ -57,6 +57,13 @@ constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 8 * kNumBars + 16;
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
 constexpr uint64_t kPeerDrainNs = 2ull * 1000 * 1000;
 constexpr uint16_t kPairMask = 0x3;
+// K blocks between the L2 prefetch of a block and its load into the ring:
+// the ring holds about 3,500 MMA cycles, less than a miss to HBM under load,
+// so loads are made to hit L2 instead.
+#ifndef TPMLP_PREFETCH_KBLOCKS
+#define TPMLP_PREFETCH_KBLOCKS 0
+#endif
+constexpr int kPrefetchKBlocks = TPMLP_PREFETCH_KBLOCKS;
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kNumAcc * kAccCols <= kTmemCols, "TMEM budget");
@@ -134,28 +141,122 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
   }
 }
 
-// What CTA `rank` of the pair loads and computes for one tile.
+// What CTA `rank` of the pair loads and computes for one tile.  A K-major
+// operand tile (128 rows x 64 K) is one 128-row box; an MN-major one is up to
+// two 64 x 64 boxes (64 contiguous MN elements per K row).  Boxes wholly
+// outside the valid rows / columns are not loaded: the MMA rows / columns
+// they would feed are never stored.
 struct PairShape {
-  int n_mma;   // MMA N (multiple of 32, covers the tile's valid columns)
-  int half;    // B columns held by each CTA (n_mma / 2)
-  int vm[2];   // valid A/D rows of each CTA
-  int nA[2];   // A boxes each CTA loads
-  int nB[2];   // B boxes (per B operand) each CTA loads
+  int n_mma;        // MMA N (multiple of 32, covers the tile's valid columns)
+  int half;         // B columns held by each CTA (n_mma / 2)
+  int nA[2];        // A copies each CTA issues
+  int nB[2];        // B copies (per B operand) each CTA issues
+  uint32_t bytes[2];  // bytes each CTA loads per K block
 };
 
-__device__ __forceinline__ PairShape pair_shape(const TileInfo& ti, bool dual) {
+__device__ __forceinline__ int copies_for(int major, int valid) {
+  if (valid <= 0) return 0;
+  return major == MAJOR_K ? 1 : (valid + 63) / 64;
+}
+
+__device__ __forceinline__ int box_bytes(int major) { return major == MAJOR_K ? 2 * kBoxBytes : kBoxBytes; }
+
+__device__ __forceinline__ PairShape pair_shape(const TileInfo& ti, bool dual, int a_major, int b_major) {
   PairShape s;
   const int cap = dual ? 128 : 256;
   s.n_mma = min(cap, (ti.valid_n + 31) & ~31);
   s.half = s.n_mma >> 1;
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    s.vm[r] = max(0, min(kBM, ti.valid_m - kBM * r));
-    s.nA[r] = s.vm[r] > 64 ? 2 : (s.vm[r] > 0 ? 1 : 0);
+    const int vm = max(0, min(kBM, ti.valid_m - kBM * r));
     const int vb = max(0, min(s.half, ti.valid_n - s.half * r));
-    s.nB[r] = (vb + 63) / 64;
+    s.nA[r] = copies_for(a_major, vm);
+    s.nB[r] = copies_for(b_major, vb);
+    s.bytes[r] = static_cast<uint32_t>(s.nA[r] * box_bytes(a_major) + (dual ? 2 : 1) * s.nB[r] * box_bytes(b_major));
   }
   return s;
+}
+
+// Walks the (tile, segment, K block) sequence of one CTA of a pair in the
+// order the main loop consumes it; the producer keeps one cursor for the
+// loads into the ring and one running ahead for the L2 prefetches.
+struct Cursor {
+  const void* ma;      // tensor maps of the current segment
+  const void* mb;
+  const void* mb2;
+  int tile, seg, seg_end, kb, kblocks;
+  int a_major, b_major, dual;
+  int m0, n0;          // this CTA's first row of A and first column of B
+  int nA, nB;          // boxes this CTA loads per operand
+  uint32_t bytes_pair; // bytes both CTAs load per K block (counted on the even CTA)
+};
+
+__device__ __forceinline__ void cursor_segment(Cursor& c, const GemmParams& p) {
+  const Seg& S = p.segs[c.seg];
+  c.kb = 0;
+  c.kblocks = (S.K + kBK - 1) / kBK;
+  c.ma = &p.maps[S.a_map];
+  c.mb = &p.maps[S.b_map];
+  c.mb2 = c.dual ? static_cast<const void*>(&p.maps[S.b2_map]) : nullptr;
+}
+
+__device__ __forceinline__ void cursor_tile(Cursor& c, const GemmParams& p, int tile, uint32_t rank) {
+  c.tile = tile;
+  if (tile >= p.total_tiles) return;
+  const TileInfo ti = decode_tile(p, tile);
+  const Prob& P = p.probs[ti.prob];
+  c.dual = P.epi == EPI_SWIGLU_FWD;
+  const PairShape ps = pair_shape(ti, c.dual, P.a_major, P.b_major);
+  c.nA = rank ? ps.nA[1] : ps.nA[0];
+  c.nB = rank ? ps.nB[1] : ps.nB[0];
+  c.bytes_pair = ps.bytes[0] + ps.bytes[1];
+  c.m0 = ti.m0 + kBM * static_cast<int>(rank);
+  c.n0 = ti.n0 + ps.half * static_cast<int>(rank);
+  c.a_major = P.a_major;
+  c.b_major = P.b_major;
+  c.seg = P.seg_begin;
+  c.seg_end = P.seg_begin + P.seg_count;
+  cursor_segment(c, p);
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& c, const GemmParams& p, int npairs, uint32_t rank) {
+  if (++c.kb < c.kblocks) return;
+  if (++c.seg < c.seg_end) {
+    cursor_segment(c, p);
+    return;
+  }
+  cursor_tile(c, p, c.tile + npairs, rank);
+}
+
+// Issue this CTA's box copies (or L2 prefetches) for the cursor's K block.
+template <bool kPrefetch>
+__device__ __forceinline__ void cursor_issue(const Cursor& c, uint32_t sb, uint32_t fb) {
+  const void* ma = c.ma;
+  const void* mb = c.mb;
+  const int k0 = c.kb * kBK;
+  for (int b = 0; b < c.nA; ++b) {  // K-major: nA <= 1 (a 128-row box)
+    const int x = c.a_major == MAJOR_MN ? c.m0 + 64 * b : k0;
+    const int y = c.a_major == MAJOR_MN ? k0 : c.m0;
+    if (kPrefetch)
+      ptx::tma_prefetch_2d(ma, x, y);
+    else
+      ptx::tma_load_2d_pair(sb + b * kBoxBytes, ma, x, y, fb);
+  }
+  for (int j = 0; j < c.nB; ++j) {  // K-major: nB <= 1 (a 128-row box)
+    const int x = c.b_major == MAJOR_MN ? c.n0 + 64 * j : k0;
+    const int y = c.b_major == MAJOR_MN ? k0 : c.n0;
+    if (kPrefetch)
+      ptx::tma_prefetch_2d(mb, x, y);
+    else
+      ptx::tma_load_2d_pair(sb + (2 + j) * kBoxBytes, mb, x, y, fb);
+  }
+  if (c.dual && c.nB > 0) {  // SwiGLU up projection (MN-major like the gate)
+    const void* mb2 = c.mb2;
+    if (kPrefetch)
+      ptx::tma_prefetch_2d(mb2, c.n0, k0);
+    else
+      ptx::tma_load_2d_pair(sb + 3 * kBoxBytes, mb2, c.n0, k0, fb);
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -215,7 +316,7 @@ __device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int c
       store_row32(P.out0, P.ldo, row, col, nvalid, acc);  // A (pre-activation)
       float h[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) h[j] = act::gelu(acc[j]);
+      for (int j = 0; j < 32; ++j) h[j] = act::gelu_fast(acc[j]);
       store_row32(P.out1, P.ldo, row, col, nvalid, h);
       break;
     }
@@ -223,7 +324,7 @@ __device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int c
       float a[32];
       load_row32(P.aux0, P.ldo, row, col, nvalid, a);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) a[j] = acc[j] * act::gelu_grad(a[j]);
+      for (int j = 0; j < 32; ++j) a[j] = acc[j] * act::gelu_grad_fast(a[j]);
       store_row32(P.out0, P.ldo, row, col, nvalid, a);
       break;
     }
@@ -234,7 +335,7 @@ __device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int c
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float dg, du;
-        act::swiglu_grads(acc[j], g[j], u[j], dg, du);
+        act::swiglu_grads_fast(acc[j], g[j], u[j], dg, du);
         g[j] = dg;
         u[j] = du;
       }
@@ -305,55 +406,32 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       for (int s = 0; s < kStages; ++s) armed_parity[s] = -1;
       bool ok = true;
       bool issued = false;
-      for (int tile = pair; ok && tile < p.total_tiles; tile += npairs) {
-        const TileInfo ti = decode_tile(p, tile);
-        const Prob& P = p.probs[ti.prob];
-        const bool dual = P.epi == EPI_SWIGLU_FWD;
-        const PairShape ps = pair_shape(ti, dual);
-        const int nops = dual ? 2 : 1;
-        const uint32_t bytes_pair =
-            static_cast<uint32_t>((ps.nA[0] + ps.nA[1] + nops * (ps.nB[0] + ps.nB[1])) * kBoxBytes);
-        const int my_nA = leader ? ps.nA[0] : ps.nA[1];
-        const int my_nB = leader ? ps.nB[0] : ps.nB[1];
-        const int a_row = ti.m0 + kBM * static_cast<int>(rank);
-        const int b_col = ti.n0 + ps.half * static_cast<int>(rank);
-        for (int s = P.seg_begin; ok && s < P.seg_begin + P.seg_count; ++s) {
-          const Seg& S = p.segs[s];
-          const void* ma = &p.maps[S.a_map];
-          const void* mb = &p.maps[S.b_map];
-          const void* mb2 = dual ? static_cast<const void*>(&p.maps[S.b2_map]) : nullptr;
-          const int kblocks = (S.K + kBK - 1) / kBK;
-          for (int kb = 0; kb < kblocks; ++kb) {
-            if (!bounded_wait(empty_bar(stage), phase ^ 1u, ctl, kDevTimeoutProducer)) {
-              ok = false;
-              break;
-            }
-            if (leader) {
-              ptx::mbar_arrive_expect_tx(full_bar(stage), bytes_pair);
-              armed_parity[stage] = static_cast<int>(phase);
-            }
-            const uint32_t fb = ptx::map_to_cta(full_bar(stage), 0);
-            const uint32_t sb = smem_base + stage * kStageBytes;
-            const int k0 = kb * kBK;
-            for (int b = 0; b < my_nA; ++b) {
-              if (P.a_major == MAJOR_MN)
-                ptx::tma_load_2d_pair(sb + b * kBoxBytes, ma, a_row + 64 * b, k0, fb);
-              else
-                ptx::tma_load_2d_pair(sb + b * kBoxBytes, ma, k0, a_row + 64 * b, fb);
-            }
-            for (int j = 0; j < my_nB; ++j) {
-              if (P.b_major == MAJOR_MN)
-                ptx::tma_load_2d_pair(sb + (2 + j) * kBoxBytes, mb, b_col + 64 * j, k0, fb);
-              else
-                ptx::tma_load_2d_pair(sb + (2 + j) * kBoxBytes, mb, k0, b_col + 64 * j, fb);
-            }
-            if (dual && my_nB > 0) ptx::tma_load_2d_pair(sb + 3 * kBoxBytes, mb2, b_col, k0, fb);
-            issued = true;
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
+      Cursor ld, pf;
+      cursor_tile(ld, p, pair, rank);
+      cursor_tile(pf, p, pair, rank);
+      for (int i = 0; i < kPrefetchKBlocks && pf.tile < p.total_tiles; ++i) {
+        cursor_issue<true>(pf, 0, 0);
+        cursor_next(pf, p, npairs, rank);
+      }
+      while (ld.tile < p.total_tiles) {
+        if (!bounded_wait(empty_bar(stage), phase ^ 1u, ctl, kDevTimeoutProducer)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          ptx::mbar_arrive_expect_tx(full_bar(stage), ld.bytes_pair);
+          armed_parity[stage] = static_cast<int>(phase);
+        }
+        cursor_issue<false>(ld, smem_base + stage * kStageBytes, ptx::map_to_cta(full_bar(stage), 0));
+        issued = true;
+        cursor_next(ld, p, npairs, rank);
+        if (kPrefetchKBlocks > 0 && pf.tile < p.total_tiles) {
+          cursor_issue<true>(pf, 0, 0);
+          cursor_next(pf, p, npairs, rank);
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
       if (!ok && issued) {
@@ -374,12 +452,25 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       uint32_t acc_phase = 0;
       bool ok = true;
       bool issued = false;
+      // Descriptors of stage 0 for each operand layout; a stage and a K step
+      // are added to the start-address field (16-byte units, no carry: the
+      // ring lies below 256 KB).
+      const uint64_t a_k_desc = ptx::make_sdesc_sw128(smem_base, 16, 1024);
+      const uint64_t a_mn_desc = ptx::make_sdesc_sw128(smem_base, kBoxBytes, 1024);
+      const uint64_t b_k_desc = ptx::make_sdesc_sw128(smem_base + 2 * kBoxBytes, 16, 1024);
+      const uint64_t b_mn_desc = ptx::make_sdesc_sw128(smem_base + 2 * kBoxBytes, kBoxBytes, 1024);
       for (int tile = pair; ok && tile < p.total_tiles; tile += npairs) {
         const TileInfo ti = decode_tile(p, tile);
         const Prob& P = p.probs[ti.prob];
+        const int a_major = P.a_major, b_major = P.b_major;
         const bool dual = P.epi == EPI_SWIGLU_FWD;
-        const PairShape ps = pair_shape(ti, dual);
-        const uint32_t idesc = ptx::make_idesc_bf16(kPairM, ps.n_mma, P.a_major, P.b_major);
+        const int seg_begin = P.seg_begin, seg_end = P.seg_begin + P.seg_count;
+        const PairShape ps = pair_shape(ti, dual, a_major, b_major);
+        const uint32_t idesc = ptx::make_idesc_bf16(kPairM, ps.n_mma, a_major, b_major);
+        const uint64_t a_desc0 = a_major == MAJOR_MN ? a_mn_desc : a_k_desc;
+        const uint64_t b_desc0 = b_major == MAJOR_MN ? b_mn_desc : b_k_desc;
+        const uint64_t a_step = a_major == MAJOR_MN ? 2048 >> 4 : 32 >> 4;  // one K16 step
+        const uint64_t b_step = b_major == MAJOR_MN ? 2048 >> 4 : 32 >> 4;
         if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, ctl, kDevTimeoutMma)) {
           ok = false;
           break;
@@ -387,32 +478,29 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         uint32_t accumulate = 0;
-        for (int s = P.seg_begin; ok && s < P.seg_begin + P.seg_count; ++s) {
-          const Seg& S = p.segs[s];
-          const int kblocks = (S.K + kBK - 1) / kBK;
-          for (int kb = 0; kb < kblocks; ++kb) {
+        for (int s = seg_begin; ok && s < seg_end; ++s) {
+          const int K = p.segs[s].K;
+          for (int k0 = 0; k0 < K; k0 += kBK) {
             if (!bounded_wait(full_bar(stage), phase, ctl, kDevTimeoutMma)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            const uint32_t sa = smem_base + stage * kStageBytes;
-            const uint32_t sb = sa + 2 * kBoxBytes;
-            const int rem = S.K - kb * kBK;
-            const int nk = min(kBK / 16, (rem + 15) / 16);
-            for (int j = 0; j < nk; ++j) {
-              const uint64_t ad = P.a_major == MAJOR_MN ? ptx::make_sdesc_sw128(sa + 2048u * j, kBoxBytes, 1024)
-                                                        : ptx::make_sdesc_sw128(sa + 32u * j, 16, 1024);
-              const uint64_t bd = P.b_major == MAJOR_MN ? ptx::make_sdesc_sw128(sb + 2048u * j, kBoxBytes, 1024)
-                                                        : ptx::make_sdesc_sw128(sb + 32u * j, 16, 1024);
-              ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
-              if (dual) {
-                const uint64_t bd2 = ptx::make_sdesc_sw128(sb + kBoxBytes + 2048u * j, kBoxBytes, 1024);
-                ptx::mma_bf16_pair(d_tmem + 128u, ad, bd2, idesc, accumulate);
+            const uint64_t st = static_cast<uint64_t>((stage * kStageBytes) >> 4);
+            uint64_t ad = a_desc0 + st;
+            uint64_t bd = b_desc0 + st;
+            const int nk = min(kBK / 16, (K - k0 + 15) >> 4);
+#pragma unroll
+            for (int j = 0; j < kBK / 16; ++j) {
+              if (j < nk) {
+                ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+                if (dual) ptx::mma_bf16_pair(d_tmem + 128u, ad, bd + (kBoxBytes >> 4), idesc, accumulate);
+                accumulate = 1;
+                ad += a_step;
+                bd += b_step;
               }
-              accumulate = 1;
-              issued = true;
             }
+            issued = true;
             ptx::mma_commit_pair_mc(empty_bar(stage), kPairMask);  // stage free in both CTAs
             if (++stage == kStages) {
               stage = 0;
@@ -442,12 +530,29 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
     for (int tile = pair; tile < p.total_tiles; tile += npairs) {
       const TileInfo ti = decode_tile(p, tile);
       const Prob& P = p.probs[ti.prob];
-      if (!bounded_wait(tfull_bar(acc), acc_phase, ctl, kDevTimeoutEpilogue)) break;
-      ptx::tc_fence_after();
       const int row = q * 32 + lane;
       const int vm = max(0, min(kBM, ti.valid_m - kBM * static_cast<int>(rank)));
       const bool row_ok = row < vm;
       const int64_t grow = static_cast<int64_t>(ti.m0) + kBM * static_cast<int>(rank) + row;
+      if (row_ok && (P.epi == EPI_GELU_BWD || P.epi == EPI_SWIGLU_BWD)) {
+        // Pull this thread's row of the saved pre-activation(s) into L2
+        // while the accumulator is still being computed.
+        const int c0 = half * 128;
+        const int cn = min(128, ti.valid_n - c0);
+        if (cn > 0) {
+          const int64_t off = grow * P.ldo + ti.n0 + c0;
+          const __nv_bfloat16* a0 = static_cast<const __nv_bfloat16*>(P.aux0) + off;
+          for (int b = 0; b < 2 * cn; b += 128) ptx::prefetch_l2(reinterpret_cast<const char*>(a0) + b);
+          ptx::prefetch_l2(reinterpret_cast<const char*>(a0) + 2 * cn - 1);
+          if (P.epi == EPI_SWIGLU_BWD) {
+            const __nv_bfloat16* a1 = static_cast<const __nv_bfloat16*>(P.aux1) + off;
+            for (int b = 0; b < 2 * cn; b += 128) ptx::prefetch_l2(reinterpret_cast<const char*>(a1) + b);
+            ptx::prefetch_l2(reinterpret_cast<const char*>(a1) + 2 * cn - 1);
+          }
+        }
+      }
+      if (!bounded_wait(tfull_bar(acc), acc_phase, ctl, kDevTimeoutEpilogue)) break;
+      ptx::tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
       if (vm > 0) {
         if (P.epi == EPI_SWIGLU_FWD) {
@@ -466,7 +571,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
               for (int j = 0; j < 32; ++j) {
                 g[j] = __uint_as_float(rg[j]);
                 u[j] = __uint_as_float(ru[j]);
-                h[j] = u[j] * act::swish(g[j]);
+                h[j] = u[j] * act::swish_fast(g[j]);
               }
               store_row32(P.out0, P.ldo, grow, ti.n0 + col, nvalid, g);
               store_row32(P.out1, P.ldo, grow, ti.n0 + col, nvalid, u);

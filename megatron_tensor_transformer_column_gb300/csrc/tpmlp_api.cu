@@ -108,15 +108,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D row-major bf16 [rows x cols]; 64 x 64 boxes, 128-byte swizzle,
-// out-of-range elements read as zero.
+// 2-D row-major bf16 [rows x cols]; boxes of 64 columns (128 bytes, the
+// swizzle span) by box_rows rows, 128-byte swizzle, out-of-range elements read
+// as zero.  K-major operand tiles use 128-row boxes (one copy per 128 x 64
+// tile), MN-major ones 64-row boxes (64 K rows of a 64-wide MN block).
 // Returns 0 on success, the CUresult otherwise (-1: entry point unavailable).
-int encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+int encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return -1;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -131,6 +133,7 @@ struct Builder {
   int tile_m;
   std::vector<const void*> map_ptr;
   std::vector<int64_t> map_rows, map_cols;
+  std::vector<int> map_box;
   bool map_error = false;
   int cur_group = -1;
 
@@ -140,17 +143,18 @@ struct Builder {
     p->tile_m = tile_m;
   }
 
-  int map(const void* ptr, int64_t rows, int64_t cols) {
+  int map(const void* ptr, int64_t rows, int64_t cols, int box_rows) {
     if (!tc) return -1;
     for (size_t i = 0; i < map_ptr.size(); ++i)
-      if (map_ptr[i] == ptr && map_rows[i] == rows && map_cols[i] == cols) return static_cast<int>(i);
+      if (map_ptr[i] == ptr && map_rows[i] == rows && map_cols[i] == cols && map_box[i] == box_rows)
+        return static_cast<int>(i);
     if (p->num_maps >= kMaxMaps) {
       map_error = true;
       fail(TPMLP_ERR_INVALID_ARG, "more than %d tensor maps in one launch", kMaxMaps);
       return 0;
     }
     const int idx = p->num_maps++;
-    const int r = encode_map(&p->maps[idx], ptr, rows, cols);
+    const int r = encode_map(&p->maps[idx], ptr, rows, cols, box_rows);
     if (r != 0) {
       map_error = true;
       fail(TPMLP_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for %p [%lld x %lld]", r, ptr,
@@ -159,6 +163,7 @@ struct Builder {
     map_ptr.push_back(ptr);
     map_rows.push_back(rows);
     map_cols.push_back(cols);
+    map_box.push_back(box_rows);
     return idx;
   }
 
@@ -199,9 +204,11 @@ struct Builder {
     S.b2 = b2;
     S.lda = a_cols;
     S.ldb = b_cols;
-    S.a_map = map(a, a_rows, a_cols);
-    S.b_map = map(b, b_rows, b_cols);
-    S.b2_map = b2 ? map(b2, b_rows, b_cols) : -1;
+    const int a_box = P.a_major == MAJOR_K ? 128 : 64;
+    const int b_box = P.b_major == MAJOR_K ? 128 : 64;
+    S.a_map = map(a, a_rows, a_cols, a_box);
+    S.b_map = map(b, b_rows, b_cols, b_box);
+    S.b2_map = b2 ? map(b2, b_rows, b_cols, b_box) : -1;
     S.K = static_cast<int32_t>(K);
     P.seg_count++;
   }

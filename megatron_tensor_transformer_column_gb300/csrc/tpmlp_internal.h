@@ -16,7 +16,10 @@
 namespace tpmlp {
 
 constexpr int kMaxShards = 16;
-constexpr int kMaxMaps = 4 * kMaxShards + 2;
+// A tensor used both K-major (128-row boxes) and MN-major (64-row boxes) in
+// one launch needs two maps: the SwiGLU f-sum launch has X, dG_i and dU_i
+// twice each, W1_i and W3_i (6t + 1).
+constexpr int kMaxMaps = 6 * kMaxShards + 2;
 constexpr int kMaxProbs = 2 * kMaxShards + 2;
 constexpr int kMaxGroups = kMaxShards + 2;
 constexpr int kMaxSegs = 4 * kMaxShards + 2;
