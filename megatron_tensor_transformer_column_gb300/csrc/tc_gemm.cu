@@ -43,10 +43,18 @@ namespace {
 
 constexpr int kBM = 128;                        // rows of A / D per CTA
 constexpr int kPairM = 2 * kBM;                 // rows of a pair's tile
-constexpr int kBK = 64;                         // K per stage (one 128-byte swizzle row of bf16)
-constexpr int kStages = 7;
-constexpr int kBoxBytes = 64 * 64 * 2;          // one TMA box: 64 x 64 bf16
-constexpr int kStageBytes = 4 * kBoxBytes;      // 2 A boxes + 2 B boxes
+// A stage holds, per CTA, a 128 x kBK slice of A and of its half of B, each
+// as 128-byte-swizzled rows.  A K-major slice is kBK/64 boxes of 128 rows x
+// 64 K; an MN-major one is two boxes of 64 MN columns x kBK K rows.
+constexpr int kBK = kTcBK;                      // K per stage
+constexpr int kRowBytes = 128;                  // one swizzle row: 64 bf16
+constexpr int kKBoxBytes = 128 * kRowBytes;     // K-major box: 128 rows x 64 K (16 KB)
+constexpr int kMNBoxBytes = kBK * kRowBytes;    // MN-major box: kBK K rows x 64 MN
+constexpr int kOperandBytes = 128 * kBK * 2;    // one operand slice per stage
+constexpr int kStageBytes = 2 * kOperandBytes;  // A + B
+constexpr int kStages = (224 * 1024) / kStageBytes;
+static_assert(kBK % 64 == 0, "stage depth is a whole number of 64-wide boxes");
+static_assert(kOperandBytes == (kBK / 64) * kKBoxBytes && kOperandBytes == 2 * kMNBoxBytes, "stage layout");
 constexpr int kNumEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kNumEpiWarps);
 constexpr int kTmemCols = 512;
@@ -141,11 +149,10 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
   }
 }
 
-// What CTA `rank` of the pair loads and computes for one tile.  A K-major
-// operand tile (128 rows x 64 K) is one 128-row box; an MN-major one is up to
-// two 64 x 64 boxes (64 contiguous MN elements per K row).  Boxes wholly
-// outside the valid rows / columns are not loaded: the MMA rows / columns
-// they would feed are never stored.
+// What CTA `rank` of the pair loads and computes for one tile.  MN-major
+// boxes wholly outside the valid rows / columns are not loaded (nor are the
+// A boxes of a CTA with no valid rows): the MMA rows / columns they would
+// feed are never stored.
 struct PairShape {
   int n_mma;        // MMA N (multiple of 32, covers the tile's valid columns)
   int half;         // B columns held by each CTA (n_mma / 2)
@@ -154,12 +161,14 @@ struct PairShape {
   uint32_t bytes[2];  // bytes each CTA loads per K block
 };
 
+// TMA copies of one operand slice: K-major, kBK/64 boxes covering all 128
+// rows; MN-major, one box per 64 valid columns.
 __device__ __forceinline__ int copies_for(int major, int valid) {
   if (valid <= 0) return 0;
-  return major == MAJOR_K ? 1 : (valid + 63) / 64;
+  return major == MAJOR_K ? kBK / 64 : (valid + 63) / 64;
 }
 
-__device__ __forceinline__ int box_bytes(int major) { return major == MAJOR_K ? 2 * kBoxBytes : kBoxBytes; }
+__device__ __forceinline__ int box_bytes(int major) { return major == MAJOR_K ? kKBoxBytes : kMNBoxBytes; }
 
 __device__ __forceinline__ PairShape pair_shape(const TileInfo& ti, bool dual, int a_major, int b_major) {
   PairShape s;
@@ -234,28 +243,33 @@ __device__ __forceinline__ void cursor_issue(const Cursor& c, uint32_t sb, uint3
   const void* ma = c.ma;
   const void* mb = c.mb;
   const int k0 = c.kb * kBK;
-  for (int b = 0; b < c.nA; ++b) {  // K-major: nA <= 1 (a 128-row box)
-    const int x = c.a_major == MAJOR_MN ? c.m0 + 64 * b : k0;
-    const int y = c.a_major == MAJOR_MN ? k0 : c.m0;
+  const uint32_t sbB = sb + kOperandBytes;
+  for (int b = 0; b < c.nA; ++b) {
+    // K-major: box b covers K [k0 + 64 b, +64) of the 128 rows;
+    // MN-major: box b covers columns [m0 + 64 b, +64) of K rows [k0, k0 + kBK).
+    const bool mn = c.a_major == MAJOR_MN;
+    const int x = mn ? c.m0 + 64 * b : k0 + 64 * b;
+    const int y = mn ? k0 : c.m0;
     if (kPrefetch)
       ptx::tma_prefetch_2d(ma, x, y);
     else
-      ptx::tma_load_2d_pair(sb + b * kBoxBytes, ma, x, y, fb);
+      ptx::tma_load_2d_pair(sb + b * (mn ? kMNBoxBytes : kKBoxBytes), ma, x, y, fb);
   }
-  for (int j = 0; j < c.nB; ++j) {  // K-major: nB <= 1 (a 128-row box)
-    const int x = c.b_major == MAJOR_MN ? c.n0 + 64 * j : k0;
-    const int y = c.b_major == MAJOR_MN ? k0 : c.n0;
+  for (int j = 0; j < c.nB; ++j) {
+    const bool mn = c.b_major == MAJOR_MN;
+    const int x = mn ? c.n0 + 64 * j : k0 + 64 * j;
+    const int y = mn ? k0 : c.n0;
     if (kPrefetch)
       ptx::tma_prefetch_2d(mb, x, y);
     else
-      ptx::tma_load_2d_pair(sb + (2 + j) * kBoxBytes, mb, x, y, fb);
+      ptx::tma_load_2d_pair(sbB + j * (mn ? kMNBoxBytes : kKBoxBytes), mb, x, y, fb);
   }
-  if (c.dual && c.nB > 0) {  // SwiGLU up projection (MN-major like the gate)
+  if (c.dual && c.nB > 0) {  // SwiGLU up projection (MN-major like the gate), second B box
     const void* mb2 = c.mb2;
     if (kPrefetch)
       ptx::tma_prefetch_2d(mb2, c.n0, k0);
     else
-      ptx::tma_load_2d_pair(sb + 3 * kBoxBytes, mb2, c.n0, k0, fb);
+      ptx::tma_load_2d_pair(sbB + kMNBoxBytes, mb2, c.n0, k0, fb);
   }
 }
 
@@ -454,11 +468,14 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       bool issued = false;
       // Descriptors of stage 0 for each operand layout; a stage and a K step
       // are added to the start-address field (16-byte units, no carry: the
-      // ring lies below 256 KB).
+      // ring lies below 256 KB).  K-major: 8-row groups 1024 B apart; K16
+      // step j is +32 B inside a 64-wide box, box j/4 is +16 KB.  MN-major:
+      // the two 64-column blocks are kMNBoxBytes apart (leading offset), 8-row
+      // K groups 1024 B apart, K16 step j is +2048 B.
       const uint64_t a_k_desc = ptx::make_sdesc_sw128(smem_base, 16, 1024);
-      const uint64_t a_mn_desc = ptx::make_sdesc_sw128(smem_base, kBoxBytes, 1024);
-      const uint64_t b_k_desc = ptx::make_sdesc_sw128(smem_base + 2 * kBoxBytes, 16, 1024);
-      const uint64_t b_mn_desc = ptx::make_sdesc_sw128(smem_base + 2 * kBoxBytes, kBoxBytes, 1024);
+      const uint64_t a_mn_desc = ptx::make_sdesc_sw128(smem_base, kMNBoxBytes, 1024);
+      const uint64_t b_k_desc = ptx::make_sdesc_sw128(smem_base + kOperandBytes, 16, 1024);
+      const uint64_t b_mn_desc = ptx::make_sdesc_sw128(smem_base + kOperandBytes, kMNBoxBytes, 1024);
       for (int tile = pair; ok && tile < p.total_tiles; tile += npairs) {
         const TileInfo ti = decode_tile(p, tile);
         const Prob& P = p.probs[ti.prob];
@@ -469,8 +486,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
         const uint32_t idesc = ptx::make_idesc_bf16(kPairM, ps.n_mma, a_major, b_major);
         const uint64_t a_desc0 = a_major == MAJOR_MN ? a_mn_desc : a_k_desc;
         const uint64_t b_desc0 = b_major == MAJOR_MN ? b_mn_desc : b_k_desc;
-        const uint64_t a_step = a_major == MAJOR_MN ? 2048 >> 4 : 32 >> 4;  // one K16 step
-        const uint64_t b_step = b_major == MAJOR_MN ? 2048 >> 4 : 32 >> 4;
+        const bool a_mn = a_major == MAJOR_MN, b_mn = b_major == MAJOR_MN;
         if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, ctl, kDevTimeoutMma)) {
           ok = false;
           break;
@@ -487,17 +503,19 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
             }
             ptx::tc_fence_after();
             const uint64_t st = static_cast<uint64_t>((stage * kStageBytes) >> 4);
-            uint64_t ad = a_desc0 + st;
-            uint64_t bd = b_desc0 + st;
+            const uint64_t ad0 = a_desc0 + st;
+            const uint64_t bd0 = b_desc0 + st;
             const int nk = min(kBK / 16, (K - k0 + 15) >> 4);
 #pragma unroll
             for (int j = 0; j < kBK / 16; ++j) {
               if (j < nk) {
+                const uint64_t koff = static_cast<uint64_t>(((j >> 2) * kKBoxBytes + (j & 3) * 32) >> 4);
+                const uint64_t moff = static_cast<uint64_t>((j * 2048) >> 4);
+                const uint64_t ad = ad0 + (a_mn ? moff : koff);
+                const uint64_t bd = bd0 + (b_mn ? moff : koff);
                 ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
-                if (dual) ptx::mma_bf16_pair(d_tmem + 128u, ad, bd + (kBoxBytes >> 4), idesc, accumulate);
+                if (dual) ptx::mma_bf16_pair(d_tmem + 128u, ad, bd + (kMNBoxBytes >> 4), idesc, accumulate);
                 accumulate = 1;
-                ad += a_step;
-                bd += b_step;
               }
             }
             issued = true;

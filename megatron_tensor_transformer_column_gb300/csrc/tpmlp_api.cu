@@ -110,8 +110,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D row-major bf16 [rows x cols]; boxes of 64 columns (128 bytes, the
 // swizzle span) by box_rows rows, 128-byte swizzle, out-of-range elements read
-// as zero.  K-major operand tiles use 128-row boxes (one copy per 128 x 64
-// tile), MN-major ones 64-row boxes (64 K rows of a 64-wide MN block).
+// as zero.  K-major operand tiles use 128-row boxes (128 M/N rows x 64 K),
+// MN-major ones kTcBK-row boxes (kTcBK K rows of a 64-wide M/N block).
 // Returns 0 on success, the CUresult otherwise (-1: entry point unavailable).
 int encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
   auto fn = encode_fn();
@@ -204,8 +204,8 @@ struct Builder {
     S.b2 = b2;
     S.lda = a_cols;
     S.ldb = b_cols;
-    const int a_box = P.a_major == MAJOR_K ? 128 : 64;
-    const int b_box = P.b_major == MAJOR_K ? 128 : 64;
+    const int a_box = P.a_major == MAJOR_K ? 128 : kTcBK;
+    const int b_box = P.b_major == MAJOR_K ? 128 : kTcBK;
     S.a_map = map(a, a_rows, a_cols, a_box);
     S.b_map = map(b, b_rows, b_cols, b_box);
     S.b2_map = b2 ? map(b2, b_rows, b_cols, b_box) : -1;

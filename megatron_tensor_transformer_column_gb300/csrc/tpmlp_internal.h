@@ -16,6 +16,14 @@
 namespace tpmlp {
 
 constexpr int kMaxShards = 16;
+
+// K depth of one shared-memory stage of the tensor-core GEMM (a multiple of
+// 64).  TMA boxes are 64 columns wide: 128 rows for K-major operand tiles,
+// kTcBK K rows for MN-major ones.
+#ifndef TPMLP_TC_BK
+#define TPMLP_TC_BK 128
+#endif
+constexpr int kTcBK = TPMLP_TC_BK;
 // A tensor used both K-major (128-row boxes) and MN-major (64-row boxes) in
 // one launch needs two maps: the SwiGLU f-sum launch has X, dG_i and dU_i
 // twice each, W1_i and W3_i (6t + 1).
