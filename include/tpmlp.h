@@ -173,6 +173,21 @@ TPMLP_API tpmlp_status tpmlp_backward_fsum(const tpmlp_plan* plan, const void* X
                                  const void* const* W3, const void* const* dact, void* dX, void* const* dW1,
                                  void* const* dW3, void* workspace, tpmlp_stream_t stream);
 
+/* Watchdog controls, for testing the failure path without faulting a GPU.
+ * Neither may run while another call uses the plan.
+ *   tpmlp_plan_set_timeout: bound, in milliseconds (>= 1), of every wait
+ *     inside this plan's kernels (default 2000; the environment variable
+ *     TPMLP_WAIT_TIMEOUT_MS sets the default of new plans).
+ *   tpmlp_plan_set_stall_injection: with enable != 0 the tensor-core kernels
+ *     of this plan load nothing, so the first wait of their MMA issuer is
+ *     never satisfied and runs out after the timeout; the kernel then records
+ *     TPMLP_ERR_DEVICE_TIMEOUT in the status word, every role leaves its loop,
+ *     the CTAs free their TMEM and exit, and the CUDA context stays usable.
+ *     Outputs are undefined while it is enabled.  The fp32 path has no waits
+ *     and ignores it.                                                        */
+TPMLP_API tpmlp_status tpmlp_plan_set_timeout(tpmlp_plan* plan, uint32_t timeout_ms);
+TPMLP_API tpmlp_status tpmlp_plan_set_stall_injection(tpmlp_plan* plan, int enable);
+
 /* Synchronise the stream, read the workspace's status word and clear it.
  * Returns TPMLP_OK, TPMLP_ERR_DEVICE_TIMEOUT, or TPMLP_ERR_CUDA.               */
 TPMLP_API tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpmlp_stream_t stream);

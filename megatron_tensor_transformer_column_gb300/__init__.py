@@ -22,6 +22,7 @@ from . import _build
 
 __all__ = [
     "TpmlpError", "load", "Plan", "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size",
+    "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection",
     "tpmlp_forward", "tpmlp_backward", "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad",
     "tpmlp_backward_fsum", "tpmlp_check", "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version",
     "tpmlp_last_launch_count", "tpmlp_last_error", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
@@ -38,7 +39,7 @@ EXPORTED_SYMBOLS = (
     "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size", "tpmlp_forward", "tpmlp_backward",
     "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad", "tpmlp_backward_fsum", "tpmlp_check",
     "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version", "tpmlp_last_launch_count",
-    "tpmlp_last_error", "tpmlp_forward_row_noalloc",
+    "tpmlp_last_error", "tpmlp_forward_row_noalloc", "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection",
 )
 
 
@@ -82,6 +83,10 @@ def load():
         lib.tpmlp_plan_create.restype = st
         lib.tpmlp_plan_destroy.argtypes = [vp]
         lib.tpmlp_plan_destroy.restype = None
+        lib.tpmlp_plan_set_timeout.argtypes = [vp, ctypes.c_uint32]
+        lib.tpmlp_plan_set_timeout.restype = st
+        lib.tpmlp_plan_set_stall_injection.argtypes = [vp, ctypes.c_int]
+        lib.tpmlp_plan_set_stall_injection.restype = st
         lib.tpmlp_workspace_size.argtypes = [vp]
         lib.tpmlp_workspace_size.restype = ctypes.c_size_t
         lib.tpmlp_forward.argtypes = [vp, vp, pp, pp, pp, vp, pp, pp, vp, vp]
@@ -188,6 +193,14 @@ def tpmlp_plan_destroy(plan: Plan):
     if plan.handle is not None and plan.handle.value:
         load().tpmlp_plan_destroy(plan.handle)
         plan.handle = None
+
+
+def tpmlp_plan_set_timeout(plan: Plan, timeout_ms: int):
+    _ok(load().tpmlp_plan_set_timeout(plan.handle, int(timeout_ms)), "tpmlp_plan_set_timeout")
+
+
+def tpmlp_plan_set_stall_injection(plan: Plan, enable: bool):
+    _ok(load().tpmlp_plan_set_stall_injection(plan.handle, 1 if enable else 0), "tpmlp_plan_set_stall_injection")
 
 
 def tpmlp_workspace_size(plan: Plan) -> int:

@@ -28,6 +28,7 @@ struct tpmlp_plan {
   tpmlp_act act;
   tpmlp_dtype dtype;
   uint64_t timeout_ns;
+  int32_t stall_injection;
 };
 
 namespace {
@@ -240,6 +241,7 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
   if (p.total_tiles == 0) return TPMLP_OK;
   p.status = static_cast<int32_t*>(workspace);
   p.timeout_ns = plan->timeout_ns;
+  p.stall_injection = plan->stall_injection;
   cudaError_t e;
   if (B.tc) {
     e = launch_tc_gemm(p, tag, di.sms / 2, stream);
@@ -479,6 +481,7 @@ tpmlp_status tpmlp_plan_create(const tpmlp_desc* desc, tpmlp_plan** out) {
   pl->act = desc->act;
   pl->dtype = desc->dtype;
   pl->timeout_ns = kDefaultTimeoutNs;
+  pl->stall_injection = 0;
   if (const char* s = std::getenv("TPMLP_WAIT_TIMEOUT_MS")) {
     const long long ms = std::atoll(s);
     if (ms > 0) pl->timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
@@ -488,6 +491,21 @@ tpmlp_status tpmlp_plan_create(const tpmlp_desc* desc, tpmlp_plan** out) {
 }
 
 void tpmlp_plan_destroy(tpmlp_plan* plan) { delete plan; }
+
+tpmlp_status tpmlp_plan_set_timeout(tpmlp_plan* plan, uint32_t timeout_ms) {
+  g_last_error[0] = 0;
+  if (!plan) return fail(TPMLP_ERR_INVALID_ARG, "plan is NULL");
+  if (timeout_ms < 1) return fail(TPMLP_ERR_INVALID_ARG, "timeout must be at least 1 ms");
+  plan->timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_plan_set_stall_injection(tpmlp_plan* plan, int enable) {
+  g_last_error[0] = 0;
+  if (!plan) return fail(TPMLP_ERR_INVALID_ARG, "plan is NULL");
+  plan->stall_injection = enable ? 1 : 0;
+  return TPMLP_OK;
+}
 
 size_t tpmlp_workspace_size(const tpmlp_plan* plan) { return plan ? 256 : 0; }
 

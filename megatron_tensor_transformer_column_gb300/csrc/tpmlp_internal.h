@@ -97,6 +97,7 @@ struct GemmParams {
   int32_t tile_m;
   int32_t* status;          // device status word (workspace)
   uint64_t timeout_ns;      // bound on every wait inside the kernel
+  int32_t stall_injection;  // test hook: producers load nothing, so the waits run out
 };
 
 // Kernel parameters live in the 32 KB parameter space (__grid_constant__).
