@@ -65,17 +65,19 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH, extra_flag
 def _bind(lib):
     i64, i32, ci, dp = ctypes.c_int64, ctypes.c_int32, ctypes.c_int, ctypes.c_void_p
     pp = ctypes.POINTER(ctypes.c_void_p)
-    lib.oracle_forward.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, dp]
+    lib.oracle_forward.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp]
     lib.oracle_forward.restype = ci
-    lib.oracle_backward.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp]
+    lib.oracle_backward.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                                    dp]
     lib.oracle_backward.restype = ci
-    lib.oracle_forward_sharded.argtypes = [i64, i64, i32, dp, ci, dp, pp, pp, pp, dp, pp]
+    lib.oracle_forward_sharded.argtypes = [i64, i64, i32, dp, ci, dp, pp, pp, pp, pp, pp, dp, dp, pp]
     lib.oracle_forward_sharded.restype = ci
-    lib.oracle_backward_sharded.argtypes = [i64, i64, i32, dp, ci, dp, pp, pp, pp, dp, dp, pp, pp, pp]
+    lib.oracle_backward_sharded.argtypes = [i64, i64, i32, dp, ci, dp, pp, pp, pp, pp, pp, dp, dp, pp, pp, pp, pp,
+                                            pp, dp]
     lib.oracle_backward_sharded.restype = ci
-    lib.oracle_rows.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, i64, dp, dp, dp]
+    lib.oracle_rows.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, dp, i64, dp, dp, dp]
     lib.oracle_rows.restype = ci
-    lib.oracle_wgrad_units.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, i64, dp, dp, dp, dp]
+    lib.oracle_wgrad_units.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, i64, dp, dp, dp, dp, dp, dp]
     lib.oracle_wgrad_units.restype = ci
     lib.oracle_act_value.argtypes = [ci, ctypes.c_double]
     lib.oracle_act_value.restype = ctypes.c_double
@@ -139,24 +141,26 @@ class COracle:
     def act_grad(self, act, a: float) -> float:
         return float(self.lib.oracle_act_grad(_act(act), float(a)))
 
-    def forward(self, X, W1, W2, act="gelu", W3=None):
+    def forward(self, X, W1, W2, act="gelu", W3=None, b1=None, b3=None, b2=None):
         """Unsharded forward.  Returns dict with A (SwiGLU: G), U, H, Y (fp64)."""
         lib = self.lib
         a = _act(act)
         X, W1, W2, W3 = _f64(X), _f64(W1), _f64(W2), _f64(W3)
+        b1, b3, b2 = _f64(b1), _f64(b3), _f64(b2)
         T, d = X.shape
         dff = W1.shape[1]
         A = np.empty((T, dff)); H = np.empty((T, dff)); Y = np.empty((T, d))
         U = np.empty((T, dff)) if a == ACT_SWIGLU else None
-        _check(lib.oracle_forward(T, d, dff, a, _ptr(X), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(A), _ptr(U),
-                                  _ptr(H), _ptr(Y)), "oracle_forward")
+        _check(lib.oracle_forward(T, d, dff, a, _ptr(X), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(b1), _ptr(b3), _ptr(b2),
+                                  _ptr(A), _ptr(U), _ptr(H), _ptr(Y)), "oracle_forward")
         return {"A": A, "U": U, "H": H, "Y": Y}
 
-    def backward(self, X, W1, W2, dY, act="gelu", W3=None):
-        """Unsharded backward.  Returns dict with dX, dW1, dW3, dW2, dA (SwiGLU: dG), dU."""
+    def backward(self, X, W1, W2, dY, act="gelu", W3=None, b1=None, b3=None, b2=None):
+        """Unsharded backward.  Returns dict with dX, dW1, dW3, dW2, db1, db3, db2, dA (SwiGLU: dG), dU."""
         lib = self.lib
         a = _act(act)
         X, W1, W2, W3, dY = _f64(X), _f64(W1), _f64(W2), _f64(W3), _f64(dY)
+        b1, b3, b2 = _f64(b1), _f64(b3), _f64(b2)
         T, d = X.shape
         dff = W1.shape[1]
         dX = np.empty((T, d)); dW1 = np.empty((d, dff)); dW2 = np.empty((dff, d))
@@ -164,34 +168,43 @@ class COracle:
         sw = a == ACT_SWIGLU
         dW3 = np.empty((d, dff)) if sw else None
         dU = np.empty((T, dff)) if sw else None
-        _check(lib.oracle_backward(T, d, dff, a, _ptr(X), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dY), _ptr(dX),
-                                   _ptr(dW1), _ptr(dW3), _ptr(dW2), _ptr(dA), _ptr(dU)), "oracle_backward")
-        return {"dX": dX, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dA": dA, "dU": dU}
+        db1, db2 = np.empty(dff), np.empty(d)
+        db3 = np.empty(dff) if sw else None
+        _check(lib.oracle_backward(T, d, dff, a, _ptr(X), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(b1), _ptr(b3), _ptr(b2),
+                                   _ptr(dY), _ptr(dX), _ptr(dW1), _ptr(dW3), _ptr(dW2), _ptr(db1), _ptr(db3), _ptr(db2),
+                                   _ptr(dA), _ptr(dU)), "oracle_backward")
+        return {"dX": dX, "dW1": dW1, "dW3": dW3, "dW2": dW2, "db1": db1, "db3": db3, "db2": db2, "dA": dA, "dU": dU}
 
-    def forward_sharded(self, X, W1_i, W2_i, act="gelu", W3_i=None):
-        """The pages' per-shard forward with the g-sum.  Returns (Y, [H_i])."""
+    def forward_sharded(self, X, W1_i, W2_i, act="gelu", W3_i=None, b1_i=None, b3_i=None, b2=None):
+        """The pages' per-shard forward with the g-sum (b2 added once after it).  Returns (Y, [H_i])."""
         lib = self.lib
         a = _act(act)
         X = _f64(X)
         W1_i = [_f64(w) for w in W1_i]; W2_i = [_f64(w) for w in W2_i]
         W3_i = [_f64(w) for w in W3_i] if W3_i is not None else None
+        b1_i = [_f64(b) for b in b1_i] if b1_i is not None else None
+        b3_i = [_f64(b) for b in b3_i] if b3_i is not None else None
+        b2 = _f64(b2)
         T, d = X.shape
         t = len(W1_i)
         d_i = np.array([w.shape[1] for w in W1_i], dtype=np.int64)
         Y = np.empty((T, d))
         H_i = [np.empty((T, int(di))) for di in d_i]
         _check(lib.oracle_forward_sharded(T, d, t, d_i.ctypes.data_as(ctypes.c_void_p), a, _ptr(X), _ptrs(W1_i),
-                                          _ptrs(W3_i) if W3_i else None, _ptrs(W2_i), _ptr(Y), _ptrs(H_i)),
+                                          _ptrs(W3_i) if W3_i else None, _ptrs(W2_i), _ptrs(b1_i) if b1_i else None,
+                                          _ptrs(b3_i) if b3_i else None, _ptr(b2), _ptr(Y), _ptrs(H_i)),
                "oracle_forward_sharded")
         return Y, H_i
 
-    def backward_sharded(self, X, W1_i, W2_i, dY, act="gelu", W3_i=None):
-        """The pages' per-shard backward with the f-sum.  Returns dict dX, dW1_i, dW3_i, dW2_i."""
+    def backward_sharded(self, X, W1_i, W2_i, dY, act="gelu", W3_i=None, b1_i=None, b3_i=None):
+        """The pages' per-shard backward with the f-sum.  Returns dict dX, dW1_i, dW3_i, dW2_i, db1_i, db3_i, db2."""
         lib = self.lib
         a = _act(act)
         X, dY = _f64(X), _f64(dY)
         W1_i = [_f64(w) for w in W1_i]; W2_i = [_f64(w) for w in W2_i]
         W3_i = [_f64(w) for w in W3_i] if W3_i is not None else None
+        b1_i = [_f64(b) for b in b1_i] if b1_i is not None else None
+        b3_i = [_f64(b) for b in b3_i] if b3_i is not None else None
         T, d = X.shape
         t = len(W1_i)
         d_i = np.array([w.shape[1] for w in W1_i], dtype=np.int64)
@@ -199,39 +212,52 @@ class COracle:
         dW1_i = [np.empty((d, int(di))) for di in d_i]
         dW2_i = [np.empty((int(di), d)) for di in d_i]
         dW3_i = [np.empty((d, int(di))) for di in d_i] if W3_i else None
+        db1_i = [np.empty(int(di)) for di in d_i]
+        db3_i = [np.empty(int(di)) for di in d_i] if W3_i else None
+        db2 = np.empty(d)
         _check(lib.oracle_backward_sharded(T, d, t, d_i.ctypes.data_as(ctypes.c_void_p), a, _ptr(X), _ptrs(W1_i),
-                                           _ptrs(W3_i) if W3_i else None, _ptrs(W2_i), _ptr(dY), _ptr(dX),
-                                           _ptrs(dW1_i), _ptrs(dW3_i) if dW3_i else None, _ptrs(dW2_i)),
+                                           _ptrs(W3_i) if W3_i else None, _ptrs(W2_i), _ptrs(b1_i) if b1_i else None,
+                                           _ptrs(b3_i) if b3_i else None, _ptr(dY), _ptr(dX), _ptrs(dW1_i),
+                                           _ptrs(dW3_i) if dW3_i else None, _ptrs(dW2_i), _ptrs(db1_i),
+                                           _ptrs(db3_i) if db3_i else None, _ptr(db2)),
                "oracle_backward_sharded")
-        return {"dX": dX, "dW1_i": dW1_i, "dW3_i": dW3_i, "dW2_i": dW2_i}
+        return {"dX": dX, "dW1_i": dW1_i, "dW3_i": dW3_i, "dW2_i": dW2_i, "db1_i": db1_i, "db3_i": db3_i, "db2": db2}
 
-    def rows(self, X, W1, W2, dY, rows_idx, act="gelu", W3=None):
+    def rows(self, X, W1, W2, dY, rows_idx, act="gelu", W3=None, b1=None, b3=None, b2=None):
         """Y[r, :] and dX[r, :] for the listed token rows.  Returns (Y_rows, dX_rows)."""
         lib = self.lib
         a = _act(act)
         X, W1, W2, W3, dY = _f64(X), _f64(W1), _f64(W2), _f64(W3), _f64(dY)
+        b1, b3, b2 = _f64(b1), _f64(b3), _f64(b2)
         T, d = X.shape
         dff = W1.shape[1]
         r = np.ascontiguousarray(rows_idx, dtype=np.int64)
         Yr = np.empty((len(r), d)); dXr = np.empty((len(r), d))
-        _check(lib.oracle_rows(T, d, dff, a, _ptr(X), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dY), len(r),
-                               _ptr(r), _ptr(Yr), _ptr(dXr)), "oracle_rows")
+        _check(lib.oracle_rows(T, d, dff, a, _ptr(X), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(b1), _ptr(b3), _ptr(b2),
+                               _ptr(dY), len(r), _ptr(r), _ptr(Yr), _ptr(dXr)), "oracle_rows")
         return Yr, dXr
 
-    def wgrad_units(self, X, W1, W2, dY, units, act="gelu", W3=None):
+    def wgrad_units(self, X, W1, W2, dY, units, act="gelu", W3=None, b1=None, b3=None, with_bias_grads=False):
         """dW1[:, j], dW3[:, j], dW2[j, :] for the listed hidden units j.
 
-        Returns (dW1_cols, dW3_cols or None, dW2_rows), each [len(units) x d]."""
+        Returns (dW1_cols, dW3_cols or None, dW2_rows), each [len(units) x d], and with
+        with_bias_grads also (db1_units, db3_units or None), each [len(units)]."""
         lib = self.lib
         a = _act(act)
         X, W1, W2, W3, dY = _f64(X), _f64(W1), _f64(W2), _f64(W3), _f64(dY)
+        b1, b3 = _f64(b1), _f64(b3)
         T, d = X.shape
         dff = W1.shape[1]
         u = np.ascontiguousarray(units, dtype=np.int64)
         c1 = np.empty((len(u), d)); c2 = np.empty((len(u), d))
         c3 = np.empty((len(u), d)) if a == ACT_SWIGLU else None
-        _check(lib.oracle_wgrad_units(T, d, dff, a, _ptr(X), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dY), len(u),
-                                      _ptr(u), _ptr(c1), _ptr(c3), _ptr(c2)), "oracle_wgrad_units")
+        g1 = np.empty(len(u))
+        g3 = np.empty(len(u)) if a == ACT_SWIGLU else None
+        _check(lib.oracle_wgrad_units(T, d, dff, a, _ptr(X), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(b1), _ptr(b3), _ptr(dY),
+                                      len(u), _ptr(u), _ptr(c1), _ptr(c3), _ptr(c2), _ptr(g1), _ptr(g3)),
+               "oracle_wgrad_units")
+        if with_bias_grads:
+            return c1, c3, c2, g1, g3
         return c1, c3, c2
 
 

@@ -24,31 +24,36 @@ def _sig(g):
     return 1.0 / (1.0 + np.exp(-g))
 
 
-def forward(X, W1, W2, act="gelu", W3=None):
+def _vec(b, n):
+    return np.zeros(n) if b is None else np.asarray(b, dtype=np.float64)
+
+
+def forward(X, W1, W2, act="gelu", W3=None, b1=None, b3=None, b2=None):
     X, W1, W2 = (np.asarray(m, dtype=np.float64) for m in (X, W1, W2))
-    A = X @ W1
+    A = X @ W1 + _vec(b1, W1.shape[1])
     if act == "swiglu":
-        U = X @ np.asarray(W3, dtype=np.float64)
+        U = X @ np.asarray(W3, dtype=np.float64) + _vec(b3, W1.shape[1])
         H = U * (A * _sig(A))
     else:
         U = None
         H = A * ndtr(A)
-    return {"A": A, "U": U, "H": H, "Y": H @ W2}
+    return {"A": A, "U": U, "H": H, "Y": H @ W2 + _vec(b2, W2.shape[1])}
 
 
-def backward(X, W1, W2, dY, act="gelu", W3=None):
+def backward(X, W1, W2, dY, act="gelu", W3=None, b1=None, b3=None, b2=None):
     X, W1, W2, dY = (np.asarray(m, dtype=np.float64) for m in (X, W1, W2, dY))
-    f = forward(X, W1, W2, act, W3)
+    f = forward(X, W1, W2, act, W3, b1, b3, b2)
     A, U, H = f["A"], f["U"], f["H"]
     dH = dY @ W2.T
-    out = {"dW2": H.T @ dY}
+    out = {"dW2": H.T @ dY, "db2": dY.sum(axis=0)}
     if act == "swiglu":
         W3 = np.asarray(W3, dtype=np.float64)
         s = _sig(A)
         dU = dH * (A * s)
         dG = dH * U * (s * (1.0 + A * (1.0 - s)))
-        out.update(dW1=X.T @ dG, dW3=X.T @ dU, dX=dG @ W1.T + dU @ W3.T, dA=dG, dU=dU)
+        out.update(dW1=X.T @ dG, dW3=X.T @ dU, dX=dG @ W1.T + dU @ W3.T, dA=dG, dU=dU, db1=dG.sum(axis=0),
+                   db3=dU.sum(axis=0))
     else:
         dA = dH * (ndtr(A) + A * _phi(A))
-        out.update(dW1=X.T @ dA, dW3=None, dX=dA @ W1.T, dA=dA, dU=None)
+        out.update(dW1=X.T @ dA, dW3=None, dX=dA @ W1.T, dA=dA, dU=None, db1=dA.sum(axis=0), db3=None)
     return out

@@ -33,6 +33,14 @@
  * dX_i are summed by the f operator) and exist so the tests can check the
  * identities the pages state.
  *
+ * Biases (optional, NULL = none): b1 [dff] (and b3 [dff] for SwiGLU) are
+ * added to the first linear's output before the activation, b2 [d] to Y once
+ * after the g-sum -- "Tensor parallelism" (brunomaga.github.io),
+ * Megatron_FeedForward: fc1 carries its bias, fc2 has none and fc2_bias is
+ * added after the all-reduce so that it is not counted once per shard.
+ * Their gradients are column sums over tokens: db1 = sum_r dA[r, :],
+ * db3 = sum_r dU[r, :], db2 = sum_r dY[r, :].
+ *
  * Two extra activations, identity and ReLU, are test hooks: they keep
  * small-integer inputs integral so sharded and unsharded results can be
  * compared exactly.
@@ -115,35 +123,56 @@ static int valid_act(int act) {
          act == ORACLE_ACT_RELU;
 }
 
+/* M[r][c] += b[c] for every row (no-op for b == NULL). */
+static void add_row_bias(int64_t rows, int64_t cols, double* M, const double* b) {
+  if (!b) return;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) M[r * cols + c] += b[c];
+}
+
+/* out[c] = sum over rows r of M[r][c] (r increasing). */
+static void col_sums(int64_t rows, int64_t cols, const double* M, double* out) {
+  if (!out) return;
+  for (int64_t c = 0; c < cols; ++c) out[c] = 0.0;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) out[c] += M[r * cols + c];
+}
+
 /* ---- unsharded forward ----------------------------------------------------
  * Outputs: A (SwiGLU: G) [T x dff], U [T x dff] (SwiGLU only, may be NULL
  * otherwise), H [T x dff], Y [T x d].                                        */
 int oracle_forward(int64_t T, int64_t d, int64_t dff, int act, const double* X, const double* W1,
-                   const double* W3, const double* W2, double* A, double* U, double* H, double* Y) {
+                   const double* W3, const double* W2, const double* b1, const double* b3, const double* b2,
+                   double* A, double* U, double* H, double* Y) {
   if (T < 0 || d < 1 || dff < 1 || !valid_act(act) || !X || !W1 || !W2 || !A || !H || !Y)
     return ORACLE_ERR_ARG;
   if (act == ORACLE_ACT_SWIGLU && (!W3 || !U)) return ORACLE_ERR_ARG;
-  /* A = X W1 */
+  /* A = X W1 + b1 */
   matmul(T, dff, d, X, d, 1, W1, dff, 1, A, dff);
+  add_row_bias(T, dff, A, b1);
   if (act == ORACLE_ACT_SWIGLU) {
-    /* U = X W3; H = U * Swish(G) */
+    /* U = X W3 + b3; H = U * Swish(G) */
     matmul(T, dff, d, X, d, 1, W3, dff, 1, U, dff);
+    add_row_bias(T, dff, U, b3);
     for (int64_t i = 0; i < T * dff; ++i) H[i] = U[i] * swish(A[i]);
   } else {
     for (int64_t i = 0; i < T * dff; ++i) H[i] = act_value(act, A[i]);
   }
-  /* Y = H W2 */
+  /* Y = H W2 + b2 */
   matmul(T, d, dff, H, dff, 1, W2, d, 1, Y, d);
+  add_row_bias(T, d, Y, b2);
   return ORACLE_OK;
 }
 
 /* ---- unsharded backward ---------------------------------------------------
- * Given dY = dL/dY, returns dX, dW1, dW3 (SwiGLU only), dW2 and the
- * activation gradient dA (SwiGLU: dG) / dU, recomputing the forward from X.
- * Any of dAct/dUo may be NULL if not wanted.                                 */
+ * Given dY = dL/dY, returns dX, dW1, dW3 (SwiGLU only), dW2, the bias
+ * gradients db1, db3, db2 (each may be NULL) and the activation gradient dA
+ * (SwiGLU: dG) / dU, recomputing the forward from X.  Any of dAct/dUo may be
+ * NULL if not wanted.                                                        */
 int oracle_backward(int64_t T, int64_t d, int64_t dff, int act, const double* X, const double* W1,
-                    const double* W3, const double* W2, const double* dY, double* dX, double* dW1,
-                    double* dW3, double* dW2, double* dAct, double* dUo) {
+                    const double* W3, const double* W2, const double* b1, const double* b3, const double* b2,
+                    const double* dY, double* dX, double* dW1, double* dW3, double* dW2, double* db1,
+                    double* db3, double* db2, double* dAct, double* dUo) {
   if (T < 0 || d < 1 || dff < 1 || !valid_act(act) || !X || !W1 || !W2 || !dY || !dX || !dW1 || !dW2)
     return ORACLE_ERR_ARG;
   int swiglu = act == ORACLE_ACT_SWIGLU;
@@ -159,7 +188,7 @@ int oracle_backward(int64_t T, int64_t d, int64_t dff, int act, const double* X,
   double* Y = (double*)malloc((size_t)(T * d ? T * d : 1) * sizeof(double));
   int rc = ORACLE_ERR_NOMEM;
   if (!A || !H || !dH || !dA || !Y || (swiglu && (!U || !dU))) goto done;
-  rc = oracle_forward(T, d, dff, act, X, W1, W3, W2, A, U, H, Y);
+  rc = oracle_forward(T, d, dff, act, X, W1, W3, W2, b1, b3, b2, A, U, H, Y);
   if (rc) goto done;
   /* dH = dY W2^T : dH[r][j] = sum_n dY[r][n] W2[j][n] */
   matmul(T, dff, d, dY, d, 1, W2, 1, d, dH, dff);
@@ -186,6 +215,9 @@ int oracle_backward(int64_t T, int64_t d, int64_t dff, int act, const double* X,
     for (int64_t i = 0; i < T * d; ++i) dX[i] += dX3[i];
     free(dX3);
   }
+  col_sums(T, dff, dA, db1);
+  if (swiglu) col_sums(T, dff, dU, db3);
+  col_sums(T, d, dY, db2);
   if (dAct) memcpy(dAct, dA, n * sizeof(double));
   if (dUo && swiglu) memcpy(dUo, dU, n * sizeof(double));
   rc = ORACLE_OK;
@@ -201,7 +233,8 @@ done:
  * [d_i x d], H_i is [T x d_i] (optional output; pass NULL to skip).          */
 int oracle_forward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i, int act,
                            const double* X, const double* const* W1_i, const double* const* W3_i,
-                           const double* const* W2_i, double* Y, double* const* H_i) {
+                           const double* const* W2_i, const double* const* b1_i, const double* const* b3_i,
+                           const double* b2, double* Y, double* const* H_i) {
   if (T < 0 || d < 1 || t < 1 || !d_i || !valid_act(act) || !X || !W1_i || !W2_i || !Y)
     return ORACLE_ERR_ARG;
   int swiglu = act == ORACLE_ACT_SWIGLU;
@@ -220,8 +253,10 @@ int oracle_forward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i, 
       return ORACLE_ERR_NOMEM;
     }
     matmul(T, di, d, X, d, 1, W1_i[s], di, 1, A, di);
+    add_row_bias(T, di, A, b1_i ? b1_i[s] : NULL);
     if (swiglu) {
       matmul(T, di, d, X, d, 1, W3_i[s], di, 1, U, di);
+      add_row_bias(T, di, U, b3_i ? b3_i[s] : NULL);
       for (int64_t i = 0; i < T * di; ++i) H[i] = U[i] * swish(A[i]);
     } else {
       for (int64_t i = 0; i < T * di; ++i) H[i] = act_value(act, A[i]);
@@ -231,6 +266,7 @@ int oracle_forward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i, 
     if (H_i && H_i[s]) memcpy(H_i[s], H, (size_t)(T * di) * sizeof(double));
     free(A); free(U); free(H); free(Z);
   }
+  add_row_bias(T, d, Y, b2); /* once, after the g-sum */
   return ORACLE_OK;
 }
 
@@ -242,8 +278,9 @@ int oracle_forward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i, 
  * dX = sum_i dX_i, summed in shard order.                                    */
 int oracle_backward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i, int act,
                             const double* X, const double* const* W1_i, const double* const* W3_i,
-                            const double* const* W2_i, const double* dY, double* dX,
-                            double* const* dW1_i, double* const* dW3_i, double* const* dW2_i) {
+                            const double* const* W2_i, const double* const* b1_i, const double* const* b3_i,
+                            const double* dY, double* dX, double* const* dW1_i, double* const* dW3_i,
+                            double* const* dW2_i, double* const* db1_i, double* const* db3_i, double* db2) {
   if (T < 0 || d < 1 || t < 1 || !d_i || !valid_act(act) || !X || !W1_i || !W2_i || !dY || !dX ||
       !dW1_i || !dW2_i)
     return ORACLE_ERR_ARG;
@@ -266,8 +303,10 @@ int oracle_backward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i,
     int bad = !A || !H || !dH || !dA || !dXs || (swiglu && (!U || !dU || !dX3));
     if (!bad) {
       matmul(T, di, d, X, d, 1, W1_i[s], di, 1, A, di);
+      add_row_bias(T, di, A, b1_i ? b1_i[s] : NULL);
       if (swiglu) {
         matmul(T, di, d, X, d, 1, W3_i[s], di, 1, U, di);
+        add_row_bias(T, di, U, b3_i ? b3_i[s] : NULL);
         for (int64_t i = 0; i < T * di; ++i) H[i] = U[i] * swish(A[i]);
       } else {
         for (int64_t i = 0; i < T * di; ++i) H[i] = act_value(act, A[i]);
@@ -290,10 +329,13 @@ int oracle_backward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i,
         for (int64_t i = 0; i < T * d; ++i) dXs[i] += dX3[i];
       }
       for (int64_t i = 0; i < T * d; ++i) dX[i] += dXs[i]; /* f: sum of partial dX */
+      col_sums(T, di, dA, db1_i ? db1_i[s] : NULL);
+      if (swiglu) col_sums(T, di, dU, db3_i ? db3_i[s] : NULL);
     }
     free(A); free(U); free(H); free(dH); free(dA); free(dU); free(dXs); free(dX3);
     if (bad) return ORACLE_ERR_NOMEM;
   }
+  col_sums(T, d, dY, db2); /* g backward is the identity: b2 sees dY once */
   return ORACLE_OK;
 }
 
@@ -302,8 +344,8 @@ int oracle_backward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i,
  * its own definition (a token's forward and input gradient depend only on
  * that token's row of X and dY).  Y_rows and dX_rows are [nrows x d].       */
 int oracle_rows(int64_t T, int64_t d, int64_t dff, int act, const double* X, const double* W1,
-                const double* W3, const double* W2, const double* dY, int64_t nrows,
-                const int64_t* rows, double* Y_rows, double* dX_rows) {
+                const double* W3, const double* W2, const double* b1, const double* b3, const double* b2,
+                const double* dY, int64_t nrows, const int64_t* rows, double* Y_rows, double* dX_rows) {
   if (T < 1 || d < 1 || dff < 1 || !valid_act(act) || nrows < 0 || !rows || !X || !W1 || !W2 ||
       !dY || !Y_rows || !dX_rows)
     return ORACLE_ERR_ARG;
@@ -328,6 +370,8 @@ int oracle_rows(int64_t T, int64_t d, int64_t dff, int act, const double* X, con
         s += x[k] * W1[k * dff + j];
         if (swiglu) s3 += x[k] * W3[k * dff + j];
       }
+      if (b1) s += b1[j];
+      if (swiglu && b3) s3 += b3[j];
       for (int64_t n = 0; n < d; ++n) sg += g[n] * W2[j * d + n];
       a[j] = s;
       u[j] = s3;
@@ -347,7 +391,7 @@ int oracle_rows(int64_t T, int64_t d, int64_t dff, int act, const double* X, con
         dx += da[j] * W1[n * dff + j];
         if (swiglu) dx += dh[j] * swish(a[j]) * W3[n * dff + j];
       }
-      Y_rows[q * d + n] = y;
+      Y_rows[q * d + n] = y + (b2 ? b2[n] : 0.0);
       dX_rows[q * d + n] = dx;
     }
     free(a);
@@ -360,8 +404,9 @@ int oracle_rows(int64_t T, int64_t d, int64_t dff, int act, const double* X, con
  * tokens of its definition.  Outputs are [nunits x d]: dW1_cols[q*d + k] =
  * dW1[k][j_q], dW2_rows[q*d + n] = dW2[j_q][n].                              */
 int oracle_wgrad_units(int64_t T, int64_t d, int64_t dff, int act, const double* X, const double* W1,
-                       const double* W3, const double* W2, const double* dY, int64_t nunits,
-                       const int64_t* units, double* dW1_cols, double* dW3_cols, double* dW2_rows) {
+                       const double* W3, const double* W2, const double* b1, const double* b3,
+                       const double* dY, int64_t nunits, const int64_t* units, double* dW1_cols,
+                       double* dW3_cols, double* dW2_rows, double* db1_units, double* db3_units) {
   if (T < 0 || d < 1 || dff < 1 || !valid_act(act) || nunits < 0 || !units || !X || !W1 || !W2 ||
       !dY || !dW1_cols || !dW2_rows)
     return ORACLE_ERR_ARG;
@@ -384,6 +429,8 @@ int oracle_wgrad_units(int64_t T, int64_t d, int64_t dff, int act, const double*
         a += X[r * d + k] * W1[k * dff + j];
         if (swiglu) u += X[r * d + k] * W3[k * dff + j];
       }
+      if (b1) a += b1[j];
+      if (swiglu && b3) u += b3[j];
       for (int64_t n = 0; n < d; ++n) dh += dY[r * d + n] * W2[j * d + n];
       if (swiglu) {
         h[r] = u * swish(a);
@@ -405,6 +452,16 @@ int oracle_wgrad_units(int64_t T, int64_t d, int64_t dff, int act, const double*
       dW1_cols[q * d + k] = s1;
       if (swiglu) dW3_cols[q * d + k] = s3;
       dW2_rows[q * d + k] = s2;
+    }
+    if (db1_units) {
+      double s = 0.0;
+      for (int64_t r = 0; r < T; ++r) s += da[r];
+      db1_units[q] = s;
+    }
+    if (db3_units && swiglu) {
+      double s = 0.0;
+      for (int64_t r = 0; r < T; ++r) s += du[r];
+      db3_units[q] = s;
     }
     free(h);
   }

@@ -356,3 +356,144 @@ def test_planted_mistake_is_caught(mutant, tmp_path):
         assert check_normal_table(clean) < 2e-15
     else:
         assert _row_identity_error(clean) == 0.0
+
+
+# ---------------------------------------------------------------- biases (b1 before the activation, b2 after g)
+
+def test_hand_worked_bias_example():
+    f = _fixture("tiny_mlp_identity_t2_bias.txt")
+    b1, b2 = f["b1"][0], f["b2"][0]
+    fw = oracle.forward(f["X"], f["W1"], f["W2"], act="identity", b1=b1, b2=b2)
+    bw = oracle.backward(f["X"], f["W1"], f["W2"], f["dY"], act="identity", b1=b1, b2=b2)
+    assert np.array_equal(fw["Y"], f["Y"])
+    for k in ("dX", "dW1", "dW2"):
+        assert np.array_equal(bw[k], f[k]), k
+    assert np.array_equal(bw["db1"], f["db1"][0]) and np.array_equal(bw["db2"], f["db2"][0])
+    sl = si.shard_slices([2, 2])
+    Y, _ = oracle.forward_sharded(f["X"], [f["W1"][:, a:b] for a, b in sl], [f["W2"][a:b] for a, b in sl],
+                                  act="identity", b1_i=[b1[a:b] for a, b in sl], b2=b2)
+    assert np.array_equal(Y, f["Y"])
+
+
+def _bias_inputs(rng, d, dff, act, scale=1.0):
+    b1 = rng.normal(size=dff) * scale
+    b3 = rng.normal(size=dff) * scale if act == "swiglu" else None
+    b2 = rng.normal(size=d) * scale
+    return b1, b3, b2
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+@pytest.mark.parametrize("act", ["identity", "relu"])
+def test_bias_sharded_equals_unsharded_exact(t, act):
+    """b2 added once after the g-sum: sharded == unsharded exactly on integers."""
+    inp = si.small_int_inputs(4, 8, [16 // t] * t, act)
+    g = np.random.default_rng(t)
+    b1 = g.integers(-3, 4, 16).astype(np.float64)
+    b2 = g.integers(-3, 4, 8).astype(np.float64)
+    sl = si.shard_slices(inp.d_i)
+    b1_i = [b1[a:b] for a, b in sl]
+    ff = oracle.forward(inp.X, inp.W1, inp.W2, act=act, b1=b1, b2=b2)
+    fb = oracle.backward(inp.X, inp.W1, inp.W2, inp.dY, act=act, b1=b1, b2=b2)
+    Y, _ = oracle.forward_sharded(inp.X, inp.W1_i, inp.W2_i, act=act, b1_i=b1_i, b2=b2)
+    b = oracle.backward_sharded(inp.X, inp.W1_i, inp.W2_i, inp.dY, act=act, b1_i=b1_i)
+    assert np.array_equal(Y, ff["Y"])
+    assert np.array_equal(b["dX"], fb["dX"])
+    assert np.array_equal(np.concatenate(b["db1_i"]), fb["db1"])
+    assert np.array_equal(b["db2"], fb["db2"])
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_bias_finite_differences(act):
+    rng = np.random.default_rng(21)
+    T, d, dff, h = 3, 5, 7, 1e-6
+    X = rng.normal(size=(T, d)); W1 = rng.normal(size=(d, dff)) * 0.5; W2 = rng.normal(size=(dff, d)) * 0.5
+    W3 = rng.normal(size=(d, dff)) * 0.5 if act == "swiglu" else None
+    b1, b3, b2 = _bias_inputs(rng, d, dff, act, 0.5)
+    dY = rng.normal(size=(T, d))
+    P = {"b1": b1, "b2": b2}
+    if b3 is not None:
+        P["b3"] = b3
+
+    def loss(p):
+        return float(np.sum(dY * oracle.forward(X, W1, W2, act=act, W3=W3, b1=p["b1"], b3=p.get("b3"),
+                                                 b2=p["b2"])["Y"]))
+
+    g = oracle.backward(X, W1, W2, dY, act=act, W3=W3, b1=b1, b3=b3, b2=b2)
+    for name, val in P.items():
+        num = np.zeros_like(val)
+        for i in range(val.size):
+            pp = {k: v.copy() for k, v in P.items()}; pp[name][i] += h
+            pm = {k: v.copy() for k, v in P.items()}; pm[name][i] -= h
+            num[i] = (loss(pp) - loss(pm)) / (2 * h)
+        ana = g["d" + name]
+        assert np.max(np.abs(num - ana)) / np.max(np.abs(ana)) < 1e-7, name
+    # the weight gradients still match finite differences with biases present
+    num = np.zeros_like(X)
+    for idx in np.ndindex(X.shape):
+        Xp = X.copy(); Xp[idx] += h
+        Xm = X.copy(); Xm[idx] -= h
+        yp = oracle.forward(Xp, W1, W2, act=act, W3=W3, b1=b1, b3=b3, b2=b2)["Y"]
+        ym = oracle.forward(Xm, W1, W2, act=act, W3=W3, b1=b1, b3=b3, b2=b2)["Y"]
+        num[idx] = np.sum(dY * (yp - ym)) / (2 * h)
+    assert np.max(np.abs(num - g["dX"])) / np.max(np.abs(g["dX"])) < 1e-7
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_bias_c_oracle_matches_numpy(act):
+    rng = np.random.default_rng(31)
+    T, d, dff = 17, 12, 40
+    X = rng.normal(size=(T, d)); W1 = rng.normal(size=(d, dff)) * 0.2; W2 = rng.normal(size=(dff, d)) * 0.2
+    W3 = rng.normal(size=(d, dff)) * 0.2
+    b1, b3, b2 = _bias_inputs(rng, d, dff, act)
+    dY = rng.normal(size=(T, d))
+    c_f = oracle.forward(X, W1, W2, act=act, W3=W3, b1=b1, b3=b3, b2=b2)
+    c_b = oracle.backward(X, W1, W2, dY, act=act, W3=W3, b1=b1, b3=b3, b2=b2)
+    n_f = np_oracle.forward(X, W1, W2, act=act, W3=W3, b1=b1, b3=b3, b2=b2)
+    n_b = np_oracle.backward(X, W1, W2, dY, act=act, W3=W3, b1=b1, b3=b3, b2=b2)
+    pairs = [(c_f["Y"], n_f["Y"]), (c_b["dX"], n_b["dX"]), (c_b["dW1"], n_b["dW1"]), (c_b["dW2"], n_b["dW2"]),
+             (c_b["db1"], n_b["db1"]), (c_b["db2"], n_b["db2"])]
+    if act == "swiglu":
+        pairs += [(c_b["db3"], n_b["db3"]), (c_b["dW3"], n_b["dW3"])]
+    for a, b in pairs:
+        assert np.max(np.abs(a - b)) <= 1e-12 * max(1.0, np.max(np.abs(b)))
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_bias_sampled_rows_and_units(act):
+    rng = np.random.default_rng(41)
+    T, d, dff = 29, 16, 24
+    X = rng.normal(size=(T, d)); W1 = rng.normal(size=(d, dff)) * 0.2; W2 = rng.normal(size=(dff, d)) * 0.2
+    W3 = rng.normal(size=(d, dff)) * 0.2 if act == "swiglu" else None
+    b1, b3, b2 = _bias_inputs(rng, d, dff, act)
+    dY = rng.normal(size=(T, d))
+    f = np_oracle.forward(X, W1, W2, act=act, W3=W3, b1=b1, b3=b3, b2=b2)
+    b = np_oracle.backward(X, W1, W2, dY, act=act, W3=W3, b1=b1, b3=b3, b2=b2)
+    r = np.array([0, 3, 28])
+    Yr, dXr = oracle.rows(X, W1, W2, dY, r, act=act, W3=W3, b1=b1, b3=b3, b2=b2)
+    np.testing.assert_allclose(Yr, f["Y"][r], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dXr, b["dX"][r], rtol=0, atol=1e-12)
+    u = np.array([0, 7, 23])
+    c1, c3, c2, g1, g3 = oracle.wgrad_units(X, W1, W2, dY, u, act=act, W3=W3, b1=b1, b3=b3, with_bias_grads=True)
+    np.testing.assert_allclose(c1, b["dW1"][:, u].T, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(c2, b["dW2"][u, :], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(g1, b["db1"][u], rtol=0, atol=1e-11)
+    if act == "swiglu":
+        np.testing.assert_allclose(g3, b["db3"][u], rtol=0, atol=1e-11)
+
+
+def test_planted_bias_per_shard_is_caught(tmp_path):
+    """Adding b2 inside every shard (before the g-sum) counts it t times; the
+    exact sharded == unsharded pin must catch it."""
+    src = open(_SRC).read()
+    find = "    matmul(T, d, di, H, di, 1, W2_i[s], d, 1, Z, d);\n"
+    assert src.count(find) == 1
+    msrc = tmp_path / "mutant_bias.c"
+    msrc.write_text(src.replace(find, find + "    add_row_bias(T, d, Z, b2);\n"))
+    o = oracle.load_variant(oracle.build(force=True, src=str(msrc), out=str(tmp_path / "libmutant_bias.so")))
+    inp = si.small_int_inputs(4, 8, [4, 4, 8], "relu")
+    b2 = np.arange(8, dtype=np.float64) - 3
+    Y, _ = o.forward_sharded(inp.X, inp.W1_i, inp.W2_i, act="relu", b2=b2)
+    ff = o.forward(inp.X, inp.W1, inp.W2, act="relu", b2=b2)
+    assert np.max(np.abs(Y - ff["Y"])) >= 1.0
+    Yc, _ = oracle.forward_sharded(inp.X, inp.W1_i, inp.W2_i, act="relu", b2=b2)
+    assert np.array_equal(Yc, oracle.forward(inp.X, inp.W1, inp.W2, act="relu", b2=b2)["Y"])
