@@ -61,6 +61,35 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ("tc_gemm.cu", "ptx.cuh", "act.cuh", "tpmlp_internal.h", "tpmlp_api.cu")
+
+
+def kernel_sources_sha256() -> str:
+    """Hash of the sources that define the tensor-core kernel and its launches."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "megatron_tensor_transformer_column_gb300", "csrc")
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from profiles/dram_traffic.json when they were taken
+    with the current kernel sources on this workload (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    for r in rec.get("records", []):
+        if (r.get("kernel") == kernel and r.get("workload") == workload
+                and r.get("sources_sha256") == kernel_sources_sha256()):
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
 def workload_config(w: si.Workload, extra=None):
     cfg = {"workload": w.name, "T": w.T, "b": w.b, "s": w.s, "d": w.d, "d_ff": w.dff, "t": w.t,
            "d_i": list(w.d_i), "act": w.act,
@@ -255,20 +284,27 @@ def run_ours(args, w: si.Workload):
     dact, dX, dW1, dW3, dW2 = mlp.alloc_backward()
     stream = torch.cuda.current_stream(dev)
     plan, wsp = mlp.plan, mlp.workspace
+    b1 = b3 = b2 = db1 = db3 = db2 = None
+    if args.bias:  # b1 (b3) before the activation, b2 after the g-sum, and their gradients
+        bias = si.make_biases(w.d, w.d_i, w.act, w.dtype)
+        b1 = [x.to(dev) for x in bias["b1_i"]]
+        b3 = [x.to(dev) for x in bias["b3_i"]] if sw else None
+        b2 = bias["b2"].to(dev)
+        db1, db3, db2 = mlp.alloc_bias_grads()
 
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        tp.tpmlp_forward_column(plan, X, W1, W3, saved, H, wsp, stream)
+        tp.tpmlp_forward_column(plan, X, W1, W3, b1, b3, saved, H, wsp, stream)
         if ev:
             ev[1].record(stream)
-        tp.tpmlp_forward_row(plan, W2, H, Y, wsp, stream)
+        tp.tpmlp_forward_row(plan, W2, b2, H, Y, wsp, stream)
         if ev:
             ev[2].record(stream)
-        tp.tpmlp_backward_dgrad(plan, W2, saved, H, dY, dact, dW2, wsp, stream)
+        tp.tpmlp_backward_dgrad(plan, W2, saved, H, dY, dact, dW2, db2, wsp, stream)
         if ev:
             ev[3].record(stream)
-        tp.tpmlp_backward_fsum(plan, X, W1, W3, dact, dX, dW1, dW3, wsp, stream)
+        tp.tpmlp_backward_fsum(plan, X, W1, W3, dact, dX, dW1, dW3, db1, db3, wsp, stream)
         if ev:
             ev[4].record(stream)
 
@@ -312,7 +348,7 @@ def run_ours(args, w: si.Workload):
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": achieved / peak_sus, "traffic": None,
+                "frac": achieved / peak_sus, "traffic": None if args.bias else measured_traffic(dom, w.name),
                 "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); "
                              f"frac of {peak_src} burst {peak_burst}: {achieved / peak_burst:.3f}"}
     if rank != 0:
@@ -324,14 +360,16 @@ def run_ours(args, w: si.Workload):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) X/dY, N(0,0.02) W, rounded once to bf16)",
-        "config": workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)"}),
+        "config": workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)",
+                                      **({"bias": "b1/b3 before the activation, b2 after the g-sum, with db"}
+                                         if args.bias else {})}),
         "pct_of_peak": {"sustained": value / ws / peak_sus, "burst": value / ws / peak_burst, "source": peak_src},
         "tokens_per_s": w.T * ws * args.steps / (elapsed_ms / 1e3),
         "phase_ms": per_phase,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (6 if args.bias else 4) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -368,10 +406,10 @@ def run_e2e(args, w, tp, mlp, inp, dev, stream, ws):
         ddY.copy_(hdY, non_blocking=True)
         for d_, h_ in zip(dW1_in + dW2_in + dW3_in, hW1 + hW2 + hW3):
             d_.copy_(h_, non_blocking=True)
-        tp.tpmlp_forward(mlp.plan, dX_in, dW1_in, dW3_in if sw else None, dW2_in, Y, saved, H, mlp.workspace,
-                         stream)
+        tp.tpmlp_forward(mlp.plan, dX_in, dW1_in, dW3_in if sw else None, dW2_in, None, None, None, Y, saved, H,
+                         mlp.workspace, stream)
         tp.tpmlp_backward(mlp.plan, dX_in, dW1_in, dW3_in if sw else None, dW2_in, saved, H, ddY, dact, dX, dW1,
-                          dW3, dW2, mlp.workspace, stream)
+                          dW3, dW2, None, None, None, mlp.workspace, stream)
         for h_, d_ in zip(outs_host, outs_dev):
             h_.copy_(d_, non_blocking=True)
 
@@ -403,6 +441,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="C5", choices=sorted(si.WORKLOADS))
     ap.add_argument("--oracle-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bias", action="store_true", help="include the optional biases and their gradients")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     w = si.WORKLOADS[args.workload]

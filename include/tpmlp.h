@@ -16,6 +16,14 @@
  *     forward and the identity backward: same page, the f/g operator table;
  *     "Tensor parallelism" (brunomaga.github.io), Megatron_f / Megatron_g;
  *     "AI Training Network Primer" ch. 3, section 3.4, Fig. 3.4 and 3.6.
+ * Optional biases (any may be NULL): b1_i [d_i] (SwiGLU also b3_i [d_i]) are
+ * added to X W1_i (X W3_i) before the activation; b2 [d] is added to Y once,
+ * after the g-sum, not once per shard ("Tensor parallelism",
+ * brunomaga.github.io, Megatron_FeedForward: fc2 has no bias, fc2_bias is
+ * added after the all-reduce).  Their gradients are sums over tokens:
+ * db2 = sum_r dY[r, :], db1_i = sum_r dA_i[r, :] (SwiGLU dG_i), db3_i =
+ * sum_r dU_i[r, :]; they cost one extra, HBM-bound launch per backward phase
+ * that asks for them.
  * On one GPU the t shards sit side by side in HBM and both sums are
  * accumulations in the kernels' fp32 accumulators: the g-sum inside the
  * row-parallel GEMM's K loop, the f-sum inside the dX GEMM's K loop.  There
@@ -100,7 +108,9 @@ TPMLP_API void tpmlp_plan_destroy(tpmlp_plan* plan);
 TPMLP_API size_t tpmlp_workspace_size(const tpmlp_plan* plan);
 
 /* Forward.  Inputs X [T x d]; W1[i], W3[i] (SwiGLU only; pass NULL for GeLU)
- * [d x d_i]; W2[i] [d_i x d].  Outputs: Y [T x d]; H[i] [T x d_i]; saved =
+ * [d x d_i]; W2[i] [d_i x d]; optional biases b1[i], b3[i] (SwiGLU) [d_i] and
+ * b2 [d] (NULL for none; b1 and b3 are arrays of t device pointers).
+ * Outputs: Y [T x d]; H[i] [T x d_i]; saved =
  * the pre-activations kept for backward: GeLU t pointers A_i [T x d_i];
  * SwiGLU 2t pointers, G_0..G_{t-1} then U_0..U_{t-1}, each [T x d_i].
  * Two kernels run: the column-parallel GEMM with the activation fused into
@@ -108,34 +118,37 @@ TPMLP_API size_t tpmlp_workspace_size(const tpmlp_plan* plan);
  * row-parallel GEMM whose K loop walks shard 0..t-1 into one fp32
  * accumulator (the g-sum).                                                    */
 TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_plan* plan, const void* X, const void* const* W1,
-                           const void* const* W3, const void* const* W2, void* Y, void* const* saved,
-                           void* const* H, void* workspace, tpmlp_stream_t stream);
+                                     const void* const* W3, const void* const* W2, const void* const* b1,
+                                     const void* const* b3, const void* b2, void* Y, void* const* saved,
+                                     void* const* H, void* workspace, tpmlp_stream_t stream);
 
 /* Backward.  Inputs: X, W1, W3, W2 as in forward; saved and H as written by
  * tpmlp_forward; dY [T x d].  Outputs: dact = per-shard activation gradients
  * (GeLU t pointers dA_i; SwiGLU 2t pointers dG_0..dG_{t-1}, dU_0..dU_{t-1},
  * each [T x d_i]), dX [T x d], dW1[i], dW3[i] (SwiGLU only, else NULL)
- * [d x d_i], dW2[i] [d_i x d].
+ * [d x d_i], dW2[i] [d_i x d], and optionally the bias gradients db1[i],
+ * db3[i] [d_i] and db2 [d] (NULL: not computed).
  * g backward is the identity (every shard reads the same dY).  Two kernels
  * run: (1) dH_i = dY W2_i^T with act' fused (writes dact) together with
  * dW2_i = H_i^T dY; (2) dX = sum_i dA_i W1_i^T (SwiGLU: + dU_i W3_i^T) with
  * the f-sum in one fp32 accumulator, together with dW1_i = X^T dA_i
  * (dW3_i = X^T dU_i).  With T = 0 the weight gradients are zero-filled.       */
 TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_plan* plan, const void* X, const void* const* W1,
-                            const void* const* W3, const void* const* W2, const void* const* saved,
-                            const void* const* H, const void* dY, void* const* dact, void* dX,
-                            void* const* dW1, void* const* dW3, void* const* dW2, void* workspace,
-                            tpmlp_stream_t stream);
+                                      const void* const* W3, const void* const* W2, const void* const* saved,
+                                      const void* const* H, const void* dY, void* const* dact, void* dX,
+                                      void* const* dW1, void* const* dW3, void* const* dW2, void* const* db1,
+                                      void* const* db3, void* db2, void* workspace, tpmlp_stream_t stream);
 
 /* The two launches of tpmlp_forward, callable one at a time (same arguments
  * and layouts; each is exactly one kernel launch):
- *   tpmlp_forward_column: saved and H from X, W1 (and W3).
- *   tpmlp_forward_row:    Y = sum_i H_i W2_i (the g-sum in the accumulator). */
+ *   tpmlp_forward_column: saved and H from X, W1 (and W3), b1 (and b3).
+ *   tpmlp_forward_row:    Y = sum_i H_i W2_i + b2 (the g-sum in the accumulator). */
 TPMLP_API tpmlp_status tpmlp_forward_column(const tpmlp_plan* plan, const void* X, const void* const* W1,
-                                  const void* const* W3, void* const* saved, void* const* H, void* workspace,
-                                  tpmlp_stream_t stream);
-TPMLP_API tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* const* W2, void* const* H, void* Y,
-                               void* workspace, tpmlp_stream_t stream);
+                                            const void* const* W3, const void* const* b1, const void* const* b3,
+                                            void* const* saved, void* const* H, void* workspace,
+                                            tpmlp_stream_t stream);
+TPMLP_API tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* const* W2, const void* b2,
+                                         void* const* H, void* Y, void* workspace, tpmlp_stream_t stream);
 
 /* tpmlp_forward_row without a workspace argument, for callers that cannot
  * allocate device memory: code handed only its input and output buffers by a
@@ -144,8 +157,8 @@ TPMLP_API tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* con
  * call cudaMalloc because it synchronises the whole device.  The pages have
  * no counterpart: it is an interface variant, not a step of the method.
  *
- * Same arguments, layouts and result as tpmlp_forward_row (one launch of the
- * row-parallel GEMM whose K loop carries the g-sum).  Its only scratch, the
+ * Same arguments, layouts and result as tpmlp_forward_row with b2 = NULL
+ * (one launch of the row-parallel GEMM whose K loop carries the g-sum).  Its only scratch, the
  * device status word, lives in a library-owned static device array of
  * 256 bytes (held by every GPU that loads the library until the process
  * exits); the call allocates and frees nothing.  The first call on a device
@@ -162,16 +175,20 @@ TPMLP_API tpmlp_status tpmlp_forward_row_noalloc(const tpmlp_plan* plan, const v
 
 /* The two launches of tpmlp_backward, callable one at a time:
  *   tpmlp_backward_dgrad: dact from dY, W2 and saved (act' fused), and dW2
- *                         from H and dY.
+ *                         from H and dY; db2 (optional) from dY.
  *   tpmlp_backward_fsum:  dX = sum_i dact_i W1_i^T (+ dU_i W3_i^T) (the
  *                         f-sum in the accumulator), dW1 and dW3 from X and
- *                         dact.  Must follow tpmlp_backward_dgrad.          */
+ *                         dact; db1, db3 (optional) from dact.  Must follow
+ *                         tpmlp_backward_dgrad.
+ * Each is one GEMM launch, plus one column-sum launch when bias gradients are
+ * requested.                                                                 */
 TPMLP_API tpmlp_status tpmlp_backward_dgrad(const tpmlp_plan* plan, const void* const* W2, const void* const* saved,
-                                  const void* const* H, const void* dY, void* const* dact, void* const* dW2,
-                                  void* workspace, tpmlp_stream_t stream);
+                                            const void* const* H, const void* dY, void* const* dact,
+                                            void* const* dW2, void* db2, void* workspace, tpmlp_stream_t stream);
 TPMLP_API tpmlp_status tpmlp_backward_fsum(const tpmlp_plan* plan, const void* X, const void* const* W1,
-                                 const void* const* W3, const void* const* dact, void* dX, void* const* dW1,
-                                 void* const* dW3, void* workspace, tpmlp_stream_t stream);
+                                           const void* const* W3, const void* const* dact, void* dX,
+                                           void* const* dW1, void* const* dW3, void* const* db1, void* const* db3,
+                                           void* workspace, tpmlp_stream_t stream);
 
 /* Watchdog controls, for testing the failure path without faulting a GPU.
  * Neither may run while another call uses the plan.
@@ -200,7 +217,7 @@ TPMLP_API int tpmlp_last_cuda_error(void);
  * map error; empty string after a successful call).  Static storage per
  * thread, valid until the next call on the same thread.                      */
 TPMLP_API const char* tpmlp_last_error(void);
-/* ABI version: 100 * major + minor. */
+/* ABI version: 100 * major + minor (1.01: optional biases). */
 TPMLP_API int tpmlp_version(void);
 
 /* Kernel launches the last tpmlp_forward / tpmlp_backward call on this

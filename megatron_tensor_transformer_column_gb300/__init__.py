@@ -89,19 +89,19 @@ def load():
         lib.tpmlp_plan_set_stall_injection.restype = st
         lib.tpmlp_workspace_size.argtypes = [vp]
         lib.tpmlp_workspace_size.restype = ctypes.c_size_t
-        lib.tpmlp_forward.argtypes = [vp, vp, pp, pp, pp, vp, pp, pp, vp, vp]
+        lib.tpmlp_forward.argtypes = [vp, vp, pp, pp, pp, pp, pp, vp, vp, pp, pp, vp, vp]
         lib.tpmlp_forward.restype = st
-        lib.tpmlp_backward.argtypes = [vp, vp, pp, pp, pp, pp, pp, vp, pp, vp, pp, pp, pp, vp, vp]
+        lib.tpmlp_backward.argtypes = [vp, vp, pp, pp, pp, pp, pp, vp, pp, vp, pp, pp, pp, pp, pp, vp, vp, vp]
         lib.tpmlp_backward.restype = st
-        lib.tpmlp_forward_column.argtypes = [vp, vp, pp, pp, pp, pp, vp, vp]
+        lib.tpmlp_forward_column.argtypes = [vp, vp, pp, pp, pp, pp, pp, pp, vp, vp]
         lib.tpmlp_forward_column.restype = st
-        lib.tpmlp_forward_row.argtypes = [vp, pp, pp, vp, vp, vp]
+        lib.tpmlp_forward_row.argtypes = [vp, pp, vp, pp, vp, vp, vp]
         lib.tpmlp_forward_row.restype = st
         lib.tpmlp_forward_row_noalloc.argtypes = [vp, pp, pp, vp, vp]
         lib.tpmlp_forward_row_noalloc.restype = st
-        lib.tpmlp_backward_dgrad.argtypes = [vp, pp, pp, pp, vp, pp, pp, vp, vp]
+        lib.tpmlp_backward_dgrad.argtypes = [vp, pp, pp, pp, vp, pp, pp, vp, vp, vp]
         lib.tpmlp_backward_dgrad.restype = st
-        lib.tpmlp_backward_fsum.argtypes = [vp, vp, pp, pp, pp, vp, pp, pp, vp, vp]
+        lib.tpmlp_backward_fsum.argtypes = [vp, vp, pp, pp, pp, vp, pp, pp, pp, pp, vp, vp]
         lib.tpmlp_backward_fsum.restype = st
         lib.tpmlp_check.argtypes = [vp, vp, vp]
         lib.tpmlp_check.restype = st
@@ -207,25 +207,26 @@ def tpmlp_workspace_size(plan: Plan) -> int:
     return int(load().tpmlp_workspace_size(plan.handle))
 
 
-def tpmlp_forward(plan, X, W1, W3, W2, Y, saved, H, workspace, stream=None):
-    _ok(load().tpmlp_forward(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(W2), _addr(Y), _arr(saved), _arr(H),
-                             _addr(workspace), _stream(stream)), "tpmlp_forward")
+def tpmlp_forward(plan, X, W1, W3, W2, b1, b3, b2, Y, saved, H, workspace, stream=None):
+    _ok(load().tpmlp_forward(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(W2), _arr(b1), _arr(b3), _addr(b2),
+                             _addr(Y), _arr(saved), _arr(H), _addr(workspace), _stream(stream)), "tpmlp_forward")
 
 
-def tpmlp_backward(plan, X, W1, W3, W2, saved, H, dY, dact, dX, dW1, dW3, dW2, workspace, stream=None):
+def tpmlp_backward(plan, X, W1, W3, W2, saved, H, dY, dact, dX, dW1, dW3, dW2, db1, db3, db2, workspace,
+                   stream=None):
     _ok(load().tpmlp_backward(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(W2), _arr(saved), _arr(H),
-                              _addr(dY), _arr(dact), _addr(dX), _arr(dW1), _arr(dW3), _arr(dW2), _addr(workspace),
-                              _stream(stream)), "tpmlp_backward")
+                              _addr(dY), _arr(dact), _addr(dX), _arr(dW1), _arr(dW3), _arr(dW2), _arr(db1),
+                              _arr(db3), _addr(db2), _addr(workspace), _stream(stream)), "tpmlp_backward")
 
 
-def tpmlp_forward_column(plan, X, W1, W3, saved, H, workspace, stream=None):
-    _ok(load().tpmlp_forward_column(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(saved), _arr(H),
-                                    _addr(workspace), _stream(stream)), "tpmlp_forward_column")
+def tpmlp_forward_column(plan, X, W1, W3, b1, b3, saved, H, workspace, stream=None):
+    _ok(load().tpmlp_forward_column(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(b1), _arr(b3), _arr(saved),
+                                    _arr(H), _addr(workspace), _stream(stream)), "tpmlp_forward_column")
 
 
-def tpmlp_forward_row(plan, W2, H, Y, workspace, stream=None):
-    _ok(load().tpmlp_forward_row(plan.handle, _arr(W2), _arr(H), _addr(Y), _addr(workspace), _stream(stream)),
-        "tpmlp_forward_row")
+def tpmlp_forward_row(plan, W2, b2, H, Y, workspace, stream=None):
+    _ok(load().tpmlp_forward_row(plan.handle, _arr(W2), _addr(b2), _arr(H), _addr(Y), _addr(workspace),
+                                 _stream(stream)), "tpmlp_forward_row")
 
 
 def tpmlp_forward_row_noalloc(plan, W2, H, Y, stream=None):
@@ -236,14 +237,15 @@ def tpmlp_forward_row_noalloc(plan, W2, H, Y, stream=None):
         "tpmlp_forward_row_noalloc")
 
 
-def tpmlp_backward_dgrad(plan, W2, saved, H, dY, dact, dW2, workspace, stream=None):
+def tpmlp_backward_dgrad(plan, W2, saved, H, dY, dact, dW2, db2, workspace, stream=None):
     _ok(load().tpmlp_backward_dgrad(plan.handle, _arr(W2), _arr(saved), _arr(H), _addr(dY), _arr(dact), _arr(dW2),
-                                    _addr(workspace), _stream(stream)), "tpmlp_backward_dgrad")
+                                    _addr(db2), _addr(workspace), _stream(stream)), "tpmlp_backward_dgrad")
 
 
-def tpmlp_backward_fsum(plan, X, W1, W3, dact, dX, dW1, dW3, workspace, stream=None):
+def tpmlp_backward_fsum(plan, X, W1, W3, dact, dX, dW1, dW3, db1, db3, workspace, stream=None):
     _ok(load().tpmlp_backward_fsum(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(dact), _addr(dX), _arr(dW1),
-                                   _arr(dW3), _addr(workspace), _stream(stream)), "tpmlp_backward_fsum")
+                                   _arr(dW3), _arr(db1), _arr(db3), _addr(workspace), _stream(stream)),
+        "tpmlp_backward_fsum")
 
 
 def tpmlp_check(plan, workspace, stream=None):
@@ -321,17 +323,26 @@ class ShardedMLP:
         dW2 = [self._empty(w, p.d) for w in p.d_i]
         return dact, dX, dW1, dW3, dW2
 
-    def forward(self, X, W1_i, W2_i, W3_i=None, out=None, stream=None):
+    def forward(self, X, W1_i, W2_i, W3_i=None, out=None, stream=None, b1_i=None, b3_i=None, b2=None):
+        """Y = sum_i act(X W1_i + b1_i) W2_i + b2 (biases optional).  Returns (Y, saved, H)."""
         self.check_inputs(X, W1_i, W2_i, W3_i)
         Y, saved, H = out if out is not None else self.alloc_forward()
-        tpmlp_forward(self.plan, X, W1_i, W3_i, W2_i, Y, saved, H, self.workspace, stream)
+        tpmlp_forward(self.plan, X, W1_i, W3_i, W2_i, b1_i, b3_i, b2, Y, saved, H, self.workspace, stream)
         return Y, saved, H
 
-    def backward(self, X, W1_i, W2_i, saved, H, dY, W3_i=None, out=None, stream=None):
+    def alloc_bias_grads(self):
+        p = self.plan
+        db1 = [self._empty(w) for w in p.d_i]
+        db3 = [self._empty(w) for w in p.d_i] if self.swiglu else None
+        return db1, db3, self._empty(p.d)
+
+    def backward(self, X, W1_i, W2_i, saved, H, dY, W3_i=None, out=None, stream=None, bias_grads=False):
+        """Gradients of X, the weights and, with bias_grads, the biases."""
         dact, dX, dW1, dW3, dW2 = out if out is not None else self.alloc_backward()
-        tpmlp_backward(self.plan, X, W1_i, W3_i, W2_i, saved, H, dY, dact, dX, dW1, dW3, dW2, self.workspace,
-                       stream)
-        return {"dX": dX, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dact": dact}
+        db1, db3, db2 = self.alloc_bias_grads() if bias_grads else (None, None, None)
+        tpmlp_backward(self.plan, X, W1_i, W3_i, W2_i, saved, H, dY, dact, dX, dW1, dW3, dW2, db1, db3, db2,
+                       self.workspace, stream)
+        return {"dX": dX, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dact": dact, "db1": db1, "db3": db3, "db2": db2}
 
     def check(self, stream=None):
         tpmlp_check(self.plan, self.workspace, stream)

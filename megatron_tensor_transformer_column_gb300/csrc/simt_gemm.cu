@@ -98,20 +98,26 @@ __global__ void __launch_bounds__(kThreads) tpmlp_fp32_simt_gemm(const __grid_co
     const int64_t row = m0 + 4 * ty + i;
     if (row >= P.M) continue;
     const int64_t o = row * P.ldo + col;
-    const float v = acc[i];
+    float v = acc[i];
     switch (P.epi) {
       case EPI_STORE:
+        if (P.aux0) v += static_cast<const float*>(P.aux0)[col];
         static_cast<float*>(P.out0)[o] = v;
         break;
       case EPI_GELU_FWD:
+        if (P.aux0) v += static_cast<const float*>(P.aux0)[col];
         static_cast<float*>(P.out0)[o] = v;
         static_cast<float*>(P.out1)[o] = act::gelu(v);
         break;
-      case EPI_SWIGLU_FWD:
+      case EPI_SWIGLU_FWD: {
+        float u = acc2[i];
+        if (P.aux0) v += static_cast<const float*>(P.aux0)[col];
+        if (P.aux1) u += static_cast<const float*>(P.aux1)[col];
         static_cast<float*>(P.out0)[o] = v;
-        static_cast<float*>(P.out1)[o] = acc2[i];
-        static_cast<float*>(P.out2)[o] = acc2[i] * act::swish(v);
+        static_cast<float*>(P.out1)[o] = u;
+        static_cast<float*>(P.out2)[o] = u * act::swish(v);
         break;
+      }
       case EPI_GELU_BWD:
         static_cast<float*>(P.out0)[o] = v * act::gelu_grad(static_cast<const float*>(P.aux0)[o]);
         break;

@@ -316,6 +316,15 @@ __device__ __forceinline__ void load_row32(const void* src, int64_t ld, int64_t 
   }
 }
 
+// v[j] += bias[col + j] for the chunk's valid columns (bias may be null).
+__device__ __forceinline__ void add_bias32(const void* bias, int col, int nvalid, float (&v)[32]) {
+  if (!bias) return;
+  float b[32];
+  load_row32(bias, 0, 0, col, nvalid, b);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] += b[j];
+}
+
 // Epilogue of one 32-column chunk of one accumulator row (single accumulator).
 __device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int col, int nvalid,
                                                const uint32_t (&r)[32]) {
@@ -324,9 +333,11 @@ __device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int c
   for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
   switch (P.epi) {
     case EPI_STORE:
+      add_bias32(P.aux0, col, nvalid, acc);
       store_row32(P.out0, P.ldo, row, col, nvalid, acc);
       break;
     case EPI_GELU_FWD: {
+      add_bias32(P.aux0, col, nvalid, acc);
       store_row32(P.out0, P.ldo, row, col, nvalid, acc);  // A (pre-activation)
       float h[32];
 #pragma unroll
@@ -589,8 +600,11 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
               for (int j = 0; j < 32; ++j) {
                 g[j] = __uint_as_float(rg[j]);
                 u[j] = __uint_as_float(ru[j]);
-                h[j] = u[j] * act::swish_fast(g[j]);
               }
+              add_bias32(P.aux0, ti.n0 + col, nvalid, g);
+              add_bias32(P.aux1, ti.n0 + col, nvalid, u);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) h[j] = u[j] * act::swish_fast(g[j]);
               store_row32(P.out0, P.ldo, grow, ti.n0 + col, nvalid, g);
               store_row32(P.out1, P.ldo, grow, ti.n0 + col, nvalid, u);
               store_row32(P.out2, P.ldo, grow, ti.n0 + col, nvalid, h);

@@ -288,9 +288,35 @@ tpmlp_status common_checks(const tpmlp_plan* pl, void* workspace, DeviceInfo* di
   return device_info(di);
 }
 
+// ------------------------------------------------------------------ bias gradients
+// dst_j[c] = sum over the T rows of src_j[r][c], one launch for all jobs.
+struct ColsumBuilder {
+  ColsumParams p{};
+  int strip_cols;
+  explicit ColsumBuilder(bool bf16) : strip_cols(colsum_strip_cols(bf16)) {}
+  void add(const void* src, void* dst, int64_t rows, int64_t cols) {
+    ColsumJob& J = p.jobs[p.num_jobs++];
+    J.src = src;
+    J.dst = dst;
+    J.rows = rows;
+    J.cols = static_cast<int32_t>(cols);
+    J.strip_begin = p.total_strips;
+    p.total_strips += static_cast<int32_t>((cols + strip_cols - 1) / strip_cols);
+  }
+};
+
+tpmlp_status launch_colsums(const ColsumBuilder& C, const tpmlp_plan* pl, cudaStream_t st) {
+  if (C.p.num_jobs == 0) return TPMLP_OK;
+  cudaError_t e = launch_colsum(C.p, pl->dtype == TPMLP_BF16, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  ++g_last_launches;
+  return TPMLP_OK;
+}
+
 // ------------------------------------------------------------------ phases
 tpmlp_status fwd_column(const tpmlp_plan* pl, const DeviceInfo& di, const void* X, const void* const* W1,
-                        const void* const* W3, void* const* saved, void* const* H, void* ws, cudaStream_t st) {
+                        const void* const* W3, const void* const* b1, const void* const* b3, void* const* saved,
+                        void* const* H, void* ws, cudaStream_t st) {
   if (pl->T == 0) return TPMLP_OK;
   const bool tc = pl->dtype == TPMLP_BF16;
   const bool sw = swiglu(pl);
@@ -302,19 +328,22 @@ tpmlp_status fwd_column(const tpmlp_plan* pl, const DeviceInfo& di, const void* 
     P.out0 = saved[i];
     P.out1 = sw ? saved[pl->t + i] : H[i];
     P.out2 = sw ? H[i] : nullptr;
+    P.aux0 = b1 ? b1[i] : nullptr;
+    P.aux1 = (sw && b3) ? b3[i] : nullptr;
     B.add_seg(P, X, pl->T, pl->d, W1[i], pl->d, di_, sw ? W3[i] : nullptr, pl->d);
   }
   B.end_group();
   return launch(B, TAG_FWD_COLUMN, di, pl, ws, st);
 }
 
-tpmlp_status fwd_row(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* W2, void* Y,
+tpmlp_status fwd_row(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* W2, const void* b2, void* Y,
                      void* const* H, void* ws, cudaStream_t st) {
   if (pl->T == 0) return TPMLP_OK;
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
   B.begin_group(pl->T, band_for(di.sms));
   Prob& P = B.add_prob(pl->T, pl->d, 256, MAJOR_K, MAJOR_MN, EPI_STORE, pl->d);
   P.out0 = Y;
+  P.aux0 = b2;  // added once, after the whole g-sum
   // g operator: every shard's H_i W2_i accumulates into the same tile.
   for (int i = 0; i < pl->t; ++i) B.add_seg(P, H[i], pl->T, pl->d_i[i], W2[i], pl->d_i[i], pl->d, nullptr, pl->d_i[i]);
   B.end_group();
@@ -323,12 +352,16 @@ tpmlp_status fwd_row(const tpmlp_plan* pl, const DeviceInfo& di, const void* con
 
 tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* W2,
                        const void* const* saved, const void* const* H, const void* dY, void* const* dact,
-                       void* const* dW2, void* ws, cudaStream_t st) {
+                       void* const* dW2, void* db2, void* ws, cudaStream_t st) {
   const bool sw = swiglu(pl);
   if (pl->T == 0) {
     const size_t es = pl->dtype == TPMLP_BF16 ? 2 : 4;
     for (int i = 0; i < pl->t; ++i) {
       cudaError_t e = cudaMemsetAsync(dW2[i], 0, static_cast<size_t>(pl->d_i[i] * pl->d) * es, st);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (db2) {
+      cudaError_t e = cudaMemsetAsync(db2, 0, static_cast<size_t>(pl->d) * es, st);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     return TPMLP_OK;
@@ -356,19 +389,28 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
     B.add_seg(P, dY, pl->T, pl->d, W2[i], di_, pl->d, nullptr, pl->d);
   }
   B.end_group();
-  return launch(B, TAG_BWD_DGRAD, di, pl, ws, st);
+  TPMLP_TRY(launch(B, TAG_BWD_DGRAD, di, pl, ws, st));
+  if (db2) {  // g backward is the identity: b2's gradient is that of Y
+    ColsumBuilder C(pl->dtype == TPMLP_BF16);
+    C.add(dY, db2, pl->T, pl->d);
+    TPMLP_TRY(launch_colsums(C, pl, st));
+  }
+  return TPMLP_OK;
 }
 
 tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X, const void* const* W1,
                       const void* const* W3, const void* const* dact, void* dX, void* const* dW1,
-                      void* const* dW3, void* ws, cudaStream_t st) {
+                      void* const* dW3, void* const* db1, void* const* db3, void* ws, cudaStream_t st) {
   const bool sw = swiglu(pl);
   if (pl->T == 0) {
     const size_t es = pl->dtype == TPMLP_BF16 ? 2 : 4;
     for (int i = 0; i < pl->t; ++i) {
       const size_t n = static_cast<size_t>(pl->d * pl->d_i[i]) * es;
+      const size_t nb = static_cast<size_t>(pl->d_i[i]) * es;
       cudaError_t e = cudaMemsetAsync(dW1[i], 0, n, st);
       if (e == cudaSuccess && sw) e = cudaMemsetAsync(dW3[i], 0, n, st);
+      if (e == cudaSuccess && db1) e = cudaMemsetAsync(db1[i], 0, nb, st);
+      if (e == cudaSuccess && sw && db3) e = cudaMemsetAsync(db3[i], 0, nb, st);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     return TPMLP_OK;
@@ -402,7 +444,16 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
     for (int i = 0; i < pl->t; ++i)
       B.add_seg(P, dact[pl->t + i], pl->T, pl->d_i[i], W3[i], pl->d, pl->d_i[i], nullptr, pl->d_i[i]);
   B.end_group();
-  return launch(B, TAG_BWD_FSUM, di, pl, ws, st);
+  TPMLP_TRY(launch(B, TAG_BWD_FSUM, di, pl, ws, st));
+  if (db1 || (sw && db3)) {
+    ColsumBuilder C(pl->dtype == TPMLP_BF16);
+    for (int i = 0; i < pl->t; ++i) {
+      if (db1) C.add(dact[i], db1[i], pl->T, pl->d_i[i]);
+      if (sw && db3) C.add(dact[pl->t + i], db3[i], pl->T, pl->d_i[i]);
+    }
+    TPMLP_TRY(launch_colsums(C, pl, st));
+  }
+  return TPMLP_OK;
 }
 
 }  // namespace
@@ -509,9 +560,14 @@ tpmlp_status tpmlp_plan_set_stall_injection(tpmlp_plan* plan, int enable) {
 
 size_t tpmlp_workspace_size(const tpmlp_plan* plan) { return plan ? 256 : 0; }
 
+// Optional bias arrays: NULL, or t pointers each non-NULL and 16-byte aligned.
+tpmlp_status check_bias(const char* name, const void* const* b, int t) {
+  return b ? check_array(name, b, t, false) : TPMLP_OK;
+}
+
 tpmlp_status tpmlp_forward_column(const tpmlp_plan* plan, const void* X, const void* const* W1,
-                                  const void* const* W3, void* const* saved, void* const* H, void* workspace,
-                                  tpmlp_stream_t stream) {
+                                  const void* const* W3, const void* const* b1, const void* const* b3,
+                                  void* const* saved, void* const* H, void* workspace, tpmlp_stream_t stream) {
   g_last_launches = 0;
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
@@ -521,11 +577,14 @@ tpmlp_status tpmlp_forward_column(const tpmlp_plan* plan, const void* X, const v
   if (swiglu(plan)) TPMLP_TRY(check_array("W3", W3, plan->t, false));
   TPMLP_TRY(check_array("saved", saved, nsaved(plan), tz));
   TPMLP_TRY(check_array("H", H, plan->t, tz));
-  return fwd_column(plan, di, X, W1, W3, saved, H, workspace, reinterpret_cast<cudaStream_t>(stream));
+  TPMLP_TRY(check_bias("b1", b1, plan->t));
+  if (swiglu(plan)) TPMLP_TRY(check_bias("b3", b3, plan->t));
+  return fwd_column(plan, di, X, W1, W3, b1, swiglu(plan) ? b3 : nullptr, saved, H, workspace,
+                    reinterpret_cast<cudaStream_t>(stream));
 }
 
-tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* const* W2, void* const* H, void* Y,
-                               void* workspace, tpmlp_stream_t stream) {
+tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* const* W2, const void* b2, void* const* H,
+                               void* Y, void* workspace, tpmlp_stream_t stream) {
   g_last_launches = 0;
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
@@ -533,7 +592,8 @@ tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* const* W2, vo
   TPMLP_TRY(check_array("W2", W2, plan->t, false));
   TPMLP_TRY(check_array("H", H, plan->t, tz));
   TPMLP_TRY(check_ptr("Y", Y, tz));
-  return fwd_row(plan, di, W2, Y, H, workspace, reinterpret_cast<cudaStream_t>(stream));
+  TPMLP_TRY(check_ptr("b2", b2, true));
+  return fwd_row(plan, di, W2, b2, Y, H, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tpmlp_status tpmlp_forward_row_noalloc(const tpmlp_plan* plan, const void* const* W2, void* const* H, void* Y,
@@ -557,7 +617,7 @@ tpmlp_status tpmlp_forward_row_noalloc(const tpmlp_plan* plan, const void* const
   // The status word must start at zero; the array keeps the last call's contents.
   cudaError_t e = cudaMemsetAsync(scratch, 0, need, st);
   if (e != cudaSuccess) return cuda_fail(e);
-  TPMLP_TRY(fwd_row(plan, di, W2, Y, H, scratch, st));
+  TPMLP_TRY(fwd_row(plan, di, W2, nullptr, Y, H, scratch, st));
   int32_t word = 0;
   e = cudaMemcpyAsync(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -567,8 +627,8 @@ tpmlp_status tpmlp_forward_row_noalloc(const tpmlp_plan* plan, const void* const
 }
 
 tpmlp_status tpmlp_forward(const tpmlp_plan* plan, const void* X, const void* const* W1, const void* const* W3,
-                           const void* const* W2, void* Y, void* const* saved, void* const* H, void* workspace,
-                           tpmlp_stream_t stream) {
+                           const void* const* W2, const void* const* b1, const void* const* b3, const void* b2,
+                           void* Y, void* const* saved, void* const* H, void* workspace, tpmlp_stream_t stream) {
   g_last_launches = 0;
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
@@ -579,14 +639,17 @@ tpmlp_status tpmlp_forward(const tpmlp_plan* plan, const void* X, const void* co
   TPMLP_TRY(check_array("W2", W2, plan->t, false));
   TPMLP_TRY(check_array("saved", saved, nsaved(plan), tz));
   TPMLP_TRY(check_array("H", H, plan->t, tz));
+  TPMLP_TRY(check_bias("b1", b1, plan->t));
+  if (swiglu(plan)) TPMLP_TRY(check_bias("b3", b3, plan->t));
+  TPMLP_TRY(check_ptr("b2", b2, true));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  TPMLP_TRY(fwd_column(plan, di, X, W1, W3, saved, H, workspace, st));
-  return fwd_row(plan, di, W2, Y, H, workspace, st);
+  TPMLP_TRY(fwd_column(plan, di, X, W1, W3, b1, swiglu(plan) ? b3 : nullptr, saved, H, workspace, st));
+  return fwd_row(plan, di, W2, b2, Y, H, workspace, st);
 }
 
 tpmlp_status tpmlp_backward_dgrad(const tpmlp_plan* plan, const void* const* W2, const void* const* saved,
                                   const void* const* H, const void* dY, void* const* dact, void* const* dW2,
-                                  void* workspace, tpmlp_stream_t stream) {
+                                  void* db2, void* workspace, tpmlp_stream_t stream) {
   g_last_launches = 0;
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
@@ -597,12 +660,14 @@ tpmlp_status tpmlp_backward_dgrad(const tpmlp_plan* plan, const void* const* W2,
   TPMLP_TRY(check_ptr("dY", dY, tz));
   TPMLP_TRY(check_array("dact", dact, nsaved(plan), tz));
   TPMLP_TRY(check_array("dW2", dW2, plan->t, false));
-  return bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, workspace, reinterpret_cast<cudaStream_t>(stream));
+  TPMLP_TRY(check_ptr("db2", db2, true));
+  return bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, db2, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tpmlp_status tpmlp_backward_fsum(const tpmlp_plan* plan, const void* X, const void* const* W1,
                                  const void* const* W3, const void* const* dact, void* dX, void* const* dW1,
-                                 void* const* dW3, void* workspace, tpmlp_stream_t stream) {
+                                 void* const* dW3, void* const* db1, void* const* db3, void* workspace,
+                                 tpmlp_stream_t stream) {
   g_last_launches = 0;
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
@@ -615,13 +680,16 @@ tpmlp_status tpmlp_backward_fsum(const tpmlp_plan* plan, const void* X, const vo
   }
   TPMLP_TRY(check_array("dact", dact, nsaved(plan), tz));
   TPMLP_TRY(check_array("dW1", dW1, plan->t, false));
-  return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, workspace, reinterpret_cast<cudaStream_t>(stream));
+  TPMLP_TRY(check_bias("db1", db1, plan->t));
+  if (swiglu(plan)) TPMLP_TRY(check_bias("db3", db3, plan->t));
+  return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, db1, swiglu(plan) ? db3 : nullptr, workspace,
+                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 tpmlp_status tpmlp_backward(const tpmlp_plan* plan, const void* X, const void* const* W1, const void* const* W3,
                             const void* const* W2, const void* const* saved, const void* const* H, const void* dY,
                             void* const* dact, void* dX, void* const* dW1, void* const* dW3, void* const* dW2,
-                            void* workspace, tpmlp_stream_t stream) {
+                            void* const* db1, void* const* db3, void* db2, void* workspace, tpmlp_stream_t stream) {
   g_last_launches = 0;
   DeviceInfo di;
   TPMLP_TRY(common_checks(plan, workspace, &di));
@@ -638,9 +706,12 @@ tpmlp_status tpmlp_backward(const tpmlp_plan* plan, const void* X, const void* c
   TPMLP_TRY(check_array("dact", dact, nsaved(plan), tz));
   TPMLP_TRY(check_array("dW1", dW1, plan->t, false));
   TPMLP_TRY(check_array("dW2", dW2, plan->t, false));
+  TPMLP_TRY(check_bias("db1", db1, plan->t));
+  if (swiglu(plan)) TPMLP_TRY(check_bias("db3", db3, plan->t));
+  TPMLP_TRY(check_ptr("db2", db2, true));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  TPMLP_TRY(bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, workspace, st));
-  return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, workspace, st);
+  TPMLP_TRY(bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, db2, workspace, st));
+  return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, db1, swiglu(plan) ? db3 : nullptr, workspace, st);
 }
 
 tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpmlp_stream_t stream) {
@@ -675,7 +746,7 @@ const char* tpmlp_status_string(tpmlp_status s) {
 
 int tpmlp_last_cuda_error(void) { return g_last_cuda_error; }
 const char* tpmlp_last_error(void) { return g_last_error; }
-int tpmlp_version(void) { return 100; }
+int tpmlp_version(void) { return 101; }
 int tpmlp_last_launch_count(void) { return g_last_launches; }
 
 }  // extern "C"

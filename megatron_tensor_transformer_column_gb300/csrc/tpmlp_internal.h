@@ -32,12 +32,13 @@ constexpr int kMaxProbs = 2 * kMaxShards + 2;
 constexpr int kMaxGroups = kMaxShards + 2;
 constexpr int kMaxSegs = 4 * kMaxShards + 2;
 
-// Fused epilogues.  acc is the fp32 accumulator tile.
+// Fused epilogues.  acc is the fp32 accumulator tile; bias vectors are
+// optional (null = none) and indexed by output column.
 enum EpiKind : int32_t {
-  EPI_STORE = 0,       // out0 = acc
-  EPI_GELU_FWD = 1,    // out0 = A = acc (pre-activation, kept for backward), out1 = H = GeLU(acc)
-  EPI_SWIGLU_FWD = 2,  // two accumulators G (B = W1_i) and U (B2 = W3_i):
-                       // out0 = G, out1 = U, out2 = H = U * Swish(G)
+  EPI_STORE = 0,       // out0 = acc (+ aux0[n]: b2, added once after the g-sum)
+  EPI_GELU_FWD = 1,    // A = acc (+ aux0[n]: b1_i); out0 = A (kept for backward), out1 = H = GeLU(A)
+  EPI_SWIGLU_FWD = 2,  // two accumulators (B = W1_i, B2 = W3_i): G = acc_G (+ aux0[n]: b1_i),
+                       // U = acc_U (+ aux1[n]: b3_i); out0 = G, out1 = U, out2 = H = U * Swish(G)
   EPI_GELU_BWD = 3,    // acc = dH; aux0 = A: out0 = dA = dH * GeLU'(A)
   EPI_SWIGLU_BWD = 4,  // acc = dH; aux0 = G, aux1 = U:
                        // out0 = dG = dH * U * Swish'(G), out1 = dU = dH * Swish(G)
@@ -99,6 +100,23 @@ struct GemmParams {
   uint64_t timeout_ns;      // bound on every wait inside the kernel
   int32_t stall_injection;  // test hook: producers load nothing, so the waits run out
 };
+
+// Column sums over tokens (bias gradients): dst[c] = sum_r src[r][c].
+constexpr int kMaxColsumJobs = 2 * kMaxShards + 1;
+struct ColsumJob {
+  const void* src;  // [rows x cols] row-major, the plan's dtype
+  void* dst;        // [cols], the plan's dtype
+  int64_t rows;
+  int32_t cols;
+  int32_t strip_begin;  // first CTA of this job
+};
+struct ColsumParams {
+  ColsumJob jobs[kMaxColsumJobs];
+  int32_t num_jobs;
+  int32_t total_strips;
+};
+int colsum_strip_cols(bool bf16);
+cudaError_t launch_colsum(const ColsumParams& p, bool bf16, cudaStream_t stream);
 
 // Kernel parameters live in the 32 KB parameter space (__grid_constant__).
 static_assert(sizeof(GemmParams) <= 32000, "kernel parameter block too large");

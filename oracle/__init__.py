@@ -79,6 +79,8 @@ def _bind(lib):
     lib.oracle_rows.restype = ci
     lib.oracle_wgrad_units.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, i64, dp, dp, dp, dp, dp, dp]
     lib.oracle_wgrad_units.restype = ci
+    lib.oracle_db2.argtypes = [i64, i64, dp, dp]
+    lib.oracle_db2.restype = ci
     lib.oracle_act_value.argtypes = [ci, ctypes.c_double]
     lib.oracle_act_value.restype = ctypes.c_double
     lib.oracle_act_grad.argtypes = [ci, ctypes.c_double]
@@ -237,6 +239,13 @@ class COracle:
                                _ptr(dY), len(r), _ptr(r), _ptr(Yr), _ptr(dXr)), "oracle_rows")
         return Yr, dXr
 
+    def db2(self, dY):
+        """Column sums of dY over tokens (gradient of the bias added after the g-sum)."""
+        dY = _f64(dY)
+        out = np.empty(dY.shape[1])
+        _check(self.lib.oracle_db2(dY.shape[0], dY.shape[1], _ptr(dY), _ptr(out)), "oracle_db2")
+        return out
+
     def wgrad_units(self, X, W1, W2, dY, units, act="gelu", W3=None, b1=None, b3=None, with_bias_grads=False):
         """dW1[:, j], dW3[:, j], dW2[j, :] for the listed hidden units j.
 
@@ -305,6 +314,10 @@ def rows(*args, **kwargs):
 
 def wgrad_units(*args, **kwargs):
     return default().wgrad_units(*args, **kwargs)
+
+
+def db2(*args, **kwargs):
+    return default().db2(*args, **kwargs)
 
 
 num_threads.__doc__ = "OpenMP threads the C oracle uses."

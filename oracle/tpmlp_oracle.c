@@ -468,6 +468,14 @@ int oracle_wgrad_units(int64_t T, int64_t d, int64_t dff, int act, const double*
   return err ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
 
+/* db2 = sum over the T tokens of dY[r, :] -- the gradient of the bias added
+ * once after the g-sum (g backward is the identity).  db2 is [d].           */
+int oracle_db2(int64_t T, int64_t d, const double* dY, double* db2) {
+  if (T < 0 || d < 1 || !dY || !db2) return ORACLE_ERR_ARG;
+  col_sums(T, d, dY, db2);
+  return ORACLE_OK;
+}
+
 /* Scalar access for the closed-form pins (value of the activation, its
  * derivative, for act in {GeLU, Swish-as-SwiGLU-gate, identity, ReLU}).      */
 double oracle_act_value(int act, double a) { return act == ORACLE_ACT_SWIGLU ? swish(a) : act_value(act, a); }

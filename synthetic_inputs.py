@@ -145,3 +145,16 @@ def small_int_inputs(T: int, d: int, d_i, act: str, seed: int = 7, lo: int = -3,
     if W3 is not None:
         inp.W3_i = [W3[:, a:b].contiguous() for a, b in shard_slices(d_i)]
     return inp
+
+
+def make_biases(d: int, d_i, act: str = "gelu", dtype: str = "bf16", seed: int = BASE_SEED, std: float = 0.5):
+    """Optional biases: b1 (and b3 for SwiGLU) [d_ff] cut into shards, b2 [d];
+    N(0, std), sub-seeds +5 b1, +6 b3, +7 b2, rounded once to the dtype."""
+    td = torch_dtype(dtype)
+    dff = int(sum(d_i))
+    b1 = _randn((dff,), seed + 5, std).to(td)
+    b3 = _randn((dff,), seed + 6, std).to(td) if act == "swiglu" else None
+    b2 = _randn((d,), seed + 7, std).to(td)
+    sl = shard_slices(d_i)
+    return {"b1": b1, "b3": b3, "b2": b2, "b1_i": [b1[lo:hi].contiguous() for lo, hi in sl],
+            "b3_i": [b3[lo:hi].contiguous() for lo, hi in sl] if b3 is not None else None}

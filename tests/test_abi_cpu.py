@@ -47,7 +47,7 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert tp.tpmlp_version() == 100
+    assert tp.tpmlp_version() == 101
     for code, name in tp.STATUS.items():
         assert tp.tpmlp_status_string(code) == name
     assert tp.tpmlp_status_string(99) == "TPMLP_ERR_UNKNOWN"
@@ -83,7 +83,7 @@ def test_null_arguments_rejected(lib):
     h = ctypes.c_void_p()
     assert lib.tpmlp_plan_create(None, ctypes.byref(h)) == 1
     assert lib.tpmlp_workspace_size(None) == 0
-    assert lib.tpmlp_forward(None, None, None, None, None, None, None, None, None, None) == 1
+    assert lib.tpmlp_forward(None, None, None, None, None, None, None, None, None, None, None, None, None) == 1
     lib.tpmlp_plan_destroy(None)  # no-op
 
 
@@ -93,5 +93,5 @@ def test_no_cpu_fallback_without_gpu(lib):
     p = tp.Plan(16, 64, [64], "gelu", "bf16")
     fake = 1 << 20  # never dereferenced: the device query fails first
     with pytest.raises(tp.TpmlpError) as e:
-        tp.tpmlp_forward(p, fake, [fake], None, [fake], fake, [fake], [fake], fake, stream=0)
+        tp.tpmlp_forward(p, fake, [fake], None, [fake], None, None, None, fake, [fake], [fake], fake, stream=0)
     assert e.value.status in (4, 5)

@@ -72,21 +72,21 @@ def test_argument_errors_with_device(gpu_lib):
     # misaligned X (offset by one element = 2 bytes)
     raw = torch.zeros(64 * 64 + 8, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(tp.TpmlpError) as e:
-        tp.tpmlp_forward(mlp.plan, raw.data_ptr() + 2, W1, None, W2, Y, saved, H, mlp.workspace)
+        tp.tpmlp_forward(mlp.plan, raw.data_ptr() + 2, W1, None, W2, None, None, None, Y, saved, H, mlp.workspace)
     assert e.value.status == 3
     # null weight
     with pytest.raises(tp.TpmlpError) as e:
-        tp.tpmlp_forward(mlp.plan, X, [0], None, W2, Y, saved, H, mlp.workspace)
+        tp.tpmlp_forward(mlp.plan, X, [0], None, W2, None, None, None, Y, saved, H, mlp.workspace)
     assert e.value.status == 1
     # null workspace
     with pytest.raises(tp.TpmlpError) as e:
-        tp.tpmlp_forward(mlp.plan, X, W1, None, W2, Y, saved, H, 0)
+        tp.tpmlp_forward(mlp.plan, X, W1, None, W2, None, None, None, Y, saved, H, 0)
     assert e.value.status == 1
     # SwiGLU plan without W3
     ms = tp.ShardedMLP(64, 64, (64,), "swiglu", "bf16")
     Ys, saveds, Hs = ms.alloc_forward()
     with pytest.raises(tp.TpmlpError) as e:
-        tp.tpmlp_forward(ms.plan, X, W1, None, W2, Ys, saveds, Hs, ms.workspace)
+        tp.tpmlp_forward(ms.plan, X, W1, None, W2, None, None, None, Ys, saveds, Hs, ms.workspace)
     assert e.value.status == 1
 
 
@@ -101,11 +101,11 @@ def test_phase_entry_points_match_fused_calls(gpu_lib):
     W1 = [inp.W1[:, a:b].contiguous().cuda() for a, b in sl]
     W2 = [inp.W2[a:b].contiguous().cuda() for a, b in sl]
     Y, saved, H = mlp.alloc_forward()
-    tp.tpmlp_forward_column(mlp.plan, X, W1, None, saved, H, mlp.workspace)
-    tp.tpmlp_forward_row(mlp.plan, W2, H, Y, mlp.workspace)
+    tp.tpmlp_forward_column(mlp.plan, X, W1, None, None, None, saved, H, mlp.workspace)
+    tp.tpmlp_forward_row(mlp.plan, W2, None, H, Y, mlp.workspace)
     dact, dX, dW1, dW3, dW2 = mlp.alloc_backward()
-    tp.tpmlp_backward_dgrad(mlp.plan, W2, saved, H, dY, dact, dW2, mlp.workspace)
-    tp.tpmlp_backward_fsum(mlp.plan, X, W1, None, dact, dX, dW1, None, mlp.workspace)
+    tp.tpmlp_backward_dgrad(mlp.plan, W2, saved, H, dY, dact, dW2, None, mlp.workspace)
+    tp.tpmlp_backward_fsum(mlp.plan, X, W1, None, dact, dX, dW1, None, None, None, mlp.workspace)
     torch.cuda.synchronize()
     assert torch.equal(Y, ref["Y"]) and torch.equal(dX, ref["dX"])
     for x, y in zip(dW1 + dW2, ref["dW1"] + ref["dW2"]):

@@ -26,7 +26,7 @@ def test_injected_stall_reports_timeout_and_context_survives(gpu_lib):
     tp.tpmlp_plan_set_stall_injection(mlp.plan, True)
     Y, saved, H = mlp.alloc_forward()
     t0 = time.time()
-    tp.tpmlp_forward(mlp.plan, X, W1, None, W2, Y, saved, H, mlp.workspace)  # asynchronous: returns OK
+    tp.tpmlp_forward(mlp.plan, X, W1, None, W2, None, None, None, Y, saved, H, mlp.workspace)  # asynchronous
     with pytest.raises(tp.TpmlpError) as e:
         mlp.check()
     assert e.value.status == 6  # TPMLP_ERR_DEVICE_TIMEOUT

@@ -479,6 +479,7 @@ def test_bias_sampled_rows_and_units(act):
     np.testing.assert_allclose(g1, b["db1"][u], rtol=0, atol=1e-11)
     if act == "swiglu":
         np.testing.assert_allclose(g3, b["db3"][u], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(oracle.db2(dY), b["db2"], rtol=0, atol=1e-12)
 
 
 def test_planted_bias_per_shard_is_caught(tmp_path):

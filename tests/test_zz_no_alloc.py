@@ -29,8 +29,8 @@ def test_forward_row_noalloc_matches_workspace_entry_point(gpu_lib, act):
     W2 = [w.cuda() for w in inp.W2_i]
     W3 = [w.cuda() for w in inp.W3_i] if act == "swiglu" else None
     Y_ref, saved, H = mlp.alloc_forward()
-    tp.tpmlp_forward_column(mlp.plan, X, W1, W3, saved, H, mlp.workspace)
-    tp.tpmlp_forward_row(mlp.plan, W2, H, Y_ref, mlp.workspace)
+    tp.tpmlp_forward_column(mlp.plan, X, W1, W3, None, None, saved, H, mlp.workspace)
+    tp.tpmlp_forward_row(mlp.plan, W2, None, H, Y_ref, mlp.workspace)
     torch.cuda.synchronize()
     mlp.check()
     ref = to_np(Y_ref)
