@@ -293,6 +293,21 @@ def run_ours(args, w: si.Workload):
         db1, db3, db2 = mlp.alloc_bias_grads()
 
     def step(ev=None):
+        if args.recompute:  # backward with H recomputed from the pre-activations (H treated as scratch)
+            if ev:
+                ev[0].record(stream)
+            tp.tpmlp_forward_column(plan, X, W1, W3, b1, b3, saved, H, wsp, stream)
+            if ev:
+                ev[1].record(stream)
+            tp.tpmlp_forward_row(plan, W2, b2, H, Y, wsp, stream)
+            if ev:
+                ev[2].record(stream)
+                ev[3].record(stream)
+            tp.tpmlp_backward_recompute(plan, X, W1, W3, W2, saved, H, dY, dact, dX, dW1, dW3, dW2, db1, db3, db2,
+                                        wsp, stream)
+            if ev:
+                ev[4].record(stream)
+            return
         if ev:
             ev[0].record(stream)
         tp.tpmlp_forward_column(plan, X, W1, W3, b1, b3, saved, H, wsp, stream)
@@ -333,6 +348,8 @@ def run_ours(args, w: si.Workload):
     elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
     ms_per_step = elapsed_ms / args.steps
     names = ["fwd_column", "fwd_row", "bwd_dgrad", "bwd_fsum"]
+    if args.recompute:
+        names = ["fwd_column", "fwd_row", "bwd_none", "bwd_recompute"]
     per_phase = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
                  for i, n in enumerate(names)}
     total_flops = flops_fwd_bwd(w) * ws
@@ -343,12 +360,17 @@ def run_ours(args, w: si.Workload):
 
     peaks, peak_src = load_peaks()
     pf = phase_flops(w)
+    if args.recompute:
+        pf = {"fwd_column": pf["fwd_column"], "fwd_row": pf["fwd_row"], "bwd_none": 0,
+              "bwd_recompute": pf["bwd_dgrad"] + pf["bwd_fsum"]}
+        per_phase.pop("bwd_none", None)
     dom = max(per_phase, key=per_phase.get)
     achieved = pf[dom] / (per_phase[dom] / 1e3) / 1e12
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": achieved / peak_sus, "traffic": None if args.bias else measured_traffic(dom, w.name),
+                "frac": achieved / peak_sus,
+                "traffic": None if (args.bias or args.recompute) else measured_traffic(dom, w.name),
                 "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); "
                              f"frac of {peak_src} burst {peak_burst}: {achieved / peak_burst:.3f}"}
     if rank != 0:
@@ -362,7 +384,9 @@ def run_ours(args, w: si.Workload):
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) X/dY, N(0,0.02) W, rounded once to bf16)",
         "config": workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)",
                                       **({"bias": "b1/b3 before the activation, b2 after the g-sum, with db"}
-                                         if args.bias else {})}),
+                                         if args.bias else {}),
+                                      **({"recompute": "backward recomputes H from the saved pre-activations"}
+                                         if args.recompute else {})}),
         "pct_of_peak": {"sustained": value / ws / peak_sus, "burst": value / ws / peak_burst, "source": peak_src},
         "tokens_per_s": w.T * ws * args.steps / (elapsed_ms / 1e3),
         "phase_ms": per_phase,
@@ -442,6 +466,7 @@ def main(argv=None):
     ap.add_argument("--oracle-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bias", action="store_true", help="include the optional biases and their gradients")
+    ap.add_argument("--recompute", action="store_true", help="backward recomputes H instead of reading it")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     w = si.WORKLOADS[args.workload]

@@ -139,6 +139,26 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_plan* plan, const void* X, con
                                       void* const* dW1, void* const* dW3, void* const* dW2, void* const* db1,
                                       void* const* db3, void* db2, void* workspace, tpmlp_stream_t stream);
 
+/* Backward with recomputation: the same arguments and results as
+ * tpmlp_backward, except that H is not read: the contents of H[i] may have
+ * been discarded after tpmlp_forward (only X and the pre-activations in
+ * saved must survive), and H[i] is used as scratch that ends up holding the
+ * recomputed H_i = act(saved_i).  The first launch computes dact and writes
+ * H_i from the saved pre-activations it already reads for act' (GeLU: A_i;
+ * SwiGLU: U_i * Swish(G_i)); the second computes dX (the f-sum), dW1, dW3 and
+ * dW2 = H_i^T dY.  This trades nothing in FLOPs for not keeping H between the
+ * passes ("AI Training Network Primer" ch. 3, section 3.1, and the
+ * "Parallelism" page's GPipe post: activation recomputation saves memory by
+ * recomputing what the backward pass needs from what was kept).  Because H is
+ * recomputed from the bf16 pre-activation rather than from the fp32
+ * accumulator, dW2 may differ from tpmlp_backward's in the last bits.       */
+TPMLP_API tpmlp_status tpmlp_backward_recompute(const tpmlp_plan* plan, const void* X, const void* const* W1,
+                                                const void* const* W3, const void* const* W2,
+                                                const void* const* saved, void* const* H, const void* dY,
+                                                void* const* dact, void* dX, void* const* dW1, void* const* dW3,
+                                                void* const* dW2, void* const* db1, void* const* db3, void* db2,
+                                                void* workspace, tpmlp_stream_t stream);
+
 /* The two launches of tpmlp_forward, callable one at a time (same arguments
  * and layouts; each is exactly one kernel launch):
  *   tpmlp_forward_column: saved and H from X, W1 (and W3), b1 (and b3).

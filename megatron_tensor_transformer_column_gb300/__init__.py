@@ -23,7 +23,7 @@ from . import _build
 __all__ = [
     "TpmlpError", "load", "Plan", "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size",
     "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection",
-    "tpmlp_forward", "tpmlp_backward", "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad",
+    "tpmlp_forward", "tpmlp_backward", "tpmlp_backward_recompute", "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad",
     "tpmlp_backward_fsum", "tpmlp_check", "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version",
     "tpmlp_last_launch_count", "tpmlp_last_error", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
 ]
@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad", "tpmlp_backward_fsum", "tpmlp_check",
     "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version", "tpmlp_last_launch_count",
     "tpmlp_last_error", "tpmlp_forward_row_noalloc", "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection",
+    "tpmlp_backward_recompute",
 )
 
 
@@ -93,6 +94,9 @@ def load():
         lib.tpmlp_forward.restype = st
         lib.tpmlp_backward.argtypes = [vp, vp, pp, pp, pp, pp, pp, vp, pp, vp, pp, pp, pp, pp, pp, vp, vp, vp]
         lib.tpmlp_backward.restype = st
+        lib.tpmlp_backward_recompute.argtypes = [vp, vp, pp, pp, pp, pp, pp, vp, pp, vp, pp, pp, pp, pp, pp, vp, vp,
+                                                 vp]
+        lib.tpmlp_backward_recompute.restype = st
         lib.tpmlp_forward_column.argtypes = [vp, vp, pp, pp, pp, pp, pp, pp, vp, vp]
         lib.tpmlp_forward_column.restype = st
         lib.tpmlp_forward_row.argtypes = [vp, pp, vp, pp, vp, vp, vp]
@@ -219,6 +223,14 @@ def tpmlp_backward(plan, X, W1, W3, W2, saved, H, dY, dact, dX, dW1, dW3, dW2, d
                               _arr(db3), _addr(db2), _addr(workspace), _stream(stream)), "tpmlp_backward")
 
 
+def tpmlp_backward_recompute(plan, X, W1, W3, W2, saved, H, dY, dact, dX, dW1, dW3, dW2, db1, db3, db2, workspace,
+                             stream=None):
+    _ok(load().tpmlp_backward_recompute(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(W2), _arr(saved), _arr(H),
+                                        _addr(dY), _arr(dact), _addr(dX), _arr(dW1), _arr(dW3), _arr(dW2), _arr(db1),
+                                        _arr(db3), _addr(db2), _addr(workspace), _stream(stream)),
+        "tpmlp_backward_recompute")
+
+
 def tpmlp_forward_column(plan, X, W1, W3, b1, b3, saved, H, workspace, stream=None):
     _ok(load().tpmlp_forward_column(plan.handle, _addr(X), _arr(W1), _arr(W3), _arr(b1), _arr(b3), _arr(saved),
                                     _arr(H), _addr(workspace), _stream(stream)), "tpmlp_forward_column")
@@ -336,12 +348,15 @@ class ShardedMLP:
         db3 = [self._empty(w) for w in p.d_i] if self.swiglu else None
         return db1, db3, self._empty(p.d)
 
-    def backward(self, X, W1_i, W2_i, saved, H, dY, W3_i=None, out=None, stream=None, bias_grads=False):
-        """Gradients of X, the weights and, with bias_grads, the biases."""
+    def backward(self, X, W1_i, W2_i, saved, H, dY, W3_i=None, out=None, stream=None, bias_grads=False,
+                 recompute=False):
+        """Gradients of X, the weights and, with bias_grads, the biases.  With
+        recompute, H is scratch (its contents are not read) and is rewritten."""
         dact, dX, dW1, dW3, dW2 = out if out is not None else self.alloc_backward()
         db1, db3, db2 = self.alloc_bias_grads() if bias_grads else (None, None, None)
-        tpmlp_backward(self.plan, X, W1_i, W3_i, W2_i, saved, H, dY, dact, dX, dW1, dW3, dW2, db1, db3, db2,
-                       self.workspace, stream)
+        fn = tpmlp_backward_recompute if recompute else tpmlp_backward
+        fn(self.plan, X, W1_i, W3_i, W2_i, saved, H, dY, dact, dX, dW1, dW3, dW2, db1, db3, db2, self.workspace,
+           stream)
         return {"dX": dX, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dact": dact, "db1": db1, "db3": db3, "db2": db2}
 
     def check(self, stream=None):

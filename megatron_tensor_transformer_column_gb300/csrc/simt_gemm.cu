@@ -118,14 +118,19 @@ __global__ void __launch_bounds__(kThreads) tpmlp_fp32_simt_gemm(const __grid_co
         static_cast<float*>(P.out2)[o] = u * act::swish(v);
         break;
       }
-      case EPI_GELU_BWD:
-        static_cast<float*>(P.out0)[o] = v * act::gelu_grad(static_cast<const float*>(P.aux0)[o]);
+      case EPI_GELU_BWD: {
+        const float a = static_cast<const float*>(P.aux0)[o];
+        static_cast<float*>(P.out0)[o] = v * act::gelu_grad(a);
+        if (P.out1) static_cast<float*>(P.out1)[o] = act::gelu(a);  // recomputed H
         break;
+      }
       case EPI_SWIGLU_BWD: {
         float dg, du;
-        act::swiglu_grads(v, static_cast<const float*>(P.aux0)[o], static_cast<const float*>(P.aux1)[o], dg, du);
+        const float gg = static_cast<const float*>(P.aux0)[o], uu = static_cast<const float*>(P.aux1)[o];
+        act::swiglu_grads(v, gg, uu, dg, du);
         static_cast<float*>(P.out0)[o] = dg;
         static_cast<float*>(P.out1)[o] = du;
+        if (P.out2) static_cast<float*>(P.out2)[o] = uu * act::swish(gg);  // recomputed H
         break;
       }
       default:

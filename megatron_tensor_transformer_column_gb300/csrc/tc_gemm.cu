@@ -348,8 +348,19 @@ __device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int c
     case EPI_GELU_BWD: {
       float a[32];
       load_row32(P.aux0, P.ldo, row, col, nvalid, a);
+      if (P.out1) {  // recompute H = GeLU(A) for the weight gradient of W2
+        float h[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) a[j] = acc[j] * act::gelu_grad_fast(a[j]);
+        for (int j = 0; j < 32; ++j) {
+          const act::NormTerms n = act::norm_terms_fast(a[j]);
+          h[j] = a[j] * n.cdf;
+          a[j] = acc[j] * fmaf(a[j] * act::kInvSqrt2Pi, n.e, n.cdf);
+        }
+        store_row32(P.out1, P.ldo, row, col, nvalid, h);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a[j] = acc[j] * act::gelu_grad_fast(a[j]);
+      }
       store_row32(P.out0, P.ldo, row, col, nvalid, a);
       break;
     }
@@ -357,6 +368,12 @@ __device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int c
       float g[32], u[32];
       load_row32(P.aux0, P.ldo, row, col, nvalid, g);
       load_row32(P.aux1, P.ldo, row, col, nvalid, u);
+      if (P.out2) {  // recompute H = U * Swish(G) for the weight gradient of W2
+        float h[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) h[j] = u[j] * act::swish_fast(g[j]);
+        store_row32(P.out2, P.ldo, row, col, nvalid, h);
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float dg, du;

@@ -350,9 +350,11 @@ tpmlp_status fwd_row(const tpmlp_plan* pl, const DeviceInfo& di, const void* con
   return launch(B, TAG_FWD_ROW, di, pl, ws, st);
 }
 
+// With recompute, H is an output: the dgrad epilogue writes H_i = act(saved_i)
+// and dW2 moves to the f-sum launch (bwd_fsum's dW2 problems).
 tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* W2,
                        const void* const* saved, const void* const* H, const void* dY, void* const* dact,
-                       void* const* dW2, void* db2, void* ws, cudaStream_t st) {
+                       void* const* dW2, void* db2, void* ws, cudaStream_t st, bool recompute = false) {
   const bool sw = swiglu(pl);
   if (pl->T == 0) {
     const size_t es = pl->dtype == TPMLP_BF16 ? 2 : 4;
@@ -369,7 +371,7 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
   const int band = band_for(di.sms);
   // dW2_i = H_i^T dY (K = T: the long tiles go first)
-  for (int i = 0; i < pl->t; ++i) {
+  for (int i = 0; i < pl->t && !recompute; ++i) {
     const int64_t di_ = pl->d_i[i];
     B.begin_group(di_, band);
     Prob& P = B.add_prob(di_, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
@@ -385,7 +387,8 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
     P.aux0 = saved[i];
     P.aux1 = sw ? saved[pl->t + i] : nullptr;
     P.out0 = dact[i];
-    P.out1 = sw ? dact[pl->t + i] : nullptr;
+    P.out1 = sw ? dact[pl->t + i] : (recompute ? const_cast<void*>(H[i]) : nullptr);
+    P.out2 = (sw && recompute) ? const_cast<void*>(H[i]) : nullptr;
     B.add_seg(P, dY, pl->T, pl->d, W2[i], di_, pl->d, nullptr, pl->d);
   }
   B.end_group();
@@ -400,7 +403,8 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
 
 tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X, const void* const* W1,
                       const void* const* W3, const void* const* dact, void* dX, void* const* dW1,
-                      void* const* dW3, void* const* db1, void* const* db3, void* ws, cudaStream_t st) {
+                      void* const* dW3, void* const* db1, void* const* db3, void* ws, cudaStream_t st,
+                      const void* const* H_for_dW2 = nullptr, const void* dY = nullptr, void* const* dW2 = nullptr) {
   const bool sw = swiglu(pl);
   if (pl->T == 0) {
     const size_t es = pl->dtype == TPMLP_BF16 ? 2 : 4;
@@ -417,6 +421,16 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
   }
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
   const int band = band_for(di.sms);
+  if (H_for_dW2) {  // recompute mode: dW2_i = H_i^T dY from the H the dgrad launch rewrote
+    for (int i = 0; i < pl->t; ++i) {
+      const int64_t di_ = pl->d_i[i];
+      B.begin_group(di_, band);
+      Prob& P = B.add_prob(di_, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
+      P.out0 = dW2[i];
+      B.add_seg(P, H_for_dW2[i], pl->T, di_, dY, pl->T, pl->d, nullptr, pl->T);
+      B.end_group();
+    }
+  }
   // dW1_i = X^T dA_i (SwiGLU: X^T dG_i) and dW3_i = X^T dU_i (K = T)
   B.begin_group(pl->d, band);
   for (int i = 0; i < pl->t; ++i) {
@@ -712,6 +726,40 @@ tpmlp_status tpmlp_backward(const tpmlp_plan* plan, const void* X, const void* c
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   TPMLP_TRY(bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, db2, workspace, st));
   return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, db1, swiglu(plan) ? db3 : nullptr, workspace, st);
+}
+
+tpmlp_status tpmlp_backward_recompute(const tpmlp_plan* plan, const void* X, const void* const* W1,
+                                      const void* const* W3, const void* const* W2, const void* const* saved,
+                                      void* const* H, const void* dY, void* const* dact, void* dX,
+                                      void* const* dW1, void* const* dW3, void* const* dW2, void* const* db1,
+                                      void* const* db3, void* db2, void* workspace, tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_ptr("X", X, tz)); TPMLP_TRY(check_ptr("dY", dY, tz)); TPMLP_TRY(check_ptr("dX", dX, tz));
+  TPMLP_TRY(check_array("W1", W1, plan->t, false));
+  TPMLP_TRY(check_array("W2", W2, plan->t, false));
+  if (swiglu(plan)) {
+    TPMLP_TRY(check_array("W3", W3, plan->t, false));
+    TPMLP_TRY(check_array("dW3", dW3, plan->t, false));
+  }
+  TPMLP_TRY(check_array("saved", saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array("H", H, plan->t, tz));
+  TPMLP_TRY(check_array("dact", dact, nsaved(plan), tz));
+  TPMLP_TRY(check_array("dW1", dW1, plan->t, false));
+  TPMLP_TRY(check_array("dW2", dW2, plan->t, false));
+  TPMLP_TRY(check_bias("db1", db1, plan->t));
+  if (swiglu(plan)) TPMLP_TRY(check_bias("db3", db3, plan->t));
+  TPMLP_TRY(check_ptr("db2", db2, true));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (tz) {  // nothing to recompute; zero-filled gradients as in tpmlp_backward
+    TPMLP_TRY(bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, db2, workspace, st));
+    return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, db1, swiglu(plan) ? db3 : nullptr, workspace, st);
+  }
+  TPMLP_TRY(bwd_dgrad(plan, di, W2, saved, H, dY, dact, dW2, db2, workspace, st, /*recompute=*/true));
+  return bwd_fsum(plan, di, X, W1, W3, dact, dX, dW1, dW3, db1, swiglu(plan) ? db3 : nullptr, workspace, st, H,
+                  dY, dW2);
 }
 
 tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpmlp_stream_t stream) {

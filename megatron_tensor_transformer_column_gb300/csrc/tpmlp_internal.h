@@ -40,8 +40,10 @@ enum EpiKind : int32_t {
   EPI_SWIGLU_FWD = 2,  // two accumulators (B = W1_i, B2 = W3_i): G = acc_G (+ aux0[n]: b1_i),
                        // U = acc_U (+ aux1[n]: b3_i); out0 = G, out1 = U, out2 = H = U * Swish(G)
   EPI_GELU_BWD = 3,    // acc = dH; aux0 = A: out0 = dA = dH * GeLU'(A)
+                       //   (+ out1, if set: H = GeLU(A) recomputed from the saved A)
   EPI_SWIGLU_BWD = 4,  // acc = dH; aux0 = G, aux1 = U:
                        // out0 = dG = dH * U * Swish'(G), out1 = dU = dH * Swish(G)
+                       //   (+ out2, if set: H = U * Swish(G) recomputed)
 };
 
 // Operand majors.  A(m, k) is K-major when a[m][k] is contiguous in k,

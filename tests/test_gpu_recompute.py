@@ -1,0 +1,98 @@
+"""Backward with recomputation (tpmlp_backward_recompute): H is not read;
+the dgrad launch rewrites H_i from the saved pre-activations and the second
+launch takes dW2 from it.  H is filled with NaN before the backward, so any
+read of the forward's H would poison the gradients."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic_inputs as si
+from gpu_helpers import cat_cols, cat_rows, rel_err, to_np, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _fwd(tp, inp, act, dtype, bias=None):
+    T, d = inp.X.shape
+    mlp = tp.ShardedMLP(T, d, inp.d_i, act, dtype)
+    cu = lambda xs: [x.cuda() for x in xs] if xs is not None else None
+    X, dY = inp.X.cuda(), inp.dY.cuda()
+    W1, W2, W3 = cu(inp.W1_i), cu(inp.W2_i), cu(inp.W3_i)
+    kw = {}
+    if bias is not None:
+        kw = dict(b1_i=cu(bias["b1_i"]), b3_i=cu(bias["b3_i"]), b2=bias["b2"].cuda())
+    Y, saved, H = mlp.forward(X, W1, W2, W3, **kw)
+    return mlp, X, dY, W1, W2, W3, Y, saved, H
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_recompute_matches_oracle(gpu_lib, act, dtype, with_bias):
+    tp = gpu_lib
+    T, d, d_i = (333, 200, (8, 96, 264, 152)) if dtype == "bf16" else (45, 36, (20, 44))
+    inp = si.make_inputs(T, d, d_i, act, dtype, seed=17)
+    bias = si.make_biases(d, d_i, act, dtype, seed=17) if with_bias else None
+    mlp, X, dY, W1, W2, W3, Y, saved, H = _fwd(tp, inp, act, dtype, bias)
+    for h in H:
+        h.fill_(float("nan"))
+    g = mlp.backward(X, W1, W2, saved, H, dY, W3, bias_grads=with_bias, recompute=True)
+    torch.cuda.synchronize()
+    mlp.check()
+    kw = dict(act=act, W3=inp.W3)
+    if with_bias:
+        kw.update(b1=bias["b1"], b3=bias["b3"], b2=bias["b2"])
+    f = oracle.forward(inp.X, inp.W1, inp.W2, **kw)
+    b = oracle.backward(inp.X, inp.W1, inp.W2, inp.dY, **kw)
+    errs = {"H": rel_err(cat_cols(H), f["H"]), "dX": rel_err(to_np(g["dX"]), b["dX"]),
+            "dW1": rel_err(cat_cols(g["dW1"]), b["dW1"]), "dW2": rel_err(cat_rows(g["dW2"]), b["dW2"])}
+    if act == "swiglu":
+        errs["dW3"] = rel_err(cat_cols(g["dW3"]), b["dW3"])
+    if with_bias:
+        errs["db1"] = rel_err(np.concatenate([to_np(x) for x in g["db1"]]), b["db1"])
+        errs["db2"] = rel_err(to_np(g["db2"]), b["db2"])
+    tol = tol_for(dtype)
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"over tolerance {tol}: {bad} (all {errs})"
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_recompute_same_activation_gradients(gpu_lib, act):
+    """dact, dX and dW1 (dW3) come from identical arithmetic in both modes."""
+    tp = gpu_lib
+    inp = si.make_inputs(1024, 384, (512, 384, 640, 256), act, "bf16", seed=23)
+    mlp, X, dY, W1, W2, W3, Y, saved, H = _fwd(tp, inp, act, "bf16")
+    ref = mlp.backward(X, W1, W2, saved, H, dY, W3)
+    H2 = [torch.full_like(h, float("nan")) for h in H]
+    rec = mlp.backward(X, W1, W2, saved, H2, dY, W3, recompute=True)
+    torch.cuda.synchronize()
+    assert torch.equal(ref["dX"], rec["dX"])
+    for k in ("dact", "dW1") + (("dW3",) if act == "swiglu" else ()):
+        for x, y in zip(ref[k], rec[k]):
+            assert torch.equal(x, y), k
+    for x, y in zip(ref["dW2"], rec["dW2"]):
+        assert rel_err(to_np(y), to_np(x)) <= 1e-2
+
+
+@pytest.mark.parametrize("name", ["C4", "C5"])
+def test_recompute_workload_sampled(gpu_lib, name):
+    w = si.WORKLOADS[name]
+    inp = si.make_workload_inputs(w)
+    mlp, X, dY, W1, W2, W3, Y, saved, H = _fwd(gpu_lib, inp, w.act, w.dtype)
+    for h in H:
+        h.fill_(float("nan"))
+    g = mlp.backward(X, W1, W2, saved, H, dY, W3, recompute=True)
+    torch.cuda.synchronize()
+    mlp.check()
+    rng = np.random.default_rng(9)
+    rows = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, 12, replace=False)]))
+    units = np.unique(np.concatenate([[0, w.dff - 1], rng.choice(w.dff, 12, replace=False)]))
+    Yr, dXr = oracle.rows(inp.X, inp.W1, inp.W2, inp.dY, rows, act=w.act, W3=inp.W3)
+    c1, c3, c2 = oracle.wgrad_units(inp.X, inp.W1, inp.W2, inp.dY, units, act=w.act, W3=inp.W3)
+    errs = {"dX": rel_err(to_np(g["dX"])[rows], dXr), "dW1": rel_err(cat_cols(g["dW1"])[:, units].T, c1),
+            "dW2": rel_err(cat_rows(g["dW2"])[units], c2)}
+    if w.act == "swiglu":
+        errs["dW3"] = rel_err(cat_cols(g["dW3"])[:, units].T, c3)
+    bad = {k: v for k, v in errs.items() if not v <= 2e-2}
+    assert not bad, f"{w.name}: {bad} (all {errs})"
