@@ -57,3 +57,15 @@ def backward(X, W1, W2, dY, act="gelu", W3=None, b1=None, b3=None, b2=None):
         dA = dH * (ndtr(A) + A * _phi(A))
         out.update(dW1=X.T @ dA, dW3=None, dX=dA @ W1.T, dA=dA, dU=None, db1=dA.sum(axis=0), db3=None)
     return out
+
+
+def attn_forward(X, WQ, WK, WV, O, WO):
+    X, WQ, WK, WV, O, WO = (np.asarray(m, dtype=np.float64) for m in (X, WQ, WK, WV, O, WO))
+    return {"Q": X @ WQ, "K": X @ WK, "V": X @ WV, "Z": O @ WO}
+
+
+def attn_backward(X, WQ, WK, WV, O, WO, dZ, dQ, dK, dV):
+    X, WQ, WK, WV, O, WO, dZ, dQ, dK, dV = (np.asarray(m, dtype=np.float64)
+                                            for m in (X, WQ, WK, WV, O, WO, dZ, dQ, dK, dV))
+    return {"dO": dZ @ WO.T, "dWO": O.T @ dZ, "dX": dQ @ WQ.T + dK @ WK.T + dV @ WV.T, "dWQ": X.T @ dQ,
+            "dWK": X.T @ dK, "dWV": X.T @ dV}

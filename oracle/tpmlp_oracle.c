@@ -41,6 +41,11 @@
  * Their gradients are column sums over tokens: db1 = sum_r dA[r, :],
  * db3 = sum_r dU[r, :], db2 = sum_r dY[r, :].
  *
+ * The attention block's two projections (QKV, column-split by heads, and the
+ * output projection, row-split with the g-sum) have their own functions
+ * below; the attention core between them is a different operation and is an
+ * input here (O, and dQ/dK/dV in the backward).
+ *
  * Two extra activations, identity and ReLU, are test hooks: they keep
  * small-integer inputs integral so sharded and unsharded results can be
  * compared exactly.
@@ -466,6 +471,86 @@ int oracle_wgrad_units(int64_t T, int64_t d, int64_t dff, int act, const double*
     free(h);
   }
   return err ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* ---- tensor-parallel attention projections -------------------------------
+ * The attention core (softmax) is a different operation and is not part of
+ * this library; O (the attention output per token) is an input here.
+ *   Q = X WQ, K = X WK, V = X WV      (WQ, WK, WV [d x dh], dh = all heads)
+ *   Z = O WO                          (O [T x dh], WO [dh x d])
+ * Backward, given dZ and the attention core's dQ, dK, dV:
+ *   dO = dZ WO^T, dWO = O^T dZ, dX = dQ WQ^T + dK WK^T + dV WV^T,
+ *   dWQ = X^T dQ, dWK = X^T dK, dWV = X^T dV.
+ * Sharded by heads ("Parallelism" tag page of Jiang Yi's homepage, post
+ * "megatron-lm", Method / Attention: W_Q = [W_Q1 ... W_Qh] by heads,
+ * O = [o_1 ... o_h] W_O; "Tensor parallelism" (brunomaga.github.io),
+ * Megatron_MHA: column-parallel QKV, row-parallel output projection, f on the
+ * input, g on the output): shard i owns columns [o_i, o_i + w_i) of WQ, WK,
+ * WV and rows of WO; Z = sum_i O_i WO_i (g) and dX = sum_i of the shard's
+ * three products (f).                                                        */
+int oracle_attn_forward(int64_t T, int64_t d, int64_t dh, const double* X, const double* WQ, const double* WK,
+                        const double* WV, const double* O, const double* WO, double* Q, double* K, double* V,
+                        double* Z) {
+  if (T < 0 || d < 1 || dh < 1 || !X || !WQ || !WK || !WV || !O || !WO || !Q || !K || !V || !Z)
+    return ORACLE_ERR_ARG;
+  matmul(T, dh, d, X, d, 1, WQ, dh, 1, Q, dh);
+  matmul(T, dh, d, X, d, 1, WK, dh, 1, K, dh);
+  matmul(T, dh, d, X, d, 1, WV, dh, 1, V, dh);
+  matmul(T, d, dh, O, dh, 1, WO, d, 1, Z, d);
+  return ORACLE_OK;
+}
+
+int oracle_attn_backward(int64_t T, int64_t d, int64_t dh, const double* X, const double* WQ, const double* WK,
+                         const double* WV, const double* O, const double* WO, const double* dZ, const double* dQ,
+                         const double* dK, const double* dV, double* dO, double* dWO, double* dX, double* dWQ,
+                         double* dWK, double* dWV) {
+  if (T < 0 || d < 1 || dh < 1 || !X || !WQ || !WK || !WV || !O || !WO || !dZ || !dQ || !dK || !dV || !dO ||
+      !dWO || !dX || !dWQ || !dWK || !dWV)
+    return ORACLE_ERR_ARG;
+  double* tmp = (double*)malloc((size_t)(T * d ? T * d : 1) * sizeof(double));
+  if (!tmp) return ORACLE_ERR_NOMEM;
+  matmul(T, dh, d, dZ, d, 1, WO, 1, d, dO, dh);   /* dO = dZ WO^T */
+  matmul(dh, d, T, O, 1, dh, dZ, d, 1, dWO, d);   /* dWO = O^T dZ */
+  matmul(T, d, dh, dQ, dh, 1, WQ, 1, dh, dX, d);  /* dX = dQ WQ^T ... */
+  matmul(T, d, dh, dK, dh, 1, WK, 1, dh, tmp, d);
+  for (int64_t i = 0; i < T * d; ++i) dX[i] += tmp[i];
+  matmul(T, d, dh, dV, dh, 1, WV, 1, dh, tmp, d);
+  for (int64_t i = 0; i < T * d; ++i) dX[i] += tmp[i];
+  matmul(d, dh, T, X, 1, d, dQ, dh, 1, dWQ, dh);  /* dWQ = X^T dQ */
+  matmul(d, dh, T, X, 1, d, dK, dh, 1, dWK, dh);
+  matmul(d, dh, T, X, 1, d, dV, dh, 1, dWV, dh);
+  free(tmp);
+  return ORACLE_OK;
+}
+
+/* Per-shard form: arrays of t shard pointers; the g-sum gives Z, the f-sum dX. */
+int oracle_attn_sharded(int64_t T, int64_t d, int32_t t, const int64_t* w_i, const double* X,
+                        const double* const* WQ_i, const double* const* WK_i, const double* const* WV_i,
+                        const double* const* O_i, const double* const* WO_i, const double* dZ,
+                        const double* const* dQ_i, const double* const* dK_i, const double* const* dV_i, double* Z,
+                        double* dX, double* const* dWO_i, double* const* dWQ_i) {
+  if (T < 0 || d < 1 || t < 1 || !w_i || !X || !WQ_i || !WK_i || !WV_i || !O_i || !WO_i || !dZ || !dQ_i || !dK_i ||
+      !dV_i || !Z || !dX || !dWO_i || !dWQ_i)
+    return ORACLE_ERR_ARG;
+  size_t nx = (size_t)(T * d ? T * d : 1);
+  double* part = (double*)malloc(nx * sizeof(double));
+  if (!part) return ORACLE_ERR_NOMEM;
+  for (int64_t i = 0; i < T * d; ++i) Z[i] = dX[i] = 0.0;
+  for (int32_t s = 0; s < t; ++s) {
+    int64_t w = w_i[s];
+    matmul(T, d, w, O_i[s], w, 1, WO_i[s], d, 1, part, d);
+    for (int64_t i = 0; i < T * d; ++i) Z[i] += part[i]; /* g */
+    matmul(w, d, T, O_i[s], 1, w, dZ, d, 1, dWO_i[s], d);
+    matmul(d, w, T, X, 1, d, dQ_i[s], w, 1, dWQ_i[s], w);
+    matmul(T, d, w, dQ_i[s], w, 1, WQ_i[s], 1, w, part, d);
+    for (int64_t i = 0; i < T * d; ++i) dX[i] += part[i]; /* f */
+    matmul(T, d, w, dK_i[s], w, 1, WK_i[s], 1, w, part, d);
+    for (int64_t i = 0; i < T * d; ++i) dX[i] += part[i];
+    matmul(T, d, w, dV_i[s], w, 1, WV_i[s], 1, w, part, d);
+    for (int64_t i = 0; i < T * d; ++i) dX[i] += part[i];
+  }
+  free(part);
+  return ORACLE_OK;
 }
 
 /* db2 = sum over the T tokens of dY[r, :] -- the gradient of the bias added

@@ -498,3 +498,79 @@ def test_planted_bias_per_shard_is_caught(tmp_path):
     assert np.max(np.abs(Y - ff["Y"])) >= 1.0
     Yc, _ = oracle.forward_sharded(inp.X, inp.W1_i, inp.W2_i, act="relu", b2=b2)
     assert np.array_equal(Yc, oracle.forward(inp.X, inp.W1, inp.W2, act="relu", b2=b2)["Y"])
+
+
+# ---------------------------------------------------------------- attention projections (QKV by heads, row-split WO)
+
+def _attn_inputs(rng, T, d, dh, integer=False):
+    draw = (lambda *s: rng.integers(-3, 4, s).astype(np.float64)) if integer else (lambda *s: rng.normal(size=s))
+    return {"X": draw(T, d), "WQ": draw(d, dh), "WK": draw(d, dh), "WV": draw(d, dh), "O": draw(T, dh),
+            "WO": draw(dh, d), "dZ": draw(T, d), "dQ": draw(T, dh), "dK": draw(T, dh), "dV": draw(T, dh)}
+
+
+@pytest.mark.parametrize("w_i", [[16], [8, 8], [4, 4, 4, 4], [4, 12]])
+def test_attn_sharded_equals_unsharded_exact(w_i):
+    """g-sum of the row-split output projection and f-sum of the three QKV
+    input gradients: exact on small integers."""
+    rng = np.random.default_rng(len(w_i))
+    P = _attn_inputs(rng, 5, 8, sum(w_i), integer=True)
+    f = oracle.attn_forward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"])
+    b = oracle.attn_backward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"], P["dV"])
+    sl = si.shard_slices(w_i)
+    cols = lambda M: [M[:, a:c] for a, c in sl]
+    rows = lambda M: [M[a:c] for a, c in sl]
+    s = oracle.attn_sharded(P["X"], cols(P["WQ"]), cols(P["WK"]), cols(P["WV"]), cols(P["O"]), rows(P["WO"]),
+                            P["dZ"], cols(P["dQ"]), cols(P["dK"]), cols(P["dV"]))
+    assert np.array_equal(s["Z"], f["Z"])
+    assert np.array_equal(s["dX"], b["dX"])
+    assert np.array_equal(np.concatenate(s["dWO_i"], 0), b["dWO"])
+    assert np.array_equal(np.concatenate(s["dWQ_i"], 1), b["dWQ"])
+
+
+def test_attn_finite_differences():
+    """L = <dZ, Z> + <dQ, Q> + <dK, K> + <dV, V>: its gradients are the backward's outputs."""
+    rng = np.random.default_rng(51)
+    P = _attn_inputs(rng, 3, 5, 6)
+    h = 1e-6
+
+    def loss(p):
+        f = oracle.attn_forward(p["X"], p["WQ"], p["WK"], p["WV"], p["O"], p["WO"])
+        return float(sum(np.sum(p[g] * f[k]) for g, k in (("dZ", "Z"), ("dQ", "Q"), ("dK", "K"), ("dV", "V"))))
+
+    b = oracle.attn_backward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"], P["dV"])
+    for name, grad in (("X", "dX"), ("WQ", "dWQ"), ("WK", "dWK"), ("WV", "dWV"), ("O", "dO"), ("WO", "dWO")):
+        num = np.zeros_like(P[name])
+        for idx in np.ndindex(P[name].shape):
+            pp = {k: v.copy() for k, v in P.items()}; pp[name][idx] += h
+            pm = {k: v.copy() for k, v in P.items()}; pm[name][idx] -= h
+            num[idx] = (loss(pp) - loss(pm)) / (2 * h)
+        assert np.max(np.abs(num - b[grad])) / np.max(np.abs(b[grad])) < 1e-7, name
+
+
+def test_attn_c_oracle_matches_numpy():
+    rng = np.random.default_rng(61)
+    P = _attn_inputs(rng, 19, 16, 24)
+    c_f = oracle.attn_forward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"])
+    n_f = np_oracle.attn_forward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"])
+    args = (P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"], P["dV"])
+    c_b, n_b = oracle.attn_backward(*args), np_oracle.attn_backward(*args)
+    for k in ("Q", "K", "V", "Z"):
+        assert np.max(np.abs(c_f[k] - n_f[k])) <= 1e-12 * max(1.0, np.max(np.abs(n_f[k])))
+    for k in n_b:
+        assert np.max(np.abs(c_b[k] - n_b[k])) <= 1e-12 * max(1.0, np.max(np.abs(n_b[k])))
+
+
+def test_planted_attn_f_sum_missing_term_is_caught(tmp_path):
+    """Dropping the dV term of the f-sum must fail the finite-difference pin."""
+    src = open(_SRC).read()
+    find = "  matmul(T, d, dh, dV, dh, 1, WV, 1, dh, tmp, d);\n  for (int64_t i = 0; i < T * d; ++i) dX[i] += tmp[i];\n"
+    assert src.count(find) == 1
+    msrc = tmp_path / "mutant_attn.c"
+    msrc.write_text(src.replace(find, ""))
+    o = oracle.load_variant(oracle.build(force=True, src=str(msrc), out=str(tmp_path / "libmutant_attn.so")))
+    rng = np.random.default_rng(71)
+    P = _attn_inputs(rng, 3, 4, 4)
+    b = o.attn_backward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"], P["dV"])
+    good = oracle.attn_backward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"],
+                                P["dV"])
+    assert np.max(np.abs(b["dX"] - good["dX"])) > 1e-3
