@@ -80,11 +80,12 @@ def _bind(lib):
     lib.oracle_rows.restype = ci
     lib.oracle_wgrad_units.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, i64, dp, dp, dp, dp, dp, dp]
     lib.oracle_wgrad_units.restype = ci
-    lib.oracle_attn_forward.argtypes = [i64, i64, i64, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp]
+    lib.oracle_attn_forward.argtypes = [i64, i64, i64, i64] + [dp] * 10
     lib.oracle_attn_forward.restype = ci
-    lib.oracle_attn_backward.argtypes = [i64, i64, i64] + [dp] * 16
+    lib.oracle_attn_backward.argtypes = [i64, i64, i64, i64] + [dp] * 16
     lib.oracle_attn_backward.restype = ci
-    lib.oracle_attn_sharded.argtypes = [i64, i64, i32, dp, dp, pp, pp, pp, pp, pp, dp, pp, pp, pp, dp, dp, pp, pp]
+    lib.oracle_attn_sharded.argtypes = [i64, i64, i32, dp, dp, dp, pp, pp, pp, pp, pp, dp, pp, pp, pp, dp, dp, pp, pp,
+                                        pp, pp]
     lib.oracle_attn_sharded.restype = ci
     lib.oracle_db2.argtypes = [i64, i64, dp, dp]
     lib.oracle_db2.restype = ci
@@ -247,12 +248,13 @@ class COracle:
         return Yr, dXr
 
     def attn_forward(self, X, WQ, WK, WV, O, WO):
-        """Attention projections: Q, K, V = X WQ, X WK, X WV and Z = O WO (fp64)."""
+        """Attention projections: Q, K, V = X WQ, X WK, X WV and Z = O WO (fp64).
+        WQ [d x dq], WK and WV [d x dkv], O [T x dq], WO [dq x d]."""
         X, WQ, WK, WV, O, WO = (_f64(m) for m in (X, WQ, WK, WV, O, WO))
         T, d = X.shape
-        dh = WQ.shape[1]
-        Q, K, V, Z = np.empty((T, dh)), np.empty((T, dh)), np.empty((T, dh)), np.empty((T, d))
-        _check(self.lib.oracle_attn_forward(T, d, dh, _ptr(X), _ptr(WQ), _ptr(WK), _ptr(WV), _ptr(O), _ptr(WO),
+        dq, dkv = WQ.shape[1], WK.shape[1]
+        Q, K, V, Z = np.empty((T, dq)), np.empty((T, dkv)), np.empty((T, dkv)), np.empty((T, d))
+        _check(self.lib.oracle_attn_forward(T, d, dq, dkv, _ptr(X), _ptr(WQ), _ptr(WK), _ptr(WV), _ptr(O), _ptr(WO),
                                             _ptr(Q), _ptr(K), _ptr(V), _ptr(Z)), "oracle_attn_forward")
         return {"Q": Q, "K": K, "V": V, "Z": Z}
 
@@ -260,30 +262,35 @@ class COracle:
         """Gradients of the attention projections given dZ and the core's dQ, dK, dV."""
         X, WQ, WK, WV, O, WO, dZ, dQ, dK, dV = (_f64(m) for m in (X, WQ, WK, WV, O, WO, dZ, dQ, dK, dV))
         T, d = X.shape
-        dh = WQ.shape[1]
-        out = {"dO": np.empty((T, dh)), "dWO": np.empty((dh, d)), "dX": np.empty((T, d)), "dWQ": np.empty((d, dh)),
-               "dWK": np.empty((d, dh)), "dWV": np.empty((d, dh))}
-        _check(self.lib.oracle_attn_backward(T, d, dh, _ptr(X), _ptr(WQ), _ptr(WK), _ptr(WV), _ptr(O), _ptr(WO),
-                                             _ptr(dZ), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(out["dO"]),
+        dq, dkv = WQ.shape[1], WK.shape[1]
+        out = {"dO": np.empty((T, dq)), "dWO": np.empty((dq, d)), "dX": np.empty((T, d)), "dWQ": np.empty((d, dq)),
+               "dWK": np.empty((d, dkv)), "dWV": np.empty((d, dkv))}
+        _check(self.lib.oracle_attn_backward(T, d, dq, dkv, _ptr(X), _ptr(WQ), _ptr(WK), _ptr(WV), _ptr(O),
+                                             _ptr(WO), _ptr(dZ), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(out["dO"]),
                                              _ptr(out["dWO"]), _ptr(out["dX"]), _ptr(out["dWQ"]), _ptr(out["dWK"]),
                                              _ptr(out["dWV"])), "oracle_attn_backward")
         return out
 
     def attn_sharded(self, X, WQ_i, WK_i, WV_i, O_i, WO_i, dZ, dQ_i, dK_i, dV_i):
-        """Per-shard projections with the g-sum (Z) and the f-sum (dX); also dWO_i, dWQ_i."""
+        """Per-shard projections with the g-sum (Z) and the f-sum (dX), and the
+        per-shard weight gradients dWO_i, dWQ_i, dWK_i, dWV_i."""
         X, dZ = _f64(X), _f64(dZ)
         L = lambda xs: [_f64(x) for x in xs]
         WQ_i, WK_i, WV_i, O_i, WO_i, dQ_i, dK_i, dV_i = map(L, (WQ_i, WK_i, WV_i, O_i, WO_i, dQ_i, dK_i, dV_i))
         T, d = X.shape
-        w = np.array([m.shape[1] for m in WQ_i], dtype=np.int64)
+        wq = np.array([m.shape[1] for m in WQ_i], dtype=np.int64)
+        wkv = np.array([m.shape[1] for m in WK_i], dtype=np.int64)
         Z, dX = np.empty((T, d)), np.empty((T, d))
-        dWO_i = [np.empty((int(x), d)) for x in w]
-        dWQ_i = [np.empty((d, int(x))) for x in w]
-        _check(self.lib.oracle_attn_sharded(T, d, len(w), w.ctypes.data_as(ctypes.c_void_p), _ptr(X), _ptrs(WQ_i),
-                                            _ptrs(WK_i), _ptrs(WV_i), _ptrs(O_i), _ptrs(WO_i), _ptr(dZ), _ptrs(dQ_i),
-                                            _ptrs(dK_i), _ptrs(dV_i), _ptr(Z), _ptr(dX), _ptrs(dWO_i), _ptrs(dWQ_i)),
-               "oracle_attn_sharded")
-        return {"Z": Z, "dX": dX, "dWO_i": dWO_i, "dWQ_i": dWQ_i}
+        dWO_i = [np.empty((int(x), d)) for x in wq]
+        dWQ_i = [np.empty((d, int(x))) for x in wq]
+        dWK_i = [np.empty((d, int(x))) for x in wkv]
+        dWV_i = [np.empty((d, int(x))) for x in wkv]
+        _check(self.lib.oracle_attn_sharded(T, d, len(wq), wq.ctypes.data_as(ctypes.c_void_p),
+                                            wkv.ctypes.data_as(ctypes.c_void_p), _ptr(X), _ptrs(WQ_i), _ptrs(WK_i),
+                                            _ptrs(WV_i), _ptrs(O_i), _ptrs(WO_i), _ptr(dZ), _ptrs(dQ_i), _ptrs(dK_i),
+                                            _ptrs(dV_i), _ptr(Z), _ptr(dX), _ptrs(dWO_i), _ptrs(dWQ_i), _ptrs(dWK_i),
+                                            _ptrs(dWV_i)), "oracle_attn_sharded")
+        return {"Z": Z, "dX": dX, "dWO_i": dWO_i, "dWQ_i": dWQ_i, "dWK_i": dWK_i, "dWV_i": dWV_i}
 
     def db2(self, dY):
         """Column sums of dY over tokens (gradient of the bias added after the g-sum)."""

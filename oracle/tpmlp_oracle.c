@@ -476,8 +476,10 @@ int oracle_wgrad_units(int64_t T, int64_t d, int64_t dff, int act, const double*
 /* ---- tensor-parallel attention projections -------------------------------
  * The attention core (softmax) is a different operation and is not part of
  * this library; O (the attention output per token) is an input here.
- *   Q = X WQ, K = X WK, V = X WV      (WQ, WK, WV [d x dh], dh = all heads)
- *   Z = O WO                          (O [T x dh], WO [dh x d])
+ *   Q = X WQ, K = X WK, V = X WV      (WQ [d x dq]; WK, WV [d x dkv])
+ *   Z = O WO                          (O [T x dq], WO [dq x d])
+ * dq = query heads x head size, dkv = key/value heads x head size (equal
+ * to dq without grouped-query attention).
  * Backward, given dZ and the attention core's dQ, dK, dV:
  *   dO = dZ WO^T, dWO = O^T dZ, dX = dQ WQ^T + dK WK^T + dV WV^T,
  *   dWQ = X^T dQ, dWK = X^T dK, dWV = X^T dV.
@@ -485,68 +487,74 @@ int oracle_wgrad_units(int64_t T, int64_t d, int64_t dff, int act, const double*
  * "megatron-lm", Method / Attention: W_Q = [W_Q1 ... W_Qh] by heads,
  * O = [o_1 ... o_h] W_O; "Tensor parallelism" (brunomaga.github.io),
  * Megatron_MHA: column-parallel QKV, row-parallel output projection, f on the
- * input, g on the output): shard i owns columns [o_i, o_i + w_i) of WQ, WK,
- * WV and rows of WO; Z = sum_i O_i WO_i (g) and dX = sum_i of the shard's
- * three products (f).                                                        */
-int oracle_attn_forward(int64_t T, int64_t d, int64_t dh, const double* X, const double* WQ, const double* WK,
-                        const double* WV, const double* O, const double* WO, double* Q, double* K, double* V,
-                        double* Z) {
-  if (T < 0 || d < 1 || dh < 1 || !X || !WQ || !WK || !WV || !O || !WO || !Q || !K || !V || !Z)
+ * input, g on the output; "AI Training Network Primer" ch. 3, Fig. 3.5: with
+ * grouped-query attention a shard owns 16 query heads and one key/value head,
+ * so its W_Q slice is wider than its W_K and W_V slices).  Shard i owns
+ * wq_i columns of WQ (and rows of WO) and wkv_i columns of WK and WV;
+ * Z = sum_i O_i WO_i (g) and dX = sum_i of the shard's three products (f).   */
+int oracle_attn_forward(int64_t T, int64_t d, int64_t dq, int64_t dkv, const double* X, const double* WQ,
+                        const double* WK, const double* WV, const double* O, const double* WO, double* Q, double* K,
+                        double* V, double* Z) {
+  if (T < 0 || d < 1 || dq < 1 || dkv < 1 || !X || !WQ || !WK || !WV || !O || !WO || !Q || !K || !V || !Z)
     return ORACLE_ERR_ARG;
-  matmul(T, dh, d, X, d, 1, WQ, dh, 1, Q, dh);
-  matmul(T, dh, d, X, d, 1, WK, dh, 1, K, dh);
-  matmul(T, dh, d, X, d, 1, WV, dh, 1, V, dh);
-  matmul(T, d, dh, O, dh, 1, WO, d, 1, Z, d);
+  matmul(T, dq, d, X, d, 1, WQ, dq, 1, Q, dq);
+  matmul(T, dkv, d, X, d, 1, WK, dkv, 1, K, dkv);
+  matmul(T, dkv, d, X, d, 1, WV, dkv, 1, V, dkv);
+  matmul(T, d, dq, O, dq, 1, WO, d, 1, Z, d);
   return ORACLE_OK;
 }
 
-int oracle_attn_backward(int64_t T, int64_t d, int64_t dh, const double* X, const double* WQ, const double* WK,
-                         const double* WV, const double* O, const double* WO, const double* dZ, const double* dQ,
-                         const double* dK, const double* dV, double* dO, double* dWO, double* dX, double* dWQ,
-                         double* dWK, double* dWV) {
-  if (T < 0 || d < 1 || dh < 1 || !X || !WQ || !WK || !WV || !O || !WO || !dZ || !dQ || !dK || !dV || !dO ||
-      !dWO || !dX || !dWQ || !dWK || !dWV)
+int oracle_attn_backward(int64_t T, int64_t d, int64_t dq, int64_t dkv, const double* X, const double* WQ,
+                         const double* WK, const double* WV, const double* O, const double* WO, const double* dZ,
+                         const double* dQ, const double* dK, const double* dV, double* dO, double* dWO, double* dX,
+                         double* dWQ, double* dWK, double* dWV) {
+  if (T < 0 || d < 1 || dq < 1 || dkv < 1 || !X || !WQ || !WK || !WV || !O || !WO || !dZ || !dQ || !dK || !dV ||
+      !dO || !dWO || !dX || !dWQ || !dWK || !dWV)
     return ORACLE_ERR_ARG;
   double* tmp = (double*)malloc((size_t)(T * d ? T * d : 1) * sizeof(double));
   if (!tmp) return ORACLE_ERR_NOMEM;
-  matmul(T, dh, d, dZ, d, 1, WO, 1, d, dO, dh);   /* dO = dZ WO^T */
-  matmul(dh, d, T, O, 1, dh, dZ, d, 1, dWO, d);   /* dWO = O^T dZ */
-  matmul(T, d, dh, dQ, dh, 1, WQ, 1, dh, dX, d);  /* dX = dQ WQ^T ... */
-  matmul(T, d, dh, dK, dh, 1, WK, 1, dh, tmp, d);
+  matmul(T, dq, d, dZ, d, 1, WO, 1, d, dO, dq);      /* dO = dZ WO^T */
+  matmul(dq, d, T, O, 1, dq, dZ, d, 1, dWO, d);      /* dWO = O^T dZ */
+  matmul(T, d, dq, dQ, dq, 1, WQ, 1, dq, dX, d);     /* dX = dQ WQ^T ... */
+  matmul(T, d, dkv, dK, dkv, 1, WK, 1, dkv, tmp, d);
   for (int64_t i = 0; i < T * d; ++i) dX[i] += tmp[i];
-  matmul(T, d, dh, dV, dh, 1, WV, 1, dh, tmp, d);
+  matmul(T, d, dkv, dV, dkv, 1, WV, 1, dkv, tmp, d);
   for (int64_t i = 0; i < T * d; ++i) dX[i] += tmp[i];
-  matmul(d, dh, T, X, 1, d, dQ, dh, 1, dWQ, dh);  /* dWQ = X^T dQ */
-  matmul(d, dh, T, X, 1, d, dK, dh, 1, dWK, dh);
-  matmul(d, dh, T, X, 1, d, dV, dh, 1, dWV, dh);
+  matmul(d, dq, T, X, 1, d, dQ, dq, 1, dWQ, dq);     /* dWQ = X^T dQ */
+  matmul(d, dkv, T, X, 1, d, dK, dkv, 1, dWK, dkv);
+  matmul(d, dkv, T, X, 1, d, dV, dkv, 1, dWV, dkv);
   free(tmp);
   return ORACLE_OK;
 }
 
-/* Per-shard form: arrays of t shard pointers; the g-sum gives Z, the f-sum dX. */
-int oracle_attn_sharded(int64_t T, int64_t d, int32_t t, const int64_t* w_i, const double* X,
-                        const double* const* WQ_i, const double* const* WK_i, const double* const* WV_i,
-                        const double* const* O_i, const double* const* WO_i, const double* dZ,
-                        const double* const* dQ_i, const double* const* dK_i, const double* const* dV_i, double* Z,
-                        double* dX, double* const* dWO_i, double* const* dWQ_i) {
-  if (T < 0 || d < 1 || t < 1 || !w_i || !X || !WQ_i || !WK_i || !WV_i || !O_i || !WO_i || !dZ || !dQ_i || !dK_i ||
-      !dV_i || !Z || !dX || !dWO_i || !dWQ_i)
+/* Per-shard form: arrays of t shard pointers; the g-sum gives Z, the f-sum dX;
+ * every weight gradient is per shard.                                         */
+int oracle_attn_sharded(int64_t T, int64_t d, int32_t t, const int64_t* wq_i, const int64_t* wkv_i,
+                        const double* X, const double* const* WQ_i, const double* const* WK_i,
+                        const double* const* WV_i, const double* const* O_i, const double* const* WO_i,
+                        const double* dZ, const double* const* dQ_i, const double* const* dK_i,
+                        const double* const* dV_i, double* Z, double* dX, double* const* dWO_i, double* const* dWQ_i,
+                        double* const* dWK_i, double* const* dWV_i) {
+  if (T < 0 || d < 1 || t < 1 || !wq_i || !wkv_i || !X || !WQ_i || !WK_i || !WV_i || !O_i || !WO_i || !dZ ||
+      !dQ_i || !dK_i || !dV_i || !Z || !dX || !dWO_i || !dWQ_i || !dWK_i || !dWV_i)
     return ORACLE_ERR_ARG;
   size_t nx = (size_t)(T * d ? T * d : 1);
   double* part = (double*)malloc(nx * sizeof(double));
   if (!part) return ORACLE_ERR_NOMEM;
   for (int64_t i = 0; i < T * d; ++i) Z[i] = dX[i] = 0.0;
   for (int32_t s = 0; s < t; ++s) {
-    int64_t w = w_i[s];
-    matmul(T, d, w, O_i[s], w, 1, WO_i[s], d, 1, part, d);
+    const int64_t wq = wq_i[s], wkv = wkv_i[s];
+    matmul(T, d, wq, O_i[s], wq, 1, WO_i[s], d, 1, part, d);
     for (int64_t i = 0; i < T * d; ++i) Z[i] += part[i]; /* g */
-    matmul(w, d, T, O_i[s], 1, w, dZ, d, 1, dWO_i[s], d);
-    matmul(d, w, T, X, 1, d, dQ_i[s], w, 1, dWQ_i[s], w);
-    matmul(T, d, w, dQ_i[s], w, 1, WQ_i[s], 1, w, part, d);
+    matmul(wq, d, T, O_i[s], 1, wq, dZ, d, 1, dWO_i[s], d);
+    matmul(d, wq, T, X, 1, d, dQ_i[s], wq, 1, dWQ_i[s], wq);
+    matmul(d, wkv, T, X, 1, d, dK_i[s], wkv, 1, dWK_i[s], wkv);
+    matmul(d, wkv, T, X, 1, d, dV_i[s], wkv, 1, dWV_i[s], wkv);
+    matmul(T, d, wq, dQ_i[s], wq, 1, WQ_i[s], 1, wq, part, d);
     for (int64_t i = 0; i < T * d; ++i) dX[i] += part[i]; /* f */
-    matmul(T, d, w, dK_i[s], w, 1, WK_i[s], 1, w, part, d);
+    matmul(T, d, wkv, dK_i[s], wkv, 1, WK_i[s], 1, wkv, part, d);
     for (int64_t i = 0; i < T * d; ++i) dX[i] += part[i];
-    matmul(T, d, w, dV_i[s], w, 1, WV_i[s], 1, w, part, d);
+    matmul(T, d, wkv, dV_i[s], wkv, 1, WV_i[s], 1, wkv, part, d);
     for (int64_t i = 0; i < T * d; ++i) dX[i] += part[i];
   }
   free(part);

@@ -502,42 +502,50 @@ def test_planted_bias_per_shard_is_caught(tmp_path):
 
 # ---------------------------------------------------------------- attention projections (QKV by heads, row-split WO)
 
-def _attn_inputs(rng, T, d, dh, integer=False):
+def _attn_inputs(rng, T, d, dq, dkv, integer=False):
     draw = (lambda *s: rng.integers(-3, 4, s).astype(np.float64)) if integer else (lambda *s: rng.normal(size=s))
-    return {"X": draw(T, d), "WQ": draw(d, dh), "WK": draw(d, dh), "WV": draw(d, dh), "O": draw(T, dh),
-            "WO": draw(dh, d), "dZ": draw(T, d), "dQ": draw(T, dh), "dK": draw(T, dh), "dV": draw(T, dh)}
+    return {"X": draw(T, d), "WQ": draw(d, dq), "WK": draw(d, dkv), "WV": draw(d, dkv), "O": draw(T, dq),
+            "WO": draw(dq, d), "dZ": draw(T, d), "dQ": draw(T, dq), "dK": draw(T, dkv), "dV": draw(T, dkv)}
 
 
-@pytest.mark.parametrize("w_i", [[16], [8, 8], [4, 4, 4, 4], [4, 12]])
-def test_attn_sharded_equals_unsharded_exact(w_i):
+def _attn_args(P):
+    return (P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"], P["dV"])
+
+
+@pytest.mark.parametrize("wq_i,wkv_i", [([16], [16]), ([8, 8], [8, 8]), ([4, 4, 4, 4], [4, 4, 4, 4]),
+                                        ([4, 12], [4, 12]), ([8, 8], [4, 4]), ([12, 4, 8], [4, 4, 8])])
+def test_attn_sharded_equals_unsharded_exact(wq_i, wkv_i):
     """g-sum of the row-split output projection and f-sum of the three QKV
-    input gradients: exact on small integers."""
-    rng = np.random.default_rng(len(w_i))
-    P = _attn_inputs(rng, 5, 8, sum(w_i), integer=True)
-    f = oracle.attn_forward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"])
-    b = oracle.attn_backward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"], P["dV"])
-    sl = si.shard_slices(w_i)
-    cols = lambda M: [M[:, a:c] for a, c in sl]
-    rows = lambda M: [M[a:c] for a, c in sl]
-    s = oracle.attn_sharded(P["X"], cols(P["WQ"]), cols(P["WK"]), cols(P["WV"]), cols(P["O"]), rows(P["WO"]),
-                            P["dZ"], cols(P["dQ"]), cols(P["dK"]), cols(P["dV"]))
+    input gradients, with and without grouped-query widths: exact on small
+    integers."""
+    rng = np.random.default_rng(len(wq_i) + sum(wkv_i))
+    P = _attn_inputs(rng, 5, 8, sum(wq_i), sum(wkv_i), integer=True)
+    f = oracle.attn_forward(*_attn_args(P)[:6])
+    b = oracle.attn_backward(*_attn_args(P))
+    sq, skv = si.shard_slices(wq_i), si.shard_slices(wkv_i)
+    cols = lambda M, sl: [M[:, a:c] for a, c in sl]
+    rows = lambda M, sl: [M[a:c] for a, c in sl]
+    s = oracle.attn_sharded(P["X"], cols(P["WQ"], sq), cols(P["WK"], skv), cols(P["WV"], skv), cols(P["O"], sq),
+                            rows(P["WO"], sq), P["dZ"], cols(P["dQ"], sq), cols(P["dK"], skv), cols(P["dV"], skv))
     assert np.array_equal(s["Z"], f["Z"])
     assert np.array_equal(s["dX"], b["dX"])
     assert np.array_equal(np.concatenate(s["dWO_i"], 0), b["dWO"])
     assert np.array_equal(np.concatenate(s["dWQ_i"], 1), b["dWQ"])
+    assert np.array_equal(np.concatenate(s["dWK_i"], 1), b["dWK"])
+    assert np.array_equal(np.concatenate(s["dWV_i"], 1), b["dWV"])
 
 
 def test_attn_finite_differences():
     """L = <dZ, Z> + <dQ, Q> + <dK, K> + <dV, V>: its gradients are the backward's outputs."""
     rng = np.random.default_rng(51)
-    P = _attn_inputs(rng, 3, 5, 6)
+    P = _attn_inputs(rng, 3, 5, 6, 2)
     h = 1e-6
 
     def loss(p):
-        f = oracle.attn_forward(p["X"], p["WQ"], p["WK"], p["WV"], p["O"], p["WO"])
+        f = oracle.attn_forward(*_attn_args(p)[:6])
         return float(sum(np.sum(p[g] * f[k]) for g, k in (("dZ", "Z"), ("dQ", "Q"), ("dK", "K"), ("dV", "V"))))
 
-    b = oracle.attn_backward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"], P["dV"])
+    b = oracle.attn_backward(*_attn_args(P))
     for name, grad in (("X", "dX"), ("WQ", "dWQ"), ("WK", "dWK"), ("WV", "dWV"), ("O", "dO"), ("WO", "dWO")):
         num = np.zeros_like(P[name])
         for idx in np.ndindex(P[name].shape):
@@ -549,28 +557,68 @@ def test_attn_finite_differences():
 
 def test_attn_c_oracle_matches_numpy():
     rng = np.random.default_rng(61)
-    P = _attn_inputs(rng, 19, 16, 24)
-    c_f = oracle.attn_forward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"])
-    n_f = np_oracle.attn_forward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"])
-    args = (P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"], P["dV"])
-    c_b, n_b = oracle.attn_backward(*args), np_oracle.attn_backward(*args)
+    P = _attn_inputs(rng, 19, 16, 24, 8)
+    c_f, n_f = oracle.attn_forward(*_attn_args(P)[:6]), np_oracle.attn_forward(*_attn_args(P)[:6])
+    c_b, n_b = oracle.attn_backward(*_attn_args(P)), np_oracle.attn_backward(*_attn_args(P))
     for k in ("Q", "K", "V", "Z"):
         assert np.max(np.abs(c_f[k] - n_f[k])) <= 1e-12 * max(1.0, np.max(np.abs(n_f[k])))
     for k in n_b:
         assert np.max(np.abs(c_b[k] - n_b[k])) <= 1e-12 * max(1.0, np.max(np.abs(n_b[k])))
 
 
+def test_attn_row_and_column_subsets():
+    """The projections are row-separable (Q, K, V, Z and dX, dO of a token
+    depend on that token's rows only) and the weight gradients column-separable
+    (a column of dWQ needs only that column of dQ): the property the sampled
+    checks at full size rely on."""
+    rng = np.random.default_rng(81)
+    P = _attn_inputs(rng, 11, 8, 12, 4)
+    f = oracle.attn_forward(*_attn_args(P)[:6])
+    b = oracle.attn_backward(*_attn_args(P))
+    rows = np.array([0, 4, 10])
+    Pr = dict(P)
+    for k in ("X", "O", "dZ", "dQ", "dK", "dV"):
+        Pr[k] = P[k][rows]
+    fr, br = oracle.attn_forward(*_attn_args(Pr)[:6]), oracle.attn_backward(*_attn_args(Pr))
+    for k in ("Q", "K", "V", "Z"):
+        assert np.allclose(fr[k], f[k][rows], rtol=1e-13, atol=1e-13)
+    for k in ("dX", "dO"):
+        assert np.allclose(br[k], b[k][rows], rtol=1e-13, atol=1e-13)
+    cq, ckv = np.array([1, 7, 11]), np.array([0, 3])
+    Pc = dict(P)
+    Pc["WQ"], Pc["O"], Pc["WO"], Pc["dQ"] = P["WQ"][:, cq], P["O"][:, cq], P["WO"][cq], P["dQ"][:, cq]
+    Pc["WK"], Pc["WV"], Pc["dK"], Pc["dV"] = P["WK"][:, ckv], P["WV"][:, ckv], P["dK"][:, ckv], P["dV"][:, ckv]
+    bc = oracle.attn_backward(*_attn_args(Pc))
+    assert np.allclose(bc["dWQ"], b["dWQ"][:, cq], rtol=1e-13, atol=1e-13)
+    assert np.allclose(bc["dWK"], b["dWK"][:, ckv], rtol=1e-13, atol=1e-13)
+    assert np.allclose(bc["dWV"], b["dWV"][:, ckv], rtol=1e-13, atol=1e-13)
+    assert np.allclose(bc["dWO"], b["dWO"][cq], rtol=1e-13, atol=1e-13)
+
+
 def test_planted_attn_f_sum_missing_term_is_caught(tmp_path):
-    """Dropping the dV term of the f-sum must fail the finite-difference pin."""
+    """Dropping the dV term of the f-sum must change dX (so the finite-difference pin catches it)."""
     src = open(_SRC).read()
-    find = "  matmul(T, d, dh, dV, dh, 1, WV, 1, dh, tmp, d);\n  for (int64_t i = 0; i < T * d; ++i) dX[i] += tmp[i];\n"
+    find = "  matmul(T, d, dkv, dV, dkv, 1, WV, 1, dkv, tmp, d);\n  for (int64_t i = 0; i < T * d; ++i) dX[i] += tmp[i];\n"
     assert src.count(find) == 1
     msrc = tmp_path / "mutant_attn.c"
     msrc.write_text(src.replace(find, ""))
     o = oracle.load_variant(oracle.build(force=True, src=str(msrc), out=str(tmp_path / "libmutant_attn.so")))
     rng = np.random.default_rng(71)
-    P = _attn_inputs(rng, 3, 4, 4)
-    b = o.attn_backward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"], P["dV"])
-    good = oracle.attn_backward(P["X"], P["WQ"], P["WK"], P["WV"], P["O"], P["WO"], P["dZ"], P["dQ"], P["dK"],
-                                P["dV"])
-    assert np.max(np.abs(b["dX"] - good["dX"])) > 1e-3
+    P = _attn_inputs(rng, 3, 4, 4, 2)
+    bad, good = o.attn_backward(*_attn_args(P)), oracle.attn_backward(*_attn_args(P))
+    assert np.max(np.abs(bad["dX"] - good["dX"])) > 1e-3
+
+
+def test_planted_attn_kv_operand_swap_is_caught(tmp_path):
+    """Projecting K with WV (a swapped operand) must break the numpy cross-check."""
+    src = open(_SRC).read()
+    find = "  matmul(T, dkv, d, X, d, 1, WK, dkv, 1, K, dkv);\n"
+    assert src.count(find) == 1
+    msrc = tmp_path / "mutant_kv.c"
+    msrc.write_text(src.replace(find, "  matmul(T, dkv, d, X, d, 1, WV, dkv, 1, K, dkv);\n"))
+    o = oracle.load_variant(oracle.build(force=True, src=str(msrc), out=str(tmp_path / "libmutant_kv.so")))
+    rng = np.random.default_rng(72)
+    P = _attn_inputs(rng, 6, 8, 8, 4)
+    bad = o.attn_forward(*_attn_args(P)[:6])
+    good = np_oracle.attn_forward(*_attn_args(P)[:6])
+    assert np.max(np.abs(bad["K"] - good["K"])) > 1e-3
