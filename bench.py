@@ -15,6 +15,13 @@ ranks around the timed region, value = total FLOPs of all ranks / time.
 --impl reference times the fp64 CPU oracle instead (on the host cores, a
 bounded token sample of the same workload): there is no other implementation
 of this block to run.
+
+--workload A1 / A2 measures the attention block's projections instead: one
+step = the column-parallel QKV projection, the row-parallel output projection
+with the g-sum, the output projection's backward (dO, dWO) and the QKV
+backward with the f-sum (dX, dW_QKV); the attention core between them is not
+part of the library and is not run (its output O and input gradients dQKV are
+seeded inputs).
 """
 from __future__ import annotations
 
@@ -33,6 +40,7 @@ if ROOT not in sys.path:
 import synthetic_inputs as si  # noqa: E402
 
 METRIC = "TP-sharded MLP fwd+bwd TFLOP/s on 1 GB300 (% of dense BF16 peak)"
+ATTN_METRIC = "TP-sharded attention projections fwd+bwd TFLOP/s on 1 GB300 (% of dense BF16 peak)"
 UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -50,6 +58,16 @@ def phase_flops(w: si.Workload) -> dict:
     if w.act == "swiglu":
         return {"fwd_column": 2 * g, "fwd_row": g, "bwd_dgrad": 2 * g, "bwd_fsum": 4 * g}
     return {"fwd_column": g, "fwd_row": g, "bwd_dgrad": 2 * g, "bwd_fsum": 2 * g}
+
+
+def attn_phase_flops(w: si.AttnWorkload, T: int | None = None, n_i=None, dq_i=None) -> dict:
+    """Algorithmic FLOPs of the four attention-projection launches (N = sum of
+    the fused QKV widths, dq = sum of the query widths)."""
+    T = w.T if T is None else T
+    N = sum(w.n_i if n_i is None else n_i)
+    dq = sum(w.dq_i if dq_i is None else dq_i)
+    return {"qkv_fwd": 2 * T * w.d * N, "out_fwd": 2 * T * dq * w.d, "out_bwd": 4 * T * dq * w.d,
+            "qkv_bwd": 4 * T * w.d * N}
 
 
 def load_peaks():
@@ -88,6 +106,15 @@ def measured_traffic(kernel: str, workload: str):
                 and r.get("sources_sha256") == kernel_sources_sha256()):
             return r.get("dram_bytes_per_launch")
     return None
+
+
+def attn_workload_config(w: si.AttnWorkload, extra=None):
+    cfg = {"workload": w.name, "T": w.T, "b": w.b, "s": w.s, "d": w.d, "t": w.t, "dq_i": list(w.dq_i),
+           "dkv_i": list(w.dkv_i), "n_i": list(w.n_i),
+           "l2": "no flush: every launch reads more than the 129 MB L2"}
+    if extra:
+        cfg.update(extra)
+    return cfg
 
 
 def workload_config(w: si.Workload, extra=None):
@@ -203,6 +230,34 @@ class OracleLeg:
         return time.perf_counter() - t0
 
 
+class AttnOracleLeg:
+    """The fp64 oracle of the attention projections on a bounded sample: the
+    first `tokens` tokens with the full weights (all shards).  Inputs are
+    converted to fp64 once, outside the timed calls."""
+
+    def __init__(self, w: si.AttnWorkload, max_tokens: int, seed: int = si.BASE_SEED):
+        import numpy as np
+        import torch
+        self.w = w
+        a = si.make_attn_inputs(max_tokens, w.d, w.dq_i, w.dkv_i, w.dtype, seed)
+        f64 = lambda t: np.ascontiguousarray(t.to(torch.float64).numpy())
+        self.X, self.WQ, self.WK, self.WV = f64(a.X), f64(a.WQ), f64(a.WK), f64(a.WV)
+        self.O, self.WO, self.dZ = f64(a.O), f64(a.WO), f64(a.dZ)
+        self.dQ, self.dK, self.dV = f64(a.dQ), f64(a.dK), f64(a.dV)
+
+    def flops(self, tokens: int, shards: int) -> int:
+        return sum(attn_phase_flops(self.w, tokens).values())
+
+    def step(self, tokens: int, shards: int = 0) -> float:
+        import oracle
+        n = tokens
+        t0 = time.perf_counter()
+        oracle.attn_forward(self.X[:n], self.WQ, self.WK, self.WV, self.O[:n], self.WO)
+        oracle.attn_backward(self.X[:n], self.WQ, self.WK, self.WV, self.O[:n], self.WO, self.dZ[:n], self.dQ[:n],
+                             self.dK[:n], self.dV[:n])
+        return time.perf_counter() - t0
+
+
 def oracle_threads() -> int:
     import oracle
     return oracle.num_threads()
@@ -215,6 +270,48 @@ def cpu_baseline(w: si.Workload, tokens: int):
     return {"value": v, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
             "sample": f"fp64 oracle forward+backward on the first {tokens} of {w.T} tokens with all {w.t} shards "
                       f"(full weights), one call of {dt:.1f} s; TFLOP/s = algorithmic FLOPs of that sample / time"}
+
+
+def attn_cpu_baseline(w: si.AttnWorkload, tokens: int):
+    leg = AttnOracleLeg(w, tokens)
+    dt = leg.step(tokens)
+    v = leg.flops(tokens, w.t) / dt / 1e12
+    return {"value": v, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle attention projections forward+backward on the first {tokens} of {w.T} tokens "
+                      f"(full weights, all {w.t} shards), one call of {dt:.1f} s; TFLOP/s = algorithmic FLOPs of "
+                      f"that sample / time"}
+
+
+def run_reference_attn(args, w: si.AttnWorkload):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    leg = AttnOracleLeg(w, 64)
+    budget = 150.0 / (args.steps + args.warmup)
+    t1 = leg.step(1)
+    t8 = leg.step(8)
+    per_tok = max(1e-9, (t8 - t1) / 7)
+    tokens = 1
+    for tk in (64, 32, 16, 8, 4, 2, 1):
+        if t1 + (tk - 1) * per_tok <= budget:
+            tokens = tk
+            break
+    for _ in range(args.warmup):
+        leg.step(tokens)
+    times = [leg.step(tokens) for _ in range(args.steps)]
+    total = sum(times)
+    value = leg.flops(tokens, w.t) * len(times) / total / 1e12
+    sample = (f"per step: fp64 oracle attention projections forward+backward on the first {tokens} of {w.T} "
+              f"tokens (full weights); TFLOP/s = algorithmic FLOPs of the sample / time")
+    line = {"impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) X/O/gradients, N(0,0.02) W)", "config": attn_workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def run_reference(args, w: si.Workload):
@@ -456,19 +553,155 @@ def run_e2e(args, w, tp, mlp, inp, dev, stream, ws):
             "api": "tpmlp_forward + tpmlp_backward, inputs from pinned host memory"}
 
 
+def run_ours_attn(args, w: si.AttnWorkload):
+    import torch
+    import megatron_tensor_transformer_column_gb300 as tp
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tp.load()
+
+    a = si.make_attn_workload_inputs(w)
+    m = tp.ShardedAttentionProj(w.T, w.d, w.dq_i, w.dkv_i, w.dtype, device=dev)
+    X, dZ = a.X.to(dev), a.dZ.to(dev)
+    Wqkv = [x.to(dev) for x in a.Wqkv_i]
+    O = [x.to(dev) for x in a.O_i]
+    WO = [x.to(dev) for x in a.WO_i]
+    dQKV = [x.to(dev) for x in a.dQKV_i]
+    QKV = [torch.empty(w.T, n, dtype=X.dtype, device=dev) for n in w.n_i]
+    Z = torch.empty(w.T, w.d, dtype=X.dtype, device=dev)
+    dO = [torch.empty(w.T, q, dtype=X.dtype, device=dev) for q in w.dq_i]
+    dWO = [torch.empty(q, w.d, dtype=X.dtype, device=dev) for q in w.dq_i]
+    dX = torch.empty(w.T, w.d, dtype=X.dtype, device=dev)
+    dWqkv = [torch.empty(w.d, n, dtype=X.dtype, device=dev) for n in w.n_i]
+    stream = torch.cuda.current_stream(dev)
+    plan, wsp = m.plan, m.workspace
+
+    def step(ev=None):
+        calls = (lambda: tp.tpmlp_attn_qkv_forward(plan, X, Wqkv, QKV, wsp, stream),
+                 lambda: tp.tpmlp_attn_out_forward(plan, WO, O, Z, wsp, stream),
+                 lambda: tp.tpmlp_attn_out_backward(plan, WO, O, dZ, dO, dWO, wsp, stream),
+                 lambda: tp.tpmlp_attn_qkv_backward(plan, X, Wqkv, dQKV, dX, dWqkv, wsp, stream))
+        for i, c in enumerate(calls):
+            if ev:
+                ev[i].record(stream)
+            c()
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    m.check(stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
+    barrier(ws)
+    m.check(stream)
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), ws, dev)
+    names = ["qkv_fwd", "out_fwd", "out_bwd", "qkv_bwd"]
+    per_phase = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
+                 for i, n in enumerate(names)}
+    pf = attn_phase_flops(w)
+    step_flops = sum(pf.values())
+    value = step_flops * ws * args.steps / (elapsed_ms / 1e3) / 1e12
+
+    # ---- end to end: every input from pinned host memory, every output read back
+    pin = lambda t: t.contiguous().pin_memory()
+    hin = [pin(a.X), pin(a.dZ), *[pin(x) for x in a.Wqkv_i + a.O_i + a.WO_i + a.dQKV_i]]
+    din = [X, dZ, *Wqkv, *O, *WO, *dQKV]
+    douts = [*QKV, Z, *dO, *dWO, dX, *dWqkv]
+    houts = [torch.empty_like(o, device="cpu").pin_memory() for o in douts]
+
+    def e2e_step():
+        for d_, h_ in zip(din, hin):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip(houts, douts):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    n = max(3, min(args.steps, 20))
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    m.check(stream)
+    e2e = {"value": step_flops * ws * n / (ms / 1e3) / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in hin),
+           "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in houts), "steps": n, "ms_per_step": ms / n,
+           "api": "tpmlp_attn_* (four calls), inputs from pinned host memory, every output read back"}
+
+    peaks, peak_src = load_peaks()
+    dom = max(per_phase, key=per_phase.get)
+    achieved = pf[dom] / (per_phase[dom] / 1e3) / 1e12
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": achieved / peak_sus, "traffic": measured_traffic(dom, w.name),
+                "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); "
+                             f"frac of {peak_src} burst {peak_burst}: {achieved / peak_burst:.3f}"}
+    if rank != 0:
+        return 0
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        cpu = attn_cpu_baseline(w, args.oracle_tokens)
+    line = {
+        "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) X/O/dZ/dQKV, N(0,0.02) W, rounded once to bf16)",
+        "config": attn_workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)"}),
+        "pct_of_peak": {"sustained": value / ws / peak_sus, "burst": value / ws / peak_burst, "source": peak_src},
+        "tokens_per_s": w.T * ws * args.steps / (elapsed_ms / 1e3),
+        "phase_ms": per_phase, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 4 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="C5", choices=sorted(si.WORKLOADS))
+    ap.add_argument("--workload", default="C5", choices=sorted(si.WORKLOADS) + sorted(si.ATTN_WORKLOADS))
     ap.add_argument("--oracle-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bias", action="store_true", help="include the optional biases and their gradients")
     ap.add_argument("--recompute", action="store_true", help="backward recomputes H instead of reading it")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.workload in si.ATTN_WORKLOADS:
+        w = si.ATTN_WORKLOADS[args.workload]
+        return run_reference_attn(args, w) if args.impl == "reference" else run_ours_attn(args, w)
     w = si.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

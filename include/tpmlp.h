@@ -210,6 +210,69 @@ TPMLP_API tpmlp_status tpmlp_backward_fsum(const tpmlp_plan* plan, const void* X
                                            void* const* dW1, void* const* dW3, void* const* db1, void* const* db3,
                                            void* workspace, tpmlp_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Attention projections of the tensor-parallel self-attention block.
+ *
+ * Q/K/V are column-parallel (split by heads: shard i owns a subset of the
+ * heads) and the output projection is row-parallel with the g-sum; the f
+ * operator sums the shards' input gradients in backward ("Parallelism" tag
+ * page of Jiang Yi's homepage, post "megatron-lm", Method / Attention:
+ * W_Q = [W_Q1, ..., W_Qh], O = [o_1, ..., o_h] W_O; "Tensor parallelism"
+ * (brunomaga.github.io), Megatron_MHA: one column-parallel QKV linear of
+ * width 3 x (local heads x head size) whose output is split into q, k, v, and a
+ * row-parallel output projection followed by Megatron_g; "AI Training
+ * Network Primer" ch. 3, section 3.4, Fig. 3.5: with grouped-query attention
+ * a shard owns 16 query heads and one key/value head).  The attention core
+ * (scores, mask, softmax, the product with V) runs between these calls and is
+ * not part of this library.  Neither projection has a bias (Megatron_MHA
+ * builds both linears with bias=False).
+ *
+ * Per shard i, with dq_i = its query heads x head size, dkv_i = its key/value
+ * heads x head size (dkv_i = dq_i without grouped-query attention) and
+ * n_i = dq_i + 2 dkv_i:
+ *   Wqkv[i] [d x n_i]  = [WQ_i | WK_i | WV_i]  (columns 0..dq_i-1 are WQ_i,
+ *                        then dkv_i columns of WK_i, then dkv_i of WV_i)
+ *   QKV[i]  [T x n_i]  = X Wqkv[i]             (= [Q_i | K_i | V_i])
+ *   O[i]    [T x dq_i]   the attention core's output for the shard's heads
+ *   WO[i]   [dq_i x d]   row shard i of the output projection
+ *   Z       [T x d]    = sum_i O_i WO_i         (g: summed in the accumulator)
+ * Backward, from dZ [T x d] and the core's dQKV[i] [T x n_i] =
+ * [dQ_i | dK_i | dV_i]:
+ *   dO[i]    = dZ WO_i^T              dWO[i]   = O_i^T dZ
+ *   dX       = sum_i dQKV_i Wqkv_i^T  (f: summed in the accumulator)
+ *   dWqkv[i] = X^T dQKV_i
+ * Every call is one kernel launch; layouts, ownership, alignment, streams and
+ * errors follow the conventions above (dq_i and dkv_i play the role of d_i).
+ * The plan is an attention plan (tpmlp_attn_plan_create); passing it to an
+ * MLP entry point, or an MLP plan here, is TPMLP_ERR_INVALID_ARG.  With T = 0
+ * the weight gradients are zero-filled.                                       */
+typedef struct {
+  int64_t T;             /* tokens (b * s); may be 0 */
+  int64_t d;             /* hidden size */
+  int32_t t;             /* number of shards, 1 .. TPMLP_MAX_SHARDS */
+  const int64_t* dq_i;   /* t query widths (host memory, copied) */
+  const int64_t* dkv_i;  /* t key/value widths (host memory, copied) */
+  tpmlp_dtype dtype;
+} tpmlp_attn_desc;
+
+/* Validate desc and build an attention plan (destroy with tpmlp_plan_destroy;
+ * its workspace size is tpmlp_workspace_size's).                              */
+TPMLP_API tpmlp_status tpmlp_attn_plan_create(const tpmlp_attn_desc* desc, tpmlp_plan** out);
+/* QKV[i] = X Wqkv[i] for every shard (f forward is the identity). */
+TPMLP_API tpmlp_status tpmlp_attn_qkv_forward(const tpmlp_plan* plan, const void* X, const void* const* Wqkv,
+                                              void* const* QKV, void* workspace, tpmlp_stream_t stream);
+/* Z = sum_i O[i] WO[i], the g-sum inside one fp32 accumulator. */
+TPMLP_API tpmlp_status tpmlp_attn_out_forward(const tpmlp_plan* plan, const void* const* WO, const void* const* O,
+                                              void* Z, void* workspace, tpmlp_stream_t stream);
+/* dO[i] = dZ WO[i]^T and dWO[i] = O[i]^T dZ (g backward is the identity). */
+TPMLP_API tpmlp_status tpmlp_attn_out_backward(const tpmlp_plan* plan, const void* const* WO, const void* const* O,
+                                               const void* dZ, void* const* dO, void* const* dWO, void* workspace,
+                                               tpmlp_stream_t stream);
+/* dX = sum_i dQKV[i] Wqkv[i]^T (the f-sum) and dWqkv[i] = X^T dQKV[i]. */
+TPMLP_API tpmlp_status tpmlp_attn_qkv_backward(const tpmlp_plan* plan, const void* X, const void* const* Wqkv,
+                                               const void* const* dQKV, void* dX, void* const* dWqkv,
+                                               void* workspace, tpmlp_stream_t stream);
+
 /* Watchdog controls, for testing the failure path without faulting a GPU.
  * Neither may run while another call uses the plan.
  *   tpmlp_plan_set_timeout: bound, in milliseconds (>= 1), of every wait
@@ -237,11 +300,13 @@ TPMLP_API int tpmlp_last_cuda_error(void);
  * map error; empty string after a successful call).  Static storage per
  * thread, valid until the next call on the same thread.                      */
 TPMLP_API const char* tpmlp_last_error(void);
-/* ABI version: 100 * major + minor (1.01: optional biases). */
+/* ABI version: 100 * major + minor (1.01: optional biases; 1.02: attention
+ * projections). */
 TPMLP_API int tpmlp_version(void);
 
-/* Kernel launches the last tpmlp_forward / tpmlp_backward call on this
- * thread made (for accounting; 0 before the first call).                     */
+/* Kernel launches the last compute call (tpmlp_forward, tpmlp_backward, a
+ * phase or an attention entry point) on this thread made (for accounting; 0
+ * before the first call).                                                    */
 TPMLP_API int tpmlp_last_launch_count(void);
 
 #ifdef __cplusplus

@@ -10,6 +10,8 @@ CPU or PyTorch fallback, and :func:`load` raises if the library is missing.
 ``ShardedMLP`` is a small convenience layer that allocates the outputs with
 PyTorch (device memory and streams are all PyTorch provides here) and
 ``TPMLPFunction`` wraps forward/backward as a ``torch.autograd.Function``.
+``ShardedAttentionProj`` does the same for the attention block's QKV and
+output projections (``tpmlp_attn_*``).
 """
 from __future__ import annotations
 
@@ -26,6 +28,8 @@ __all__ = [
     "tpmlp_forward", "tpmlp_backward", "tpmlp_backward_recompute", "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad",
     "tpmlp_backward_fsum", "tpmlp_check", "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version",
     "tpmlp_last_launch_count", "tpmlp_last_error", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
+    "AttnPlan", "tpmlp_attn_plan_create", "tpmlp_attn_qkv_forward", "tpmlp_attn_out_forward",
+    "tpmlp_attn_out_backward", "tpmlp_attn_qkv_backward", "ShardedAttentionProj",
 ]
 
 ACT = {"gelu": 0, "swiglu": 1}
@@ -37,10 +41,11 @@ MAX_SHARDS = 16
 
 EXPORTED_SYMBOLS = (
     "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size", "tpmlp_forward", "tpmlp_backward",
-    "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad", "tpmlp_backward_fsum", "tpmlp_check",
-    "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version", "tpmlp_last_launch_count",
-    "tpmlp_last_error", "tpmlp_forward_row_noalloc", "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection",
-    "tpmlp_backward_recompute",
+    "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad",
+    "tpmlp_backward_fsum", "tpmlp_check", "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version",
+    "tpmlp_last_launch_count", "tpmlp_last_error", "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection",
+    "tpmlp_backward_recompute", "tpmlp_attn_plan_create", "tpmlp_attn_qkv_forward", "tpmlp_attn_out_forward",
+    "tpmlp_attn_out_backward", "tpmlp_attn_qkv_backward",
 )
 
 
@@ -59,6 +64,12 @@ class TpmlpError(RuntimeError):
 class _Desc(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int64), ("t", ctypes.c_int32),
                 ("d_i", ctypes.POINTER(ctypes.c_int64)), ("act", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class _AttnDesc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int64), ("t", ctypes.c_int32),
+                ("dq_i", ctypes.POINTER(ctypes.c_int64)), ("dkv_i", ctypes.POINTER(ctypes.c_int64)),
+                ("dtype", ctypes.c_int)]
 
 
 _lib = None
@@ -107,6 +118,16 @@ def load():
         lib.tpmlp_backward_dgrad.restype = st
         lib.tpmlp_backward_fsum.argtypes = [vp, vp, pp, pp, pp, vp, pp, pp, pp, pp, vp, vp]
         lib.tpmlp_backward_fsum.restype = st
+        lib.tpmlp_attn_plan_create.argtypes = [ctypes.POINTER(_AttnDesc), ctypes.POINTER(vp)]
+        lib.tpmlp_attn_plan_create.restype = st
+        lib.tpmlp_attn_qkv_forward.argtypes = [vp, vp, pp, pp, vp, vp]
+        lib.tpmlp_attn_qkv_forward.restype = st
+        lib.tpmlp_attn_out_forward.argtypes = [vp, pp, pp, vp, vp, vp]
+        lib.tpmlp_attn_out_forward.restype = st
+        lib.tpmlp_attn_out_backward.argtypes = [vp, pp, pp, vp, pp, pp, vp, vp]
+        lib.tpmlp_attn_out_backward.restype = st
+        lib.tpmlp_attn_qkv_backward.argtypes = [vp, vp, pp, pp, vp, pp, vp, vp]
+        lib.tpmlp_attn_qkv_backward.restype = st
         lib.tpmlp_check.argtypes = [vp, vp, vp]
         lib.tpmlp_check.restype = st
         lib.tpmlp_status_string.argtypes = [i32]
@@ -197,6 +218,53 @@ def tpmlp_plan_destroy(plan: Plan):
     if plan.handle is not None and plan.handle.value:
         load().tpmlp_plan_destroy(plan.handle)
         plan.handle = None
+
+
+class AttnPlan(Plan):
+    """Owns an attention ``tpmlp_plan*``: per-shard query widths dq_i and
+    key/value widths dkv_i (fused QKV width n_i = dq_i + 2 dkv_i)."""
+
+    def __init__(self, T: int, d: int, dq_i: Sequence[int], dkv_i: Sequence[int], dtype: str = "bf16"):
+        lib = load()
+        self.T, self.d = int(T), int(d)
+        self.dq_i, self.dkv_i = tuple(int(v) for v in dq_i), tuple(int(v) for v in dkv_i)
+        if len(self.dq_i) != len(self.dkv_i):
+            raise ValueError("dq_i and dkv_i must have one entry per shard")
+        self.t = len(self.dq_i)
+        self.d_i = tuple(q + 2 * kv for q, kv in zip(self.dq_i, self.dkv_i))
+        self.act, self.dtype = None, dtype
+        self._dq = (ctypes.c_int64 * max(1, self.t))(*self.dq_i)
+        self._dkv = (ctypes.c_int64 * max(1, self.t))(*self.dkv_i)
+        desc = _AttnDesc(self.T, self.d, self.t, ctypes.cast(self._dq, ctypes.POINTER(ctypes.c_int64)),
+                         ctypes.cast(self._dkv, ctypes.POINTER(ctypes.c_int64)),
+                         DTYPE[dtype] if isinstance(dtype, str) else int(dtype))
+        h = ctypes.c_void_p()
+        _ok(lib.tpmlp_attn_plan_create(ctypes.byref(desc), ctypes.byref(h)), "tpmlp_attn_plan_create")
+        self.handle = h
+
+
+def tpmlp_attn_plan_create(T, d, dq_i, dkv_i, dtype="bf16") -> AttnPlan:
+    return AttnPlan(T, d, dq_i, dkv_i, dtype)
+
+
+def tpmlp_attn_qkv_forward(plan, X, Wqkv, QKV, workspace, stream=None):
+    _ok(load().tpmlp_attn_qkv_forward(plan.handle, _addr(X), _arr(Wqkv), _arr(QKV), _addr(workspace),
+                                      _stream(stream)), "tpmlp_attn_qkv_forward")
+
+
+def tpmlp_attn_out_forward(plan, WO, O, Z, workspace, stream=None):
+    _ok(load().tpmlp_attn_out_forward(plan.handle, _arr(WO), _arr(O), _addr(Z), _addr(workspace), _stream(stream)),
+        "tpmlp_attn_out_forward")
+
+
+def tpmlp_attn_out_backward(plan, WO, O, dZ, dO, dWO, workspace, stream=None):
+    _ok(load().tpmlp_attn_out_backward(plan.handle, _arr(WO), _arr(O), _addr(dZ), _arr(dO), _arr(dWO),
+                                       _addr(workspace), _stream(stream)), "tpmlp_attn_out_backward")
+
+
+def tpmlp_attn_qkv_backward(plan, X, Wqkv, dQKV, dX, dWqkv, workspace, stream=None):
+    _ok(load().tpmlp_attn_qkv_backward(plan.handle, _addr(X), _arr(Wqkv), _arr(dQKV), _addr(dX), _arr(dWqkv),
+                                       _addr(workspace), _stream(stream)), "tpmlp_attn_qkv_backward")
 
 
 def tpmlp_plan_set_timeout(plan: Plan, timeout_ms: int):
@@ -358,6 +426,53 @@ class ShardedMLP:
         fn(self.plan, X, W1_i, W3_i, W2_i, saved, H, dY, dact, dX, dW1, dW3, dW2, db1, db3, db2, self.workspace,
            stream)
         return {"dX": dX, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dact": dact, "db1": db1, "db3": db3, "db2": db2}
+
+    def check(self, stream=None):
+        tpmlp_check(self.plan, self.workspace, stream)
+
+
+class ShardedAttentionProj:
+    """Attention plan + workspace + output allocation for one shape.
+
+    Tensors follow the C ABI: X [T, d]; Wqkv_i [d, n_i] = [WQ_i | WK_i | WV_i];
+    QKV_i [T, n_i]; O_i [T, dq_i]; WO_i [dq_i, d]; Z [T, d].
+    """
+
+    def __init__(self, T: int, d: int, dq_i: Sequence[int], dkv_i: Sequence[int], dtype: str = "bf16",
+                 device=None):
+        import torch
+        self.plan = AttnPlan(T, d, dq_i, dkv_i, dtype)
+        self.device = torch.device(device or "cuda")
+        self.tdtype = {"bf16": torch.bfloat16, "fp32": torch.float32}[dtype]
+        self.workspace = torch.zeros(tpmlp_workspace_size(self.plan), dtype=torch.uint8, device=self.device)
+
+    def _empty(self, *shape):
+        import torch
+        return torch.empty(*shape, dtype=self.tdtype, device=self.device)
+
+    def qkv_forward(self, X, Wqkv_i, out=None, stream=None):
+        p = self.plan
+        QKV = out if out is not None else [self._empty(p.T, n) for n in p.d_i]
+        tpmlp_attn_qkv_forward(p, X, Wqkv_i, QKV, self.workspace, stream)
+        return QKV
+
+    def out_forward(self, WO_i, O_i, out=None, stream=None):
+        Z = out if out is not None else self._empty(self.plan.T, self.plan.d)
+        tpmlp_attn_out_forward(self.plan, WO_i, O_i, Z, self.workspace, stream)
+        return Z
+
+    def out_backward(self, WO_i, O_i, dZ, out=None, stream=None):
+        p = self.plan
+        dO, dWO = out if out is not None else ([self._empty(p.T, q) for q in p.dq_i],
+                                               [self._empty(q, p.d) for q in p.dq_i])
+        tpmlp_attn_out_backward(p, WO_i, O_i, dZ, dO, dWO, self.workspace, stream)
+        return dO, dWO
+
+    def qkv_backward(self, X, Wqkv_i, dQKV_i, out=None, stream=None):
+        p = self.plan
+        dX, dWqkv = out if out is not None else (self._empty(p.T, p.d), [self._empty(p.d, n) for n in p.d_i])
+        tpmlp_attn_qkv_backward(p, X, Wqkv_i, dQKV_i, dX, dWqkv, self.workspace, stream)
+        return dX, dWqkv
 
     def check(self, stream=None):
         tpmlp_check(self.plan, self.workspace, stream)

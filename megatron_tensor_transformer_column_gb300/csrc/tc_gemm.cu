@@ -660,7 +660,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
 
 }  // namespace
 
-// One kernel symbol per launch kind of a training step (same body).
+// One kernel symbol per launch kind (same body).
 #define TPMLP_TC_KERNEL(name)                                                          \
   __global__ void __launch_bounds__(kThreads, 1) name(const __grid_constant__ GemmParams p) { \
     extern __shared__ __align__(1024) uint8_t smem_raw[];                              \
@@ -671,6 +671,10 @@ TPMLP_TC_KERNEL(tpmlp_fwd_column_gemm_act)
 TPMLP_TC_KERNEL(tpmlp_fwd_row_gemm_gsum)
 TPMLP_TC_KERNEL(tpmlp_bwd_dgrad_act_wgrad2)
 TPMLP_TC_KERNEL(tpmlp_bwd_dx_fsum_wgrad1)
+TPMLP_TC_KERNEL(tpmlp_attn_qkv_proj)
+TPMLP_TC_KERNEL(tpmlp_attn_out_proj_gsum)
+TPMLP_TC_KERNEL(tpmlp_attn_out_proj_bwd)
+TPMLP_TC_KERNEL(tpmlp_attn_qkv_bwd_dx_fsum)
 
 int tc_gemm_max_smem_bytes() { return kSmemBytes; }
 
@@ -682,6 +686,10 @@ KernelFn kernel_for(int tag) {
     case TAG_FWD_ROW: return tpmlp_fwd_row_gemm_gsum;
     case TAG_BWD_DGRAD: return tpmlp_bwd_dgrad_act_wgrad2;
     case TAG_BWD_FSUM: return tpmlp_bwd_dx_fsum_wgrad1;
+    case TAG_ATTN_QKV: return tpmlp_attn_qkv_proj;
+    case TAG_ATTN_OUT: return tpmlp_attn_out_proj_gsum;
+    case TAG_ATTN_OUT_BWD: return tpmlp_attn_out_proj_bwd;
+    case TAG_ATTN_QKV_BWD: return tpmlp_attn_qkv_bwd_dx_fsum;
     default: return nullptr;
   }
 }
@@ -689,9 +697,9 @@ KernelFn kernel_for(int tag) {
 // Pairs (clusters of two CTAs) that can be resident at once on this device.
 int tc_gemm_max_pairs(int tag) {
   static std::mutex mu;
-  static int cache[64][4] = {};
+  static int cache[64][kNumKernelTags] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || tag < 0 || tag > 3) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || tag < 0 || tag >= kNumKernelTags) return 0;
   std::lock_guard<std::mutex> lk(mu);
   if (cache[dev][tag] > 0) return cache[dev][tag];
   KernelFn k = kernel_for(tag);

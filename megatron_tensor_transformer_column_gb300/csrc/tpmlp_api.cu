@@ -19,12 +19,16 @@
 
 using namespace tpmlp;
 
+enum PlanKind : int32_t { PLAN_MLP = 0, PLAN_ATTN = 1 };
+
 struct tpmlp_plan {
+  PlanKind kind;
   int64_t T, d;
   int32_t t;
-  std::vector<int64_t> d_i;
+  std::vector<int64_t> d_i;  // MLP: shard widths; attention: fused QKV widths n_i = dq_i + 2 dkv_i
   std::vector<int64_t> o_i;
   int64_t dff;
+  std::vector<int64_t> dq_i, dkv_i;  // attention only
   tpmlp_act act;
   tpmlp_dtype dtype;
   uint64_t timeout_ns;
@@ -281,9 +285,16 @@ tpmlp_status check_array(const char* name, const void* const* arr, int n, bool m
 bool swiglu(const tpmlp_plan* pl) { return pl->act == TPMLP_ACT_SWIGLU; }
 int nsaved(const tpmlp_plan* pl) { return swiglu(pl) ? 2 * pl->t : pl->t; }
 
-tpmlp_status common_checks(const tpmlp_plan* pl, void* workspace, DeviceInfo* di) {
+tpmlp_status check_kind(const tpmlp_plan* pl, PlanKind kind) {
+  if (pl->kind == kind) return TPMLP_OK;
+  return fail(TPMLP_ERR_INVALID_ARG, kind == PLAN_MLP ? "an attention plan was passed to an MLP entry point"
+                                                      : "an MLP plan was passed to an attention entry point");
+}
+
+tpmlp_status common_checks(const tpmlp_plan* pl, void* workspace, DeviceInfo* di, PlanKind kind = PLAN_MLP) {
   g_last_error[0] = 0;
   if (!pl) return fail(TPMLP_ERR_INVALID_ARG, "plan is NULL");
+  TPMLP_TRY(check_kind(pl, kind));
   TPMLP_TRY(check_ptr("workspace", workspace, false));
   return device_info(di);
 }
@@ -470,6 +481,101 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
   return TPMLP_OK;
 }
 
+// ------------------------------------------------------------------ attention projections
+// Shard i: W_QKV,i [d x n_i] = [WQ_i | WK_i | WV_i], n_i = dq_i + 2 dkv_i;
+// O_i [T x dq_i]; WO_i [dq_i x d].  Every epilogue is a plain store.
+tpmlp_status attn_qkv_fwd(const tpmlp_plan* pl, const DeviceInfo& di, const void* X, const void* const* Wqkv,
+                          void* const* QKV, void* ws, cudaStream_t st) {
+  if (pl->T == 0) return TPMLP_OK;
+  Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
+  B.begin_group(pl->T, band_for(di.sms));
+  for (int i = 0; i < pl->t; ++i) {  // f forward is the identity: every shard reads X
+    const int64_t n = pl->d_i[i];
+    Prob& P = B.add_prob(pl->T, n, 256, MAJOR_K, MAJOR_MN, EPI_STORE, n);
+    P.out0 = QKV[i];
+    B.add_seg(P, X, pl->T, pl->d, Wqkv[i], pl->d, n, nullptr, pl->d);
+  }
+  B.end_group();
+  return launch(B, TAG_ATTN_QKV, di, pl, ws, st);
+}
+
+tpmlp_status attn_out_fwd(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* WO, const void* const* O,
+                          void* Z, void* ws, cudaStream_t st) {
+  if (pl->T == 0) return TPMLP_OK;
+  Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
+  B.begin_group(pl->T, band_for(di.sms));
+  Prob& P = B.add_prob(pl->T, pl->d, 256, MAJOR_K, MAJOR_MN, EPI_STORE, pl->d);
+  P.out0 = Z;
+  // g operator: every shard's O_i WO_i accumulates into the same tile.
+  for (int i = 0; i < pl->t; ++i)
+    B.add_seg(P, O[i], pl->T, pl->dq_i[i], WO[i], pl->dq_i[i], pl->d, nullptr, pl->dq_i[i]);
+  B.end_group();
+  return launch(B, TAG_ATTN_OUT, di, pl, ws, st);
+}
+
+tpmlp_status attn_out_bwd(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* WO, const void* const* O,
+                          const void* dZ, void* const* dO, void* const* dWO, void* ws, cudaStream_t st) {
+  if (pl->T == 0) {
+    const size_t es = pl->dtype == TPMLP_BF16 ? 2 : 4;
+    for (int i = 0; i < pl->t; ++i) {
+      cudaError_t e = cudaMemsetAsync(dWO[i], 0, static_cast<size_t>(pl->dq_i[i] * pl->d) * es, st);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TPMLP_OK;
+  }
+  Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
+  const int band = band_for(di.sms);
+  // dWO_i = O_i^T dZ (K = T: the long tiles go first)
+  for (int i = 0; i < pl->t; ++i) {
+    const int64_t w = pl->dq_i[i];
+    B.begin_group(w, band);
+    Prob& P = B.add_prob(w, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
+    P.out0 = dWO[i];
+    B.add_seg(P, O[i], pl->T, w, dZ, pl->T, pl->d, nullptr, pl->T);
+    B.end_group();
+  }
+  // dO_i = dZ WO_i^T (g backward is the identity: every shard reads dZ)
+  B.begin_group(pl->T, band);
+  for (int i = 0; i < pl->t; ++i) {
+    const int64_t w = pl->dq_i[i];
+    Prob& P = B.add_prob(pl->T, w, 256, MAJOR_K, MAJOR_K, EPI_STORE, w);
+    P.out0 = dO[i];
+    B.add_seg(P, dZ, pl->T, pl->d, WO[i], w, pl->d, nullptr, pl->d);
+  }
+  B.end_group();
+  return launch(B, TAG_ATTN_OUT_BWD, di, pl, ws, st);
+}
+
+tpmlp_status attn_qkv_bwd(const tpmlp_plan* pl, const DeviceInfo& di, const void* X, const void* const* Wqkv,
+                          const void* const* dQKV, void* dX, void* const* dWqkv, void* ws, cudaStream_t st) {
+  if (pl->T == 0) {
+    const size_t es = pl->dtype == TPMLP_BF16 ? 2 : 4;
+    for (int i = 0; i < pl->t; ++i) {
+      cudaError_t e = cudaMemsetAsync(dWqkv[i], 0, static_cast<size_t>(pl->d * pl->d_i[i]) * es, st);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TPMLP_OK;
+  }
+  Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
+  const int band = band_for(di.sms);
+  // dW_QKV,i = X^T dQKV_i (K = T)
+  B.begin_group(pl->d, band);
+  for (int i = 0; i < pl->t; ++i) {
+    const int64_t n = pl->d_i[i];
+    Prob& P = B.add_prob(pl->d, n, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, n);
+    P.out0 = dWqkv[i];
+    B.add_seg(P, X, pl->T, pl->d, dQKV[i], pl->T, n, nullptr, pl->T);
+  }
+  B.end_group();
+  // dX = sum_i dQKV_i W_QKV,i^T (= dQ_i WQ_i^T + dK_i WK_i^T + dV_i WV_i^T): the f-sum.
+  B.begin_group(pl->T, band);
+  Prob& P = B.add_prob(pl->T, pl->d, 256, MAJOR_K, MAJOR_K, EPI_STORE, pl->d);
+  P.out0 = dX;
+  for (int i = 0; i < pl->t; ++i) B.add_seg(P, dQKV[i], pl->T, pl->d_i[i], Wqkv[i], pl->d, pl->d_i[i], nullptr, pl->d_i[i]);
+  B.end_group();
+  return launch(B, TAG_ATTN_QKV_BWD, di, pl, ws, st);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ library-owned scratch
@@ -532,6 +638,7 @@ tpmlp_status tpmlp_plan_create(const tpmlp_desc* desc, tpmlp_plan** out) {
     return fail(TPMLP_ERR_UNSUPPORTED, "T, d and d_ff must each be below 2^31");
   tpmlp_plan* pl = new (std::nothrow) tpmlp_plan;
   if (!pl) return TPMLP_ERR_INVALID_ARG;
+  pl->kind = PLAN_MLP;
   pl->T = desc->T;
   pl->d = desc->d;
   pl->t = desc->t;
@@ -615,6 +722,7 @@ tpmlp_status tpmlp_forward_row_noalloc(const tpmlp_plan* plan, const void* const
   g_last_launches = 0;
   g_last_error[0] = 0;
   if (!plan) return fail(TPMLP_ERR_INVALID_ARG, "plan is NULL");
+  TPMLP_TRY(check_kind(plan, PLAN_MLP));
   DeviceInfo di;
   TPMLP_TRY(device_info(&di));  // also makes the device's primary context current
   const size_t need = tpmlp_workspace_size(plan);
@@ -762,6 +870,118 @@ tpmlp_status tpmlp_backward_recompute(const tpmlp_plan* plan, const void* X, con
                   dY, dW2);
 }
 
+tpmlp_status tpmlp_attn_plan_create(const tpmlp_attn_desc* desc, tpmlp_plan** out) {
+  g_last_error[0] = 0;
+  if (!out) return fail(TPMLP_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!desc || !desc->dq_i || !desc->dkv_i) return fail(TPMLP_ERR_INVALID_ARG, "desc, dq_i or dkv_i is NULL");
+  if (desc->dtype != TPMLP_BF16 && desc->dtype != TPMLP_FP32)
+    return fail(TPMLP_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(desc->dtype));
+  if (desc->T < 0 || desc->d < 1 || desc->t < 1 || desc->t > TPMLP_MAX_SHARDS)
+    return fail(TPMLP_ERR_SHAPE, "need T >= 0, d >= 1, 1 <= t <= %d (got T=%lld d=%lld t=%d)", TPMLP_MAX_SHARDS,
+                static_cast<long long>(desc->T), static_cast<long long>(desc->d), desc->t);
+  const int64_t mult = desc->dtype == TPMLP_BF16 ? 8 : 4;
+  const int64_t kMax32 = (int64_t(1) << 31) - 1;
+  int64_t total = 0;
+  for (int i = 0; i < desc->t; ++i) {
+    if (desc->dq_i[i] < 1 || desc->dkv_i[i] < 1)
+      return fail(TPMLP_ERR_SHAPE, "shard %d: dq_i = %lld and dkv_i = %lld must be >= 1", i,
+                  static_cast<long long>(desc->dq_i[i]), static_cast<long long>(desc->dkv_i[i]));
+    total += desc->dq_i[i] + 2 * desc->dkv_i[i];
+  }
+  if (desc->d % mult)
+    return fail(TPMLP_ERR_ALIGNMENT, "d = %lld is not a multiple of %lld", static_cast<long long>(desc->d),
+                static_cast<long long>(mult));
+  for (int i = 0; i < desc->t; ++i)
+    if (desc->dq_i[i] % mult || desc->dkv_i[i] % mult)
+      return fail(TPMLP_ERR_ALIGNMENT, "shard %d: dq_i = %lld and dkv_i = %lld must be multiples of %lld", i,
+                  static_cast<long long>(desc->dq_i[i]), static_cast<long long>(desc->dkv_i[i]),
+                  static_cast<long long>(mult));
+  if (desc->T > kMax32 || desc->d > kMax32 || total > kMax32)
+    return fail(TPMLP_ERR_UNSUPPORTED, "T, d and the total QKV width must each be below 2^31");
+  tpmlp_plan* pl = new (std::nothrow) tpmlp_plan;
+  if (!pl) return TPMLP_ERR_INVALID_ARG;
+  pl->kind = PLAN_ATTN;
+  pl->T = desc->T;
+  pl->d = desc->d;
+  pl->t = desc->t;
+  pl->dq_i.assign(desc->dq_i, desc->dq_i + desc->t);
+  pl->dkv_i.assign(desc->dkv_i, desc->dkv_i + desc->t);
+  pl->d_i.resize(desc->t);
+  pl->o_i.resize(desc->t);
+  int64_t o = 0;
+  for (int i = 0; i < desc->t; ++i) {
+    pl->d_i[i] = pl->dq_i[i] + 2 * pl->dkv_i[i];
+    pl->o_i[i] = o;
+    o += pl->d_i[i];
+  }
+  pl->dff = o;
+  pl->act = TPMLP_ACT_GELU;  // unused by the attention entry points
+  pl->dtype = desc->dtype;
+  pl->timeout_ns = kDefaultTimeoutNs;
+  pl->stall_injection = 0;
+  if (const char* s = std::getenv("TPMLP_WAIT_TIMEOUT_MS")) {
+    const long long ms = std::atoll(s);
+    if (ms > 0) pl->timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
+  }
+  *out = pl;
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_attn_qkv_forward(const tpmlp_plan* plan, const void* X, const void* const* Wqkv,
+                                    void* const* QKV, void* workspace, tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di, PLAN_ATTN));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_ptr("X", X, tz));
+  TPMLP_TRY(check_array("Wqkv", Wqkv, plan->t, false));
+  TPMLP_TRY(check_array("QKV", QKV, plan->t, tz));
+  return attn_qkv_fwd(plan, di, X, Wqkv, QKV, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_attn_out_forward(const tpmlp_plan* plan, const void* const* WO, const void* const* O, void* Z,
+                                    void* workspace, tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di, PLAN_ATTN));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_array("WO", WO, plan->t, false));
+  TPMLP_TRY(check_array("O", O, plan->t, tz));
+  TPMLP_TRY(check_ptr("Z", Z, tz));
+  return attn_out_fwd(plan, di, WO, O, Z, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_attn_out_backward(const tpmlp_plan* plan, const void* const* WO, const void* const* O,
+                                     const void* dZ, void* const* dO, void* const* dWO, void* workspace,
+                                     tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di, PLAN_ATTN));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_array("WO", WO, plan->t, false));
+  TPMLP_TRY(check_array("O", O, plan->t, tz));
+  TPMLP_TRY(check_ptr("dZ", dZ, tz));
+  TPMLP_TRY(check_array("dO", dO, plan->t, tz));
+  TPMLP_TRY(check_array("dWO", dWO, plan->t, false));
+  return attn_out_bwd(plan, di, WO, O, dZ, dO, dWO, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_attn_qkv_backward(const tpmlp_plan* plan, const void* X, const void* const* Wqkv,
+                                     const void* const* dQKV, void* dX, void* const* dWqkv, void* workspace,
+                                     tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di, PLAN_ATTN));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_ptr("X", X, tz));
+  TPMLP_TRY(check_ptr("dX", dX, tz));
+  TPMLP_TRY(check_array("Wqkv", Wqkv, plan->t, false));
+  TPMLP_TRY(check_array("dQKV", dQKV, plan->t, tz));
+  TPMLP_TRY(check_array("dWqkv", dWqkv, plan->t, false));
+  return attn_qkv_bwd(plan, di, X, Wqkv, dQKV, dX, dWqkv, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
 tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpmlp_stream_t stream) {
   if (!plan || !workspace) return TPMLP_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -794,7 +1014,7 @@ const char* tpmlp_status_string(tpmlp_status s) {
 
 int tpmlp_last_cuda_error(void) { return g_last_cuda_error; }
 const char* tpmlp_last_error(void) { return g_last_error; }
-int tpmlp_version(void) { return 101; }
+int tpmlp_version(void) { return 102; }
 int tpmlp_last_launch_count(void) { return g_last_launches; }
 
 }  // extern "C"

@@ -137,12 +137,17 @@ cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int max_pairs_hi
 cudaError_t launch_simt_gemm(const GemmParams& p, cudaStream_t stream);
 
 // Kernel tags: one kernel symbol per launch kind, so that profiles tell the
-// four launches of a training step apart.
+// launches of a training step apart.
 enum KernelTag : int {
   TAG_FWD_COLUMN = 0,   // column-parallel GEMM + activation
   TAG_FWD_ROW = 1,      // row-parallel GEMM with the g-sum
   TAG_BWD_DGRAD = 2,    // dH_i -> dA_i (act') and dW2_i
   TAG_BWD_FSUM = 3,     // dX with the f-sum, and dW1_i (dW3_i)
+  TAG_ATTN_QKV = 4,     // attention: column-parallel QKV projection
+  TAG_ATTN_OUT = 5,     // attention: row-parallel output projection with the g-sum
+  TAG_ATTN_OUT_BWD = 6, // attention: dO_i and dWO_i
+  TAG_ATTN_QKV_BWD = 7, // attention: dX with the f-sum, and dW_QKV,i
+  kNumKernelTags = 8,
 };
 
 }  // namespace tpmlp

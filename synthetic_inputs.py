@@ -158,3 +158,84 @@ def make_biases(d: int, d_i, act: str = "gelu", dtype: str = "bf16", seed: int =
     sl = shard_slices(d_i)
     return {"b1": b1, "b3": b3, "b2": b2, "b1_i": [b1[lo:hi].contiguous() for lo, hi in sl],
             "b3_i": [b3[lo:hi].contiguous() for lo, hi in sl] if b3 is not None else None}
+
+
+# ---------------------------------------------------------------- attention projections
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    name: str
+    T: int
+    d: int
+    dq_i: tuple   # per-shard query width (query heads x head size)
+    dkv_i: tuple  # per-shard key/value width (key/value heads x head size)
+    dtype: str
+    b: int = 0
+    s: int = 0
+
+    @property
+    def t(self) -> int:
+        return len(self.dq_i)
+
+    @property
+    def n_i(self) -> tuple:
+        return tuple(q + 2 * kv for q, kv in zip(self.dq_i, self.dkv_i))
+
+
+# The pages' attention shapes: the Megatron GPT-2 8.3B row (hidden 3072, 32 heads of size 96, TP = 8: four
+# heads per shard) and Llama 3 405B at TP = 8 (hidden 16384; 16 query heads and one key/value head of size
+# 128 per shard).
+ATTN_WORKLOADS = {
+    "A1": AttnWorkload("A1 attn-proj bf16 GPT-2 8.3B b=8 s=2048 d=3072 32 heads x 96 t=8 (4 heads/shard)", 16384,
+                       3072, (384,) * 8, (384,) * 8, "bf16", 8, 2048),
+    "A2": AttnWorkload("A2 attn-proj bf16 Llama-3-405B b=1 s=8192 d=16384 GQA 128q/8kv x 128 t=8", 8192, 16384,
+                       (2048,) * 8, (128,) * 8, "bf16", 1, 8192),
+}
+
+
+@dataclass
+class AttnInputs:
+    """Full tensors (CPU, storage dtype) and the per-shard layout of the
+    library: W_QKV,i = [WQ_i | WK_i | WV_i] (columns), O_i, WO_i (rows) and
+    dQKV_i = [dQ_i | dK_i | dV_i]."""
+    X: torch.Tensor
+    WQ: torch.Tensor
+    WK: torch.Tensor
+    WV: torch.Tensor
+    O: torch.Tensor
+    WO: torch.Tensor
+    dZ: torch.Tensor
+    dQ: torch.Tensor
+    dK: torch.Tensor
+    dV: torch.Tensor
+    dq_i: tuple
+    dkv_i: tuple
+    Wqkv_i: List[torch.Tensor] = field(default_factory=list)
+    O_i: List[torch.Tensor] = field(default_factory=list)
+    WO_i: List[torch.Tensor] = field(default_factory=list)
+    dQKV_i: List[torch.Tensor] = field(default_factory=list)
+
+
+def make_attn_inputs(T: int, d: int, dq_i, dkv_i, dtype: str = "bf16", seed: int = BASE_SEED,
+                     w_std: float = 0.02) -> AttnInputs:
+    """Sub-seeds +20 X, +21 WQ, +22 WK, +23 WV, +24 O, +25 WO, +26 dZ, +27 dQ, +28 dK, +29 dV.
+    X, O and the gradients ~ N(0, 1); weights ~ N(0, w_std); rounded once to the dtype.
+    O stands in for the attention core's output and dQ, dK, dV for its input
+    gradients: the core itself is not part of the projections."""
+    td = torch_dtype(dtype)
+    dq, dkv = int(sum(dq_i)), int(sum(dkv_i))
+    r = lambda shape, k, std=1.0: _randn(shape, seed + k, std).to(td)
+    a = AttnInputs(X=r((T, d), 20), WQ=r((d, dq), 21, w_std), WK=r((d, dkv), 22, w_std), WV=r((d, dkv), 23, w_std),
+                   O=r((T, dq), 24), WO=r((dq, d), 25, w_std), dZ=r((T, d), 26), dQ=r((T, dq), 27),
+                   dK=r((T, dkv), 28), dV=r((T, dkv), 29), dq_i=tuple(int(v) for v in dq_i),
+                   dkv_i=tuple(int(v) for v in dkv_i))
+    for (q0, q1), (k0, k1) in zip(shard_slices(dq_i), shard_slices(dkv_i)):
+        a.Wqkv_i.append(torch.cat([a.WQ[:, q0:q1], a.WK[:, k0:k1], a.WV[:, k0:k1]], 1).contiguous())
+        a.O_i.append(a.O[:, q0:q1].contiguous())
+        a.WO_i.append(a.WO[q0:q1].contiguous())
+        a.dQKV_i.append(torch.cat([a.dQ[:, q0:q1], a.dK[:, k0:k1], a.dV[:, k0:k1]], 1).contiguous())
+    return a
+
+
+def make_attn_workload_inputs(w: AttnWorkload, seed: int = BASE_SEED) -> AttnInputs:
+    return make_attn_inputs(w.T, w.d, w.dq_i, w.dkv_i, w.dtype, seed)

@@ -47,7 +47,7 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert tp.tpmlp_version() == 101
+    assert tp.tpmlp_version() == 102
     for code, name in tp.STATUS.items():
         assert tp.tpmlp_status_string(code) == name
     assert tp.tpmlp_status_string(99) == "TPMLP_ERR_UNKNOWN"
@@ -95,3 +95,60 @@ def test_no_cpu_fallback_without_gpu(lib):
     with pytest.raises(tp.TpmlpError) as e:
         tp.tpmlp_forward(p, fake, [fake], None, [fake], None, None, None, fake, [fake], [fake], fake, stream=0)
     assert e.value.status in (4, 5)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((16, 64, [64], [64], "bf16"), 0),
+    ((0, 64, [128, 64], [16, 8], "bf16"), 0),
+    ((16, 64, [12], [4], "fp32"), 0),
+    ((-1, 64, [64], [64], "bf16"), 2),
+    ((16, 0, [64], [64], "bf16"), 2),
+    ((16, 64, [], [], "bf16"), 2),
+    ((16, 64, [64, 0], [8, 8], "bf16"), 2),
+    ((16, 64, [64], [0], "bf16"), 2),
+    ((16, 64, [8] * 17, [8] * 17, "bf16"), 2),
+    ((16, 60, [64], [64], "bf16"), 3),
+    ((16, 64, [64], [12], "bf16"), 3),
+    ((16, 64, [60], [64], "bf16"), 3),
+    ((16, 64, [64], [64], 9), 1),
+    ((2 ** 31, 64, [64], [64], "bf16"), 4),
+])
+def test_attn_plan_validation(lib, args, status):
+    if status == 0:
+        p = tp.AttnPlan(*args)
+        assert tp.tpmlp_workspace_size(p) == 256
+        assert p.d_i == tuple(q + 2 * kv for q, kv in zip(args[2], args[3]))
+    else:
+        with pytest.raises(tp.TpmlpError) as e:
+            tp.AttnPlan(*args)
+        assert e.value.status == status
+
+
+def test_plan_kinds_are_not_interchangeable(lib):
+    """An attention plan is refused by the MLP entry points and the reverse,
+    before any device query."""
+    ap = tp.AttnPlan(16, 64, [64], [64])
+    mp = tp.Plan(16, 64, [64], "gelu", "bf16")
+    fake = 1 << 20  # never dereferenced: the plan kind is checked first
+    with pytest.raises(tp.TpmlpError) as e:
+        tp.tpmlp_forward(ap, fake, [fake], None, [fake], None, None, None, fake, [fake], [fake], fake, stream=0)
+    assert e.value.status == 1 and "attention plan" in str(e.value)
+    with pytest.raises(tp.TpmlpError) as e:
+        tp.tpmlp_forward_row_noalloc(ap, [fake], [fake], fake, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(tp.TpmlpError) as e:
+        tp.tpmlp_attn_qkv_forward(mp, fake, [fake], [fake], fake, stream=0)
+    assert e.value.status == 1 and "MLP plan" in str(e.value)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_attn_no_cpu_fallback_without_gpu(lib):
+    p = tp.AttnPlan(16, 64, [64], [64])
+    fake = 1 << 20
+    for call in (lambda: tp.tpmlp_attn_qkv_forward(p, fake, [fake], [fake], fake, stream=0),
+                 lambda: tp.tpmlp_attn_out_forward(p, [fake], [fake], fake, fake, stream=0),
+                 lambda: tp.tpmlp_attn_out_backward(p, [fake], [fake], fake, [fake], [fake], fake, stream=0),
+                 lambda: tp.tpmlp_attn_qkv_backward(p, fake, [fake], [fake], fake, [fake], fake, stream=0)):
+        with pytest.raises(tp.TpmlpError) as e:
+            call()
+        assert e.value.status in (4, 5)
