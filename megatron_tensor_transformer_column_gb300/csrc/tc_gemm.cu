@@ -6,9 +6,10 @@
 // in its shared memory; the even CTA issues tcgen05.mma.cta_group::2, which
 // reads both CTAs' operands and writes each CTA's 128 rows of D into that
 // CTA's TMEM.  Per CTA:
-//   * warp 0 (one lane): TMA producer -- 2 A boxes and 2 B boxes of 64 x 64
-//     bf16 (32 KB) per 64-wide K block into a 7-stage ring; the completion of
-//     both CTAs' copies is counted on the even CTA's "full" barrier;
+//   * warp 0 (one lane): TMA producer -- per 128-deep K stage, this CTA's
+//     128 x 128 slice of A and of its half of B (boxes of 64 columns x 128
+//     rows, 64 KB) into a 3-stage ring; the completion of both CTAs' copies
+//     is counted on the even CTA's "full" barrier;
 //   * warp 1 (one lane, even CTA): allocates 512 TMEM columns in both CTAs,
 //     issues the MMAs into one of two 256-column accumulators and multicasts
 //     its commits (stage free, accumulator ready) to both CTAs;
@@ -16,6 +17,9 @@
 //     epilogue (store, GeLU / SwiGLU forward, GeLU' / SwiGLU' backward) and
 //     write bf16 rows to HBM; the two accumulators let the epilogue of one
 //     tile run under the main loop of the next.
+// The MMAs of a stage are issued as straight-line code (issue_stage): on
+// GB300 a branch between two tcgen05.mma instructions cost about a third of
+// the tensor throughput.
 //
 // The shard sums of the tensor-parallel MLP are K loops here: a problem
 // with several segments (one per shard) accumulates every segment's product
@@ -270,6 +274,42 @@ __device__ __forceinline__ void cursor_issue(const Cursor& c, uint32_t sb, uint3
       ptx::tma_prefetch_2d(mb2, c.n0, k0);
     else
       ptx::tma_load_2d_pair(sbB + kMNBoxBytes, mb2, c.n0, k0, fb);
+  }
+}
+
+// The MMAs of one stage: K steps j = 0 .. nk-1 of 16, each one (SwiGLU:
+// two, gate and up projection into the two 128-column halves) pair MMA.
+// Descriptors advance by offsets in 16-byte units: K-major, +32 B per K step
+// inside a 64-wide box and +16 KB per box; MN-major, +2048 B per K step.
+// A full stage is straight-line code.  A branch between two tcgen05.mma
+// instructions delays the issue of the second one (about 45 cycles per MMA
+// on GB300, against 128 cycles of tensor work for a 256 x 256 x 16 pair
+// MMA), so every choice -- SwiGLU or not, full or partial stage -- is made
+// once, before the sequence.
+template <bool kDual>
+__device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t ad0, uint64_t bd0, bool a_mn, bool b_mn,
+                                            uint32_t idesc, int nk, uint32_t& accumulate) {
+  if (nk == kBK / 16) {
+#pragma unroll
+    for (int j = 0; j < kBK / 16; ++j) {
+      const uint64_t koff = static_cast<uint64_t>(((j >> 2) * kKBoxBytes + (j & 3) * 32) >> 4);
+      const uint64_t moff = static_cast<uint64_t>((j * 2048) >> 4);
+      const uint64_t ad = ad0 + (a_mn ? moff : koff);
+      const uint64_t bd = bd0 + (b_mn ? moff : koff);
+      ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+      if (kDual) ptx::mma_bf16_pair(d_tmem + 128u, ad, bd + (kMNBoxBytes >> 4), idesc, accumulate);
+      accumulate = 1;
+    }
+    return;
+  }
+  for (int j = 0; j < nk; ++j) {  // the last, partial stage of a segment
+    const uint64_t koff = static_cast<uint64_t>(((j >> 2) * kKBoxBytes + (j & 3) * 32) >> 4);
+    const uint64_t moff = static_cast<uint64_t>((j * 2048) >> 4);
+    const uint64_t ad = ad0 + (a_mn ? moff : koff);
+    const uint64_t bd = bd0 + (b_mn ? moff : koff);
+    ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+    if (kDual) ptx::mma_bf16_pair(d_tmem + 128u, ad, bd + (kMNBoxBytes >> 4), idesc, accumulate);
+    accumulate = 1;
   }
 }
 
@@ -534,18 +574,10 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
             const uint64_t ad0 = a_desc0 + st;
             const uint64_t bd0 = b_desc0 + st;
             const int nk = min(kBK / 16, (K - k0 + 15) >> 4);
-#pragma unroll
-            for (int j = 0; j < kBK / 16; ++j) {
-              if (j < nk) {
-                const uint64_t koff = static_cast<uint64_t>(((j >> 2) * kKBoxBytes + (j & 3) * 32) >> 4);
-                const uint64_t moff = static_cast<uint64_t>((j * 2048) >> 4);
-                const uint64_t ad = ad0 + (a_mn ? moff : koff);
-                const uint64_t bd = bd0 + (b_mn ? moff : koff);
-                ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
-                if (dual) ptx::mma_bf16_pair(d_tmem + 128u, ad, bd + (kMNBoxBytes >> 4), idesc, accumulate);
-                accumulate = 1;
-              }
-            }
+            if (dual)
+              issue_stage<true>(d_tmem, ad0, bd0, a_mn, b_mn, idesc, nk, accumulate);
+            else
+              issue_stage<false>(d_tmem, ad0, bd0, a_mn, b_mn, idesc, nk, accumulate);
             issued = true;
             ptx::mma_commit_pair_mc(empty_bar(stage), kPairMask);  // stage free in both CTAs
             if (++stage == kStages) {
