@@ -65,7 +65,12 @@ constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
 constexpr int kNumAcc = 2;
 constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 8 * kNumBars + 16;
+// Epilogue staging: each epilogue warp owns two 32 x 32 bf16 blocks (its 32
+// TMEM lanes x 32 columns), written row by row with a 64-byte swizzle and
+// stored by TMA while the other block is being filled.
+constexpr int kEpiBlockBytes = 32 * 32 * 2;
+constexpr int kEpiBytes = kNumEpiWarps * 2 * kEpiBlockBytes;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + 8 * kNumBars + 16;
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
 constexpr uint64_t kPeerDrainNs = 2ull * 1000 * 1000;
 constexpr uint16_t kPairMask = 0x3;
@@ -323,22 +328,44 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
   return __bfloat1622float2(h);
 }
 
-// Store 32 consecutive values of one row (nvalid of them, a multiple of 8)
-// as bf16 with 16-byte stores.
-__device__ __forceinline__ void store_row32(void* out, int64_t ldo, int64_t row, int col, int nvalid,
-                                            const float (&v)[32]) {
-  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out) + row * ldo + col;
+// One epilogue warp's output path: 32 rows (its TMEM lanes) x 32 columns of
+// bf16 at a time go through one of its two shared-memory blocks and out with
+// a TMA store.  A thread writes its row as four 16-byte chunks, chunk g at
+// position g ^ ((row / 2) % 4) (the 64-byte swizzle of the output maps), so
+// every 8 consecutive rows fill all 32 banks once.  Rows and columns past the
+// tensor's end are clipped by the TMA unit.  Compared with each thread
+// storing its own row to global memory (32 cache lines per warp store), this
+// moves a warp's 2 KB in four shared-memory wavefronts and one bulk copy.
+struct EpiStore {
+  uint32_t buf;  // this warp's two blocks
+  uint32_t next;
+  int rows;      // rows of the current problem's outputs
+};
+
+__device__ __forceinline__ void store_block(EpiStore& es, const GemmParams& p, int map, int x, int y,
+                                            const float (&v)[32], int lane) {
+  if (y >= es.rows) return;  // every row of this warp is past the end: no store starts out of range
+  const uint32_t b = es.buf + es.next * kEpiBlockBytes;
+  if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last used block b has read it
+  __syncwarp();
+  const uint32_t row = b + static_cast<uint32_t>(lane) * 64u;
+  const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    if (8 * g < nvalid) {
-      uint4 o;
-      o.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
-      o.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
-      o.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
-      o.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
-      *reinterpret_cast<uint4*>(dst + 8 * g) = o;
-    }
+    uint4 o;
+    o.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
+    o.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
+    o.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
+    o.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
+    ptx::st_shared_v4(row + ((static_cast<uint32_t>(g) ^ sw) << 4), o);
   }
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_store_2d(&p.maps[map], b, x, y);
+    ptx::bulk_commit_group();
+  }
+  es.next ^= 1u;
 }
 
 __device__ __forceinline__ void load_row32(const void* src, int64_t ld, int64_t row, int col, int nvalid,
@@ -365,29 +392,33 @@ __device__ __forceinline__ void add_bias32(const void* bias, int col, int nvalid
   for (int j = 0; j < 32; ++j) v[j] += b[j];
 }
 
-// Epilogue of one 32-column chunk of one accumulator row (single accumulator).
-__device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int col, int nvalid,
-                                               const uint32_t (&r)[32]) {
+// Epilogue of one 32-column chunk (columns x .. x+31 of rows y .. y+31, this
+// thread's row grow) of a single accumulator.  Every lane takes part (the
+// stores are per warp); inputs are read only for valid rows and columns.
+__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& P, EpiStore& es, int64_t grow,
+                                               bool row_ok, int x, int y, int nvalid, const uint32_t (&r)[32],
+                                               int lane) {
   float acc[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
+  const int nload = row_ok ? nvalid : 0;
   switch (P.epi) {
     case EPI_STORE:
-      add_bias32(P.aux0, col, nvalid, acc);
-      store_row32(P.out0, P.ldo, row, col, nvalid, acc);
+      add_bias32(P.aux0, x, nvalid, acc);
+      store_block(es, p, P.out_map[0], x, y, acc, lane);
       break;
     case EPI_GELU_FWD: {
-      add_bias32(P.aux0, col, nvalid, acc);
-      store_row32(P.out0, P.ldo, row, col, nvalid, acc);  // A (pre-activation)
+      add_bias32(P.aux0, x, nvalid, acc);
+      store_block(es, p, P.out_map[0], x, y, acc, lane);  // A (pre-activation)
       float h[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) h[j] = act::gelu_fast(acc[j]);
-      store_row32(P.out1, P.ldo, row, col, nvalid, h);
+      store_block(es, p, P.out_map[1], x, y, h, lane);
       break;
     }
     case EPI_GELU_BWD: {
       float a[32];
-      load_row32(P.aux0, P.ldo, row, col, nvalid, a);
+      load_row32(P.aux0, P.ldo, grow, x, nload, a);
       if (P.out1) {  // recompute H = GeLU(A) for the weight gradient of W2
         float h[32];
 #pragma unroll
@@ -396,23 +427,23 @@ __device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int c
           h[j] = a[j] * n.cdf;
           a[j] = acc[j] * fmaf(a[j] * act::kInvSqrt2Pi, n.e, n.cdf);
         }
-        store_row32(P.out1, P.ldo, row, col, nvalid, h);
+        store_block(es, p, P.out_map[1], x, y, h, lane);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) a[j] = acc[j] * act::gelu_grad_fast(a[j]);
       }
-      store_row32(P.out0, P.ldo, row, col, nvalid, a);
+      store_block(es, p, P.out_map[0], x, y, a, lane);
       break;
     }
     case EPI_SWIGLU_BWD: {
       float g[32], u[32];
-      load_row32(P.aux0, P.ldo, row, col, nvalid, g);
-      load_row32(P.aux1, P.ldo, row, col, nvalid, u);
+      load_row32(P.aux0, P.ldo, grow, x, nload, g);
+      load_row32(P.aux1, P.ldo, grow, x, nload, u);
       if (P.out2) {  // recompute H = U * Swish(G) for the weight gradient of W2
         float h[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) h[j] = u[j] * act::swish_fast(g[j]);
-        store_row32(P.out2, P.ldo, row, col, nvalid, h);
+        store_block(es, p, P.out_map[2], x, y, h, lane);
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -421,8 +452,8 @@ __device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int c
         g[j] = dg;
         u[j] = du;
       }
-      store_row32(P.out0, P.ldo, row, col, nvalid, g);
-      store_row32(P.out1, P.ldo, row, col, nvalid, u);
+      store_block(es, p, P.out_map[0], x, y, g, lane);
+      store_block(es, p, P.out_map[1], x, y, u, lane);
       break;
     }
     default:
@@ -432,7 +463,7 @@ __device__ __forceinline__ void epilogue_chunk(const Prob& P, int64_t row, int c
 
 __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_raw) {
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kEpiBytes);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_holder + 1);
 
@@ -603,6 +634,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;              // TMEM lane quarter this warp may read
     const int half = (warp - 2) >> 2;    // which half of the tile's columns
+    EpiStore es{smem_base + static_cast<uint32_t>(kStages * kStageBytes + (warp - 2) * 2 * kEpiBlockBytes), 0u, 0};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < p.total_tiles; tile += npairs) {
@@ -612,6 +644,8 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       const int vm = max(0, min(kBM, ti.valid_m - kBM * static_cast<int>(rank)));
       const bool row_ok = row < vm;
       const int64_t grow = static_cast<int64_t>(ti.m0) + kBM * static_cast<int>(rank) + row;
+      const int wrow = ti.m0 + kBM * static_cast<int>(rank) + q * 32;  // this warp's first row
+      es.rows = P.M;
       if (row_ok && (P.epi == EPI_GELU_BWD || P.epi == EPI_SWIGLU_BWD)) {
         // Pull this thread's row of the saved pre-activation(s) into L2
         // while the accumulator is still being computed.
@@ -642,22 +676,20 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
             ptx::tmem_ld_32x32b_x32(tacc + col, rg);
             ptx::tmem_ld_32x32b_x32(tacc + 128u + col, ru);
             ptx::tmem_wait_ld();
-            if (row_ok) {
-              const int nvalid = min(32, ti.valid_n - col);
-              float g[32], u[32], h[32];
+            const int nvalid = min(32, ti.valid_n - col);
+            float g[32], u[32], h[32];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                g[j] = __uint_as_float(rg[j]);
-                u[j] = __uint_as_float(ru[j]);
-              }
-              add_bias32(P.aux0, ti.n0 + col, nvalid, g);
-              add_bias32(P.aux1, ti.n0 + col, nvalid, u);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) h[j] = u[j] * act::swish_fast(g[j]);
-              store_row32(P.out0, P.ldo, grow, ti.n0 + col, nvalid, g);
-              store_row32(P.out1, P.ldo, grow, ti.n0 + col, nvalid, u);
-              store_row32(P.out2, P.ldo, grow, ti.n0 + col, nvalid, h);
+            for (int j = 0; j < 32; ++j) {
+              g[j] = __uint_as_float(rg[j]);
+              u[j] = __uint_as_float(ru[j]);
             }
+            add_bias32(P.aux0, ti.n0 + col, nvalid, g);
+            add_bias32(P.aux1, ti.n0 + col, nvalid, u);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) h[j] = u[j] * act::swish_fast(g[j]);
+            store_block(es, p, P.out_map[0], ti.n0 + col, wrow, g, lane);
+            store_block(es, p, P.out_map[1], ti.n0 + col, wrow, u, lane);
+            store_block(es, p, P.out_map[2], ti.n0 + col, wrow, h, lane);
           }
         } else {
 #pragma unroll 1
@@ -667,7 +699,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
             uint32_t r[32];
             ptx::tmem_ld_32x32b_x32(tacc + col, r);
             ptx::tmem_wait_ld();
-            if (row_ok) epilogue_chunk(P, grow, ti.n0 + col, min(32, ti.valid_n - col), r);
+            epilogue_chunk(p, P, es, grow, row_ok, ti.n0 + col, wrow, min(32, ti.valid_n - col), r, lane);
           }
         }
       }
@@ -679,6 +711,8 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) ptx::bulk_wait_group_all();  // this warp's TMA stores are complete
+    __syncwarp();
   }
 
   ptx::tc_fence_before();

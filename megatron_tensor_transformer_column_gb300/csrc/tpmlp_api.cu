@@ -113,20 +113,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D row-major bf16 [rows x cols]; boxes of 64 columns (128 bytes, the
-// swizzle span) by box_rows rows, 128-byte swizzle, out-of-range elements read
-// as zero.  K-major operand tiles use 128-row boxes (128 M/N rows x 64 K),
+// 2-D row-major bf16 [rows x cols] with row stride ld elements.
+// Operand maps (box_rows > 0): boxes of 64 columns (128 bytes, the swizzle
+// span) by box_rows rows, 128-byte swizzle, out-of-range elements read as
+// zero.  K-major operand tiles use 128-row boxes (128 M/N rows x 64 K),
 // MN-major ones kTcBK-row boxes (kTcBK K rows of a 64-wide M/N block).
+// Output maps (box_rows == kOutputMap): 32 x 32 boxes, 64-byte swizzle, for
+// the epilogue's TMA stores (out-of-range elements are not written).
 // Returns 0 on success, the CUresult otherwise (-1: entry point unavailable).
-int encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+constexpr int kOutputMap = -1;
+int encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return -1;
+  const bool out = box_rows == kOutputMap;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {out ? 32u : 64u, out ? 32u : static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, out ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                  out ? CU_TENSOR_MAP_L2_PROMOTION_NONE : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return static_cast<int>(r);
 }
@@ -139,6 +145,7 @@ struct Builder {
   std::vector<const void*> map_ptr;
   std::vector<int64_t> map_rows, map_cols;
   std::vector<int> map_box;
+  std::vector<int64_t> map_ld;
   bool map_error = false;
   int cur_group = -1;
 
@@ -148,10 +155,12 @@ struct Builder {
     p->tile_m = tile_m;
   }
 
-  int map(const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  int map(const void* ptr, int64_t rows, int64_t cols, int box_rows, int64_t ld = -1) {
     if (!tc) return -1;
+    if (ld < 0) ld = cols;
     for (size_t i = 0; i < map_ptr.size(); ++i)
-      if (map_ptr[i] == ptr && map_rows[i] == rows && map_cols[i] == cols && map_box[i] == box_rows)
+      if (map_ptr[i] == ptr && map_rows[i] == rows && map_cols[i] == cols && map_box[i] == box_rows &&
+          map_ld[i] == ld)
         return static_cast<int>(i);
     if (p->num_maps >= kMaxMaps) {
       map_error = true;
@@ -159,7 +168,7 @@ struct Builder {
       return 0;
     }
     const int idx = p->num_maps++;
-    const int r = encode_map(&p->maps[idx], ptr, rows, cols, box_rows);
+    const int r = encode_map(&p->maps[idx], ptr, rows, cols, ld, box_rows);
     if (r != 0) {
       map_error = true;
       fail(TPMLP_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for %p [%lld x %lld]", r, ptr,
@@ -169,6 +178,7 @@ struct Builder {
     map_rows.push_back(rows);
     map_cols.push_back(cols);
     map_box.push_back(box_rows);
+    map_ld.push_back(ld);
     return idx;
   }
 
@@ -194,6 +204,7 @@ struct Builder {
     P.a_major = a_major;
     P.b_major = b_major;
     P.epi = epi;
+    P.out_map[0] = P.out_map[1] = P.out_map[2] = -1;
     P.ldo = ldo;
     Group& G = p->groups[cur_group];
     G.num_probs++;
@@ -240,9 +251,17 @@ int band_for(int sms) {
 
 tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan* plan, void* workspace,
                     cudaStream_t stream) {
-  if (B.map_error) return TPMLP_ERR_INVALID_ARG;  // message set by Builder::map
   GemmParams& p = *B.p;
   if (p.total_tiles == 0) return TPMLP_OK;
+  if (B.tc) {  // the tensor-core epilogue writes every output with TMA stores
+    for (int i = 0; i < p.num_probs; ++i) {
+      Prob& P = p.probs[i];
+      void* outs[3] = {P.out0, P.out1, P.out2};
+      for (int k = 0; k < 3; ++k)
+        if (outs[k]) P.out_map[k] = B.map(outs[k], P.M, P.N, kOutputMap, P.ldo);
+    }
+  }
+  if (B.map_error) return TPMLP_ERR_INVALID_ARG;  // message set by Builder::map
   p.status = static_cast<int32_t*>(workspace);
   p.timeout_ns = plan->timeout_ns;
   p.stall_injection = plan->stall_injection;

@@ -27,7 +27,11 @@ constexpr int kTcBK = TPMLP_TC_BK;
 // A tensor used both K-major (128-row boxes) and MN-major (64-row boxes) in
 // one launch needs two maps: the SwiGLU f-sum launch has X, dG_i and dU_i
 // twice each, W1_i and W3_i (6t + 1).
-constexpr int kMaxMaps = 6 * kMaxShards + 2;
+// Output tensors get maps of their own (32 x 32 boxes, 64-byte swizzle) for
+// the tensor-core epilogue's TMA stores: the SwiGLU f-sum launch adds dW1_i,
+// dW3_i and dX (2t + 1), the SwiGLU dgrad launch dG_i, dU_i, dW2_i and, when
+// H is recomputed, H_i (4t).
+constexpr int kMaxMaps = 8 * kMaxShards + 4;
 constexpr int kMaxProbs = 2 * kMaxShards + 2;
 constexpr int kMaxGroups = kMaxShards + 2;
 constexpr int kMaxSegs = 4 * kMaxShards + 2;
@@ -69,6 +73,7 @@ struct Prob {
   int32_t seg_begin, seg_count;
   int32_t a_major, b_major;
   int32_t epi;
+  int32_t out_map[3];  // tensor maps of out0..out2 for TMA stores (-1: none)
   int32_t pad_;
   int64_t ldo;       // row stride of out*/aux*, in elements
   void* out0;
