@@ -11,6 +11,8 @@ Two independent implementations live here:
   unsharded block, the pages' sharded formulation, and per-row / per-unit
   sampled outputs for problems too large to compute in full; also the
   attention block's QKV and output projections, unsharded and split by heads;
+  and the sequence-parallel layout (token stripes gathered before the block,
+  the partial outputs reduce-scattered into stripes after it);
 * ``np_oracle.py``: the same block written with numpy float64 matrix products,
   used to cross-check the C oracle on small shapes.
 
@@ -76,6 +78,11 @@ def _bind(lib):
     lib.oracle_backward_sharded.argtypes = [i64, i64, i32, dp, ci, dp, pp, pp, pp, pp, pp, dp, dp, pp, pp, pp, pp,
                                             pp, dp]
     lib.oracle_backward_sharded.restype = ci
+    lib.oracle_forward_sp.argtypes = [i64, i64, i32, dp, ci, i32, dp, pp, pp, pp, pp, pp, pp, dp, pp, pp]
+    lib.oracle_forward_sp.restype = ci
+    lib.oracle_backward_sp.argtypes = [i64, i64, i32, dp, ci, i32, dp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp,
+                                       pp, dp]
+    lib.oracle_backward_sp.restype = ci
     lib.oracle_rows.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, dp, i64, dp, dp, dp]
     lib.oracle_rows.restype = ci
     lib.oracle_wgrad_units.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, i64, dp, dp, dp, dp, dp, dp]
@@ -233,6 +240,56 @@ class COracle:
                "oracle_backward_sharded")
         return {"dX": dX, "dW1_i": dW1_i, "dW3_i": dW3_i, "dW2_i": dW2_i, "db1_i": db1_i, "db3_i": db3_i, "db2": db2}
 
+    def forward_sp(self, X_j, W1_i, W2_i, act="gelu", W3_i=None, b1_i=None, b3_i=None, b2=None):
+        """Sequence-parallel layout: X given as token stripes X_j; returns (Y_j stripes, [H_i])."""
+        lib = self.lib
+        a = _act(act)
+        X_j = [_f64(x) for x in X_j]
+        W1_i = [_f64(w) for w in W1_i]; W2_i = [_f64(w) for w in W2_i]
+        W3_i = [_f64(w) for w in W3_i] if W3_i is not None else None
+        b1_i = [_f64(b) for b in b1_i] if b1_i is not None else None
+        b3_i = [_f64(b) for b in b3_i] if b3_i is not None else None
+        b2 = _f64(b2)
+        rows = np.array([x.shape[0] for x in X_j], dtype=np.int64)
+        T, d = int(rows.sum()), W2_i[0].shape[1]
+        d_i = np.array([w.shape[1] for w in W1_i], dtype=np.int64)
+        Y_j = [np.empty((int(r), d)) for r in rows]
+        H_i = [np.empty((T, int(di))) for di in d_i]
+        _check(lib.oracle_forward_sp(T, d, len(W1_i), d_i.ctypes.data_as(ctypes.c_void_p), a, len(X_j),
+                                     rows.ctypes.data_as(ctypes.c_void_p), _ptrs(X_j), _ptrs(W1_i),
+                                     _ptrs(W3_i) if W3_i else None, _ptrs(W2_i), _ptrs(b1_i) if b1_i else None,
+                                     _ptrs(b3_i) if b3_i else None, _ptr(b2), _ptrs(Y_j), _ptrs(H_i)),
+               "oracle_forward_sp")
+        return Y_j, H_i
+
+    def backward_sp(self, X_j, W1_i, W2_i, dY_j, act="gelu", W3_i=None, b1_i=None, b3_i=None):
+        """Sequence-parallel layout: X, dY as token stripes; returns dict dX_j, dW1_i, dW3_i, dW2_i, db1_i, db3_i, db2."""
+        lib = self.lib
+        a = _act(act)
+        X_j = [_f64(x) for x in X_j]; dY_j = [_f64(x) for x in dY_j]
+        W1_i = [_f64(w) for w in W1_i]; W2_i = [_f64(w) for w in W2_i]
+        W3_i = [_f64(w) for w in W3_i] if W3_i is not None else None
+        b1_i = [_f64(b) for b in b1_i] if b1_i is not None else None
+        b3_i = [_f64(b) for b in b3_i] if b3_i is not None else None
+        rows = np.array([x.shape[0] for x in X_j], dtype=np.int64)
+        T, d = int(rows.sum()), W2_i[0].shape[1]
+        d_i = np.array([w.shape[1] for w in W1_i], dtype=np.int64)
+        dX_j = [np.empty((int(r), d)) for r in rows]
+        dW1_i = [np.empty((d, int(di))) for di in d_i]
+        dW2_i = [np.empty((int(di), d)) for di in d_i]
+        dW3_i = [np.empty((d, int(di))) for di in d_i] if W3_i else None
+        db1_i = [np.empty(int(di)) for di in d_i]
+        db3_i = [np.empty(int(di)) for di in d_i] if W3_i else None
+        db2 = np.empty(d)
+        _check(lib.oracle_backward_sp(T, d, len(W1_i), d_i.ctypes.data_as(ctypes.c_void_p), a, len(X_j),
+                                      rows.ctypes.data_as(ctypes.c_void_p), _ptrs(X_j), _ptrs(W1_i),
+                                      _ptrs(W3_i) if W3_i else None, _ptrs(W2_i), _ptrs(b1_i) if b1_i else None,
+                                      _ptrs(b3_i) if b3_i else None, _ptrs(dY_j), _ptrs(dX_j), _ptrs(dW1_i),
+                                      _ptrs(dW3_i) if dW3_i else None, _ptrs(dW2_i), _ptrs(db1_i),
+                                      _ptrs(db3_i) if db3_i else None, _ptr(db2)),
+               "oracle_backward_sp")
+        return {"dX_j": dX_j, "dW1_i": dW1_i, "dW3_i": dW3_i, "dW2_i": dW2_i, "db1_i": db1_i, "db3_i": db3_i, "db2": db2}
+
     def rows(self, X, W1, W2, dY, rows_idx, act="gelu", W3=None, b1=None, b3=None, b2=None):
         """Y[r, :] and dX[r, :] for the listed token rows.  Returns (Y_rows, dX_rows)."""
         lib = self.lib
@@ -363,6 +420,14 @@ def backward_sharded(*args, **kwargs):
 
 def rows(*args, **kwargs):
     return default().rows(*args, **kwargs)
+
+
+def forward_sp(*args, **kwargs):
+    return default().forward_sp(*args, **kwargs)
+
+
+def backward_sp(*args, **kwargs):
+    return default().backward_sp(*args, **kwargs)
 
 
 def wgrad_units(*args, **kwargs):

@@ -41,6 +41,10 @@
  * Their gradients are column sums over tokens: db1 = sum_r dA[r, :],
  * db3 = sum_r dU[r, :], db2 = sum_r dY[r, :].
  *
+ * The sequence-parallel layout (forward_sp / backward_sp) takes X and dY as
+ * stripes of tokens and returns Y and dX as stripes, gathering before the
+ * block and reduce-scattering after it.
+ *
  * The attention block's two projections (QKV, column-split by heads, and the
  * output projection, row-split with the g-sum) have their own functions
  * below; the attention core between them is a different operation and is an
@@ -471,6 +475,113 @@ int oracle_wgrad_units(int64_t T, int64_t d, int64_t dff, int act, const double*
     free(h);
   }
   return err ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* ---- sequence-parallel layout ----------------------------------------------
+ * "AI Training Network Primer" ch. 3, section 3.4, Fig. 3.7 (sequence
+ * parallelism with TP = t): every rank keeps a stripe of the tokens; an
+ * all-gather rebuilds the full X before the block, and a reduce-scatter after
+ * it sums the shards' partial outputs and gives every rank the rows of its
+ * own stripe; the backward pass mirrors it (all-gather of the dY stripes,
+ * reduce-scatter of the partial dX).  Here the stripes are arrays of
+ * nstripes pointers with stripe_rows[j] rows each (their sum is T), in token
+ * order.  The activations H_i and the weight gradients are full per shard.  */
+static int gather_rows(int64_t d, int32_t nstripes, const int64_t* stripe_rows, const double* const* src,
+                       double* dst) {
+  int64_t r = 0;
+  for (int32_t j = 0; j < nstripes; ++j) {
+    if (stripe_rows[j] < 0 || (stripe_rows[j] > 0 && !src[j])) return ORACLE_ERR_ARG;
+    if (stripe_rows[j]) memcpy(dst + r * d, src[j], (size_t)(stripe_rows[j] * d) * sizeof(double));
+    r += stripe_rows[j];
+  }
+  return ORACLE_OK;
+}
+
+static int64_t stripes_total(int32_t nstripes, const int64_t* stripe_rows) {
+  int64_t r = 0;
+  for (int32_t j = 0; j < nstripes; ++j) r += stripe_rows[j];
+  return r;
+}
+
+/* Y_j = sum over shards i of the rows of stripe j of Z_i (+ b2, once). */
+int oracle_forward_sp(int64_t T, int64_t d, int32_t t, const int64_t* d_i, int act, int32_t nstripes,
+                      const int64_t* stripe_rows, const double* const* X_j, const double* const* W1_i,
+                      const double* const* W3_i, const double* const* W2_i, const double* const* b1_i,
+                      const double* const* b3_i, const double* b2, double* const* Y_j, double* const* H_i) {
+  if (T < 0 || d < 1 || t < 1 || nstripes < 1 || !stripe_rows || !X_j || !Y_j || !d_i || !valid_act(act) ||
+      !W1_i || !W2_i || stripes_total(nstripes, stripe_rows) != T)
+    return ORACLE_ERR_ARG;
+  int swiglu = act == ORACLE_ACT_SWIGLU;
+  if (swiglu && !W3_i) return ORACLE_ERR_ARG;
+  size_t nx = (size_t)(T * d ? T * d : 1);
+  double* X = (double*)malloc(nx * sizeof(double));       /* all-gather */
+  double* Z = (double*)malloc((size_t)t * nx * sizeof(double)); /* partial outputs Z_i */
+  if (!X || !Z) { free(X); free(Z); return ORACLE_ERR_NOMEM; }
+  int rc = gather_rows(d, nstripes, stripe_rows, X_j, X);
+  for (int32_t s = 0; rc == ORACLE_OK && s < t; ++s) {
+    int64_t di = d_i[s];
+    if (di < 1) { rc = ORACLE_ERR_ARG; break; }
+    size_t n = (size_t)(T * di ? T * di : 1);
+    double* A = (double*)malloc(n * sizeof(double));
+    double* U = swiglu ? (double*)malloc(n * sizeof(double)) : NULL;
+    double* H = (double*)malloc(n * sizeof(double));
+    if (!A || !H || (swiglu && !U)) { free(A); free(U); free(H); rc = ORACLE_ERR_NOMEM; break; }
+    matmul(T, di, d, X, d, 1, W1_i[s], di, 1, A, di);
+    add_row_bias(T, di, A, b1_i ? b1_i[s] : NULL);
+    if (swiglu) {
+      matmul(T, di, d, X, d, 1, W3_i[s], di, 1, U, di);
+      add_row_bias(T, di, U, b3_i ? b3_i[s] : NULL);
+      for (int64_t i = 0; i < T * di; ++i) H[i] = U[i] * swish(A[i]);
+    } else {
+      for (int64_t i = 0; i < T * di; ++i) H[i] = act_value(act, A[i]);
+    }
+    matmul(T, d, di, H, di, 1, W2_i[s], d, 1, Z + (size_t)s * nx, d);
+    if (H_i && H_i[s]) memcpy(H_i[s], H, (size_t)(T * di) * sizeof(double));
+    free(A); free(U); free(H);
+  }
+  /* reduce-scatter: stripe j receives the shard sum of its own rows */
+  int64_t r0 = 0;
+  for (int32_t j = 0; rc == ORACLE_OK && j < nstripes; ++j) {
+    for (int64_t r = 0; r < stripe_rows[j]; ++r)
+      for (int64_t c = 0; c < d; ++c) {
+        double v = 0.0;
+        for (int32_t s = 0; s < t; ++s) v += Z[(size_t)s * nx + (size_t)((r0 + r) * d + c)];
+        Y_j[j][r * d + c] = v + (b2 ? b2[c] : 0.0);
+      }
+    r0 += stripe_rows[j];
+  }
+  free(X); free(Z);
+  return rc;
+}
+
+/* dX_j = sum over shards of the rows of stripe j of dX_i; weight and bias
+ * gradients from the gathered X and dY.                                      */
+int oracle_backward_sp(int64_t T, int64_t d, int32_t t, const int64_t* d_i, int act, int32_t nstripes,
+                       const int64_t* stripe_rows, const double* const* X_j, const double* const* W1_i,
+                       const double* const* W3_i, const double* const* W2_i, const double* const* b1_i,
+                       const double* const* b3_i, const double* const* dY_j, double* const* dX_j,
+                       double* const* dW1_i, double* const* dW3_i, double* const* dW2_i, double* const* db1_i,
+                       double* const* db3_i, double* db2) {
+  if (T < 0 || d < 1 || t < 1 || nstripes < 1 || !stripe_rows || !X_j || !dY_j || !dX_j ||
+      stripes_total(nstripes, stripe_rows) != T)
+    return ORACLE_ERR_ARG;
+  size_t nx = (size_t)(T * d ? T * d : 1);
+  double* X = (double*)malloc(nx * sizeof(double));
+  double* dY = (double*)malloc(nx * sizeof(double));
+  double* dX = (double*)malloc(nx * sizeof(double));
+  if (!X || !dY || !dX) { free(X); free(dY); free(dX); return ORACLE_ERR_NOMEM; }
+  int rc = gather_rows(d, nstripes, stripe_rows, X_j, X);        /* all-gather of X */
+  if (rc == ORACLE_OK) rc = gather_rows(d, nstripes, stripe_rows, dY_j, dY); /* all-gather of dY */
+  if (rc == ORACLE_OK)
+    rc = oracle_backward_sharded(T, d, t, d_i, act, X, W1_i, W3_i, W2_i, b1_i, b3_i, dY, dX, dW1_i, dW3_i, dW2_i,
+                                 db1_i, db3_i, db2);
+  int64_t r0 = 0;  /* the f-sum of the partial dX_i, scattered by stripe */
+  for (int32_t j = 0; rc == ORACLE_OK && j < nstripes; ++j) {
+    if (stripe_rows[j]) memcpy(dX_j[j], dX + r0 * d, (size_t)(stripe_rows[j] * d) * sizeof(double));
+    r0 += stripe_rows[j];
+  }
+  free(X); free(dY); free(dX);
+  return rc;
 }
 
 /* ---- tensor-parallel attention projections -------------------------------

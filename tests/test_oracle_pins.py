@@ -622,3 +622,60 @@ def test_planted_attn_kv_operand_swap_is_caught(tmp_path):
     bad = o.attn_forward(*_attn_args(P)[:6])
     good = np_oracle.attn_forward(*_attn_args(P)[:6])
     assert np.max(np.abs(bad["K"] - good["K"])) > 1e-3
+
+
+# ---------------------------------------------------------------- sequence-parallel layout (stripes of tokens)
+
+def _stripes(M, rows):
+    out, r = [], 0
+    for n in rows:
+        out.append(M[r:r + n].copy())
+        r += n
+    return out
+
+
+@pytest.mark.parametrize("act", ["identity", "relu", "swiglu"])
+@pytest.mark.parametrize("rows", [[7], [3, 4], [1, 2, 4], [0, 7], [2, 0, 5]])
+def test_sp_equals_gathered_sharded_block_exact(act, rows):
+    """The SP layout (all-gather of X before the block, reduce-scatter of the
+    partial outputs after it, and the mirror in backward) is the sharded block
+    with its rows cut into stripes: exact on small integers."""
+    inp = si.small_int_inputs(7, 6, (4, 2), "swiglu" if act == "swiglu" else "gelu", seed=len(rows) + 3)
+    W3_i = inp.W3_i if act == "swiglu" else None
+    Y, H_i = oracle.forward_sharded(inp.X, inp.W1_i, inp.W2_i, act=act, W3_i=W3_i)
+    b = oracle.backward_sharded(inp.X, inp.W1_i, inp.W2_i, inp.dY, act=act, W3_i=W3_i)
+    Y_j, H_sp = oracle.forward_sp(_stripes(inp.X.numpy(), rows), inp.W1_i, inp.W2_i, act=act, W3_i=W3_i)
+    bs = oracle.backward_sp(_stripes(inp.X.numpy(), rows), inp.W1_i, inp.W2_i, _stripes(inp.dY.numpy(), rows),
+                            act=act, W3_i=W3_i)
+    assert [y.shape[0] for y in Y_j] == rows
+    assert np.array_equal(np.concatenate(Y_j, 0), Y)
+    assert np.array_equal(np.concatenate(bs["dX_j"], 0), b["dX"])
+    for k in ("dW1_i", "dW2_i") + (("dW3_i",) if act == "swiglu" else ()):
+        for x, y in zip(bs[k], b[k]):
+            assert np.array_equal(x, y)
+    for x, y in zip(H_sp, H_i):
+        assert np.array_equal(x, y)
+    assert np.array_equal(bs["db2"], b["db2"])
+
+
+def test_sp_bias_added_once_per_token():
+    """b2 is added to every stripe row once, after the reduce-scatter sum."""
+    inp = si.small_int_inputs(6, 4, (2, 2), "gelu", seed=9)
+    b2 = np.arange(4, dtype=np.float64)
+    Y, _ = oracle.forward_sharded(inp.X, inp.W1_i, inp.W2_i, act="identity", b2=b2)
+    Y_j, _ = oracle.forward_sp(_stripes(inp.X.numpy(), [2, 4]), inp.W1_i, inp.W2_i, act="identity", b2=b2)
+    assert np.array_equal(np.concatenate(Y_j, 0), Y)
+
+
+def test_planted_sp_reduce_scatter_without_sum_is_caught(tmp_path):
+    """A reduce-scatter that keeps only shard 0's partial output must fail the exact pin."""
+    src = open(_SRC).read()
+    find = "for (int32_t s = 0; s < t; ++s) v += Z["
+    assert src.count(find) == 1
+    msrc = tmp_path / "mutant_sp.c"
+    msrc.write_text(src.replace(find, "for (int32_t s = 0; s < 1; ++s) v += Z["))
+    o = oracle.load_variant(oracle.build(force=True, src=str(msrc), out=str(tmp_path / "libmutant_sp.so")))
+    inp = si.small_int_inputs(5, 4, (2, 2), "gelu", seed=11)
+    Y, _ = oracle.forward_sharded(inp.X, inp.W1_i, inp.W2_i, act="identity")
+    Y_j, _ = o.forward_sp(_stripes(inp.X.numpy(), [2, 3]), inp.W1_i, inp.W2_i, act="identity")
+    assert not np.array_equal(np.concatenate(Y_j, 0), Y)
