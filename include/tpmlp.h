@@ -211,6 +211,42 @@ TPMLP_API tpmlp_status tpmlp_backward_fsum(const tpmlp_plan* plan, const void* X
                                            void* workspace, tpmlp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Sequence-parallel layout ("AI Training Network Primer" ch. 3, section 3.4,
+ * Fig. 3.7): each rank of the TP group keeps a stripe of the tokens; an
+ * all-gather rebuilds the full X before the block, and a reduce-scatter after
+ * it sums the shards' partial outputs and gives each rank its own stripe of
+ * Y; the backward pass mirrors it (all-gather of the dY stripes,
+ * reduce-scatter of the partial dX).  On one GPU both collectives are layout:
+ * the kernels read X and dY directly from the stripe buffers (the g- and
+ * f-sums stay in the accumulators) and write each stripe's rows of Y and dX
+ * into that stripe's buffer.  The activations (saved, H, dact) and all
+ * weight and bias gradients keep their full layouts.
+ *
+ * tpmlp_plan_set_sequence_stripes: stripe j holds stripe_rows[j] >= 0
+ * consecutive tokens, in token order; the rows sum to the plan's T; every
+ * stripe but the first starts at a multiple of 128 tokens (no tensor-memory-
+ * access box crosses a stripe).  Copied into the plan; may not be changed
+ * while another call uses the plan.
+ * Stripe arguments are HOST arrays of nstripes DEVICE pointers, each a dense
+ * row-major [stripe_rows[j] x d] array (16-byte aligned; NULL allowed for an
+ * empty stripe).  Otherwise the arguments, results and launches are those of
+ * tpmlp_forward / tpmlp_backward (no recompute variant); db2 sums dY over all
+ * stripes.  Without stripes set on the plan the calls fail with
+ * TPMLP_ERR_INVALID_ARG.                                                      */
+TPMLP_API tpmlp_status tpmlp_plan_set_sequence_stripes(tpmlp_plan* plan, int32_t nstripes,
+                                                       const int64_t* stripe_rows);
+TPMLP_API tpmlp_status tpmlp_forward_sp(const tpmlp_plan* plan, const void* const* X_stripes, const void* const* W1,
+                                        const void* const* W3, const void* const* W2, const void* const* b1,
+                                        const void* const* b3, const void* b2, void* const* Y_stripes,
+                                        void* const* saved, void* const* H, void* workspace, tpmlp_stream_t stream);
+TPMLP_API tpmlp_status tpmlp_backward_sp(const tpmlp_plan* plan, const void* const* X_stripes,
+                                         const void* const* W1, const void* const* W3, const void* const* W2,
+                                         const void* const* saved, const void* const* H,
+                                         const void* const* dY_stripes, void* const* dact, void* const* dX_stripes,
+                                         void* const* dW1, void* const* dW3, void* const* dW2, void* const* db1,
+                                         void* const* db3, void* db2, void* workspace, tpmlp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Attention projections of the tensor-parallel self-attention block.
  *
  * Q/K/V are column-parallel (split by heads: shard i owns a subset of the
@@ -301,7 +337,7 @@ TPMLP_API int tpmlp_last_cuda_error(void);
  * thread, valid until the next call on the same thread.                      */
 TPMLP_API const char* tpmlp_last_error(void);
 /* ABI version: 100 * major + minor (1.01: optional biases; 1.02: attention
- * projections). */
+ * projections; 1.03: sequence-parallel layout). */
 TPMLP_API int tpmlp_version(void);
 
 /* Kernel launches the last compute call (tpmlp_forward, tpmlp_backward, a

@@ -30,6 +30,7 @@ __all__ = [
     "tpmlp_last_launch_count", "tpmlp_last_error", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
     "AttnPlan", "tpmlp_attn_plan_create", "tpmlp_attn_qkv_forward", "tpmlp_attn_out_forward",
     "tpmlp_attn_out_backward", "tpmlp_attn_qkv_backward", "ShardedAttentionProj",
+    "tpmlp_plan_set_sequence_stripes", "tpmlp_forward_sp", "tpmlp_backward_sp",
 ]
 
 ACT = {"gelu": 0, "swiglu": 1}
@@ -45,7 +46,8 @@ EXPORTED_SYMBOLS = (
     "tpmlp_backward_fsum", "tpmlp_check", "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version",
     "tpmlp_last_launch_count", "tpmlp_last_error", "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection",
     "tpmlp_backward_recompute", "tpmlp_attn_plan_create", "tpmlp_attn_qkv_forward", "tpmlp_attn_out_forward",
-    "tpmlp_attn_out_backward", "tpmlp_attn_qkv_backward",
+    "tpmlp_attn_out_backward", "tpmlp_attn_qkv_backward", "tpmlp_plan_set_sequence_stripes", "tpmlp_forward_sp",
+    "tpmlp_backward_sp",
 )
 
 
@@ -128,6 +130,12 @@ def load():
         lib.tpmlp_attn_out_backward.restype = st
         lib.tpmlp_attn_qkv_backward.argtypes = [vp, vp, pp, pp, vp, pp, vp, vp]
         lib.tpmlp_attn_qkv_backward.restype = st
+        lib.tpmlp_plan_set_sequence_stripes.argtypes = [vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)]
+        lib.tpmlp_plan_set_sequence_stripes.restype = st
+        lib.tpmlp_forward_sp.argtypes = [vp, pp, pp, pp, pp, pp, pp, vp, pp, pp, pp, vp, vp]
+        lib.tpmlp_forward_sp.restype = st
+        lib.tpmlp_backward_sp.argtypes = [vp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp, vp, vp, vp]
+        lib.tpmlp_backward_sp.restype = st
         lib.tpmlp_check.argtypes = [vp, vp, vp]
         lib.tpmlp_check.restype = st
         lib.tpmlp_status_string.argtypes = [i32]
@@ -198,6 +206,7 @@ class Plan:
         h = ctypes.c_void_p()
         _ok(lib.tpmlp_plan_create(ctypes.byref(desc), ctypes.byref(h)), "tpmlp_plan_create")
         self.handle = h
+        self.stripe_rows = ()  # sequence-parallel token stripes (tpmlp_plan_set_sequence_stripes)
 
     @property
     def dff(self) -> int:
@@ -265,6 +274,27 @@ def tpmlp_attn_out_backward(plan, WO, O, dZ, dO, dWO, workspace, stream=None):
 def tpmlp_attn_qkv_backward(plan, X, Wqkv, dQKV, dX, dWqkv, workspace, stream=None):
     _ok(load().tpmlp_attn_qkv_backward(plan.handle, _addr(X), _arr(Wqkv), _arr(dQKV), _addr(dX), _arr(dWqkv),
                                        _addr(workspace), _stream(stream)), "tpmlp_attn_qkv_backward")
+
+
+def tpmlp_plan_set_sequence_stripes(plan: Plan, stripe_rows: Sequence[int]):
+    rows = (ctypes.c_int64 * max(1, len(stripe_rows)))(*[int(r) for r in stripe_rows])
+    _ok(load().tpmlp_plan_set_sequence_stripes(plan.handle, len(stripe_rows), rows),
+        "tpmlp_plan_set_sequence_stripes")
+    plan.stripe_rows = tuple(int(r) for r in stripe_rows)
+
+
+def tpmlp_forward_sp(plan, X_stripes, W1, W3, W2, b1, b3, b2, Y_stripes, saved, H, workspace, stream=None):
+    _ok(load().tpmlp_forward_sp(plan.handle, _arr(X_stripes), _arr(W1), _arr(W3), _arr(W2), _arr(b1), _arr(b3),
+                                _addr(b2), _arr(Y_stripes), _arr(saved), _arr(H), _addr(workspace), _stream(stream)),
+        "tpmlp_forward_sp")
+
+
+def tpmlp_backward_sp(plan, X_stripes, W1, W3, W2, saved, H, dY_stripes, dact, dX_stripes, dW1, dW3, dW2, db1, db3,
+                      db2, workspace, stream=None):
+    _ok(load().tpmlp_backward_sp(plan.handle, _arr(X_stripes), _arr(W1), _arr(W3), _arr(W2), _arr(saved), _arr(H),
+                                 _arr(dY_stripes), _arr(dact), _arr(dX_stripes), _arr(dW1), _arr(dW3), _arr(dW2),
+                                 _arr(db1), _arr(db3), _addr(db2), _addr(workspace), _stream(stream)),
+        "tpmlp_backward_sp")
 
 
 def tpmlp_plan_set_timeout(plan: Plan, timeout_ms: int):
@@ -429,6 +459,31 @@ class ShardedMLP:
 
     def check(self, stream=None):
         tpmlp_check(self.plan, self.workspace, stream)
+
+    # ---- sequence-parallel layout: X, dY in and Y, dX out as token stripes
+    def set_sequence_stripes(self, stripe_rows: Sequence[int]):
+        tpmlp_plan_set_sequence_stripes(self.plan, stripe_rows)
+
+    def alloc_stripes(self):
+        return [self._empty(r, self.plan.d) for r in self.plan.stripe_rows]
+
+    def forward_sp(self, X_stripes, W1_i, W2_i, W3_i=None, stream=None, b1_i=None, b3_i=None, b2=None):
+        """Y stripes = reduce-scatter of sum_i act(X W1_i + b1_i) W2_i (+ b2), X gathered from its stripes.
+        Returns (Y_stripes, saved, H)."""
+        Y_j = self.alloc_stripes()
+        _, saved, H = self.alloc_forward()
+        tpmlp_forward_sp(self.plan, X_stripes, W1_i, W3_i, W2_i, b1_i, b3_i, b2, Y_j, saved, H, self.workspace,
+                         stream)
+        return Y_j, saved, H
+
+    def backward_sp(self, X_stripes, W1_i, W2_i, saved, H, dY_stripes, W3_i=None, stream=None, bias_grads=False):
+        dact, _, dW1, dW3, dW2 = self.alloc_backward()
+        dX_j = self.alloc_stripes()
+        db1, db3, db2 = self.alloc_bias_grads() if bias_grads else (None, None, None)
+        tpmlp_backward_sp(self.plan, X_stripes, W1_i, W3_i, W2_i, saved, H, dY_stripes, dact, dX_j, dW1, dW3, dW2,
+                          db1, db3, db2, self.workspace, stream)
+        return {"dX_stripes": dX_j, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dact": dact, "db1": db1, "db3": db3,
+                "db2": db2}
 
 
 class ShardedAttentionProj:

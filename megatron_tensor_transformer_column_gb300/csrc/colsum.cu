@@ -12,7 +12,9 @@
 // flight per thread); the 32 lane partials of a column are added in a fixed
 // tree order in shared memory; CTA 0 of the cluster then adds the 8 chunk
 // partials in rank order through distributed shared memory.  The result is
-// the same on every run: no atomics, no global scratch.
+// the same on every run: no atomics, no global scratch.  A job without a
+// source reads the launch's token stripes (the dY stripes of the
+// sequence-parallel layout) as one tensor.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -71,7 +73,14 @@ __global__ void __launch_bounds__(kThreads) tpmlp_bias_grad_colsum(const __grid_
   float acc[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-  if (col_ok) {
+  if (col_ok && !J.src) {
+    // token stripes (sequence-parallel layout): walk the rows stripe by stripe
+    int sj = 0;
+    for (int64_t r = r_begin + lane_row; r < r_end; r += kRowLanes) {
+      while (sj + 1 < p.num_stripes && r >= p.stripe_row0[sj + 1]) ++sj;
+      accumulate_row<kBf16, kPer>(p.stripe_src[sj], (r - p.stripe_row0[sj]) * J.cols + col0, acc);
+    }
+  } else if (col_ok) {
     int64_t r = r_begin + lane_row;
     for (; r + (kUnroll - 1) * kRowLanes < r_end; r += kUnroll * kRowLanes) {
       float a[kUnroll][kPer];

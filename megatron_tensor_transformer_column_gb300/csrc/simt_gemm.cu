@@ -19,14 +19,26 @@ constexpr int kT = 32;        // tile edge (M and N)
 constexpr int kK = 32;        // K chunk
 constexpr int kThreads = 256; // 32 columns x 8 row groups of 4 rows
 
-__device__ __forceinline__ float load_a(const Seg& S, int major, int64_t m, int64_t k) {
-  const float* a = static_cast<const float*>(S.a);
-  return major == MAJOR_MN ? a[k * S.lda + m] : a[m * S.lda + k];
+// Element (row, col) of a stored row-major array, or of the launch's striped
+// input (token stripes) when `striped`.
+__device__ __forceinline__ float load_elem(const GemmParams& p, const void* base, int64_t ld, bool striped,
+                                           int64_t row, int64_t col) {
+  if (striped) {
+    const Stripes& st = p.stripes;
+    int j = 0;
+    while (j + 1 < st.num && row >= st.row0[j + 1]) ++j;
+    return static_cast<const float*>(st.in[j])[(row - st.row0[j]) * st.in_ld + col];
+  }
+  return static_cast<const float*>(base)[row * ld + col];
 }
 
-__device__ __forceinline__ float load_b(const void* b, int64_t ldb, int major, int64_t k, int64_t n) {
-  const float* bp = static_cast<const float*>(b);
-  return major == MAJOR_MN ? bp[k * ldb + n] : bp[n * ldb + k];
+__device__ __forceinline__ float load_a(const GemmParams& p, const Seg& S, int major, int64_t m, int64_t k) {
+  return major == MAJOR_MN ? load_elem(p, S.a, S.lda, S.a_striped, k, m) : load_elem(p, S.a, S.lda, S.a_striped, m, k);
+}
+
+__device__ __forceinline__ float load_b(const GemmParams& p, const void* b, int64_t ldb, bool striped, int major,
+                                        int64_t k, int64_t n) {
+  return major == MAJOR_MN ? load_elem(p, b, ldb, striped, k, n) : load_elem(p, b, ldb, striped, n, k);
 }
 
 __global__ void __launch_bounds__(kThreads) tpmlp_fp32_simt_gemm(const __grid_constant__ GemmParams p) {
@@ -71,10 +83,10 @@ __global__ void __launch_bounds__(kThreads) tpmlp_fp32_simt_gemm(const __grid_co
         if (P.a_major == MAJOR_MN) { mm = e & 31; kk = e >> 5; } else { kk = e & 31; mm = e >> 5; }
         if (P.b_major == MAJOR_MN) { nn = e & 31; kb = e >> 5; } else { kb = e & 31; nn = e >> 5; }
         const int64_t gm = m0 + mm, gk = k0 + kk, gn = n0 + nn, gkb = k0 + kb;
-        As[kk][mm] = (gm < P.M && gk < S.K) ? load_a(S, P.a_major, gm, gk) : 0.f;
+        As[kk][mm] = (gm < P.M && gk < S.K) ? load_a(p, S, P.a_major, gm, gk) : 0.f;
         const bool bin = gn < P.N && gkb < S.K;
-        Bs[kb][nn] = bin ? load_b(S.b, S.ldb, P.b_major, gkb, gn) : 0.f;
-        if (dual) B2s[kb][nn] = bin ? load_b(S.b2, S.ldb, P.b_major, gkb, gn) : 0.f;
+        Bs[kb][nn] = bin ? load_b(p, S.b, S.ldb, S.b_striped, P.b_major, gkb, gn) : 0.f;
+        if (dual) B2s[kb][nn] = bin ? load_b(p, S.b2, S.ldb, false, P.b_major, gkb, gn) : 0.f;
       }
       __syncthreads();
 #pragma unroll 8
@@ -102,7 +114,14 @@ __global__ void __launch_bounds__(kThreads) tpmlp_fp32_simt_gemm(const __grid_co
     switch (P.epi) {
       case EPI_STORE:
         if (P.aux0) v += static_cast<const float*>(P.aux0)[col];
-        static_cast<float*>(P.out0)[o] = v;
+        if (P.out_striped) {  // token stripes of the sequence-parallel layout
+          const Stripes& st = p.stripes;
+          int j = 0;
+          while (j + 1 < st.num && row >= st.row0[j + 1]) ++j;
+          static_cast<float*>(st.out[j])[(row - st.row0[j]) * st.out_ld + col] = v;
+        } else {
+          static_cast<float*>(P.out0)[o] = v;
+        }
         break;
       case EPI_GELU_FWD:
         if (P.aux0) v += static_cast<const float*>(P.aux0)[col];

@@ -116,6 +116,14 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
   return t;
 }
 
+// Stripe of a token row (sequence-parallel layout): the last j with
+// row0[j] <= row.  Empty stripes are never selected.
+__device__ __forceinline__ int stripe_of(const Stripes& st, int64_t row) {
+  int j = 0;
+  while (j + 1 < st.num && row >= st.row0[j + 1]) ++j;
+  return j;
+}
+
 struct Ctl {
   volatile int32_t* abort_flag;
   uint32_t peer_abort;  // cluster address of the peer CTA's abort flag
@@ -204,6 +212,7 @@ struct Cursor {
   const void* mb2;
   int tile, seg, seg_end, kb, kblocks;
   int a_major, b_major, dual;
+  int a_striped, b_striped;  // operand read from the launch's token stripes
   int m0, n0;          // this CTA's first row of A and first column of B
   int nA, nB;          // boxes this CTA loads per operand
   uint32_t bytes_pair; // bytes both CTAs load per K block (counted on the even CTA)
@@ -216,6 +225,8 @@ __device__ __forceinline__ void cursor_segment(Cursor& c, const GemmParams& p) {
   c.ma = &p.maps[S.a_map];
   c.mb = &p.maps[S.b_map];
   c.mb2 = c.dual ? static_cast<const void*>(&p.maps[S.b2_map]) : nullptr;
+  c.a_striped = S.a_striped;
+  c.b_striped = S.b_striped;
 }
 
 __device__ __forceinline__ void cursor_tile(Cursor& c, const GemmParams& p, int tile, uint32_t rank) {
@@ -248,9 +259,7 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const GemmParams& p, int 
 
 // Issue this CTA's box copies (or L2 prefetches) for the cursor's K block.
 template <bool kPrefetch>
-__device__ __forceinline__ void cursor_issue(const Cursor& c, uint32_t sb, uint32_t fb) {
-  const void* ma = c.ma;
-  const void* mb = c.mb;
+__device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor& c, uint32_t sb, uint32_t fb) {
   const int k0 = c.kb * kBK;
   const uint32_t sbB = sb + kOperandBytes;
   for (int b = 0; b < c.nA; ++b) {
@@ -258,7 +267,13 @@ __device__ __forceinline__ void cursor_issue(const Cursor& c, uint32_t sb, uint3
     // MN-major: box b covers columns [m0 + 64 b, +64) of K rows [k0, k0 + kBK).
     const bool mn = c.a_major == MAJOR_MN;
     const int x = mn ? c.m0 + 64 * b : k0 + 64 * b;
-    const int y = mn ? k0 : c.m0;
+    int y = mn ? k0 : c.m0;
+    const CUtensorMap* ma = static_cast<const CUtensorMap*>(c.ma);
+    if (c.a_striped) {  // the stored rows are tokens: pick the stripe, make y stripe-local
+      const int j = stripe_of(p.stripes, y);
+      ma += j;
+      y -= static_cast<int>(p.stripes.row0[j]);
+    }
     if (kPrefetch)
       ptx::tma_prefetch_2d(ma, x, y);
     else
@@ -267,7 +282,13 @@ __device__ __forceinline__ void cursor_issue(const Cursor& c, uint32_t sb, uint3
   for (int j = 0; j < c.nB; ++j) {
     const bool mn = c.b_major == MAJOR_MN;
     const int x = mn ? c.n0 + 64 * j : k0 + 64 * j;
-    const int y = mn ? k0 : c.n0;
+    int y = mn ? k0 : c.n0;
+    const CUtensorMap* mb = static_cast<const CUtensorMap*>(c.mb);
+    if (c.b_striped) {
+      const int s = stripe_of(p.stripes, y);
+      mb += s;
+      y -= static_cast<int>(p.stripes.row0[s]);
+    }
     if (kPrefetch)
       ptx::tma_prefetch_2d(mb, x, y);
     else
@@ -343,8 +364,13 @@ struct EpiStore {
 };
 
 __device__ __forceinline__ void store_block(EpiStore& es, const GemmParams& p, int map, int x, int y,
-                                            const float (&v)[32], int lane) {
+                                            const float (&v)[32], int lane, bool striped = false) {
   if (y >= es.rows) return;  // every row of this warp is past the end: no store starts out of range
+  if (striped) {  // token stripes: the stripe's own map, stripe-local rows
+    const int j = stripe_of(p.stripes, y);
+    map += j;
+    y -= static_cast<int>(p.stripes.row0[j]);
+  }
   const uint32_t b = es.buf + es.next * kEpiBlockBytes;
   if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last used block b has read it
   __syncwarp();
@@ -405,7 +431,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& 
   switch (P.epi) {
     case EPI_STORE:
       add_bias32(P.aux0, x, nvalid, acc);
-      store_block(es, p, P.out_map[0], x, y, acc, lane);
+      store_block(es, p, P.out_map[0], x, y, acc, lane, P.out_striped != 0);
       break;
     case EPI_GELU_FWD: {
       add_bias32(P.aux0, x, nvalid, acc);
@@ -523,7 +549,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       cursor_tile(ld, p, p.stall_injection ? p.total_tiles : pair, rank);  // injected stall: nothing to load
       cursor_tile(pf, p, p.stall_injection ? p.total_tiles : pair, rank);
       for (int i = 0; i < kPrefetchKBlocks && pf.tile < p.total_tiles; ++i) {
-        cursor_issue<true>(pf, 0, 0);
+        cursor_issue<true>(p, pf, 0, 0);
         cursor_next(pf, p, npairs, rank);
       }
       while (ld.tile < p.total_tiles) {
@@ -535,11 +561,11 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
           ptx::mbar_arrive_expect_tx(full_bar(stage), ld.bytes_pair);
           armed_parity[stage] = static_cast<int>(phase);
         }
-        cursor_issue<false>(ld, smem_base + stage * kStageBytes, ptx::map_to_cta(full_bar(stage), 0));
+        cursor_issue<false>(p, ld, smem_base + stage * kStageBytes, ptx::map_to_cta(full_bar(stage), 0));
         issued = true;
         cursor_next(ld, p, npairs, rank);
         if (kPrefetchKBlocks > 0 && pf.tile < p.total_tiles) {
-          cursor_issue<true>(pf, 0, 0);
+          cursor_issue<true>(p, pf, 0, 0);
           cursor_next(pf, p, npairs, rank);
         }
         if (++stage == kStages) {

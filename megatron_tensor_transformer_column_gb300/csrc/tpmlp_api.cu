@@ -33,6 +33,7 @@ struct tpmlp_plan {
   tpmlp_dtype dtype;
   uint64_t timeout_ns;
   int32_t stall_injection;
+  std::vector<int64_t> stripe_rows;  // sequence-parallel token stripes (empty: not set)
 };
 
 namespace {
@@ -138,6 +139,11 @@ int encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int6
 }
 
 // ------------------------------------------------------------------ problem lists
+// Stand-ins passed for an operand (or out0) that is the launch's striped
+// input (output) in the sequence-parallel layout; never dereferenced.
+const void* const kStripedIn = reinterpret_cast<const void*>(uintptr_t{16});
+void* const kStripedOut = reinterpret_cast<void*>(uintptr_t{32});
+
 struct Builder {
   GemmParams* p;
   bool tc;  // tensor-core path (tensor maps) or fp32 SIMT path
@@ -153,6 +159,61 @@ struct Builder {
     std::memset(static_cast<void*>(p), 0, sizeof(GemmParams));
     tile_m = tc ? kTileM : kSimtTile;
     p->tile_m = tile_m;
+  }
+
+  // Sequence-parallel layout: this launch's token-striped input (X or dY,
+  // in_cols wide) and output (Y or dX, out_cols wide), stripes as the plan set.
+  int stripe_map_base[3] = {-1, -1, -1};  // input K-major, input MN-major, output
+  void set_stripes(const tpmlp_plan* pl, const void* const* in, int64_t in_cols, void* const* out,
+                   int64_t out_cols) {
+    Stripes& st = p->stripes;
+    st.num = static_cast<int32_t>(pl->stripe_rows.size());
+    st.row0[0] = 0;
+    for (int j = 0; j < st.num; ++j) {
+      st.row0[j + 1] = st.row0[j] + pl->stripe_rows[j];
+      st.in[j] = in ? in[j] : nullptr;
+      st.out[j] = out ? out[j] : nullptr;
+    }
+    st.in_ld = in_cols;
+    st.out_ld = out_cols;
+  }
+
+  // num consecutive maps, one per stripe (an empty stripe reuses a non-empty
+  // stripe's map: no box ever selects it).
+  int stripe_maps(bool output, int box_rows) {
+    if (!tc) return -1;
+    const int slot = output ? 2 : (box_rows == 128 ? 0 : 1);
+    if (stripe_map_base[slot] >= 0) return stripe_map_base[slot];
+    const Stripes& st = p->stripes;
+    int ref = 0;
+    while (ref < st.num && st.row0[ref + 1] == st.row0[ref]) ++ref;
+    if (ref == st.num || p->num_maps + st.num > kMaxMaps) {
+      map_error = true;
+      fail(TPMLP_ERR_INVALID_ARG, ref == st.num ? "every stripe is empty" : "more than %d tensor maps in one launch",
+           kMaxMaps);
+      return 0;
+    }
+    const int base = p->num_maps;
+    for (int j = 0; j < st.num; ++j) {
+      const int jj = st.row0[j + 1] > st.row0[j] ? j : ref;
+      const void* ptr = output ? st.out[jj] : st.in[jj];
+      const int64_t cols = output ? st.out_ld : st.in_ld;
+      const int idx = p->num_maps++;
+      const int r = encode_map(&p->maps[idx], ptr, st.row0[jj + 1] - st.row0[jj], cols, cols,
+                               output ? kOutputMap : box_rows);
+      if (r != 0) {
+        map_error = true;
+        fail(TPMLP_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for stripe %d", r, j);
+      }
+      // keep the dedupe tables aligned with the map array (never matched: null pointer)
+      map_ptr.push_back(nullptr);
+      map_rows.push_back(0);
+      map_cols.push_back(0);
+      map_box.push_back(0);
+      map_ld.push_back(0);
+    }
+    stripe_map_base[slot] = base;
+    return base;
   }
 
   int map(const void* ptr, int64_t rows, int64_t cols, int box_rows, int64_t ld = -1) {
@@ -205,6 +266,7 @@ struct Builder {
     P.b_major = b_major;
     P.epi = epi;
     P.out_map[0] = P.out_map[1] = P.out_map[2] = -1;
+    P.out_striped = 0;
     P.ldo = ldo;
     Group& G = p->groups[cur_group];
     G.num_probs++;
@@ -222,8 +284,12 @@ struct Builder {
     S.ldb = b_cols;
     const int a_box = P.a_major == MAJOR_K ? 128 : kTcBK;
     const int b_box = P.b_major == MAJOR_K ? 128 : kTcBK;
-    S.a_map = map(a, a_rows, a_cols, a_box);
-    S.b_map = map(b, b_rows, b_cols, b_box);
+    S.a_striped = a == kStripedIn ? 1 : 0;
+    S.b_striped = b == kStripedIn ? 1 : 0;
+    if (S.a_striped) S.a = nullptr;
+    if (S.b_striped) S.b = nullptr;
+    S.a_map = S.a_striped ? stripe_maps(false, a_box) : map(a, a_rows, a_cols, a_box);
+    S.b_map = S.b_striped ? stripe_maps(false, b_box) : map(b, b_rows, b_cols, b_box);
     S.b2_map = b2 ? map(b2, b_rows, b_cols, b_box) : -1;
     S.K = static_cast<int32_t>(K);
     P.seg_count++;
@@ -253,6 +319,14 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
                     cudaStream_t stream) {
   GemmParams& p = *B.p;
   if (p.total_tiles == 0) return TPMLP_OK;
+  for (int i = 0; i < p.num_probs; ++i) {  // token-striped output (sequence-parallel layout)
+    Prob& P = p.probs[i];
+    if (P.out0 == kStripedOut) {
+      P.out0 = nullptr;
+      P.out_striped = 1;
+      P.out_map[0] = B.stripe_maps(true, kOutputMap);
+    }
+  }
   if (B.tc) {  // the tensor-core epilogue writes every output with TMA stores
     for (int i = 0; i < p.num_probs; ++i) {
       Prob& P = p.probs[i];
@@ -324,6 +398,14 @@ struct ColsumBuilder {
   ColsumParams p{};
   int strip_cols;
   explicit ColsumBuilder(bool bf16) : strip_cols(colsum_strip_cols(bf16)) {}
+  void set_stripes(const tpmlp_plan* pl, const void* const* src) {
+    p.num_stripes = static_cast<int32_t>(pl->stripe_rows.size());
+    p.stripe_row0[0] = 0;
+    for (int j = 0; j < p.num_stripes; ++j) {
+      p.stripe_row0[j + 1] = p.stripe_row0[j] + pl->stripe_rows[j];
+      p.stripe_src[j] = src[j];
+    }
+  }
   void add(const void* src, void* dst, int64_t rows, int64_t cols) {
     ColsumJob& J = p.jobs[p.num_jobs++];
     J.src = src;
@@ -346,11 +428,15 @@ tpmlp_status launch_colsums(const ColsumBuilder& C, const tpmlp_plan* pl, cudaSt
 // ------------------------------------------------------------------ phases
 tpmlp_status fwd_column(const tpmlp_plan* pl, const DeviceInfo& di, const void* X, const void* const* W1,
                         const void* const* W3, const void* const* b1, const void* const* b3, void* const* saved,
-                        void* const* H, void* ws, cudaStream_t st) {
+                        void* const* H, void* ws, cudaStream_t st, const void* const* X_stripes = nullptr) {
   if (pl->T == 0) return TPMLP_OK;
   const bool tc = pl->dtype == TPMLP_BF16;
   const bool sw = swiglu(pl);
   Builder B(scratch_params(), tc);
+  if (X_stripes) {  // all-gather of the X stripes: every shard reads all of them
+    B.set_stripes(pl, X_stripes, pl->d, nullptr, 0);
+    X = kStripedIn;
+  }
   B.begin_group(pl->T, band_for(di.sms));
   for (int i = 0; i < pl->t; ++i) {
     const int64_t di_ = pl->d_i[i];
@@ -367,9 +453,13 @@ tpmlp_status fwd_column(const tpmlp_plan* pl, const DeviceInfo& di, const void* 
 }
 
 tpmlp_status fwd_row(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* W2, const void* b2, void* Y,
-                     void* const* H, void* ws, cudaStream_t st) {
+                     void* const* H, void* ws, cudaStream_t st, void* const* Y_stripes = nullptr) {
   if (pl->T == 0) return TPMLP_OK;
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
+  if (Y_stripes) {  // reduce-scatter: the summed rows of stripe j go to Y_j
+    B.set_stripes(pl, nullptr, 0, Y_stripes, pl->d);
+    Y = kStripedOut;
+  }
   B.begin_group(pl->T, band_for(di.sms));
   Prob& P = B.add_prob(pl->T, pl->d, 256, MAJOR_K, MAJOR_MN, EPI_STORE, pl->d);
   P.out0 = Y;
@@ -384,7 +474,8 @@ tpmlp_status fwd_row(const tpmlp_plan* pl, const DeviceInfo& di, const void* con
 // and dW2 moves to the f-sum launch (bwd_fsum's dW2 problems).
 tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* W2,
                        const void* const* saved, const void* const* H, const void* dY, void* const* dact,
-                       void* const* dW2, void* db2, void* ws, cudaStream_t st, bool recompute = false) {
+                       void* const* dW2, void* db2, void* ws, cudaStream_t st, bool recompute = false,
+                       const void* const* dY_stripes = nullptr) {
   const bool sw = swiglu(pl);
   if (pl->T == 0) {
     const size_t es = pl->dtype == TPMLP_BF16 ? 2 : 4;
@@ -400,6 +491,11 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
   }
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
   const int band = band_for(di.sms);
+  const void* dY_dense = dY;
+  if (dY_stripes) {  // all-gather of the dY stripes (backward of the reduce-scatter)
+    B.set_stripes(pl, dY_stripes, pl->d, nullptr, 0);
+    dY = kStripedIn;
+  }
   // dW2_i = H_i^T dY (K = T: the long tiles go first)
   for (int i = 0; i < pl->t && !recompute; ++i) {
     const int64_t di_ = pl->d_i[i];
@@ -425,7 +521,8 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
   TPMLP_TRY(launch(B, TAG_BWD_DGRAD, di, pl, ws, st));
   if (db2) {  // g backward is the identity: b2's gradient is that of Y
     ColsumBuilder C(pl->dtype == TPMLP_BF16);
-    C.add(dY, db2, pl->T, pl->d);
+    if (dY_stripes) C.set_stripes(pl, dY_stripes);
+    C.add(dY_stripes ? nullptr : dY_dense, db2, pl->T, pl->d);
     TPMLP_TRY(launch_colsums(C, pl, st));
   }
   return TPMLP_OK;
@@ -434,7 +531,8 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
 tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X, const void* const* W1,
                       const void* const* W3, const void* const* dact, void* dX, void* const* dW1,
                       void* const* dW3, void* const* db1, void* const* db3, void* ws, cudaStream_t st,
-                      const void* const* H_for_dW2 = nullptr, const void* dY = nullptr, void* const* dW2 = nullptr) {
+                      const void* const* H_for_dW2 = nullptr, const void* dY = nullptr, void* const* dW2 = nullptr,
+                      const void* const* X_stripes = nullptr, void* const* dX_stripes = nullptr) {
   const bool sw = swiglu(pl);
   if (pl->T == 0) {
     const size_t es = pl->dtype == TPMLP_BF16 ? 2 : 4;
@@ -451,6 +549,11 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
   }
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
   const int band = band_for(di.sms);
+  if (X_stripes || dX_stripes) {  // X gathered from its stripes; dX reduce-scattered into stripes
+    B.set_stripes(pl, X_stripes, pl->d, dX_stripes, pl->d);
+    if (X_stripes) X = kStripedIn;
+    if (dX_stripes) dX = kStripedOut;
+  }
   if (H_for_dW2) {  // recompute mode: dW2_i = H_i^T dY from the H the dgrad launch rewrote
     for (int i = 0; i < pl->t; ++i) {
       const int64_t di_ = pl->d_i[i];
@@ -1001,6 +1104,97 @@ tpmlp_status tpmlp_attn_qkv_backward(const tpmlp_plan* plan, const void* X, cons
   return attn_qkv_bwd(plan, di, X, Wqkv, dQKV, dX, dWqkv, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
+tpmlp_status tpmlp_plan_set_sequence_stripes(tpmlp_plan* plan, int32_t nstripes, const int64_t* stripe_rows) {
+  g_last_error[0] = 0;
+  if (!plan) return fail(TPMLP_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->kind != PLAN_MLP) return fail(TPMLP_ERR_INVALID_ARG, "sequence stripes apply to MLP plans");
+  if (!stripe_rows) return fail(TPMLP_ERR_INVALID_ARG, "stripe_rows is NULL");
+  if (nstripes < 1 || nstripes > TPMLP_MAX_SHARDS)
+    return fail(TPMLP_ERR_SHAPE, "need 1 <= nstripes <= %d (got %d)", TPMLP_MAX_SHARDS, nstripes);
+  int64_t r = 0;
+  for (int j = 0; j < nstripes; ++j) {
+    if (stripe_rows[j] < 0) return fail(TPMLP_ERR_SHAPE, "stripe %d has %lld rows", j, (long long)stripe_rows[j]);
+    if (j > 0 && r % 128)
+      return fail(TPMLP_ERR_ALIGNMENT, "stripe %d starts at row %lld, not a multiple of 128", j, (long long)r);
+    r += stripe_rows[j];
+  }
+  if (r != plan->T)
+    return fail(TPMLP_ERR_SHAPE, "the stripes hold %lld rows, the plan %lld tokens", (long long)r, (long long)plan->T);
+  plan->stripe_rows.assign(stripe_rows, stripe_rows + nstripes);
+  return TPMLP_OK;
+}
+
+// Stripe pointer arrays: one entry per stripe; entries of non-empty stripes
+// non-NULL and 16-byte aligned (empty stripes may be NULL).
+tpmlp_status check_stripes(const char* name, const void* const* arr, const tpmlp_plan* pl) {
+  if (pl->stripe_rows.empty())
+    return fail(TPMLP_ERR_INVALID_ARG, "no sequence stripes set (tpmlp_plan_set_sequence_stripes)");
+  if (!arr) return fail(TPMLP_ERR_INVALID_ARG, "stripe array %s is NULL", name);
+  for (size_t j = 0; j < pl->stripe_rows.size(); ++j) {
+    if (pl->stripe_rows[j] == 0) continue;
+    if (!arr[j]) return fail(TPMLP_ERR_INVALID_ARG, "%s[%zu] is NULL", name, j);
+    if (!aligned16(arr[j])) return fail(TPMLP_ERR_ALIGNMENT, "%s[%zu] (%p) is not 16-byte aligned", name, j, arr[j]);
+  }
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_forward_sp(const tpmlp_plan* plan, const void* const* X_stripes, const void* const* W1,
+                              const void* const* W3, const void* const* W2, const void* const* b1,
+                              const void* const* b3, const void* b2, void* const* Y_stripes, void* const* saved,
+                              void* const* H, void* workspace, tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_stripes("X_stripes", X_stripes, plan));
+  TPMLP_TRY(check_stripes("Y_stripes", Y_stripes, plan));
+  TPMLP_TRY(check_array("W1", W1, plan->t, false));
+  if (swiglu(plan)) TPMLP_TRY(check_array("W3", W3, plan->t, false));
+  TPMLP_TRY(check_array("W2", W2, plan->t, false));
+  TPMLP_TRY(check_array("saved", saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array("H", H, plan->t, tz));
+  TPMLP_TRY(check_bias("b1", b1, plan->t));
+  if (swiglu(plan)) TPMLP_TRY(check_bias("b3", b3, plan->t));
+  TPMLP_TRY(check_ptr("b2", b2, true));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  TPMLP_TRY(fwd_column(plan, di, nullptr, W1, W3, b1, swiglu(plan) ? b3 : nullptr, saved, H, workspace, st,
+                       X_stripes));
+  return fwd_row(plan, di, W2, b2, nullptr, H, workspace, st, Y_stripes);
+}
+
+tpmlp_status tpmlp_backward_sp(const tpmlp_plan* plan, const void* const* X_stripes, const void* const* W1,
+                               const void* const* W3, const void* const* W2, const void* const* saved,
+                               const void* const* H, const void* const* dY_stripes, void* const* dact,
+                               void* const* dX_stripes, void* const* dW1, void* const* dW3, void* const* dW2,
+                               void* const* db1, void* const* db3, void* db2, void* workspace,
+                               tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  DeviceInfo di;
+  TPMLP_TRY(common_checks(plan, workspace, &di));
+  const bool tz = plan->T == 0;
+  TPMLP_TRY(check_stripes("X_stripes", X_stripes, plan));
+  TPMLP_TRY(check_stripes("dY_stripes", dY_stripes, plan));
+  TPMLP_TRY(check_stripes("dX_stripes", dX_stripes, plan));
+  TPMLP_TRY(check_array("W1", W1, plan->t, false));
+  TPMLP_TRY(check_array("W2", W2, plan->t, false));
+  if (swiglu(plan)) {
+    TPMLP_TRY(check_array("W3", W3, plan->t, false));
+    TPMLP_TRY(check_array("dW3", dW3, plan->t, false));
+  }
+  TPMLP_TRY(check_array("saved", saved, nsaved(plan), tz));
+  TPMLP_TRY(check_array("H", H, plan->t, tz));
+  TPMLP_TRY(check_array("dact", dact, nsaved(plan), tz));
+  TPMLP_TRY(check_array("dW1", dW1, plan->t, false));
+  TPMLP_TRY(check_array("dW2", dW2, plan->t, false));
+  TPMLP_TRY(check_bias("db1", db1, plan->t));
+  if (swiglu(plan)) TPMLP_TRY(check_bias("db3", db3, plan->t));
+  TPMLP_TRY(check_ptr("db2", db2, true));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  TPMLP_TRY(bwd_dgrad(plan, di, W2, saved, H, nullptr, dact, dW2, db2, workspace, st, false, dY_stripes));
+  return bwd_fsum(plan, di, nullptr, W1, W3, dact, nullptr, dW1, dW3, db1, swiglu(plan) ? db3 : nullptr, workspace,
+                  st, nullptr, nullptr, nullptr, X_stripes, dX_stripes);
+}
+
 tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpmlp_stream_t stream) {
   if (!plan || !workspace) return TPMLP_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -1033,7 +1227,7 @@ const char* tpmlp_status_string(tpmlp_status s) {
 
 int tpmlp_last_cuda_error(void) { return g_last_cuda_error; }
 const char* tpmlp_last_error(void) { return g_last_error; }
-int tpmlp_version(void) { return 102; }
+int tpmlp_version(void) { return 103; }
 int tpmlp_last_launch_count(void) { return g_last_launches; }
 
 }  // extern "C"

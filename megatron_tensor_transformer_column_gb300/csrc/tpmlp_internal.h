@@ -64,6 +64,11 @@ struct Seg {
   int32_t b_map;
   int32_t b2_map;
   int32_t K;
+  // Sequence-parallel layout: the operand is the launch's striped input
+  // (GemmParams::in_stripe), stored as token stripes; its map index is the
+  // first of num_stripes consecutive maps and its raw pointer is unused.
+  int32_t a_striped;
+  int32_t b_striped;
 };
 
 struct Prob {
@@ -74,7 +79,7 @@ struct Prob {
   int32_t a_major, b_major;
   int32_t epi;
   int32_t out_map[3];  // tensor maps of out0..out2 for TMA stores (-1: none)
-  int32_t pad_;
+  int32_t out_striped; // out0 is the launch's striped output (token stripes)
   int64_t ldo;       // row stride of out*/aux*, in elements
   void* out0;
   void* out1;
@@ -95,8 +100,23 @@ struct Group {
   int32_t tile_start;     // first global tile index of the group
 };
 
+// Token stripes of the sequence-parallel layout: stripe j holds rows
+// [row0[j], row0[j+1]) of a [T x cols] tensor in its own buffer.  Internal
+// boundaries are multiples of 128 rows, so no TMA box (128 rows of A, 128 K
+// rows of an MN-major operand, 32 rows of an output block) crosses one.
+constexpr int kMaxStripes = kMaxShards;
+struct Stripes {
+  int32_t num;                      // 0: the launch has no striped tensor
+  int32_t pad_;
+  int64_t row0[kMaxStripes + 1];
+  const void* in[kMaxStripes];      // striped input (X or dY), raw pointers (fp32 path)
+  void* out[kMaxStripes];           // striped output (Y or dX), raw pointers (fp32 path)
+  int64_t in_ld, out_ld;            // row strides of the stripes, in elements
+};
+
 struct GemmParams {
   CUtensorMap maps[kMaxMaps];
+  Stripes stripes;
   Prob probs[kMaxProbs];
   Group groups[kMaxGroups];
   Seg segs[kMaxSegs];
@@ -121,6 +141,11 @@ struct ColsumParams {
   ColsumJob jobs[kMaxColsumJobs];
   int32_t num_jobs;
   int32_t total_strips;
+  // A job whose src is null reads the stripes below as one [rows x cols]
+  // tensor (db2 of the sequence-parallel layout, from the dY stripes).
+  int32_t num_stripes;
+  int64_t stripe_row0[kMaxStripes + 1];
+  const void* stripe_src[kMaxStripes];
 };
 int colsum_strip_cols(bool bf16);
 cudaError_t launch_colsum(const ColsumParams& p, bool bf16, cudaStream_t stream);

@@ -47,7 +47,7 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert tp.tpmlp_version() == 102
+    assert tp.tpmlp_version() == 103
     for code, name in tp.STATUS.items():
         assert tp.tpmlp_status_string(code) == name
     assert tp.tpmlp_status_string(99) == "TPMLP_ERR_UNKNOWN"
@@ -152,3 +152,42 @@ def test_attn_no_cpu_fallback_without_gpu(lib):
         with pytest.raises(tp.TpmlpError) as e:
             call()
         assert e.value.status in (4, 5)
+
+
+@pytest.mark.parametrize("T,rows,status", [
+    (1000, [1000], 0),
+    (1000, [256, 744], 0),
+    (1000, [128, 0, 384, 488], 0),
+    (0, [0, 0], 0),
+    (1000, [500, 500], 3),     # the second stripe starts at 500, not a multiple of 128
+    (1000, [256, 700], 2),     # rows do not add up to T
+    (1000, [256, -1, 745], 2),
+    (1000, [], 2),
+    (1000, [64] * 17, 2),
+])
+def test_sequence_stripe_validation(lib, T, rows, status):
+    p = tp.Plan(T, 64, [64], "gelu", "bf16")
+    if status == 0:
+        tp.tpmlp_plan_set_sequence_stripes(p, rows)
+        assert p.stripe_rows == tuple(rows)
+    else:
+        with pytest.raises(tp.TpmlpError) as e:
+            tp.tpmlp_plan_set_sequence_stripes(p, rows)
+        assert e.value.status == status
+
+
+def test_sequence_stripes_refused_on_attention_plans(lib):
+    with pytest.raises(tp.TpmlpError) as e:
+        tp.tpmlp_plan_set_sequence_stripes(tp.AttnPlan(256, 64, [64], [64]), [256])
+    assert e.value.status == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_sp_no_cpu_fallback_without_gpu(lib):
+    p = tp.Plan(256, 64, [64], "gelu", "bf16")
+    tp.tpmlp_plan_set_sequence_stripes(p, [128, 128])
+    fake = 1 << 20
+    with pytest.raises(tp.TpmlpError) as e:
+        tp.tpmlp_forward_sp(p, [fake, fake], [fake], None, [fake], None, None, None, [fake, fake], [fake], [fake],
+                            fake, stream=0)
+    assert e.value.status in (4, 5)
