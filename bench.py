@@ -686,6 +686,136 @@ def run_ours_attn(args, w: si.AttnWorkload):
     return 0
 
 
+def run_ours_sp(args, w: si.Workload):
+    """The same step in the sequence-parallel layout: X and dY read from t token
+    stripes, Y and dX written as stripes (tpmlp_forward_sp / tpmlp_backward_sp)."""
+    import torch
+    import megatron_tensor_transformer_column_gb300 as tp
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tp.load()
+    if w.T % w.t or (w.T // w.t) % 128:
+        raise SystemExit(f"{w.name}: T/t must be a multiple of 128 tokens for the stripe layout")
+    rows = [w.T // w.t] * w.t
+    inp = si.make_workload_inputs(w)
+    sw = w.act == "swiglu"
+    mlp = tp.ShardedMLP(w.T, w.d, w.d_i, w.act, w.dtype, device=dev)
+    mlp.set_sequence_stripes(rows)
+    X_j = [x.contiguous().to(dev) for x in inp.X.split(rows)]
+    dY_j = [x.contiguous().to(dev) for x in inp.dY.split(rows)]
+    W1 = [x.to(dev) for x in inp.W1_i]
+    W2 = [x.to(dev) for x in inp.W2_i]
+    W3 = [x.to(dev) for x in inp.W3_i] if sw else None
+    Y_j = mlp.alloc_stripes()
+    dX_j = mlp.alloc_stripes()
+    _, saved, H = mlp.alloc_forward()
+    dact, _, dW1, dW3, dW2 = mlp.alloc_backward()
+    stream = torch.cuda.current_stream(dev)
+    plan, wsp = mlp.plan, mlp.workspace
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        tp.tpmlp_forward_sp(plan, X_j, W1, W3, W2, None, None, None, Y_j, saved, H, wsp, stream)
+        if ev:
+            ev[1].record(stream)
+        tp.tpmlp_backward_sp(plan, X_j, W1, W3, W2, saved, H, dY_j, dact, dX_j, dW1, dW3, dW2, None, None, None, wsp,
+                             stream)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    mlp.check(stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
+    barrier(ws)
+    mlp.check(stream)
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
+    per_phase = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
+                 for i, n in enumerate(["forward_sp", "backward_sp"])}
+    pf = phase_flops(w)
+    pflops = {"forward_sp": pf["fwd_column"] + pf["fwd_row"], "backward_sp": pf["bwd_dgrad"] + pf["bwd_fsum"]}
+    value = flops_fwd_bwd(w) * ws * args.steps / (elapsed_ms / 1e3) / 1e12
+
+    # end to end: the stripes and weights from pinned host memory, Y / dX / dW read back
+    pin = lambda t: t.contiguous().pin_memory()
+    hin = [pin(x) for x in inp.X.split(rows)] + [pin(x) for x in inp.dY.split(rows)] + \
+        [pin(x) for x in inp.W1_i + inp.W2_i + (inp.W3_i if sw else [])]
+    din = X_j + dY_j + W1 + W2 + (W3 or [])
+    douts = Y_j + dX_j + dW1 + dW2 + (dW3 or [])
+    houts = [torch.empty_like(o, device="cpu").pin_memory() for o in douts]
+
+    def e2e_step():
+        for d_, h_ in zip(din, hin):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip(houts, douts):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    n = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    e2e = {"value": flops_fwd_bwd(w) * ws * n / (ms / 1e3) / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in hin),
+           "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in houts), "steps": n,
+           "ms_per_step": ms / n, "api": "tpmlp_forward_sp + tpmlp_backward_sp, stripes from pinned host memory"}
+    peaks, peak_src = load_peaks()
+    dom = max(per_phase, key=per_phase.get)
+    achieved = pflops[dom] / (per_phase[dom] / 1e3) / 1e12
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {"bound": "tensor", "kernel": dom + " (two launches: dgrad + f-sum, or column + row)",
+                "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
+                "traffic": None,
+                "peak_note": f"{peak_src} sustained bf16; frac of {peak_src} burst {peak_burst}: "
+                             f"{achieved / peak_burst:.3f}"}
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) X/dY, N(0,0.02) W, rounded once to bf16)",
+        "config": workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)",
+                                      "layout": f"sequence-parallel: {w.t} token stripes of {rows[0]}"}),
+        "pct_of_peak": {"sustained": value / ws / peak_sus, "burst": value / ws / peak_burst, "source": peak_src},
+        "tokens_per_s": w.T * ws * args.steps / (elapsed_ms / 1e3),
+        "phase_ms": per_phase, "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
+        "gpu_launches": 4 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -697,6 +827,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bias", action="store_true", help="include the optional biases and their gradients")
     ap.add_argument("--recompute", action="store_true", help="backward recomputes H instead of reading it")
+    ap.add_argument("--sp", action="store_true",
+                    help="sequence-parallel layout: X, dY in and Y, dX out as t token stripes of T/t tokens")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.workload in si.ATTN_WORKLOADS:
@@ -705,6 +837,8 @@ def main(argv=None):
     w = si.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.sp:
+        return run_ours_sp(args, w)
     return run_ours(args, w)
 
 

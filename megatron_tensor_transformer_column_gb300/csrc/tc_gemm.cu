@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <mutex>
 
 #include "act.cuh"
@@ -213,6 +214,9 @@ struct Cursor {
   int tile, seg, seg_end, kb, kblocks;
   int a_major, b_major, dual;
   int a_striped, b_striped;  // operand read from the launch's token stripes
+  int a_sj, b_sj;            // its current stripe,
+  int a_y0, b_y0;            //   that stripe's first token row,
+  int a_next, b_next;        //   and the next stripe's (an MN-major K walk crosses it)
   int m0, n0;          // this CTA's first row of A and first column of B
   int nA, nB;          // boxes this CTA loads per operand
   uint32_t bytes_pair; // bytes both CTAs load per K block (counted on the even CTA)
@@ -227,6 +231,29 @@ __device__ __forceinline__ void cursor_segment(Cursor& c, const GemmParams& p) {
   c.mb2 = c.dual ? static_cast<const void*>(&p.maps[S.b2_map]) : nullptr;
   c.a_striped = S.a_striped;
   c.b_striped = S.b_striped;
+  // The stripe of the first box: K-major operands keep it for the whole
+  // segment (their token rows are this CTA's M or N rows); MN-major ones walk
+  // the tokens along K and move to the next stripe in cursor_next.
+  if (c.a_striped) {
+    const int j = stripe_of(p.stripes, c.a_major == MAJOR_MN ? 0 : c.m0);
+    c.a_sj = j;
+    c.a_y0 = static_cast<int>(p.stripes.row0[j]);
+    c.a_next = j + 1 < p.stripes.num ? static_cast<int>(p.stripes.row0[j + 1]) : INT_MAX;
+  }
+  if (c.b_striped) {
+    const int j = stripe_of(p.stripes, c.b_major == MAJOR_MN ? 0 : c.n0);
+    c.b_sj = j;
+    c.b_y0 = static_cast<int>(p.stripes.row0[j]);
+    c.b_next = j + 1 < p.stripes.num ? static_cast<int>(p.stripes.row0[j + 1]) : INT_MAX;
+  }
+}
+
+__device__ __forceinline__ void stripe_advance(const GemmParams& p, int k0, int& sj, int& y0, int& next) {
+  while (k0 >= next) {
+    ++sj;
+    y0 = next;
+    next = sj + 1 < p.stripes.num ? static_cast<int>(p.stripes.row0[sj + 1]) : INT_MAX;
+  }
 }
 
 __device__ __forceinline__ void cursor_tile(Cursor& c, const GemmParams& p, int tile, uint32_t rank) {
@@ -249,7 +276,11 @@ __device__ __forceinline__ void cursor_tile(Cursor& c, const GemmParams& p, int 
 }
 
 __device__ __forceinline__ void cursor_next(Cursor& c, const GemmParams& p, int npairs, uint32_t rank) {
-  if (++c.kb < c.kblocks) return;
+  if (++c.kb < c.kblocks) {
+    if (c.a_striped && c.a_major == MAJOR_MN) stripe_advance(p, c.kb * kBK, c.a_sj, c.a_y0, c.a_next);
+    if (c.b_striped && c.b_major == MAJOR_MN) stripe_advance(p, c.kb * kBK, c.b_sj, c.b_y0, c.b_next);
+    return;
+  }
   if (++c.seg < c.seg_end) {
     cursor_segment(c, p);
     return;
@@ -269,10 +300,9 @@ __device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor& 
     const int x = mn ? c.m0 + 64 * b : k0 + 64 * b;
     int y = mn ? k0 : c.m0;
     const CUtensorMap* ma = static_cast<const CUtensorMap*>(c.ma);
-    if (c.a_striped) {  // the stored rows are tokens: pick the stripe, make y stripe-local
-      const int j = stripe_of(p.stripes, y);
-      ma += j;
-      y -= static_cast<int>(p.stripes.row0[j]);
+    if (c.a_striped) {  // the stored rows are tokens: the stripe's map, stripe-local y
+      ma += c.a_sj;
+      y -= c.a_y0;
     }
     if (kPrefetch)
       ptx::tma_prefetch_2d(ma, x, y);
@@ -285,9 +315,8 @@ __device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor& 
     int y = mn ? k0 : c.n0;
     const CUtensorMap* mb = static_cast<const CUtensorMap*>(c.mb);
     if (c.b_striped) {
-      const int s = stripe_of(p.stripes, y);
-      mb += s;
-      y -= static_cast<int>(p.stripes.row0[s]);
+      mb += c.b_sj;
+      y -= c.b_y0;
     }
     if (kPrefetch)
       ptx::tma_prefetch_2d(mb, x, y);
@@ -361,15 +390,15 @@ struct EpiStore {
   uint32_t buf;  // this warp's two blocks
   uint32_t next;
   int rows;      // rows of the current problem's outputs
+  int sj, sy0;   // striped out0: the stripe of this warp's rows and its first row
 };
 
 __device__ __forceinline__ void store_block(EpiStore& es, const GemmParams& p, int map, int x, int y,
                                             const float (&v)[32], int lane, bool striped = false) {
   if (y >= es.rows) return;  // every row of this warp is past the end: no store starts out of range
   if (striped) {  // token stripes: the stripe's own map, stripe-local rows
-    const int j = stripe_of(p.stripes, y);
-    map += j;
-    y -= static_cast<int>(p.stripes.row0[j]);
+    map += es.sj;
+    y -= es.sy0;
   }
   const uint32_t b = es.buf + es.next * kEpiBlockBytes;
   if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last used block b has read it
@@ -485,6 +514,17 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& 
     default:
       break;
   }
+}
+
+// Whether a SwiGLU forward tile was computed with merged N = 256 MMAs: full
+// tiles (128 output columns, 64 per CTA of the pair).  Each CTA's B stage
+// holds 64 gate columns then 64 up columns (two MN-major blocks), so the
+// accumulator columns are, per CTA-half h of B (h = 0, 1): gate columns
+// 64 h .. 64 h + 63 of the tile at 128 h .. 128 h + 63, the matching up
+// columns at 128 h + 64 .. 128 h + 127.  Partial tiles use two MMAs of
+// N = 2 x 64-or-fewer columns: gate at 0 .., up at 128 ...
+__device__ __forceinline__ bool swiglu_merged(const TileInfo& ti, const Prob& P) {
+  return pair_shape(ti, true, P.a_major, P.b_major).n_mma == 128;
 }
 
 __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_raw) {
@@ -608,7 +648,11 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
         const bool dual = P.epi == EPI_SWIGLU_FWD;
         const int seg_begin = P.seg_begin, seg_end = P.seg_begin + P.seg_count;
         const PairShape ps = pair_shape(ti, dual, a_major, b_major);
-        const uint32_t idesc = ptx::make_idesc_bf16(kPairM, ps.n_mma, a_major, b_major);
+        // A full SwiGLU tile issues one N = 256 MMA over each CTA's [gate | up]
+        // column blocks instead of two N = 128 MMAs (the wider MMA runs at the
+        // full tensor rate, N = 128 at about 88 %); see swiglu_merged().
+        const bool merged = dual && ps.n_mma == 128;
+        const uint32_t idesc = ptx::make_idesc_bf16(kPairM, merged ? 256 : ps.n_mma, a_major, b_major);
         const uint64_t a_desc0 = a_major == MAJOR_MN ? a_mn_desc : a_k_desc;
         const uint64_t b_desc0 = b_major == MAJOR_MN ? b_mn_desc : b_k_desc;
         const bool a_mn = a_major == MAJOR_MN, b_mn = b_major == MAJOR_MN;
@@ -631,7 +675,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
             const uint64_t ad0 = a_desc0 + st;
             const uint64_t bd0 = b_desc0 + st;
             const int nk = min(kBK / 16, (K - k0 + 15) >> 4);
-            if (dual)
+            if (dual && !merged)
               issue_stage<true>(d_tmem, ad0, bd0, a_mn, b_mn, idesc, nk, accumulate);
             else
               issue_stage<false>(d_tmem, ad0, bd0, a_mn, b_mn, idesc, nk, accumulate);
@@ -660,7 +704,8 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;              // TMEM lane quarter this warp may read
     const int half = (warp - 2) >> 2;    // which half of the tile's columns
-    EpiStore es{smem_base + static_cast<uint32_t>(kStages * kStageBytes + (warp - 2) * 2 * kEpiBlockBytes), 0u, 0};
+    EpiStore es{smem_base + static_cast<uint32_t>(kStages * kStageBytes + (warp - 2) * 2 * kEpiBlockBytes), 0u, 0, 0,
+                0};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < p.total_tiles; tile += npairs) {
@@ -672,6 +717,10 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       const int64_t grow = static_cast<int64_t>(ti.m0) + kBM * static_cast<int>(rank) + row;
       const int wrow = ti.m0 + kBM * static_cast<int>(rank) + q * 32;  // this warp's first row
       es.rows = P.M;
+      if (P.out_striped && wrow < P.M) {  // a warp's 32 rows never cross a stripe boundary
+        es.sj = stripe_of(p.stripes, wrow);
+        es.sy0 = static_cast<int>(p.stripes.row0[es.sj]);
+      }
       if (row_ok && (P.epi == EPI_GELU_BWD || P.epi == EPI_SWIGLU_BWD)) {
         // Pull this thread's row of the saved pre-activation(s) into L2
         // while the accumulator is still being computed.
@@ -694,13 +743,18 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
       if (vm > 0) {
         if (P.epi == EPI_SWIGLU_FWD) {
+          const bool merged = swiglu_merged(ti, P);
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             const int col = half * 64 + c * 32;
             if (col >= ti.valid_n) break;
+            // output columns 64 half + 32 c ..: merged, gate at accumulator
+            // column 128 half + 32 c, up 64 further; split, gate at col, up at 128 + col
+            const uint32_t g_col = merged ? static_cast<uint32_t>(half * 128 + c * 32) : static_cast<uint32_t>(col);
+            const uint32_t u_col = merged ? g_col + 64u : 128u + static_cast<uint32_t>(col);
             uint32_t rg[32], ru[32];
-            ptx::tmem_ld_32x32b_x32(tacc + col, rg);
-            ptx::tmem_ld_32x32b_x32(tacc + 128u + col, ru);
+            ptx::tmem_ld_32x32b_x32(tacc + g_col, rg);
+            ptx::tmem_ld_32x32b_x32(tacc + u_col, ru);
             ptx::tmem_wait_ld();
             const int nvalid = min(32, ti.valid_n - col);
             float g[32], u[32], h[32];
