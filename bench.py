@@ -500,57 +500,100 @@ def run_ours(args, w: si.Workload):
     return 0
 
 
+class E2EPipeline:
+    """End-to-end steps through the public API with host buffers.
+
+    Every step copies its activations in from pinned host memory (H2D) and its
+    results back (D2H); the model's weights stay resident on the device (they
+    are state, not per-step input, and their gradients are consumed by the
+    optimizer on the device).  The copies run on a second stream into double
+    buffers: the inputs of step k+1 upload and the results of step k-1
+    download while step k computes, as a training loop's data loader would.
+    All of it is inside the timed region (CUDA events on the compute stream,
+    which waits for the last downloads at the end)."""
+
+    def __init__(self, dev, stream, host_in, host_out_like):
+        import torch
+        self.torch = torch
+        self.stream = stream
+        self.copy = torch.cuda.Stream(dev)
+        self.h_in = [x.contiguous().pin_memory() for x in host_in]
+        self.d_in = [[torch.empty_like(x, device=dev) for x in self.h_in] for _ in range(2)]
+        self.h_out = [torch.empty_like(o, device="cpu").pin_memory() for o in host_out_like]
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.out_ready = [torch.cuda.Event() for _ in range(2)]
+        self.in_free = [torch.cuda.Event() for _ in range(2)]
+        self.out_free = [torch.cuda.Event() for _ in range(2)]
+        self.h2d = sum(x.numel() * x.element_size() for x in self.h_in)
+        self.d2h = sum(x.numel() * x.element_size() for x in self.h_out)
+
+    def upload(self, slot):
+        with self.torch.cuda.stream(self.copy):
+            self.copy.wait_event(self.in_free[slot])
+            for d_, h_ in zip(self.d_in[slot], self.h_in):
+                d_.copy_(h_, non_blocking=True)
+            self.in_ready[slot].record(self.copy)
+
+    def run(self, n, compute):
+        """compute(inputs, slot) enqueues one step on the compute stream and
+        returns its device results."""
+        for e in self.in_free + self.out_free:
+            e.record(self.stream)
+        self.upload(0)
+        for k in range(n):
+            slot = k & 1
+            if k + 1 < n:
+                self.upload(slot ^ 1)
+            self.stream.wait_event(self.in_ready[slot])
+            self.stream.wait_event(self.out_free[slot])  # step k-2's results in this slot are read back
+            outs = compute(self.d_in[slot], slot)
+            self.in_free[slot].record(self.stream)
+            self.out_ready[slot].record(self.stream)
+            with self.torch.cuda.stream(self.copy):
+                self.copy.wait_event(self.out_ready[slot])
+                for h_, d_ in zip(self.h_out, outs):
+                    h_.copy_(d_, non_blocking=True)
+                self.out_free[slot].record(self.copy)
+        done = self.torch.cuda.Event()
+        done.record(self.copy)
+        self.stream.wait_event(done)
+
+
 def run_e2e(args, w, tp, mlp, inp, dev, stream, ws):
-    """Same metric through tpmlp_forward / tpmlp_backward with the inputs copied
-    from pinned host memory every step and the results (Y, dX, dW*) read back."""
+    """Same metric through tpmlp_forward / tpmlp_backward with X and dY copied in
+    from pinned host memory and Y and dX read back every step (E2EPipeline)."""
     import torch
     sw = w.act == "swiglu"
-    pin = lambda t: t.contiguous().pin_memory()
-    hX, hdY = pin(inp.X), pin(inp.dY)
-    hW1 = [pin(x) for x in inp.W1_i]
-    hW2 = [pin(x) for x in inp.W2_i]
-    hW3 = [pin(x) for x in inp.W3_i] if sw else []
-    dX_in = torch.empty_like(hX, device=dev)
-    ddY = torch.empty_like(hdY, device=dev)
-    dW1_in = [torch.empty_like(x, device=dev) for x in hW1]
-    dW2_in = [torch.empty_like(x, device=dev) for x in hW2]
-    dW3_in = [torch.empty_like(x, device=dev) for x in hW3]
-    Y, saved, H = mlp.alloc_forward()
-    dact, dX, dW1, dW3, dW2 = mlp.alloc_backward()
-    outs_dev = [Y, dX, *dW1, *dW2, *(dW3 or [])]
-    outs_host = [torch.empty_like(o, device="cpu").pin_memory() for o in outs_dev]
-    h2d = sum(x.numel() * x.element_size() for x in [hX, hdY, *hW1, *hW2, *hW3])
-    d2h = sum(x.numel() * x.element_size() for x in outs_host)
+    W1 = [x.to(dev) for x in inp.W1_i]
+    W2 = [x.to(dev) for x in inp.W2_i]
+    W3 = [x.to(dev) for x in inp.W3_i] if sw else None
+    bufs = [(mlp.alloc_forward(), mlp.alloc_backward()) for _ in range(2)]
+    pipe = E2EPipeline(dev, stream, [inp.X, inp.dY], [bufs[0][0][0], bufs[0][1][1]])
 
-    def step():
-        dX_in.copy_(hX, non_blocking=True)
-        ddY.copy_(hdY, non_blocking=True)
-        for d_, h_ in zip(dW1_in + dW2_in + dW3_in, hW1 + hW2 + hW3):
-            d_.copy_(h_, non_blocking=True)
-        tp.tpmlp_forward(mlp.plan, dX_in, dW1_in, dW3_in if sw else None, dW2_in, None, None, None, Y, saved, H,
-                         mlp.workspace, stream)
-        tp.tpmlp_backward(mlp.plan, dX_in, dW1_in, dW3_in if sw else None, dW2_in, saved, H, ddY, dact, dX, dW1,
-                          dW3, dW2, None, None, None, mlp.workspace, stream)
-        for h_, d_ in zip(outs_host, outs_dev):
-            h_.copy_(d_, non_blocking=True)
+    def compute(d_in, slot):
+        X, dY = d_in
+        (Y, saved, H), (dact, dX, dW1, dW3, dW2) = bufs[slot]
+        tp.tpmlp_forward(mlp.plan, X, W1, W3, W2, None, None, None, Y, saved, H, mlp.workspace, stream)
+        tp.tpmlp_backward(mlp.plan, X, W1, W3, W2, saved, H, dY, dact, dX, dW1, dW3, dW2, None, None, None,
+                          mlp.workspace, stream)
+        return [Y, dX]
 
-    for _ in range(2):
-        step()
+    pipe.run(2, compute)
     torch.cuda.synchronize(dev)
     n = max(3, min(args.steps, 20))
     barrier(ws)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(n):
-        step()
+    pipe.run(n, compute)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     mlp.check(stream)
-    return {"value": flops_fwd_bwd(w) * ws * n / (ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
-            "api": "tpmlp_forward + tpmlp_backward, inputs from pinned host memory"}
+    return {"value": flops_fwd_bwd(w) * ws * n / (ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": pipe.h2d,
+            "d2h_bytes_per_step": pipe.d2h, "steps": n, "ms_per_step": ms / n,
+            "api": "tpmlp_forward + tpmlp_backward; X and dY uploaded from pinned host memory and Y, dX read back "
+                   "every step on a copy stream overlapped with the previous/next step; weights resident"}
 
 
 def run_ours_attn(args, w: si.AttnWorkload):
@@ -622,37 +665,39 @@ def run_ours_attn(args, w: si.AttnWorkload):
     step_flops = sum(pf.values())
     value = step_flops * ws * args.steps / (elapsed_ms / 1e3) / 1e12
 
-    # ---- end to end: every input from pinned host memory, every output read back
-    pin = lambda t: t.contiguous().pin_memory()
-    hin = [pin(a.X), pin(a.dZ), *[pin(x) for x in a.Wqkv_i + a.O_i + a.WO_i + a.dQKV_i]]
-    din = [X, dZ, *Wqkv, *O, *WO, *dQKV]
-    douts = [*QKV, Z, *dO, *dWO, dX, *dWqkv]
-    houts = [torch.empty_like(o, device="cpu").pin_memory() for o in douts]
+    # ---- end to end: the per-step activations (X, the attention core's O, dZ
+    # and dQKV) uploaded and the results (QKV, Z, dO, dX) read back every step,
+    # overlapped with compute; weights and their gradients stay on the device
+    outs2 = [([torch.empty_like(x) for x in QKV], torch.empty_like(Z), [torch.empty_like(x) for x in dO],
+              torch.empty_like(dX)) for _ in range(2)]
+    pipe = E2EPipeline(dev, stream, [a.X, a.dZ, *a.O_i, *a.dQKV_i], [*QKV, Z, *dO, dX])
+    nsh = w.t
 
-    def e2e_step():
-        for d_, h_ in zip(din, hin):
-            d_.copy_(h_, non_blocking=True)
-        step()
-        for h_, d_ in zip(houts, douts):
-            h_.copy_(d_, non_blocking=True)
+    def compute(d_in, slot):
+        Xs, dZs = d_in[0], d_in[1]
+        Os, dQKVs = d_in[2:2 + nsh], d_in[2 + nsh:]
+        QKVs, Zs, dOs, dXs = outs2[slot]
+        tp.tpmlp_attn_qkv_forward(plan, Xs, Wqkv, QKVs, wsp, stream)
+        tp.tpmlp_attn_out_forward(plan, WO, Os, Zs, wsp, stream)
+        tp.tpmlp_attn_out_backward(plan, WO, Os, dZs, dOs, dWO, wsp, stream)
+        tp.tpmlp_attn_qkv_backward(plan, Xs, Wqkv, dQKVs, dXs, dWqkv, wsp, stream)
+        return [*QKVs, Zs, *dOs, dXs]
 
-    for _ in range(2):
-        e2e_step()
+    pipe.run(2, compute)
     torch.cuda.synchronize(dev)
     n = max(3, min(args.steps, 20))
     barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(n):
-        e2e_step()
+    pipe.run(n, compute)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     m.check(stream)
-    e2e = {"value": step_flops * ws * n / (ms / 1e3) / 1e12, "unit": UNIT,
-           "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in hin),
-           "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in houts), "steps": n, "ms_per_step": ms / n,
-           "api": "tpmlp_attn_* (four calls), inputs from pinned host memory, every output read back"}
+    e2e = {"value": step_flops * ws * n / (ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": pipe.h2d,
+           "d2h_bytes_per_step": pipe.d2h, "steps": n, "ms_per_step": ms / n,
+           "api": "tpmlp_attn_* (four calls); X, O, dZ, dQKV uploaded from pinned host memory and QKV, Z, dO, dX "
+                  "read back every step on a copy stream overlapped with compute; weights resident"}
 
     peaks, peak_src = load_peaks()
     dom = max(per_phase, key=per_phase.get)
@@ -756,36 +801,35 @@ def run_ours_sp(args, w: si.Workload):
     pflops = {"forward_sp": pf["fwd_column"] + pf["fwd_row"], "backward_sp": pf["bwd_dgrad"] + pf["bwd_fsum"]}
     value = flops_fwd_bwd(w) * ws * args.steps / (elapsed_ms / 1e3) / 1e12
 
-    # end to end: the stripes and weights from pinned host memory, Y / dX / dW read back
-    pin = lambda t: t.contiguous().pin_memory()
-    hin = [pin(x) for x in inp.X.split(rows)] + [pin(x) for x in inp.dY.split(rows)] + \
-        [pin(x) for x in inp.W1_i + inp.W2_i + (inp.W3_i if sw else [])]
-    din = X_j + dY_j + W1 + W2 + (W3 or [])
-    douts = Y_j + dX_j + dW1 + dW2 + (dW3 or [])
-    houts = [torch.empty_like(o, device="cpu").pin_memory() for o in douts]
+    # end to end: the X and dY stripes uploaded and the Y and dX stripes read
+    # back every step, overlapped with compute; weights stay on the device
+    outs2 = [(mlp.alloc_stripes(), mlp.alloc_stripes()) for _ in range(2)]
+    pipe = E2EPipeline(dev, stream, [*inp.X.split(rows), *inp.dY.split(rows)], [*Y_j, *dX_j])
+    ns = len(rows)
 
-    def e2e_step():
-        for d_, h_ in zip(din, hin):
-            d_.copy_(h_, non_blocking=True)
-        step()
-        for h_, d_ in zip(houts, douts):
-            h_.copy_(d_, non_blocking=True)
+    def compute(d_in, slot):
+        Xs, dYs = d_in[:ns], d_in[ns:]
+        Ys, dXs = outs2[slot]
+        tp.tpmlp_forward_sp(plan, Xs, W1, W3, W2, None, None, None, Ys, saved, H, wsp, stream)
+        tp.tpmlp_backward_sp(plan, Xs, W1, W3, W2, saved, H, dYs, dact, dXs, dW1, dW3, dW2, None, None, None, wsp,
+                             stream)
+        return [*Ys, *dXs]
 
-    for _ in range(2):
-        e2e_step()
+    pipe.run(2, compute)
     torch.cuda.synchronize(dev)
     n = max(3, min(args.steps, 20))
+    barrier(ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(n):
-        e2e_step()
+    pipe.run(n, compute)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
-    e2e = {"value": flops_fwd_bwd(w) * ws * n / (ms / 1e3) / 1e12, "unit": UNIT,
-           "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in hin),
-           "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in houts), "steps": n,
-           "ms_per_step": ms / n, "api": "tpmlp_forward_sp + tpmlp_backward_sp, stripes from pinned host memory"}
+    mlp.check(stream)
+    e2e = {"value": flops_fwd_bwd(w) * ws * n / (ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": pipe.h2d,
+           "d2h_bytes_per_step": pipe.d2h, "steps": n, "ms_per_step": ms / n,
+           "api": "tpmlp_forward_sp + tpmlp_backward_sp; X and dY stripes uploaded from pinned host memory and Y, "
+                  "dX stripes read back every step on a copy stream overlapped with compute; weights resident"}
     peaks, peak_src = load_peaks()
     dom = max(per_phase, key=per_phase.get)
     achieved = pflops[dom] / (per_phase[dom] / 1e3) / 1e12
