@@ -86,11 +86,12 @@ def test_config_C1_fp32(gpu_lib):
 
 # ------------------------------------------------------------- full-size workloads (sampled)
 
-def _sampled_compare(tp, w: si.Workload, nrows=24, nunits=24, seed=1234):
+def _sampled_compare(tp, w: si.Workload, nrows=24, nunits=24, seed=1234, extra_rows=()):
     inp = si.make_workload_inputs(w, seed)
     g = run_gpu(tp, inp, w.act, w.dtype)
     rng = np.random.default_rng(7)
-    rows = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, nrows, replace=False)]))
+    rows = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, nrows, replace=False),
+                                     np.asarray(extra_rows, dtype=np.int64)]))
     units = np.unique(np.concatenate([[0, w.dff - 1], rng.choice(w.dff, nunits, replace=False)]))
     # include the first and last unit of every shard (shard boundaries)
     for lo, hi in si.shard_slices(w.d_i):
@@ -135,3 +136,14 @@ def test_C2_shard_count_invariance(gpu_lib):
         for k in outs[1]:
             e = rel_err(outs[b][k], outs[a][k])
             assert e <= 2e-2, f"t={a} vs t={b}: {k} differs by {e}"
+
+
+def test_tensors_beyond_2_pow_31_elements(gpu_lib):
+    """T = 2^21 + 96 tokens (ragged against the 256-row tiles) with one shard
+    of 1536: A, H and dA hold 3.2e9 elements each, so element offsets pass
+    2^31 (32-bit index arithmetic anywhere would show up).  Sampled rows include
+    those where the offset into A / H / dA crosses 2^31."""
+    w = si.Workload("large gelu bf16 T=2^21+96 d=256 t=1x1536", 2 ** 21 + 96, 256, (1536,), "gelu", "bf16")
+    cross = (2 ** 31) // 1536
+    _sampled_compare(gpu_lib, w, nrows=12, nunits=12, extra_rows=(cross - 1, cross, cross + 1, 2 ** 21 + 95))
+    torch.cuda.empty_cache()
