@@ -341,30 +341,53 @@ __device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor& 
 // on GB300, against 128 cycles of tensor work for a 256 x 256 x 16 pair
 // MMA), so every choice -- SwiGLU or not, full or partial stage -- is made
 // once, before the sequence.
-template <bool kDual>
-__device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t ad0, uint64_t bd0, bool a_mn, bool b_mn,
-                                            uint32_t idesc, int nk, uint32_t& accumulate) {
+template <bool kDual, bool kAmn, bool kBmn>
+__device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint32_t a_lo0, uint32_t a_hi, uint32_t b_lo0,
+                                            uint32_t b_hi, uint32_t idesc, int nk, uint32_t& accumulate) {
   if (nk == kBK / 16) {
 #pragma unroll
     for (int j = 0; j < kBK / 16; ++j) {
-      const uint64_t koff = static_cast<uint64_t>(((j >> 2) * kKBoxBytes + (j & 3) * 32) >> 4);
-      const uint64_t moff = static_cast<uint64_t>((j * 2048) >> 4);
-      const uint64_t ad = ad0 + (a_mn ? moff : koff);
-      const uint64_t bd = bd0 + (b_mn ? moff : koff);
-      ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
-      if (kDual) ptx::mma_bf16_pair(d_tmem + 128u, ad, bd + (kMNBoxBytes >> 4), idesc, accumulate);
-      accumulate = 1;
+      constexpr uint32_t kBoxOff = kMNBoxBytes >> 4;
+      const uint32_t koff = static_cast<uint32_t>(((j >> 2) * kKBoxBytes + (j & 3) * 32) >> 4);
+      const uint32_t moff = static_cast<uint32_t>((j * 2048) >> 4);
+      const uint32_t al = a_lo0 + (kAmn ? moff : koff);
+      const uint32_t bl = b_lo0 + (kBmn ? moff : koff);
+      if (j == 0) {
+        ptx::mma_bf16_pair_lohi(d_tmem, al, a_hi, bl, b_hi, idesc, accumulate);
+        if (kDual) ptx::mma_bf16_pair_lohi(d_tmem + 128u, al, a_hi, bl + kBoxOff, b_hi, idesc, accumulate);
+      } else {
+        ptx::mma_bf16_pair_lohi_acc(d_tmem, al, a_hi, bl, b_hi, idesc);
+        if (kDual) ptx::mma_bf16_pair_lohi_acc(d_tmem + 128u, al, a_hi, bl + kBoxOff, b_hi, idesc);
+      }
     }
+    accumulate = 1;
     return;
   }
   for (int j = 0; j < nk; ++j) {  // the last, partial stage of a segment
-    const uint64_t koff = static_cast<uint64_t>(((j >> 2) * kKBoxBytes + (j & 3) * 32) >> 4);
-    const uint64_t moff = static_cast<uint64_t>((j * 2048) >> 4);
-    const uint64_t ad = ad0 + (a_mn ? moff : koff);
-    const uint64_t bd = bd0 + (b_mn ? moff : koff);
-    ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
-    if (kDual) ptx::mma_bf16_pair(d_tmem + 128u, ad, bd + (kMNBoxBytes >> 4), idesc, accumulate);
+    const uint32_t koff = static_cast<uint32_t>(((j >> 2) * kKBoxBytes + (j & 3) * 32) >> 4);
+    const uint32_t moff = static_cast<uint32_t>((j * 2048) >> 4);
+    const uint32_t al = a_lo0 + (kAmn ? moff : koff);
+    const uint32_t bl = b_lo0 + (kBmn ? moff : koff);
+    ptx::mma_bf16_pair_lohi(d_tmem, al, a_hi, bl, b_hi, idesc, accumulate);
+    if (kDual) ptx::mma_bf16_pair_lohi(d_tmem + 128u, al, a_hi, bl + (kMNBoxBytes >> 4), b_hi, idesc, accumulate);
     accumulate = 1;
+  }
+}
+
+// One stage's MMAs, with every choice (SwiGLU split pair, operand majors)
+// resolved by a single switch ahead of the straight-line sequence.
+__device__ __forceinline__ void issue_stage_any(int kind, uint32_t d_tmem, uint32_t a_lo0, uint32_t a_hi,
+                                                uint32_t b_lo0, uint32_t b_hi, uint32_t idesc, int nk,
+                                                uint32_t& accumulate) {
+  switch (kind) {
+    case 0: issue_stage<false, false, false>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
+    case 1: issue_stage<false, false, true>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
+    case 2: issue_stage<false, true, false>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
+    case 3: issue_stage<false, true, true>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
+    case 4: issue_stage<true, false, false>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
+    case 5: issue_stage<true, false, true>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
+    case 6: issue_stage<true, true, false>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
+    default: issue_stage<true, true, true>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
   }
 }
 
@@ -655,7 +678,9 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
         const uint32_t idesc = ptx::make_idesc_bf16(kPairM, merged ? 256 : ps.n_mma, a_major, b_major);
         const uint64_t a_desc0 = a_major == MAJOR_MN ? a_mn_desc : a_k_desc;
         const uint64_t b_desc0 = b_major == MAJOR_MN ? b_mn_desc : b_k_desc;
-        const bool a_mn = a_major == MAJOR_MN, b_mn = b_major == MAJOR_MN;
+        const uint32_t a_lo = static_cast<uint32_t>(a_desc0), a_hi = static_cast<uint32_t>(a_desc0 >> 32);
+        const uint32_t b_lo = static_cast<uint32_t>(b_desc0), b_hi = static_cast<uint32_t>(b_desc0 >> 32);
+        const int kind = (dual && !merged ? 4 : 0) | (a_major == MAJOR_MN ? 2 : 0) | (b_major == MAJOR_MN ? 1 : 0);
         if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, ctl, kDevTimeoutMma)) {
           ok = false;
           break;
@@ -671,14 +696,9 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
               break;
             }
             ptx::tc_fence_after();
-            const uint64_t st = static_cast<uint64_t>((stage * kStageBytes) >> 4);
-            const uint64_t ad0 = a_desc0 + st;
-            const uint64_t bd0 = b_desc0 + st;
+            const uint32_t st = static_cast<uint32_t>((stage * kStageBytes) >> 4);
             const int nk = min(kBK / 16, (K - k0 + 15) >> 4);
-            if (dual && !merged)
-              issue_stage<true>(d_tmem, ad0, bd0, a_mn, b_mn, idesc, nk, accumulate);
-            else
-              issue_stage<false>(d_tmem, ad0, bd0, a_mn, b_mn, idesc, nk, accumulate);
+            issue_stage_any(kind, d_tmem, a_lo + st, a_hi, b_lo + st, b_hi, idesc, nk, accumulate);
             issued = true;
             ptx::mma_commit_pair_mc(empty_bar(stage), kPairMask);  // stage free in both CTAs
             if (++stage == kStages) {
