@@ -7,6 +7,8 @@
 // listing (silu on the W1 projection, times the W3 projection).
 #pragma once
 
+#include <stdint.h>
+
 namespace tpmlp {
 namespace act {
 
@@ -71,6 +73,135 @@ __device__ __forceinline__ void swiglu_grads_fast(float dh, float g, float u, fl
   du = dh * (g * s);
   dg = dh * u * (s + g * s * (1.0f - s));
 }
+
+// ---- packed forms for the tensor-core epilogue: two elements per fp32x2
+// instruction (fma/mul/add.rn.f32x2).  Same approximations and constants as
+// the scalar fast forms above, regrouped so that every step but the two
+// special-function calls (reciprocal, exponential) acts on a pair:
+//   q = Phi(-|a|) = 0.5 * poly(t) * exp(-a^2/2), t = 1 / (1 + p |a|);
+//   GeLU(a) = a Phi(a) = max(a, 0) - |a| q;
+//   Phi(a) = 0.5 + copysign(0.5 - q, a),  GeLU'(a) = Phi(a) + a phi(a).
+namespace x2 {
+
+__device__ __forceinline__ uint64_t pk(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t splat(float a) { return pk(a, a); }
+
+// q = Phi(-|a|) and e = exp(-a^2/2) for a pair; nx = -|a|.
+__device__ __forceinline__ void norm_q(uint64_t a, uint64_t& nx, uint64_t& q, uint64_t& e) {
+  constexpr float p = 0.3275911f * kInvSqrt2;
+  // Abramowitz & Stegun 7.1.26 coefficients, halved: q = 0.5 * poly * e
+  constexpr float c1 = 0.5f * 0.254829592f, c2 = 0.5f * -0.284496736f, c3 = 0.5f * 1.421413741f,
+                  c4 = 0.5f * -1.453152027f, c5 = 0.5f * 1.061405429f;
+  float a0, a1;
+  upk(a, a0, a1);
+  nx = pk(-fabsf(a0), -fabsf(a1));
+  const uint64_t den = fma2(splat(-p), nx, splat(1.0f));  // 1 + p |a|
+  float d0, d1;
+  upk(den, d0, d1);
+  const uint64_t t = pk(__fdividef(1.0f, d0), __fdividef(1.0f, d1));
+  uint64_t poly = fma2(t, splat(c5), splat(c4));
+  poly = fma2(t, poly, splat(c3));
+  poly = fma2(t, poly, splat(c2));
+  poly = fma2(t, poly, splat(c1));
+  poly = mul2(t, poly);
+  const uint64_t arg = mul2(mul2(a, a), splat(-0.5f));
+  float g0, g1;
+  upk(arg, g0, g1);
+  e = pk(__expf(g0), __expf(g1));
+  q = mul2(poly, e);
+}
+
+// h = GeLU(a) for v[0..31] in place.
+__device__ __forceinline__ void gelu_x32(float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const uint64_t a = pk(v[j], v[j + 1]);
+    uint64_t nx, q, e;
+    norm_q(a, nx, q, e);
+    const uint64_t h = fma2(nx, q, pk(fmaxf(v[j], 0.0f), fmaxf(v[j + 1], 0.0f)));
+    upk(h, v[j], v[j + 1]);
+  }
+}
+
+// dA = dH * GeLU'(A): acc holds dH, a holds A on entry and dA on exit; with
+// h non-null, h receives GeLU(A) as well.
+template <bool kWithH>
+__device__ __forceinline__ void gelu_bwd_x32(const float (&acc)[32], float (&a)[32], float (&h)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const uint64_t av = pk(a[j], a[j + 1]);
+    uint64_t nx, q, e;
+    norm_q(av, nx, q, e);
+    float m0, m1;
+    upk(fma2(q, splat(-1.0f), splat(0.5f)), m0, m1);  // 0.5 - q, then its sign from a
+    const uint64_t cdf = add2(splat(0.5f), pk(copysignf(m0, a[j]), copysignf(m1, a[j + 1])));
+    const uint64_t grad = fma2(av, mul2(e, splat(kInvSqrt2Pi)), cdf);
+    if (kWithH) {
+      const uint64_t hv = fma2(nx, q, pk(fmaxf(a[j], 0.0f), fmaxf(a[j + 1], 0.0f)));
+      upk(hv, h[j], h[j + 1]);
+    }
+    upk(mul2(pk(acc[j], acc[j + 1]), grad), a[j], a[j + 1]);
+  }
+}
+
+// s = sigmoid(g) for a pair.
+__device__ __forceinline__ uint64_t sigmoid2(float g0, float g1) {
+  const uint64_t den = add2(splat(1.0f), pk(__expf(-g0), __expf(-g1)));
+  float d0, d1;
+  upk(den, d0, d1);
+  return pk(__fdividef(1.0f, d0), __fdividef(1.0f, d1));
+}
+
+// h = u * Swish(g) for 32 pairs of (g, u).
+__device__ __forceinline__ void swiglu_x32(const float (&g)[32], const float (&u)[32], float (&h)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const uint64_t gv = pk(g[j], g[j + 1]);
+    const uint64_t s = sigmoid2(g[j], g[j + 1]);
+    upk(mul2(pk(u[j], u[j + 1]), mul2(gv, s)), h[j], h[j + 1]);
+  }
+}
+
+// dG = dH * U * Swish'(G), dU = dH * Swish(G); g, u hold G, U on entry and
+// dG, dU on exit; with kWithH, h receives U * Swish(G).
+template <bool kWithH>
+__device__ __forceinline__ void swiglu_bwd_x32(const float (&acc)[32], float (&g)[32], float (&u)[32],
+                                               float (&h)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const uint64_t gv = pk(g[j], g[j + 1]), uv = pk(u[j], u[j + 1]), dh = pk(acc[j], acc[j + 1]);
+    const uint64_t s = sigmoid2(g[j], g[j + 1]);
+    const uint64_t gs = mul2(gv, s);                                      // Swish(G)
+    if (kWithH) upk(mul2(uv, gs), h[j], h[j + 1]);
+    const uint64_t ds = fma2(gs, fma2(s, splat(-1.0f), splat(1.0f)), s);  // s + g s (1 - s)
+    upk(mul2(mul2(dh, uv), ds), g[j], g[j + 1]);
+    upk(mul2(dh, gs), u[j], u[j + 1]);
+  }
+}
+
+}  // namespace x2
 
 }  // namespace act
 }  // namespace tpmlp

@@ -488,10 +488,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& 
     case EPI_GELU_FWD: {
       add_bias32(P.aux0, x, nvalid, acc);
       store_block(es, p, P.out_map[0], x, y, acc, lane);  // A (pre-activation)
-      float h[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) h[j] = act::gelu_fast(acc[j]);
-      store_block(es, p, P.out_map[1], x, y, h, lane);
+      act::x2::gelu_x32(acc);
+      store_block(es, p, P.out_map[1], x, y, acc, lane);
       break;
     }
     case EPI_GELU_BWD: {
@@ -499,16 +497,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& 
       load_row32(P.aux0, P.ldo, grow, x, nload, a);
       if (P.out1) {  // recompute H = GeLU(A) for the weight gradient of W2
         float h[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const act::NormTerms n = act::norm_terms_fast(a[j]);
-          h[j] = a[j] * n.cdf;
-          a[j] = acc[j] * fmaf(a[j] * act::kInvSqrt2Pi, n.e, n.cdf);
-        }
+        act::x2::gelu_bwd_x32<true>(acc, a, h);
         store_block(es, p, P.out_map[1], x, y, h, lane);
       } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) a[j] = acc[j] * act::gelu_grad_fast(a[j]);
+        act::x2::gelu_bwd_x32<false>(acc, a, acc);
       }
       store_block(es, p, P.out_map[0], x, y, a, lane);
       break;
@@ -519,16 +511,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& 
       load_row32(P.aux1, P.ldo, grow, x, nload, u);
       if (P.out2) {  // recompute H = U * Swish(G) for the weight gradient of W2
         float h[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) h[j] = u[j] * act::swish_fast(g[j]);
+        act::x2::swiglu_bwd_x32<true>(acc, g, u, h);
         store_block(es, p, P.out_map[2], x, y, h, lane);
-      }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float dg, du;
-        act::swiglu_grads_fast(acc[j], g[j], u[j], dg, du);
-        g[j] = dg;
-        u[j] = du;
+      } else {
+        act::x2::swiglu_bwd_x32<false>(acc, g, u, acc);
       }
       store_block(es, p, P.out_map[0], x, y, g, lane);
       store_block(es, p, P.out_map[1], x, y, u, lane);
@@ -785,8 +771,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
             }
             add_bias32(P.aux0, ti.n0 + col, nvalid, g);
             add_bias32(P.aux1, ti.n0 + col, nvalid, u);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) h[j] = u[j] * act::swish_fast(g[j]);
+            act::x2::swiglu_x32(g, u, h);
             store_block(es, p, P.out_map[0], ti.n0 + col, wrow, g, lane);
             store_block(es, p, P.out_map[1], ti.n0 + col, wrow, u, lane);
             store_block(es, p, P.out_map[2], ti.n0 + col, wrow, h, lane);
