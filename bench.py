@@ -506,17 +506,19 @@ class E2EPipeline:
     Every step copies its activations in from pinned host memory (H2D) and its
     results back (D2H); the model's weights stay resident on the device (they
     are state, not per-step input, and their gradients are consumed by the
-    optimizer on the device).  The copies run on a second stream into double
-    buffers: the inputs of step k+1 upload and the results of step k-1
-    download while step k computes, as a training loop's data loader would.
-    All of it is inside the timed region (CUDA events on the compute stream,
-    which waits for the last downloads at the end)."""
+    optimizer on the device).  The copies run on two more streams (uploads,
+    downloads: one copy engine each) into double buffers: the inputs of step
+    k+1 upload and the results of step k-1 download while step k computes, as
+    a training loop's data loader would.  All of it is inside the timed region
+    (CUDA events on the compute stream, which waits for the last downloads at
+    the end)."""
 
     def __init__(self, dev, stream, host_in, host_out_like):
         import torch
         self.torch = torch
         self.stream = stream
-        self.copy = torch.cuda.Stream(dev)
+        self.copy = torch.cuda.Stream(dev)  # uploads
+        self.down = torch.cuda.Stream(dev)  # downloads
         self.h_in = [x.contiguous().pin_memory() for x in host_in]
         self.d_in = [[torch.empty_like(x, device=dev) for x in self.h_in] for _ in range(2)]
         self.h_out = [torch.empty_like(o, device="cpu").pin_memory() for o in host_out_like]
@@ -549,13 +551,13 @@ class E2EPipeline:
             outs = compute(self.d_in[slot], slot)
             self.in_free[slot].record(self.stream)
             self.out_ready[slot].record(self.stream)
-            with self.torch.cuda.stream(self.copy):
-                self.copy.wait_event(self.out_ready[slot])
+            with self.torch.cuda.stream(self.down):
+                self.down.wait_event(self.out_ready[slot])
                 for h_, d_ in zip(self.h_out, outs):
                     h_.copy_(d_, non_blocking=True)
-                self.out_free[slot].record(self.copy)
+                self.out_free[slot].record(self.down)
         done = self.torch.cuda.Event()
-        done.record(self.copy)
+        done.record(self.down)
         self.stream.wait_event(done)
 
 
@@ -593,7 +595,7 @@ def run_e2e(args, w, tp, mlp, inp, dev, stream, ws):
     return {"value": flops_fwd_bwd(w) * ws * n / (ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": pipe.h2d,
             "d2h_bytes_per_step": pipe.d2h, "steps": n, "ms_per_step": ms / n,
             "api": "tpmlp_forward + tpmlp_backward; X and dY uploaded from pinned host memory and Y, dX read back "
-                   "every step on a copy stream overlapped with the previous/next step; weights resident"}
+                   "every step on copy streams overlapped with the previous/next step; weights resident"}
 
 
 def run_ours_attn(args, w: si.AttnWorkload):
@@ -697,7 +699,7 @@ def run_ours_attn(args, w: si.AttnWorkload):
     e2e = {"value": step_flops * ws * n / (ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": pipe.h2d,
            "d2h_bytes_per_step": pipe.d2h, "steps": n, "ms_per_step": ms / n,
            "api": "tpmlp_attn_* (four calls); X, O, dZ, dQKV uploaded from pinned host memory and QKV, Z, dO, dX "
-                  "read back every step on a copy stream overlapped with compute; weights resident"}
+                  "read back every step on copy streams overlapped with compute; weights resident"}
 
     peaks, peak_src = load_peaks()
     dom = max(per_phase, key=per_phase.get)
@@ -829,7 +831,7 @@ def run_ours_sp(args, w: si.Workload):
     e2e = {"value": flops_fwd_bwd(w) * ws * n / (ms / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": pipe.h2d,
            "d2h_bytes_per_step": pipe.d2h, "steps": n, "ms_per_step": ms / n,
            "api": "tpmlp_forward_sp + tpmlp_backward_sp; X and dY stripes uploaded from pinned host memory and Y, "
-                  "dX stripes read back every step on a copy stream overlapped with compute; weights resident"}
+                  "dX stripes read back every step on copy streams overlapped with compute; weights resident"}
     peaks, peak_src = load_peaks()
     dom = max(per_phase, key=per_phase.get)
     achieved = pflops[dom] / (per_phase[dom] / 1e3) / 1e12
