@@ -42,6 +42,7 @@ import synthetic_inputs as si  # noqa: E402
 METRIC = "TP-sharded MLP fwd+bwd TFLOP/s on 1 GB300 (% of dense BF16 peak)"
 ATTN_METRIC = "TP-sharded attention projections fwd+bwd TFLOP/s on 1 GB300 (% of dense BF16 peak)"
 UNIT = "TFLOP/s"
+STREAM_K_MODES = {"off": 0, "auto": 1, "always": 2}
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -79,7 +80,8 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = ("tc_gemm.cu", "ptx.cuh", "act.cuh", "tpmlp_internal.h", "tpmlp_api.cu")
+KERNEL_SOURCES = ("tc_gemm.cu", "tc_gemm_sk.cu", "tc_gemm_common.cuh", "ptx.cuh", "act.cuh", "tpmlp_internal.h",
+                  "tpmlp_api.cu")
 
 
 def kernel_sources_sha256() -> str:
@@ -371,6 +373,7 @@ def run_ours(args, w: si.Workload):
     inp = si.make_workload_inputs(w)
     td = si.torch_dtype(w.dtype)
     mlp = tp.ShardedMLP(w.T, w.d, w.d_i, w.act, w.dtype, device=dev)
+    tp.tpmlp_plan_set_stream_k(mlp.plan, STREAM_K_MODES[args.stream_k])
     sw = w.act == "swiglu"
     X = inp.X.to(dev)
     dY = inp.dY.to(dev)
@@ -479,7 +482,7 @@ def run_ours(args, w: si.Workload):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) X/dY, N(0,0.02) W, rounded once to bf16)",
-        "config": workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)",
+        "config": workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)", "stream_k": args.stream_k,
                                       **({"bias": "b1/b3 before the activation, b2 after the g-sum, with db"}
                                          if args.bias else {}),
                                       **({"recompute": "backward recomputes H from the saved pre-activations"}
@@ -614,6 +617,7 @@ def run_ours_attn(args, w: si.AttnWorkload):
 
     a = si.make_attn_workload_inputs(w)
     m = tp.ShardedAttentionProj(w.T, w.d, w.dq_i, w.dkv_i, w.dtype, device=dev)
+    tp.tpmlp_plan_set_stream_k(m.plan, STREAM_K_MODES[args.stream_k])
     X, dZ = a.X.to(dev), a.dZ.to(dev)
     Wqkv = [x.to(dev) for x in a.Wqkv_i]
     O = [x.to(dev) for x in a.O_i]
@@ -720,7 +724,7 @@ def run_ours_attn(args, w: si.AttnWorkload):
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) X/O/dZ/dQKV, N(0,0.02) W, rounded once to bf16)",
-        "config": attn_workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)"}),
+        "config": attn_workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)", "stream_k": args.stream_k}),
         "pct_of_peak": {"sustained": value / ws / peak_sus, "burst": value / ws / peak_burst, "source": peak_src},
         "tokens_per_s": w.T * ws * args.steps / (elapsed_ms / 1e3),
         "phase_ms": per_phase, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
@@ -754,6 +758,7 @@ def run_ours_sp(args, w: si.Workload):
     inp = si.make_workload_inputs(w)
     sw = w.act == "swiglu"
     mlp = tp.ShardedMLP(w.T, w.d, w.d_i, w.act, w.dtype, device=dev)
+    tp.tpmlp_plan_set_stream_k(mlp.plan, STREAM_K_MODES[args.stream_k])
     mlp.set_sequence_stripes(rows)
     X_j = [x.contiguous().to(dev) for x in inp.X.split(rows)]
     dY_j = [x.contiguous().to(dev) for x in inp.dY.split(rows)]
@@ -848,7 +853,7 @@ def run_ours_sp(args, w: si.Workload):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) X/dY, N(0,0.02) W, rounded once to bf16)",
-        "config": workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)",
+        "config": workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)", "stream_k": args.stream_k,
                                       "layout": f"sequence-parallel: {w.t} token stripes of {rows[0]}"}),
         "pct_of_peak": {"sustained": value / ws / peak_sus, "burst": value / ws / peak_burst, "source": peak_src},
         "tokens_per_s": w.T * ws * args.steps / (elapsed_ms / 1e3),
@@ -873,6 +878,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bias", action="store_true", help="include the optional biases and their gradients")
     ap.add_argument("--recompute", action="store_true", help="backward recomputes H instead of reading it")
+    ap.add_argument("--stream-k", choices=sorted(STREAM_K_MODES), default="auto",
+                    help="stream-K tail of the launches (auto: where it shortens the busiest pair's work)")
     ap.add_argument("--sp", action="store_true",
                     help="sequence-parallel layout: X, dY in and Y, dX out as t token stripes of T/t tokens")
     args = ap.parse_args(argv)

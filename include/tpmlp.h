@@ -43,7 +43,9 @@
  *     kernels) records TPMLP_ERR_DEVICE_TIMEOUT in the workspace's status
  *     word instead of hanging; tpmlp_check() reads and clears it.
  *   - Outputs are overwritten, never accumulated into.  Results are
- *     deterministic: every reduction has a fixed order, with no atomics.
+ *     deterministic: every reduction has a fixed order, with no atomics
+ *     on data (see tpmlp_plan_set_stream_k for the one dependence on the
+ *     device's SM count).
  *   - Thread safety: a plan is immutable after creation and may be used from
  *     several threads; calls that share a workspace must be ordered on the
  *     device (same stream or events).
@@ -102,9 +104,12 @@ TPMLP_API tpmlp_status tpmlp_plan_create(const tpmlp_desc* desc, tpmlp_plan** ou
 /* Free a plan (NULL is a no-op). */
 TPMLP_API void tpmlp_plan_destroy(tpmlp_plan* plan);
 
-/* Bytes of device workspace every call needs: a 256-byte block holding the
- * device status word.  The caller allocates it once, zero-filled, and passes
- * it to every call of this plan.                                              */
+/* Bytes of device workspace every call needs.  fp32 plans: a 256-byte block
+ * holding the device status word.  bf16 plans: that block, then the flags and
+ * fp32 partial accumulators of the stream-K tail (8 KB + 80 x 256 KB, about
+ * 21 MB; see tpmlp_plan_set_stream_k).  The caller allocates it once,
+ * zero-filled, and passes it to every call of this plan; calls that share it
+ * must be ordered on the device.                                             */
 TPMLP_API size_t tpmlp_workspace_size(const tpmlp_plan* plan);
 
 /* Forward.  Inputs X [T x d]; W1[i], W3[i] (SwiGLU only; pass NULL for GeLU)
@@ -188,8 +193,9 @@ TPMLP_API tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* con
  * reports the kernel's status itself (TPMLP_ERR_DEVICE_TIMEOUT if a bounded
  * wait expired), so it blocks until its kernel has finished.  All calls on a
  * device share the array: calls that overlap on the GPU (other streams, other
- * host threads) race on the status word.  A plan whose scratch would exceed
- * the array is rejected with TPMLP_ERR_UNSUPPORTED.                          */
+ * host threads) race on the status word.  It never uses the stream-K tail
+ * (whose flags and partial sums need the full workspace), so its results are
+ * those of tpmlp_forward_row with TPMLP_STREAM_K_OFF.                       */
 TPMLP_API tpmlp_status tpmlp_forward_row_noalloc(const tpmlp_plan* plan, const void* const* W2, void* const* H,
                                                  void* Y, tpmlp_stream_t stream);
 
@@ -324,6 +330,30 @@ TPMLP_API tpmlp_status tpmlp_attn_qkv_backward(const tpmlp_plan* plan, const voi
 TPMLP_API tpmlp_status tpmlp_plan_set_timeout(tpmlp_plan* plan, uint32_t timeout_ms);
 TPMLP_API tpmlp_status tpmlp_plan_set_stall_injection(tpmlp_plan* plan, int enable);
 
+/* Stream-K tail of the bf16 (tensor-core) launches.  A launch deals its 256 x
+ * 256 tiles to the resident CTA pairs round robin; when the tile count is
+ * not a multiple of the pairs, the last wave leaves pairs idle.  With the
+ * tail, each of the last wave's R tiles is split along K into k parts run by
+ * k pairs (k <= pairs / R).  The pair holding a tile's first K block
+ * finishes it: it adds the other parts' fp32 accumulators (left in the
+ * workspace) in a fixed order, so results stay deterministic for a given
+ * device, but differ in rounding from the unsplit K sum (within the fp32
+ * accumulation bound) and depend on the pair count, i.e. on the device's SM
+ * count.
+ *   TPMLP_STREAM_K_AUTO (default): per launch, only when the full waves load
+ *     every pair equally, the last wave's tiles have equal depth, and the
+ *     split shortens a pair's work by at least 2 % and 16 K blocks of 128,
+ *     after charging each extra part its read-back;
+ *   TPMLP_STREAM_K_ALWAYS: on every launch whose last wave has at most
+ *     pairs / 2 tiles, with as many parts as fit (tests);
+ *   TPMLP_STREAM_K_OFF: plain round robin.
+ * tpmlp_forward_row_noalloc never uses it.  Not while another call uses the
+ * plan.                                                                      */
+#define TPMLP_STREAM_K_OFF 0
+#define TPMLP_STREAM_K_AUTO 1
+#define TPMLP_STREAM_K_ALWAYS 2
+TPMLP_API tpmlp_status tpmlp_plan_set_stream_k(tpmlp_plan* plan, int mode);
+
 /* Synchronise the stream, read the workspace's status word and clear it.
  * Returns TPMLP_OK, TPMLP_ERR_DEVICE_TIMEOUT, or TPMLP_ERR_CUDA.               */
 TPMLP_API tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpmlp_stream_t stream);
@@ -337,7 +367,8 @@ TPMLP_API int tpmlp_last_cuda_error(void);
  * thread, valid until the next call on the same thread.                      */
 TPMLP_API const char* tpmlp_last_error(void);
 /* ABI version: 100 * major + minor (1.01: optional biases; 1.02: attention
- * projections; 1.03: sequence-parallel layout). */
+ * projections; 1.03: sequence-parallel layout; 1.04: stream-K tail, larger
+ * bf16 workspace). */
 TPMLP_API int tpmlp_version(void);
 
 /* Kernel launches the last compute call (tpmlp_forward, tpmlp_backward, a

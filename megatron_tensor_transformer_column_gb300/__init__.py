@@ -24,7 +24,8 @@ from . import _build
 
 __all__ = [
     "TpmlpError", "load", "Plan", "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size",
-    "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection",
+    "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection", "tpmlp_plan_set_stream_k",
+    "STREAM_K_OFF", "STREAM_K_AUTO", "STREAM_K_ALWAYS",
     "tpmlp_forward", "tpmlp_backward", "tpmlp_backward_recompute", "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad",
     "tpmlp_backward_fsum", "tpmlp_check", "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version",
     "tpmlp_last_launch_count", "tpmlp_last_error", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
@@ -47,7 +48,7 @@ EXPORTED_SYMBOLS = (
     "tpmlp_last_launch_count", "tpmlp_last_error", "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection",
     "tpmlp_backward_recompute", "tpmlp_attn_plan_create", "tpmlp_attn_qkv_forward", "tpmlp_attn_out_forward",
     "tpmlp_attn_out_backward", "tpmlp_attn_qkv_backward", "tpmlp_plan_set_sequence_stripes", "tpmlp_forward_sp",
-    "tpmlp_backward_sp",
+    "tpmlp_backward_sp", "tpmlp_plan_set_stream_k",
 )
 
 
@@ -101,6 +102,8 @@ def load():
         lib.tpmlp_plan_set_timeout.restype = st
         lib.tpmlp_plan_set_stall_injection.argtypes = [vp, ctypes.c_int]
         lib.tpmlp_plan_set_stall_injection.restype = st
+        lib.tpmlp_plan_set_stream_k.argtypes = [vp, ctypes.c_int]
+        lib.tpmlp_plan_set_stream_k.restype = st
         lib.tpmlp_workspace_size.argtypes = [vp]
         lib.tpmlp_workspace_size.restype = ctypes.c_size_t
         lib.tpmlp_forward.argtypes = [vp, vp, pp, pp, pp, pp, pp, vp, vp, pp, pp, vp, vp]
@@ -303,6 +306,14 @@ def tpmlp_plan_set_timeout(plan: Plan, timeout_ms: int):
 
 def tpmlp_plan_set_stall_injection(plan: Plan, enable: bool):
     _ok(load().tpmlp_plan_set_stall_injection(plan.handle, 1 if enable else 0), "tpmlp_plan_set_stall_injection")
+
+
+STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_ALWAYS = 0, 1, 2
+
+
+def tpmlp_plan_set_stream_k(plan: Plan, mode: int):
+    """Stream-K tail of the bf16 launches: STREAM_K_AUTO (default), _ALWAYS or _OFF."""
+    _ok(load().tpmlp_plan_set_stream_k(plan.handle, int(mode)), "tpmlp_plan_set_stream_k")
 
 
 def tpmlp_workspace_size(plan: Plan) -> int:

@@ -29,180 +29,20 @@
 // Method / FFN: the partial-sum identity [H1, H2][W21; W22] = H1 W21 + H2 W22
 // and the f/g table.)
 //
+// This file holds the data-parallel variant: pair q computes tiles q,
+// q + pairs, q + 2 pairs, ...  tc_gemm_sk.cu holds the variant with a
+// stream-K tail for the last, partial wave; both share tc_gemm_common.cuh.
+//
 // Every wait is bounded: after GemmParams::timeout_ns a waiting role records
 // a status code in the workspace, raises the abort flag of both CTAs, which
 // makes the other roles leave their loops, waits (again bounded) for its own
 // copies and MMAs in flight, and the pair frees its TMEM and exits.
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-
-#include <climits>
 #include <mutex>
 
-#include "act.cuh"
-#include "ptx.cuh"
-#include "tpmlp_internal.h"
+#include "tc_gemm_common.cuh"
 
 namespace tpmlp {
 namespace {
-
-constexpr int kBM = 128;                        // rows of A / D per CTA
-constexpr int kPairM = 2 * kBM;                 // rows of a pair's tile
-// A stage holds, per CTA, a 128 x kBK slice of A and of its half of B, each
-// as 128-byte-swizzled rows.  A K-major slice is kBK/64 boxes of 128 rows x
-// 64 K; an MN-major one is two boxes of 64 MN columns x kBK K rows.
-constexpr int kBK = kTcBK;                      // K per stage
-constexpr int kRowBytes = 128;                  // one swizzle row: 64 bf16
-constexpr int kKBoxBytes = 128 * kRowBytes;     // K-major box: 128 rows x 64 K (16 KB)
-constexpr int kMNBoxBytes = kBK * kRowBytes;    // MN-major box: kBK K rows x 64 MN
-constexpr int kOperandBytes = 128 * kBK * 2;    // one operand slice per stage
-constexpr int kStageBytes = 2 * kOperandBytes;  // A + B
-constexpr int kStages = (224 * 1024) / kStageBytes;
-static_assert(kBK % 64 == 0, "stage depth is a whole number of 64-wide boxes");
-static_assert(kOperandBytes == (kBK / 64) * kKBoxBytes && kOperandBytes == 2 * kMNBoxBytes, "stage layout");
-constexpr int kNumEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kNumEpiWarps);
-constexpr int kTmemCols = 512;
-constexpr int kAccCols = 256;
-constexpr int kNumAcc = 2;
-constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1;
-// Epilogue staging: each epilogue warp owns two 32 x 32 bf16 blocks (its 32
-// TMEM lanes x 32 columns), written row by row with a 64-byte swizzle and
-// stored by TMA while the other block is being filled.
-constexpr int kEpiBlockBytes = 32 * 32 * 2;
-constexpr int kEpiBytes = kNumEpiWarps * 2 * kEpiBlockBytes;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + 8 * kNumBars + 16;
-constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
-constexpr uint64_t kPeerDrainNs = 2ull * 1000 * 1000;
-constexpr uint16_t kPairMask = 0x3;
-// K blocks between the L2 prefetch of a block and its load into the ring:
-// the ring holds about 3,500 MMA cycles, less than a miss to HBM under load,
-// so loads are made to hit L2 instead.
-#ifndef TPMLP_PREFETCH_KBLOCKS
-#define TPMLP_PREFETCH_KBLOCKS 0
-#endif
-constexpr int kPrefetchKBlocks = TPMLP_PREFETCH_KBLOCKS;
-
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(kNumAcc * kAccCols <= kTmemCols, "TMEM budget");
-
-struct TileInfo {
-  int prob, m0, n0, valid_m, valid_n;
-};
-
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
-  int g = 0;
-  while (g + 1 < p.num_groups && tile >= p.groups[g + 1].tile_start) ++g;
-  const Group& G = p.groups[g];
-  const int local = tile - G.tile_start;
-  const int full_band = G.band_m * G.tiles_per_row;
-  const int band = local / full_band;
-  const int m_first = band * G.band_m;
-  const int bm = min(G.band_m, G.tiles_m - m_first);
-  const int r = local - band * full_band;
-  int n_lin = r / bm;
-  const int mt = m_first + (r - n_lin * bm);
-  int pi = G.first_prob;
-  while (n_lin >= p.probs[pi].tiles_n) {
-    n_lin -= p.probs[pi].tiles_n;
-    ++pi;
-  }
-  const Prob& P = p.probs[pi];
-  TileInfo t;
-  t.prob = pi;
-  t.m0 = mt * kPairM;
-  t.n0 = n_lin * P.tile_n;
-  t.valid_m = min(kPairM, P.M - t.m0);
-  t.valid_n = min(P.tile_n, P.N - t.n0);
-  return t;
-}
-
-// Stripe of a token row (sequence-parallel layout): the last j with
-// row0[j] <= row.  Empty stripes are never selected.
-__device__ __forceinline__ int stripe_of(const Stripes& st, int64_t row) {
-  int j = 0;
-  while (j + 1 < st.num && row >= st.row0[j + 1]) ++j;
-  return j;
-}
-
-struct Ctl {
-  volatile int32_t* abort_flag;
-  uint32_t peer_abort;  // cluster address of the peer CTA's abort flag
-  int32_t* status;
-  uint64_t timeout_ns;
-};
-
-__device__ __forceinline__ void raise_abort(const Ctl& c, int32_t code) {
-  *c.abort_flag = 1;
-  ptx::st_cluster_u32(c.peer_abort, 1u);
-  if (c.status) atomicCAS(c.status, 0, code);
-}
-
-// Wait for the phase of `bar` with the given parity; false if the wait
-// timed out (status recorded, both CTAs aborted) or an abort was raised.
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const Ctl& c, int32_t code) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*c.abort_flag) return false;
-    if (ptx::globaltimer_ns() - t0 > c.timeout_ns) {
-      raise_abort(c, code);
-      return false;
-    }
-  }
-}
-
-// Wait used while draining after an abort: bounded, ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer_ns() - t0 > kDrainTimeoutNs) return;
-  }
-}
-
-__device__ __forceinline__ void spin_ns(uint64_t ns) {
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (ptx::globaltimer_ns() - t0 < ns) {
-  }
-}
-
-// What CTA `rank` of the pair loads and computes for one tile.  MN-major
-// boxes wholly outside the valid rows / columns are not loaded (nor are the
-// A boxes of a CTA with no valid rows): the MMA rows / columns they would
-// feed are never stored.
-struct PairShape {
-  int n_mma;        // MMA N (multiple of 32, covers the tile's valid columns)
-  int half;         // B columns held by each CTA (n_mma / 2)
-  int nA[2];        // A copies each CTA issues
-  int nB[2];        // B copies (per B operand) each CTA issues
-  uint32_t bytes[2];  // bytes each CTA loads per K block
-};
-
-// TMA copies of one operand slice: K-major, kBK/64 boxes covering all 128
-// rows; MN-major, one box per 64 valid columns.
-__device__ __forceinline__ int copies_for(int major, int valid) {
-  if (valid <= 0) return 0;
-  return major == MAJOR_K ? kBK / 64 : (valid + 63) / 64;
-}
-
-__device__ __forceinline__ int box_bytes(int major) { return major == MAJOR_K ? kKBoxBytes : kMNBoxBytes; }
-
-__device__ __forceinline__ PairShape pair_shape(const TileInfo& ti, bool dual, int a_major, int b_major) {
-  PairShape s;
-  const int cap = dual ? 128 : 256;
-  s.n_mma = min(cap, (ti.valid_n + 31) & ~31);
-  s.half = s.n_mma >> 1;
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int vm = max(0, min(kBM, ti.valid_m - kBM * r));
-    const int vb = max(0, min(s.half, ti.valid_n - s.half * r));
-    s.nA[r] = copies_for(a_major, vm);
-    s.nB[r] = copies_for(b_major, vb);
-    s.bytes[r] = static_cast<uint32_t>(s.nA[r] * box_bytes(a_major) + (dual ? 2 : 1) * s.nB[r] * box_bytes(b_major));
-  }
-  return s;
-}
 
 // Walks the (tile, segment, K block) sequence of one CTA of a pair in the
 // order the main loop consumes it; the producer keeps one cursor for the
@@ -330,210 +170,6 @@ __device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor& 
     else
       ptx::tma_load_2d_pair(sbB + kMNBoxBytes, mb2, c.n0, k0, fb);
   }
-}
-
-// The MMAs of one stage: K steps j = 0 .. nk-1 of 16, each one (SwiGLU:
-// two, gate and up projection into the two 128-column halves) pair MMA.
-// Descriptors advance by offsets in 16-byte units: K-major, +32 B per K step
-// inside a 64-wide box and +16 KB per box; MN-major, +2048 B per K step.
-// A full stage is straight-line code.  A branch between two tcgen05.mma
-// instructions delays the issue of the second one (about 45 cycles per MMA
-// on GB300, against 128 cycles of tensor work for a 256 x 256 x 16 pair
-// MMA), so every choice -- SwiGLU or not, full or partial stage -- is made
-// once, before the sequence.
-template <bool kDual, bool kAmn, bool kBmn>
-__device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint32_t a_lo0, uint32_t a_hi, uint32_t b_lo0,
-                                            uint32_t b_hi, uint32_t idesc, int nk, uint32_t& accumulate) {
-  if (nk == kBK / 16) {
-#pragma unroll
-    for (int j = 0; j < kBK / 16; ++j) {
-      constexpr uint32_t kBoxOff = kMNBoxBytes >> 4;
-      const uint32_t koff = static_cast<uint32_t>(((j >> 2) * kKBoxBytes + (j & 3) * 32) >> 4);
-      const uint32_t moff = static_cast<uint32_t>((j * 2048) >> 4);
-      const uint32_t al = a_lo0 + (kAmn ? moff : koff);
-      const uint32_t bl = b_lo0 + (kBmn ? moff : koff);
-      if (j == 0) {
-        ptx::mma_bf16_pair_lohi(d_tmem, al, a_hi, bl, b_hi, idesc, accumulate);
-        if (kDual) ptx::mma_bf16_pair_lohi(d_tmem + 128u, al, a_hi, bl + kBoxOff, b_hi, idesc, accumulate);
-      } else {
-        ptx::mma_bf16_pair_lohi_acc(d_tmem, al, a_hi, bl, b_hi, idesc);
-        if (kDual) ptx::mma_bf16_pair_lohi_acc(d_tmem + 128u, al, a_hi, bl + kBoxOff, b_hi, idesc);
-      }
-    }
-    accumulate = 1;
-    return;
-  }
-  for (int j = 0; j < nk; ++j) {  // the last, partial stage of a segment
-    const uint32_t koff = static_cast<uint32_t>(((j >> 2) * kKBoxBytes + (j & 3) * 32) >> 4);
-    const uint32_t moff = static_cast<uint32_t>((j * 2048) >> 4);
-    const uint32_t al = a_lo0 + (kAmn ? moff : koff);
-    const uint32_t bl = b_lo0 + (kBmn ? moff : koff);
-    ptx::mma_bf16_pair_lohi(d_tmem, al, a_hi, bl, b_hi, idesc, accumulate);
-    if (kDual) ptx::mma_bf16_pair_lohi(d_tmem + 128u, al, a_hi, bl + (kMNBoxBytes >> 4), b_hi, idesc, accumulate);
-    accumulate = 1;
-  }
-}
-
-// One stage's MMAs, with every choice (SwiGLU split pair, operand majors)
-// resolved by a single switch ahead of the straight-line sequence.
-__device__ __forceinline__ void issue_stage_any(int kind, uint32_t d_tmem, uint32_t a_lo0, uint32_t a_hi,
-                                                uint32_t b_lo0, uint32_t b_hi, uint32_t idesc, int nk,
-                                                uint32_t& accumulate) {
-  switch (kind) {
-    case 0: issue_stage<false, false, false>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
-    case 1: issue_stage<false, false, true>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
-    case 2: issue_stage<false, true, false>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
-    case 3: issue_stage<false, true, true>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
-    case 4: issue_stage<true, false, false>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
-    case 5: issue_stage<true, false, true>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
-    case 6: issue_stage<true, true, false>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
-    default: issue_stage<true, true, true>(d_tmem, a_lo0, a_hi, b_lo0, b_hi, idesc, nk, accumulate); break;
-  }
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
-  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
-  return __bfloat1622float2(h);
-}
-
-// One epilogue warp's output path: 32 rows (its TMEM lanes) x 32 columns of
-// bf16 at a time go through one of its two shared-memory blocks and out with
-// a TMA store.  A thread writes its row as four 16-byte chunks, chunk g at
-// position g ^ ((row / 2) % 4) (the 64-byte swizzle of the output maps), so
-// every 8 consecutive rows fill all 32 banks once.  Rows and columns past the
-// tensor's end are clipped by the TMA unit.  Compared with each thread
-// storing its own row to global memory (32 cache lines per warp store), this
-// moves a warp's 2 KB in four shared-memory wavefronts and one bulk copy.
-struct EpiStore {
-  uint32_t buf;  // this warp's two blocks
-  uint32_t next;
-  int rows;      // rows of the current problem's outputs
-  int sj, sy0;   // striped out0: the stripe of this warp's rows and its first row
-};
-
-__device__ __forceinline__ void store_block(EpiStore& es, const GemmParams& p, int map, int x, int y,
-                                            const float (&v)[32], int lane, bool striped = false) {
-  if (y >= es.rows) return;  // every row of this warp is past the end: no store starts out of range
-  if (striped) {  // token stripes: the stripe's own map, stripe-local rows
-    map += es.sj;
-    y -= es.sy0;
-  }
-  const uint32_t b = es.buf + es.next * kEpiBlockBytes;
-  if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last used block b has read it
-  __syncwarp();
-  const uint32_t row = b + static_cast<uint32_t>(lane) * 64u;
-  const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    uint4 o;
-    o.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
-    o.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
-    o.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
-    o.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
-    ptx::st_shared_v4(row + ((static_cast<uint32_t>(g) ^ sw) << 4), o);
-  }
-  ptx::fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    ptx::tma_store_2d(&p.maps[map], b, x, y);
-    ptx::bulk_commit_group();
-  }
-  es.next ^= 1u;
-}
-
-__device__ __forceinline__ void load_row32(const void* src, int64_t ld, int64_t row, int col, int nvalid,
-                                           float (&v)[32]) {
-  const __nv_bfloat16* s = reinterpret_cast<const __nv_bfloat16*>(src) + row * ld + col;
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    uint4 q = make_uint4(0, 0, 0, 0);
-    if (8 * g < nvalid) q = __ldg(reinterpret_cast<const uint4*>(s + 8 * g));
-    float2 f;
-    f = unpack_bf16x2(q.x); v[8 * g + 0] = f.x; v[8 * g + 1] = f.y;
-    f = unpack_bf16x2(q.y); v[8 * g + 2] = f.x; v[8 * g + 3] = f.y;
-    f = unpack_bf16x2(q.z); v[8 * g + 4] = f.x; v[8 * g + 5] = f.y;
-    f = unpack_bf16x2(q.w); v[8 * g + 6] = f.x; v[8 * g + 7] = f.y;
-  }
-}
-
-// v[j] += bias[col + j] for the chunk's valid columns (bias may be null).
-__device__ __forceinline__ void add_bias32(const void* bias, int col, int nvalid, float (&v)[32]) {
-  if (!bias) return;
-  float b[32];
-  load_row32(bias, 0, 0, col, nvalid, b);
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] += b[j];
-}
-
-// Epilogue of one 32-column chunk (columns x .. x+31 of rows y .. y+31, this
-// thread's row grow) of a single accumulator.  Every lane takes part (the
-// stores are per warp); inputs are read only for valid rows and columns.
-__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& P, EpiStore& es, int64_t grow,
-                                               bool row_ok, int x, int y, int nvalid, const uint32_t (&r)[32],
-                                               int lane) {
-  float acc[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
-  const int nload = row_ok ? nvalid : 0;
-  switch (P.epi) {
-    case EPI_STORE:
-      add_bias32(P.aux0, x, nvalid, acc);
-      store_block(es, p, P.out_map[0], x, y, acc, lane, P.out_striped != 0);
-      break;
-    case EPI_GELU_FWD: {
-      add_bias32(P.aux0, x, nvalid, acc);
-      store_block(es, p, P.out_map[0], x, y, acc, lane);  // A (pre-activation)
-      act::x2::gelu_x32(acc);
-      store_block(es, p, P.out_map[1], x, y, acc, lane);
-      break;
-    }
-    case EPI_GELU_BWD: {
-      float a[32];
-      load_row32(P.aux0, P.ldo, grow, x, nload, a);
-      if (P.out1) {  // recompute H = GeLU(A) for the weight gradient of W2
-        float h[32];
-        act::x2::gelu_bwd_x32<true>(acc, a, h);
-        store_block(es, p, P.out_map[1], x, y, h, lane);
-      } else {
-        act::x2::gelu_bwd_x32<false>(acc, a, acc);
-      }
-      store_block(es, p, P.out_map[0], x, y, a, lane);
-      break;
-    }
-    case EPI_SWIGLU_BWD: {
-      float g[32], u[32];
-      load_row32(P.aux0, P.ldo, grow, x, nload, g);
-      load_row32(P.aux1, P.ldo, grow, x, nload, u);
-      if (P.out2) {  // recompute H = U * Swish(G) for the weight gradient of W2
-        float h[32];
-        act::x2::swiglu_bwd_x32<true>(acc, g, u, h);
-        store_block(es, p, P.out_map[2], x, y, h, lane);
-      } else {
-        act::x2::swiglu_bwd_x32<false>(acc, g, u, acc);
-      }
-      store_block(es, p, P.out_map[0], x, y, g, lane);
-      store_block(es, p, P.out_map[1], x, y, u, lane);
-      break;
-    }
-    default:
-      break;
-  }
-}
-
-// Whether a SwiGLU forward tile was computed with merged N = 256 MMAs: full
-// tiles (128 output columns, 64 per CTA of the pair).  Each CTA's B stage
-// holds 64 gate columns then 64 up columns (two MN-major blocks), so the
-// accumulator columns are, per CTA-half h of B (h = 0, 1): gate columns
-// 64 h .. 64 h + 63 of the tile at 128 h .. 128 h + 63, the matching up
-// columns at 128 h + 64 .. 128 h + 127.  Partial tiles use two MMAs of
-// N = 2 x 64-or-fewer columns: gate at 0 .., up at 128 ...
-__device__ __forceinline__ bool swiglu_merged(const TileInfo& ti, const Prob& P) {
-  return pair_shape(ti, true, P.a_major, P.b_major).n_mma == 128;
 }
 
 __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_raw) {
@@ -873,13 +509,14 @@ int tc_gemm_max_pairs(int tag) {
 }
 
 cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int max_pairs_hint, cudaStream_t stream) {
-  KernelFn k = kernel_for(kernel_tag);
+  KernelFn k = p.sk.on ? tc_gemm_sk_kernel(kernel_tag) : kernel_for(kernel_tag);
   if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   int pairs = tc_gemm_max_pairs(kernel_tag);
   if (pairs <= 0) pairs = max_pairs_hint > 0 ? max_pairs_hint : 1;
   pairs = pairs < p.total_tiles ? pairs : p.total_tiles;
+  if (p.sk.on) pairs = p.sk.pairs;  // the stream-K ranges were cut for exactly this many pairs
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -1,0 +1,675 @@
+// tc_gemm_sk.cu -- the stream-K variant of the persistent 2-SM tcgen05 GEMM
+// (tc_gemm.cu): the same pipeline, MMA issue and fused epilogues, but a pair
+// walks items instead of whole tiles.  Its data-parallel tiles come first
+// (tile = pair, pair + pairs, ... below the launch's full waves); then the
+// items of its stream-K range: parts of the last, partial wave's tiles, each
+// a range of the tile's K blocks counted over all of its segments.  A tile
+// cut between ranges is finished by the pair holding its K block 0 (the
+// owner, whose part is the last item of its range): it waits for the other
+// parts (one flag per epilogue warp of each contributing pair, raised after
+// the pair left its fp32 accumulator chunks in its workspace slot), adds
+// them in range order into its TMEM accumulator and runs the tile's normal
+// epilogue.  Ranges are handed to pairs in reverse, so an owner waits only on
+// lower-numbered pairs, which start first; every wait is bounded like the
+// pipeline's own.  The host (tpmlp_api.cu) cuts the ranges and launches this
+// variant only where the cut shortens the launch.
+#include "tc_gemm_common.cuh"
+
+namespace tpmlp {
+namespace {
+
+// The work of a pair, in the order every role walks it: its data-parallel
+// tiles (tile = pair, pair + pairs, ... below sk.dp_tiles), then the items of
+// its stream-K range r = pairs - 1 - pair.  An item is a tile and a range
+// [kb0, kb1) of its K blocks, counted over all of its segments: the whole
+// tile (ITEM_FULL), a part that another pair finishes (ITEM_PART), or the
+// part holding K block 0 of a tile cut between ranges (ITEM_OWNER).
+enum ItemKind : int { ITEM_FULL = 0, ITEM_PART = 1, ITEM_OWNER = 2 };
+
+struct Sched {
+  TileInfo ti;     // the current item's tile
+  int tile;        // -1: no more items
+  int kb0, kb1;    // its K blocks
+  int kind;
+  int dp;          // next data-parallel tile
+  int r;           // this pair's stream-K range
+  int sk_tile, sk_kb;  // next position in that range
+  bool in_dp;
+};
+
+__device__ __forceinline__ void sched_next(Sched& s, const GemmParams& p, int npairs) {
+  if (s.in_dp) {
+    if (s.dp < p.sk.dp_tiles) {
+      s.tile = s.dp;
+      s.dp += npairs;
+      s.ti = decode_tile(p, s.tile);
+      s.kb0 = 0;
+      s.kb1 = p.probs[s.ti.prob].kblocks;
+      s.kind = ITEM_FULL;
+      return;
+    }
+    s.in_dp = false;
+    if (!p.sk.on || s.r < 0 || s.r >= p.sk.pairs) {
+      s.tile = -1;
+      return;
+    }
+    s.sk_tile = p.sk.start_tile[s.r];
+    s.sk_kb = p.sk.start_kb[s.r];
+  }
+  const int end_tile = p.sk.start_tile[s.r + 1], end_kb = p.sk.start_kb[s.r + 1];
+  while (s.sk_tile < end_tile || (s.sk_tile == end_tile && s.sk_kb < end_kb)) {
+    const int t = s.sk_tile;
+    const TileInfo ti = decode_tile(p, t);
+    const int kbt = p.probs[ti.prob].kblocks;
+    const int kb0 = s.sk_kb, kb1 = t == end_tile ? end_kb : kbt;
+    s.sk_tile = t + 1;
+    s.sk_kb = 0;
+    if (kb1 > kb0) {
+      s.tile = t;
+      s.ti = ti;
+      s.kb0 = kb0;
+      s.kb1 = kb1;
+      s.kind = kb0 > 0 ? ITEM_PART : (kb1 < kbt ? ITEM_OWNER : ITEM_FULL);
+      return;
+    }
+  }
+  s.tile = -1;
+}
+
+// pair < 0: an empty schedule.
+__device__ __forceinline__ void sched_init(Sched& s, const GemmParams& p, int pair, int npairs) {
+  s.dp = pair < 0 ? INT_MAX : pair;
+  s.r = pair < 0 ? -1 : npairs - 1 - pair;
+  s.in_dp = true;
+  sched_next(s, p, npairs);
+}
+
+// Walks the (item, segment, K block) sequence of one CTA of a pair in the
+// order the main loop consumes it.
+struct Cursor {
+  Sched s;             // the current item
+  const void* ma;      // tensor maps of the current segment
+  const void* mb;
+  const void* mb2;
+  int seg, kb, kblocks, left;  // segment, K block in it, its K blocks; K blocks left in the item
+  int a_major, b_major, dual;
+  int a_striped, b_striped;  // operand read from the launch's token stripes
+  int a_sj, b_sj;            // its current stripe,
+  int a_y0, b_y0;            //   that stripe's first token row,
+  int a_next, b_next;        //   and the next stripe's (an MN-major K walk crosses it)
+  int m0, n0;          // this CTA's first row of A and first column of B
+  int nA, nB;          // boxes this CTA loads per operand
+  uint32_t bytes_pair; // bytes both CTAs load per K block (counted on the even CTA)
+};
+
+__device__ __forceinline__ void cursor_segment(Cursor& c, const GemmParams& p) {
+  const Seg& S = p.segs[c.seg];
+  c.kb = 0;
+  c.kblocks = (S.K + kBK - 1) / kBK;
+  c.ma = &p.maps[S.a_map];
+  c.mb = &p.maps[S.b_map];
+  c.mb2 = c.dual ? static_cast<const void*>(&p.maps[S.b2_map]) : nullptr;
+  c.a_striped = S.a_striped;
+  c.b_striped = S.b_striped;
+  // The stripe of the first box: K-major operands keep it for the whole
+  // segment (their token rows are this CTA's M or N rows); MN-major ones walk
+  // the tokens along K and move to the next stripe in cursor_next.
+  if (c.a_striped) {
+    const int j = stripe_of(p.stripes, c.a_major == MAJOR_MN ? 0 : c.m0);
+    c.a_sj = j;
+    c.a_y0 = static_cast<int>(p.stripes.row0[j]);
+    c.a_next = j + 1 < p.stripes.num ? static_cast<int>(p.stripes.row0[j + 1]) : INT_MAX;
+  }
+  if (c.b_striped) {
+    const int j = stripe_of(p.stripes, c.b_major == MAJOR_MN ? 0 : c.n0);
+    c.b_sj = j;
+    c.b_y0 = static_cast<int>(p.stripes.row0[j]);
+    c.b_next = j + 1 < p.stripes.num ? static_cast<int>(p.stripes.row0[j + 1]) : INT_MAX;
+  }
+}
+
+__device__ __forceinline__ void stripe_advance(const GemmParams& p, int k0, int& sj, int& y0, int& next) {
+  while (k0 >= next) {
+    ++sj;
+    y0 = next;
+    next = sj + 1 < p.stripes.num ? static_cast<int>(p.stripes.row0[sj + 1]) : INT_MAX;
+  }
+}
+
+__device__ __forceinline__ void cursor_stripes(Cursor& c, const GemmParams& p) {
+  if (c.a_striped && c.a_major == MAJOR_MN) stripe_advance(p, c.kb * kBK, c.a_sj, c.a_y0, c.a_next);
+  if (c.b_striped && c.b_major == MAJOR_MN) stripe_advance(p, c.kb * kBK, c.b_sj, c.b_y0, c.b_next);
+}
+
+// Set the cursor on the first K block of its schedule's current item.
+__device__ __forceinline__ void cursor_item(Cursor& c, const GemmParams& p, uint32_t rank) {
+  if (c.s.tile < 0) return;
+  const TileInfo& ti = c.s.ti;
+  const Prob& P = p.probs[ti.prob];
+  c.dual = P.epi == EPI_SWIGLU_FWD;
+  const PairShape ps = pair_shape(ti, c.dual, P.a_major, P.b_major);
+  c.nA = rank ? ps.nA[1] : ps.nA[0];
+  c.nB = rank ? ps.nB[1] : ps.nB[0];
+  c.bytes_pair = ps.bytes[0] + ps.bytes[1];
+  c.m0 = ti.m0 + kBM * static_cast<int>(rank);
+  c.n0 = ti.n0 + ps.half * static_cast<int>(rank);
+  c.a_major = P.a_major;
+  c.b_major = P.b_major;
+  c.seg = P.seg_begin;
+  c.left = c.s.kb1 - c.s.kb0;
+  int skip = c.s.kb0;
+  cursor_segment(c, p);
+  while (skip >= c.kblocks) {  // a stream-K part may start in a later segment
+    skip -= c.kblocks;
+    ++c.seg;
+    cursor_segment(c, p);
+  }
+  if (skip > 0) {
+    c.kb = skip;
+    cursor_stripes(c, p);
+  }
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& c, const GemmParams& p, int npairs, uint32_t rank) {
+  if (--c.left == 0) {
+    sched_next(c.s, p, npairs);
+    cursor_item(c, p, rank);
+    return;
+  }
+  if (++c.kb < c.kblocks) {
+    cursor_stripes(c, p);
+    return;
+  }
+  ++c.seg;
+  cursor_segment(c, p);
+}
+
+// Issue this CTA's box copies for the cursor's K block.
+__device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor& c, uint32_t sb, uint32_t fb) {
+  const int k0 = c.kb * kBK;
+  const uint32_t sbB = sb + kOperandBytes;
+  for (int b = 0; b < c.nA; ++b) {
+    // K-major: box b covers K [k0 + 64 b, +64) of the 128 rows;
+    // MN-major: box b covers columns [m0 + 64 b, +64) of K rows [k0, k0 + kBK).
+    const bool mn = c.a_major == MAJOR_MN;
+    const int x = mn ? c.m0 + 64 * b : k0 + 64 * b;
+    int y = mn ? k0 : c.m0;
+    const CUtensorMap* ma = static_cast<const CUtensorMap*>(c.ma);
+    if (c.a_striped) {  // the stored rows are tokens: the stripe's map, stripe-local y
+      ma += c.a_sj;
+      y -= c.a_y0;
+    }
+    ptx::tma_load_2d_pair(sb + b * (mn ? kMNBoxBytes : kKBoxBytes), ma, x, y, fb);
+  }
+  for (int j = 0; j < c.nB; ++j) {
+    const bool mn = c.b_major == MAJOR_MN;
+    const int x = mn ? c.n0 + 64 * j : k0 + 64 * j;
+    int y = mn ? k0 : c.n0;
+    const CUtensorMap* mb = static_cast<const CUtensorMap*>(c.mb);
+    if (c.b_striped) {
+      mb += c.b_sj;
+      y -= c.b_y0;
+    }
+    ptx::tma_load_2d_pair(sbB + j * (mn ? kMNBoxBytes : kKBoxBytes), mb, x, y, fb);
+  }
+  if (c.dual && c.nB > 0)  // SwiGLU up projection (MN-major like the gate), second B box
+    ptx::tma_load_2d_pair(sbB + kMNBoxBytes, c.mb2, c.n0, k0, fb);
+}
+
+// ---- stream-K partials.  Range r's slot holds, per epilogue warp wi of the
+// pair (rank * 8 + warp - 2), the four 32 x 32 fp32 accumulator chunks that
+// warp reads as owner (the same TMEM lanes and columns in every pair), laid
+// out so that each 16-byte store / load of a warp covers 512 contiguous bytes.
+__device__ __forceinline__ uint32_t* sk_flag(const GemmParams& p, int r, int wi) {
+  return reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(p.status) + kSkFlagsOffset) + r * kSkWarpsPerPair + wi;
+}
+
+__device__ __forceinline__ char* sk_chunk(const GemmParams& p, int r, int wi, int cslot) {
+  return reinterpret_cast<char*>(p.status) + kSkSlotsOffset + static_cast<size_t>(r) * kSkSlotBytes +
+         static_cast<size_t>(wi * 4 + cslot) * (32 * 32 * sizeof(float));
+}
+
+__device__ __forceinline__ bool sk_range_empty(const GemmParams& p, int r) {
+  return p.sk.start_tile[r] == p.sk.start_tile[r + 1] && p.sk.start_kb[r] == p.sk.start_kb[r + 1];
+}
+
+__device__ __forceinline__ void sk_store_chunk(const GemmParams& p, int r, int wi, int cslot, int lane,
+                                               const uint32_t (&v)[32]) {
+  char* dst = sk_chunk(p, r, wi, cslot) + lane * 16;
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) ptx::st_cg_v4(dst + j4 * 512, v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+}
+
+// The first contributing range q' >= q of the owner's tile (a non-empty
+// range that starts inside it), or -1.
+__device__ __forceinline__ int sk_next_part(const GemmParams& p, const Sched& s, int q) {
+  for (; q < p.sk.pairs && p.sk.start_tile[q] == s.tile; ++q)
+    if (!sk_range_empty(p, q)) return q;
+  return -1;
+}
+
+// Owner: add the parts of the tile that ranges r + 1, r + 2, ... computed, in
+// that order, to this warp's chunk (eight 16-byte loads in flight per lane).
+__device__ __forceinline__ void sk_add_parts(const GemmParams& p, const Sched& s, int wi, int cslot, int lane,
+                                             uint32_t (&v)[32]) {
+  for (int q = sk_next_part(p, s, s.r + 1); q >= 0; q = sk_next_part(p, s, q + 1)) {
+    const char* src = sk_chunk(p, q, wi, cslot) + lane * 16;
+    float4 f[8];
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) f[j4] = ptx::ld_cg_v4f(src + j4 * 512);
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+      v[4 * j4 + 0] = __float_as_uint(__uint_as_float(v[4 * j4 + 0]) + f[j4].x);
+      v[4 * j4 + 1] = __float_as_uint(__uint_as_float(v[4 * j4 + 1]) + f[j4].y);
+      v[4 * j4 + 2] = __float_as_uint(__uint_as_float(v[4 * j4 + 2]) + f[j4].z);
+      v[4 * j4 + 3] = __float_as_uint(__uint_as_float(v[4 * j4 + 3]) + f[j4].w);
+    }
+  }
+}
+
+// Part: publish this warp's chunks (every lane's stores, then one flag).
+__device__ __forceinline__ void sk_publish(const GemmParams& p, int r, int wi, int lane) {
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) ptx::st_release_gpu_u32(sk_flag(p, r, wi), p.sk.epoch);
+}
+
+// Owner: wait until every part of the tile has been published by this warp's
+// counterparts, then lower their flags again (each flag has one reader).
+// Bounded: false after an abort or a timeout (status recorded).
+__device__ __forceinline__ bool sk_wait_parts(const GemmParams& p, const Sched& s, int wi, int lane, const Ctl& c) {
+  for (int q = s.r + 1; q < p.sk.pairs && p.sk.start_tile[q] == s.tile; ++q) {
+    if (sk_range_empty(p, q)) continue;
+    uint32_t* f = sk_flag(p, q, wi);
+    int ok = 1;
+    if (lane == 0 && ptx::ld_acquire_gpu_u32(f) != p.sk.epoch) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (ptx::ld_acquire_gpu_u32(f) != p.sk.epoch) {
+        if (*c.abort_flag) {
+          ok = 0;
+          break;
+        }
+        if (ptx::globaltimer_ns() - t0 > c.timeout_ns) {
+          raise_abort(c, kDevTimeoutPartial);
+          ok = 0;
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    (void)ptx::ld_acquire_gpu_u32(f);  // every lane acquires the part's stores
+    __syncwarp();
+    if (lane == 0) ptx::st_relaxed_gpu_u32(f, 0u);
+  }
+  return true;
+}
+
+// TMEM column of this warp's chunk cslot (0..3) of a tile -- the chunks the
+// epilogue reads, in its order -- or -1 past the tile's valid columns.
+// SwiGLU forward: chunk 2c is the gate, 2c + 1 the up projection of output
+// columns 64 half + 32 c ..; otherwise chunk c is columns 128 half + 32 c ...
+__device__ __forceinline__ int sk_chunk_col(const Prob& P, const TileInfo& ti, int half, int cslot) {
+  if (P.epi == EPI_SWIGLU_FWD) {
+    const int c = cslot >> 1;
+    const int col = half * 64 + c * 32;
+    if (col >= ti.valid_n) return -1;
+    const bool merged = swiglu_merged(ti, P);
+    const int g_col = merged ? half * 128 + c * 32 : col;
+    return (cslot & 1) ? (merged ? g_col + 64 : 128 + col) : g_col;
+  }
+  const int col = half * 128 + cslot * 32;
+  return col < ti.valid_n ? col : -1;
+}
+
+// Part: this warp's chunks, raw fp32, to this pair's stream-K slot.
+__device__ __forceinline__ void sk_part_store(const GemmParams& p, const Prob& P, const Sched& it, uint32_t tacc,
+                                              int half, int wi, int lane) {
+#pragma unroll 1
+  for (int cs = 0; cs < 4; ++cs) {
+    const int tc = sk_chunk_col(P, it.ti, half, cs);
+    if (tc < 0) continue;
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(tc), r);
+    ptx::tmem_wait_ld();
+    sk_store_chunk(p, it.r, wi, cs, lane, r);
+  }
+}
+
+// Owner: fold the other parts into this warp's accumulator chunks in TMEM,
+// after which the tile's normal epilogue runs on the complete sums.
+__device__ __forceinline__ void sk_owner_fold(const GemmParams& p, const Prob& P, const Sched& it, uint32_t tacc,
+                                              int half, int wi, int lane) {
+#pragma unroll 1
+  for (int cs = 0; cs < 4; ++cs) {
+    const int tc = sk_chunk_col(P, it.ti, half, cs);
+    if (tc < 0) continue;
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(tc), r);
+    ptx::tmem_wait_ld();
+    sk_add_parts(p, it, wi, cs, lane, r);
+    ptx::tmem_st_32x32b_x32(tacc + static_cast<uint32_t>(tc), r);
+  }
+  ptx::tmem_wait_st();
+}
+
+__device__ __forceinline__ void tc_gemm_body_sk(const GemmParams& p, uint8_t* smem_raw) {
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kEpiBytes);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_holder + 1);
+
+  const uint32_t smem_base = ptx::smem_u32(smem);
+  const uint32_t bar0 = ptx::smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };                        // even CTA: copies landed
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };           // both: stage consumed
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };       // both: accumulator ready
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kNumAcc + a); };  // even CTA: drained
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kNumAcc);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < kNumAcc; ++a) {
+      ptx::mbar_init(tfull_bar(a), 1);
+      ptx::mbar_init(tempty_bar(a), 2 * kNumEpiWarps);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.num_maps; ++i) ptx::prefetch_tmap(&p.maps[i]);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_holder), kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const Ctl ctl{abort_flag, ptx::map_to_cta(ptx::smem_u32(const_cast<int32_t*>(abort_flag)), rank ^ 1u), p.status,
+                p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed_parity[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) armed_parity[s] = -1;
+      bool ok = true;
+      bool issued = false;
+      Cursor ld;
+      sched_init(ld.s, p, p.stall_injection ? -1 : pair, npairs);  // injected stall: nothing to load
+      cursor_item(ld, p, rank);
+      while (ld.s.tile >= 0) {
+        if (!bounded_wait(empty_bar(stage), phase ^ 1u, ctl, kDevTimeoutProducer)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          ptx::mbar_arrive_expect_tx(full_bar(stage), ld.bytes_pair);
+          armed_parity[stage] = static_cast<int>(phase);
+        }
+        cursor_issue(p, ld, smem_base + stage * kStageBytes, ptx::map_to_cta(full_bar(stage), 0));
+        issued = true;
+        cursor_next(ld, p, npairs, rank);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok && issued) {
+        // Let every copy already issued land before the CTA can exit.
+        if (leader) {
+          for (int s = 0; s < kStages; ++s)
+            if (armed_parity[s] >= 0) drain_wait(full_bar(s), static_cast<uint32_t>(armed_parity[s]));
+        }
+        spin_ns(kPeerDrainNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      // Descriptors of stage 0 for each operand layout; a stage and a K step
+      // are added to the start-address field (16-byte units, no carry: the
+      // ring lies below 256 KB).  K-major: 8-row groups 1024 B apart; K16
+      // step j is +32 B inside a 64-wide box, box j/4 is +16 KB.  MN-major:
+      // the two 64-column blocks are kMNBoxBytes apart (leading offset), 8-row
+      // K groups 1024 B apart, K16 step j is +2048 B.
+      const uint64_t a_k_desc = ptx::make_sdesc_sw128(smem_base, 16, 1024);
+      const uint64_t a_mn_desc = ptx::make_sdesc_sw128(smem_base, kMNBoxBytes, 1024);
+      const uint64_t b_k_desc = ptx::make_sdesc_sw128(smem_base + kOperandBytes, 16, 1024);
+      const uint64_t b_mn_desc = ptx::make_sdesc_sw128(smem_base + kOperandBytes, kMNBoxBytes, 1024);
+      Sched it;
+      for (sched_init(it, p, pair, npairs); ok && it.tile >= 0; sched_next(it, p, npairs)) {
+        const TileInfo& ti = it.ti;
+        const Prob& P = p.probs[ti.prob];
+        const int a_major = P.a_major, b_major = P.b_major;
+        const bool dual = P.epi == EPI_SWIGLU_FWD;
+        const PairShape ps = pair_shape(ti, dual, a_major, b_major);
+        // A full SwiGLU tile issues one N = 256 MMA over each CTA's [gate | up]
+        // column blocks instead of two N = 128 MMAs (the wider MMA runs at the
+        // full tensor rate, N = 128 at about 88 %); see swiglu_merged().
+        const bool merged = dual && ps.n_mma == 128;
+        const uint32_t idesc = ptx::make_idesc_bf16(kPairM, merged ? 256 : ps.n_mma, a_major, b_major);
+        const uint64_t a_desc0 = a_major == MAJOR_MN ? a_mn_desc : a_k_desc;
+        const uint64_t b_desc0 = b_major == MAJOR_MN ? b_mn_desc : b_k_desc;
+        const uint32_t a_lo = static_cast<uint32_t>(a_desc0), a_hi = static_cast<uint32_t>(a_desc0 >> 32);
+        const uint32_t b_lo = static_cast<uint32_t>(b_desc0), b_hi = static_cast<uint32_t>(b_desc0 >> 32);
+        const int kind = (dual && !merged ? 4 : 0) | (a_major == MAJOR_MN ? 2 : 0) | (b_major == MAJOR_MN ? 1 : 0);
+        if (!bounded_wait(tempty_bar(acc), acc_phase ^ 1u, ctl, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+        uint32_t accumulate = 0;
+        // The item's K blocks [kb0, kb1), counted over the tile's segments.
+        int sg = P.seg_begin;
+        int K = p.segs[sg].K;
+        int skip = it.kb0;
+        while (skip >= (K + kBK - 1) / kBK) {
+          skip -= (K + kBK - 1) / kBK;
+          K = p.segs[++sg].K;
+        }
+        int k0 = skip * kBK;
+        for (int left = it.kb1 - it.kb0; left > 0; --left) {
+          if (!bounded_wait(full_bar(stage), phase, ctl, kDevTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t st = static_cast<uint32_t>((stage * kStageBytes) >> 4);
+          const int nk = min(kBK / 16, (K - k0 + 15) >> 4);
+          issue_stage_any(kind, d_tmem, a_lo + st, a_hi, b_lo + st, b_hi, idesc, nk, accumulate);
+          issued = true;
+          ptx::mma_commit_pair_mc(empty_bar(stage), kPairMask);  // stage free in both CTAs
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          k0 += kBK;
+          if (k0 >= K && left > 1) {
+            K = p.segs[++sg].K;
+            k0 = 0;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair_mc(tfull_bar(acc), kPairMask);  // accumulator ready in both CTAs
+        if (++acc == kNumAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok && issued) {
+        // Every MMA issued so far must finish before TMEM is released.
+        ptx::mma_commit_pair(drain_bar);
+        drain_wait(drain_bar, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;              // TMEM lane quarter this warp may read
+    const int half = (warp - 2) >> 2;    // which half of the tile's columns
+    EpiStore es{smem_base + static_cast<uint32_t>(kStages * kStageBytes + (warp - 2) * 2 * kEpiBlockBytes), 0u, 0, 0,
+                0};
+    const int wi = static_cast<int>(rank) * kNumEpiWarps + (warp - 2);  // stream-K partial slot of this warp
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    Sched it;
+    for (sched_init(it, p, pair, npairs); it.tile >= 0; sched_next(it, p, npairs)) {
+      const TileInfo ti = it.ti;
+      const Prob& P = p.probs[ti.prob];
+      const bool part = it.kind == ITEM_PART;
+      const int row = q * 32 + lane;
+      const int vm = max(0, min(kBM, ti.valid_m - kBM * static_cast<int>(rank)));
+      const bool row_ok = row < vm;
+      const int64_t grow = static_cast<int64_t>(ti.m0) + kBM * static_cast<int>(rank) + row;
+      const int wrow = ti.m0 + kBM * static_cast<int>(rank) + q * 32;  // this warp's first row
+      es.rows = P.M;
+      if (P.out_striped && wrow < P.M) {  // a warp's 32 rows never cross a stripe boundary
+        es.sj = stripe_of(p.stripes, wrow);
+        es.sy0 = static_cast<int>(p.stripes.row0[es.sj]);
+      }
+      if (!part && row_ok && (P.epi == EPI_GELU_BWD || P.epi == EPI_SWIGLU_BWD)) {
+        // Pull this thread's row of the saved pre-activation(s) into L2
+        // while the accumulator is still being computed.
+        const int c0 = half * 128;
+        const int cn = min(128, ti.valid_n - c0);
+        if (cn > 0) {
+          const int64_t off = grow * P.ldo + ti.n0 + c0;
+          const __nv_bfloat16* a0 = static_cast<const __nv_bfloat16*>(P.aux0) + off;
+          for (int b = 0; b < 2 * cn; b += 128) ptx::prefetch_l2(reinterpret_cast<const char*>(a0) + b);
+          ptx::prefetch_l2(reinterpret_cast<const char*>(a0) + 2 * cn - 1);
+          if (P.epi == EPI_SWIGLU_BWD) {
+            const __nv_bfloat16* a1 = static_cast<const __nv_bfloat16*>(P.aux1) + off;
+            for (int b = 0; b < 2 * cn; b += 128) ptx::prefetch_l2(reinterpret_cast<const char*>(a1) + b);
+            ptx::prefetch_l2(reinterpret_cast<const char*>(a1) + 2 * cn - 1);
+          }
+        }
+      }
+      if (!bounded_wait(tfull_bar(acc), acc_phase, ctl, kDevTimeoutEpilogue)) break;
+      ptx::tc_fence_after();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
+      if (part) {
+        if (vm > 0) sk_part_store(p, P, it, tacc, half, wi, lane);
+        sk_publish(p, it.r, wi, lane);  // even with nothing stored: the owner waits for every warp
+      } else {
+        if (it.kind == ITEM_OWNER) {
+          if (!sk_wait_parts(p, it, wi, lane, ctl)) break;
+          if (vm > 0) sk_owner_fold(p, P, it, tacc, half, wi, lane);
+        }
+        if (vm > 0) {
+          if (P.epi == EPI_SWIGLU_FWD) {
+            const bool merged = swiglu_merged(ti, P);
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+              const int col = half * 64 + c * 32;
+              if (col >= ti.valid_n) break;
+              // output columns 64 half + 32 c ..: merged, gate at accumulator
+              // column 128 half + 32 c, up 64 further; split, gate at col, up at 128 + col
+              const uint32_t g_col = merged ? static_cast<uint32_t>(half * 128 + c * 32) : static_cast<uint32_t>(col);
+              const uint32_t u_col = merged ? g_col + 64u : 128u + static_cast<uint32_t>(col);
+              uint32_t rg[32], ru[32];
+              ptx::tmem_ld_32x32b_x32(tacc + g_col, rg);
+              ptx::tmem_ld_32x32b_x32(tacc + u_col, ru);
+              ptx::tmem_wait_ld();
+              const int nvalid = min(32, ti.valid_n - col);
+              float g[32], u[32], h[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                g[j] = __uint_as_float(rg[j]);
+                u[j] = __uint_as_float(ru[j]);
+              }
+              add_bias32(P.aux0, ti.n0 + col, nvalid, g);
+              add_bias32(P.aux1, ti.n0 + col, nvalid, u);
+              act::x2::swiglu_x32(g, u, h);
+              store_block(es, p, P.out_map[0], ti.n0 + col, wrow, g, lane);
+              store_block(es, p, P.out_map[1], ti.n0 + col, wrow, u, lane);
+              store_block(es, p, P.out_map[2], ti.n0 + col, wrow, h, lane);
+            }
+          } else {
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              const int col = half * 128 + c * 32;
+              if (col >= ti.valid_n) break;
+              uint32_t r[32];
+              ptx::tmem_ld_32x32b_x32(tacc + col, r);
+              ptx::tmem_wait_ld();
+              epilogue_chunk(p, P, es, grow, row_ok, ti.n0 + col, wrow, min(32, ti.valid_n - col), r, lane);
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::map_to_cta(tempty_bar(acc), 0));
+      if (++acc == kNumAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) ptx::bulk_wait_group_all();  // this warp's TMA stores are complete
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // no CTA leaves while its peer may still signal it
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+#define TPMLP_TC_KERNEL_SK(name)                                                       \
+  __global__ void __launch_bounds__(kThreads, 1) name(const __grid_constant__ GemmParams p) { \
+    extern __shared__ __align__(1024) uint8_t smem_raw[];                              \
+    tc_gemm_body_sk(p, smem_raw);                                                      \
+  }
+
+TPMLP_TC_KERNEL_SK(tpmlp_fwd_column_gemm_act_sk)
+TPMLP_TC_KERNEL_SK(tpmlp_fwd_row_gemm_gsum_sk)
+TPMLP_TC_KERNEL_SK(tpmlp_bwd_dgrad_act_wgrad2_sk)
+TPMLP_TC_KERNEL_SK(tpmlp_bwd_dx_fsum_wgrad1_sk)
+TPMLP_TC_KERNEL_SK(tpmlp_attn_qkv_proj_sk)
+TPMLP_TC_KERNEL_SK(tpmlp_attn_out_proj_gsum_sk)
+TPMLP_TC_KERNEL_SK(tpmlp_attn_out_proj_bwd_sk)
+TPMLP_TC_KERNEL_SK(tpmlp_attn_qkv_bwd_dx_fsum_sk)
+
+TcKernelFn tc_gemm_sk_kernel(int tag) {
+  switch (tag) {
+    case TAG_FWD_COLUMN: return tpmlp_fwd_column_gemm_act_sk;
+    case TAG_FWD_ROW: return tpmlp_fwd_row_gemm_gsum_sk;
+    case TAG_BWD_DGRAD: return tpmlp_bwd_dgrad_act_wgrad2_sk;
+    case TAG_BWD_FSUM: return tpmlp_bwd_dx_fsum_wgrad1_sk;
+    case TAG_ATTN_QKV: return tpmlp_attn_qkv_proj_sk;
+    case TAG_ATTN_OUT: return tpmlp_attn_out_proj_gsum_sk;
+    case TAG_ATTN_OUT_BWD: return tpmlp_attn_out_proj_bwd_sk;
+    case TAG_ATTN_QKV_BWD: return tpmlp_attn_qkv_bwd_dx_fsum_sk;
+    default: return nullptr;
+  }
+}
+
+}  // namespace tpmlp

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -33,6 +34,7 @@ struct tpmlp_plan {
   tpmlp_dtype dtype;
   uint64_t timeout_ns;
   int32_t stall_injection;
+  int32_t stream_k;  // TPMLP_STREAM_K_OFF / _AUTO / _ALWAYS
   std::vector<int64_t> stripe_rows;  // sequence-parallel token stripes (empty: not set)
 };
 
@@ -315,8 +317,108 @@ int band_for(int sms) {
   return b;
 }
 
+// Tile -> problem, as the kernel's decode_tile maps it.
+int tile_prob(const GemmParams& p, int tile) {
+  int g = 0;
+  while (g + 1 < p.num_groups && tile >= p.groups[g + 1].tile_start) ++g;
+  const Group& G = p.groups[g];
+  const int local = tile - G.tile_start;
+  const int full_band = G.band_m * G.tiles_per_row;
+  const int band = local / full_band;
+  const int bm = std::min(G.band_m, G.tiles_m - band * G.band_m);
+  int n_lin = (local - band * full_band) / bm;
+  int pi = G.first_prob;
+  while (n_lin >= p.probs[pi].tiles_n) {
+    n_lin -= p.probs[pi].tiles_n;
+    ++pi;
+  }
+  return pi;
+}
+
+std::atomic<uint32_t> g_sk_epoch{0};
+
+// Cut the stream-K tail of a tensor-core launch (see StreamK).  Every full
+// wave of tiles stays data-parallel: the pairs of a wave start together and
+// walk their tiles' K loops in step, so tiles that share a row block of A or
+// a column block of B read it from L2 once.  (Cutting more than the last
+// wave was measured slower: parts that run out of step lose that sharing and
+// become bound by HBM.)  Only the last, partial wave of R tiles is cut, and
+// only when every pair carries the same data-parallel load and the R tiles
+// have the same depth KB: each tile is then split into k parts of KB / k K
+// blocks (rounded), on k ranges, with k <= pairs / R chosen to minimise
+// KB / k + kPartCost (k - 1).  kPartCost, in K blocks, is what one more part
+// costs the owner: reading a 256 KB partial accumulator per pair back from
+// L2 (about 2.8 us each on GB300, about five K blocks).  Auto mode keeps the
+// plain round robin unless the cut saves at least max(16, 2 %) of a pair's K
+// blocks: measured on GB300, smaller savings were lost to the launch's fixed
+// costs and, under the power cap, to lower clocks in the following launches.
+void plan_stream_k(GemmParams& p, int pairs, int mode) {
+  StreamK& sk = p.sk;
+  sk.on = 0;
+  sk.dp_tiles = p.total_tiles;
+  sk.pairs = 0;
+  sk.epoch = 0;
+  const int n = p.total_tiles;
+  if (mode == TPMLP_STREAM_K_OFF || pairs < 2 || pairs > kMaxSkPairs || n <= 0) return;
+  const int dp_tiles = (n / pairs) * pairs;
+  const int R = n - dp_tiles;
+  if (R == 0) return;  // no partial wave
+  std::vector<int32_t> kb(n);
+  for (int t = 0; t < n; ++t) kb[t] = p.probs[tile_prob(p, t)].kblocks;
+  std::vector<int64_t> dp(pairs, 0);
+  for (int t = 0; t < dp_tiles; ++t) dp[t % pairs] += kb[t];
+  const int64_t dp_lo = *std::min_element(dp.begin(), dp.end());
+  const int64_t dp_hi = *std::max_element(dp.begin(), dp.end());
+  int kb_lo = kb[dp_tiles], kb_hi = kb[dp_tiles];
+  for (int t = dp_tiles; t < n; ++t) {
+    kb_lo = std::min(kb_lo, kb[t]);
+    kb_hi = std::max(kb_hi, kb[t]);
+  }
+  const bool uniform = dp_lo == dp_hi && kb_lo == kb_hi;
+  if (!uniform && mode == TPMLP_STREAM_K_AUTO) return;
+  constexpr int64_t kPartCost = 5;
+  constexpr int64_t kMinSaving = 16;  // K blocks (about 9 us): below that, launch and power effects dominate
+  const int k_max = std::max(1, pairs / R);
+  int k = 1;
+  int64_t best = kb_hi;
+  for (int c = 2; c <= k_max; ++c) {
+    const int64_t m = (kb_hi + c - 1) / c + kPartCost * (c - 1);
+    if (m < best) {
+      best = m;
+      k = c;
+    }
+  }
+  if (mode == TPMLP_STREAM_K_ALWAYS) k = std::min(k_max, kb_hi);  // as many parts as fit: a stress test
+  if (mode == TPMLP_STREAM_K_AUTO) {
+    const int64_t rr = dp_hi + kb_hi, cut = dp_hi + best;
+    if (k == 1 || rr - cut < std::max<int64_t>(kMinSaving, rr / 50)) return;
+  }
+  if (k < 2) return;
+  // Range r = j k + i (held by pair pairs - 1 - r) is part i of tail tile j;
+  // a part of a tile cut between ranges is owned by the higher-numbered pair
+  // (part 0); ranges from R k on are empty.
+  for (int r = 0; r <= pairs; ++r) {
+    const int j = r / k, i = r % k;
+    if (j >= R) {
+      sk.start_tile[r] = n;
+      sk.start_kb[r] = 0;
+    } else {
+      sk.start_tile[r] = dp_tiles + j;
+      sk.start_kb[r] = static_cast<int32_t>(static_cast<int64_t>(kb[dp_tiles + j]) * i / k);
+    }
+  }
+  uint32_t e = ++g_sk_epoch;
+  if (e == 0) e = ++g_sk_epoch;
+  sk.on = 1;
+  sk.dp_tiles = dp_tiles;
+  sk.pairs = pairs;
+  sk.epoch = e;
+}
+
+// sk_workspace: the workspace holds the stream-K flags and partial slots
+// (tpmlp_workspace_size bytes); false for the library's status-only scratch.
 tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan* plan, void* workspace,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, bool sk_workspace = true) {
   GemmParams& p = *B.p;
   if (p.total_tiles == 0) return TPMLP_OK;
   for (int i = 0; i < p.num_probs; ++i) {  // token-striped output (sequence-parallel layout)
@@ -339,6 +441,16 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
   p.status = static_cast<int32_t*>(workspace);
   p.timeout_ns = plan->timeout_ns;
   p.stall_injection = plan->stall_injection;
+  p.sk.on = 0;
+  p.sk.dp_tiles = p.total_tiles;
+  if (B.tc) {
+    for (int i = 0; i < p.num_probs; ++i) {
+      Prob& P = p.probs[i];
+      P.kblocks = 0;
+      for (int sg = P.seg_begin; sg < P.seg_begin + P.seg_count; ++sg) P.kblocks += (p.segs[sg].K + kTcBK - 1) / kTcBK;
+    }
+    if (sk_workspace) plan_stream_k(p, tc_gemm_max_pairs(tag), plan->stream_k);
+  }
   cudaError_t e;
   if (B.tc) {
     e = launch_tc_gemm(p, tag, di.sms / 2, stream);
@@ -453,7 +565,8 @@ tpmlp_status fwd_column(const tpmlp_plan* pl, const DeviceInfo& di, const void* 
 }
 
 tpmlp_status fwd_row(const tpmlp_plan* pl, const DeviceInfo& di, const void* const* W2, const void* b2, void* Y,
-                     void* const* H, void* ws, cudaStream_t st, void* const* Y_stripes = nullptr) {
+                     void* const* H, void* ws, cudaStream_t st, void* const* Y_stripes = nullptr,
+                     bool sk_workspace = true) {
   if (pl->T == 0) return TPMLP_OK;
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
   if (Y_stripes) {  // reduce-scatter: the summed rows of stripe j go to Y_j
@@ -467,7 +580,7 @@ tpmlp_status fwd_row(const tpmlp_plan* pl, const DeviceInfo& di, const void* con
   // g operator: every shard's H_i W2_i accumulates into the same tile.
   for (int i = 0; i < pl->t; ++i) B.add_seg(P, H[i], pl->T, pl->d_i[i], W2[i], pl->d_i[i], pl->d, nullptr, pl->d_i[i]);
   B.end_group();
-  return launch(B, TAG_FWD_ROW, di, pl, ws, st);
+  return launch(B, TAG_FWD_ROW, di, pl, ws, st, sk_workspace);
 }
 
 // With recompute, H is an output: the dgrad epilogue writes H_i = act(saved_i)
@@ -776,6 +889,7 @@ tpmlp_status tpmlp_plan_create(const tpmlp_desc* desc, tpmlp_plan** out) {
   pl->dtype = desc->dtype;
   pl->timeout_ns = kDefaultTimeoutNs;
   pl->stall_injection = 0;
+  pl->stream_k = TPMLP_STREAM_K_AUTO;
   if (const char* s = std::getenv("TPMLP_WAIT_TIMEOUT_MS")) {
     const long long ms = std::atoll(s);
     if (ms > 0) pl->timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
@@ -801,7 +915,19 @@ tpmlp_status tpmlp_plan_set_stall_injection(tpmlp_plan* plan, int enable) {
   return TPMLP_OK;
 }
 
-size_t tpmlp_workspace_size(const tpmlp_plan* plan) { return plan ? 256 : 0; }
+size_t tpmlp_workspace_size(const tpmlp_plan* plan) {
+  if (!plan) return 0;
+  return plan->dtype == TPMLP_BF16 ? kSkWorkspaceBytes : kStatusBytes;
+}
+
+tpmlp_status tpmlp_plan_set_stream_k(tpmlp_plan* plan, int mode) {
+  g_last_error[0] = 0;
+  if (!plan) return fail(TPMLP_ERR_INVALID_ARG, "plan is NULL");
+  if (mode != TPMLP_STREAM_K_OFF && mode != TPMLP_STREAM_K_AUTO && mode != TPMLP_STREAM_K_ALWAYS)
+    return fail(TPMLP_ERR_INVALID_ARG, "stream-K mode %d is not one of 0, 1, 2", mode);
+  plan->stream_k = mode;
+  return TPMLP_OK;
+}
 
 // Optional bias arrays: NULL, or t pointers each non-NULL and 16-byte aligned.
 tpmlp_status check_bias(const char* name, const void* const* b, int t) {
@@ -847,7 +973,7 @@ tpmlp_status tpmlp_forward_row_noalloc(const tpmlp_plan* plan, const void* const
   TPMLP_TRY(check_kind(plan, PLAN_MLP));
   DeviceInfo di;
   TPMLP_TRY(device_info(&di));  // also makes the device's primary context current
-  const size_t need = tpmlp_workspace_size(plan);
+  const size_t need = kStatusBytes;  // the status word only: no stream-K tail here
   if (need > kStaticScratchBytes)
     return fail(TPMLP_ERR_UNSUPPORTED, "this plan needs %zu bytes of scratch; the static scratch holds %zu", need,
                 kStaticScratchBytes);
@@ -861,7 +987,7 @@ tpmlp_status tpmlp_forward_row_noalloc(const tpmlp_plan* plan, const void* const
   // The status word must start at zero; the array keeps the last call's contents.
   cudaError_t e = cudaMemsetAsync(scratch, 0, need, st);
   if (e != cudaSuccess) return cuda_fail(e);
-  TPMLP_TRY(fwd_row(plan, di, W2, nullptr, Y, H, scratch, st));
+  TPMLP_TRY(fwd_row(plan, di, W2, nullptr, Y, H, scratch, st, nullptr, /*sk_workspace=*/false));
   int32_t word = 0;
   e = cudaMemcpyAsync(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -1042,6 +1168,7 @@ tpmlp_status tpmlp_attn_plan_create(const tpmlp_attn_desc* desc, tpmlp_plan** ou
   pl->dtype = desc->dtype;
   pl->timeout_ns = kDefaultTimeoutNs;
   pl->stall_injection = 0;
+  pl->stream_k = TPMLP_STREAM_K_AUTO;
   if (const char* s = std::getenv("TPMLP_WAIT_TIMEOUT_MS")) {
     const long long ms = std::atoll(s);
     if (ms > 0) pl->timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
@@ -1204,7 +1331,10 @@ tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpmlp_stream_t
   e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e);
   if (word != kDevOk) {
-    e = cudaMemset(workspace, 0, sizeof(word));
+    // Clear the status word and, for bf16 plans, the stream-K flags that an
+    // aborted launch may have left raised.
+    const size_t n = plan->dtype == TPMLP_BF16 ? kSkSlotsOffset : sizeof(word);
+    e = cudaMemset(workspace, 0, n);
     if (e != cudaSuccess) return cuda_fail(e);
     return TPMLP_ERR_DEVICE_TIMEOUT;
   }
@@ -1227,7 +1357,7 @@ const char* tpmlp_status_string(tpmlp_status s) {
 
 int tpmlp_last_cuda_error(void) { return g_last_cuda_error; }
 const char* tpmlp_last_error(void) { return g_last_error; }
-int tpmlp_version(void) { return 103; }
+int tpmlp_version(void) { return 104; }
 int tpmlp_last_launch_count(void) { return g_last_launches; }
 
 }  // extern "C"

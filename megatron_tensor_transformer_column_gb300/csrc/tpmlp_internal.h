@@ -80,6 +80,8 @@ struct Prob {
   int32_t epi;
   int32_t out_map[3];  // tensor maps of out0..out2 for TMA stores (-1: none)
   int32_t out_striped; // out0 is the launch's striped output (token stripes)
+  int32_t kblocks;     // K blocks of a tile, over all segments (tensor-core path)
+  int32_t pad_;
   int64_t ldo;       // row stride of out*/aux*, in elements
   void* out0;
   void* out1;
@@ -114,9 +116,39 @@ struct Stripes {
   int64_t in_ld, out_ld;            // row strides of the stripes, in elements
 };
 
+// Stream-K tail (tensor-core path).  Tiles [0, dp_tiles) are dealt out round
+// robin, tile i to pair i mod pairs.  The K blocks of the remaining tiles,
+// in tile order, are cut into one contiguous range per pair, sized so that
+// every pair ends with about the same number of K blocks; range r (held by
+// pair pairs - 1 - r) starts at (start_tile[r], start_kb[r]) and ends where
+// range r + 1 starts.  A tile cut between ranges is finished by the pair
+// holding its K block 0 (the owner: that part is the last of its range);
+// each other part is the first of its range, and its pair leaves the fp32
+// accumulator in the range's workspace slot and raises one flag per epilogue
+// warp.  The owner adds the parts in range order, so the result is the same
+// on every run.  Owners wait only on lower-numbered pairs, which the hardware
+// starts first.
+constexpr int kMaxSkPairs = 80;
+constexpr int kSkWarpsPerPair = 16;                        // epilogue warps of a pair
+constexpr size_t kStatusBytes = 256;                       // workspace: status word block
+constexpr size_t kSkFlagsOffset = kStatusBytes;            // kMaxSkPairs x kSkWarpsPerPair uint32 flags
+constexpr size_t kSkSlotsOffset = 8192;                    // partial accumulators, one slot per range
+constexpr size_t kSkSlotBytes = 256 * 256 * sizeof(float);
+constexpr size_t kSkWorkspaceBytes = kSkSlotsOffset + kMaxSkPairs * kSkSlotBytes;
+static_assert(kSkFlagsOffset + kMaxSkPairs * kSkWarpsPerPair * sizeof(uint32_t) <= kSkSlotsOffset, "flags fit");
+struct StreamK {
+  int32_t on;
+  int32_t dp_tiles;  // data-parallel tiles (all of them when on == 0)
+  int32_t pairs;     // pairs the ranges were made for (the launched pairs)
+  uint32_t epoch;    // value of a raised flag in this launch (never 0)
+  int32_t start_tile[kMaxSkPairs + 1];
+  int32_t start_kb[kMaxSkPairs + 1];
+};
+
 struct GemmParams {
   CUtensorMap maps[kMaxMaps];
   Stripes stripes;
+  StreamK sk;
   Prob probs[kMaxProbs];
   Group groups[kMaxGroups];
   Seg segs[kMaxSegs];
@@ -158,12 +190,21 @@ constexpr int32_t kDevOk = 0;
 constexpr int32_t kDevTimeoutProducer = 1;
 constexpr int32_t kDevTimeoutMma = 2;
 constexpr int32_t kDevTimeoutEpilogue = 3;
+constexpr int32_t kDevTimeoutPartial = 4;  // an owner waited too long for another pair's partial
 
 // Launchers (defined next to their kernels).
 int tc_gemm_max_smem_bytes();
-// Launches clusters of two CTAs, as many pairs as fit on the device (at most
-// one per tile); max_pairs_hint is used if the occupancy query fails.
+// Launches clusters of two CTAs: p.sk.pairs of them when the stream-K tail is
+// on, else as many as fit on the device (at most one per tile);
+// max_pairs_hint is used if the occupancy query fails.
 cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int max_pairs_hint, cudaStream_t stream);
+// Pairs (clusters of two CTAs) of a launch kind that can be resident at once
+// on the current device (0 if the query fails).
+int tc_gemm_max_pairs(int kernel_tag);
+// The stream-K variant's kernel of a launch kind (tc_gemm_sk.cu; same
+// resources as the data-parallel kernel), or null for an unknown tag.
+using TcKernelFn = void (*)(GemmParams);
+TcKernelFn tc_gemm_sk_kernel(int kernel_tag);
 cudaError_t launch_simt_gemm(const GemmParams& p, cudaStream_t stream);
 
 // Kernel tags: one kernel symbol per launch kind, so that profiles tell the

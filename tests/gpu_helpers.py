@@ -33,11 +33,14 @@ def to_np(x: torch.Tensor) -> np.ndarray:
     return x.detach().to("cpu", torch.float64).numpy()
 
 
-def run_gpu(tp, inp: si.Inputs, act: str, dtype: str, d_i=None, device="cuda"):
-    """Forward + backward through the binding.  Returns a dict of device tensors."""
+def run_gpu(tp, inp: si.Inputs, act: str, dtype: str, d_i=None, device="cuda", stream_k=None):
+    """Forward + backward through the binding.  Returns a dict of device tensors.
+    stream_k: the plan's stream-K mode (None: the default, automatic)."""
     d_i = tuple(d_i if d_i is not None else inp.d_i)
     T, d = inp.X.shape
     mlp = tp.ShardedMLP(T, d, d_i, act, dtype, device=device)
+    if stream_k is not None:
+        tp.tpmlp_plan_set_stream_k(mlp.plan, stream_k)
     X = inp.X.to(device)
     dY = inp.dY.to(device)
     sl = si.shard_slices(d_i)

@@ -12,6 +12,7 @@ import megatron_tensor_transformer_column_gb300 as tp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "tpmlp.h")
+SK_WORKSPACE = 8192 + 80 * 256 * 256 * 4  # status block, stream-K flags, 80 partial slots
 
 
 @pytest.fixture(scope="module")
@@ -47,7 +48,7 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert tp.tpmlp_version() == 103
+    assert tp.tpmlp_version() == 104
     for code, name in tp.STATUS.items():
         assert tp.tpmlp_status_string(code) == name
     assert tp.tpmlp_status_string(99) == "TPMLP_ERR_UNKNOWN"
@@ -72,7 +73,7 @@ def test_version_and_status_strings(lib):
 def test_plan_validation(lib, args, status):
     if status == 0:
         p = tp.Plan(*args)
-        assert tp.tpmlp_workspace_size(p) == 256
+        assert tp.tpmlp_workspace_size(p) == (SK_WORKSPACE if args[4] == "bf16" else 256)
     else:
         with pytest.raises(tp.TpmlpError) as e:
             tp.Plan(*args)
@@ -116,7 +117,7 @@ def test_no_cpu_fallback_without_gpu(lib):
 def test_attn_plan_validation(lib, args, status):
     if status == 0:
         p = tp.AttnPlan(*args)
-        assert tp.tpmlp_workspace_size(p) == 256
+        assert tp.tpmlp_workspace_size(p) == (SK_WORKSPACE if args[4] == "bf16" else 256)
         assert p.d_i == tuple(q + 2 * kv for q, kv in zip(args[2], args[3]))
     else:
         with pytest.raises(tp.TpmlpError) as e:
@@ -191,3 +192,16 @@ def test_sp_no_cpu_fallback_without_gpu(lib):
         tp.tpmlp_forward_sp(p, [fake, fake], [fake], None, [fake], None, None, None, [fake, fake], [fake], [fake],
                             fake, stream=0)
     assert e.value.status in (4, 5)
+
+
+def test_stream_k_mode_validation(lib):
+    p = tp.Plan(512, 64, [64], "gelu", "bf16")
+    for mode in (tp.STREAM_K_OFF, tp.STREAM_K_ALWAYS, tp.STREAM_K_AUTO):
+        tp.tpmlp_plan_set_stream_k(p, mode)
+    for bad in (-1, 3, 100):
+        with pytest.raises(tp.TpmlpError) as e:
+            tp.tpmlp_plan_set_stream_k(p, bad)
+        assert e.value.status == 1
+    assert lib.tpmlp_plan_set_stream_k(None, 1) == 1
+    a = tp.AttnPlan(512, 64, [64], [64], "bf16")
+    tp.tpmlp_plan_set_stream_k(a, tp.STREAM_K_OFF)

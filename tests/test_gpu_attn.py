@@ -21,9 +21,11 @@ from gpu_helpers import cat_cols, cat_rows, rel_err, to_np, tol_for
 pytestmark = pytest.mark.gpu
 
 
-def run_attn(tp, a: si.AttnInputs, dtype: str, device="cuda"):
+def run_attn(tp, a: si.AttnInputs, dtype: str, device="cuda", stream_k=None):
     T, d = a.X.shape
     m = tp.ShardedAttentionProj(T, d, a.dq_i, a.dkv_i, dtype, device=device)
+    if stream_k is not None:
+        tp.tpmlp_plan_set_stream_k(m.plan, stream_k)
     X = a.X.to(device)
     Wqkv = [w.to(device) for w in a.Wqkv_i]
     O = [o.to(device) for o in a.O_i]
@@ -48,9 +50,9 @@ def split_qkv(mats, dq_i, dkv_i):
     return cat_cols(q), cat_cols(k), cat_cols(v)
 
 
-def _full_compare(tp, T, d, dq_i, dkv_i, dtype, seed=1234):
+def _full_compare(tp, T, d, dq_i, dkv_i, dtype, seed=1234, stream_k=None):
     a = si.make_attn_inputs(T, d, dq_i, dkv_i, dtype, seed)
-    g = run_attn(tp, a, dtype)
+    g = run_attn(tp, a, dtype, stream_k=stream_k)
     f = oracle.attn_forward(a.X, a.WQ, a.WK, a.WV, a.O, a.WO)
     b = oracle.attn_backward(a.X, a.WQ, a.WK, a.WV, a.O, a.WO, a.dZ, a.dQ, a.dK, a.dV)
     Q, K, V = split_qkv(g["QKV"], dq_i, dkv_i)
@@ -76,6 +78,11 @@ SMALL = [
 @pytest.mark.parametrize("case", SMALL)
 def test_attn_small_bf16_all_outputs(gpu_lib, case):
     _full_compare(gpu_lib, *case, "bf16")
+
+
+@pytest.mark.parametrize("case", SMALL[:3])
+def test_attn_small_stream_k_always(gpu_lib, case):
+    _full_compare(gpu_lib, *case, "bf16", stream_k=gpu_lib.STREAM_K_ALWAYS)
 
 
 def test_attn_multi_wave_bf16(gpu_lib):

@@ -18,9 +18,9 @@ from gpu_helpers import cat_cols, cat_rows, rel_err, run_gpu, to_np, tol_for
 pytestmark = pytest.mark.gpu
 
 
-def _full_compare(tp, T, d, d_i, act, dtype, seed=1234, check_intermediates=True):
+def _full_compare(tp, T, d, d_i, act, dtype, seed=1234, check_intermediates=True, stream_k=None):
     inp = si.make_inputs(T, d, d_i, act, dtype, seed)
-    g = run_gpu(tp, inp, act, dtype)
+    g = run_gpu(tp, inp, act, dtype, stream_k=stream_k)
     f = oracle.forward(inp.X, inp.W1, inp.W2, act=act, W3=inp.W3)
     b = oracle.backward(inp.X, inp.W1, inp.W2, inp.dY, act=act, W3=inp.W3)
     tol = tol_for(dtype)
@@ -79,6 +79,47 @@ def test_fp32_path(gpu_lib, act, case):
     _full_compare(gpu_lib, T, d, d_i, act, "fp32")
 
 
+# ------------------------------------------------------------- stream-K tail
+# Cases whose launches cut tiles into parts spread over many pairs: parts
+# that start inside a later shard's segment (row and dX launches), ragged K
+# blocks, partial tiles, SwiGLU tiles in both MMA forms (merged N = 256 for
+# full tiles, split for partial ones).
+SK_CASES = [
+    (1024, 384, (512, 384, 640, 256)),
+    (333, 200, (8, 96, 264, 152)),
+    (257, 136, (120, 392)),
+    (2000, 520, (1024, 136)),
+    (640, 1000, (256, 256, 256, 256)),
+]
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("case", SK_CASES, ids=[f"T{c[0]}_d{c[1]}_t{len(c[2])}" for c in SK_CASES])
+def test_stream_k_always_bf16_all_outputs(gpu_lib, act, case):
+    T, d, d_i = case
+    _full_compare(gpu_lib, T, d, d_i, act, "bf16", stream_k=gpu_lib.STREAM_K_ALWAYS)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_stream_k_deterministic_and_within_bound_of_round_robin(gpu_lib, act):
+    """The parts of a split tile are added in a fixed order: two runs agree bit
+    for bit.  Against plain round robin (one K loop per tile) only the fp32
+    summation order differs."""
+    T, d, d_i = 1024, 384, (512, 384, 640, 256)
+    inp = si.make_inputs(T, d, d_i, act, "bf16", seed=77)
+    runs = [run_gpu(gpu_lib, inp, act, "bf16", stream_k=m)
+            for m in (gpu_lib.STREAM_K_ALWAYS, gpu_lib.STREAM_K_ALWAYS, gpu_lib.STREAM_K_OFF)]
+    keys = ("Y", "dX")
+    lists = ("dW1", "dW2", "H", "saved", "dact") + (("dW3",) if act == "swiglu" else ())
+    for k in keys:
+        assert torch.equal(runs[0][k], runs[1][k]), k
+        assert rel_err(to_np(runs[0][k]), to_np(runs[2][k])) <= 1e-2, k
+    for k in lists:
+        for a, b, c in zip(runs[0][k], runs[1][k], runs[2][k]):
+            assert torch.equal(a, b), k
+            assert rel_err(to_np(a), to_np(c)) <= 1e-2, k
+
+
 def test_config_C1_fp32(gpu_lib):
     w = si.WORKLOADS["C1"]
     _full_compare(gpu_lib, w.T, w.d, w.d_i, w.act, w.dtype)
@@ -86,9 +127,9 @@ def test_config_C1_fp32(gpu_lib):
 
 # ------------------------------------------------------------- full-size workloads (sampled)
 
-def _sampled_compare(tp, w: si.Workload, nrows=24, nunits=24, seed=1234, extra_rows=()):
+def _sampled_compare(tp, w: si.Workload, nrows=24, nunits=24, seed=1234, extra_rows=(), stream_k=None):
     inp = si.make_workload_inputs(w, seed)
-    g = run_gpu(tp, inp, w.act, w.dtype)
+    g = run_gpu(tp, inp, w.act, w.dtype, stream_k=stream_k)
     rng = np.random.default_rng(7)
     rows = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, nrows, replace=False),
                                      np.asarray(extra_rows, dtype=np.int64)]))
@@ -119,6 +160,13 @@ def _sampled_compare(tp, w: si.Workload, nrows=24, nunits=24, seed=1234, extra_r
 @pytest.mark.parametrize("name", ["C2t1", "C2t2", "C2t4", "C3", "C4", "C5"])
 def test_workload_sampled_parity(gpu_lib, name):
     _sampled_compare(gpu_lib, si.WORKLOADS[name])
+
+
+@pytest.mark.parametrize("name", ["C2t4", "C4"])
+def test_workload_sampled_parity_stream_k_always(gpu_lib, name):
+    """The stream-K tail on every launch of the workload (C4: SwiGLU with
+    merged N = 256 MMAs; C2: tiles split across many pairs)."""
+    _sampled_compare(gpu_lib, si.WORKLOADS[name], stream_k=gpu_lib.STREAM_K_ALWAYS)
 
 
 def test_C2_shard_count_invariance(gpu_lib):

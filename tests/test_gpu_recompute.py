@@ -13,9 +13,11 @@ from gpu_helpers import cat_cols, cat_rows, rel_err, to_np, tol_for
 pytestmark = pytest.mark.gpu
 
 
-def _fwd(tp, inp, act, dtype, bias=None):
+def _fwd(tp, inp, act, dtype, bias=None, stream_k=None):
     T, d = inp.X.shape
     mlp = tp.ShardedMLP(T, d, inp.d_i, act, dtype)
+    if stream_k is not None:
+        tp.tpmlp_plan_set_stream_k(mlp.plan, stream_k)
     cu = lambda xs: [x.cuda() for x in xs] if xs is not None else None
     X, dY = inp.X.cuda(), inp.dY.cuda()
     W1, W2, W3 = cu(inp.W1_i), cu(inp.W2_i), cu(inp.W3_i)
@@ -59,10 +61,12 @@ def test_recompute_matches_oracle(gpu_lib, act, dtype, with_bias):
 
 @pytest.mark.parametrize("act", ["gelu", "swiglu"])
 def test_recompute_same_activation_gradients(gpu_lib, act):
-    """dact, dX and dW1 (dW3) come from identical arithmetic in both modes."""
+    """dact, dX and dW1 (dW3) come from identical arithmetic in both modes.
+    With the stream-K tail off: recompute moves the dW2 tiles into the second
+    launch, and the tail cuts that launch's tiles differently."""
     tp = gpu_lib
     inp = si.make_inputs(1024, 384, (512, 384, 640, 256), act, "bf16", seed=23)
-    mlp, X, dY, W1, W2, W3, Y, saved, H = _fwd(tp, inp, act, "bf16")
+    mlp, X, dY, W1, W2, W3, Y, saved, H = _fwd(tp, inp, act, "bf16", stream_k=tp.STREAM_K_OFF)
     ref = mlp.backward(X, W1, W2, saved, H, dY, W3)
     H2 = [torch.full_like(h, float("nan")) for h in H]
     rec = mlp.backward(X, W1, W2, saved, H2, dY, W3, recompute=True)

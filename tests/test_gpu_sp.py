@@ -23,9 +23,11 @@ def _cut(M, rows):
     return out
 
 
-def run_sp(tp, inp, act, dtype, rows, bias=None):
+def run_sp(tp, inp, act, dtype, rows, bias=None, stream_k=None):
     T, d = inp.X.shape
     mlp = tp.ShardedMLP(T, d, inp.d_i, act, dtype)
+    if stream_k is not None:
+        tp.tpmlp_plan_set_stream_k(mlp.plan, stream_k)
     mlp.set_sequence_stripes(rows)
     X_j = [x.cuda() for x in _cut(inp.X, rows)]
     dY_j = [x.cuda() for x in _cut(inp.dY, rows)]
@@ -51,12 +53,16 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("stream_k", [None, "always"])
 @pytest.mark.parametrize("act,shape,rows", CASES)
-def test_sp_matches_oracle(gpu_lib, act, shape, rows):
+def test_sp_matches_oracle(gpu_lib, act, shape, rows, stream_k):
+    """stream_k "always": the stream-K tail on every launch, so that parts
+    start inside the MN-major token walks across the stripes."""
     T, d, d_i = shape
     inp = si.make_inputs(T, d, d_i, act, "bf16", seed=31)
     bias = si.make_biases(d, d_i, act, "bf16", seed=31)
-    Y_j, H, g = run_sp(gpu_lib, inp, act, "bf16", rows, bias)
+    Y_j, H, g = run_sp(gpu_lib, inp, act, "bf16", rows, bias,
+                       stream_k=gpu_lib.STREAM_K_ALWAYS if stream_k else None)
     W3 = inp.W3_i if act == "swiglu" else None
     b3 = bias["b3_i"] if act == "swiglu" else None
     Yr_j, H_r = oracle.forward_sp(_cut(inp.X, rows), inp.W1_i, inp.W2_i, act=act, W3_i=W3, b1_i=bias["b1_i"],
