@@ -363,8 +363,14 @@ void plan_stream_k(GemmParams& p, int pairs, int mode) {
   const int dp_tiles = (n / pairs) * pairs;
   const int R = n - dp_tiles;
   if (R == 0) return;  // no partial wave
-  std::vector<int32_t> kb(n);
-  for (int t = 0; t < n; ++t) kb[t] = p.probs[tile_prob(p, t)].kblocks;
+  // Auto mode needs tiles of one depth; that holds exactly when every
+  // problem has the same K blocks, which spares the per-tile walk below.
+  bool same_depth = true;
+  for (int i = 1; i < p.num_probs; ++i) same_depth = same_depth && p.probs[i].kblocks == p.probs[0].kblocks;
+  if (!same_depth && mode == TPMLP_STREAM_K_AUTO) return;
+  std::vector<int32_t> kb(n, p.probs[0].kblocks);
+  if (!same_depth)
+    for (int t = 0; t < n; ++t) kb[t] = p.probs[tile_prob(p, t)].kblocks;
   std::vector<int64_t> dp(pairs, 0);
   for (int t = 0; t < dp_tiles; ++t) dp[t % pairs] += kb[t];
   const int64_t dp_lo = *std::min_element(dp.begin(), dp.end());
