@@ -326,7 +326,11 @@ TPMLP_API tpmlp_status tpmlp_attn_qkv_backward(const tpmlp_plan* plan, const voi
  *     TPMLP_ERR_DEVICE_TIMEOUT in the status word, every role leaves its loop,
  *     the CTAs free their TMEM and exit, and the CUDA context stays usable.
  *     Outputs are undefined while it is enabled.  The fp32 path has no waits
- *     and ignores it.                                                        */
+ *     and ignores it.  enable == 2 instead keeps the loads and withholds the
+ *     stream-K tail's parts (see tpmlp_plan_set_stream_k): the owners of the
+ *     split tiles wait for flags that nothing raises, their bounded waits run
+ *     out and the kernel records TPMLP_ERR_DEVICE_TIMEOUT the same way;
+ *     tpmlp_check then clears the status word and the tail's flags.          */
 TPMLP_API tpmlp_status tpmlp_plan_set_timeout(tpmlp_plan* plan, uint32_t timeout_ms);
 TPMLP_API tpmlp_status tpmlp_plan_set_stall_injection(tpmlp_plan* plan, int enable);
 

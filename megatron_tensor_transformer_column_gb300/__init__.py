@@ -304,8 +304,10 @@ def tpmlp_plan_set_timeout(plan: Plan, timeout_ms: int):
     _ok(load().tpmlp_plan_set_timeout(plan.handle, int(timeout_ms)), "tpmlp_plan_set_timeout")
 
 
-def tpmlp_plan_set_stall_injection(plan: Plan, enable: bool):
-    _ok(load().tpmlp_plan_set_stall_injection(plan.handle, 1 if enable else 0), "tpmlp_plan_set_stall_injection")
+def tpmlp_plan_set_stall_injection(plan: Plan, enable):
+    """False / True (1): producers load nothing; 2: stream-K parts are never published."""
+    mode = 2 if enable == 2 else (1 if enable else 0)
+    _ok(load().tpmlp_plan_set_stall_injection(plan.handle, mode), "tpmlp_plan_set_stall_injection")
 
 
 STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_ALWAYS = 0, 1, 2

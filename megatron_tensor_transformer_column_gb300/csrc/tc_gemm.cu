@@ -231,8 +231,8 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       bool ok = true;
       bool issued = false;
       Cursor ld, pf;
-      cursor_tile(ld, p, p.stall_injection ? p.total_tiles : pair, rank);  // injected stall: nothing to load
-      cursor_tile(pf, p, p.stall_injection ? p.total_tiles : pair, rank);
+      cursor_tile(ld, p, p.stall_injection == 1 ? p.total_tiles : pair, rank);  // injected stall: nothing to load
+      cursor_tile(pf, p, p.stall_injection == 1 ? p.total_tiles : pair, rank);
       for (int i = 0; i < kPrefetchKBlocks && pf.tile < p.total_tiles; ++i) {
         cursor_issue<true>(p, pf, 0, 0);
         cursor_next(pf, p, npairs, rank);

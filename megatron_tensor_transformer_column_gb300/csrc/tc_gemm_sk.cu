@@ -412,7 +412,7 @@ __device__ __forceinline__ void tc_gemm_body_sk(const GemmParams& p, uint8_t* sm
       bool ok = true;
       bool issued = false;
       Cursor ld;
-      sched_init(ld.s, p, p.stall_injection ? -1 : pair, npairs);  // injected stall: nothing to load
+      sched_init(ld.s, p, p.stall_injection == 1 ? -1 : pair, npairs);  // injected stall: nothing to load
       cursor_item(ld, p, rank);
       while (ld.s.tile >= 0) {
         if (!bounded_wait(empty_bar(stage), phase ^ 1u, ctl, kDevTimeoutProducer)) {
@@ -572,7 +572,9 @@ __device__ __forceinline__ void tc_gemm_body_sk(const GemmParams& p, uint8_t* sm
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
       if (part) {
         if (vm > 0) sk_part_store(p, P, it, tacc, half, wi, lane);
-        sk_publish(p, it.r, wi, lane);  // even with nothing stored: the owner waits for every warp
+        // Even with nothing stored: the owner waits for every warp.  (Test hook:
+        // with stall injection 2 no part is published, so the owners' waits run out.)
+        if (p.stall_injection != 2) sk_publish(p, it.r, wi, lane);
       } else {
         if (it.kind == ITEM_OWNER) {
           if (!sk_wait_parts(p, it, wi, lane, ctl)) break;

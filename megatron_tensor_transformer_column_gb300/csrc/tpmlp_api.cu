@@ -917,7 +917,7 @@ tpmlp_status tpmlp_plan_set_timeout(tpmlp_plan* plan, uint32_t timeout_ms) {
 tpmlp_status tpmlp_plan_set_stall_injection(tpmlp_plan* plan, int enable) {
   g_last_error[0] = 0;
   if (!plan) return fail(TPMLP_ERR_INVALID_ARG, "plan is NULL");
-  plan->stall_injection = enable ? 1 : 0;
+  plan->stall_injection = enable == 2 ? 2 : (enable ? 1 : 0);
   return TPMLP_OK;
 }
 

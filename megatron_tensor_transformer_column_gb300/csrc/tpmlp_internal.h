@@ -157,7 +157,7 @@ struct GemmParams {
   int32_t tile_m;
   int32_t* status;          // device status word (workspace)
   uint64_t timeout_ns;      // bound on every wait inside the kernel
-  int32_t stall_injection;  // test hook: producers load nothing, so the waits run out
+  int32_t stall_injection;  // test hook: 1, producers load nothing; 2, stream-K parts are never published
 };
 
 // Column sums over tokens (bias gradients): dst[c] = sum_r src[r][c].
