@@ -71,6 +71,45 @@ def attn_phase_flops(w: si.AttnWorkload, T: int | None = None, n_i=None, dq_i=No
             "qkv_bwd": 4 * T * w.d * N}
 
 
+def _rec(ev, i, stream):
+    """Record event i of a step's event list, if the list has one there."""
+    if ev is not None and ev[i] is not None:
+        ev[i].record(stream)
+
+
+def pick_dominant(step, names, dev, drop=()):
+    """Per-launch timing that does not slow the timed steps: three untimed
+    steps after the warm-up, with an event between every launch, give each
+    phase's duration and pick the longest; the timed steps then carry events
+    only around that one (dominant_events).  Returns (phase ms, name, index)."""
+    import torch
+    pre = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(3)]
+    for ev in pre:
+        step(ev)
+    torch.cuda.synchronize(dev)
+    phase = {n: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in pre) for i, n in enumerate(names)}
+    for n in drop:
+        phase.pop(n, None)
+    dom = max(phase, key=phase.get)
+    return phase, dom, names.index(dom)
+
+
+def dominant_events(steps, nphase, di):
+    """Per-step event lists with events only at the dominant launch's two ends."""
+    import torch
+    out = []
+    for _ in range(steps):
+        ev = [None] * (nphase + 1)
+        ev[di] = torch.cuda.Event(enable_timing=True)
+        ev[di + 1] = torch.cuda.Event(enable_timing=True)
+        out.append(ev)
+    return out
+
+
+PHASE_NOTE = ("the dominant launch: mean over the timed steps, whose only per-launch events bracket it; "
+              "the others: three untimed steps after the warm-up")
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -394,42 +433,38 @@ def run_ours(args, w: si.Workload):
 
     def step(ev=None):
         if args.recompute:  # backward with H recomputed from the pre-activations (H treated as scratch)
-            if ev:
-                ev[0].record(stream)
+            _rec(ev, 0, stream)
             tp.tpmlp_forward_column(plan, X, W1, W3, b1, b3, saved, H, wsp, stream)
-            if ev:
-                ev[1].record(stream)
+            _rec(ev, 1, stream)
             tp.tpmlp_forward_row(plan, W2, b2, H, Y, wsp, stream)
-            if ev:
-                ev[2].record(stream)
-                ev[3].record(stream)
+            _rec(ev, 2, stream)
+            _rec(ev, 3, stream)
             tp.tpmlp_backward_recompute(plan, X, W1, W3, W2, saved, H, dY, dact, dX, dW1, dW3, dW2, db1, db3, db2,
                                         wsp, stream)
-            if ev:
-                ev[4].record(stream)
+            _rec(ev, 4, stream)
             return
-        if ev:
-            ev[0].record(stream)
+        _rec(ev, 0, stream)
         tp.tpmlp_forward_column(plan, X, W1, W3, b1, b3, saved, H, wsp, stream)
-        if ev:
-            ev[1].record(stream)
+        _rec(ev, 1, stream)
         tp.tpmlp_forward_row(plan, W2, b2, H, Y, wsp, stream)
-        if ev:
-            ev[2].record(stream)
+        _rec(ev, 2, stream)
         tp.tpmlp_backward_dgrad(plan, W2, saved, H, dY, dact, dW2, db2, wsp, stream)
-        if ev:
-            ev[3].record(stream)
+        _rec(ev, 3, stream)
         tp.tpmlp_backward_fsum(plan, X, W1, W3, dact, dX, dW1, dW3, db1, db3, wsp, stream)
-        if ev:
-            ev[4].record(stream)
+        _rec(ev, 4, stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     mlp.check(stream)
 
+    names = ["fwd_column", "fwd_row", "bwd_dgrad", "bwd_fsum"]
+    if args.recompute:
+        names = ["fwd_column", "fwd_row", "bwd_none", "bwd_recompute"]
+    per_phase, dom, di = pick_dominant(step, names, dev, drop=("bwd_none",))
+
     # ---- timed region: K steps, CUDA events on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = dominant_events(args.steps, len(names), di)
     barrier(ws)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
@@ -447,11 +482,7 @@ def run_ours(args, w: si.Workload):
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
     ms_per_step = elapsed_ms / args.steps
-    names = ["fwd_column", "fwd_row", "bwd_dgrad", "bwd_fsum"]
-    if args.recompute:
-        names = ["fwd_column", "fwd_row", "bwd_none", "bwd_recompute"]
-    per_phase = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
-                 for i, n in enumerate(names)}
+    per_phase[dom] = statistics.mean(ev[di].elapsed_time(ev[di + 1]) for ev in evs)
     total_flops = flops_fwd_bwd(w) * ws
     value = total_flops * args.steps / (elapsed_ms / 1e3) / 1e12
 
@@ -463,8 +494,6 @@ def run_ours(args, w: si.Workload):
     if args.recompute:
         pf = {"fwd_column": pf["fwd_column"], "fwd_row": pf["fwd_row"], "bwd_none": 0,
               "bwd_recompute": pf["bwd_dgrad"] + pf["bwd_fsum"]}
-        per_phase.pop("bwd_none", None)
-    dom = max(per_phase, key=per_phase.get)
     achieved = pf[dom] / (per_phase[dom] / 1e3) / 1e12
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -490,6 +519,7 @@ def run_ours(args, w: si.Workload):
         "pct_of_peak": {"sustained": value / ws / peak_sus, "burst": value / ws / peak_burst, "source": peak_src},
         "tokens_per_s": w.T * ws * args.steps / (elapsed_ms / 1e3),
         "phase_ms": per_phase,
+        "phase_ms_note": PHASE_NOTE,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -638,17 +668,17 @@ def run_ours_attn(args, w: si.AttnWorkload):
                  lambda: tp.tpmlp_attn_out_backward(plan, WO, O, dZ, dO, dWO, wsp, stream),
                  lambda: tp.tpmlp_attn_qkv_backward(plan, X, Wqkv, dQKV, dX, dWqkv, wsp, stream))
         for i, c in enumerate(calls):
-            if ev:
-                ev[i].record(stream)
+            _rec(ev, i, stream)
             c()
-        if ev:
-            ev[4].record(stream)
+        _rec(ev, 4, stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     m.check(stream)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    names = ["qkv_fwd", "out_fwd", "out_bwd", "qkv_bwd"]
+    per_phase, dom, di = pick_dominant(step, names, dev)
+    evs = dominant_events(args.steps, len(names), di)
     barrier(ws)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
@@ -664,9 +694,7 @@ def run_ours_attn(args, w: si.AttnWorkload):
     barrier(ws)
     m.check(stream)
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), ws, dev)
-    names = ["qkv_fwd", "out_fwd", "out_bwd", "qkv_bwd"]
-    per_phase = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
-                 for i, n in enumerate(names)}
+    per_phase[dom] = statistics.mean(ev[di].elapsed_time(ev[di + 1]) for ev in evs)
     pf = attn_phase_flops(w)
     step_flops = sum(pf.values())
     value = step_flops * ws * args.steps / (elapsed_ms / 1e3) / 1e12
@@ -706,7 +734,6 @@ def run_ours_attn(args, w: si.AttnWorkload):
                   "read back every step on copy streams overlapped with compute; weights resident"}
 
     peaks, peak_src = load_peaks()
-    dom = max(per_phase, key=per_phase.get)
     achieved = pf[dom] / (per_phase[dom] / 1e3) / 1e12
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -727,7 +754,7 @@ def run_ours_attn(args, w: si.AttnWorkload):
         "config": attn_workload_config(w, {"parallelism": f"replicas x{ws} (t={w.t} shards on each GPU)", "stream_k": args.stream_k}),
         "pct_of_peak": {"sustained": value / ws / peak_sus, "burst": value / ws / peak_burst, "source": peak_src},
         "tokens_per_s": w.T * ws * args.steps / (elapsed_ms / 1e3),
-        "phase_ms": per_phase, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "phase_ms": per_phase, "phase_ms_note": PHASE_NOTE, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": 4 * args.steps, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -773,21 +800,20 @@ def run_ours_sp(args, w: si.Workload):
     plan, wsp = mlp.plan, mlp.workspace
 
     def step(ev=None):
-        if ev:
-            ev[0].record(stream)
+        _rec(ev, 0, stream)
         tp.tpmlp_forward_sp(plan, X_j, W1, W3, W2, None, None, None, Y_j, saved, H, wsp, stream)
-        if ev:
-            ev[1].record(stream)
+        _rec(ev, 1, stream)
         tp.tpmlp_backward_sp(plan, X_j, W1, W3, W2, saved, H, dY_j, dact, dX_j, dW1, dW3, dW2, None, None, None, wsp,
                              stream)
-        if ev:
-            ev[2].record(stream)
+        _rec(ev, 2, stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     mlp.check(stream)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    names = ["forward_sp", "backward_sp"]
+    per_phase, dom, di = pick_dominant(step, names, dev)
+    evs = dominant_events(args.steps, len(names), di)
     barrier(ws)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
@@ -802,8 +828,7 @@ def run_ours_sp(args, w: si.Workload):
     barrier(ws)
     mlp.check(stream)
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
-    per_phase = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
-                 for i, n in enumerate(["forward_sp", "backward_sp"])}
+    per_phase[dom] = statistics.mean(ev[di].elapsed_time(ev[di + 1]) for ev in evs)
     pf = phase_flops(w)
     pflops = {"forward_sp": pf["fwd_column"] + pf["fwd_row"], "backward_sp": pf["bwd_dgrad"] + pf["bwd_fsum"]}
     value = flops_fwd_bwd(w) * ws * args.steps / (elapsed_ms / 1e3) / 1e12
@@ -838,7 +863,6 @@ def run_ours_sp(args, w: si.Workload):
            "api": "tpmlp_forward_sp + tpmlp_backward_sp; X and dY stripes uploaded from pinned host memory and Y, "
                   "dX stripes read back every step on copy streams overlapped with compute; weights resident"}
     peaks, peak_src = load_peaks()
-    dom = max(per_phase, key=per_phase.get)
     achieved = pflops[dom] / (per_phase[dom] / 1e3) / 1e12
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -857,7 +881,7 @@ def run_ours_sp(args, w: si.Workload):
                                       "layout": f"sequence-parallel: {w.t} token stripes of {rows[0]}"}),
         "pct_of_peak": {"sustained": value / ws / peak_sus, "burst": value / ws / peak_burst, "source": peak_src},
         "tokens_per_s": w.T * ws * args.steps / (elapsed_ms / 1e3),
-        "phase_ms": per_phase, "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
+        "phase_ms": per_phase, "phase_ms_note": PHASE_NOTE, "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
         "gpu_launches": 4 * args.steps, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
