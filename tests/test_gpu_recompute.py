@@ -29,14 +29,17 @@ def _fwd(tp, inp, act, dtype, bias=None, stream_k=None):
 
 
 @pytest.mark.parametrize("act", ["gelu", "swiglu"])
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("dtype,stream_k", [("bf16", False), ("bf16", True), ("fp32", False)])
 @pytest.mark.parametrize("with_bias", [False, True])
-def test_recompute_matches_oracle(gpu_lib, act, dtype, with_bias):
+def test_recompute_matches_oracle(gpu_lib, act, dtype, stream_k, with_bias):
+    """stream_k: the stream-K tail forced on every launch (the H-writing dgrad
+    epilogue and the f-sum launch carrying dW2 then run on split tiles)."""
     tp = gpu_lib
     T, d, d_i = (333, 200, (8, 96, 264, 152)) if dtype == "bf16" else (45, 36, (20, 44))
     inp = si.make_inputs(T, d, d_i, act, dtype, seed=17)
     bias = si.make_biases(d, d_i, act, dtype, seed=17) if with_bias else None
-    mlp, X, dY, W1, W2, W3, Y, saved, H = _fwd(tp, inp, act, dtype, bias)
+    mlp, X, dY, W1, W2, W3, Y, saved, H = _fwd(tp, inp, act, dtype, bias,
+                                               stream_k=tp.STREAM_K_ALWAYS if stream_k else None)
     for h in H:
         h.fill_(float("nan"))
     g = mlp.backward(X, W1, W2, saved, H, dY, W3, bias_grads=with_bias, recompute=True)
