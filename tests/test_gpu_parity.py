@@ -162,6 +162,36 @@ def test_workload_sampled_parity(gpu_lib, name):
     _sampled_compare(gpu_lib, si.WORKLOADS[name])
 
 
+def test_stream_k_soak_bitwise(gpu_lib):
+    """60 forward + backward steps with the stream-K tail forced on (parts of
+    many tiles exchanged between pairs through the workspace every launch):
+    every step's outputs equal the first step's bit for bit -- a lost or
+    early-read partial, or a stale flag from the previous launch, would show
+    up as a difference."""
+    tp = gpu_lib
+    T, d, d_i = 1024, 384, (512, 384, 640, 256)
+    inp = si.make_inputs(T, d, d_i, "swiglu", "bf16", seed=5)
+    mlp = tp.ShardedMLP(T, d, d_i, "swiglu", "bf16")
+    tp.tpmlp_plan_set_stream_k(mlp.plan, tp.STREAM_K_ALWAYS)
+    X, dY = inp.X.cuda(), inp.dY.cuda()
+    W1 = [w.cuda() for w in inp.W1_i]
+    W2 = [w.cuda() for w in inp.W2_i]
+    W3 = [w.cuda() for w in inp.W3_i]
+    ref = None
+    for step in range(60):
+        Y, saved, H = mlp.forward(X, W1, W2, W3)
+        g = mlp.backward(X, W1, W2, saved, H, dY, W3)
+        got = [Y, g["dX"], *g["dW1"], *g["dW2"], *g["dW3"]]
+        if ref is None:
+            torch.cuda.synchronize()
+            ref = [x.clone() for x in got]
+            continue
+        for i, (a, b) in enumerate(zip(got, ref)):
+            assert torch.equal(a, b), f"step {step}: output {i} differs"
+    torch.cuda.synchronize()
+    mlp.check()
+
+
 @pytest.mark.parametrize("name", ["C2t4", "C4"])
 def test_workload_sampled_parity_stream_k_always(gpu_lib, name):
     """The stream-K tail on every launch of the workload (C4: SwiGLU with
