@@ -83,7 +83,7 @@ def _bind(lib):
     lib.oracle_backward_sp.argtypes = [i64, i64, i32, dp, ci, i32, dp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp, pp,
                                        pp, dp]
     lib.oracle_backward_sp.restype = ci
-    lib.oracle_rows.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, dp, i64, dp, dp, dp]
+    lib.oracle_rows.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, dp, i64, dp, dp, dp] + [dp] * 5
     lib.oracle_rows.restype = ci
     lib.oracle_wgrad_units.argtypes = [i64, i64, i64, ci, dp, dp, dp, dp, dp, dp, dp, i64, dp, dp, dp, dp, dp, dp]
     lib.oracle_wgrad_units.restype = ci
@@ -290,8 +290,12 @@ class COracle:
                "oracle_backward_sp")
         return {"dX_j": dX_j, "dW1_i": dW1_i, "dW3_i": dW3_i, "dW2_i": dW2_i, "db1_i": db1_i, "db3_i": db3_i, "db2": db2}
 
-    def rows(self, X, W1, W2, dY, rows_idx, act="gelu", W3=None, b1=None, b3=None, b2=None):
-        """Y[r, :] and dX[r, :] for the listed token rows.  Returns (Y_rows, dX_rows)."""
+    def rows(self, X, W1, W2, dY, rows_idx, act="gelu", W3=None, b1=None, b3=None, b2=None,
+             intermediates=False):
+        """Y[r, :] and dX[r, :] for the listed token rows.  Returns (Y_rows, dX_rows);
+        with intermediates=True (Y_rows, dX_rows, inter), inter holding the same
+        rows of A (SwiGLU: G), H and dA (SwiGLU: dG), and for SwiGLU U and dU,
+        each [len(rows) x dff]."""
         lib = self.lib
         a = _act(act)
         X, W1, W2, W3, dY = _f64(X), _f64(W1), _f64(W2), _f64(W3), _f64(dY)
@@ -300,8 +304,17 @@ class COracle:
         dff = W1.shape[1]
         r = np.ascontiguousarray(rows_idx, dtype=np.int64)
         Yr = np.empty((len(r), d)); dXr = np.empty((len(r), d))
+        sw = act == "swiglu"
+        inter = {}
+        if intermediates:
+            names = ("A", "U", "H", "dA", "dU") if sw else ("A", "H", "dA")
+            inter = {k: np.empty((len(r), dff)) for k in names}
         _check(lib.oracle_rows(T, d, dff, a, _ptr(X), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(b1), _ptr(b3), _ptr(b2),
-                               _ptr(dY), len(r), _ptr(r), _ptr(Yr), _ptr(dXr)), "oracle_rows")
+                               _ptr(dY), len(r), _ptr(r), _ptr(Yr), _ptr(dXr), _ptr(inter.get("A")),
+                               _ptr(inter.get("U")), _ptr(inter.get("H")), _ptr(inter.get("dA")),
+                               _ptr(inter.get("dU"))), "oracle_rows")
+        if intermediates:
+            return Yr, dXr, inter
         return Yr, dXr
 
     def attn_forward(self, X, WQ, WK, WV, O, WO):

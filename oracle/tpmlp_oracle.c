@@ -351,10 +351,16 @@ int oracle_backward_sharded(int64_t T, int64_t d, int32_t t, const int64_t* d_i,
 /* ---- sampled outputs for large problems -----------------------------------
  * oracle_rows: Y[r, :] and dX[r, :] for the listed token rows r, each from
  * its own definition (a token's forward and input gradient depend only on
- * that token's row of X and dY).  Y_rows and dX_rows are [nrows x d].       */
+ * that token's row of X and dY).  Y_rows and dX_rows are [nrows x d].
+ * Optionally (NULL = not wanted) the same rows of the per-token
+ * intermediates, each [nrows x dff]: A_rows = X W1 (+ b1) (SwiGLU: G),
+ * U_rows = X W3 (+ b3) (SwiGLU only), H_rows = act(A) (SwiGLU: U Swish(G)),
+ * dA_rows = the gradient of A (SwiGLU: of G), dU_rows = the gradient of U
+ * (SwiGLU only).                                                             */
 int oracle_rows(int64_t T, int64_t d, int64_t dff, int act, const double* X, const double* W1,
                 const double* W3, const double* W2, const double* b1, const double* b3, const double* b2,
-                const double* dY, int64_t nrows, const int64_t* rows, double* Y_rows, double* dX_rows) {
+                const double* dY, int64_t nrows, const int64_t* rows, double* Y_rows, double* dX_rows,
+                double* A_rows, double* U_rows, double* H_rows, double* dA_rows, double* dU_rows) {
   if (T < 1 || d < 1 || dff < 1 || !valid_act(act) || nrows < 0 || !rows || !X || !W1 || !W2 ||
       !dY || !Y_rows || !dX_rows)
     return ORACLE_ERR_ARG;
@@ -402,6 +408,13 @@ int oracle_rows(int64_t T, int64_t d, int64_t dff, int act, const double* X, con
       }
       Y_rows[q * d + n] = y + (b2 ? b2[n] : 0.0);
       dX_rows[q * d + n] = dx;
+    }
+    for (int64_t j = 0; j < dff; ++j) {
+      if (A_rows) A_rows[q * dff + j] = a[j];
+      if (H_rows) H_rows[q * dff + j] = h[j];
+      if (dA_rows) dA_rows[q * dff + j] = da[j];
+      if (swiglu && U_rows) U_rows[q * dff + j] = u[j];
+      if (swiglu && dU_rows) dU_rows[q * dff + j] = dh[j] * swish(a[j]);
     }
     free(a);
   }

@@ -292,6 +292,18 @@ def test_sampled_rows_and_units_match_full(act):
     Yr, dXr = oracle.rows(X, W1, W2, dY, r, act=act, W3=W3)
     np.testing.assert_allclose(Yr, full_f["Y"][r], rtol=0, atol=1e-12)
     np.testing.assert_allclose(dXr, full_b["dX"][r], rtol=0, atol=1e-12)
+    # the same rows with the per-token intermediates, against the independent
+    # numpy oracle's full tensors
+    Yr2, dXr2, inter = oracle.rows(X, W1, W2, dY, r, act=act, W3=W3, intermediates=True)
+    assert np.array_equal(Yr2, Yr) and np.array_equal(dXr2, dXr)
+    np.testing.assert_allclose(inter["A"], full_f["A"][r], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(inter["H"], full_f["H"][r], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(inter["dA"], full_b["dA"][r], rtol=0, atol=1e-12)
+    if act == "swiglu":
+        np.testing.assert_allclose(inter["U"], full_f["U"][r], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(inter["dU"], full_b["dU"][r], rtol=0, atol=1e-12)
+    else:
+        assert set(inter) == {"A", "H", "dA"}
     u = np.array([0, 39, 13])
     c1, c3, c2 = oracle.wgrad_units(X, W1, W2, dY, u, act=act, W3=W3)
     np.testing.assert_allclose(c1, full_b["dW1"][:, u].T, rtol=0, atol=1e-11)
@@ -319,7 +331,20 @@ MUTANTS = [
     ("g_sum_drops_partials", "Y[i] += Z[i]; /* g: sum of partial outputs */", "Y[i] = Z[i];", "row_identity"),
     ("f_sum_drops_partials", "dX[i] += dXs[i]; /* f: sum of partial dX */", "dX[i] = dXs[i];", "row_identity"),
     ("swish_grad_sign", "return s + g * s * (1.0 - s);", "return s - g * s * (1.0 - s);", "fd_swiglu"),
+    ("rows_dU_uses_swish_grad", "dU_rows[q * dff + j] = dh[j] * swish(a[j]);",
+     "dU_rows[q * dff + j] = dh[j] * swish_grad(a[j]);", "rows_intermediates"),
 ]
+
+
+def _rows_intermediates_error(o):
+    rng = np.random.default_rng(12)
+    T, d, dff = 9, 8, 12
+    X = rng.normal(size=(T, d)); W1 = rng.normal(size=(d, dff)) * 0.3; W3 = rng.normal(size=(d, dff)) * 0.3
+    W2 = rng.normal(size=(dff, d)) * 0.3; dY = rng.normal(size=(T, d))
+    r = np.array([1, 4, 8])
+    _, _, inter = o.rows(X, W1, W2, dY, r, act="swiglu", W3=W3, intermediates=True)
+    fb = np_oracle.backward(X, W1, W2, dY, act="swiglu", W3=W3)
+    return float(np.max(np.abs(inter["dU"] - fb["dU"][r])))
 
 
 def _row_identity_error(o):
@@ -348,12 +373,16 @@ def test_planted_mistake_is_caught(mutant, tmp_path):
         assert check_normal_table(o) > 1e-6
     elif pin == "row_identity":
         assert _row_identity_error(o) >= 1.0
+    elif pin == "rows_intermediates":
+        assert _rows_intermediates_error(o) > 1e-3
     # and the unmodified oracle passes the same pin
     clean = oracle.default()
     if pin.startswith("fd"):
         assert fd_check(clean, pin[3:]) < 1e-7
     elif pin == "table":
         assert check_normal_table(clean) < 2e-15
+    elif pin == "rows_intermediates":
+        assert _rows_intermediates_error(clean) < 1e-12
     else:
         assert _row_identity_error(clean) == 0.0
 
