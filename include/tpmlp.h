@@ -188,7 +188,10 @@ TPMLP_API tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* con
  * 256 bytes (held by every GPU that loads the library until the process
  * exits); the call allocates and frees nothing.  The first call on a device
  * looks up that array's device address (cudaGetSymbolAddress) with the device
- * current; make that first call before any stream capture.  Each call clears
+ * current; make that first call before any stream capture.  The address is
+ * kept for the life of the process: after a cudaDeviceReset, which destroys
+ * the device's context and the array with it, the kept address is stale, and
+ * this entry point must not be called again in that process.  Each call clears
  * the status word on the stream, launches, then waits for the stream and
  * reports the kernel's status itself (TPMLP_ERR_DEVICE_TIMEOUT if a bounded
  * wait expired), so it blocks until its kernel has finished.  All calls on a
@@ -326,11 +329,10 @@ TPMLP_API tpmlp_status tpmlp_attn_qkv_backward(const tpmlp_plan* plan, const voi
  *     TPMLP_ERR_DEVICE_TIMEOUT in the status word, every role leaves its loop,
  *     the CTAs free their TMEM and exit, and the CUDA context stays usable.
  *     Outputs are undefined while it is enabled.  The fp32 path has no waits
- *     and ignores it.  enable == 2 instead keeps the loads and withholds the
- *     stream-K tail's parts (see tpmlp_plan_set_stream_k): the owners of the
- *     split tiles wait for flags that nothing raises, their bounded waits run
- *     out and the kernel records TPMLP_ERR_DEVICE_TIMEOUT the same way;
- *     tpmlp_check then clears the status word and the tail's flags.          */
+ *     and ignores it.  enable == 2 instead delays every part of a split
+ *     stream-K tile but its first (see tpmlp_plan_set_stream_k) by 20 ms, as
+ *     if their CTA pairs ran late: another part than the first then finishes
+ *     the tile; results and status must be those of a run without it.      */
 TPMLP_API tpmlp_status tpmlp_plan_set_timeout(tpmlp_plan* plan, uint32_t timeout_ms);
 TPMLP_API tpmlp_status tpmlp_plan_set_stall_injection(tpmlp_plan* plan, int enable);
 
@@ -338,12 +340,14 @@ TPMLP_API tpmlp_status tpmlp_plan_set_stall_injection(tpmlp_plan* plan, int enab
  * 256 tiles to the resident CTA pairs round robin; when the tile count is
  * not a multiple of the pairs, the last wave leaves pairs idle.  With the
  * tail, each of the last wave's R tiles is split along K into k parts run by
- * k pairs (k <= pairs / R).  The pair holding a tile's first K block
- * finishes it: it adds the other parts' fp32 accumulators (left in the
- * workspace) in a fixed order, so results stay deterministic for a given
- * device, but differ in rounding from the unsplit K sum (within the fp32
- * accumulation bound) and depend on the pair count, i.e. on the device's SM
- * count.
+ * k pairs (k <= pairs / R).  Every part leaves its fp32 accumulator in the
+ * workspace and takes a ticket; the part that takes the last ticket adds all
+ * parts in K order and finishes the tile.  No pair waits for another, so
+ * the tail makes no assumption about which pairs are resident or when they
+ * run (other kernels may share the GPU).  The fixed order keeps results
+ * deterministic for a given device, but they differ in rounding from the
+ * unsplit K sum (within the fp32 accumulation bound) and depend on the pair
+ * count, i.e. on the device's SM count.
  *   TPMLP_STREAM_K_AUTO (default): per launch, only when the full waves load
  *     every pair equally, the last wave's tiles have equal depth, and the
  *     split shortens a pair's work by at least 2 % and 16 K blocks of 128,
@@ -372,13 +376,67 @@ TPMLP_API int tpmlp_last_cuda_error(void);
 TPMLP_API const char* tpmlp_last_error(void);
 /* ABI version: 100 * major + minor (1.01: optional biases; 1.02: attention
  * projections; 1.03: sequence-parallel layout; 1.04: stream-K tail, larger
- * bf16 workspace). */
+ * bf16 workspace; 1.05: tpmlp_last_split_tiles, tpmlp_eval_activation). */
 TPMLP_API int tpmlp_version(void);
 
 /* Kernel launches the last compute call (tpmlp_forward, tpmlp_backward, a
  * phase or an attention entry point) on this thread made (for accounting; 0
  * before the first call).                                                    */
 TPMLP_API int tpmlp_last_launch_count(void);
+
+/* Diagnostics of the stream-K tail (see tpmlp_plan_set_stream_k), for tests
+ * that must know which output tiles were computed in parts.  launch_kind
+ * names a launch of the block:
+ *   0 the column-parallel GEMM (tpmlp_forward_column), 1 the row-parallel
+ *   GEMM with the g-sum (tpmlp_forward_row), 2 the dgrad launch
+ *   (tpmlp_backward_dgrad), 3 the f-sum launch (tpmlp_backward_fsum),
+ *   4..7 the attention projections' QKV forward, output forward, output
+ *   backward and QKV backward.
+ * Returns how many tiles the last launch of that kind made on this thread
+ * split into parts (0 if none, or no such launch yet; -1 for an unknown
+ * kind) and writes the first min(count, cap) of them to tiles (host memory,
+ * may be NULL) as triples: the problem's index in its launch, the tile's
+ * first output row and its first output column.  Problems are numbered in
+ * the order each launch lists them: column launch, shard i's problem is i;
+ * row launch, one problem (Y); dgrad launch, dW2_i (i = 0..t-1) then shard
+ * i's dact at t + i (recompute: no dW2 problems); f-sum launch, dW1_i
+ * (i = 0..t-1), SwiGLU dW3_i at t + i, then dX (recompute: dW2_i first).  */
+TPMLP_API int tpmlp_last_split_tiles(int launch_kind, int64_t* tiles, int cap);
+
+/* The activation forms of the kernels' epilogues, evaluated on plain fp32
+ * device arrays of n elements (x = the pre-activation A or the gate G, y =
+ * the up projection U, dh = the incoming gradient dH), so that they can be
+ * checked against a reference over any set of inputs.  The bf16 tensor-core
+ * epilogues compute Phi from the rational approximation of erf given as
+ * formula 7.1.26 in Abramowitz & Stegun (absolute error at most 1.5e-7) and
+ * the sigmoid from the fast exponential and reciprocal; the fp32 path calls
+ * erff and expf.  The GeLU forms are those of GeLU(a) = a Phi(a) and
+ * GeLU'(a) = Phi(a) + a phi(a); Swish is g sigmoid(g) ("Parallelism" tag page
+ * of Jiang Yi's homepage, post "megatron-lm", Method / FFN and the SwiGLU
+ * listing; "Tensor parallelism", brunomaga.github.io, Megatron_FeedForward's
+ * F.gelu).  Outputs (device, fp32, n elements; unused ones may be NULL):
+ *   TPMLP_ACT_EVAL_GELU        out0 = GeLU(x)                       (bf16 column epilogue)
+ *   TPMLP_ACT_EVAL_GELU_BWD    out0 = dh GeLU'(x)                   (bf16 dgrad epilogue)
+ *   TPMLP_ACT_EVAL_GELU_BWD_H  out0 = dh GeLU'(x), out1 = GeLU(x)   (same, with H recomputed)
+ *   TPMLP_ACT_EVAL_SWIGLU      out0 = y Swish(x)                    (bf16 column epilogue)
+ *   TPMLP_ACT_EVAL_SWIGLU_BWD  out0 = dG = dh y Swish'(x), out1 = dU = dh Swish(x)
+ *   TPMLP_ACT_EVAL_SWIGLU_BWD_H  the same and out2 = y Swish(x)     (H recomputed)
+ *   TPMLP_ACT_EVAL_FP32_GELU   out0 = GeLU(x), out1 = dh GeLU'(x)   (fp32 path)
+ *   TPMLP_ACT_EVAL_FP32_SWIGLU out0 = y Swish(x), out1 = dG, out2 = dU (fp32 path)
+ * Inputs an entry does not read may be NULL.  Asynchronous on the stream;
+ * one kernel launch.  Errors: TPMLP_ERR_INVALID_ARG (unknown fn, n < 0, a
+ * needed pointer NULL), TPMLP_ERR_ALIGNMENT (a pointer not 4-byte aligned),
+ * TPMLP_ERR_UNSUPPORTED (not sm_103), TPMLP_ERR_CUDA.                        */
+#define TPMLP_ACT_EVAL_GELU 0
+#define TPMLP_ACT_EVAL_GELU_BWD 1
+#define TPMLP_ACT_EVAL_GELU_BWD_H 2
+#define TPMLP_ACT_EVAL_SWIGLU 3
+#define TPMLP_ACT_EVAL_SWIGLU_BWD 4
+#define TPMLP_ACT_EVAL_SWIGLU_BWD_H 5
+#define TPMLP_ACT_EVAL_FP32_GELU 6
+#define TPMLP_ACT_EVAL_FP32_SWIGLU 7
+TPMLP_API tpmlp_status tpmlp_eval_activation(int fn, const float* x, const float* y, const float* dh, float* out0,
+                                             float* out1, float* out2, int64_t n, tpmlp_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -31,7 +31,9 @@ __all__ = [
     "tpmlp_last_launch_count", "tpmlp_last_error", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
     "AttnPlan", "tpmlp_attn_plan_create", "tpmlp_attn_qkv_forward", "tpmlp_attn_out_forward",
     "tpmlp_attn_out_backward", "tpmlp_attn_qkv_backward", "ShardedAttentionProj",
-    "tpmlp_plan_set_sequence_stripes", "tpmlp_forward_sp", "tpmlp_backward_sp",
+    "tpmlp_plan_set_sequence_stripes", "tpmlp_forward_sp", "tpmlp_backward_sp", "tpmlp_last_split_tiles",
+    "LAUNCH_FWD_COLUMN", "LAUNCH_FWD_ROW", "LAUNCH_BWD_DGRAD", "LAUNCH_BWD_FSUM", "tpmlp_eval_activation",
+    "ACT_EVAL",
 ]
 
 ACT = {"gelu": 0, "swiglu": 1}
@@ -48,8 +50,15 @@ EXPORTED_SYMBOLS = (
     "tpmlp_last_launch_count", "tpmlp_last_error", "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection",
     "tpmlp_backward_recompute", "tpmlp_attn_plan_create", "tpmlp_attn_qkv_forward", "tpmlp_attn_out_forward",
     "tpmlp_attn_out_backward", "tpmlp_attn_qkv_backward", "tpmlp_plan_set_sequence_stripes", "tpmlp_forward_sp",
-    "tpmlp_backward_sp", "tpmlp_plan_set_stream_k",
+    "tpmlp_backward_sp", "tpmlp_plan_set_stream_k", "tpmlp_last_split_tiles", "tpmlp_eval_activation",
 )
+
+# forms of tpmlp_eval_activation
+ACT_EVAL = {"gelu": 0, "gelu_bwd": 1, "gelu_bwd_h": 2, "swiglu": 3, "swiglu_bwd": 4, "swiglu_bwd_h": 5,
+            "fp32_gelu": 6, "fp32_swiglu": 7}
+
+# launch kinds of tpmlp_last_split_tiles
+LAUNCH_FWD_COLUMN, LAUNCH_FWD_ROW, LAUNCH_BWD_DGRAD, LAUNCH_BWD_FSUM = 0, 1, 2, 3
 
 
 class TpmlpError(RuntimeError):
@@ -151,6 +160,10 @@ def load():
         lib.tpmlp_version.restype = i32
         lib.tpmlp_last_launch_count.argtypes = []
         lib.tpmlp_last_launch_count.restype = i32
+        lib.tpmlp_last_split_tiles.argtypes = [i32, ctypes.POINTER(ctypes.c_int64), i32]
+        lib.tpmlp_last_split_tiles.restype = i32
+        lib.tpmlp_eval_activation.argtypes = [i32, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp]
+        lib.tpmlp_eval_activation.restype = st
         _lib = lib
         return lib
 
@@ -393,6 +406,26 @@ def tpmlp_version() -> int:
 
 def tpmlp_last_launch_count() -> int:
     return int(load().tpmlp_last_launch_count())
+
+
+def tpmlp_eval_activation(form: str, x, y=None, dh=None, out0=None, out1=None, out2=None, stream=None):
+    """The epilogues' activation forms on fp32 device tensors of n elements
+    (form: a key of ACT_EVAL); outputs are caller tensors like x."""
+    n = x.numel()
+    _ok(load().tpmlp_eval_activation(ACT_EVAL[form], _addr(x), _addr(y), _addr(dh), _addr(out0), _addr(out1),
+                                     _addr(out2), n, _stream(stream)), "tpmlp_eval_activation")
+
+
+def tpmlp_last_split_tiles(launch_kind: int) -> List[tuple]:
+    """(problem, first row, first column) of every tile the stream-K tail split in
+    the last launch of this kind on the calling thread."""
+    lib = load()
+    n = int(lib.tpmlp_last_split_tiles(int(launch_kind), None, 0))
+    if n < 0:
+        raise ValueError(f"unknown launch kind {launch_kind}")
+    buf = (ctypes.c_int64 * max(1, 3 * n))()
+    lib.tpmlp_last_split_tiles(int(launch_kind), buf, n)
+    return [(int(buf[3 * i]), int(buf[3 * i + 1]), int(buf[3 * i + 2])) for i in range(n)]
 
 
 # ---------------------------------------------------------------- convenience layer

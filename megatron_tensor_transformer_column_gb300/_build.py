@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtpmlp.so")
-SOURCES = ["tpmlp_api.cu", "tc_gemm.cu", "tc_gemm_sk.cu", "simt_gemm.cu", "colsum.cu"]
+SOURCES = ["tpmlp_api.cu", "tc_gemm.cu", "simt_gemm.cu", "colsum.cu", "act_eval.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -138,6 +138,15 @@ __device__ __forceinline__ void st_release_gpu_u32(uint32_t* p, uint32_t v) {
 __device__ __forceinline__ void st_relaxed_gpu_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Compare-and-swap (ticket counters): returns the value found.
+__device__ __forceinline__ uint32_t atom_cas_acq_rel_gpu_u32(uint32_t* p, uint32_t expected, uint32_t desired) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b32 %0, [%1], %2, %3;"
+               : "=r"(old)
+               : "l"(p), "r"(expected), "r"(desired)
+               : "memory");
+  return old;
+}
 // 16-byte global store / load that bypass L1 (data exchanged through L2).
 __device__ __forceinline__ void st_cg_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.cg.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");

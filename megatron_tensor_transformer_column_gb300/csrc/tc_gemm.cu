@@ -29,9 +29,16 @@
 // Method / FFN: the partial-sum identity [H1, H2][W21; W22] = H1 W21 + H2 W22
 // and the f/g table.)
 //
-// This file holds the data-parallel variant: pair q computes tiles q,
-// q + pairs, q + 2 pairs, ...  tc_gemm_sk.cu holds the variant with a
-// stream-K tail for the last, partial wave; both share tc_gemm_common.cuh.
+// One body, two schedules (template parameter kSK):
+//   * data-parallel: pair q computes tiles q, q + pairs, q + 2 pairs, ...;
+//   * stream-K tail: the same for the launch's full waves, then each pair
+//     takes one item of the last, partial wave: a range of one tile's K
+//     blocks (a part).  Every part leaves its fp32 accumulator in the
+//     workspace and takes a ticket; the part whose ticket is the last one
+//     adds all parts, in range order, into its own accumulator and runs the
+//     tile's epilogue.  No pair ever waits for another pair, so the result
+//     does not depend on which pairs are resident or when they run, and the
+//     fixed order makes it the same on every run.
 //
 // Every wait is bounded: after GemmParams::timeout_ns a waiting role records
 // a status code in the workspace, raises the abort flag of both CTAs, which
@@ -44,14 +51,89 @@
 namespace tpmlp {
 namespace {
 
-// Walks the (tile, segment, K block) sequence of one CTA of a pair in the
-// order the main loop consumes it; the producer keeps one cursor for the
-// loads into the ring and one running ahead for the L2 prefetches.
+// ------------------------------------------------------------------ schedules
+// An item is a tile and a range [kb0, kb1) of its K blocks, counted over all
+// of its segments: the whole tile, or (stream-K) a part of a split tile.
+struct Item {
+  TileInfo ti;
+  int tile;      // -1: no more items
+  int kb0, kb1;
+  bool split;    // a part of a tile split between stream-K ranges
+};
+
+template <bool kSK>
+struct Sched {
+  Item it;
+  int dp;              // next data-parallel tile
+  int r;               // stream-K: this pair's range
+  int sk_tile, sk_kb;  // stream-K: next position in that range
+  bool in_dp;
+};
+
+template <bool kSK>
+__device__ __forceinline__ void sched_next(Sched<kSK>& s, const GemmParams& p, int npairs) {
+  const int dp_end = kSK ? p.sk.dp_tiles : p.total_tiles;
+  if (!kSK || s.in_dp) {
+    if (s.dp < dp_end) {
+      s.it.tile = s.dp;
+      s.dp += npairs;
+      s.it.ti = decode_tile(p, s.it.tile);
+      s.it.kb0 = 0;
+      s.it.kb1 = p.probs[s.it.ti.prob].kblocks;
+      s.it.split = false;
+      return;
+    }
+    if (!kSK) {
+      s.it.tile = -1;
+      return;
+    }
+    s.in_dp = false;
+    if (s.r < 0 || s.r >= p.sk.pairs) {
+      s.it.tile = -1;
+      return;
+    }
+    s.sk_tile = p.sk.start_tile[s.r];
+    s.sk_kb = p.sk.start_kb[s.r];
+  }
+  const int end_tile = p.sk.start_tile[s.r + 1], end_kb = p.sk.start_kb[s.r + 1];
+  while (s.sk_tile < end_tile || (s.sk_tile == end_tile && s.sk_kb < end_kb)) {
+    const int t = s.sk_tile;
+    const TileInfo ti = decode_tile(p, t);
+    const int kbt = p.probs[ti.prob].kblocks;
+    const int kb0 = s.sk_kb, kb1 = t == end_tile ? end_kb : kbt;
+    s.sk_tile = t + 1;
+    s.sk_kb = 0;
+    if (kb1 > kb0) {
+      s.it.tile = t;
+      s.it.ti = ti;
+      s.it.kb0 = kb0;
+      s.it.kb1 = kb1;
+      s.it.split = kb0 > 0 || kb1 < kbt;
+      return;
+    }
+  }
+  s.it.tile = -1;
+}
+
+// pair < 0: an empty schedule.
+template <bool kSK>
+__device__ __forceinline__ void sched_init(Sched<kSK>& s, const GemmParams& p, int pair, int npairs) {
+  s.dp = pair < 0 ? INT_MAX : pair;
+  s.r = pair < 0 ? -1 : npairs - 1 - pair;
+  s.in_dp = true;
+  sched_next(s, p, npairs);
+}
+
+// ------------------------------------------------------------------ producer cursor
+// Walks the (item, segment, K block) sequence of one CTA of a pair in the
+// order the main loop consumes it.
+template <bool kSK>
 struct Cursor {
+  Sched<kSK> s;        // the current item
   const void* ma;      // tensor maps of the current segment
   const void* mb;
   const void* mb2;
-  int tile, seg, seg_end, kb, kblocks;
+  int seg, kb, kblocks, left;  // segment, K block in it, its K blocks; K blocks left in the item
   int a_major, b_major, dual;
   int a_striped, b_striped;  // operand read from the launch's token stripes
   int a_sj, b_sj;            // its current stripe,
@@ -62,7 +144,8 @@ struct Cursor {
   uint32_t bytes_pair; // bytes both CTAs load per K block (counted on the even CTA)
 };
 
-__device__ __forceinline__ void cursor_segment(Cursor& c, const GemmParams& p) {
+template <bool kSK>
+__device__ __forceinline__ void cursor_segment(Cursor<kSK>& c, const GemmParams& p) {
   const Seg& S = p.segs[c.seg];
   c.kb = 0;
   c.kblocks = (S.K + kBK - 1) / kBK;
@@ -96,10 +179,17 @@ __device__ __forceinline__ void stripe_advance(const GemmParams& p, int k0, int&
   }
 }
 
-__device__ __forceinline__ void cursor_tile(Cursor& c, const GemmParams& p, int tile, uint32_t rank) {
-  c.tile = tile;
-  if (tile >= p.total_tiles) return;
-  const TileInfo ti = decode_tile(p, tile);
+template <bool kSK>
+__device__ __forceinline__ void cursor_stripes(Cursor<kSK>& c, const GemmParams& p) {
+  if (c.a_striped && c.a_major == MAJOR_MN) stripe_advance(p, c.kb * kBK, c.a_sj, c.a_y0, c.a_next);
+  if (c.b_striped && c.b_major == MAJOR_MN) stripe_advance(p, c.kb * kBK, c.b_sj, c.b_y0, c.b_next);
+}
+
+// Set the cursor on the first K block of its schedule's current item.
+template <bool kSK>
+__device__ __forceinline__ void cursor_item(Cursor<kSK>& c, const GemmParams& p, uint32_t rank) {
+  if (c.s.it.tile < 0) return;
+  const TileInfo& ti = c.s.it.ti;
   const Prob& P = p.probs[ti.prob];
   c.dual = P.epi == EPI_SWIGLU_FWD;
   const PairShape ps = pair_shape(ti, c.dual, P.a_major, P.b_major);
@@ -111,26 +201,40 @@ __device__ __forceinline__ void cursor_tile(Cursor& c, const GemmParams& p, int 
   c.a_major = P.a_major;
   c.b_major = P.b_major;
   c.seg = P.seg_begin;
-  c.seg_end = P.seg_begin + P.seg_count;
+  c.left = c.s.it.kb1 - c.s.it.kb0;
+  int skip = c.s.it.kb0;
+  cursor_segment(c, p);
+  if (kSK) {
+    while (skip >= c.kblocks) {  // a stream-K part may start in a later segment
+      skip -= c.kblocks;
+      ++c.seg;
+      cursor_segment(c, p);
+    }
+    if (skip > 0) {
+      c.kb = skip;
+      cursor_stripes(c, p);
+    }
+  }
+}
+
+template <bool kSK>
+__device__ __forceinline__ void cursor_next(Cursor<kSK>& c, const GemmParams& p, int npairs, uint32_t rank) {
+  if (--c.left == 0) {
+    sched_next(c.s, p, npairs);
+    cursor_item(c, p, rank);
+    return;
+  }
+  if (++c.kb < c.kblocks) {
+    cursor_stripes(c, p);
+    return;
+  }
+  ++c.seg;
   cursor_segment(c, p);
 }
 
-__device__ __forceinline__ void cursor_next(Cursor& c, const GemmParams& p, int npairs, uint32_t rank) {
-  if (++c.kb < c.kblocks) {
-    if (c.a_striped && c.a_major == MAJOR_MN) stripe_advance(p, c.kb * kBK, c.a_sj, c.a_y0, c.a_next);
-    if (c.b_striped && c.b_major == MAJOR_MN) stripe_advance(p, c.kb * kBK, c.b_sj, c.b_y0, c.b_next);
-    return;
-  }
-  if (++c.seg < c.seg_end) {
-    cursor_segment(c, p);
-    return;
-  }
-  cursor_tile(c, p, c.tile + npairs, rank);
-}
-
-// Issue this CTA's box copies (or L2 prefetches) for the cursor's K block.
-template <bool kPrefetch>
-__device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor& c, uint32_t sb, uint32_t fb) {
+// Issue this CTA's box copies for the cursor's K block.
+template <bool kSK>
+__device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor<kSK>& c, uint32_t sb, uint32_t fb) {
   const int k0 = c.kb * kBK;
   const uint32_t sbB = sb + kOperandBytes;
   for (int b = 0; b < c.nA; ++b) {
@@ -144,10 +248,7 @@ __device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor& 
       ma += c.a_sj;
       y -= c.a_y0;
     }
-    if (kPrefetch)
-      ptx::tma_prefetch_2d(ma, x, y);
-    else
-      ptx::tma_load_2d_pair(sb + b * (mn ? kMNBoxBytes : kKBoxBytes), ma, x, y, fb);
+    ptx::tma_load_2d_pair(sb + b * (mn ? kMNBoxBytes : kKBoxBytes), ma, x, y, fb);
   }
   for (int j = 0; j < c.nB; ++j) {
     const bool mn = c.b_major == MAJOR_MN;
@@ -158,20 +259,163 @@ __device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor& 
       mb += c.b_sj;
       y -= c.b_y0;
     }
-    if (kPrefetch)
-      ptx::tma_prefetch_2d(mb, x, y);
-    else
-      ptx::tma_load_2d_pair(sbB + j * (mn ? kMNBoxBytes : kKBoxBytes), mb, x, y, fb);
+    ptx::tma_load_2d_pair(sbB + j * (mn ? kMNBoxBytes : kKBoxBytes), mb, x, y, fb);
   }
-  if (c.dual && c.nB > 0) {  // SwiGLU up projection (MN-major like the gate), second B box
-    const void* mb2 = c.mb2;
-    if (kPrefetch)
-      ptx::tma_prefetch_2d(mb2, c.n0, k0);
-    else
-      ptx::tma_load_2d_pair(sbB + kMNBoxBytes, mb2, c.n0, k0, fb);
+  if (c.dual && c.nB > 0)  // SwiGLU up projection (MN-major like the gate), second B box
+    ptx::tma_load_2d_pair(sbB + kMNBoxBytes, c.mb2, c.n0, k0, fb);
+}
+
+// ------------------------------------------------------------------ stream-K parts
+// Range r's workspace slot holds, per epilogue warp wi of the pair
+// (rank * 8 + warp - 2), the four 32 x 32 fp32 accumulator chunks that warp
+// drains (the same TMEM lanes and columns in every pair), laid out so that
+// each 16-byte store / load of a warp covers 512 contiguous bytes.  The
+// ticket counter of a split tile, one per epilogue warp position, is the
+// flag word of the tile's first range.
+__device__ __forceinline__ uint32_t* sk_counter(const GemmParams& p, int q0, int wi) {
+  return reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(p.status) + kSkFlagsOffset) + q0 * kSkWarpsPerPair + wi;
+}
+
+__device__ __forceinline__ char* sk_chunk(const GemmParams& p, int r, int wi, int cslot) {
+  return reinterpret_cast<char*>(p.status) + kSkSlotsOffset + static_cast<size_t>(r) * kSkSlotBytes +
+         static_cast<size_t>(wi * 4 + cslot) * (32 * 32 * sizeof(float));
+}
+
+__device__ __forceinline__ bool sk_range_empty(const GemmParams& p, int r) {
+  return p.sk.start_tile[r] == p.sk.start_tile[r + 1] && p.sk.start_kb[r] == p.sk.start_kb[r + 1];
+}
+
+// TMEM column of this warp's chunk cslot (0..3) of a tile -- the chunks the
+// epilogue reads, in its order -- or -1 past the tile's valid columns.
+// SwiGLU forward: chunk 2c is the gate, 2c + 1 the up projection of output
+// columns 64 half + 32 c ..; otherwise chunk c is columns 128 half + 32 c ...
+__device__ __forceinline__ int sk_chunk_col(const Prob& P, const TileInfo& ti, int half, int cslot) {
+  if (P.epi == EPI_SWIGLU_FWD) {
+    const int c = cslot >> 1;
+    const int col = half * 64 + c * 32;
+    if (col >= ti.valid_n) return -1;
+    const bool merged = swiglu_merged(ti, P);
+    const int g_col = merged ? half * 128 + c * 32 : col;
+    return (cslot & 1) ? (merged ? g_col + 64 : 128 + col) : g_col;
+  }
+  const int col = half * 128 + cslot * 32;
+  return col < ti.valid_n ? col : -1;
+}
+
+// This warp's chunks of a part, raw fp32, to its range's slot.
+__device__ __forceinline__ void sk_part_store(const GemmParams& p, const Prob& P, const Item& it, int r,
+                                              uint32_t tacc, int half, int wi, int lane) {
+#pragma unroll 1
+  for (int cs = 0; cs < 4; ++cs) {
+    const int tc = sk_chunk_col(P, it.ti, half, cs);
+    if (tc < 0) continue;
+    uint32_t v[32];
+    ptx::tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(tc), v);
+    ptx::tmem_wait_ld();
+    char* dst = sk_chunk(p, r, wi, cs) + lane * 16;
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4)
+      ptx::st_cg_v4(dst + j4 * 512, v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
   }
 }
 
+// After its stores: take this warp's ticket of the tile.  A counter holds
+// the launch's epoch (low 24 bits) above an 8-bit count of the parts that
+// arrived; a value from another launch (an aborted one) counts as zero, so
+// no reset is needed.  The compare-and-swap loop retries only when another
+// part arrived in between: at most nparts + 1 rounds, and it never waits for
+// a part that has not arrived.  True for the warp holding the last ticket;
+// that warp then acquires every other part's stores.
+__device__ __forceinline__ bool sk_ticket(const GemmParams& p, int q0, int nparts, int wi, int lane) {
+  __threadfence();
+  __syncwarp();
+  uint32_t* ctr = sk_counter(p, q0, wi);
+  uint32_t count = 0;
+  if (lane == 0) {
+    const uint32_t tag = (p.sk.epoch & 0xFFFFFFu) << 8;
+    uint32_t cur = tag;
+    for (int round = 0; round <= kMaxSkPairs + 1; ++round) {
+      const uint32_t want = ((cur & ~0xFFu) == tag ? cur : tag) + 1u;
+      const uint32_t seen = ptx::atom_cas_acq_rel_gpu_u32(ctr, cur, want);
+      if (seen == cur) {
+        count = want & 0xFFu;
+        break;
+      }
+      cur = seen;
+    }
+  }
+  count = __shfl_sync(0xffffffffu, count, 0);
+  if (count != static_cast<uint32_t>(nparts)) return false;
+  (void)ptx::ld_acquire_gpu_u32(ctr);  // every lane acquires the other parts' stores
+  __syncwarp();
+  return true;
+}
+
+// Add one part's chunk to v: from this pair's TMEM accumulator, or from
+// range q's slot (eight 16-byte loads in flight).
+__device__ __forceinline__ void sk_add_tmem(uint32_t taddr, uint32_t (&v)[32]) {
+  uint32_t t[32];
+  ptx::tmem_ld_32x32b_x32(taddr, t);
+  ptx::tmem_wait_ld();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(t[j]));
+}
+
+__device__ __forceinline__ void sk_add_slot(const char* src, uint32_t (&v)[32]) {
+  float4 f[8];
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) f[j4] = ptx::ld_cg_v4f(src + j4 * 512);
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) {
+    v[4 * j4 + 0] = __float_as_uint(__uint_as_float(v[4 * j4 + 0]) + f[j4].x);
+    v[4 * j4 + 1] = __float_as_uint(__uint_as_float(v[4 * j4 + 1]) + f[j4].y);
+    v[4 * j4 + 2] = __float_as_uint(__uint_as_float(v[4 * j4 + 2]) + f[j4].z);
+    v[4 * j4 + 3] = __float_as_uint(__uint_as_float(v[4 * j4 + 3]) + f[j4].w);
+  }
+}
+
+// The last part: the sum of all parts, added in range order (its own from
+// TMEM, the others from their slots), written back into its accumulator, on
+// which the tile's normal epilogue then runs.  The parts of a tile are the
+// non-empty ranges from q0 (the tile's first non-empty one) on that start in
+// it: the host cuts one part per range.
+__device__ __forceinline__ void sk_fold(const GemmParams& p, const Prob& P, const Item& it, int r, int q0,
+                                        uint32_t tacc, int half, int wi, int lane) {
+#pragma unroll 1
+  for (int cs = 0; cs < 4; ++cs) {
+    const int tc = sk_chunk_col(P, it.ti, half, cs);
+    if (tc < 0) continue;
+    const uint32_t taddr = tacc + static_cast<uint32_t>(tc);
+    uint32_t v[32];
+    if (q0 == r) {
+      ptx::tmem_ld_32x32b_x32(taddr, v);
+      ptx::tmem_wait_ld();
+    } else {
+      const char* src = sk_chunk(p, q0, wi, cs) + lane * 16;
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 f = ptx::ld_cg_v4f(src + j4 * 512);
+        v[4 * j4 + 0] = __float_as_uint(f.x);
+        v[4 * j4 + 1] = __float_as_uint(f.y);
+        v[4 * j4 + 2] = __float_as_uint(f.z);
+        v[4 * j4 + 3] = __float_as_uint(f.w);
+      }
+    }
+#pragma unroll 1
+    for (int q = q0 + 1; q < p.sk.pairs && p.sk.start_tile[q] == it.tile; ++q) {
+      if (sk_range_empty(p, q)) continue;
+      if (q == r)
+        sk_add_tmem(taddr, v);
+      else
+        sk_add_slot(sk_chunk(p, q, wi, cs) + lane * 16, v);
+    }
+    ptx::tmem_st_32x32b_x32(taddr, v);
+  }
+  ptx::tmem_wait_st();
+}
+
+// ------------------------------------------------------------------ the kernel body
+template <bool kSK>
 __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_raw) {
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kEpiBytes);
@@ -230,14 +474,10 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       for (int s = 0; s < kStages; ++s) armed_parity[s] = -1;
       bool ok = true;
       bool issued = false;
-      Cursor ld, pf;
-      cursor_tile(ld, p, p.stall_injection == 1 ? p.total_tiles : pair, rank);  // injected stall: nothing to load
-      cursor_tile(pf, p, p.stall_injection == 1 ? p.total_tiles : pair, rank);
-      for (int i = 0; i < kPrefetchKBlocks && pf.tile < p.total_tiles; ++i) {
-        cursor_issue<true>(p, pf, 0, 0);
-        cursor_next(pf, p, npairs, rank);
-      }
-      while (ld.tile < p.total_tiles) {
+      Cursor<kSK> ld;
+      sched_init(ld.s, p, p.stall_injection == 1 ? -1 : pair, npairs);  // injected stall: nothing to load
+      cursor_item(ld, p, rank);
+      while (ld.s.it.tile >= 0) {
         if (!bounded_wait(empty_bar(stage), phase ^ 1u, ctl, kDevTimeoutProducer)) {
           ok = false;
           break;
@@ -246,13 +486,9 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
           ptx::mbar_arrive_expect_tx(full_bar(stage), ld.bytes_pair);
           armed_parity[stage] = static_cast<int>(phase);
         }
-        cursor_issue<false>(p, ld, smem_base + stage * kStageBytes, ptx::map_to_cta(full_bar(stage), 0));
+        cursor_issue(p, ld, smem_base + stage * kStageBytes, ptx::map_to_cta(full_bar(stage), 0));
         issued = true;
         cursor_next(ld, p, npairs, rank);
-        if (kPrefetchKBlocks > 0 && pf.tile < p.total_tiles) {
-          cursor_issue<true>(p, pf, 0, 0);
-          cursor_next(pf, p, npairs, rank);
-        }
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
@@ -286,12 +522,13 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       const uint64_t a_mn_desc = ptx::make_sdesc_sw128(smem_base, kMNBoxBytes, 1024);
       const uint64_t b_k_desc = ptx::make_sdesc_sw128(smem_base + kOperandBytes, 16, 1024);
       const uint64_t b_mn_desc = ptx::make_sdesc_sw128(smem_base + kOperandBytes, kMNBoxBytes, 1024);
-      for (int tile = pair; ok && tile < p.total_tiles; tile += npairs) {
-        const TileInfo ti = decode_tile(p, tile);
+      Sched<kSK> s;
+      for (sched_init(s, p, pair, npairs); ok && s.it.tile >= 0; sched_next(s, p, npairs)) {
+        const Item& it = s.it;
+        const TileInfo& ti = it.ti;
         const Prob& P = p.probs[ti.prob];
         const int a_major = P.a_major, b_major = P.b_major;
         const bool dual = P.epi == EPI_SWIGLU_FWD;
-        const int seg_begin = P.seg_begin, seg_end = P.seg_begin + P.seg_count;
         const PairShape ps = pair_shape(ti, dual, a_major, b_major);
         // A full SwiGLU tile issues one N = 256 MMA over each CTA's [gate | up]
         // column blocks instead of two N = 128 MMAs (the wider MMA runs at the
@@ -310,23 +547,36 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         uint32_t accumulate = 0;
-        for (int s = seg_begin; ok && s < seg_end; ++s) {
-          const int K = p.segs[s].K;
-          for (int k0 = 0; k0 < K; k0 += kBK) {
-            if (!bounded_wait(full_bar(stage), phase, ctl, kDevTimeoutMma)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t st = static_cast<uint32_t>((stage * kStageBytes) >> 4);
-            const int nk = min(kBK / 16, (K - k0 + 15) >> 4);
-            issue_stage_any(kind, d_tmem, a_lo + st, a_hi, b_lo + st, b_hi, idesc, nk, accumulate);
-            issued = true;
-            ptx::mma_commit_pair_mc(empty_bar(stage), kPairMask);  // stage free in both CTAs
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
+        // The item's K blocks [kb0, kb1), counted over the tile's segments.
+        int sg = P.seg_begin;
+        int K = p.segs[sg].K;
+        int skip = it.kb0;
+        if (kSK) {
+          while (skip >= (K + kBK - 1) / kBK) {
+            skip -= (K + kBK - 1) / kBK;
+            K = p.segs[++sg].K;
+          }
+        }
+        int k0 = skip * kBK;
+        for (int left = it.kb1 - it.kb0; left > 0; --left) {
+          if (!bounded_wait(full_bar(stage), phase, ctl, kDevTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t st = static_cast<uint32_t>((stage * kStageBytes) >> 4);
+          const int nk = min(kBK / 16, (K - k0 + 15) >> 4);
+          issue_stage_any(kind, d_tmem, a_lo + st, a_hi, b_lo + st, b_hi, idesc, nk, accumulate);
+          issued = true;
+          ptx::mma_commit_pair_mc(empty_bar(stage), kPairMask);  // stage free in both CTAs
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          k0 += kBK;
+          if (k0 >= K && left > 1) {
+            K = p.segs[++sg].K;
+            k0 = 0;
           }
         }
         if (!ok) break;
@@ -348,10 +598,13 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
     const int half = (warp - 2) >> 2;    // which half of the tile's columns
     EpiStore es{smem_base + static_cast<uint32_t>(kStages * kStageBytes + (warp - 2) * 2 * kEpiBlockBytes), 0u, 0, 0,
                 0};
+    const int wi = static_cast<int>(rank) * kNumEpiWarps + (warp - 2);  // stream-K slot position of this warp
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = pair; tile < p.total_tiles; tile += npairs) {
-      const TileInfo ti = decode_tile(p, tile);
+    Sched<kSK> s;
+    for (sched_init(s, p, pair, npairs); s.it.tile >= 0; sched_next(s, p, npairs)) {
+      const Item& it = s.it;
+      const TileInfo ti = it.ti;
       const Prob& P = p.probs[ti.prob];
       const int row = q * 32 + lane;
       const int vm = max(0, min(kBM, ti.valid_m - kBM * static_cast<int>(rank)));
@@ -383,7 +636,19 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       if (!bounded_wait(tfull_bar(acc), acc_phase, ctl, kDevTimeoutEpilogue)) break;
       ptx::tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
-      if (vm > 0) {
+      bool finish = true;
+      if (kSK && it.split) {
+        // A part of a split tile: publish it; the last part to arrive adds
+        // them all and runs the epilogue.  (Test hook, stall injection 2:
+        // every part but the tile's first runs late, so that another part
+        // than the first finishes the tile.)
+        if (vm > 0) sk_part_store(p, P, it, s.r, tacc, half, wi, lane);
+        const int q0 = p.sk.first_range[s.r];
+        if (p.stall_injection == 2 && s.r != q0) spin_ns(20ull * 1000 * 1000);
+        finish = sk_ticket(p, q0, p.sk.num_parts[s.r], wi, lane);
+        if (finish && vm > 0) sk_fold(p, P, it, s.r, q0, tacc, half, wi, lane);
+      }
+      if (finish && vm > 0) {
         if (P.epi == EPI_SWIGLU_FWD) {
           const bool merged = swiglu_merged(ti, P);
 #pragma unroll 1
@@ -447,36 +712,41 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
 
 }  // namespace
 
-// One kernel symbol per launch kind (same body).
-#define TPMLP_TC_KERNEL(name)                                                          \
-  __global__ void __launch_bounds__(kThreads, 1) name(const __grid_constant__ GemmParams p) { \
-    extern __shared__ __align__(1024) uint8_t smem_raw[];                              \
-    tc_gemm_body(p, smem_raw);                                                         \
+// Two kernel symbols per launch kind (same body): the data-parallel schedule
+// and, with the suffix _sk, the one with a stream-K tail.
+#define TPMLP_TC_KERNELS(name)                                                                    \
+  __global__ void __launch_bounds__(kThreads, 1) name(const __grid_constant__ GemmParams p) {     \
+    extern __shared__ __align__(1024) uint8_t smem_raw[];                                         \
+    tc_gemm_body<false>(p, smem_raw);                                                             \
+  }                                                                                               \
+  __global__ void __launch_bounds__(kThreads, 1) name##_sk(const __grid_constant__ GemmParams p) { \
+    extern __shared__ __align__(1024) uint8_t smem_raw[];                                         \
+    tc_gemm_body<true>(p, smem_raw);                                                              \
   }
 
-TPMLP_TC_KERNEL(tpmlp_fwd_column_gemm_act)
-TPMLP_TC_KERNEL(tpmlp_fwd_row_gemm_gsum)
-TPMLP_TC_KERNEL(tpmlp_bwd_dgrad_act_wgrad2)
-TPMLP_TC_KERNEL(tpmlp_bwd_dx_fsum_wgrad1)
-TPMLP_TC_KERNEL(tpmlp_attn_qkv_proj)
-TPMLP_TC_KERNEL(tpmlp_attn_out_proj_gsum)
-TPMLP_TC_KERNEL(tpmlp_attn_out_proj_bwd)
-TPMLP_TC_KERNEL(tpmlp_attn_qkv_bwd_dx_fsum)
+TPMLP_TC_KERNELS(tpmlp_fwd_column_gemm_act)
+TPMLP_TC_KERNELS(tpmlp_fwd_row_gemm_gsum)
+TPMLP_TC_KERNELS(tpmlp_bwd_dgrad_act_wgrad2)
+TPMLP_TC_KERNELS(tpmlp_bwd_dx_fsum_wgrad1)
+TPMLP_TC_KERNELS(tpmlp_attn_qkv_proj)
+TPMLP_TC_KERNELS(tpmlp_attn_out_proj_gsum)
+TPMLP_TC_KERNELS(tpmlp_attn_out_proj_bwd)
+TPMLP_TC_KERNELS(tpmlp_attn_qkv_bwd_dx_fsum)
 
 int tc_gemm_max_smem_bytes() { return kSmemBytes; }
 
 using KernelFn = void (*)(GemmParams);
 
-KernelFn kernel_for(int tag) {
+KernelFn kernel_for(int tag, bool stream_k) {
   switch (tag) {
-    case TAG_FWD_COLUMN: return tpmlp_fwd_column_gemm_act;
-    case TAG_FWD_ROW: return tpmlp_fwd_row_gemm_gsum;
-    case TAG_BWD_DGRAD: return tpmlp_bwd_dgrad_act_wgrad2;
-    case TAG_BWD_FSUM: return tpmlp_bwd_dx_fsum_wgrad1;
-    case TAG_ATTN_QKV: return tpmlp_attn_qkv_proj;
-    case TAG_ATTN_OUT: return tpmlp_attn_out_proj_gsum;
-    case TAG_ATTN_OUT_BWD: return tpmlp_attn_out_proj_bwd;
-    case TAG_ATTN_QKV_BWD: return tpmlp_attn_qkv_bwd_dx_fsum;
+    case TAG_FWD_COLUMN: return stream_k ? tpmlp_fwd_column_gemm_act_sk : tpmlp_fwd_column_gemm_act;
+    case TAG_FWD_ROW: return stream_k ? tpmlp_fwd_row_gemm_gsum_sk : tpmlp_fwd_row_gemm_gsum;
+    case TAG_BWD_DGRAD: return stream_k ? tpmlp_bwd_dgrad_act_wgrad2_sk : tpmlp_bwd_dgrad_act_wgrad2;
+    case TAG_BWD_FSUM: return stream_k ? tpmlp_bwd_dx_fsum_wgrad1_sk : tpmlp_bwd_dx_fsum_wgrad1;
+    case TAG_ATTN_QKV: return stream_k ? tpmlp_attn_qkv_proj_sk : tpmlp_attn_qkv_proj;
+    case TAG_ATTN_OUT: return stream_k ? tpmlp_attn_out_proj_gsum_sk : tpmlp_attn_out_proj_gsum;
+    case TAG_ATTN_OUT_BWD: return stream_k ? tpmlp_attn_out_proj_bwd_sk : tpmlp_attn_out_proj_bwd;
+    case TAG_ATTN_QKV_BWD: return stream_k ? tpmlp_attn_qkv_bwd_dx_fsum_sk : tpmlp_attn_qkv_bwd_dx_fsum;
     default: return nullptr;
   }
 }
@@ -489,7 +759,7 @@ int tc_gemm_max_pairs(int tag) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || tag < 0 || tag >= kNumKernelTags) return 0;
   std::lock_guard<std::mutex> lk(mu);
   if (cache[dev][tag] > 0) return cache[dev][tag];
-  KernelFn k = kernel_for(tag);
+  KernelFn k = kernel_for(tag, false);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
@@ -509,7 +779,7 @@ int tc_gemm_max_pairs(int tag) {
 }
 
 cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int max_pairs_hint, cudaStream_t stream) {
-  KernelFn k = p.sk.on ? tc_gemm_sk_kernel(kernel_tag) : kernel_for(kernel_tag);
+  KernelFn k = kernel_for(kernel_tag, p.sk.on != 0);
   if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -1,8 +1,7 @@
-// tc_gemm_common.cuh -- device code shared by the two variants of the
-// persistent 2-SM tcgen05 GEMM (tc_gemm.cu: data-parallel tiles;
-// tc_gemm_sk.cu: the same with a stream-K tail): tile geometry, bounded
-// waits, the per-pair load shape, the straight-line MMA issue of a stage and
-// the fused epilogue of a 32-column chunk.
+// tc_gemm_common.cuh -- device building blocks of the persistent 2-SM
+// tcgen05 GEMM (tc_gemm.cu): tile geometry, bounded waits, the per-pair load
+// shape, the straight-line MMA issue of a stage and the fused epilogue of a
+// 32-column chunk.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,13 +44,6 @@ constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + 8 * kNumBa
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
 constexpr uint64_t kPeerDrainNs = 2ull * 1000 * 1000;
 constexpr uint16_t kPairMask = 0x3;
-// K blocks between the L2 prefetch of a block and its load into the ring:
-// the ring holds about 3,500 MMA cycles, less than a miss to HBM under load,
-// so loads are made to hit L2 instead.
-#ifndef TPMLP_PREFETCH_KBLOCKS
-#define TPMLP_PREFETCH_KBLOCKS 0
-#endif
-constexpr int kPrefetchKBlocks = TPMLP_PREFETCH_KBLOCKS;
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kNumAcc * kAccCols <= kTmemCols, "TMEM budget");

@@ -42,6 +42,9 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 thread_local int g_last_launches = 0;
+// Tiles the stream-K tail split in the last launch of each kind on this
+// thread: (problem, first row, first column) per tile.
+thread_local std::vector<int64_t> g_last_split[kNumKernelTags];
 thread_local char g_last_error[256] = "";
 
 tpmlp_status fail(tpmlp_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -245,7 +248,26 @@ struct Builder {
     return idx;
   }
 
+  // Table overflow (too many problems, segments or groups for one launch):
+  // sticky like map_error; the entries past the end go to a dummy slot that
+  // is never launched.
+  bool table_error = false;
+  Prob dummy_prob{};
+  Seg dummy_seg{};
+  Group dummy_group{};
+  bool table_full(int used, int cap, const char* what) {
+    if (used < cap) return false;
+    if (!table_error) fail(TPMLP_ERR_UNSUPPORTED, "more than %d %s in one launch", cap, what);
+    table_error = true;
+    return true;
+  }
+  Group& group_at(int g) { return g >= 0 && g < kMaxGroups ? p->groups[g] : dummy_group; }
+
   void begin_group(int64_t M, int band_m) {
+    if (table_full(p->num_groups, kMaxGroups, "problem groups")) {
+      cur_group = -1;
+      return;
+    }
     Group& G = p->groups[p->num_groups];
     cur_group = p->num_groups++;
     G.first_prob = p->num_probs;
@@ -257,6 +279,11 @@ struct Builder {
   }
 
   Prob& add_prob(int64_t M, int64_t N, int tile_n, int a_major, int b_major, int epi, int64_t ldo) {
+    if (cur_group < 0 || table_full(p->num_probs, kMaxProbs, "GEMM problems")) {
+      table_error = true;
+      dummy_prob = Prob{};
+      return dummy_prob;
+    }
     Prob& P = p->probs[p->num_probs++];
     P.M = static_cast<int32_t>(M);
     P.N = static_cast<int32_t>(N);
@@ -270,7 +297,7 @@ struct Builder {
     P.out_map[0] = P.out_map[1] = P.out_map[2] = -1;
     P.out_striped = 0;
     P.ldo = ldo;
-    Group& G = p->groups[cur_group];
+    Group& G = group_at(cur_group);
     G.num_probs++;
     G.tiles_per_row += P.tiles_n;
     return P;
@@ -278,6 +305,7 @@ struct Builder {
 
   void add_seg(Prob& P, const void* a, int64_t a_rows, int64_t a_cols, const void* b, int64_t b_rows,
                int64_t b_cols, const void* b2, int64_t K) {
+    if (&P == &dummy_prob || table_full(p->num_segs, kMaxSegs, "K segments")) return;
     Seg& S = p->segs[p->num_segs++];
     S.a = a;
     S.b = b;
@@ -298,6 +326,7 @@ struct Builder {
   }
 
   void end_group() {
+    if (cur_group < 0) return;
     Group& G = p->groups[cur_group];
     p->total_tiles += G.tiles_m * G.tiles_per_row;
   }
@@ -317,8 +346,9 @@ int band_for(int sms) {
   return b;
 }
 
-// Tile -> problem, as the kernel's decode_tile maps it.
-int tile_prob(const GemmParams& p, int tile) {
+// Tile -> problem and its first output row and column, as the kernel's
+// decode_tile maps it.
+int tile_prob(const GemmParams& p, int tile, int* m0 = nullptr, int* n0 = nullptr) {
   int g = 0;
   while (g + 1 < p.num_groups && tile >= p.groups[g + 1].tile_start) ++g;
   const Group& G = p.groups[g];
@@ -326,16 +356,20 @@ int tile_prob(const GemmParams& p, int tile) {
   const int full_band = G.band_m * G.tiles_per_row;
   const int band = local / full_band;
   const int bm = std::min(G.band_m, G.tiles_m - band * G.band_m);
-  int n_lin = (local - band * full_band) / bm;
+  const int r = local - band * full_band;
+  int n_lin = r / bm;
+  const int mt = band * G.band_m + (r - n_lin * bm);
   int pi = G.first_prob;
   while (n_lin >= p.probs[pi].tiles_n) {
     n_lin -= p.probs[pi].tiles_n;
     ++pi;
   }
+  if (m0) *m0 = mt * p.tile_m;
+  if (n0) *n0 = n_lin * p.probs[pi].tile_n;
   return pi;
 }
 
-std::atomic<uint32_t> g_sk_epoch{0};
+std::atomic<uint32_t> g_sk_epoch{0};  // tags of the stream-K launches' ticket counts
 
 // Cut the stream-K tail of a tensor-core launch (see StreamK).  Every full
 // wave of tiles stays data-parallel: the pairs of a wave start together and
@@ -413,8 +447,22 @@ void plan_stream_k(GemmParams& p, int pairs, int mode) {
       sk.start_kb[r] = static_cast<int32_t>(static_cast<int64_t>(kb[dp_tiles + j]) * i / k);
     }
   }
-  uint32_t e = ++g_sk_epoch;
-  if (e == 0) e = ++g_sk_epoch;
+  // Each range holds one part of one tile.  Per range: its tile's first
+  // non-empty range (a tile with fewer K blocks than k has empty ranges, and
+  // they may come first) and its tile's number of non-empty ranges.
+  for (int r = 0; r < pairs; ++r) {
+    const int j = r / k;
+    int first = -1, parts = 0;
+    for (int q = j * k; q < std::min(pairs, (j + 1) * k); ++q) {
+      if (sk.start_tile[q] == sk.start_tile[q + 1] && sk.start_kb[q] == sk.start_kb[q + 1]) continue;
+      if (first < 0) first = q;
+      ++parts;
+    }
+    sk.first_range[r] = static_cast<int16_t>(first < 0 ? r : first);
+    sk.num_parts[r] = static_cast<int16_t>(parts);
+  }
+  uint32_t e = ++g_sk_epoch & 0xFFFFFFu;  // 24-bit tag of this launch's ticket counts
+  if (e == 0) e = ++g_sk_epoch & 0xFFFFFFu;
   sk.on = 1;
   sk.dp_tiles = dp_tiles;
   sk.pairs = pairs;
@@ -443,6 +491,7 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
         if (outs[k]) P.out_map[k] = B.map(outs[k], P.M, P.N, kOutputMap, P.ldo);
     }
   }
+  if (B.table_error) return TPMLP_ERR_UNSUPPORTED;  // message set by Builder::table_full
   if (B.map_error) return TPMLP_ERR_INVALID_ARG;  // message set by Builder::map
   p.status = static_cast<int32_t*>(workspace);
   p.timeout_ns = plan->timeout_ns;
@@ -456,6 +505,15 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
       for (int sg = P.seg_begin; sg < P.seg_begin + P.seg_count; ++sg) P.kblocks += (p.segs[sg].K + kTcBK - 1) / kTcBK;
     }
     if (sk_workspace) plan_stream_k(p, tc_gemm_max_pairs(tag), plan->stream_k);
+  }
+  std::vector<int64_t>& split = g_last_split[tag];
+  split.clear();
+  if (p.sk.on) {
+    for (int t = p.sk.dp_tiles; t < p.total_tiles; ++t) {
+      int m0 = 0, n0 = 0;
+      const int pi = tile_prob(p, t, &m0, &n0);
+      split.insert(split.end(), {pi, m0, n0});
+    }
   }
   cudaError_t e;
   if (B.tc) {
@@ -666,14 +724,13 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
     }
     return TPMLP_OK;
   }
-  Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
+  const bool tc = pl->dtype == TPMLP_BF16;
   const int band = band_for(di.sms);
-  if (X_stripes || dX_stripes) {  // X gathered from its stripes; dX reduce-scattered into stripes
-    B.set_stripes(pl, X_stripes, pl->d, dX_stripes, pl->d);
-    if (X_stripes) X = kStripedIn;
-    if (dX_stripes) dX = kStripedOut;
-  }
-  if (H_for_dW2) {  // recompute mode: dW2_i = H_i^T dY from the H the dgrad launch rewrote
+  // Recompute mode: dW2_i = H_i^T dY from the H the dgrad launch rewrote.  It
+  // shares the f-sum launch unless that launch's tables would overflow (the
+  // SwiGLU tensor maps, 10t + 3, for t > 12); it then runs as a launch of its
+  // own just before.
+  auto add_dw2 = [&](Builder& B) {
     for (int i = 0; i < pl->t; ++i) {
       const int64_t di_ = pl->d_i[i];
       B.begin_group(di_, band);
@@ -682,7 +739,22 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
       B.add_seg(P, H_for_dW2[i], pl->T, di_, dY, pl->T, pl->d, nullptr, pl->T);
       B.end_group();
     }
+  };
+  const int t = pl->t;
+  const bool dw2_fits = (!tc || (sw ? 10 : 6) * t + 3 <= kMaxMaps) && (sw ? 3 : 2) * t + 1 <= kMaxProbs &&
+                        (sw ? 5 : 3) * t <= kMaxSegs && t + 2 <= kMaxGroups;
+  if (H_for_dW2 && !dw2_fits) {
+    Builder B2(scratch_params(), tc);
+    add_dw2(B2);
+    TPMLP_TRY(launch(B2, TAG_BWD_FSUM, di, pl, ws, st));
   }
+  Builder B(scratch_params(), tc);
+  if (X_stripes || dX_stripes) {  // X gathered from its stripes; dX reduce-scattered into stripes
+    B.set_stripes(pl, X_stripes, pl->d, dX_stripes, pl->d);
+    if (X_stripes) X = kStripedIn;
+    if (dX_stripes) dX = kStripedOut;
+  }
+  if (H_for_dW2 && dw2_fits) add_dw2(B);
   // dW1_i = X^T dA_i (SwiGLU: X^T dG_i) and dW3_i = X^T dU_i (K = T)
   B.begin_group(pl->d, band);
   for (int i = 0; i < pl->t; ++i) {
@@ -1337,8 +1409,8 @@ tpmlp_status tpmlp_check(const tpmlp_plan* plan, void* workspace, tpmlp_stream_t
   e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e);
   if (word != kDevOk) {
-    // Clear the status word and, for bf16 plans, the stream-K flags that an
-    // aborted launch may have left raised.
+    // Clear the status word and, for bf16 plans, the stream-K ticket counters
+    // that an aborted launch may have left behind.
     const size_t n = plan->dtype == TPMLP_BF16 ? kSkSlotsOffset : sizeof(word);
     e = cudaMemset(workspace, 0, n);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -1363,7 +1435,48 @@ const char* tpmlp_status_string(tpmlp_status s) {
 
 int tpmlp_last_cuda_error(void) { return g_last_cuda_error; }
 const char* tpmlp_last_error(void) { return g_last_error; }
-int tpmlp_version(void) { return 104; }
+int tpmlp_version(void) { return 105; }
 int tpmlp_last_launch_count(void) { return g_last_launches; }
+
+tpmlp_status tpmlp_eval_activation(int fn, const float* x, const float* y, const float* dh, float* out0,
+                                   float* out1, float* out2, int64_t n, tpmlp_stream_t stream) {
+  g_last_launches = 0;
+  g_last_error[0] = 0;
+  if (fn < TPMLP_ACT_EVAL_GELU || fn > TPMLP_ACT_EVAL_FP32_SWIGLU)
+    return fail(TPMLP_ERR_INVALID_ARG, "unknown activation form %d", fn);
+  if (n < 0) return fail(TPMLP_ERR_INVALID_ARG, "n = %lld < 0", static_cast<long long>(n));
+  const bool sw = fn == TPMLP_ACT_EVAL_SWIGLU || fn == TPMLP_ACT_EVAL_SWIGLU_BWD ||
+                  fn == TPMLP_ACT_EVAL_SWIGLU_BWD_H || fn == TPMLP_ACT_EVAL_FP32_SWIGLU;
+  const bool bwd = fn != TPMLP_ACT_EVAL_GELU && fn != TPMLP_ACT_EVAL_SWIGLU;
+  const int nout = fn == TPMLP_ACT_EVAL_GELU || fn == TPMLP_ACT_EVAL_GELU_BWD || fn == TPMLP_ACT_EVAL_SWIGLU
+                       ? 1
+                       : (fn == TPMLP_ACT_EVAL_GELU_BWD_H || fn == TPMLP_ACT_EVAL_SWIGLU_BWD ||
+                                  fn == TPMLP_ACT_EVAL_FP32_GELU
+                              ? 2
+                              : 3);
+  const void* need[6] = {x, sw ? y : x, bwd ? dh : x, out0, nout > 1 ? out1 : out0, nout > 2 ? out2 : out0};
+  const char* names[6] = {"x", "y", "dh", "out0", "out1", "out2"};
+  for (int i = 0; i < 6; ++i) {
+    if (n > 0 && !need[i]) return fail(TPMLP_ERR_INVALID_ARG, "%s is NULL", names[i]);
+    if (reinterpret_cast<uintptr_t>(need[i]) & 3u)
+      return fail(TPMLP_ERR_ALIGNMENT, "%s (%p) is not 4-byte aligned", names[i], need[i]);
+  }
+  DeviceInfo di;
+  TPMLP_TRY(device_info(&di));
+  cudaError_t e = launch_act_eval(fn, x, sw ? y : nullptr, bwd ? dh : nullptr, out0, nout > 1 ? out1 : nullptr,
+                                  nout > 2 ? out2 : nullptr, n, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (n > 0) ++g_last_launches;
+  return TPMLP_OK;
+}
+
+int tpmlp_last_split_tiles(int launch_kind, int64_t* tiles, int cap) {
+  if (launch_kind < 0 || launch_kind >= kNumKernelTags) return -1;
+  const std::vector<int64_t>& v = g_last_split[launch_kind];
+  const int n = static_cast<int>(v.size() / 3);
+  if (tiles)
+    for (int i = 0; i < std::min(n, cap) * 3; ++i) tiles[i] = v[i];
+  return n;
+}
 
 }  // extern "C"

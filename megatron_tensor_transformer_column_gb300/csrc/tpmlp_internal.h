@@ -31,10 +31,16 @@ constexpr int kTcBK = TPMLP_TC_BK;
 // the tensor-core epilogue's TMA stores: the SwiGLU f-sum launch adds dW1_i,
 // dW3_i and dX (2t + 1), the SwiGLU dgrad launch dG_i, dU_i, dW2_i and, when
 // H is recomputed, H_i (4t).
+// Problems, segments and groups: the largest launch is the SwiGLU f-sum
+// launch of the recompute backward, which also carries dW2_i = H_i^T dY:
+// 3t + 1 problems (dW2_i, dW1_i, dW3_i, dX), 5t segments (one each for the
+// weight gradients, 2t for dX) and t + 2 groups.  Its tensor maps (10t + 3)
+// exceed kMaxMaps for t > 12; the host then moves dW2 to a launch of its own.
+// The host checks every table bound while it builds a launch.
 constexpr int kMaxMaps = 8 * kMaxShards + 4;
-constexpr int kMaxProbs = 2 * kMaxShards + 2;
+constexpr int kMaxProbs = 3 * kMaxShards + 2;
 constexpr int kMaxGroups = kMaxShards + 2;
-constexpr int kMaxSegs = 4 * kMaxShards + 2;
+constexpr int kMaxSegs = 5 * kMaxShards + 2;
 
 // Fused epilogues.  acc is the fp32 accumulator tile; bias vectors are
 // optional (null = none) and indexed by output column.
@@ -117,21 +123,21 @@ struct Stripes {
 };
 
 // Stream-K tail (tensor-core path).  Tiles [0, dp_tiles) are dealt out round
-// robin, tile i to pair i mod pairs.  The K blocks of the remaining tiles,
-// in tile order, are cut into one contiguous range per pair, sized so that
-// every pair ends with about the same number of K blocks; range r (held by
-// pair pairs - 1 - r) starts at (start_tile[r], start_kb[r]) and ends where
-// range r + 1 starts.  A tile cut between ranges is finished by the pair
-// holding its K block 0 (the owner: that part is the last of its range);
-// each other part is the first of its range, and its pair leaves the fp32
-// accumulator in the range's workspace slot and raises one flag per epilogue
-// warp.  The owner adds the parts in range order, so the result is the same
-// on every run.  Owners wait only on lower-numbered pairs, which the hardware
-// starts first.
+// robin, tile i to pair i mod pairs.  The K blocks of each remaining tile
+// (the last, partial wave) are cut into parts, one per range: range r (held
+// by pair pairs - 1 - r) starts at (start_tile[r], start_kb[r]) and ends
+// where range r + 1 starts; the ranges of a tile are consecutive and each
+// starts inside it.  Every part leaves its fp32 accumulator in its range's
+// workspace slot and takes a ticket from a per-tile counter (one per
+// epilogue warp position, in the flag block, tagged with the launch's epoch
+// so that a count left by an aborted launch reads as zero); the part with
+// the last ticket adds all parts in range order and runs the tile's
+// epilogue.  Nobody waits for another pair, and the fixed order makes the
+// result the same on every run.
 constexpr int kMaxSkPairs = 80;
 constexpr int kSkWarpsPerPair = 16;                        // epilogue warps of a pair
 constexpr size_t kStatusBytes = 256;                       // workspace: status word block
-constexpr size_t kSkFlagsOffset = kStatusBytes;            // kMaxSkPairs x kSkWarpsPerPair uint32 flags
+constexpr size_t kSkFlagsOffset = kStatusBytes;            // kMaxSkPairs x kSkWarpsPerPair uint32 counters
 constexpr size_t kSkSlotsOffset = 8192;                    // partial accumulators, one slot per range
 constexpr size_t kSkSlotBytes = 256 * 256 * sizeof(float);
 constexpr size_t kSkWorkspaceBytes = kSkSlotsOffset + kMaxSkPairs * kSkSlotBytes;
@@ -140,9 +146,11 @@ struct StreamK {
   int32_t on;
   int32_t dp_tiles;  // data-parallel tiles (all of them when on == 0)
   int32_t pairs;     // pairs the ranges were made for (the launched pairs)
-  uint32_t epoch;    // value of a raised flag in this launch (never 0)
+  uint32_t epoch;    // tag of this launch's ticket counts (24 bits, never 0)
   int32_t start_tile[kMaxSkPairs + 1];
   int32_t start_kb[kMaxSkPairs + 1];
+  int16_t first_range[kMaxSkPairs];  // per range: the first non-empty range of its tile
+  int16_t num_parts[kMaxSkPairs];    // per range: the non-empty ranges of its tile
 };
 
 struct GemmParams {
@@ -157,7 +165,7 @@ struct GemmParams {
   int32_t tile_m;
   int32_t* status;          // device status word (workspace)
   uint64_t timeout_ns;      // bound on every wait inside the kernel
-  int32_t stall_injection;  // test hook: 1, producers load nothing; 2, stream-K parts are never published
+  int32_t stall_injection;  // test hook: 1, producers load nothing; 2, stream-K parts but a tile's first run late
 };
 
 // Column sums over tokens (bias gradients): dst[c] = sum_r src[r][c].
@@ -190,22 +198,20 @@ constexpr int32_t kDevOk = 0;
 constexpr int32_t kDevTimeoutProducer = 1;
 constexpr int32_t kDevTimeoutMma = 2;
 constexpr int32_t kDevTimeoutEpilogue = 3;
-constexpr int32_t kDevTimeoutPartial = 4;  // an owner waited too long for another pair's partial
 
 // Launchers (defined next to their kernels).
 int tc_gemm_max_smem_bytes();
 // Launches clusters of two CTAs: p.sk.pairs of them when the stream-K tail is
-// on, else as many as fit on the device (at most one per tile);
-// max_pairs_hint is used if the occupancy query fails.
+// on (the kernel's stream-K instance), else as many as fit on the device (at
+// most one per tile); max_pairs_hint is used if the occupancy query fails.
 cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int max_pairs_hint, cudaStream_t stream);
 // Pairs (clusters of two CTAs) of a launch kind that can be resident at once
 // on the current device (0 if the query fails).
 int tc_gemm_max_pairs(int kernel_tag);
-// The stream-K variant's kernel of a launch kind (tc_gemm_sk.cu; same
-// resources as the data-parallel kernel), or null for an unknown tag.
-using TcKernelFn = void (*)(GemmParams);
-TcKernelFn tc_gemm_sk_kernel(int kernel_tag);
 cudaError_t launch_simt_gemm(const GemmParams& p, cudaStream_t stream);
+// The epilogues' activation forms on plain arrays (tpmlp_eval_activation).
+cudaError_t launch_act_eval(int fn, const float* x, const float* y, const float* dh, float* o0, float* o1,
+                            float* o2, int64_t n, cudaStream_t stream);
 
 // Kernel tags: one kernel symbol per launch kind, so that profiles tell the
 // launches of a training step apart.
