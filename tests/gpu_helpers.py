@@ -62,3 +62,69 @@ def cat_cols(ts):
 
 def cat_rows(ts):
     return torch.cat([t.to("cpu", torch.float64) for t in ts], dim=0).numpy()
+
+
+# ---------------------------------------------------------------- tile-complete samples
+# The tensor-core launches compute 256 x 256 output tiles (SwiGLU forward:
+# 256 x 128), each drained by 16 epilogue warps of 32 rows (two CTAs x four
+# TMEM lane quarters, two column halves).  A sampled token row is compared
+# over all of its columns, so it checks every N-tile of its 256-row band in
+# the outputs indexed by tokens (Y, dX, A/G/U, H, dA/dU); a sampled hidden
+# unit j is compared over a whole column of dW1/dW3 and a whole row of dW2, so
+# it checks every tile of its 256-wide band of the shard in those outputs.
+
+TILE = 256
+WARP_ROWS = 32
+
+
+def tile_rows(T: int, seed: int = 7, per_band: int = 1):
+    """Token rows with at least `per_band` in every 256-row band.  Band b's
+    first row sits in the 32-row warp slot (b mod 8), so the bands together
+    reach every epilogue warp's rows; further rows of a band go to the next
+    slots.  Also the first and the last row.  Sorted, unique."""
+    rng = np.random.default_rng(seed)
+    rows = {0, T - 1}
+    for b in range((T + TILE - 1) // TILE):
+        for k in range(per_band):
+            lo = b * TILE + ((b + k) % (TILE // WARP_ROWS)) * WARP_ROWS
+            hi = min(lo + WARP_ROWS, T)
+            if lo >= T:  # ragged last band: any of its rows
+                lo, hi = b * TILE, T
+            rows.add(int(rng.integers(lo, hi)))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def band_rows(T: int, band: int):
+    """One row in each of the eight 32-row warp slots of a 256-row band (that exist)."""
+    out = [band * TILE + s * WARP_ROWS + (s * 5) % WARP_ROWS for s in range(TILE // WARP_ROWS)]
+    return [r for r in out if r < T]
+
+
+def tile_units(d_i, seed: int = 7):
+    """Hidden units with one in every 256-wide band of every shard, plus each
+    shard's first and last unit.  Sorted, unique, global unit indices."""
+    import synthetic_inputs as si
+    rng = np.random.default_rng(seed)
+    units = set()
+    for lo, hi in si.shard_slices(d_i):
+        units.update((lo, hi - 1))
+        for b0 in range(lo, hi, TILE):
+            units.add(int(rng.integers(b0, min(b0 + TILE, hi))))
+    return np.array(sorted(units), dtype=np.int64)
+
+
+def rows_of(ts, rows):
+    """Rows of a list of per-shard [T x d_i] device tensors, side by side (fp64 numpy)."""
+    idx = torch.as_tensor(rows, device=ts[0].device)
+    return torch.cat([t.index_select(0, idx).to(torch.float64) for t in ts], dim=1).cpu().numpy()
+
+
+def dev_rel_err(got: torch.Tensor, ref: torch.Tensor) -> float:
+    """rel_err of two device tensors without leaving the device (fp32 arithmetic)."""
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    if got.numel() == 0:
+        return 0.0
+    g, r = got.float(), ref.float()
+    scale = float(r.abs().max())
+    diff = float((g - r).abs().max())
+    return diff if scale == 0.0 else diff / scale

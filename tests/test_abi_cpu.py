@@ -48,7 +48,7 @@ def test_library_exports_nothing_else(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert tp.tpmlp_version() == 104
+    assert tp.tpmlp_version() == 105
     for code, name in tp.STATUS.items():
         assert tp.tpmlp_status_string(code) == name
     assert tp.tpmlp_status_string(99) == "TPMLP_ERR_UNKNOWN"

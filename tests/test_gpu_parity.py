@@ -13,7 +13,8 @@ import torch
 
 import oracle
 import synthetic_inputs as si
-from gpu_helpers import cat_cols, cat_rows, rel_err, run_gpu, to_np, tol_for
+from gpu_helpers import (TILE, band_rows, cat_cols, cat_rows, dev_rel_err, rel_err, rows_of, run_gpu,
+                         tile_rows, tile_units, to_np, tol_for)
 
 pytestmark = pytest.mark.gpu
 
@@ -126,40 +127,91 @@ def test_config_C1_fp32(gpu_lib):
 
 
 # ------------------------------------------------------------- full-size workloads (sampled)
+# Tile-complete samples (gpu_helpers.tile_rows / tile_units): a token row in
+# every 256-row band, cycling over the eight 32-row epilogue-warp slots, and a
+# hidden unit in every 256-wide band of every shard; each sampled row is
+# compared over all of its columns and each unit over a whole column of dW1
+# (dW3) and row of dW2, so every output tile of every launch is checked.
+# Tiles the stream-K tail split in the run (tpmlp_last_split_tiles) get a row
+# in each of their eight warp slots (or their units, for weight gradients).
 
-def _sampled_compare(tp, w: si.Workload, nrows=24, nunits=24, seed=1234, extra_rows=(), stream_k=None):
+def _split_samples(tp, w, rows, units):
+    """Add rows / units covering every tile the stream-K tail split in the last
+    four launches.  Returns (rows, units, split) with split = {launch: tiles}."""
+    t = len(w.d_i)
+    offs = [lo for lo, _ in si.shard_slices(w.d_i)]
+    split = {k: tp.tpmlp_last_split_tiles(k) for k in
+             (tp.LAUNCH_FWD_COLUMN, tp.LAUNCH_FWD_ROW, tp.LAUNCH_BWD_DGRAD, tp.LAUNCH_BWD_FSUM)}
+    add_r, add_u = [], []
+    nw = 3 if w.act == "swiglu" else 2  # weight-gradient problem groups ahead of dX in the f-sum launch
+    for kind, tiles in split.items():
+        for prob, m0, n0 in tiles:
+            if kind in (tp.LAUNCH_FWD_COLUMN, tp.LAUNCH_FWD_ROW) or (kind == tp.LAUNCH_BWD_DGRAD and prob >= t):
+                add_r += band_rows(w.T, m0 // TILE)  # token rows: A / H, Y, dact
+            elif kind == tp.LAUNCH_BWD_DGRAD:  # dW2_prob: rows m0.. of the shard
+                hi = offs[prob] + w.d_i[prob]
+                add_u += [u for u in (offs[prob] + m0, offs[prob] + m0 + 97, offs[prob] + m0 + 255) if u < hi]
+            elif prob >= (nw - 1) * t:  # dX
+                add_r += band_rows(w.T, m0 // TILE)
+            else:  # dW1_i / dW3_i: columns n0.. of shard i
+                i = prob % t
+                hi = offs[i] + w.d_i[i]
+                add_u += [u for u in (offs[i] + n0, offs[i] + n0 + 131, offs[i] + n0 + 255) if u < hi]
+    rows = np.union1d(rows, np.asarray(add_r, dtype=np.int64))
+    units = np.union1d(units, np.asarray(add_u, dtype=np.int64))
+    return rows, units, split
+
+
+def _sampled_compare(tp, w: si.Workload, seed=1234, extra_rows=(), stream_k=None, rows=None, units=None,
+                     intermediates=True, tile_complete=True):
     inp = si.make_workload_inputs(w, seed)
     g = run_gpu(tp, inp, w.act, w.dtype, stream_k=stream_k)
-    rng = np.random.default_rng(7)
-    rows = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, nrows, replace=False),
-                                     np.asarray(extra_rows, dtype=np.int64)]))
-    units = np.unique(np.concatenate([[0, w.dff - 1], rng.choice(w.dff, nunits, replace=False)]))
-    # include the first and last unit of every shard (shard boundaries)
-    for lo, hi in si.shard_slices(w.d_i):
-        units = np.union1d(units, [lo, hi - 1])
-    Yr, dXr = oracle.rows(inp.X, inp.W1, inp.W2, inp.dY, rows, act=w.act, W3=inp.W3)
+    if rows is None:
+        rows = tile_rows(w.T)
+    rows = np.union1d(rows, np.asarray(extra_rows, dtype=np.int64))
+    if units is None:
+        units = tile_units(w.d_i)
+    rows, units, split = _split_samples(tp, w, rows, units)
+    Yr, dXr, inter = oracle.rows(inp.X, inp.W1, inp.W2, inp.dY, rows, act=w.act, W3=inp.W3, intermediates=True)
     c1, c3, c2 = oracle.wgrad_units(inp.X, inp.W1, inp.W2, inp.dY, units, act=w.act, W3=inp.W3)
-    Y = to_np(g["Y"])[rows]
-    dX = to_np(g["dX"])[rows]
+    t = len(w.d_i)
+    ridx = torch.as_tensor(rows, device=g["Y"].device)
+    Y = g["Y"].index_select(0, ridx).double().cpu().numpy()
+    dX = g["dX"].index_select(0, ridx).double().cpu().numpy()
     dW1 = cat_cols(g["dW1"])[:, units].T
     dW2 = cat_rows(g["dW2"])[units, :]
     tol = tol_for(w.dtype)
     errs = {"Y": rel_err(Y, Yr), "dX": rel_err(dX, dXr), "dW1": rel_err(dW1, c1), "dW2": rel_err(dW2, c2)}
     if w.act == "swiglu":
         errs["dW3"] = rel_err(cat_cols(g["dW3"])[:, units].T, c3)
+    if intermediates:  # the saved pre-activations, H and the activation gradients
+        errs["A"] = rel_err(rows_of(g["saved"][:t], rows), inter["A"])
+        errs["H"] = rel_err(rows_of(g["H"], rows), inter["H"])
+        errs["dA"] = rel_err(rows_of(g["dact"][:t], rows), inter["dA"])
+        if w.act == "swiglu":
+            errs["U"] = rel_err(rows_of(g["saved"][t:], rows), inter["U"])
+            errs["dU"] = rel_err(rows_of(g["dact"][t:], rows), inter["dU"])
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{w.name}: over tolerance {tol}: {bad} (all: {errs})"
+    if tile_complete:  # every 256-row band and every 256-wide band of every shard was compared
+        assert set(rows // TILE) == set(range((w.T + TILE - 1) // TILE))
+        for lo, hi in si.shard_slices(w.d_i):
+            assert set((units[(units >= lo) & (units < hi)] - lo) // TILE) == set(range((hi - lo + TILE - 1) // TILE))
     # properties that hold at any size: finite outputs everywhere
     for k in ("Y", "dX"):
         assert torch.isfinite(g[k]).all()
-    for k in ("dW1", "dW2"):
+    for k in ("dW1", "dW2", "H", "saved", "dact"):
         assert all(torch.isfinite(x).all() for x in g[k])
-    return g, errs
+    return g, errs, split
 
 
 @pytest.mark.parametrize("name", ["C2t1", "C2t2", "C2t4", "C3", "C4", "C5"])
 def test_workload_sampled_parity(gpu_lib, name):
-    _sampled_compare(gpu_lib, si.WORKLOADS[name])
+    _, _, split = _sampled_compare(gpu_lib, si.WORKLOADS[name])
+    if name == "C5":
+        # the default (automatic) stream-K mode splits the row launch's last
+        # wave at this size; its tiles were among the compared ones
+        assert split[gpu_lib.LAUNCH_FWD_ROW], "expected the row launch's last wave to be split"
 
 
 def test_stream_k_soak_bitwise(gpu_lib):
@@ -199,21 +251,40 @@ def test_workload_sampled_parity_stream_k_always(gpu_lib, name):
     _sampled_compare(gpu_lib, si.WORKLOADS[name], stream_k=gpu_lib.STREAM_K_ALWAYS)
 
 
-def test_C2_shard_count_invariance(gpu_lib):
-    """C2 at t = 1, 2, 4: the same full weights give the same outputs within the bound."""
-    w1 = si.WORKLOADS["C2t1"]
-    inp = si.make_workload_inputs(w1)
-    outs = {}
-    for t in (1, 2, 4):
-        d_i = tuple([w1.dff // t] * t)
-        g = run_gpu(gpu_lib, inp, "gelu", "bf16", d_i=d_i)
-        outs[t] = {"Y": to_np(g["Y"]), "dX": to_np(g["dX"]), "dW1": cat_cols(g["dW1"]), "dW2": cat_rows(g["dW2"])}
-        del g
-        torch.cuda.empty_cache()
-    for a, b in ((1, 2), (1, 4), (2, 4)):
-        for k in outs[1]:
-            e = rel_err(outs[b][k], outs[a][k])
-            assert e <= 2e-2, f"t={a} vs t={b}: {k} differs by {e}"
+def _run_for_invariance(tp, inp, act, d_i):
+    g = run_gpu(tp, inp, act, "bf16", d_i=d_i)
+    out = {"Y": g["Y"], "dX": g["dX"], "dW1": torch.cat(g["dW1"], 1), "dW2": torch.cat(g["dW2"], 0),
+           "H": torch.cat(g["H"], 1), "A": torch.cat(g["saved"], 1), "dA": torch.cat(g["dact"], 1)}
+    if act == "swiglu":
+        out["dW3"] = torch.cat(g["dW3"], 1)
+    return out
+
+
+# (workload, shard layouts of the same full weights)
+INVARIANCE = [
+    ("C2t1", [(3072,), (1536,) * 2, (768,) * 4]),
+    ("C3", [(1536, 2560, 2048, 2048), (2048,) * 4, (8192,)]),
+    ("C4", [(1376,) * 8, (5504,) * 2, (11008,)]),
+    ("C5", [(1536,) * 8, (6144,) * 2, (12288,)]),
+]
+
+
+@pytest.mark.parametrize("name,layouts", INVARIANCE, ids=[c[0] for c in INVARIANCE])
+def test_shard_count_invariance(gpu_lib, name, layouts):
+    """The same full weights cut into different shard layouts (t = 1, 2, 4 or 8,
+    equal or unequal widths) give the same outputs, activations and gradients
+    within the bf16 bound, compared in full on the device (every element).  For
+    SwiGLU the saved pre-activations are [G | U] side by side."""
+    w = si.WORKLOADS[name]
+    inp = si.make_workload_inputs(w)
+    outs = [_run_for_invariance(gpu_lib, inp, w.act, d_i) for d_i in layouts]
+    for a in range(len(outs)):
+        for b in range(a + 1, len(outs)):
+            for k in outs[0]:
+                e = dev_rel_err(outs[b][k], outs[a][k])
+                assert e <= 2e-2, f"{name}: d_i={layouts[a]} vs d_i={layouts[b]}: {k} differs by {e}"
+    del outs
+    torch.cuda.empty_cache()
 
 
 def test_tensors_beyond_2_pow_31_elements(gpu_lib):
@@ -223,5 +294,9 @@ def test_tensors_beyond_2_pow_31_elements(gpu_lib):
     those where the offset into A / H / dA crosses 2^31."""
     w = si.Workload("large gelu bf16 T=2^21+96 d=256 t=1x1536", 2 ** 21 + 96, 256, (1536,), "gelu", "bf16")
     cross = (2 ** 31) // 1536
-    _sampled_compare(gpu_lib, w, nrows=12, nunits=12, extra_rows=(cross - 1, cross, cross + 1, 2 ** 21 + 95))
+    rng = np.random.default_rng(3)
+    rows = np.concatenate([[0], rng.choice(w.T, 12, replace=False)])
+    units = np.concatenate([[0, 1535], rng.choice(1536, 8, replace=False)])
+    _sampled_compare(gpu_lib, w, extra_rows=(cross - 1, cross, cross + 1, 2 ** 21 + 95), rows=rows, units=units,
+                     tile_complete=False)
     torch.cuda.empty_cache()

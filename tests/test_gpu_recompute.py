@@ -103,3 +103,32 @@ def test_recompute_workload_sampled(gpu_lib, name):
         errs["dW3"] = rel_err(cat_cols(g["dW3"])[:, units].T, c3)
     bad = {k: v for k, v in errs.items() if not v <= 2e-2}
     assert not bad, f"{w.name}: {bad} (all {errs})"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_recompute_sixteen_shards(gpu_lib, act, dtype):
+    """The largest launch tables: the recompute f-sum launch carries dW2_i next
+    to dW1_i, dW3_i and dX, 3t + 1 problems and 5t segments for SwiGLU at
+    t = 16 (bf16: more tensor maps than one launch holds, so dW2 gets a launch
+    of its own).  Compared with the oracle on every output."""
+    tp = gpu_lib
+    d_i = (8, 16, 8, 24, 8, 8, 16, 8, 8, 8, 32, 8, 8, 16, 8, 8) if dtype == "bf16" else (4, 8) * 8
+    T, d = (150, 48) if dtype == "bf16" else (37, 20)
+    inp = si.make_inputs(T, d, d_i, act, dtype, seed=31)
+    mlp, X, dY, W1, W2, W3, Y, saved, H = _fwd(tp, inp, act, dtype)
+    for h in H:
+        h.fill_(float("nan"))
+    g = mlp.backward(X, W1, W2, saved, H, dY, W3, recompute=True)
+    torch.cuda.synchronize()
+    mlp.check()
+    f = oracle.forward(inp.X, inp.W1, inp.W2, act=act, W3=inp.W3)
+    b = oracle.backward(inp.X, inp.W1, inp.W2, inp.dY, act=act, W3=inp.W3)
+    errs = {"Y": rel_err(to_np(Y), f["Y"]), "H": rel_err(cat_cols(H), f["H"]),
+            "dX": rel_err(to_np(g["dX"]), b["dX"]), "dW1": rel_err(cat_cols(g["dW1"]), b["dW1"]),
+            "dW2": rel_err(cat_rows(g["dW2"]), b["dW2"])}
+    if act == "swiglu":
+        errs["dW3"] = rel_err(cat_cols(g["dW3"]), b["dW3"])
+    tol = tol_for(dtype)
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"over tolerance {tol}: {bad} (all {errs})"
