@@ -71,6 +71,88 @@ def attn_phase_flops(w: si.AttnWorkload, T: int | None = None, n_i=None, dq_i=No
             "qkv_bwd": 4 * T * w.d * N}
 
 
+def phase_bytes(w: si.Workload) -> dict:
+    """Algorithmic HBM bytes of each launch of a step (bf16 = 2 bytes): every
+    input read once and every output written once.  GeLU (SwiGLU adds W3, U,
+    dU, dW3): column X, W1 -> A, H; row H, W2 -> Y; dgrad dY, W2, A, H -> dA,
+    dW2; f-sum dA, W1, X -> dX, dW1."""
+    e = 2 if w.dtype == "bf16" else 4
+    T, d, f = w.T, w.d, w.dff
+    n = 2 if w.act == "swiglu" else 1  # pre-activations / activation gradients per hidden unit
+    return {"fwd_column": e * (T * d + n * d * f + n * T * f + T * f),
+            "fwd_row": e * (T * f + f * d + T * d),
+            "bwd_dgrad": e * (T * d + f * d + n * T * f + T * f + n * T * f + f * d),
+            "bwd_fsum": e * (n * T * f + n * d * f + T * d + T * d + n * d * f)}
+
+
+def attn_phase_bytes(w: si.AttnWorkload) -> dict:
+    """Algorithmic HBM bytes of the four attention-projection launches (bf16),
+    every input read and every output written once (N = sum of the fused QKV
+    widths, dq = sum of the query widths)."""
+    T, d, N, dq = w.T, w.d, sum(w.n_i), sum(w.dq_i)
+    return {"qkv_fwd": 2 * (T * d + d * N + T * N), "out_fwd": 2 * (T * dq + dq * d + T * d),
+            "out_bwd": 2 * (T * d + dq * d + T * dq + T * dq + dq * d),
+            "qkv_bwd": 2 * (T * N + d * N + T * d + T * d + d * N)}
+
+
+def peak_regime(peaks: dict, peak_src: str, elapsed_ms: float, clocks) -> dict:
+    """The bf16 tensor peak the timed region ran in: the burst figure (a kernel
+    timed alone, clocks free to boost), unless the region lasted a second or
+    more with the power cap active in the clock samples, which is the
+    sustained regime the measured sustained figure was taken in."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    capped = bool(clocks) and "sw_power_cap" in clocks.get("reasons", [])
+    regime = "sustained" if (elapsed_ms >= 1000.0 and capped) else "burst"
+    return {"regime": regime, "peak": sus if regime == "sustained" else burst, "burst": burst, "sustained": sus,
+            "hbm_gbs": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), "source": peak_src,
+            "why": (f"timed region {elapsed_ms:.0f} ms, power cap "
+                    f"{'seen' if capped else 'not seen'} in the clock samples")}
+
+
+def make_roofline(dom: str, flops: dict, nbytes: dict, per_phase: dict, ms_per_step: float, pk: dict, clocks,
+                  traffic):
+    """Dominant-launch roofline (TFLOP/s against the regime's bf16 peak), both
+    peaks' fractions beside it, and the whole step's: the slower of its FLOPs
+    at the tensor peak and its algorithmic bytes at the measured HBM bandwidth,
+    against the measured step time."""
+    achieved = flops[dom] / (per_phase[dom] / 1e3) / 1e12
+    sm = clocks.get("sm_mhz") if clocks else None
+    t_tensor = sum(flops.values()) / (pk["peak"] * 1e12) * 1e3
+    t_hbm = sum(nbytes.values()) / (pk["hbm_gbs"] * 1e9) * 1e3
+    per = {}
+    for k, ms in per_phase.items():
+        if flops.get(k):
+            a = flops[k] / (ms / 1e3) / 1e12
+            per[k] = {"ms": ms, "tflops": a, "frac": a / pk["peak"],
+                      "gbs_algorithmic": nbytes.get(k, 0) / (ms / 1e3) / 1e9}
+    return {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["peak"], "unit": "TFLOP/s",
+            "frac": achieved / pk["peak"], "traffic": traffic, "algorithmic_bytes": nbytes.get(dom),
+            "regime": pk["regime"], "regime_why": pk["why"], "sm_mhz_median": sm,
+            "frac_of_burst": achieved / pk["burst"], "frac_of_sustained": achieved / pk["sustained"],
+            "peak_note": f"{pk['source']} bf16 peaks: burst {pk['burst']}, sustained {pk['sustained']} TFLOP/s",
+            "step": {"bound": "tensor" if t_tensor >= t_hbm else "hbm", "tensor_ms": t_tensor, "hbm_ms": t_hbm,
+                     "measured_ms": ms_per_step, "frac": max(t_tensor, t_hbm) / ms_per_step,
+                     "flops": sum(flops.values()), "algorithmic_bytes": sum(nbytes.values())},
+            "per_launch": per}
+
+
+def parity_rows(T: int, seed: int = 11):
+    """Token rows for the parity check of the timed results: one in every
+    256-row tile band (at the 32-row epilogue-warp slot b mod 8), the first
+    and the last row."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    rows = {0, T - 1}
+    for b in range((T + 255) // 256):
+        lo = b * 256 + (b % 8) * 32
+        hi = min(lo + 32, T)
+        if lo >= T:
+            lo, hi = b * 256, T
+        rows.add(int(rng.integers(lo, hi)))
+    return sorted(rows)
+
+
 def _rec(ev, i, stream):
     """Record event i of a step's event list, if the list has one there."""
     if ev is not None and ev[i] is not None:
@@ -119,7 +201,7 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = ("tc_gemm.cu", "tc_gemm_sk.cu", "tc_gemm_common.cuh", "ptx.cuh", "act.cuh", "tpmlp_internal.h",
+KERNEL_SOURCES = ("tc_gemm.cu", "tc_gemm_common.cuh", "ptx.cuh", "act.cuh", "tpmlp_internal.h",
                   "tpmlp_api.cu")
 
 
@@ -313,6 +395,30 @@ def cpu_baseline(w: si.Workload, tokens: int):
                       f"(full weights), one call of {dt:.1f} s; TFLOP/s = algorithmic FLOPs of that sample / time"}
 
 
+def check_timed_results(w: si.Workload, got: dict, tol: float = 2e-2):
+    """Part of the CPU leg: the last timed step's Y and dX on tile-complete
+    sampled rows, and its dW1 / dW2 on one hidden unit per shard, against the
+    fp64 oracle (each row or unit from its own definition).  Errors are
+    max|err| / max|ref| over the sample, passed at the bf16 bound."""
+    import numpy as np
+    import oracle
+    inp = si.make_workload_inputs(w)
+    t0 = time.perf_counter()
+    Yr, dXr = oracle.rows(inp.X, inp.W1, inp.W2, inp.dY, got["rows"], act=w.act, W3=inp.W3)
+    c1, _, c2 = oracle.wgrad_units(inp.X, inp.W1, inp.W2, inp.dY, got["units"], act=w.act, W3=inp.W3)
+    dt = time.perf_counter() - t0
+
+    def rel(a, b):
+        b = np.asarray(b, dtype=np.float64)
+        return float(np.max(np.abs(np.asarray(a, dtype=np.float64) - b)) / max(np.max(np.abs(b)), 1e-300))
+
+    errs = {"Y": rel(got["Y"], Yr), "dX": rel(got["dX"], dXr), "dW1": rel(got["dW1"], c1), "dW2": rel(got["dW2"], c2)}
+    return {"max_err_over_max_ref": errs, "tol": tol, "pass": all(v <= tol for v in errs.values()),
+            "sample": f"last timed step: Y, dX on {len(got['rows'])} token rows (one in every 256-row tile band), "
+                      f"dW1 columns / dW2 rows of {len(got['units'])} hidden units (one per shard); "
+                      f"oracle {dt:.1f} s"}
+
+
 def attn_cpu_baseline(w: si.AttnWorkload, tokens: int):
     leg = AttnOracleLeg(w, tokens)
     dt = leg.step(tokens)
@@ -486,27 +592,42 @@ def run_ours(args, w: si.Workload):
     total_flops = flops_fwd_bwd(w) * ws
     value = total_flops * args.steps / (elapsed_ms / 1e3) / 1e12
 
+    # ---- the last timed step's results on sampled rows / units, for the
+    # parity check of the CPU leg (copied out before anything else runs)
+    rows = parity_rows(w.T)
+    units = [lo + (hi - lo) // 3 for lo, hi in si.shard_slices(w.d_i)]
+    ridx = torch.as_tensor(rows, device=dev)
+    offs = [lo for lo, _ in si.shard_slices(w.d_i)]
+    shard_of = lambda u: max(i for i, o in enumerate(offs) if o <= u)
+    timed = {"rows": rows, "units": units,
+             "Y": Y.index_select(0, ridx).double().cpu().numpy(),
+             "dX": dX.index_select(0, ridx).double().cpu().numpy(),
+             "dW1": torch.stack([dW1[shard_of(u)][:, u - offs[shard_of(u)]] for u in units]).double().cpu().numpy(),
+             "dW2": torch.stack([dW2[shard_of(u)][u - offs[shard_of(u)], :] for u in units]).double().cpu().numpy()}
+
     # ---- end to end through the public API, host buffers (pinned), copies timed
     e2e = run_e2e(args, w, tp, mlp, inp, dev, stream, ws)
 
     peaks, peak_src = load_peaks()
+    pk = peak_regime(peaks, peak_src, elapsed_ms, clocks)
     pf = phase_flops(w)
+    pb = phase_bytes(w)
     if args.recompute:
         pf = {"fwd_column": pf["fwd_column"], "fwd_row": pf["fwd_row"], "bwd_none": 0,
               "bwd_recompute": pf["bwd_dgrad"] + pf["bwd_fsum"]}
-    achieved = pf[dom] / (per_phase[dom] / 1e3) / 1e12
-    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": achieved / peak_sus,
-                "traffic": None if (args.bias or args.recompute) else measured_traffic(dom, w.name),
-                "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); "
-                             f"frac of {peak_src} burst {peak_burst}: {achieved / peak_burst:.3f}"}
+        pb = {"fwd_column": pb["fwd_column"], "fwd_row": pb["fwd_row"], "bwd_none": 0,
+              "bwd_recompute": pb["bwd_dgrad"] + pb["bwd_fsum"]}
+    roofline = make_roofline(dom, pf, pb, per_phase, ms_per_step, pk, clocks,
+                             None if (args.bias or args.recompute) else measured_traffic(dom, w.name))
+    peak_sus, peak_burst = pk["sustained"], pk["burst"]
     if rank != 0:
         return 0
     cpu = None
+    parity = None
     if ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.oracle_tokens)
+        if not args.bias:
+            parity = check_timed_results(w, timed)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -522,6 +643,7 @@ def run_ours(args, w: si.Workload):
         "phase_ms_note": PHASE_NOTE,
         "roofline": roofline,
         "cpu_baseline": cpu,
+        "parity": parity,
         "e2e": e2e,
         "gpu_launches": (6 if args.bias else 4) * args.steps,
         "clocks": clocks,
@@ -734,13 +856,10 @@ def run_ours_attn(args, w: si.AttnWorkload):
                   "read back every step on copy streams overlapped with compute; weights resident"}
 
     peaks, peak_src = load_peaks()
-    achieved = pf[dom] / (per_phase[dom] / 1e3) / 1e12
-    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": achieved / peak_sus, "traffic": measured_traffic(dom, w.name),
-                "peak_note": f"{peak_src} sustained bf16 (kernel timed inside a long step); "
-                             f"frac of {peak_src} burst {peak_burst}: {achieved / peak_burst:.3f}"}
+    pk = peak_regime(peaks, peak_src, elapsed_ms, clocks)
+    roofline = make_roofline(dom, pf, attn_phase_bytes(w), per_phase, elapsed_ms / args.steps, pk, clocks,
+                             measured_traffic(dom, w.name))
+    peak_sus, peak_burst = pk["sustained"], pk["burst"]
     if rank != 0:
         return 0
     cpu = None
@@ -863,14 +982,12 @@ def run_ours_sp(args, w: si.Workload):
            "api": "tpmlp_forward_sp + tpmlp_backward_sp; X and dY stripes uploaded from pinned host memory and Y, "
                   "dX stripes read back every step on copy streams overlapped with compute; weights resident"}
     peaks, peak_src = load_peaks()
-    achieved = pflops[dom] / (per_phase[dom] / 1e3) / 1e12
-    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    roofline = {"bound": "tensor", "kernel": dom + " (two launches: dgrad + f-sum, or column + row)",
-                "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
-                "traffic": None,
-                "peak_note": f"{peak_src} sustained bf16; frac of {peak_src} burst {peak_burst}: "
-                             f"{achieved / peak_burst:.3f}"}
+    pk = peak_regime(peaks, peak_src, elapsed_ms, clocks)
+    pb = phase_bytes(w)
+    pbytes = {"forward_sp": pb["fwd_column"] + pb["fwd_row"], "backward_sp": pb["bwd_dgrad"] + pb["bwd_fsum"]}
+    roofline = make_roofline(dom, pflops, pbytes, per_phase, elapsed_ms / args.steps, pk, clocks, None)
+    roofline["kernel"] = dom + " (two launches: dgrad + f-sum, or column + row)"
+    peak_sus, peak_burst = pk["sustained"], pk["burst"]
     if rank != 0:
         return 0
     line = {
