@@ -105,9 +105,9 @@ TPMLP_API tpmlp_status tpmlp_plan_create(const tpmlp_desc* desc, tpmlp_plan** ou
 TPMLP_API void tpmlp_plan_destroy(tpmlp_plan* plan);
 
 /* Bytes of device workspace every call needs.  fp32 plans: a 256-byte block
- * holding the device status word.  bf16 plans: that block, then the flags and
- * fp32 partial accumulators of the stream-K tail (8 KB + 80 x 256 KB, about
- * 21 MB; see tpmlp_plan_set_stream_k).  The caller allocates it once,
+ * holding the device status word.  bf16 plans: that block, then the ticket
+ * counters and fp32 partial accumulators of the stream-K schedules (16 KB +
+ * 160 x 256 KB, about 42 MB; see tpmlp_plan_set_stream_k).  The caller allocates it once,
  * zero-filled, and passes it to every call of this plan; calls that share it
  * must be ordered on the device.                                             */
 TPMLP_API size_t tpmlp_workspace_size(const tpmlp_plan* plan);
@@ -336,30 +336,38 @@ TPMLP_API tpmlp_status tpmlp_attn_qkv_backward(const tpmlp_plan* plan, const voi
 TPMLP_API tpmlp_status tpmlp_plan_set_timeout(tpmlp_plan* plan, uint32_t timeout_ms);
 TPMLP_API tpmlp_status tpmlp_plan_set_stall_injection(tpmlp_plan* plan, int enable);
 
-/* Stream-K tail of the bf16 (tensor-core) launches.  A launch deals its 256 x
- * 256 tiles to the resident CTA pairs round robin; when the tile count is
- * not a multiple of the pairs, the last wave leaves pairs idle.  With the
- * tail, each of the last wave's R tiles is split along K into k parts run by
- * k pairs (k <= pairs / R).  Every part leaves its fp32 accumulator in the
- * workspace and takes a ticket; the part that takes the last ticket adds all
- * parts in K order and finishes the tile.  No pair waits for another, so
- * the tail makes no assumption about which pairs are resident or when they
- * run (other kernels may share the GPU).  The fixed order keeps results
- * deterministic for a given device, but they differ in rounding from the
- * unsplit K sum (within the fp32 accumulation bound) and depend on the pair
- * count, i.e. on the device's SM count.
- *   TPMLP_STREAM_K_AUTO (default): per launch, only when the full waves load
- *     every pair equally, the last wave's tiles have equal depth, and the
- *     split shortens a pair's work by at least 2 % and 16 K blocks of 128,
- *     after charging each extra part its read-back;
- *   TPMLP_STREAM_K_ALWAYS: on every launch whose last wave has at most
- *     pairs / 2 tiles, with as many parts as fit (tests);
+/* Stream-K schedules of the bf16 (tensor-core) launches.  A launch deals its
+ * 256 x 256 tiles to the resident CTA pairs round robin; when the tile count
+ * is not a multiple of the pairs, the last wave leaves pairs idle, and when
+ * a launch mixes long-K weight-gradient tiles (K = T) with short ones, the
+ * pairs that draw a long tile finish late.  A stream-K schedule cuts the K
+ * blocks of some tiles into ranges, one per pair: every part of a split tile
+ * leaves its fp32 accumulator in the workspace and takes a ticket; the part
+ * that takes the last ticket adds all parts in K order and finishes the
+ * tile.  No pair waits for another, so the schedule makes no assumption about
+ * which pairs are resident or when they run (other kernels may share the
+ * GPU).  The fixed order keeps results deterministic for a given device, but
+ * they differ in rounding from the unsplit K sum (within the fp32
+ * accumulation bound) and depend on the pair count, i.e. on the device's SM
+ * count.
+ *   TPMLP_STREAM_K_AUTO (default): per launch, the last partial wave of
+ *     equal-depth tiles is split, when that shortens a pair's work by at
+ *     least 2 % and 16 K blocks of 128 after charging each extra part its
+ *     read-back;
+ *   TPMLP_STREAM_K_ALWAYS: the last wave of every launch whose last wave has
+ *     at most pairs / 2 tiles, with as many parts as fit (tests);
+ *   TPMLP_STREAM_K_BALANCE: the launch's long-K weight-gradient tiles are
+ *     placed last and their K blocks spread over the pairs so that every pair
+ *     ends with the same estimated work (a launch without such tiles spreads
+ *     all of its tiles); a range of K blocks may then end inside one tile,
+ *     cover whole tiles and start inside another;
  *   TPMLP_STREAM_K_OFF: plain round robin.
  * tpmlp_forward_row_noalloc never uses it.  Not while another call uses the
  * plan.                                                                      */
 #define TPMLP_STREAM_K_OFF 0
 #define TPMLP_STREAM_K_AUTO 1
 #define TPMLP_STREAM_K_ALWAYS 2
+#define TPMLP_STREAM_K_BALANCE 3
 TPMLP_API tpmlp_status tpmlp_plan_set_stream_k(tpmlp_plan* plan, int mode);
 
 /* Synchronise the stream, read the workspace's status word and clear it.
@@ -376,7 +384,8 @@ TPMLP_API int tpmlp_last_cuda_error(void);
 TPMLP_API const char* tpmlp_last_error(void);
 /* ABI version: 100 * major + minor (1.01: optional biases; 1.02: attention
  * projections; 1.03: sequence-parallel layout; 1.04: stream-K tail, larger
- * bf16 workspace; 1.05: tpmlp_last_split_tiles, tpmlp_eval_activation). */
+ * bf16 workspace; 1.05: tpmlp_last_split_tiles, tpmlp_eval_activation, a
+ * 16 KB counter block in the bf16 workspace). */
 TPMLP_API int tpmlp_version(void);
 
 /* Kernel launches the last compute call (tpmlp_forward, tpmlp_backward, a
@@ -384,9 +393,9 @@ TPMLP_API int tpmlp_version(void);
  * before the first call).                                                    */
 TPMLP_API int tpmlp_last_launch_count(void);
 
-/* Diagnostics of the stream-K tail (see tpmlp_plan_set_stream_k), for tests
- * that must know which output tiles were computed in parts.  launch_kind
- * names a launch of the block:
+/* Diagnostics of the stream-K schedules (see tpmlp_plan_set_stream_k), for
+ * tests that must know which output tiles were computed in parts.
+ * launch_kind names a launch of the block:
  *   0 the column-parallel GEMM (tpmlp_forward_column), 1 the row-parallel
  *   GEMM with the g-sum (tpmlp_forward_row), 2 the dgrad launch
  *   (tpmlp_backward_dgrad), 3 the f-sum launch (tpmlp_backward_fsum),
@@ -395,12 +404,11 @@ TPMLP_API int tpmlp_last_launch_count(void);
  * Returns how many tiles the last launch of that kind made on this thread
  * split into parts (0 if none, or no such launch yet; -1 for an unknown
  * kind) and writes the first min(count, cap) of them to tiles (host memory,
- * may be NULL) as triples: the problem's index in its launch, the tile's
- * first output row and its first output column.  Problems are numbered in
- * the order each launch lists them: column launch, shard i's problem is i;
- * row launch, one problem (Y); dgrad launch, dW2_i (i = 0..t-1) then shard
- * i's dact at t + i (recompute: no dW2 problems); f-sum launch, dW1_i
- * (i = 0..t-1), SwiGLU dW3_i at t + i, then dX (recompute: dW2_i first).  */
+ * may be NULL) as quadruples: the problem's index in its launch, the tile's
+ * first output row, its first output column, and the device address of the
+ * problem's first output (Y, dX, the pre-activation, dA, dG, dW1, dW2 ... as
+ * the caller passed it; 0 for a token-striped output), which identifies the
+ * tensor the tile belongs to.                                                */
 TPMLP_API int tpmlp_last_split_tiles(int launch_kind, int64_t* tiles, int cap);
 
 /* The activation forms of the kernels' epilogues, evaluated on plain fp32

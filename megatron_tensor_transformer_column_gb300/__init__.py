@@ -25,7 +25,7 @@ from . import _build
 __all__ = [
     "TpmlpError", "load", "Plan", "tpmlp_plan_create", "tpmlp_plan_destroy", "tpmlp_workspace_size",
     "tpmlp_plan_set_timeout", "tpmlp_plan_set_stall_injection", "tpmlp_plan_set_stream_k",
-    "STREAM_K_OFF", "STREAM_K_AUTO", "STREAM_K_ALWAYS",
+    "STREAM_K_OFF", "STREAM_K_AUTO", "STREAM_K_ALWAYS", "STREAM_K_BALANCE",
     "tpmlp_forward", "tpmlp_backward", "tpmlp_backward_recompute", "tpmlp_forward_column", "tpmlp_forward_row", "tpmlp_forward_row_noalloc", "tpmlp_backward_dgrad",
     "tpmlp_backward_fsum", "tpmlp_check", "tpmlp_status_string", "tpmlp_last_cuda_error", "tpmlp_version",
     "tpmlp_last_launch_count", "tpmlp_last_error", "ShardedMLP", "TPMLPFunction", "EXPORTED_SYMBOLS",
@@ -323,7 +323,7 @@ def tpmlp_plan_set_stall_injection(plan: Plan, enable):
     _ok(load().tpmlp_plan_set_stall_injection(plan.handle, mode), "tpmlp_plan_set_stall_injection")
 
 
-STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_ALWAYS = 0, 1, 2
+STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_ALWAYS, STREAM_K_BALANCE = 0, 1, 2, 3
 
 
 def tpmlp_plan_set_stream_k(plan: Plan, mode: int):
@@ -417,15 +417,16 @@ def tpmlp_eval_activation(form: str, x, y=None, dh=None, out0=None, out1=None, o
 
 
 def tpmlp_last_split_tiles(launch_kind: int) -> List[tuple]:
-    """(problem, first row, first column) of every tile the stream-K tail split in
-    the last launch of this kind on the calling thread."""
+    """(problem, first row, first column, address of the problem's first output)
+    of every tile the stream-K schedule split in the last launch of this kind on
+    the calling thread."""
     lib = load()
     n = int(lib.tpmlp_last_split_tiles(int(launch_kind), None, 0))
     if n < 0:
         raise ValueError(f"unknown launch kind {launch_kind}")
-    buf = (ctypes.c_int64 * max(1, 3 * n))()
+    buf = (ctypes.c_int64 * max(1, 4 * n))()
     lib.tpmlp_last_split_tiles(int(launch_kind), buf, n)
-    return [(int(buf[3 * i]), int(buf[3 * i + 1]), int(buf[3 * i + 2])) for i in range(n)]
+    return [tuple(int(buf[4 * i + k]) for k in range(4)) for i in range(n)]
 
 
 # ---------------------------------------------------------------- convenience layer

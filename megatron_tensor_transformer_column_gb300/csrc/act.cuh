@@ -34,50 +34,14 @@ __device__ __forceinline__ void swiglu_grads(float dh, float g, float u, float& 
   dg = dh * u * (s + g * s * (1.0f - s));
 }
 
-// Faster forms for the bf16 tensor-core epilogues, whose outputs are rounded
-// to bf16 (relative step 2^-8): Phi from the rational approximation of erf
-// by Hastings given as formula 7.1.26 in Abramowitz & Stegun (|error of erf|
-// <= 1.5e-7), with exp(-a^2/2) shared between Phi and the density in GeLU'.
-struct NormTerms {
-  float cdf;  // Phi(a)
-  float e;    // exp(-a^2 / 2)
-};
-
-__device__ __forceinline__ NormTerms norm_terms_fast(float a) {
-  constexpr float p = 0.3275911f * kInvSqrt2;  // t = 1 / (1 + p |a| / sqrt 2)
-  constexpr float a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f, a4 = -1.453152027f,
-                  a5 = 1.061405429f;
-  const float t = __fdividef(1.0f, fmaf(p, fabsf(a), 1.0f));
-  const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1);
-  const float e = __expf(-0.5f * a * a);
-  const float q = 0.5f * poly * e;  // Phi(-|a|)
-  NormTerms r;
-  r.cdf = a >= 0.0f ? 1.0f - q : q;
-  r.e = e;
-  return r;
-}
-
-__device__ __forceinline__ float gelu_fast(float a) { return a * norm_terms_fast(a).cdf; }
-
-__device__ __forceinline__ float gelu_grad_fast(float a) {
-  const NormTerms n = norm_terms_fast(a);
-  return fmaf(a * kInvSqrt2Pi, n.e, n.cdf);
-}
-
-__device__ __forceinline__ float sigmoid_fast(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
-
-__device__ __forceinline__ float swish_fast(float g) { return g * sigmoid_fast(g); }
-
-__device__ __forceinline__ void swiglu_grads_fast(float dh, float g, float u, float& dg, float& du) {
-  const float s = sigmoid_fast(g);
-  du = dh * (g * s);
-  dg = dh * u * (s + g * s * (1.0f - s));
-}
-
-// ---- packed forms for the tensor-core epilogue: two elements per fp32x2
-// instruction (fma/mul/add.rn.f32x2).  Same approximations and constants as
-// the scalar fast forms above, regrouped so that every step but the two
-// special-function calls (reciprocal, exponential) acts on a pair:
+// ---- fast packed forms for the bf16 tensor-core epilogues, whose outputs
+// are rounded to bf16 (relative step 2^-8): Phi from the rational
+// approximation of erf by Hastings given as formula 7.1.26 in Abramowitz &
+// Stegun (|error of erf| <= 1.5e-7), with exp(-a^2/2) shared between Phi and
+// the density in GeLU', and the sigmoid from the fast exponential and
+// reciprocal.  Two elements per fp32x2 instruction (fma/mul/add.rn.f32x2):
+// every step but the two special-function calls (reciprocal, exponential)
+// acts on a pair:
 //   q = Phi(-|a|) = 0.5 * poly(t) * exp(-a^2/2), t = 1 / (1 + p |a|);
 //   GeLU(a) = a Phi(a) = max(a, 0) - |a| q;
 //   Phi(a) = 0.5 + copysign(0.5 - q, a),  GeLU'(a) = Phi(a) + a phi(a).
@@ -133,10 +97,11 @@ __device__ __forceinline__ void norm_q(uint64_t a, uint64_t& nx, uint64_t& q, ui
   q = mul2(poly, e);
 }
 
-// h = GeLU(a) for v[0..31] in place.
-__device__ __forceinline__ void gelu_x32(float (&v)[32]) {
+// h = GeLU(a) for v[0..N-1] in place (N even).
+template <int N>
+__device__ __forceinline__ void gelu_xn(float (&v)[N]) {
 #pragma unroll
-  for (int j = 0; j < 32; j += 2) {
+  for (int j = 0; j < N; j += 2) {
     const uint64_t a = pk(v[j], v[j + 1]);
     uint64_t nx, q, e;
     norm_q(a, nx, q, e);
@@ -146,11 +111,11 @@ __device__ __forceinline__ void gelu_x32(float (&v)[32]) {
 }
 
 // dA = dH * GeLU'(A): acc holds dH, a holds A on entry and dA on exit; with
-// h non-null, h receives GeLU(A) as well.
-template <bool kWithH>
-__device__ __forceinline__ void gelu_bwd_x32(const float (&acc)[32], float (&a)[32], float (&h)[32]) {
+// kWithH, h receives GeLU(A) as well.
+template <bool kWithH, int N>
+__device__ __forceinline__ void gelu_bwd_xn(const float (&acc)[N], float (&a)[N], float (&h)[N]) {
 #pragma unroll
-  for (int j = 0; j < 32; j += 2) {
+  for (int j = 0; j < N; j += 2) {
     const uint64_t av = pk(a[j], a[j + 1]);
     uint64_t nx, q, e;
     norm_q(av, nx, q, e);
@@ -174,10 +139,11 @@ __device__ __forceinline__ uint64_t sigmoid2(float g0, float g1) {
   return pk(__fdividef(1.0f, d0), __fdividef(1.0f, d1));
 }
 
-// h = u * Swish(g) for 32 pairs of (g, u).
-__device__ __forceinline__ void swiglu_x32(const float (&g)[32], const float (&u)[32], float (&h)[32]) {
+// h = u * Swish(g) for N pairs of (g, u).
+template <int N>
+__device__ __forceinline__ void swiglu_xn(const float (&g)[N], const float (&u)[N], float (&h)[N]) {
 #pragma unroll
-  for (int j = 0; j < 32; j += 2) {
+  for (int j = 0; j < N; j += 2) {
     const uint64_t gv = pk(g[j], g[j + 1]);
     const uint64_t s = sigmoid2(g[j], g[j + 1]);
     upk(mul2(pk(u[j], u[j + 1]), mul2(gv, s)), h[j], h[j + 1]);
@@ -186,11 +152,10 @@ __device__ __forceinline__ void swiglu_x32(const float (&g)[32], const float (&u
 
 // dG = dH * U * Swish'(G), dU = dH * Swish(G); g, u hold G, U on entry and
 // dG, dU on exit; with kWithH, h receives U * Swish(G).
-template <bool kWithH>
-__device__ __forceinline__ void swiglu_bwd_x32(const float (&acc)[32], float (&g)[32], float (&u)[32],
-                                               float (&h)[32]) {
+template <bool kWithH, int N>
+__device__ __forceinline__ void swiglu_bwd_xn(const float (&acc)[N], float (&g)[N], float (&u)[N], float (&h)[N]) {
 #pragma unroll
-  for (int j = 0; j < 32; j += 2) {
+  for (int j = 0; j < N; j += 2) {
     const uint64_t gv = pk(g[j], g[j + 1]), uv = pk(u[j], u[j + 1]), dh = pk(acc[j], acc[j + 1]);
     const uint64_t s = sigmoid2(g[j], g[j + 1]);
     const uint64_t gs = mul2(gv, s);                                      // Swish(G)

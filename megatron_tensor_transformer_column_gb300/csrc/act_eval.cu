@@ -11,8 +11,9 @@
 namespace tpmlp {
 namespace {
 
-// Each thread evaluates 32 consecutive elements through the same x32 entry
-// points the tensor-core epilogues call (elements past n are padded with
+// Each thread evaluates 32 consecutive elements through the same entry
+// points the tensor-core epilogues call (their arithmetic is element-wise, so
+// the chunk width does not change a result) (elements past n are padded with
 // zeros and not stored); the fp32 forms are evaluated per element, as the
 // fp32 path's epilogue does.
 __global__ void __launch_bounds__(128) tpmlp_act_eval(int fn, const float* __restrict__ x,
@@ -33,30 +34,30 @@ __global__ void __launch_bounds__(128) tpmlp_act_eval(int fn, const float* __res
   }
   switch (fn) {
     case TPMLP_ACT_EVAL_GELU:  // o0 = GeLU(x)
-      act::x2::gelu_x32(a);
+      act::x2::gelu_xn(a);
       for (int j = 0; j < cnt; ++j) o0[base + j] = a[j];
       break;
     case TPMLP_ACT_EVAL_GELU_BWD:  // o0 = dh * GeLU'(x)
-      act::x2::gelu_bwd_x32<false>(c, a, h);
+      act::x2::gelu_bwd_xn<false>(c, a, h);
       for (int j = 0; j < cnt; ++j) o0[base + j] = a[j];
       break;
     case TPMLP_ACT_EVAL_GELU_BWD_H:  // o0 = dh * GeLU'(x), o1 = GeLU(x)
-      act::x2::gelu_bwd_x32<true>(c, a, h);
+      act::x2::gelu_bwd_xn<true>(c, a, h);
       for (int j = 0; j < cnt; ++j) {
         o0[base + j] = a[j];
         o1[base + j] = h[j];
       }
       break;
     case TPMLP_ACT_EVAL_SWIGLU:  // o0 = y * Swish(x)
-      act::x2::swiglu_x32(a, b, h);
+      act::x2::swiglu_xn(a, b, h);
       for (int j = 0; j < cnt; ++j) o0[base + j] = h[j];
       break;
     case TPMLP_ACT_EVAL_SWIGLU_BWD:  // o0 = dG, o1 = dU
     case TPMLP_ACT_EVAL_SWIGLU_BWD_H:  // and o2 = y * Swish(x)
       if (fn == TPMLP_ACT_EVAL_SWIGLU_BWD_H)
-        act::x2::swiglu_bwd_x32<true>(c, a, b, h);
+        act::x2::swiglu_bwd_xn<true>(c, a, b, h);
       else
-        act::x2::swiglu_bwd_x32<false>(c, a, b, h);
+        act::x2::swiglu_bwd_xn<false>(c, a, b, h);
       for (int j = 0; j < cnt; ++j) {
         o0[base + j] = a[j];
         o1[base + j] = b[j];

@@ -13,10 +13,11 @@
 //   * warp 1 (one lane, even CTA): allocates 512 TMEM columns in both CTAs,
 //     issues the MMAs into one of two 256-column accumulators and multicasts
 //     its commits (stage free, accumulator ready) to both CTAs;
-//   * warps 2..9: drain the other accumulator through tcgen05.ld, apply the
-//     epilogue (store, GeLU / SwiGLU forward, GeLU' / SwiGLU' backward) and
-//     write bf16 rows to HBM; the two accumulators let the epilogue of one
-//     tile run under the main loop of the next.
+//   * warps 2..9 (or 2..17, see kEpiWarpsOf): drain the other accumulator
+//     through tcgen05.ld, apply the epilogue (store, GeLU / SwiGLU forward,
+//     GeLU' / SwiGLU' backward) and write bf16 rows to HBM; the two
+//     accumulators let the epilogue of one tile run under the main loop of
+//     the next.
 // The MMAs of a stage are issued as straight-line code (issue_stage): on
 // GB300 a branch between two tcgen05.mma instructions cost about a third of
 // the tensor throughput.
@@ -266,19 +267,27 @@ __device__ __forceinline__ void cursor_issue(const GemmParams& p, const Cursor<k
 }
 
 // ------------------------------------------------------------------ stream-K parts
-// Range r's workspace slot holds, per epilogue warp wi of the pair
-// (rank * 8 + warp - 2), the four 32 x 32 fp32 accumulator chunks that warp
+// A range's first split item leaves its partial in slot 2r, its last one in
+// slot 2r + 1 (a range holds at most those two parts: the items between them
+// are whole tiles).  A slot holds, per epilogue warp wi of the pair
+// (rank * kEW + warp - 2), the four 32 x N fp32 accumulator chunks that warp
 // drains (the same TMEM lanes and columns in every pair), laid out so that
 // each 16-byte store / load of a warp covers 512 contiguous bytes.  The
 // ticket counter of a split tile, one per epilogue warp position, is the
-// flag word of the tile's first range.
+// counter word of the range holding the tile's K block 0.
 __device__ __forceinline__ uint32_t* sk_counter(const GemmParams& p, int q0, int wi) {
   return reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(p.status) + kSkFlagsOffset) + q0 * kSkWarpsPerPair + wi;
 }
 
-__device__ __forceinline__ char* sk_chunk(const GemmParams& p, int r, int wi, int cslot) {
-  return reinterpret_cast<char*>(p.status) + kSkSlotsOffset + static_cast<size_t>(r) * kSkSlotBytes +
-         static_cast<size_t>(wi * 4 + cslot) * (32 * 32 * sizeof(float));
+template <int N>
+__device__ __forceinline__ char* sk_chunk(const GemmParams& p, int slot, int wi, int cslot) {
+  return reinterpret_cast<char*>(p.status) + kSkSlotsOffset + static_cast<size_t>(slot) * kSkSlotBytes +
+         static_cast<size_t>(wi * 4 + cslot) * (32 * N * sizeof(float));
+}
+
+// The slot of range q's part of tile j: its first item starts in j.
+__device__ __forceinline__ int sk_slot(const GemmParams& p, int q, int j) {
+  return 2 * q + (p.sk.start_tile[q] == j ? 0 : 1);
 }
 
 __device__ __forceinline__ bool sk_range_empty(const GemmParams& p, int r) {
@@ -286,35 +295,47 @@ __device__ __forceinline__ bool sk_range_empty(const GemmParams& p, int r) {
 }
 
 // TMEM column of this warp's chunk cslot (0..3) of a tile -- the chunks the
-// epilogue reads, in its order -- or -1 past the tile's valid columns.
-// SwiGLU forward: chunk 2c is the gate, 2c + 1 the up projection of output
-// columns 64 half + 32 c ..; otherwise chunk c is columns 128 half + 32 c ...
-__device__ __forceinline__ int sk_chunk_col(const Prob& P, const TileInfo& ti, int half, int cslot) {
+// epilogue reads, in its order -- or -1 past the tile's valid columns.  The
+// warp covers columns part * 256 / parts .. of the accumulator (parts = the
+// warps per lane quarter).  SwiGLU forward: the warp's output columns are
+// part * 128 / parts ..; chunk 2c is the gate, 2c + 1 the up projection of
+// output columns oc = part * 128 / parts + c N .. (see swiglu_cols).
+template <int N>
+__device__ __forceinline__ void swiglu_cols(bool merged, int oc, uint32_t& g_col, uint32_t& u_col) {
+  // merged: CTA-half h = oc / 64 of B holds gate columns at 128 h + oc % 64
+  // and the matching up columns 64 further; split: gate at oc, up at 128 + oc
+  const int h = oc >> 6, w = oc & 63;
+  g_col = merged ? static_cast<uint32_t>(128 * h + w) : static_cast<uint32_t>(oc);
+  u_col = merged ? g_col + 64u : 128u + static_cast<uint32_t>(oc);
+}
+
+template <int N>
+__device__ __forceinline__ int sk_chunk_col(const Prob& P, const TileInfo& ti, int part, int parts, int cslot) {
   if (P.epi == EPI_SWIGLU_FWD) {
-    const int c = cslot >> 1;
-    const int col = half * 64 + c * 32;
-    if (col >= ti.valid_n) return -1;
-    const bool merged = swiglu_merged(ti, P);
-    const int g_col = merged ? half * 128 + c * 32 : col;
-    return (cslot & 1) ? (merged ? g_col + 64 : 128 + col) : g_col;
+    const int oc = part * (128 / parts) + (cslot >> 1) * N;
+    if (oc >= ti.valid_n) return -1;
+    uint32_t g, u;
+    swiglu_cols<N>(swiglu_merged(ti, P), oc, g, u);
+    return static_cast<int>((cslot & 1) ? u : g);
   }
-  const int col = half * 128 + cslot * 32;
+  const int col = part * (256 / parts) + cslot * N;
   return col < ti.valid_n ? col : -1;
 }
 
-// This warp's chunks of a part, raw fp32, to its range's slot.
-__device__ __forceinline__ void sk_part_store(const GemmParams& p, const Prob& P, const Item& it, int r,
-                                              uint32_t tacc, int half, int wi, int lane) {
+// This warp's chunks of a part, raw fp32, to its slot.
+template <int N>
+__device__ __forceinline__ void sk_part_store(const GemmParams& p, const Prob& P, const Item& it, int slot,
+                                              uint32_t tacc, int part, int parts, int wi, int lane) {
 #pragma unroll 1
   for (int cs = 0; cs < 4; ++cs) {
-    const int tc = sk_chunk_col(P, it.ti, half, cs);
+    const int tc = sk_chunk_col<N>(P, it.ti, part, parts, cs);
     if (tc < 0) continue;
-    uint32_t v[32];
-    ptx::tmem_ld_32x32b_x32(tacc + static_cast<uint32_t>(tc), v);
+    uint32_t v[N];
+    ptx::tmem_ld_32x32b(tacc + static_cast<uint32_t>(tc), v);
     ptx::tmem_wait_ld();
-    char* dst = sk_chunk(p, r, wi, cs) + lane * 16;
+    char* dst = sk_chunk<N>(p, slot, wi, cs) + lane * 16;
 #pragma unroll
-    for (int j4 = 0; j4 < 8; ++j4)
+    for (int j4 = 0; j4 < N / 4; ++j4)
       ptx::st_cg_v4(dst + j4 * 512, v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
   }
 }
@@ -351,22 +372,14 @@ __device__ __forceinline__ bool sk_ticket(const GemmParams& p, int q0, int npart
   return true;
 }
 
-// Add one part's chunk to v: from this pair's TMEM accumulator, or from
-// range q's slot (eight 16-byte loads in flight).
-__device__ __forceinline__ void sk_add_tmem(uint32_t taddr, uint32_t (&v)[32]) {
-  uint32_t t[32];
-  ptx::tmem_ld_32x32b_x32(taddr, t);
-  ptx::tmem_wait_ld();
+// Add range q's chunk (N / 4 16-byte loads in flight per lane) to v.
+template <int N>
+__device__ __forceinline__ void sk_add_slot(const char* src, uint32_t (&v)[N]) {
+  float4 f[N / 4];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(t[j]));
-}
-
-__device__ __forceinline__ void sk_add_slot(const char* src, uint32_t (&v)[32]) {
-  float4 f[8];
+  for (int j4 = 0; j4 < N / 4; ++j4) f[j4] = ptx::ld_cg_v4f(src + j4 * 512);
 #pragma unroll
-  for (int j4 = 0; j4 < 8; ++j4) f[j4] = ptx::ld_cg_v4f(src + j4 * 512);
-#pragma unroll
-  for (int j4 = 0; j4 < 8; ++j4) {
+  for (int j4 = 0; j4 < N / 4; ++j4) {
     v[4 * j4 + 0] = __float_as_uint(__uint_as_float(v[4 * j4 + 0]) + f[j4].x);
     v[4 * j4 + 1] = __float_as_uint(__uint_as_float(v[4 * j4 + 1]) + f[j4].y);
     v[4 * j4 + 2] = __float_as_uint(__uint_as_float(v[4 * j4 + 2]) + f[j4].z);
@@ -374,26 +387,37 @@ __device__ __forceinline__ void sk_add_slot(const char* src, uint32_t (&v)[32]) 
   }
 }
 
+// Add this pair's own chunk, from TMEM, to v.
+template <int N>
+__device__ __forceinline__ void sk_add_tmem(uint32_t taddr, uint32_t (&v)[N]) {
+  uint32_t t[N];
+  ptx::tmem_ld_32x32b(taddr, t);
+  ptx::tmem_wait_ld();
+#pragma unroll
+  for (int j = 0; j < N; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(t[j]));
+}
+
 // The last part: the sum of all parts, added in range order (its own from
 // TMEM, the others from their slots), written back into its accumulator, on
-// which the tile's normal epilogue then runs.  The parts of a tile are the
-// non-empty ranges from q0 (the tile's first non-empty one) on that start in
-// it: the host cuts one part per range.
+// which the tile's normal epilogue then runs.  The parts of tile j are the
+// non-empty ranges from q0 (the one holding its K block 0) on that start in
+// j.
+template <int N>
 __device__ __forceinline__ void sk_fold(const GemmParams& p, const Prob& P, const Item& it, int r, int q0,
-                                        uint32_t tacc, int half, int wi, int lane) {
+                                        uint32_t tacc, int part, int parts, int wi, int lane) {
 #pragma unroll 1
   for (int cs = 0; cs < 4; ++cs) {
-    const int tc = sk_chunk_col(P, it.ti, half, cs);
+    const int tc = sk_chunk_col<N>(P, it.ti, part, parts, cs);
     if (tc < 0) continue;
     const uint32_t taddr = tacc + static_cast<uint32_t>(tc);
-    uint32_t v[32];
+    uint32_t v[N];
     if (q0 == r) {
-      ptx::tmem_ld_32x32b_x32(taddr, v);
+      ptx::tmem_ld_32x32b(taddr, v);
       ptx::tmem_wait_ld();
     } else {
-      const char* src = sk_chunk(p, q0, wi, cs) + lane * 16;
+      const char* src = sk_chunk<N>(p, sk_slot(p, q0, it.tile), wi, cs) + lane * 16;
 #pragma unroll
-      for (int j4 = 0; j4 < 8; ++j4) {
+      for (int j4 = 0; j4 < N / 4; ++j4) {
         const float4 f = ptx::ld_cg_v4f(src + j4 * 512);
         v[4 * j4 + 0] = __float_as_uint(f.x);
         v[4 * j4 + 1] = __float_as_uint(f.y);
@@ -405,18 +429,20 @@ __device__ __forceinline__ void sk_fold(const GemmParams& p, const Prob& P, cons
     for (int q = q0 + 1; q < p.sk.pairs && p.sk.start_tile[q] == it.tile; ++q) {
       if (sk_range_empty(p, q)) continue;
       if (q == r)
-        sk_add_tmem(taddr, v);
+        sk_add_tmem<N>(taddr, v);
       else
-        sk_add_slot(sk_chunk(p, q, wi, cs) + lane * 16, v);
+        sk_add_slot<N>(sk_chunk<N>(p, sk_slot(p, q, it.tile), wi, cs) + lane * 16, v);
     }
-    ptx::tmem_st_32x32b_x32(taddr, v);
+    ptx::tmem_st_32x32b(taddr, v);
   }
   ptx::tmem_wait_st();
 }
 
 // ------------------------------------------------------------------ the kernel body
-template <bool kSK>
+template <bool kSK, int kEW>
 __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_raw) {
+  constexpr int N = chunk_cols(kEW);  // accumulator columns per epilogue chunk
+  constexpr int kParts = kEW / 4;      // epilogue warps per TMEM lane quarter
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kEpiBytes);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
@@ -444,7 +470,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
     }
     for (int a = 0; a < kNumAcc; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
-      ptx::mbar_init(tempty_bar(a), 2 * kNumEpiWarps);
+      ptx::mbar_init(tempty_bar(a), 2 * kEW);
     }
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -595,10 +621,11 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;              // TMEM lane quarter this warp may read
-    const int half = (warp - 2) >> 2;    // which half of the tile's columns
-    EpiStore es{smem_base + static_cast<uint32_t>(kStages * kStageBytes + (warp - 2) * 2 * kEpiBlockBytes), 0u, 0, 0,
-                0};
-    const int wi = static_cast<int>(rank) * kNumEpiWarps + (warp - 2);  // stream-K slot position of this warp
+    const int part = (warp - 2) >> 2;    // which of the kParts column ranges of a tile
+    constexpr int kCols = 256 / kParts;  // accumulator columns per warp (4 chunks of N)
+    EpiStore es{smem_base + static_cast<uint32_t>(kStages * kStageBytes + (warp - 2) * 2 * epi_block_bytes<N>()), 0u,
+                0, 0, 0};
+    const int wi = static_cast<int>(rank) * kEW + (warp - 2);  // stream-K slot position of this warp
     int acc = 0;
     uint32_t acc_phase = 0;
     Sched<kSK> s;
@@ -619,8 +646,8 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
       if (row_ok && (P.epi == EPI_GELU_BWD || P.epi == EPI_SWIGLU_BWD)) {
         // Pull this thread's row of the saved pre-activation(s) into L2
         // while the accumulator is still being computed.
-        const int c0 = half * 128;
-        const int cn = min(128, ti.valid_n - c0);
+        const int c0 = part * kCols;
+        const int cn = min(kCols, ti.valid_n - c0);
         if (cn > 0) {
           const int64_t off = grow * P.ldo + ti.n0 + c0;
           const __nv_bfloat16* a0 = static_cast<const __nv_bfloat16*>(P.aux0) + off;
@@ -642,50 +669,49 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
         // them all and runs the epilogue.  (Test hook, stall injection 2:
         // every part but the tile's first runs late, so that another part
         // than the first finishes the tile.)
-        if (vm > 0) sk_part_store(p, P, it, s.r, tacc, half, wi, lane);
-        const int q0 = p.sk.first_range[s.r];
+        const bool head = p.sk.start_tile[s.r] == it.tile;  // the range's first item, else its last
+        if (vm > 0) sk_part_store<N>(p, P, it, 2 * s.r + (head ? 0 : 1), tacc, part, kParts, wi, lane);
+        const int q0 = head ? p.sk.head_q0[s.r] : p.sk.tail_q0[s.r];
         if (p.stall_injection == 2 && s.r != q0) spin_ns(20ull * 1000 * 1000);
-        finish = sk_ticket(p, q0, p.sk.num_parts[s.r], wi, lane);
-        if (finish && vm > 0) sk_fold(p, P, it, s.r, q0, tacc, half, wi, lane);
+        finish = sk_ticket(p, q0, head ? p.sk.head_n[s.r] : p.sk.tail_n[s.r], wi, lane);
+        if (finish && vm > 0) sk_fold<N>(p, P, it, s.r, q0, tacc, part, kParts, wi, lane);
       }
       if (finish && vm > 0) {
         if (P.epi == EPI_SWIGLU_FWD) {
           const bool merged = swiglu_merged(ti, P);
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
-            const int col = half * 64 + c * 32;
-            if (col >= ti.valid_n) break;
-            // output columns 64 half + 32 c ..: merged, gate at accumulator
-            // column 128 half + 32 c, up 64 further; split, gate at col, up at 128 + col
-            const uint32_t g_col = merged ? static_cast<uint32_t>(half * 128 + c * 32) : static_cast<uint32_t>(col);
-            const uint32_t u_col = merged ? g_col + 64u : 128u + static_cast<uint32_t>(col);
-            uint32_t rg[32], ru[32];
-            ptx::tmem_ld_32x32b_x32(tacc + g_col, rg);
-            ptx::tmem_ld_32x32b_x32(tacc + u_col, ru);
+            const int oc = part * (128 / kParts) + c * N;  // output columns oc .. oc + N - 1 of the tile
+            if (oc >= ti.valid_n) break;
+            uint32_t g_col, u_col;
+            swiglu_cols<N>(merged, oc, g_col, u_col);
+            uint32_t rg[N], ru[N];
+            ptx::tmem_ld_32x32b(tacc + g_col, rg);
+            ptx::tmem_ld_32x32b(tacc + u_col, ru);
             ptx::tmem_wait_ld();
-            const int nvalid = min(32, ti.valid_n - col);
-            float g[32], u[32], h[32];
+            const int nvalid = min(N, ti.valid_n - oc);
+            float g[N], u[N], h[N];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < N; ++j) {
               g[j] = __uint_as_float(rg[j]);
               u[j] = __uint_as_float(ru[j]);
             }
-            add_bias32(P.aux0, ti.n0 + col, nvalid, g);
-            add_bias32(P.aux1, ti.n0 + col, nvalid, u);
-            act::x2::swiglu_x32(g, u, h);
-            store_block(es, p, P.out_map[0], ti.n0 + col, wrow, g, lane);
-            store_block(es, p, P.out_map[1], ti.n0 + col, wrow, u, lane);
-            store_block(es, p, P.out_map[2], ti.n0 + col, wrow, h, lane);
+            add_bias<N>(P.aux0, ti.n0 + oc, nvalid, g);
+            add_bias<N>(P.aux1, ti.n0 + oc, nvalid, u);
+            act::x2::swiglu_xn(g, u, h);
+            store_block<N>(es, p, P, 0, ti.n0 + oc, wrow, nvalid, g, lane);
+            store_block<N>(es, p, P, 1, ti.n0 + oc, wrow, nvalid, u, lane);
+            store_block<N>(es, p, P, 2, ti.n0 + oc, wrow, nvalid, h, lane);
           }
         } else {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
-            const int col = half * 128 + c * 32;
+            const int col = part * kCols + c * N;
             if (col >= ti.valid_n) break;
-            uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(tacc + col, r);
+            uint32_t r[N];
+            ptx::tmem_ld_32x32b(tacc + col, r);
             ptx::tmem_wait_ld();
-            epilogue_chunk(p, P, es, grow, row_ok, ti.n0 + col, wrow, min(32, ti.valid_n - col), r, lane);
+            epilogue_chunk<N>(p, P, es, grow, row_ok, ti.n0 + col, wrow, min(N, ti.valid_n - col), r, lane);
           }
         }
       }
@@ -713,35 +739,61 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
 }  // namespace
 
 // Two kernel symbols per launch kind (same body): the data-parallel schedule
-// and, with the suffix _sk, the one with a stream-K tail.
-#define TPMLP_TC_KERNELS(name)                                                                    \
-  __global__ void __launch_bounds__(kThreads, 1) name(const __grid_constant__ GemmParams p) {     \
-    extern __shared__ __align__(1024) uint8_t smem_raw[];                                         \
-    tc_gemm_body<false>(p, smem_raw);                                                             \
-  }                                                                                               \
-  __global__ void __launch_bounds__(kThreads, 1) name##_sk(const __grid_constant__ GemmParams p) { \
-    extern __shared__ __align__(1024) uint8_t smem_raw[];                                         \
-    tc_gemm_body<true>(p, smem_raw);                                                              \
+// and, with the suffix _sk, the one with a stream-K tail; EW is the number
+// of epilogue warps (kernel_for).
+#define TPMLP_TC_KERNELS(name, EW)                                                                       \
+  __global__ void __launch_bounds__(threads_for(EW), 1) name(const __grid_constant__ GemmParams p) {     \
+    extern __shared__ __align__(1024) uint8_t smem_raw[];                                                \
+    tc_gemm_body<false, EW>(p, smem_raw);                                                                \
+  }                                                                                                      \
+  __global__ void __launch_bounds__(threads_for(EW), 1) name##_sk(const __grid_constant__ GemmParams p) { \
+    extern __shared__ __align__(1024) uint8_t smem_raw[];                                                \
+    tc_gemm_body<true, EW>(p, smem_raw);                                                                 \
   }
 
-TPMLP_TC_KERNELS(tpmlp_fwd_column_gemm_act)
-TPMLP_TC_KERNELS(tpmlp_fwd_row_gemm_gsum)
-TPMLP_TC_KERNELS(tpmlp_bwd_dgrad_act_wgrad2)
-TPMLP_TC_KERNELS(tpmlp_bwd_dx_fsum_wgrad1)
-TPMLP_TC_KERNELS(tpmlp_attn_qkv_proj)
-TPMLP_TC_KERNELS(tpmlp_attn_out_proj_gsum)
-TPMLP_TC_KERNELS(tpmlp_attn_out_proj_bwd)
-TPMLP_TC_KERNELS(tpmlp_attn_qkv_bwd_dx_fsum)
+// Launch kinds whose epilogues carry the activation (the column GEMM, the
+// dgrad GEMM) also exist with 16 epilogue warps (suffix _w16).  The host
+// takes them where the tiles' K is short (tc_epi_warps_for): there the
+// epilogue of a tile lasts longer than its main loop and is bound by each
+// warp's chain of TMEM load, arithmetic and store, which more warps overlap.
+// With longer K the epilogue hides under the next tile's main loop and the
+// extra warps only compete with the producer and the MMA issuer for issue
+// slots (measured on GB300: C2's column and dgrad launches -7 % and -5 % with
+// 16 warps; C3 to C5's +1 to +3 %).
+TPMLP_TC_KERNELS(tpmlp_fwd_column_gemm_act, 8)
+TPMLP_TC_KERNELS(tpmlp_fwd_column_gemm_act_w16, 16)
+TPMLP_TC_KERNELS(tpmlp_fwd_row_gemm_gsum, 8)
+TPMLP_TC_KERNELS(tpmlp_bwd_dgrad_act_wgrad2, 8)
+TPMLP_TC_KERNELS(tpmlp_bwd_dgrad_act_wgrad2_w16, 16)
+TPMLP_TC_KERNELS(tpmlp_bwd_dx_fsum_wgrad1, 8)
+TPMLP_TC_KERNELS(tpmlp_attn_qkv_proj, 8)
+TPMLP_TC_KERNELS(tpmlp_attn_out_proj_gsum, 8)
+TPMLP_TC_KERNELS(tpmlp_attn_out_proj_bwd, 8)
+TPMLP_TC_KERNELS(tpmlp_attn_qkv_bwd_dx_fsum, 8)
 
 int tc_gemm_max_smem_bytes() { return kSmemBytes; }
 
+int tc_epi_warps_for(const GemmParams& p, int tag) {
+  if (tag != TAG_FWD_COLUMN && tag != TAG_BWD_DGRAD) return 8;
+  for (int i = 0; i < p.num_probs; ++i) {
+    const Prob& P = p.probs[i];
+    if (P.epi != EPI_STORE && P.kblocks > kShortKBlocks) return 8;
+  }
+  return 16;
+}
+
 using KernelFn = void (*)(GemmParams);
 
-KernelFn kernel_for(int tag, bool stream_k) {
+KernelFn kernel_for(int tag, bool stream_k, int epi_warps) {
+  const bool w16 = epi_warps == 16;
   switch (tag) {
-    case TAG_FWD_COLUMN: return stream_k ? tpmlp_fwd_column_gemm_act_sk : tpmlp_fwd_column_gemm_act;
+    case TAG_FWD_COLUMN:
+      return w16 ? (stream_k ? tpmlp_fwd_column_gemm_act_w16_sk : tpmlp_fwd_column_gemm_act_w16)
+                 : (stream_k ? tpmlp_fwd_column_gemm_act_sk : tpmlp_fwd_column_gemm_act);
     case TAG_FWD_ROW: return stream_k ? tpmlp_fwd_row_gemm_gsum_sk : tpmlp_fwd_row_gemm_gsum;
-    case TAG_BWD_DGRAD: return stream_k ? tpmlp_bwd_dgrad_act_wgrad2_sk : tpmlp_bwd_dgrad_act_wgrad2;
+    case TAG_BWD_DGRAD:
+      return w16 ? (stream_k ? tpmlp_bwd_dgrad_act_wgrad2_w16_sk : tpmlp_bwd_dgrad_act_wgrad2_w16)
+                 : (stream_k ? tpmlp_bwd_dgrad_act_wgrad2_sk : tpmlp_bwd_dgrad_act_wgrad2);
     case TAG_BWD_FSUM: return stream_k ? tpmlp_bwd_dx_fsum_wgrad1_sk : tpmlp_bwd_dx_fsum_wgrad1;
     case TAG_ATTN_QKV: return stream_k ? tpmlp_attn_qkv_proj_sk : tpmlp_attn_qkv_proj;
     case TAG_ATTN_OUT: return stream_k ? tpmlp_attn_out_proj_gsum_sk : tpmlp_attn_out_proj_gsum;
@@ -751,7 +803,8 @@ KernelFn kernel_for(int tag, bool stream_k) {
   }
 }
 
-// Pairs (clusters of two CTAs) that can be resident at once on this device.
+// Pairs (clusters of two CTAs) that can be resident at once on this device
+// (every kernel has one CTA per SM: the same shared memory).
 int tc_gemm_max_pairs(int tag) {
   static std::mutex mu;
   static int cache[64][kNumKernelTags] = {};
@@ -759,11 +812,11 @@ int tc_gemm_max_pairs(int tag) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || tag < 0 || tag >= kNumKernelTags) return 0;
   std::lock_guard<std::mutex> lk(mu);
   if (cache[dev][tag] > 0) return cache[dev][tag];
-  KernelFn k = kernel_for(tag, false);
+  KernelFn k = kernel_for(tag, false, 8);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_for(8), 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -778,8 +831,9 @@ int tc_gemm_max_pairs(int tag) {
   return n;
 }
 
-cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int max_pairs_hint, cudaStream_t stream) {
-  KernelFn k = kernel_for(kernel_tag, p.sk.on != 0);
+cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int epi_warps, int max_pairs_hint,
+                           cudaStream_t stream) {
+  KernelFn k = kernel_for(kernel_tag, p.sk.on != 0, epi_warps);
   if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -789,7 +843,7 @@ cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int max_pairs_hi
   if (p.sk.on) pairs = p.sk.pairs;  // the stream-K ranges were cut for exactly this many pairs
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_for(epi_warps), 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -29,17 +29,24 @@ constexpr int kStageBytes = 2 * kOperandBytes;  // A + B
 constexpr int kStages = (224 * 1024) / kStageBytes;
 static_assert(kBK % 64 == 0, "stage depth is a whole number of 64-wide boxes");
 static_assert(kOperandBytes == (kBK / 64) * kKBoxBytes && kOperandBytes == 2 * kMNBoxBytes, "stage layout");
-constexpr int kNumEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kNumEpiWarps);
+// Epilogue configurations: kEW epilogue warps per CTA, 8 (chunks of 32
+// accumulator columns) or 16 (chunks of 16, so that a thread's registers stay
+// within 65,536 / (32 x 18) = 113).  The warps of a TMEM lane quarter split a
+// tile's 256 columns between them (2 x 128 or 4 x 64), which is four chunks
+// per warp and tile in both, and both use 32 KB of staging.
+constexpr int chunk_cols(int ew) { return ew == 8 ? 32 : 16; }
+constexpr int threads_for(int ew) { return 32 * (2 + ew); }
+constexpr int kMaxEpiWarps = 16;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
 constexpr int kNumAcc = 2;
 constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1;
-// Epilogue staging: each epilogue warp owns two 32 x 32 bf16 blocks (its 32
-// TMEM lanes x 32 columns), written row by row with a 64-byte swizzle and
-// stored by TMA while the other block is being filled.
-constexpr int kEpiBlockBytes = 32 * 32 * 2;
-constexpr int kEpiBytes = kNumEpiWarps * 2 * kEpiBlockBytes;
+// Epilogue staging: each epilogue warp owns two 32 x kCW bf16 blocks (its 32
+// TMEM lanes x kCW columns), written row by row with a swizzle and stored by
+// TMA while the other block is being filled.
+constexpr int kEpiBytes = 32 * 1024;
+static_assert(8 * 2 * 32 * chunk_cols(8) * 2 == kEpiBytes && 16 * 2 * 32 * chunk_cols(16) * 2 == kEpiBytes,
+              "staging");
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + 8 * kNumBars + 16;
 constexpr uint64_t kDrainTimeoutNs = 200ull * 1000 * 1000;
 constexpr uint64_t kPeerDrainNs = 2ull * 1000 * 1000;
@@ -235,14 +242,16 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
   return __bfloat1622float2(h);
 }
 
-// One epilogue warp's output path: 32 rows (its TMEM lanes) x 32 columns of
-// bf16 at a time go through one of its two shared-memory blocks and out with
-// a TMA store.  A thread writes its row as four 16-byte chunks, chunk g at
-// position g ^ ((row / 2) % 4) (the 64-byte swizzle of the output maps), so
-// every 8 consecutive rows fill all 32 banks once.  Rows and columns past the
-// tensor's end are clipped by the TMA unit.  Compared with each thread
+// One epilogue warp's output path: 32 rows (its TMEM lanes) x N columns of
+// bf16 at a time (N = 32 or 16, the chunk width of the kernel's epilogue
+// configuration) go through one of its two shared-memory blocks and out with
+// a TMA store.  A thread writes its row as N / 8 16-byte pieces, piece g at
+// position g ^ ((row / 2) % 4) for 64-byte rows (N = 32) or g ^ ((row / 4) % 2)
+// for 32-byte rows (N = 16) -- the 64- / 32-byte swizzle of the output maps --
+// so every 8 consecutive rows fill all 32 banks once.  Rows and columns past
+// the tensor's end are clipped by the TMA unit.  Compared with each thread
 // storing its own row to global memory (32 cache lines per warp store), this
-// moves a warp's 2 KB in four shared-memory wavefronts and one bulk copy.
+// moves a warp's block in a few shared-memory wavefronts and one bulk copy.
 struct EpiStore {
   uint32_t buf;  // this warp's two blocks
   uint32_t next;
@@ -250,20 +259,29 @@ struct EpiStore {
   int sj, sy0;   // striped out0: the stripe of this warp's rows and its first row
 };
 
-__device__ __forceinline__ void store_block(EpiStore& es, const GemmParams& p, int map, int x, int y,
-                                            const float (&v)[32], int lane, bool striped = false) {
+template <int N>
+constexpr int epi_block_bytes() { return 32 * N * 2; }
+
+// Output k (0..2) of problem P: columns x .. x + N - 1 (nvalid of them inside
+// the tensor) of this warp's rows y .. y + 31.
+template <int N>
+__device__ __forceinline__ void store_block(EpiStore& es, const GemmParams& p, const Prob& P, int k, int x, int y,
+                                            int nvalid, const float (&v)[N], int lane) {
+  static_assert(N == 32 || N == 16, "chunk width");
   if (y >= es.rows) return;  // every row of this warp is past the end: no store starts out of range
-  if (striped) {  // token stripes: the stripe's own map, stripe-local rows
+  (void)nvalid;              // the TMA unit clips columns past the end
+  int map = P.out_map[k];
+  if (k == 0 && P.out_striped) {  // token stripes: the stripe's own map, stripe-local rows
     map += es.sj;
     y -= es.sy0;
   }
-  const uint32_t b = es.buf + es.next * kEpiBlockBytes;
+  const uint32_t b = es.buf + es.next * epi_block_bytes<N>();
   if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last used block b has read it
   __syncwarp();
-  const uint32_t row = b + static_cast<uint32_t>(lane) * 64u;
-  const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+  const uint32_t row = b + static_cast<uint32_t>(lane) * (2u * N);
+  const uint32_t sw = N == 32 ? (static_cast<uint32_t>(lane) >> 1) & 3u : (static_cast<uint32_t>(lane) >> 2) & 1u;
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
+  for (int g = 0; g < N / 8; ++g) {
     uint4 o;
     o.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
     o.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
@@ -280,11 +298,14 @@ __device__ __forceinline__ void store_block(EpiStore& es, const GemmParams& p, i
   es.next ^= 1u;
 }
 
-__device__ __forceinline__ void load_row32(const void* src, int64_t ld, int64_t row, int col, int nvalid,
-                                           float (&v)[32]) {
+// N bf16 values of row `row` of a row-major array from column col on (the
+// nvalid first of them; the others read as zero).
+template <int N>
+__device__ __forceinline__ void load_row(const void* src, int64_t ld, int64_t row, int col, int nvalid,
+                                         float (&v)[N]) {
   const __nv_bfloat16* s = reinterpret_cast<const __nv_bfloat16*>(src) + row * ld + col;
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
+  for (int g = 0; g < N / 8; ++g) {
     uint4 q = make_uint4(0, 0, 0, 0);
     if (8 * g < nvalid) q = __ldg(reinterpret_cast<const uint4*>(s + 8 * g));
     float2 f;
@@ -296,62 +317,64 @@ __device__ __forceinline__ void load_row32(const void* src, int64_t ld, int64_t 
 }
 
 // v[j] += bias[col + j] for the chunk's valid columns (bias may be null).
-__device__ __forceinline__ void add_bias32(const void* bias, int col, int nvalid, float (&v)[32]) {
+template <int N>
+__device__ __forceinline__ void add_bias(const void* bias, int col, int nvalid, float (&v)[N]) {
   if (!bias) return;
-  float b[32];
-  load_row32(bias, 0, 0, col, nvalid, b);
+  float b[N];
+  load_row<N>(bias, 0, 0, col, nvalid, b);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] += b[j];
+  for (int j = 0; j < N; ++j) v[j] += b[j];
 }
 
-// Epilogue of one 32-column chunk (columns x .. x+31 of rows y .. y+31, this
+// Epilogue of one N-column chunk (columns x .. x+N-1 of rows y .. y+31, this
 // thread's row grow) of a single accumulator.  Every lane takes part (the
 // stores are per warp); inputs are read only for valid rows and columns.
+template <int N>
 __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& P, EpiStore& es, int64_t grow,
-                                               bool row_ok, int x, int y, int nvalid, const uint32_t (&r)[32],
+                                               bool row_ok, int x, int y, int nvalid, const uint32_t (&r)[N],
                                                int lane) {
-  float acc[32];
+  float acc[N];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
+  for (int j = 0; j < N; ++j) acc[j] = __uint_as_float(r[j]);
   const int nload = row_ok ? nvalid : 0;
   switch (P.epi) {
     case EPI_STORE:
-      add_bias32(P.aux0, x, nvalid, acc);
-      store_block(es, p, P.out_map[0], x, y, acc, lane, P.out_striped != 0);
+      add_bias<N>(P.aux0, x, nvalid, acc);
+      store_block<N>(es, p, P, 0, x, y, nvalid, acc, lane);
       break;
     case EPI_GELU_FWD: {
-      add_bias32(P.aux0, x, nvalid, acc);
-      store_block(es, p, P.out_map[0], x, y, acc, lane);  // A (pre-activation)
-      act::x2::gelu_x32(acc);
-      store_block(es, p, P.out_map[1], x, y, acc, lane);
+      add_bias<N>(P.aux0, x, nvalid, acc);
+      store_block<N>(es, p, P, 0, x, y, nvalid, acc, lane);  // A (pre-activation)
+      act::x2::gelu_xn(acc);
+      store_block<N>(es, p, P, 1, x, y, nvalid, acc, lane);
       break;
     }
     case EPI_GELU_BWD: {
-      float a[32];
-      load_row32(P.aux0, P.ldo, grow, x, nload, a);
+      float a[N];
+      load_row<N>(P.aux0, P.ldo, grow, x, nload, a);
       if (P.out1) {  // recompute H = GeLU(A) for the weight gradient of W2
-        float h[32];
-        act::x2::gelu_bwd_x32<true>(acc, a, h);
-        store_block(es, p, P.out_map[1], x, y, h, lane);
+        float h[N];
+        act::x2::gelu_bwd_xn<true>(acc, a, h);
+        store_block<N>(es, p, P, 1, x, y, nvalid, h, lane);
       } else {
-        act::x2::gelu_bwd_x32<false>(acc, a, acc);
+        act::x2::gelu_bwd_xn<false>(acc, a, acc);
       }
-      store_block(es, p, P.out_map[0], x, y, a, lane);
+      store_block<N>(es, p, P, 0, x, y, nvalid, a, lane);
       break;
     }
     case EPI_SWIGLU_BWD: {
-      float g[32], u[32];
-      load_row32(P.aux0, P.ldo, grow, x, nload, g);
-      load_row32(P.aux1, P.ldo, grow, x, nload, u);
+      float g[N], u[N];
+      load_row<N>(P.aux0, P.ldo, grow, x, nload, g);
+      load_row<N>(P.aux1, P.ldo, grow, x, nload, u);
       if (P.out2) {  // recompute H = U * Swish(G) for the weight gradient of W2
-        float h[32];
-        act::x2::swiglu_bwd_x32<true>(acc, g, u, h);
-        store_block(es, p, P.out_map[2], x, y, h, lane);
+        float h[N];
+        act::x2::swiglu_bwd_xn<true>(acc, g, u, h);
+        store_block<N>(es, p, P, 2, x, y, nvalid, h, lane);
       } else {
-        act::x2::swiglu_bwd_x32<false>(acc, g, u, acc);
+        act::x2::swiglu_bwd_xn<false>(acc, g, u, acc);
       }
-      store_block(es, p, P.out_map[0], x, y, g, lane);
-      store_block(es, p, P.out_map[1], x, y, u, lane);
+      store_block<N>(es, p, P, 0, x, y, nvalid, g, lane);
+      store_block<N>(es, p, P, 1, x, y, nvalid, u, lane);
       break;
     }
     default:

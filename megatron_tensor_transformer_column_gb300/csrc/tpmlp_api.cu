@@ -42,8 +42,9 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 thread_local int g_last_launches = 0;
-// Tiles the stream-K tail split in the last launch of each kind on this
-// thread: (problem, first row, first column) per tile.
+// Tiles the stream-K schedule split in the last launch of each kind on this
+// thread: (problem, first row, first column, address of the problem's first
+// output) per tile.
 thread_local std::vector<int64_t> g_last_split[kNumKernelTags];
 thread_local char g_last_error[256] = "";
 
@@ -124,20 +125,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // span) by box_rows rows, 128-byte swizzle, out-of-range elements read as
 // zero.  K-major operand tiles use 128-row boxes (128 M/N rows x 64 K),
 // MN-major ones kTcBK-row boxes (kTcBK K rows of a 64-wide M/N block).
-// Output maps (box_rows == kOutputMap): 32 x 32 boxes, 64-byte swizzle, for
-// the epilogue's TMA stores (out-of-range elements are not written).
+// Output maps, for the epilogue's TMA stores (out-of-range elements are not
+// written): box_rows == kOutputMap32, 32 rows x 32 columns with a 64-byte
+// swizzle (epilogues of 8 warps); kOutputMap16, 32 rows x 16 columns with a
+// 32-byte swizzle (epilogues of 16 warps).
 // Returns 0 on success, the CUresult otherwise (-1: entry point unavailable).
-constexpr int kOutputMap = -1;
+constexpr int kOutputMap32 = -1;
+constexpr int kOutputMap16 = -2;
 int encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return -1;
-  const bool out = box_rows == kOutputMap;
+  const bool out = box_rows < 0;
+  const bool narrow = box_rows == kOutputMap16;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {out ? 32u : 64u, out ? 32u : static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {out ? (narrow ? 16u : 32u) : 64u, out ? 32u : static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
+  const CUtensorMapSwizzle swz =
+      out ? (narrow ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B) : CU_TENSOR_MAP_SWIZZLE_128B;
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, out ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   out ? CU_TENSOR_MAP_L2_PROMOTION_NONE : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return static_cast<int>(r);
@@ -159,6 +166,7 @@ struct Builder {
   std::vector<int64_t> map_ld;
   bool map_error = false;
   int cur_group = -1;
+  int long_from = -1;  // first tile of the long-K groups placed last (balanced stream-K), or -1
 
   explicit Builder(GemmParams* params, bool tensor_cores) : p(params), tc(tensor_cores) {
     std::memset(static_cast<void*>(p), 0, sizeof(GemmParams));
@@ -187,7 +195,7 @@ struct Builder {
   // stripe's map: no box ever selects it).
   int stripe_maps(bool output, int box_rows) {
     if (!tc) return -1;
-    const int slot = output ? 2 : (box_rows == 128 ? 0 : 1);
+    const int slot = output ? 2 : (box_rows == 128 ? 0 : 1);  // one output box shape per launch
     if (stripe_map_base[slot] >= 0) return stripe_map_base[slot];
     const Stripes& st = p->stripes;
     int ref = 0;
@@ -204,8 +212,7 @@ struct Builder {
       const void* ptr = output ? st.out[jj] : st.in[jj];
       const int64_t cols = output ? st.out_ld : st.in_ld;
       const int idx = p->num_maps++;
-      const int r = encode_map(&p->maps[idx], ptr, st.row0[jj + 1] - st.row0[jj], cols, cols,
-                               output ? kOutputMap : box_rows);
+      const int r = encode_map(&p->maps[idx], ptr, st.row0[jj + 1] - st.row0[jj], cols, cols, box_rows);
       if (r != 0) {
         map_error = true;
         fail(TPMLP_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for stripe %d", r, j);
@@ -371,100 +378,210 @@ int tile_prob(const GemmParams& p, int tile, int* m0 = nullptr, int* n0 = nullpt
 
 std::atomic<uint32_t> g_sk_epoch{0};  // tags of the stream-K launches' ticket counts
 
-// Cut the stream-K tail of a tensor-core launch (see StreamK).  Every full
-// wave of tiles stays data-parallel: the pairs of a wave start together and
-// walk their tiles' K loops in step, so tiles that share a row block of A or
-// a column block of B read it from L2 once.  (Cutting more than the last
-// wave was measured slower: parts that run out of step lose that sharing and
-// become bound by HBM.)  Only the last, partial wave of R tiles is cut, and
-// only when every pair carries the same data-parallel load and the R tiles
-// have the same depth KB: each tile is then split into k parts of KB / k K
-// blocks (rounded), on k ranges, with k <= pairs / R chosen to minimise
-// KB / k + kPartCost (k - 1).  kPartCost, in K blocks, is what one more part
-// costs the owner: reading a 256 KB partial accumulator per pair back from
-// L2 (about 2.8 us each on GB300, about five K blocks).  Auto mode keeps the
-// plain round robin unless the cut saves at least max(16, 2 %) of a pair's K
-// blocks: measured on GB300, smaller savings were lost to the launch's fixed
-// costs and, under the power cap, to lower clocks in the following launches.
-void plan_stream_k(GemmParams& p, int pairs, int mode) {
+// Range bookkeeping shared by both ways of cutting (see StreamK): from the
+// ranges' starts, the head / tail split information of every range, and the
+// tiles that more than one range covers (reported by tpmlp_last_split_tiles).
+void finish_ranges(GemmParams& p, int pairs, const std::vector<int32_t>& kb, std::vector<int>* split_tiles) {
+  StreamK& sk = p.sk;
+  const int n = p.total_tiles;
+  auto empty = [&](int q) { return sk.start_tile[q] == sk.start_tile[q + 1] && sk.start_kb[q] == sk.start_kb[q + 1]; };
+  // covering ranges of each tile of the split region: first and count
+  std::vector<int> first(n, -1), count(n, 0);
+  for (int q = 0; q < pairs; ++q) {
+    if (empty(q)) continue;
+    int t = sk.start_tile[q];
+    const int end_t = sk.start_tile[q + 1], end_kb = sk.start_kb[q + 1];
+    // tiles touched: start_tile .. (end_kb > 0 ? end_t : end_t - 1)
+    const int last = end_kb > 0 ? end_t : end_t - 1;
+    for (; t <= last && t < n; ++t) {
+      if (first[t] < 0) first[t] = q;
+      ++count[t];
+    }
+  }
+  for (int q = 0; q < pairs; ++q) {
+    sk.head_q0[q] = sk.tail_q0[q] = static_cast<int16_t>(q);
+    sk.head_n[q] = sk.tail_n[q] = 1;
+    if (empty(q)) continue;
+    const int th = sk.start_tile[q];
+    const int tt = sk.start_kb[q + 1] > 0 ? sk.start_tile[q + 1] : sk.start_tile[q + 1] - 1;
+    if (th < n) {
+      sk.head_q0[q] = static_cast<int16_t>(first[th]);
+      sk.head_n[q] = static_cast<int16_t>(count[th]);
+    }
+    if (tt >= 0 && tt < n) {
+      sk.tail_q0[q] = static_cast<int16_t>(first[tt]);
+      sk.tail_n[q] = static_cast<int16_t>(count[tt]);
+    }
+  }
+  if (split_tiles) {
+    split_tiles->clear();
+    for (int t = sk.dp_tiles; t < n; ++t)
+      if (count[t] > 1) split_tiles->push_back(t);
+  }
+  (void)kb;
+}
+
+// Estimated cost of a tile in K blocks: its main loop, or its epilogue when
+// that is longer (about 20 K blocks for an activation epilogue of a 256 x 256
+// tile, 4 for a plain store; measured on GB300 on short-K launches).
+int64_t tile_cost(const Prob& P, int kb) {
+  const int64_t epi = P.epi == EPI_STORE ? 4 : 20;
+  return std::max<int64_t>(kb, epi);
+}
+
+// Cut the stream-K schedule of a tensor-core launch (see StreamK).  Two ways:
+//
+// Last wave (modes AUTO and ALWAYS, long_from < 0).  Every full wave of tiles
+// stays data-parallel: the pairs of a wave start together and walk their
+// tiles' K loops in step, so tiles that share a row block of A or a column
+// block of B read it from L2 once.  (Cutting more than the last wave was
+// measured slower on the large launches: parts that run out of step lose that
+// sharing and become bound by HBM.)  Only the last, partial wave of R tiles
+// is cut, and only when every pair carries the same data-parallel load and
+// the R tiles have the same depth KB: each tile is then split into k parts of
+// KB / k K blocks (rounded), on k ranges, with k <= pairs / R chosen to
+// minimise KB / k + kPartCost (k - 1).  kPartCost, in K blocks, is what one
+// more part costs the finisher: reading a 256 KB partial accumulator per pair
+// back from L2 (about 2.8 us each on GB300, about five K blocks).  Auto mode
+// keeps the plain round robin unless the cut saves at least max(16, 2 %) of
+// a pair's K blocks: measured on GB300, smaller savings were lost to the
+// launch's fixed costs and, under the power cap, to lower clocks in the
+// following launches.
+//
+// Balanced (long_from >= 0: the host placed the launch's long-K weight-
+// gradient tiles last, from tile long_from on; mode BALANCE, or AUTO when
+// those tiles' operands fit in L2).  The short tiles before long_from are
+// dealt out round robin; the long tiles' K blocks are cut into ranges that
+// fill every pair up to the same estimated load (water filling over the
+// round-robin loads, tile_cost).  With the operands resident in L2, parts
+// that run out of step cost no HBM traffic, and the pairs no longer wait on
+// the few that drew a long tile.
+void plan_stream_k(GemmParams& p, int pairs, int mode, int long_from, std::vector<int>* split_tiles) {
   StreamK& sk = p.sk;
   sk.on = 0;
   sk.dp_tiles = p.total_tiles;
   sk.pairs = 0;
   sk.epoch = 0;
+  if (split_tiles) split_tiles->clear();
   const int n = p.total_tiles;
   if (mode == TPMLP_STREAM_K_OFF || pairs < 2 || pairs > kMaxSkPairs || n <= 0) return;
-  const int dp_tiles = (n / pairs) * pairs;
-  const int R = n - dp_tiles;
-  if (R == 0) return;  // no partial wave
-  // Auto mode needs tiles of one depth; that holds exactly when every
-  // problem has the same K blocks, which spares the per-tile walk below.
+  std::vector<int32_t> kb(n, p.probs[0].kblocks);
   bool same_depth = true;
   for (int i = 1; i < p.num_probs; ++i) same_depth = same_depth && p.probs[i].kblocks == p.probs[0].kblocks;
-  if (!same_depth && mode == TPMLP_STREAM_K_AUTO) return;
-  std::vector<int32_t> kb(n, p.probs[0].kblocks);
-  if (!same_depth)
-    for (int t = 0; t < n; ++t) kb[t] = p.probs[tile_prob(p, t)].kblocks;
-  std::vector<int64_t> dp(pairs, 0);
-  for (int t = 0; t < dp_tiles; ++t) dp[t % pairs] += kb[t];
-  const int64_t dp_lo = *std::min_element(dp.begin(), dp.end());
-  const int64_t dp_hi = *std::max_element(dp.begin(), dp.end());
-  int kb_lo = kb[dp_tiles], kb_hi = kb[dp_tiles];
-  for (int t = dp_tiles; t < n; ++t) {
-    kb_lo = std::min(kb_lo, kb[t]);
-    kb_hi = std::max(kb_hi, kb[t]);
-  }
-  const bool uniform = dp_lo == dp_hi && kb_lo == kb_hi;
-  if (!uniform && mode == TPMLP_STREAM_K_AUTO) return;
-  constexpr int64_t kPartCost = 5;
-  constexpr int64_t kMinSaving = 16;  // K blocks (about 9 us): below that, launch and power effects dominate
-  const int k_max = std::max(1, pairs / R);
-  int k = 1;
-  int64_t best = kb_hi;
-  for (int c = 2; c <= k_max; ++c) {
-    const int64_t m = (kb_hi + c - 1) / c + kPartCost * (c - 1);
-    if (m < best) {
-      best = m;
-      k = c;
+  std::vector<int> prob_of(n, 0);
+  if (!same_depth || long_from >= 0 || mode == TPMLP_STREAM_K_BALANCE)
+    for (int t = 0; t < n; ++t) {
+      prob_of[t] = tile_prob(p, t);
+      kb[t] = p.probs[prob_of[t]].kblocks;
     }
-  }
-  if (mode == TPMLP_STREAM_K_ALWAYS) k = std::min(k_max, kb_hi);  // as many parts as fit: a stress test
-  if (mode == TPMLP_STREAM_K_AUTO) {
-    const int64_t rr = dp_hi + kb_hi, cut = dp_hi + best;
-    if (k == 1 || rr - cut < std::max<int64_t>(kMinSaving, rr / 50)) return;
-  }
-  if (k < 2) return;
-  // Range r = j k + i (held by pair pairs - 1 - r) is part i of tail tile j;
-  // a part of a tile cut between ranges is owned by the higher-numbered pair
-  // (part 0); ranges from R k on are empty.
-  for (int r = 0; r <= pairs; ++r) {
-    const int j = r / k, i = r % k;
-    if (j >= R) {
-      sk.start_tile[r] = n;
-      sk.start_kb[r] = 0;
-    } else {
-      sk.start_tile[r] = dp_tiles + j;
-      sk.start_kb[r] = static_cast<int32_t>(static_cast<int64_t>(kb[dp_tiles + j]) * i / k);
+
+  if (long_from >= 0 || mode == TPMLP_STREAM_K_BALANCE) {
+    const int dp_tiles = long_from >= 0 ? long_from : 0;
+    std::vector<int64_t> load(pairs, 0);
+    for (int t = 0; t < dp_tiles; ++t) load[t % pairs] += tile_cost(p.probs[prob_of[t]], kb[t]);
+    int64_t L = 0;
+    for (int t = dp_tiles; t < n; ++t) L += kb[t];
+    if (L == 0) return;
+    // water level lambda with sum_p max(0, lambda - load_p) = L (integer K blocks)
+    std::vector<int64_t> sorted(load);
+    std::sort(sorted.begin(), sorted.end());
+    int64_t lambda = sorted[0], below = 0;
+    int64_t rest = L;
+    for (int i = 0; i < pairs; ++i) {
+      const int64_t next = i + 1 < pairs ? sorted[i + 1] : INT64_MAX;
+      const int64_t cnt = i + 1;  // pairs at or below this level
+      const int64_t room = next == INT64_MAX ? INT64_MAX : (next - sorted[i]) * cnt;
+      (void)below;
+      if (rest <= room) {
+        lambda = sorted[i] + rest / cnt;
+        break;
+      }
+      rest -= room;
     }
-  }
-  // Each range holds one part of one tile.  Per range: its tile's first
-  // non-empty range (a tile with fewer K blocks than k has empty ranges, and
-  // they may come first) and its tile's number of non-empty ranges.
-  for (int r = 0; r < pairs; ++r) {
-    const int j = r / k;
-    int first = -1, parts = 0;
-    for (int q = j * k; q < std::min(pairs, (j + 1) * k); ++q) {
-      if (sk.start_tile[q] == sk.start_tile[q + 1] && sk.start_kb[q] == sk.start_kb[q + 1]) continue;
-      if (first < 0) first = q;
-      ++parts;
+    std::vector<int64_t> size(pairs, 0);
+    int64_t given = 0;
+    for (int q = 0; q < pairs; ++q) {
+      size[q] = std::max<int64_t>(0, lambda - load[q]);
+      given += size[q];
     }
-    sk.first_range[r] = static_cast<int16_t>(first < 0 ? r : first);
-    sk.num_parts[r] = static_cast<int16_t>(parts);
+    for (int q = 0; given < L; q = (q + 1) % pairs)  // the remainder, one K block at a time, to the lowest loads
+      if (load[q] + size[q] <= lambda) {
+        ++size[q];
+        ++given;
+      }
+    // ranges in K-block order; range r belongs to pair pairs - 1 - r
+    int t = dp_tiles, k = 0;
+    for (int r = 0; r < pairs; ++r) {
+      sk.start_tile[r] = t;
+      sk.start_kb[r] = k;
+      int64_t want = size[pairs - 1 - r];
+      while (want > 0 && t < n) {
+        const int64_t take = std::min<int64_t>(want, kb[t] - k);
+        want -= take;
+        k += static_cast<int>(take);
+        if (k == kb[t]) {
+          ++t;
+          k = 0;
+        }
+      }
+    }
+    sk.start_tile[pairs] = n;
+    sk.start_kb[pairs] = 0;
+    sk.dp_tiles = dp_tiles;
+  } else {
+    const int dp_tiles = (n / pairs) * pairs;
+    const int R = n - dp_tiles;
+    if (R == 0) return;  // no partial wave
+    // Auto mode needs tiles of one depth; that holds exactly when every
+    // problem has the same K blocks, which spares the per-tile walk above.
+    if (!same_depth && mode == TPMLP_STREAM_K_AUTO) return;
+    std::vector<int64_t> dp(pairs, 0);
+    for (int t = 0; t < dp_tiles; ++t) dp[t % pairs] += kb[t];
+    const int64_t dp_lo = *std::min_element(dp.begin(), dp.end());
+    const int64_t dp_hi = *std::max_element(dp.begin(), dp.end());
+    int kb_lo = kb[dp_tiles], kb_hi = kb[dp_tiles];
+    for (int t = dp_tiles; t < n; ++t) {
+      kb_lo = std::min(kb_lo, kb[t]);
+      kb_hi = std::max(kb_hi, kb[t]);
+    }
+    const bool uniform = dp_lo == dp_hi && kb_lo == kb_hi;
+    if (!uniform && mode == TPMLP_STREAM_K_AUTO) return;
+    constexpr int64_t kPartCost = 5;
+    constexpr int64_t kMinSaving = 16;  // K blocks (about 9 us): below that, launch and power effects dominate
+    const int k_max = std::max(1, pairs / R);
+    int kparts = 1;
+    int64_t best = kb_hi;
+    for (int c = 2; c <= k_max; ++c) {
+      const int64_t m = (kb_hi + c - 1) / c + kPartCost * (c - 1);
+      if (m < best) {
+        best = m;
+        kparts = c;
+      }
+    }
+    if (mode == TPMLP_STREAM_K_ALWAYS) kparts = std::min(k_max, kb_hi);  // as many parts as fit: a stress test
+    if (mode == TPMLP_STREAM_K_AUTO) {
+      const int64_t rr = dp_hi + kb_hi, cut = dp_hi + best;
+      if (kparts == 1 || rr - cut < std::max<int64_t>(kMinSaving, rr / 50)) return;
+    }
+    if (kparts < 2) return;
+    // Range r = j k + i (held by pair pairs - 1 - r) is part i of tail tile j;
+    // ranges from R k on are empty.
+    for (int r = 0; r <= pairs; ++r) {
+      const int j = r / kparts, i = r % kparts;
+      if (j >= R) {
+        sk.start_tile[r] = n;
+        sk.start_kb[r] = 0;
+      } else {
+        sk.start_tile[r] = dp_tiles + j;
+        sk.start_kb[r] = static_cast<int32_t>(static_cast<int64_t>(kb[dp_tiles + j]) * i / kparts);
+      }
+    }
+    sk.dp_tiles = dp_tiles;
   }
+  finish_ranges(p, pairs, kb, split_tiles);
   uint32_t e = ++g_sk_epoch & 0xFFFFFFu;  // 24-bit tag of this launch's ticket counts
   if (e == 0) e = ++g_sk_epoch & 0xFFFFFFu;
   sk.on = 1;
-  sk.dp_tiles = dp_tiles;
   sk.pairs = pairs;
   sk.epoch = e;
 }
@@ -475,12 +592,21 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
                     cudaStream_t stream, bool sk_workspace = true) {
   GemmParams& p = *B.p;
   if (p.total_tiles == 0) return TPMLP_OK;
+  if (B.tc) {
+    for (int i = 0; i < p.num_probs; ++i) {
+      Prob& P = p.probs[i];
+      P.kblocks = 0;
+      for (int sg = P.seg_begin; sg < P.seg_begin + P.seg_count; ++sg) P.kblocks += (p.segs[sg].K + kTcBK - 1) / kTcBK;
+    }
+  }
+  const int epi_warps = B.tc ? tc_epi_warps_for(p, tag) : 0;
+  const int out_box = epi_warps == 16 ? kOutputMap16 : kOutputMap32;
   for (int i = 0; i < p.num_probs; ++i) {  // token-striped output (sequence-parallel layout)
     Prob& P = p.probs[i];
     if (P.out0 == kStripedOut) {
       P.out0 = nullptr;
       P.out_striped = 1;
-      P.out_map[0] = B.stripe_maps(true, kOutputMap);
+      P.out_map[0] = B.stripe_maps(true, out_box);
     }
   }
   if (B.tc) {  // the tensor-core epilogue writes every output with TMA stores
@@ -488,7 +614,7 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
       Prob& P = p.probs[i];
       void* outs[3] = {P.out0, P.out1, P.out2};
       for (int k = 0; k < 3; ++k)
-        if (outs[k]) P.out_map[k] = B.map(outs[k], P.M, P.N, kOutputMap, P.ldo);
+        if (outs[k]) P.out_map[k] = B.map(outs[k], P.M, P.N, out_box, P.ldo);
     }
   }
   if (B.table_error) return TPMLP_ERR_UNSUPPORTED;  // message set by Builder::table_full
@@ -498,26 +624,18 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
   p.stall_injection = plan->stall_injection;
   p.sk.on = 0;
   p.sk.dp_tiles = p.total_tiles;
-  if (B.tc) {
-    for (int i = 0; i < p.num_probs; ++i) {
-      Prob& P = p.probs[i];
-      P.kblocks = 0;
-      for (int sg = P.seg_begin; sg < P.seg_begin + P.seg_count; ++sg) P.kblocks += (p.segs[sg].K + kTcBK - 1) / kTcBK;
-    }
-    if (sk_workspace) plan_stream_k(p, tc_gemm_max_pairs(tag), plan->stream_k);
-  }
+  std::vector<int> split_tiles;
+  if (B.tc && sk_workspace) plan_stream_k(p, tc_gemm_max_pairs(tag), plan->stream_k, B.long_from, &split_tiles);
   std::vector<int64_t>& split = g_last_split[tag];
   split.clear();
-  if (p.sk.on) {
-    for (int t = p.sk.dp_tiles; t < p.total_tiles; ++t) {
-      int m0 = 0, n0 = 0;
-      const int pi = tile_prob(p, t, &m0, &n0);
-      split.insert(split.end(), {pi, m0, n0});
-    }
+  for (int t : split_tiles) {
+    int m0 = 0, n0 = 0;
+    const int pi = tile_prob(p, t, &m0, &n0);
+    split.insert(split.end(), {pi, m0, n0, static_cast<int64_t>(reinterpret_cast<uintptr_t>(p.probs[pi].out0))});
   }
   cudaError_t e;
   if (B.tc) {
-    e = launch_tc_gemm(p, tag, di.sms / 2, stream);
+    e = launch_tc_gemm(p, tag, epi_warps, di.sms / 2, stream);
   } else {
     e = launch_simt_gemm(p, stream);
   }
@@ -602,6 +720,19 @@ tpmlp_status launch_colsums(const ColsumBuilder& C, const tpmlp_plan* pl, cudaSt
 }
 
 // ------------------------------------------------------------------ phases
+// Whether a launch places its long-K weight-gradient tiles last and lets the
+// stream-K planner spread them evenly over the pairs (plan_stream_k,
+// balanced): in TPMLP_STREAM_K_BALANCE mode.  Auto mode does not: measured on
+// GB300 on the GPT-2-small shape (whose weight-gradient operands stay in L2),
+// the parts' partial stores (4-7 us) and the last part's read-back of the
+// others (8-11 us) cost more than the balance gained (f-sum launch 65 -> 70
+// us; dgrad 98 -> 92 us).  long_bytes (those tiles' operands and outputs) is
+// kept for that decision.
+bool balance_long(const tpmlp_plan* pl, int64_t long_bytes) {
+  (void)long_bytes;
+  return pl->dtype == TPMLP_BF16 && pl->stream_k == TPMLP_STREAM_K_BALANCE;
+}
+
 tpmlp_status fwd_column(const tpmlp_plan* pl, const DeviceInfo& di, const void* X, const void* const* W1,
                         const void* const* W3, const void* const* b1, const void* const* b3, void* const* saved,
                         void* const* H, void* ws, cudaStream_t st, const void* const* X_stripes = nullptr) {
@@ -673,15 +804,20 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
     B.set_stripes(pl, dY_stripes, pl->d, nullptr, 0);
     dY = kStripedIn;
   }
-  // dW2_i = H_i^T dY (K = T: the long tiles go first)
-  for (int i = 0; i < pl->t && !recompute; ++i) {
-    const int64_t di_ = pl->d_i[i];
-    B.begin_group(di_, band);
-    Prob& P = B.add_prob(di_, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
-    P.out0 = dW2[i];
-    B.add_seg(P, H[i], pl->T, di_, dY, pl->T, pl->d, nullptr, pl->T);
-    B.end_group();
-  }
+  // dW2_i = H_i^T dY (K = T): the long tiles go first, or last when the
+  // stream-K planner spreads them over the pairs
+  const bool balanced = !recompute && balance_long(pl, 2 * (pl->T * pl->dff + pl->T * pl->d + pl->dff * pl->d));
+  auto add_dw2 = [&] {
+    for (int i = 0; i < pl->t && !recompute; ++i) {
+      const int64_t di_ = pl->d_i[i];
+      B.begin_group(di_, band);
+      Prob& P = B.add_prob(di_, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
+      P.out0 = dW2[i];
+      B.add_seg(P, H[i], pl->T, di_, dY, pl->T, pl->d, nullptr, pl->T);
+      B.end_group();
+    }
+  };
+  if (!balanced) add_dw2();
   // dH_i = dY W2_i^T with act' fused (g backward = identity: every shard reads dY)
   B.begin_group(pl->T, band);
   for (int i = 0; i < pl->t; ++i) {
@@ -695,6 +831,10 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
     B.add_seg(P, dY, pl->T, pl->d, W2[i], di_, pl->d, nullptr, pl->d);
   }
   B.end_group();
+  if (balanced) {
+    B.long_from = B.p->total_tiles;
+    add_dw2();
+  }
   TPMLP_TRY(launch(B, TAG_BWD_DGRAD, di, pl, ws, st));
   if (db2) {  // g backward is the identity: b2's gradient is that of Y
     ColsumBuilder C(pl->dtype == TPMLP_BF16);
@@ -743,8 +883,10 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
   const int t = pl->t;
   const bool dw2_fits = (!tc || (sw ? 10 : 6) * t + 3 <= kMaxMaps) && (sw ? 3 : 2) * t + 1 <= kMaxProbs &&
                         (sw ? 5 : 3) * t <= kMaxSegs && t + 2 <= kMaxGroups;
+  const int64_t dw2_bytes = 2 * (pl->T * pl->dff + pl->T * pl->d + pl->dff * pl->d);
   if (H_for_dW2 && !dw2_fits) {
     Builder B2(scratch_params(), tc);
+    if (balance_long(pl, dw2_bytes)) B2.long_from = 0;
     add_dw2(B2);
     TPMLP_TRY(launch(B2, TAG_BWD_FSUM, di, pl, ws, st));
   }
@@ -754,24 +896,33 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
     if (X_stripes) X = kStripedIn;
     if (dX_stripes) dX = kStripedOut;
   }
-  if (H_for_dW2 && dw2_fits) add_dw2(B);
-  // dW1_i = X^T dA_i (SwiGLU: X^T dG_i) and dW3_i = X^T dU_i (K = T)
-  B.begin_group(pl->d, band);
-  for (int i = 0; i < pl->t; ++i) {
-    const int64_t di_ = pl->d_i[i];
-    Prob& P = B.add_prob(pl->d, di_, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, di_);
-    P.out0 = dW1[i];
-    B.add_seg(P, X, pl->T, pl->d, dact[i], pl->T, di_, nullptr, pl->T);
-  }
-  if (sw) {
+  // The weight gradients (K = T) go first, or last when the stream-K planner
+  // spreads them over the pairs.
+  const int64_t nact = sw ? 2 : 1;
+  const bool with_dw2 = H_for_dW2 && dw2_fits;
+  const bool balanced =
+      balance_long(pl, 2 * (pl->T * pl->d + nact * (pl->T * pl->dff + pl->d * pl->dff)) + (with_dw2 ? dw2_bytes : 0));
+  auto add_wgrads = [&] {
+    if (with_dw2) add_dw2(B);
+    // dW1_i = X^T dA_i (SwiGLU: X^T dG_i) and dW3_i = X^T dU_i
+    B.begin_group(pl->d, band);
     for (int i = 0; i < pl->t; ++i) {
       const int64_t di_ = pl->d_i[i];
       Prob& P = B.add_prob(pl->d, di_, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, di_);
-      P.out0 = dW3[i];
-      B.add_seg(P, X, pl->T, pl->d, dact[pl->t + i], pl->T, di_, nullptr, pl->T);
+      P.out0 = dW1[i];
+      B.add_seg(P, X, pl->T, pl->d, dact[i], pl->T, di_, nullptr, pl->T);
     }
-  }
-  B.end_group();
+    if (sw) {
+      for (int i = 0; i < pl->t; ++i) {
+        const int64_t di_ = pl->d_i[i];
+        Prob& P = B.add_prob(pl->d, di_, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, di_);
+        P.out0 = dW3[i];
+        B.add_seg(P, X, pl->T, pl->d, dact[pl->t + i], pl->T, di_, nullptr, pl->T);
+      }
+    }
+    B.end_group();
+  };
+  if (!balanced) add_wgrads();
   // dX = sum_i dA_i W1_i^T (+ dU_i W3_i^T): the f operator's backward sum.
   B.begin_group(pl->T, band);
   Prob& P = B.add_prob(pl->T, pl->d, 256, MAJOR_K, MAJOR_K, EPI_STORE, pl->d);
@@ -782,6 +933,10 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
     for (int i = 0; i < pl->t; ++i)
       B.add_seg(P, dact[pl->t + i], pl->T, pl->d_i[i], W3[i], pl->d, pl->d_i[i], nullptr, pl->d_i[i]);
   B.end_group();
+  if (balanced) {
+    B.long_from = B.p->total_tiles;
+    add_wgrads();
+  }
   TPMLP_TRY(launch(B, TAG_BWD_FSUM, di, pl, ws, st));
   if (db1 || (sw && db3)) {
     ColsumBuilder C(pl->dtype == TPMLP_BF16);
@@ -838,15 +993,22 @@ tpmlp_status attn_out_bwd(const tpmlp_plan* pl, const DeviceInfo& di, const void
   }
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
   const int band = band_for(di.sms);
-  // dWO_i = O_i^T dZ (K = T: the long tiles go first)
-  for (int i = 0; i < pl->t; ++i) {
-    const int64_t w = pl->dq_i[i];
-    B.begin_group(w, band);
-    Prob& P = B.add_prob(w, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
-    P.out0 = dWO[i];
-    B.add_seg(P, O[i], pl->T, w, dZ, pl->T, pl->d, nullptr, pl->T);
-    B.end_group();
-  }
+  int64_t dq = 0;
+  for (int i = 0; i < pl->t; ++i) dq += pl->dq_i[i];
+  // dWO_i = O_i^T dZ (K = T): the long tiles go first, or last when the
+  // stream-K planner spreads them over the pairs
+  const bool balanced = balance_long(pl, 2 * (pl->T * dq + pl->T * pl->d + dq * pl->d));
+  auto add_dwo = [&] {
+    for (int i = 0; i < pl->t; ++i) {
+      const int64_t w = pl->dq_i[i];
+      B.begin_group(w, band);
+      Prob& P = B.add_prob(w, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
+      P.out0 = dWO[i];
+      B.add_seg(P, O[i], pl->T, w, dZ, pl->T, pl->d, nullptr, pl->T);
+      B.end_group();
+    }
+  };
+  if (!balanced) add_dwo();
   // dO_i = dZ WO_i^T (g backward is the identity: every shard reads dZ)
   B.begin_group(pl->T, band);
   for (int i = 0; i < pl->t; ++i) {
@@ -856,6 +1018,10 @@ tpmlp_status attn_out_bwd(const tpmlp_plan* pl, const DeviceInfo& di, const void
     B.add_seg(P, dZ, pl->T, pl->d, WO[i], w, pl->d, nullptr, pl->d);
   }
   B.end_group();
+  if (balanced) {
+    B.long_from = B.p->total_tiles;
+    add_dwo();
+  }
   return launch(B, TAG_ATTN_OUT_BWD, di, pl, ws, st);
 }
 
@@ -871,21 +1037,30 @@ tpmlp_status attn_qkv_bwd(const tpmlp_plan* pl, const DeviceInfo& di, const void
   }
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
   const int band = band_for(di.sms);
-  // dW_QKV,i = X^T dQKV_i (K = T)
-  B.begin_group(pl->d, band);
-  for (int i = 0; i < pl->t; ++i) {
-    const int64_t n = pl->d_i[i];
-    Prob& P = B.add_prob(pl->d, n, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, n);
-    P.out0 = dWqkv[i];
-    B.add_seg(P, X, pl->T, pl->d, dQKV[i], pl->T, n, nullptr, pl->T);
-  }
-  B.end_group();
+  // dW_QKV,i = X^T dQKV_i (K = T): first, or last when the stream-K planner
+  // spreads them over the pairs
+  const bool balanced = balance_long(pl, 2 * (pl->T * pl->d + pl->T * pl->dff + pl->d * pl->dff));
+  auto add_dwqkv = [&] {
+    B.begin_group(pl->d, band);
+    for (int i = 0; i < pl->t; ++i) {
+      const int64_t n = pl->d_i[i];
+      Prob& P = B.add_prob(pl->d, n, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, n);
+      P.out0 = dWqkv[i];
+      B.add_seg(P, X, pl->T, pl->d, dQKV[i], pl->T, n, nullptr, pl->T);
+    }
+    B.end_group();
+  };
+  if (!balanced) add_dwqkv();
   // dX = sum_i dQKV_i W_QKV,i^T (= dQ_i WQ_i^T + dK_i WK_i^T + dV_i WV_i^T): the f-sum.
   B.begin_group(pl->T, band);
   Prob& P = B.add_prob(pl->T, pl->d, 256, MAJOR_K, MAJOR_K, EPI_STORE, pl->d);
   P.out0 = dX;
   for (int i = 0; i < pl->t; ++i) B.add_seg(P, dQKV[i], pl->T, pl->d_i[i], Wqkv[i], pl->d, pl->d_i[i], nullptr, pl->d_i[i]);
   B.end_group();
+  if (balanced) {
+    B.long_from = B.p->total_tiles;
+    add_dwqkv();
+  }
   return launch(B, TAG_ATTN_QKV_BWD, di, pl, ws, st);
 }
 
@@ -1001,8 +1176,9 @@ size_t tpmlp_workspace_size(const tpmlp_plan* plan) {
 tpmlp_status tpmlp_plan_set_stream_k(tpmlp_plan* plan, int mode) {
   g_last_error[0] = 0;
   if (!plan) return fail(TPMLP_ERR_INVALID_ARG, "plan is NULL");
-  if (mode != TPMLP_STREAM_K_OFF && mode != TPMLP_STREAM_K_AUTO && mode != TPMLP_STREAM_K_ALWAYS)
-    return fail(TPMLP_ERR_INVALID_ARG, "stream-K mode %d is not one of 0, 1, 2", mode);
+  if (mode != TPMLP_STREAM_K_OFF && mode != TPMLP_STREAM_K_AUTO && mode != TPMLP_STREAM_K_ALWAYS &&
+      mode != TPMLP_STREAM_K_BALANCE)
+    return fail(TPMLP_ERR_INVALID_ARG, "stream-K mode %d is not one of 0, 1, 2, 3", mode);
   plan->stream_k = mode;
   return TPMLP_OK;
 }
@@ -1473,9 +1649,9 @@ tpmlp_status tpmlp_eval_activation(int fn, const float* x, const float* y, const
 int tpmlp_last_split_tiles(int launch_kind, int64_t* tiles, int cap) {
   if (launch_kind < 0 || launch_kind >= kNumKernelTags) return -1;
   const std::vector<int64_t>& v = g_last_split[launch_kind];
-  const int n = static_cast<int>(v.size() / 3);
+  const int n = static_cast<int>(v.size() / 4);
   if (tiles)
-    for (int i = 0; i < std::min(n, cap) * 3; ++i) tiles[i] = v[i];
+    for (int i = 0; i < std::min(n, cap) * 4; ++i) tiles[i] = v[i];
   return n;
 }
 

@@ -122,25 +122,27 @@ struct Stripes {
   int64_t in_ld, out_ld;            // row strides of the stripes, in elements
 };
 
-// Stream-K tail (tensor-core path).  Tiles [0, dp_tiles) are dealt out round
-// robin, tile i to pair i mod pairs.  The K blocks of each remaining tile
-// (the last, partial wave) are cut into parts, one per range: range r (held
-// by pair pairs - 1 - r) starts at (start_tile[r], start_kb[r]) and ends
-// where range r + 1 starts; the ranges of a tile are consecutive and each
-// starts inside it.  Every part leaves its fp32 accumulator in its range's
-// workspace slot and takes a ticket from a per-tile counter (one per
-// epilogue warp position, in the flag block, tagged with the launch's epoch
-// so that a count left by an aborted launch reads as zero); the part with
-// the last ticket adds all parts in range order and runs the tile's
-// epilogue.  Nobody waits for another pair, and the fixed order makes the
-// result the same on every run.
+// Stream-K schedule (tensor-core path).  Tiles [0, dp_tiles) are dealt out
+// round robin, tile i to pair i mod pairs.  The K blocks of the remaining
+// tiles, concatenated in tile order, are cut into one contiguous range per
+// pair: range r (held by pair pairs - 1 - r) starts at (start_tile[r],
+// start_kb[r]) and ends where range r + 1 starts.  A range may end inside a
+// tile, span whole tiles and start inside another, so it holds at most two
+// parts of split tiles: its first item (partial slot 2r) and its last item
+// (slot 2r + 1).  Every part leaves its fp32 accumulator in its slot and takes
+// a ticket from a per-tile counter (one per epilogue warp position, in the
+// counter block, keyed by the range holding the tile's K block 0 and tagged
+// with the launch's epoch, so that a count left by an aborted launch reads as
+// zero); the part with the last ticket adds all parts in range order and runs
+// the tile's epilogue.  Nobody waits for another pair, and the fixed order
+// makes the result the same on every run.
 constexpr int kMaxSkPairs = 80;
-constexpr int kSkWarpsPerPair = 16;                        // epilogue warps of a pair
+constexpr int kSkWarpsPerPair = 32;                        // epilogue warps of a pair, at most
 constexpr size_t kStatusBytes = 256;                       // workspace: status word block
 constexpr size_t kSkFlagsOffset = kStatusBytes;            // kMaxSkPairs x kSkWarpsPerPair uint32 counters
-constexpr size_t kSkSlotsOffset = 8192;                    // partial accumulators, one slot per range
+constexpr size_t kSkSlotsOffset = 16384;                   // partial accumulators, two slots per range
 constexpr size_t kSkSlotBytes = 256 * 256 * sizeof(float);
-constexpr size_t kSkWorkspaceBytes = kSkSlotsOffset + kMaxSkPairs * kSkSlotBytes;
+constexpr size_t kSkWorkspaceBytes = kSkSlotsOffset + 2 * kMaxSkPairs * kSkSlotBytes;
 static_assert(kSkFlagsOffset + kMaxSkPairs * kSkWarpsPerPair * sizeof(uint32_t) <= kSkSlotsOffset, "flags fit");
 struct StreamK {
   int32_t on;
@@ -149,8 +151,11 @@ struct StreamK {
   uint32_t epoch;    // tag of this launch's ticket counts (24 bits, never 0)
   int32_t start_tile[kMaxSkPairs + 1];
   int32_t start_kb[kMaxSkPairs + 1];
-  int16_t first_range[kMaxSkPairs];  // per range: the first non-empty range of its tile
-  int16_t num_parts[kMaxSkPairs];    // per range: the non-empty ranges of its tile
+  // Per range, for the tile of its first item (head) and of its last item
+  // (tail), when that tile is split: the first range covering the tile and
+  // the number of (non-empty) ranges that do.
+  int16_t head_q0[kMaxSkPairs], head_n[kMaxSkPairs];
+  int16_t tail_q0[kMaxSkPairs], tail_n[kMaxSkPairs];
 };
 
 struct GemmParams {
@@ -203,11 +208,19 @@ constexpr int32_t kDevTimeoutEpilogue = 3;
 int tc_gemm_max_smem_bytes();
 // Launches clusters of two CTAs: p.sk.pairs of them when the stream-K tail is
 // on (the kernel's stream-K instance), else as many as fit on the device (at
-// most one per tile); max_pairs_hint is used if the occupancy query fails.
-cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int max_pairs_hint, cudaStream_t stream);
+// most one per tile), with epi_warps epilogue warps per CTA; max_pairs_hint is
+// used if the occupancy query fails.
+cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int epi_warps, int max_pairs_hint,
+                           cudaStream_t stream);
 // Pairs (clusters of two CTAs) of a launch kind that can be resident at once
 // on the current device (0 if the query fails).
 int tc_gemm_max_pairs(int kernel_tag);
+// Epilogue warps per CTA for a launch (8: 32-column chunks and 32 x 32
+// output boxes; 16: 16-column chunks and 32-row x 16-column boxes): 16 for a
+// column or dgrad launch whose activation problems have at most
+// kShortKBlocks K blocks (p.probs[].kblocks must be set).
+constexpr int kShortKBlocks = 8;  // K <= 1024
+int tc_epi_warps_for(const GemmParams& p, int kernel_tag);
 cudaError_t launch_simt_gemm(const GemmParams& p, cudaStream_t stream);
 // The epilogues' activation forms on plain arrays (tpmlp_eval_activation).
 cudaError_t launch_act_eval(int fn, const float* x, const float* y, const float* dh, float* o0, float* o1,

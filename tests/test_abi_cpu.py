@@ -12,7 +12,7 @@ import megatron_tensor_transformer_column_gb300 as tp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "tpmlp.h")
-SK_WORKSPACE = 8192 + 80 * 256 * 256 * 4  # status block, stream-K flags, 80 partial slots
+SK_WORKSPACE = 16384 + 160 * 256 * 256 * 4  # status block, stream-K ticket counters, 2 partial slots per range
 
 
 @pytest.fixture(scope="module")
@@ -196,9 +196,9 @@ def test_sp_no_cpu_fallback_without_gpu(lib):
 
 def test_stream_k_mode_validation(lib):
     p = tp.Plan(512, 64, [64], "gelu", "bf16")
-    for mode in (tp.STREAM_K_OFF, tp.STREAM_K_ALWAYS, tp.STREAM_K_AUTO):
+    for mode in (tp.STREAM_K_OFF, tp.STREAM_K_ALWAYS, tp.STREAM_K_AUTO, tp.STREAM_K_BALANCE):
         tp.tpmlp_plan_set_stream_k(p, mode)
-    for bad in (-1, 3, 100):
+    for bad in (-1, 4, 100):
         with pytest.raises(tp.TpmlpError) as e:
             tp.tpmlp_plan_set_stream_k(p, bad)
         assert e.value.status == 1

@@ -102,6 +102,16 @@ def test_stream_k_always_bf16_all_outputs(gpu_lib, act, case):
 
 
 @pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("case", SK_CASES, ids=[f"T{c[0]}_d{c[1]}_t{len(c[2])}" for c in SK_CASES])
+def test_stream_k_balance_bf16_all_outputs(gpu_lib, act, case):
+    """Every launch spread evenly over the pairs: ranges that end inside one
+    tile, cover whole tiles and start inside another (two parts per range),
+    the weight-gradient tiles placed after the short ones."""
+    T, d, d_i = case
+    _full_compare(gpu_lib, T, d, d_i, act, "bf16", stream_k=gpu_lib.STREAM_K_BALANCE)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
 def test_stream_k_deterministic_and_within_bound_of_round_robin(gpu_lib, act):
     """The parts of a split tile are added in a fixed order: two runs agree bit
     for bit.  Against plain round robin (one K loop per tile) only the fp32
@@ -109,16 +119,21 @@ def test_stream_k_deterministic_and_within_bound_of_round_robin(gpu_lib, act):
     T, d, d_i = 1024, 384, (512, 384, 640, 256)
     inp = si.make_inputs(T, d, d_i, act, "bf16", seed=77)
     runs = [run_gpu(gpu_lib, inp, act, "bf16", stream_k=m)
-            for m in (gpu_lib.STREAM_K_ALWAYS, gpu_lib.STREAM_K_ALWAYS, gpu_lib.STREAM_K_OFF)]
+            for m in (gpu_lib.STREAM_K_ALWAYS, gpu_lib.STREAM_K_ALWAYS, gpu_lib.STREAM_K_OFF,
+                      gpu_lib.STREAM_K_BALANCE, gpu_lib.STREAM_K_BALANCE)]
     keys = ("Y", "dX")
     lists = ("dW1", "dW2", "H", "saved", "dact") + (("dW3",) if act == "swiglu" else ())
     for k in keys:
         assert torch.equal(runs[0][k], runs[1][k]), k
+        assert torch.equal(runs[3][k], runs[4][k]), k
         assert rel_err(to_np(runs[0][k]), to_np(runs[2][k])) <= 1e-2, k
+        assert rel_err(to_np(runs[3][k]), to_np(runs[2][k])) <= 1e-2, k
     for k in lists:
-        for a, b, c in zip(runs[0][k], runs[1][k], runs[2][k]):
+        for a, b, c, e, f in zip(runs[0][k], runs[1][k], runs[2][k], runs[3][k], runs[4][k]):
             assert torch.equal(a, b), k
+            assert torch.equal(e, f), k
             assert rel_err(to_np(a), to_np(c)) <= 1e-2, k
+            assert rel_err(to_np(e), to_np(c)) <= 1e-2, k
 
 
 def test_config_C1_fp32(gpu_lib):
@@ -135,28 +150,33 @@ def test_config_C1_fp32(gpu_lib):
 # Tiles the stream-K tail split in the run (tpmlp_last_split_tiles) get a row
 # in each of their eight warp slots (or their units, for weight gradients).
 
-def _split_samples(tp, w, rows, units):
-    """Add rows / units covering every tile the stream-K tail split in the last
-    four launches.  Returns (rows, units, split) with split = {launch: tiles}."""
-    t = len(w.d_i)
+def _split_samples(tp, w, g, rows, units):
+    """Add rows / units covering every tile the stream-K schedule split in the
+    last four launches.  A split tile is identified by its output tensor (the
+    address the launch reports).  Returns (rows, units, split) with
+    split = {launch: tiles}."""
     offs = [lo for lo, _ in si.shard_slices(w.d_i)]
+    token_out = {g["Y"].data_ptr(), g["dX"].data_ptr()} | {x.data_ptr() for x in g["saved"] + g["dact"]}
+    dw_rows = {x.data_ptr(): i for i, x in enumerate(g["dW2"])}                    # rows are shard units
+    dw_cols = {x.data_ptr(): i for i, x in enumerate(g["dW1"] + (g["dW3"] or []))}  # columns are shard units
     split = {k: tp.tpmlp_last_split_tiles(k) for k in
              (tp.LAUNCH_FWD_COLUMN, tp.LAUNCH_FWD_ROW, tp.LAUNCH_BWD_DGRAD, tp.LAUNCH_BWD_FSUM)}
     add_r, add_u = [], []
-    nw = 3 if w.act == "swiglu" else 2  # weight-gradient problem groups ahead of dX in the f-sum launch
-    for kind, tiles in split.items():
-        for prob, m0, n0 in tiles:
-            if kind in (tp.LAUNCH_FWD_COLUMN, tp.LAUNCH_FWD_ROW) or (kind == tp.LAUNCH_BWD_DGRAD and prob >= t):
-                add_r += band_rows(w.T, m0 // TILE)  # token rows: A / H, Y, dact
-            elif kind == tp.LAUNCH_BWD_DGRAD:  # dW2_prob: rows m0.. of the shard
-                hi = offs[prob] + w.d_i[prob]
-                add_u += [u for u in (offs[prob] + m0, offs[prob] + m0 + 97, offs[prob] + m0 + 255) if u < hi]
-            elif prob >= (nw - 1) * t:  # dX
+    t = len(w.d_i)
+    for tiles in split.values():
+        for _, m0, n0, out in tiles:
+            if out in token_out:
                 add_r += band_rows(w.T, m0 // TILE)
-            else:  # dW1_i / dW3_i: columns n0.. of shard i
-                i = prob % t
-                hi = offs[i] + w.d_i[i]
-                add_u += [u for u in (offs[i] + n0, offs[i] + n0 + 131, offs[i] + n0 + 255) if u < hi]
+            elif out in dw_rows:
+                i = dw_rows[out]
+                lo, hi = offs[i], offs[i] + w.d_i[i]
+                add_u += [u for u in (lo + m0, lo + m0 + 97, lo + m0 + 255) if u < hi]
+            elif out in dw_cols:
+                i = dw_cols[out] % t
+                lo, hi = offs[i], offs[i] + w.d_i[i]
+                add_u += [u for u in (lo + n0, lo + n0 + 131, lo + n0 + 255) if u < hi]
+            else:
+                raise AssertionError(f"split tile of an unknown output {out:#x}")
     rows = np.union1d(rows, np.asarray(add_r, dtype=np.int64))
     units = np.union1d(units, np.asarray(add_u, dtype=np.int64))
     return rows, units, split
@@ -171,7 +191,7 @@ def _sampled_compare(tp, w: si.Workload, seed=1234, extra_rows=(), stream_k=None
     rows = np.union1d(rows, np.asarray(extra_rows, dtype=np.int64))
     if units is None:
         units = tile_units(w.d_i)
-    rows, units, split = _split_samples(tp, w, rows, units)
+    rows, units, split = _split_samples(tp, w, g, rows, units)
     Yr, dXr, inter = oracle.rows(inp.X, inp.W1, inp.W2, inp.dY, rows, act=w.act, W3=inp.W3, intermediates=True)
     c1, c3, c2 = oracle.wgrad_units(inp.X, inp.W1, inp.W2, inp.dY, units, act=w.act, W3=inp.W3)
     t = len(w.d_i)
@@ -249,6 +269,13 @@ def test_workload_sampled_parity_stream_k_always(gpu_lib, name):
     """The stream-K tail on every launch of the workload (C4: SwiGLU with
     merged N = 256 MMAs; C2: tiles split across many pairs)."""
     _sampled_compare(gpu_lib, si.WORKLOADS[name], stream_k=gpu_lib.STREAM_K_ALWAYS)
+
+
+@pytest.mark.parametrize("name", ["C3", "C4"])
+def test_workload_sampled_parity_stream_k_balance(gpu_lib, name):
+    """Every launch of a large workload spread evenly over the pairs (auto mode
+    spreads only launches whose weight-gradient operands fit in L2, as C2's)."""
+    _sampled_compare(gpu_lib, si.WORKLOADS[name], stream_k=gpu_lib.STREAM_K_BALANCE)
 
 
 def _run_for_invariance(tp, inp, act, d_i):
