@@ -51,14 +51,8 @@ __global__ void __launch_bounds__(kThreads) tpmlp_fp32_simt_gemm(const __grid_co
   int g = 0;
   while (g + 1 < p.num_groups && tile >= p.groups[g + 1].tile_start) ++g;
   const Group& G = p.groups[g];
-  const int local = tile - G.tile_start;
-  const int full_band = G.band_m * G.tiles_per_row;
-  const int band = local / full_band;
-  const int m_first = band * G.band_m;
-  const int bm = min(G.band_m, G.tiles_m - m_first);
-  const int r = local - band * full_band;
-  int n_lin = r / bm;
-  const int mt = m_first + (r - n_lin * bm);
+  int mt, n_lin;
+  group_tile(G, tile - G.tile_start, mt, n_lin);
   int pi = G.first_prob;
   while (n_lin >= p.probs[pi].tiles_n) {
     n_lin -= p.probs[pi].tiles_n;
