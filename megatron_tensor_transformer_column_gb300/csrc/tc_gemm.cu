@@ -31,8 +31,12 @@
 // and the f/g table.)
 //
 // One body, two schedules (template parameter kSK):
-//   * data-parallel: pair q computes tiles q, q + pairs, q + 2 pairs, ...;
-//   * stream-K tail: the same for the launch's full waves, then each pair
+//   * data-parallel: pair q computes tiles q, q + pairs, q + 2 pairs, ...,
+//     or, in a launch that places long-K weight-gradient tiles first, the
+//     deal described at Deal (tpmlp_internal.h), which hands the pairs that
+//     drew one long tile fewer a head of short tiles first; a long-K tile
+//     (Prob::k_rev) walks its K blocks backwards in odd waves;
+//   * stream-K tail: round robin for the launch's full waves, then each pair
 //     takes one item of the last, partial wave: a range of one tile's K
 //     blocks (a part).  Every part leaves its fp32 accumulator in the
 //     workspace and takes a ticket; the part whose ticket is the last one
@@ -65,7 +69,8 @@ struct Item {
 template <bool kSK>
 struct Sched {
   Item it;
-  int dp;              // next data-parallel tile
+  Deal deal;           // this pair's walk over the data-parallel tiles
+  int pair;
   int r;               // stream-K: this pair's range
   int sk_tile, sk_kb;  // stream-K: next position in that range
   bool in_dp;
@@ -75,10 +80,10 @@ template <bool kSK>
 __device__ __forceinline__ void sched_next(Sched<kSK>& s, const GemmParams& p, int npairs) {
   const int dp_end = kSK ? p.sk.dp_tiles : p.total_tiles;
   if (!kSK || s.in_dp) {
-    if (s.dp < dp_end) {
-      s.it.tile = s.dp;
-      s.dp += npairs;
-      s.it.ti = decode_tile(p, s.it.tile);
+    const int t = deal_next(s.deal, p.deal_long, p.deal_s0, s.pair, npairs, dp_end);
+    if (t >= 0) {
+      s.it.tile = t;
+      s.it.ti = decode_tile(p, s.it.tile, npairs);
       s.it.kb0 = 0;
       s.it.kb1 = p.probs[s.it.ti.prob].kblocks;
       s.it.split = false;
@@ -99,7 +104,7 @@ __device__ __forceinline__ void sched_next(Sched<kSK>& s, const GemmParams& p, i
   const int end_tile = p.sk.start_tile[s.r + 1], end_kb = p.sk.start_kb[s.r + 1];
   while (s.sk_tile < end_tile || (s.sk_tile == end_tile && s.sk_kb < end_kb)) {
     const int t = s.sk_tile;
-    const TileInfo ti = decode_tile(p, t);
+    const TileInfo ti = decode_tile(p, t, 0);
     const int kbt = p.probs[ti.prob].kblocks;
     const int kb0 = s.sk_kb, kb1 = t == end_tile ? end_kb : kbt;
     s.sk_tile = t + 1;
@@ -119,7 +124,8 @@ __device__ __forceinline__ void sched_next(Sched<kSK>& s, const GemmParams& p, i
 // pair < 0: an empty schedule.
 template <bool kSK>
 __device__ __forceinline__ void sched_init(Sched<kSK>& s, const GemmParams& p, int pair, int npairs) {
-  s.dp = pair < 0 ? INT_MAX : pair;
+  deal_init(s.deal, pair);
+  s.pair = pair;
   s.r = pair < 0 ? -1 : npairs - 1 - pair;
   s.in_dp = true;
   sched_next(s, p, npairs);
@@ -180,10 +186,32 @@ __device__ __forceinline__ void stripe_advance(const GemmParams& p, int k0, int&
   }
 }
 
+// The stripe holding token row k0, from scratch (a reversed K walk).
+__device__ __forceinline__ void stripe_at(const GemmParams& p, int k0, int& sj, int& y0, int& next) {
+  sj = stripe_of(p.stripes, k0);
+  y0 = static_cast<int>(p.stripes.row0[sj]);
+  next = sj + 1 < p.stripes.num ? static_cast<int>(p.stripes.row0[sj + 1]) : INT_MAX;
+}
+
 template <bool kSK>
 __device__ __forceinline__ void cursor_stripes(Cursor<kSK>& c, const GemmParams& p) {
-  if (c.a_striped && c.a_major == MAJOR_MN) stripe_advance(p, c.kb * kBK, c.a_sj, c.a_y0, c.a_next);
-  if (c.b_striped && c.b_major == MAJOR_MN) stripe_advance(p, c.kb * kBK, c.b_sj, c.b_y0, c.b_next);
+  const bool rev = c.s.it.ti.rev;
+  if (c.a_striped && c.a_major == MAJOR_MN) {
+    if (rev) stripe_at(p, c.kb * kBK, c.a_sj, c.a_y0, c.a_next);
+    else stripe_advance(p, c.kb * kBK, c.a_sj, c.a_y0, c.a_next);
+  }
+  if (c.b_striped && c.b_major == MAJOR_MN) {
+    if (rev) stripe_at(p, c.kb * kBK, c.b_sj, c.b_y0, c.b_next);
+    else stripe_advance(p, c.kb * kBK, c.b_sj, c.b_y0, c.b_next);
+  }
+}
+
+// A reversed walk enters a segment at its last K block.
+template <bool kSK>
+__device__ __forceinline__ void cursor_segment_last(Cursor<kSK>& c, const GemmParams& p) {
+  cursor_segment(c, p);
+  c.kb = c.kblocks - 1;
+  cursor_stripes(c, p);
 }
 
 // Set the cursor on the first K block of its schedule's current item.
@@ -201,8 +229,13 @@ __device__ __forceinline__ void cursor_item(Cursor<kSK>& c, const GemmParams& p,
   c.n0 = ti.n0 + ps.half * static_cast<int>(rank);
   c.a_major = P.a_major;
   c.b_major = P.b_major;
-  c.seg = P.seg_begin;
   c.left = c.s.it.kb1 - c.s.it.kb0;
+  if (ti.rev) {  // a whole tile (kb0 = 0), its segments and K blocks last to first
+    c.seg = P.seg_begin + P.seg_count - 1;
+    cursor_segment_last(c, p);
+    return;
+  }
+  c.seg = P.seg_begin;
   int skip = c.s.it.kb0;
   cursor_segment(c, p);
   if (kSK) {
@@ -223,6 +256,15 @@ __device__ __forceinline__ void cursor_next(Cursor<kSK>& c, const GemmParams& p,
   if (--c.left == 0) {
     sched_next(c.s, p, npairs);
     cursor_item(c, p, rank);
+    return;
+  }
+  if (c.s.it.ti.rev) {
+    if (--c.kb >= 0) {
+      cursor_stripes(c, p);
+      return;
+    }
+    --c.seg;
+    cursor_segment_last(c, p);
     return;
   }
   if (++c.kb < c.kblocks) {
@@ -584,6 +626,11 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
           }
         }
         int k0 = skip * kBK;
+        if (ti.rev) {  // a whole tile walked last to first: start at the last segment's last block
+          sg = P.seg_begin + P.seg_count - 1;
+          K = p.segs[sg].K;
+          k0 = (K - 1) / kBK * kBK;
+        }
         for (int left = it.kb1 - it.kb0; left > 0; --left) {
           if (!bounded_wait(full_bar(stage), phase, ctl, kDevTimeoutMma)) {
             ok = false;
@@ -599,10 +646,18 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
             stage = 0;
             phase ^= 1u;
           }
-          k0 += kBK;
-          if (k0 >= K && left > 1) {
-            K = p.segs[++sg].K;
-            k0 = 0;
+          if (ti.rev) {
+            k0 -= kBK;
+            if (k0 < 0 && left > 1) {
+              K = p.segs[--sg].K;
+              k0 = (K - 1) / kBK * kBK;
+            }
+          } else {
+            k0 += kBK;
+            if (k0 >= K && left > 1) {
+              K = p.segs[++sg].K;
+              k0 = 0;
+            }
           }
         }
         if (!ok) break;
@@ -831,16 +886,20 @@ int tc_gemm_max_pairs(int tag) {
   return n;
 }
 
+int tc_gemm_grid_pairs(const GemmParams& p, int kernel_tag, int max_pairs_hint) {
+  int pairs = tc_gemm_max_pairs(kernel_tag);
+  if (pairs <= 0) pairs = max_pairs_hint > 0 ? max_pairs_hint : 1;
+  return pairs < p.total_tiles ? pairs : p.total_tiles;
+}
+
 cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int epi_warps, int max_pairs_hint,
                            cudaStream_t stream) {
   KernelFn k = kernel_for(kernel_tag, p.sk.on != 0, epi_warps);
   if (!k) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  int pairs = tc_gemm_max_pairs(kernel_tag);
-  if (pairs <= 0) pairs = max_pairs_hint > 0 ? max_pairs_hint : 1;
-  pairs = pairs < p.total_tiles ? pairs : p.total_tiles;
-  if (p.sk.on) pairs = p.sk.pairs;  // the stream-K ranges were cut for exactly this many pairs
+  // the stream-K ranges were cut for exactly p.sk.pairs pairs
+  const int pairs = p.sk.on ? p.sk.pairs : tc_gemm_grid_pairs(p, kernel_tag, max_pairs_hint);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(threads_for(epi_warps), 1, 1);

@@ -57,14 +57,17 @@ static_assert(kNumAcc * kAccCols <= kTmemCols, "TMEM budget");
 
 struct TileInfo {
   int prob, m0, n0, valid_m, valid_n;
+  int rev;  // walk the K blocks last to first (see Prob::k_rev)
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
+// wave: the pairs of the launch, or 0 for a stream-K part (never reversed).
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, int wave) {
   int g = 0;
   while (g + 1 < p.num_groups && tile >= p.groups[g + 1].tile_start) ++g;
   const Group& G = p.groups[g];
+  const int local = tile - G.tile_start;
   int mt, n_lin;
-  group_tile(G, tile - G.tile_start, mt, n_lin);
+  group_tile(G, local, mt, n_lin);
   int pi = G.first_prob;
   while (n_lin >= p.probs[pi].tiles_n) {
     n_lin -= p.probs[pi].tiles_n;
@@ -77,6 +80,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
   t.n0 = n_lin * P.tile_n;
   t.valid_m = min(kPairM, P.M - t.m0);
   t.valid_n = min(P.tile_n, P.N - t.n0);
+  t.rev = P.k_rev && wave > 0 && ((local / wave) & 1);
   return t;
 }
 

@@ -167,6 +167,7 @@ struct Builder {
   bool map_error = false;
   int cur_group = -1;
   int long_from = -1;  // first tile of the long-K groups placed last (balanced stream-K), or -1
+  int long_end = 0;    // tiles [0, long_end) are long-K groups placed first (see Deal)
 
   explicit Builder(GemmParams* params, bool tensor_cores) : p(params), tc(tensor_cores) {
     std::memset(static_cast<void*>(p), 0, sizeof(GemmParams));
@@ -353,6 +354,18 @@ int band_for(int sms) {
   return b;
 }
 
+// Band height of a short-K group (K = d: the column GEMM, dgrad, the QKV
+// projection, dO): taller bands read each B panel fewer times (once per
+// band), as long as the band's A panels (256 rows x K each) stay in L2 while
+// the band sweeps N: about 24 MB of them, between the square band and 32.
+// Measured on GB300: C5's column launch (K = 3072) reads 724 MB from DRAM
+// with bands of 8, 477 MB with 16, 538 MB with 24, 945 MB with 32.
+int band_short(int sms, int64_t K) {
+  const int64_t panel = int64_t{kTileM} * K * 2;  // a pair's 256 rows of A, bf16
+  const int64_t fit = (int64_t{24} << 20) / std::max<int64_t>(panel, 1);
+  return std::max(band_for(sms), static_cast<int>(std::min<int64_t>(32, fit)));
+}
+
 // Tile -> problem and its first output row and column, as the kernel's
 // decode_tile maps it.
 int tile_prob(const GemmParams& p, int tile, int* m0 = nullptr, int* n0 = nullptr) {
@@ -417,11 +430,65 @@ void finish_ranges(GemmParams& p, int pairs, const std::vector<int32_t>& kb, std
 }
 
 // Estimated cost of a tile in K blocks: its main loop, or its epilogue when
-// that is longer (about 20 K blocks for an activation epilogue of a 256 x 256
-// tile, 4 for a plain store; measured on GB300 on short-K launches).
+// that is longer (about 14 K blocks for an activation epilogue of a 256 x 256
+// tile, 4 for a plain store; measured on GB300 on the short-K launches of the
+// GPT-2-small shape: a column tile every 9 us, a K block every 0.67 us).
 int64_t tile_cost(const Prob& P, int kb) {
-  const int64_t epi = P.epi == EPI_STORE ? 4 : 20;
+  const int64_t epi = P.epi == EPI_STORE ? 4 : 14;
   return std::max<int64_t>(kb, epi);
+}
+
+// The deal of the data-parallel tiles (see Deal) for a launch whose first
+// long_end tiles are long-K weight-gradient tiles.  The plain round robin
+// leaves pairs 0 .. r - 1 (r = long_end mod P) one long tile ahead; a head of
+// s0 short tiles dealt to the other pairs first evens that out.  s0 runs over
+// whole rounds of those pairs, up to the ratio of the tile costs, and the one
+// with the smallest largest pair load (tile_cost, walked with the kernel's own
+// deal_next) is taken if it saves at least kMinDealSaving K blocks and 1 % of
+// the round robin's.  Any s0 gives the same results: every tile is computed
+// once, by one pair, with the same K order.
+void plan_deal(GemmParams& p, int pairs, int long_end) {
+  p.deal_long = 0;
+  p.deal_s0 = 0;
+  const int n = p.total_tiles;
+  if (long_end <= 0 || long_end >= n || pairs < 2 || n <= pairs) return;
+  const int r = long_end % pairs;
+  if (r == 0) return;  // every pair drew the same number of long tiles
+  std::vector<int64_t> cost(n);
+  int64_t long_max = 0, short_min = INT64_MAX;
+  for (int t = 0; t < n; ++t) {
+    const Prob& P = p.probs[tile_prob(p, t)];
+    cost[t] = tile_cost(P, P.kblocks);
+    if (t < long_end) long_max = std::max(long_max, cost[t]);
+    else short_min = std::min(short_min, cost[t]);
+  }
+  auto makespan = [&](int s0) {
+    int64_t worst = 0;
+    for (int q = 0; q < pairs; ++q) {
+      Deal d;
+      deal_init(d, q);
+      int64_t load = 0;
+      for (int t = deal_next(d, long_end, s0, q, pairs, n); t >= 0; t = deal_next(d, long_end, s0, q, pairs, n))
+        load += cost[t];
+      worst = std::max(worst, load);
+    }
+    return worst;
+  };
+  constexpr int64_t kMinDealSaving = 4;
+  const int64_t rr = makespan(0);
+  int64_t best = rr;
+  int best_s0 = 0;
+  const int rounds = static_cast<int>(long_max / std::max<int64_t>(short_min, 1)) + 1;
+  for (int k = 1; k <= rounds && k * (pairs - r) <= n - long_end; ++k) {
+    const int64_t m = makespan(k * (pairs - r));
+    if (m < best) {
+      best = m;
+      best_s0 = k * (pairs - r);
+    }
+  }
+  if (rr - best < std::max<int64_t>(kMinDealSaving, rr / 100)) return;
+  p.deal_long = long_end;
+  p.deal_s0 = best_s0;
 }
 
 // Cut the stream-K schedule of a tensor-core launch (see StreamK).  Two ways:
@@ -592,6 +659,10 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
       Prob& P = p.probs[i];
       P.kblocks = 0;
       for (int sg = P.seg_begin; sg < P.seg_begin + P.seg_count; ++sg) P.kblocks += (p.segs[sg].K + kTcBK - 1) / kTcBK;
+      // Alternate the K direction by wave where a wave's operands outgrow L2
+      // (measured on GB300, C5: the row launch reads 1.49 -> 1.22 GB from DRAM,
+      // the f-sum launch 2.85 -> 2.51 GB; short-K launches gain nothing).
+      P.k_rev = P.kblocks >= kRevKBlocks ? 1 : 0;
     }
   }
   const int epi_warps = B.tc ? tc_epi_warps_for(p, tag) : 0;
@@ -621,6 +692,7 @@ tpmlp_status launch(Builder& B, int tag, const DeviceInfo& di, const tpmlp_plan*
   p.sk.dp_tiles = p.total_tiles;
   std::vector<int> split_tiles;
   if (B.tc && sk_workspace) plan_stream_k(p, tc_gemm_max_pairs(tag), plan->stream_k, B.long_from, &split_tiles);
+  if (B.tc && !p.sk.on) plan_deal(p, tc_gemm_grid_pairs(p, tag, di.sms / 2), B.long_end);
   std::vector<int64_t>& split = g_last_split[tag];
   split.clear();
   for (int t : split_tiles) {
@@ -739,7 +811,7 @@ tpmlp_status fwd_column(const tpmlp_plan* pl, const DeviceInfo& di, const void* 
     B.set_stripes(pl, X_stripes, pl->d, nullptr, 0);
     X = kStripedIn;
   }
-  B.begin_group(pl->T, band_for(di.sms));
+  B.begin_group(pl->T, band_short(di.sms, pl->d));
   for (int i = 0; i < pl->t; ++i) {
     const int64_t di_ = pl->d_i[i];
     Prob& P = B.add_prob(pl->T, di_, sw ? 128 : 256, MAJOR_K, MAJOR_MN, sw ? EPI_SWIGLU_FWD : EPI_GELU_FWD, di_);
@@ -812,9 +884,12 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
       B.end_group();
     }
   };
-  if (!balanced) add_dw2();
+  if (!balanced) {
+    add_dw2();
+    B.long_end = B.p->total_tiles;
+  }
   // dH_i = dY W2_i^T with act' fused (g backward = identity: every shard reads dY)
-  B.begin_group(pl->T, band);
+  B.begin_group(pl->T, band_short(di.sms, pl->d));
   for (int i = 0; i < pl->t; ++i) {
     const int64_t di_ = pl->d_i[i];
     Prob& P = B.add_prob(pl->T, di_, 256, MAJOR_K, MAJOR_K, sw ? EPI_SWIGLU_BWD : EPI_GELU_BWD, di_);
@@ -917,7 +992,10 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
     }
     B.end_group();
   };
-  if (!balanced) add_wgrads();
+  if (!balanced) {
+    add_wgrads();
+    B.long_end = B.p->total_tiles;
+  }
   // dX = sum_i dA_i W1_i^T (+ dU_i W3_i^T): the f operator's backward sum.
   B.begin_group(pl->T, band);
   Prob& P = B.add_prob(pl->T, pl->d, 256, MAJOR_K, MAJOR_K, EPI_STORE, pl->d);
@@ -951,7 +1029,7 @@ tpmlp_status attn_qkv_fwd(const tpmlp_plan* pl, const DeviceInfo& di, const void
                           void* const* QKV, void* ws, cudaStream_t st) {
   if (pl->T == 0) return TPMLP_OK;
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
-  B.begin_group(pl->T, band_for(di.sms));
+  B.begin_group(pl->T, band_short(di.sms, pl->d));
   for (int i = 0; i < pl->t; ++i) {  // f forward is the identity: every shard reads X
     const int64_t n = pl->d_i[i];
     Prob& P = B.add_prob(pl->T, n, 256, MAJOR_K, MAJOR_MN, EPI_STORE, n);
@@ -1003,9 +1081,12 @@ tpmlp_status attn_out_bwd(const tpmlp_plan* pl, const DeviceInfo& di, const void
       B.end_group();
     }
   };
-  if (!balanced) add_dwo();
+  if (!balanced) {
+    add_dwo();
+    B.long_end = B.p->total_tiles;
+  }
   // dO_i = dZ WO_i^T (g backward is the identity: every shard reads dZ)
-  B.begin_group(pl->T, band);
+  B.begin_group(pl->T, band_short(di.sms, pl->d));
   for (int i = 0; i < pl->t; ++i) {
     const int64_t w = pl->dq_i[i];
     Prob& P = B.add_prob(pl->T, w, 256, MAJOR_K, MAJOR_K, EPI_STORE, w);
@@ -1045,7 +1126,10 @@ tpmlp_status attn_qkv_bwd(const tpmlp_plan* pl, const DeviceInfo& di, const void
     }
     B.end_group();
   };
-  if (!balanced) add_dwqkv();
+  if (!balanced) {
+    add_dwqkv();
+    B.long_end = B.p->total_tiles;
+  }
   // dX = sum_i dQKV_i W_QKV,i^T (= dQ_i WQ_i^T + dK_i WK_i^T + dV_i WV_i^T): the f-sum.
   B.begin_group(pl->T, band);
   Prob& P = B.add_prob(pl->T, pl->d, 256, MAJOR_K, MAJOR_K, EPI_STORE, pl->d);

@@ -87,7 +87,11 @@ struct Prob {
   int32_t out_map[3];  // tensor maps of out0..out2 for TMA stores (-1: none)
   int32_t out_striped; // out0 is the launch's striped output (token stripes)
   int32_t kblocks;     // K blocks of a tile, over all segments (tensor-core path)
-  int32_t pad_;
+  // Long K (tensor-core path): the group's tiles walk their K blocks first to
+  // last in even waves (group-local tile / pairs) and last to first in odd
+  // ones, so a wave starts on the K blocks the previous one read last, which
+  // are still in L2.
+  int32_t k_rev;
   int64_t ldo;       // row stride of out*/aux*, in elements
   void* out0;
   void* out1;
@@ -123,6 +127,54 @@ __host__ __device__ inline void group_tile(const Group& G, int local, int& mt, i
   const int nl = r / bm;
   mt = m_first + (r - nl * bm);
   n_lin = nl;
+}
+
+// The deal of a launch's data-parallel tiles [0, dp_end) to its P pairs.  A
+// launch that mixes K = T weight-gradient tiles with short ones places the
+// long tiles first, tiles [0, nl): they go round robin over all pairs, so
+// pairs r = nl mod P .. P - 1 draw one long tile fewer.  Of the short tiles
+// after them, the first s0 go round robin over those pairs only, the rest
+// round robin over all pairs from pair r on.  With s0 = 0 this is the plain
+// round robin, tile i to pair i mod P.  One pair walks its tiles with a Deal
+// cursor; the host planner runs the same walk to cost a choice of s0.
+struct Deal {
+  int phase;  // 0: long tiles, 1: the head of the short tiles, 2: the rest, 3: done
+  int next;   // the phase's next index
+};
+
+__host__ __device__ inline void deal_init(Deal& d, int pair) {
+  d.phase = pair < 0 ? 3 : 0;
+  d.next = pair;
+}
+
+// This pair's next tile, or -1.
+__host__ __device__ inline int deal_next(Deal& d, int nl, int s0, int pair, int npairs, int dp_end) {
+  const int r = nl % npairs;
+  if (d.phase == 0) {
+    if (d.next < nl && d.next < dp_end) {
+      const int t = d.next;
+      d.next += npairs;
+      return t;
+    }
+    d.phase = 1;
+    d.next = pair - r;  // negative: this pair drew one long tile more, no head tiles
+  }
+  if (d.phase == 1) {
+    if (d.next >= 0 && d.next < s0 && nl + d.next < dp_end) {
+      const int t = nl + d.next;
+      d.next += npairs - r;
+      return t;
+    }
+    d.phase = 2;
+    d.next = s0 + (pair - r + npairs) % npairs;
+  }
+  if (d.phase == 2 && nl + d.next < dp_end) {
+    const int t = nl + d.next;
+    d.next += npairs;
+    return t;
+  }
+  d.phase = 3;
+  return -1;
 }
 
 // Token stripes of the sequence-parallel layout: stripe j holds rows
@@ -184,6 +236,7 @@ struct GemmParams {
   Seg segs[kMaxSegs];
   int32_t num_maps, num_probs, num_groups, num_segs;
   int32_t total_tiles;
+  int32_t deal_long, deal_s0;  // the deal of the data-parallel tiles (see Deal); 0, 0: round robin
   int32_t tile_m;
   int32_t* status;          // device status word (workspace)
   uint64_t timeout_ns;      // bound on every wait inside the kernel
@@ -232,11 +285,16 @@ cudaError_t launch_tc_gemm(const GemmParams& p, int kernel_tag, int epi_warps, i
 // Pairs (clusters of two CTAs) of a launch kind that can be resident at once
 // on the current device (0 if the query fails).
 int tc_gemm_max_pairs(int kernel_tag);
+// The pairs launch_tc_gemm launches for p when the stream-K tail is off.
+int tc_gemm_grid_pairs(const GemmParams& p, int kernel_tag, int max_pairs_hint);
 // Epilogue warps per CTA for a launch (8: 32-column chunks and 32 x 32
 // output boxes; 16: 16-column chunks and 32-row x 16-column boxes): 16 for a
 // column or dgrad launch whose activation problems have at most
 // kShortKBlocks K blocks (p.probs[].kblocks must be set).
 constexpr int kShortKBlocks = 8;  // K <= 1024
+// Problems of at least this many K blocks alternate their K direction by wave
+// (Prob::k_rev).
+constexpr int kRevKBlocks = 48;  // K > 6016
 int tc_epi_warps_for(const GemmParams& p, int kernel_tag);
 cudaError_t launch_simt_gemm(const GemmParams& p, cudaStream_t stream);
 // The epilogues' activation forms on plain arrays (tpmlp_eval_activation).
