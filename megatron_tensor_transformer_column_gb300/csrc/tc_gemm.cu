@@ -80,7 +80,7 @@ template <bool kSK>
 __device__ __forceinline__ void sched_next(Sched<kSK>& s, const GemmParams& p, int npairs) {
   const int dp_end = kSK ? p.sk.dp_tiles : p.total_tiles;
   if (!kSK || s.in_dp) {
-    const int t = deal_next(s.deal, p.deal_long, p.deal_s0, s.pair, npairs, dp_end);
+    const int t = deal_next(s.deal, p.deal_long, p.deal_r, p.deal_s0, s.pair, npairs, dp_end);
     if (t >= 0) {
       s.it.tile = t;
       s.it.ti = decode_tile(p, s.it.tile, npairs);
@@ -141,6 +141,7 @@ struct Cursor {
   const void* mb;
   const void* mb2;
   int seg, kb, kblocks, left;  // segment, K block in it, its K blocks; K blocks left in the item
+  int dir;                     // +1, or -1 for a reversed walk (TileInfo::rev)
   int a_major, b_major, dual;
   int a_striped, b_striped;  // operand read from the launch's token stripes
   int a_sj, b_sj;            // its current stripe,
@@ -230,6 +231,7 @@ __device__ __forceinline__ void cursor_item(Cursor<kSK>& c, const GemmParams& p,
   c.a_major = P.a_major;
   c.b_major = P.b_major;
   c.left = c.s.it.kb1 - c.s.it.kb0;
+  c.dir = ti.rev ? -1 : 1;
   if (ti.rev) {  // a whole tile (kb0 = 0), its segments and K blocks last to first
     c.seg = P.seg_begin + P.seg_count - 1;
     cursor_segment_last(c, p);
@@ -258,21 +260,14 @@ __device__ __forceinline__ void cursor_next(Cursor<kSK>& c, const GemmParams& p,
     cursor_item(c, p, rank);
     return;
   }
-  if (c.s.it.ti.rev) {
-    if (--c.kb >= 0) {
-      cursor_stripes(c, p);
-      return;
-    }
-    --c.seg;
-    cursor_segment_last(c, p);
-    return;
-  }
-  if (++c.kb < c.kblocks) {
+  c.kb += c.dir;
+  if (static_cast<unsigned>(c.kb) < static_cast<unsigned>(c.kblocks)) {
     cursor_stripes(c, p);
     return;
   }
-  ++c.seg;
-  cursor_segment(c, p);
+  c.seg += c.dir;
+  if (c.dir < 0) cursor_segment_last(c, p);
+  else cursor_segment(c, p);
 }
 
 // Issue this CTA's box copies for the cursor's K block.
@@ -626,6 +621,7 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
           }
         }
         int k0 = skip * kBK;
+        const int kstep = ti.rev ? -kBK : kBK;
         if (ti.rev) {  // a whole tile walked last to first: start at the last segment's last block
           sg = P.seg_begin + P.seg_count - 1;
           K = p.segs[sg].K;
@@ -646,18 +642,11 @@ __device__ __forceinline__ void tc_gemm_body(const GemmParams& p, uint8_t* smem_
             stage = 0;
             phase ^= 1u;
           }
-          if (ti.rev) {
-            k0 -= kBK;
-            if (k0 < 0 && left > 1) {
-              K = p.segs[--sg].K;
-              k0 = (K - 1) / kBK * kBK;
-            }
-          } else {
-            k0 += kBK;
-            if (k0 >= K && left > 1) {
-              K = p.segs[++sg].K;
-              k0 = 0;
-            }
+          k0 += kstep;
+          if (static_cast<unsigned>(k0) >= static_cast<unsigned>(K) && left > 1) {  // past either end
+            sg += kstep > 0 ? 1 : -1;
+            K = p.segs[sg].K;
+            k0 = kstep > 0 ? 0 : (K - 1) / kBK * kBK;
           }
         }
         if (!ok) break;

@@ -80,7 +80,8 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, i
   t.n0 = n_lin * P.tile_n;
   t.valid_m = min(kPairM, P.M - t.m0);
   t.valid_n = min(P.tile_n, P.N - t.n0);
-  t.rev = P.k_rev && wave > 0 && ((local / wave) & 1);
+  t.rev = 0;
+  if (P.k_rev && wave > 0) t.rev = (local / wave) & 1;  // long-K tiles only: a division per tile
   return t;
 }
 

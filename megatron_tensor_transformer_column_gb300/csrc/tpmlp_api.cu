@@ -450,6 +450,7 @@ int64_t tile_cost(const Prob& P, int kb) {
 void plan_deal(GemmParams& p, int pairs, int long_end) {
   p.deal_long = 0;
   p.deal_s0 = 0;
+  p.deal_r = 0;
   const int n = p.total_tiles;
   if (long_end <= 0 || long_end >= n || pairs < 2 || n <= pairs) return;
   const int r = long_end % pairs;
@@ -468,7 +469,7 @@ void plan_deal(GemmParams& p, int pairs, int long_end) {
       Deal d;
       deal_init(d, q);
       int64_t load = 0;
-      for (int t = deal_next(d, long_end, s0, q, pairs, n); t >= 0; t = deal_next(d, long_end, s0, q, pairs, n))
+      for (int t = deal_next(d, long_end, r, s0, q, pairs, n); t >= 0; t = deal_next(d, long_end, r, s0, q, pairs, n))
         load += cost[t];
       worst = std::max(worst, load);
     }
@@ -489,6 +490,7 @@ void plan_deal(GemmParams& p, int pairs, int long_end) {
   if (rr - best < std::max<int64_t>(kMinDealSaving, rr / 100)) return;
   p.deal_long = long_end;
   p.deal_s0 = best_s0;
+  p.deal_r = r;
 }
 
 // Cut the stream-K schedule of a tensor-core launch (see StreamK).  Two ways:

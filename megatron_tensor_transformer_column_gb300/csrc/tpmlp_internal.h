@@ -147,9 +147,10 @@ __host__ __device__ inline void deal_init(Deal& d, int pair) {
   d.next = pair;
 }
 
-// This pair's next tile, or -1.
-__host__ __device__ inline int deal_next(Deal& d, int nl, int s0, int pair, int npairs, int dp_end) {
-  const int r = nl % npairs;
+// This pair's next tile, or -1 (r = nl mod npairs, computed once: this runs
+// on the kernel's critical path between tiles, where an integer division
+// costs a visible bubble).
+__host__ __device__ inline int deal_next(Deal& d, int nl, int r, int s0, int pair, int npairs, int dp_end) {
   if (d.phase == 0) {
     if (d.next < nl && d.next < dp_end) {
       const int t = d.next;
@@ -166,7 +167,7 @@ __host__ __device__ inline int deal_next(Deal& d, int nl, int s0, int pair, int 
       return t;
     }
     d.phase = 2;
-    d.next = s0 + (pair - r + npairs) % npairs;
+    d.next = s0 + (pair >= r ? pair - r : pair - r + npairs);
   }
   if (d.phase == 2 && nl + d.next < dp_end) {
     const int t = nl + d.next;
@@ -237,6 +238,7 @@ struct GemmParams {
   int32_t num_maps, num_probs, num_groups, num_segs;
   int32_t total_tiles;
   int32_t deal_long, deal_s0;  // the deal of the data-parallel tiles (see Deal); 0, 0: round robin
+  int32_t deal_r;              // deal_long mod the launch's pairs
   int32_t tile_m;
   int32_t* status;          // device status word (workspace)
   uint64_t timeout_ns;      // bound on every wait inside the kernel

@@ -25,15 +25,16 @@ using namespace tpmlp;
 int main(int argc, char** argv) {
   if (argc != 5) return 2;
   const int nl = atoi(argv[1]), s0 = atoi(argv[2]), P = atoi(argv[3]), n = atoi(argv[4]);
+  const int r = nl % P;
   for (int q = 0; q < P; ++q) {
     Deal d;
     deal_init(d, q);
-    for (int t = deal_next(d, nl, s0, q, P, n); t >= 0; t = deal_next(d, nl, s0, q, P, n)) printf("%d ", t);
+    for (int t = deal_next(d, nl, r, s0, q, P, n); t >= 0; t = deal_next(d, nl, r, s0, q, P, n)) printf("%d ", t);
     printf("\n");
   }
   Deal d;
   deal_init(d, -1);  // an empty schedule
-  return deal_next(d, nl, s0, -1, P, n) == -1 ? 0 : 3;
+  return deal_next(d, nl, r, s0, -1, P, n) == -1 ? 0 : 3;
 }
 """
 
