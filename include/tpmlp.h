@@ -188,7 +188,7 @@ TPMLP_API tpmlp_status tpmlp_forward_row(const tpmlp_plan* plan, const void* con
  * 256 bytes (held by every GPU that loads the library until the process
  * exits); the call allocates and frees nothing.  The first call on a device
  * looks up that array's device address (cudaGetSymbolAddress) with the device
- * current; make that first call before any stream capture.  The address is
+ * current.  The address is
  * kept for the life of the process: after a cudaDeviceReset, which destroys
  * the device's context and the array with it, the kept address is stale, and
  * this entry point must not be called again in that process.  Each call clears
