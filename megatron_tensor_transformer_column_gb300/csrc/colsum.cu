@@ -6,14 +6,16 @@
 // the whole Y.)
 //
 // HBM-bound: every input byte is read once.  A cluster of 8 CTAs owns one
-// 128-byte-wide column strip of one matrix and splits its rows into 8
-// chunks.  In a CTA, 8 threads cover a strip row with 16-byte loads and 32
-// row lanes walk the chunk four rows at a time (four independent loads in
-// flight per thread); the 32 lane partials of a column are added in a fixed
-// tree order in shared memory; CTA 0 of the cluster then adds the 8 chunk
-// partials in rank order through distributed shared memory.  The result is
-// the same on every run: no atomics, no global scratch.  A job without a
-// source reads the launch's token stripes (the dY stripes of the
+// column strip of one matrix and splits its rows into 8 chunks.  In a CTA of
+// 256 threads, kLaneThreads threads cover a strip row with 16-byte loads
+// (strips of 128, 64 or 32 bytes) and the other factor, the row lanes, walk
+// the chunk kUnroll rows at a time (independent loads in flight per thread);
+// the lane partials of a column are added in a fixed tree order in shared
+// memory; CTA 0 of the cluster then adds the 8 chunk partials in rank order
+// through distributed shared memory.  The result is the same on every run: no
+// atomics, no global scratch.  The host picks the widest strip that still
+// gives the launch enough CTAs to fill the GPU (colsum_lane_threads).  A job
+// without a source reads the launch's token stripes (the dY stripes of the
 // sequence-parallel layout) as one tensor.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -24,11 +26,8 @@
 namespace tpmlp {
 namespace {
 
-constexpr int kRowLanes = 32;
-constexpr int kLaneThreads = 8;  // 8 x 16 B = one 128-byte strip row
-constexpr int kThreads = kRowLanes * kLaneThreads;
-constexpr int kChunks = 8;       // CTAs per cluster (row chunks of a strip)
-constexpr int kUnroll = 4;
+constexpr int kThreads = 256;
+constexpr int kChunks = 8;  // CTAs per cluster (row chunks of a strip)
 
 template <bool kBf16, int kPer>
 __device__ __forceinline__ void accumulate_row(const void* src, int64_t off, float (&acc)[kPer]) {
@@ -50,9 +49,10 @@ __device__ __forceinline__ void accumulate_row(const void* src, int64_t off, flo
   }
 }
 
-template <bool kBf16>
+template <bool kBf16, int kLaneThreads, int kUnroll>
 __global__ void __launch_bounds__(kThreads) tpmlp_bias_grad_colsum(const __grid_constant__ ColsumParams p) {
   constexpr int kPer = kBf16 ? 8 : 4;  // elements per 16-byte load
+  constexpr int kRowLanes = kThreads / kLaneThreads;
   constexpr int kStripCols = kLaneThreads * kPer;
   __shared__ float part[kRowLanes][kStripCols + 1];
 
@@ -132,9 +132,32 @@ __global__ void __launch_bounds__(kThreads) tpmlp_bias_grad_colsum(const __grid_
 
 }  // namespace
 
-int colsum_strip_cols(bool bf16) { return bf16 ? kLaneThreads * 8 : kLaneThreads * 4; }
+int colsum_strip_cols(bool bf16, int lane_threads) { return lane_threads * (bf16 ? 8 : 4); }
 
-cudaError_t launch_colsum(const ColsumParams& p, bool bf16, cudaStream_t stream) {
+// The launch shape of a set of jobs: lane threads per strip row (strips of
+// 128, 64 or 32 bytes) and rows in flight per thread.  128-byte strips read
+// best (measured on GB300: C5's db2, the column sums of dY, 29 us with 64-byte
+// strips against 23 us with 128-byte ones, both 8 rows ahead); narrower ones
+// only for launches too small to give the GPU a fifth of its slots (8 CTAs
+// per SM) otherwise.  8 rows ahead while the launch leaves slots empty, 4
+// when it fills most of them (C5's db1: 73 us with 4, 76 us with 8).
+ColsumShape colsum_shape(const ColsumJob* jobs, int num_jobs, bool bf16, int sms) {
+  const int64_t slots = int64_t{8} * sms;
+  auto ctas = [&](int lt) {
+    int64_t n = 0;
+    for (int j = 0; j < num_jobs; ++j) n += kChunks * ((jobs[j].cols + colsum_strip_cols(bf16, lt) - 1) / colsum_strip_cols(bf16, lt));
+    return n;
+  };
+  int lt = 2;
+  for (int c : {8, 4})
+    if (ctas(c) * 5 >= slots) {
+      lt = c;
+      break;
+    }
+  return ColsumShape{lt, ctas(lt) * 5 >= slots * 4 ? 4 : 8};
+}
+
+cudaError_t launch_colsum(const ColsumParams& p, bool bf16, ColsumShape shape, cudaStream_t stream) {
   if (p.total_strips <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.total_strips * kChunks, 1, 1);
@@ -148,8 +171,18 @@ cudaError_t launch_colsum(const ColsumParams& p, bool bf16, cudaStream_t stream)
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (bf16) return cudaLaunchKernelEx(&cfg, tpmlp_bias_grad_colsum<true>, p);
-  return cudaLaunchKernelEx(&cfg, tpmlp_bias_grad_colsum<false>, p);
+  const int key = (bf16 ? 100 : 0) + 10 * shape.lane_threads + shape.unroll;
+  switch (key) {
+    case 184: return cudaLaunchKernelEx(&cfg, tpmlp_bias_grad_colsum<true, 8, 4>, p);
+    case 188: return cudaLaunchKernelEx(&cfg, tpmlp_bias_grad_colsum<true, 8, 8>, p);
+    case 148: return cudaLaunchKernelEx(&cfg, tpmlp_bias_grad_colsum<true, 4, 8>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, tpmlp_bias_grad_colsum<true, 2, 8>, p);
+    case 84: return cudaLaunchKernelEx(&cfg, tpmlp_bias_grad_colsum<false, 8, 4>, p);
+    case 88: return cudaLaunchKernelEx(&cfg, tpmlp_bias_grad_colsum<false, 8, 8>, p);
+    case 48: return cudaLaunchKernelEx(&cfg, tpmlp_bias_grad_colsum<false, 4, 8>, p);
+    case 28: return cudaLaunchKernelEx(&cfg, tpmlp_bias_grad_colsum<false, 2, 8>, p);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace tpmlp

@@ -759,8 +759,8 @@ tpmlp_status common_checks(const tpmlp_plan* pl, void* workspace, DeviceInfo* di
 // dst_j[c] = sum over the T rows of src_j[r][c], one launch for all jobs.
 struct ColsumBuilder {
   ColsumParams p{};
-  int strip_cols;
-  explicit ColsumBuilder(bool bf16) : strip_cols(colsum_strip_cols(bf16)) {}
+  bool bf16;
+  explicit ColsumBuilder(bool is_bf16) : bf16(is_bf16) {}
   void set_stripes(const tpmlp_plan* pl, const void* const* src) {
     p.num_stripes = static_cast<int32_t>(pl->stripe_rows.size());
     p.stripe_row0[0] = 0;
@@ -775,14 +775,24 @@ struct ColsumBuilder {
     J.dst = dst;
     J.rows = rows;
     J.cols = static_cast<int32_t>(cols);
-    J.strip_begin = p.total_strips;
-    p.total_strips += static_cast<int32_t>((cols + strip_cols - 1) / strip_cols);
+  }
+  // Cut every job into strips of the width the launch uses.
+  ColsumShape finish(int sms) {
+    const ColsumShape shape = colsum_shape(p.jobs, p.num_jobs, bf16, sms);
+    const int strip_cols = colsum_strip_cols(bf16, shape.lane_threads);
+    p.total_strips = 0;
+    for (int j = 0; j < p.num_jobs; ++j) {
+      p.jobs[j].strip_begin = p.total_strips;
+      p.total_strips += (p.jobs[j].cols + strip_cols - 1) / strip_cols;
+    }
+    return shape;
   }
 };
 
-tpmlp_status launch_colsums(const ColsumBuilder& C, const tpmlp_plan* pl, cudaStream_t st) {
+tpmlp_status launch_colsums(ColsumBuilder& C, const DeviceInfo& di, cudaStream_t st) {
   if (C.p.num_jobs == 0) return TPMLP_OK;
-  cudaError_t e = launch_colsum(C.p, pl->dtype == TPMLP_BF16, st);
+  const ColsumShape shape = C.finish(di.sms);
+  cudaError_t e = launch_colsum(C.p, C.bf16, shape, st);
   if (e != cudaSuccess) return cuda_fail(e);
   ++g_last_launches;
   return TPMLP_OK;
@@ -912,7 +922,7 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
     ColsumBuilder C(pl->dtype == TPMLP_BF16);
     if (dY_stripes) C.set_stripes(pl, dY_stripes);
     C.add(dY_stripes ? nullptr : dY_dense, db2, pl->T, pl->d);
-    TPMLP_TRY(launch_colsums(C, pl, st));
+    TPMLP_TRY(launch_colsums(C, di, st));
   }
   return TPMLP_OK;
 }
@@ -1019,7 +1029,7 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
       if (db1) C.add(dact[i], db1[i], pl->T, pl->d_i[i]);
       if (sw && db3) C.add(dact[pl->t + i], db3[i], pl->T, pl->d_i[i]);
     }
-    TPMLP_TRY(launch_colsums(C, pl, st));
+    TPMLP_TRY(launch_colsums(C, di, st));
   }
   return TPMLP_OK;
 }

@@ -264,8 +264,15 @@ struct ColsumParams {
   int64_t stripe_row0[kMaxStripes + 1];
   const void* stripe_src[kMaxStripes];
 };
-int colsum_strip_cols(bool bf16);
-cudaError_t launch_colsum(const ColsumParams& p, bool bf16, cudaStream_t stream);
+// Columns of a strip with lane_threads 16-byte loads per strip row, and the
+// launch shape (lane threads 8, 4 or 2; rows in flight per thread 4 or 8) of
+// a set of jobs on sms SMs.
+struct ColsumShape {
+  int lane_threads, unroll;
+};
+int colsum_strip_cols(bool bf16, int lane_threads);
+ColsumShape colsum_shape(const ColsumJob* jobs, int num_jobs, bool bf16, int sms);
+cudaError_t launch_colsum(const ColsumParams& p, bool bf16, ColsumShape shape, cudaStream_t stream);
 
 // Kernel parameters live in the 32 KB parameter space (__grid_constant__).
 static_assert(sizeof(GemmParams) <= 32000, "kernel parameter block too large");
