@@ -438,59 +438,146 @@ int64_t tile_cost(const Prob& P, int kb) {
   return std::max<int64_t>(kb, epi);
 }
 
-// The deal of the data-parallel tiles (see Deal) for a launch whose first
-// long_end tiles are long-K weight-gradient tiles.  The plain round robin
-// leaves pairs 0 .. r - 1 (r = long_end mod P) one long tile ahead; a head of
-// s0 short tiles dealt to the other pairs first evens that out.  s0 runs over
-// whole rounds of those pairs, up to the ratio of the tile costs, and the one
-// with the smallest largest pair load (tile_cost, walked with the kernel's own
-// deal_next) is taken if it saves at least kMinDealSaving K blocks and 1 % of
-// the round robin's.  Any s0 gives the same results: every tile is computed
-// once, by one pair, with the same K order.
-void plan_deal(GemmParams& p, int pairs, int long_end) {
-  p.deal_long = 0;
-  p.deal_s0 = 0;
-  p.deal_r = 0;
-  const int n = p.total_tiles;
-  if (long_end <= 0 || long_end >= n || pairs < 2 || n <= pairs) return;
-  const int r = long_end % pairs;
-  if (r == 0) return;  // every pair drew the same number of long tiles
-  std::vector<int64_t> cost(n);
-  int64_t long_max = 0, short_min = INT64_MAX;
-  for (int t = 0; t < n; ++t) {
+// Estimated cost (tile_cost) of every tile of a launch.
+std::vector<int64_t> tile_costs(const GemmParams& p) {
+  std::vector<int64_t> cost(p.total_tiles);
+  for (int t = 0; t < p.total_tiles; ++t) {
     const Prob& P = p.probs[tile_prob(p, t)];
     cost[t] = tile_cost(P, P.kblocks);
+  }
+  return cost;
+}
+
+// Each pair's load (tile_cost) under the deal (long_end, r, s0) of tiles
+// [0, dp_end), walked with the kernel's own deal_next; returns the largest.
+int64_t deal_loads(int pairs, int long_end, int r, int s0, int dp_end, const std::vector<int64_t>& cost,
+                   std::vector<int64_t>* loads = nullptr) {
+  int64_t worst = 0;
+  if (loads) loads->assign(pairs, 0);
+  for (int q = 0; q < pairs; ++q) {
+    Deal d;
+    deal_init(d, q);
+    int64_t load = 0;
+    for (int t = deal_next(d, long_end, r, s0, q, pairs, dp_end); t >= 0;
+         t = deal_next(d, long_end, r, s0, q, pairs, dp_end))
+      load += cost[t];
+    if (loads) (*loads)[q] = load;
+    worst = std::max(worst, load);
+  }
+  return worst;
+}
+
+// The deal of the data-parallel tiles [0, dp_end) (see Deal) for a launch
+// whose first long_end tiles are long-K weight-gradient tiles.  The plain
+// round robin leaves pairs 0 .. r - 1 (r = long_end mod P) one long tile
+// ahead; a head of s0 short tiles dealt to the other pairs first evens that
+// out.  s0 runs over whole rounds of those pairs, up to the ratio of the tile
+// costs, and the one with the smallest largest pair load is taken if it saves
+// at least kMinDealSaving K blocks and 1 % of the round robin's (else s0 = 0:
+// the round robin).  Any s0 gives the same results: every tile is computed
+// once, by one pair, with the same K order.
+struct DealChoice {
+  int long_end = 0, r = 0, s0 = 0;
+  int64_t makespan = 0;  // the largest pair load
+};
+DealChoice choose_deal(int pairs, int long_end, int dp_end, const std::vector<int64_t>& cost) {
+  DealChoice c;
+  c.makespan = deal_loads(pairs, 0, 0, 0, dp_end, cost);  // round robin
+  if (long_end <= 0 || long_end >= dp_end || pairs < 2 || dp_end <= pairs) return c;
+  const int r = long_end % pairs;
+  if (r == 0) return c;  // every pair drew the same number of long tiles
+  int64_t long_max = 0, short_min = INT64_MAX;
+  for (int t = 0; t < dp_end; ++t) {
     if (t < long_end) long_max = std::max(long_max, cost[t]);
     else short_min = std::min(short_min, cost[t]);
   }
-  auto makespan = [&](int s0) {
-    int64_t worst = 0;
-    for (int q = 0; q < pairs; ++q) {
-      Deal d;
-      deal_init(d, q);
-      int64_t load = 0;
-      for (int t = deal_next(d, long_end, r, s0, q, pairs, n); t >= 0; t = deal_next(d, long_end, r, s0, q, pairs, n))
-        load += cost[t];
-      worst = std::max(worst, load);
-    }
-    return worst;
-  };
   constexpr int64_t kMinDealSaving = 4;
-  const int64_t rr = makespan(0);
+  const int64_t rr = c.makespan;
   int64_t best = rr;
   int best_s0 = 0;
   const int rounds = static_cast<int>(long_max / std::max<int64_t>(short_min, 1)) + 1;
-  for (int k = 1; k <= rounds && k * (pairs - r) <= n - long_end; ++k) {
-    const int64_t m = makespan(k * (pairs - r));
+  for (int k = 1; k <= rounds && k * (pairs - r) <= dp_end - long_end; ++k) {
+    const int64_t m = deal_loads(pairs, long_end, r, k * (pairs - r), dp_end, cost);
     if (m < best) {
       best = m;
       best_s0 = k * (pairs - r);
     }
   }
-  if (rr - best < std::max<int64_t>(kMinDealSaving, rr / 100)) return;
-  p.deal_long = long_end;
-  p.deal_s0 = best_s0;
-  p.deal_r = r;
+  if (rr - best < std::max<int64_t>(kMinDealSaving, rr / 100)) return c;
+  c.long_end = long_end;
+  c.r = r;
+  c.s0 = best_s0;
+  c.makespan = best;
+  return c;
+}
+
+void set_deal(GemmParams& p, const DealChoice& c) {
+  p.deal_long = c.long_end;
+  p.deal_r = c.r;
+  p.deal_s0 = c.s0;
+}
+
+void plan_deal(GemmParams& p, int pairs, int long_end) {
+  set_deal(p, DealChoice{});
+  if (long_end <= 0 || long_end >= p.total_tiles || pairs < 2 || p.total_tiles <= pairs) return;
+  set_deal(p, choose_deal(pairs, long_end, p.total_tiles, tile_costs(p)));
+}
+
+// The water level of pair loads `load` after adding L K blocks where the
+// loads are lowest: sum over pairs of max(0, lambda - load) = L (integers).
+int64_t water_level(const std::vector<int64_t>& load, int64_t L) {
+  std::vector<int64_t> sorted(load);
+  std::sort(sorted.begin(), sorted.end());
+  const int pairs = static_cast<int>(sorted.size());
+  int64_t rest = L;
+  for (int i = 0; i < pairs; ++i) {
+    const int64_t cnt = i + 1;  // pairs at or below this level
+    if (i + 1 == pairs || rest <= (sorted[i + 1] - sorted[i]) * cnt) return sorted[i] + rest / cnt;
+    rest -= (sorted[i + 1] - sorted[i]) * cnt;
+  }
+  return sorted.empty() ? 0 : sorted.back();
+}
+
+// Cut the K blocks of tiles [dp_tiles, n), concatenated in tile order, into
+// one range per pair that fills the pair up to the common water level over
+// its data-parallel load (range r belongs to pair pairs - 1 - r).  False if
+// there is nothing to cut.
+bool water_fill(StreamK& sk, int pairs, int dp_tiles, int n, const std::vector<int32_t>& kb,
+                const std::vector<int64_t>& load) {
+  int64_t L = 0;
+  for (int t = dp_tiles; t < n; ++t) L += kb[t];
+  if (L == 0) return false;
+  const int64_t lambda = water_level(load, L);
+  std::vector<int64_t> size(pairs, 0);
+  int64_t given = 0;
+  for (int q = 0; q < pairs; ++q) {
+    size[q] = std::max<int64_t>(0, lambda - load[q]);
+    given += size[q];
+  }
+  for (int q = 0; given < L; q = (q + 1) % pairs)  // the remainder, one K block at a time, to the lowest loads
+    if (load[q] + size[q] <= lambda) {
+      ++size[q];
+      ++given;
+    }
+  int t = dp_tiles, k = 0;
+  for (int r = 0; r < pairs; ++r) {
+    sk.start_tile[r] = t;
+    sk.start_kb[r] = k;
+    int64_t want = size[pairs - 1 - r];
+    while (want > 0 && t < n) {
+      const int64_t take = std::min<int64_t>(want, kb[t] - k);
+      want -= take;
+      k += static_cast<int>(take);
+      if (k == kb[t]) {
+        ++t;
+        k = 0;
+      }
+    }
+  }
+  sk.start_tile[pairs] = n;
+  sk.start_kb[pairs] = 0;
+  sk.dp_tiles = dp_tiles;
+  return true;
 }
 
 // Cut the stream-K schedule of a tensor-core launch (see StreamK).  Two ways:
@@ -510,7 +597,10 @@ void plan_deal(GemmParams& p, int pairs, int long_end) {
 // keeps the plain round robin unless the cut saves at least max(16, 2 %) of
 // a pair's K blocks: measured on GB300, smaller savings were lost to the
 // launch's fixed costs and, under the power cap, to lower clocks in the
-// following launches.
+// following launches.  (Cutting the last wave of a mixed launch -- dealt full
+// waves, the tail water-filled over the dealt loads -- was also measured
+// slower, although the load model promised 1-2 %: C5's f-sum launch 1316 ->
+// 1324 us, C4's 1671 -> 1749 us.)
 //
 // Balanced (long_from >= 0: the host placed the launch's long-K weight-
 // gradient tiles last, from tile long_from on; mode BALANCE, or AUTO when
@@ -543,54 +633,7 @@ void plan_stream_k(GemmParams& p, int pairs, int mode, int long_from, std::vecto
     const int dp_tiles = long_from >= 0 ? long_from : 0;
     std::vector<int64_t> load(pairs, 0);
     for (int t = 0; t < dp_tiles; ++t) load[t % pairs] += tile_cost(p.probs[prob_of[t]], kb[t]);
-    int64_t L = 0;
-    for (int t = dp_tiles; t < n; ++t) L += kb[t];
-    if (L == 0) return;
-    // water level lambda with sum_p max(0, lambda - load_p) = L (integer K blocks)
-    std::vector<int64_t> sorted(load);
-    std::sort(sorted.begin(), sorted.end());
-    int64_t lambda = sorted[0], below = 0;
-    int64_t rest = L;
-    for (int i = 0; i < pairs; ++i) {
-      const int64_t next = i + 1 < pairs ? sorted[i + 1] : INT64_MAX;
-      const int64_t cnt = i + 1;  // pairs at or below this level
-      const int64_t room = next == INT64_MAX ? INT64_MAX : (next - sorted[i]) * cnt;
-      (void)below;
-      if (rest <= room) {
-        lambda = sorted[i] + rest / cnt;
-        break;
-      }
-      rest -= room;
-    }
-    std::vector<int64_t> size(pairs, 0);
-    int64_t given = 0;
-    for (int q = 0; q < pairs; ++q) {
-      size[q] = std::max<int64_t>(0, lambda - load[q]);
-      given += size[q];
-    }
-    for (int q = 0; given < L; q = (q + 1) % pairs)  // the remainder, one K block at a time, to the lowest loads
-      if (load[q] + size[q] <= lambda) {
-        ++size[q];
-        ++given;
-      }
-    // ranges in K-block order; range r belongs to pair pairs - 1 - r
-    int t = dp_tiles, k = 0;
-    for (int r = 0; r < pairs; ++r) {
-      sk.start_tile[r] = t;
-      sk.start_kb[r] = k;
-      int64_t want = size[pairs - 1 - r];
-      while (want > 0 && t < n) {
-        const int64_t take = std::min<int64_t>(want, kb[t] - k);
-        want -= take;
-        k += static_cast<int>(take);
-        if (k == kb[t]) {
-          ++t;
-          k = 0;
-        }
-      }
-    }
-    sk.start_tile[pairs] = n;
-    sk.start_kb[pairs] = 0;
+    if (!water_fill(sk, pairs, dp_tiles, n, kb, load)) return;
     sk.dp_tiles = dp_tiles;
   } else {
     const int dp_tiles = (n / pairs) * pairs;
