@@ -37,12 +37,13 @@ __device__ __forceinline__ void swiglu_grads(float dh, float g, float u, float& 
 // ---- fast packed forms for the bf16 tensor-core epilogues, whose outputs
 // are rounded to bf16 (relative step 2^-8): Phi from the rational
 // approximation of erf by Hastings given as formula 7.1.26 in Abramowitz &
-// Stegun (|error of erf| <= 1.5e-7), with exp(-a^2/2) shared between Phi and
-// the density in GeLU', and the sigmoid from the fast exponential and
-// reciprocal.  Two elements per fp32x2 instruction (fma/mul/add.rn.f32x2):
-// every step but the two special-function calls (reciprocal, exponential)
-// acts on a pair:
-//   q = Phi(-|a|) = 0.5 * poly(t) * exp(-a^2/2), t = 1 / (1 + p |a|);
+// Stegun (|error of erf| <= 1.5e-7), with e = exp(-a^2/2) shared between Phi
+// and the density in GeLU', the exponentials taken as ex2.approx of an
+// argument that carries the log2(e) scale (so e = 1 exactly at a = 0, and
+// GeLU'(0) = 1/2 exactly), and the reciprocals from the fast reciprocal.  Two
+// elements per fp32x2 instruction (fma/mul/add.rn.f32x2): every step but the
+// special-function calls (reciprocal, exponential) acts on a pair:
+//   q = Phi(-|a|) = 0.5 * poly(t) * e, t = 1 / (1 + p |a|), e = 2^(a^2 (-log2(e) / 2));
 //   GeLU(a) = a Phi(a) = max(a, 0) - |a| q;
 //   Phi(a) = 0.5 + copysign(0.5 - q, a),  GeLU'(a) = Phi(a) + a phi(a).
 namespace x2 {
@@ -72,10 +73,25 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
 }
 __device__ __forceinline__ uint64_t splat(float a) { return pk(a, a); }
 
+// 2^y, the hardware approximation (PTX ex2.approx.ftz: relative error about
+// 2^-22; results below 2^-126 flush to zero).
+__device__ __forceinline__ float ex2(float y) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+  return r;
+}
+__device__ __forceinline__ uint64_t ex2_pair(uint64_t y) {
+  float y0, y1;
+  upk(y, y0, y1);
+  return pk(ex2(y0), ex2(y1));
+}
+
+constexpr float kLog2E = 1.44269504088896340736f;
+
 // q = Phi(-|a|) and e = exp(-a^2/2) for a pair; nx = -|a|.
 __device__ __forceinline__ void norm_q(uint64_t a, uint64_t& nx, uint64_t& q, uint64_t& e) {
   constexpr float p = 0.3275911f * kInvSqrt2;
-  // Abramowitz & Stegun 7.1.26 coefficients, halved: q = 0.5 * poly * e
+  // Abramowitz & Stegun 7.1.26 coefficients, halved: q = poly * e
   constexpr float c1 = 0.5f * 0.254829592f, c2 = 0.5f * -0.284496736f, c3 = 0.5f * 1.421413741f,
                   c4 = 0.5f * -1.453152027f, c5 = 0.5f * 1.061405429f;
   float a0, a1;
@@ -90,10 +106,7 @@ __device__ __forceinline__ void norm_q(uint64_t a, uint64_t& nx, uint64_t& q, ui
   poly = fma2(t, poly, splat(c2));
   poly = fma2(t, poly, splat(c1));
   poly = mul2(t, poly);
-  const uint64_t arg = mul2(mul2(a, a), splat(-0.5f));
-  float g0, g1;
-  upk(arg, g0, g1);
-  e = pk(__expf(g0), __expf(g1));
+  e = ex2_pair(mul2(mul2(a, a), splat(-0.5f * kLog2E)));
   q = mul2(poly, e);
 }
 
@@ -131,9 +144,9 @@ __device__ __forceinline__ void gelu_bwd_xn(const float (&acc)[N], float (&a)[N]
   }
 }
 
-// s = sigmoid(g) for a pair.
+// s = sigmoid(g) for a pair: 1 / (1 + 2^(-g log2(e))).
 __device__ __forceinline__ uint64_t sigmoid2(float g0, float g1) {
-  const uint64_t den = add2(splat(1.0f), pk(__expf(-g0), __expf(-g1)));
+  const uint64_t den = add2(splat(1.0f), ex2_pair(mul2(pk(g0, g1), splat(-kLog2E))));
   float d0, d1;
   upk(den, d0, d1);
   return pk(__fdividef(1.0f, d0), __fdividef(1.0f, d1));

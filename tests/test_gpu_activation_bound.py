@@ -11,14 +11,16 @@ act_value / act_grad (fp64) on every point of [-12, 12] in steps of 2^-10,
 plus signed zeros, tiny and huge magnitudes up to the largest float.
 
 Bounds (u = 2^-24, the fp32 unit roundoff; q = Phi(-|a|) = erfc(|a|/sqrt 2)/2):
-  * the fast exponential __expf(x) is within 2 + floor(1.173 |x|) ulp (CUDA's
-    documented bound), the fast reciprocal within 2 ulp; an ulp of a result r
-    is at most 2u |r|;
+  * the exponentials are ex2.approx (relative error about 2^-22, 4u) of an
+    argument that carries the log2(e) scale (a^2 times -log2(e)/2; -g log2(e)
+    for the sigmoid), whose three roundings add a relative error of at most
+    1.5 a^2 u, resp. 2 |g| u, to the result; the fast reciprocal is within
+    2 ulp; an ulp of a result r is at most 2u |r|;
   * q: the approximation is within 7.5e-8 (half of A&S's 1.5e-7, since
     q = erfc / 2); its fp32 evaluation (reciprocal, a Horner chain whose
     condition number is at most 4.5 on t in (0, 1], the exponential of
-    -a^2/2 and the final product) adds at most C_q(a) q with
-    C_q(a) = (64 + 2 a^2) u;
+    -a^2/2 and the final product, about (30 + 1.5 a^2) u in all) adds at most
+    C_q(a) q with C_q(a) = (64 + 2 a^2) u;
   * GeLU(a) = max(a, 0) - |a| q, one fma:  |a| (7.5e-8 + C_q q) + u |GeLU|;
   * GeLU'(a) = 1/2 + sign(a)(1/2 - q) + a phi(a):
         7.5e-8 + C_q q + 2u + |a| phi(a) (8 + 2 a^2) u + 2u |GeLU'|,
