@@ -354,6 +354,16 @@ int band_for(int sms) {
   return b;
 }
 
+// Band height of a weight-gradient group (K = T): the whole M (d, or a
+// shard's width) when it is at most 16 tiles, so that every wave shares the
+// same A panels and the backward K walk of odd waves finds them in L2;
+// measured on GB300: C5's f-sum launch (dW1, 12 M-tiles) 1326 -> 1314 us,
+// C4's (16 M-tiles) 1680 -> 1672 us (bands of 12 there: 1693 us).
+int band_wgrad(int sms, int64_t M) {
+  const int64_t tiles = (M + kTileM - 1) / kTileM;
+  return tiles <= 16 ? static_cast<int>(tiles) : band_for(sms);
+}
+
 // Band height of a short-K group (K = d: the column GEMM, dgrad, the QKV
 // projection, dO): taller bands read each B panel fewer times (once per
 // band), as long as the band's A panels (256 rows x K each) stay in L2 while
@@ -920,7 +930,6 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
     return TPMLP_OK;
   }
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
-  const int band = band_for(di.sms);
   const void* dY_dense = dY;
   if (dY_stripes) {  // all-gather of the dY stripes (backward of the reduce-scatter)
     B.set_stripes(pl, dY_stripes, pl->d, nullptr, 0);
@@ -932,7 +941,7 @@ tpmlp_status bwd_dgrad(const tpmlp_plan* pl, const DeviceInfo& di, const void* c
   auto add_dw2 = [&] {
     for (int i = 0; i < pl->t && !recompute; ++i) {
       const int64_t di_ = pl->d_i[i];
-      B.begin_group(di_, band);
+      B.begin_group(di_, band_wgrad(di.sms, di_));
       Prob& P = B.add_prob(di_, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
       P.out0 = dW2[i];
       B.add_seg(P, H[i], pl->T, di_, dY, pl->T, pl->d, nullptr, pl->T);
@@ -998,7 +1007,7 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
   auto add_dw2 = [&](Builder& B) {
     for (int i = 0; i < pl->t; ++i) {
       const int64_t di_ = pl->d_i[i];
-      B.begin_group(di_, band);
+      B.begin_group(di_, band_wgrad(di.sms, di_));
       Prob& P = B.add_prob(di_, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
       P.out0 = dW2[i];
       B.add_seg(P, H_for_dW2[i], pl->T, di_, dY, pl->T, pl->d, nullptr, pl->T);
@@ -1030,7 +1039,7 @@ tpmlp_status bwd_fsum(const tpmlp_plan* pl, const DeviceInfo& di, const void* X,
   auto add_wgrads = [&] {
     if (with_dw2) add_dw2(B);
     // dW1_i = X^T dA_i (SwiGLU: X^T dG_i) and dW3_i = X^T dU_i
-    B.begin_group(pl->d, band);
+    B.begin_group(pl->d, band_wgrad(di.sms, pl->d));
     for (int i = 0; i < pl->t; ++i) {
       const int64_t di_ = pl->d_i[i];
       Prob& P = B.add_prob(pl->d, di_, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, di_);
@@ -1120,7 +1129,6 @@ tpmlp_status attn_out_bwd(const tpmlp_plan* pl, const DeviceInfo& di, const void
     return TPMLP_OK;
   }
   Builder B(scratch_params(), pl->dtype == TPMLP_BF16);
-  const int band = band_for(di.sms);
   int64_t dq = 0;
   for (int i = 0; i < pl->t; ++i) dq += pl->dq_i[i];
   // dWO_i = O_i^T dZ (K = T): the long tiles go first, or last when the
@@ -1129,7 +1137,7 @@ tpmlp_status attn_out_bwd(const tpmlp_plan* pl, const DeviceInfo& di, const void
   auto add_dwo = [&] {
     for (int i = 0; i < pl->t; ++i) {
       const int64_t w = pl->dq_i[i];
-      B.begin_group(w, band);
+      B.begin_group(w, band_wgrad(di.sms, w));
       Prob& P = B.add_prob(w, pl->d, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, pl->d);
       P.out0 = dWO[i];
       B.add_seg(P, O[i], pl->T, w, dZ, pl->T, pl->d, nullptr, pl->T);
@@ -1172,7 +1180,7 @@ tpmlp_status attn_qkv_bwd(const tpmlp_plan* pl, const DeviceInfo& di, const void
   // spreads them over the pairs
   const bool balanced = balance_long(pl, 2 * (pl->T * pl->d + pl->T * pl->dff + pl->d * pl->dff));
   auto add_dwqkv = [&] {
-    B.begin_group(pl->d, band);
+    B.begin_group(pl->d, band_wgrad(di.sms, pl->d));
     for (int i = 0; i < pl->t; ++i) {
       const int64_t n = pl->d_i[i];
       Prob& P = B.add_prob(pl->d, n, 256, MAJOR_MN, MAJOR_MN, EPI_STORE, n);
