@@ -109,3 +109,16 @@ def test_bias_workload_sampled(gpu_lib, name):
         errs["db3"] = rel_err(np.concatenate([to_np(x) for x in g["db3"]])[units], g3)
     bad = {k: v for k, v in errs.items() if not v <= 2e-2}
     assert not bad, f"{w.name}: {bad} (all {errs})"
+
+
+@pytest.mark.parametrize("dtype,d,d_i", [
+    ("bf16", 8192, (1024, 1024)),  # db2: 128-byte strips, 4 rows ahead; db1: 128-byte strips, 8 rows ahead
+    ("bf16", 1536, (256, 256)),    # db2: 64-byte strips; db1: 32-byte strips
+    ("fp32", 4096, (512, 512)),    # the same four launch shapes with 4-byte elements
+    ("fp32", 768, (128, 128)),
+])
+def test_bias_colsum_launch_shapes(gpu_lib, dtype, d, d_i):
+    """The column sums run in one of four launch shapes chosen by the number
+    of columns (strip width 128, 64 or 32 bytes; 4 or 8 rows in flight); a few
+    tokens and wide matrices reach each of them."""
+    _check(gpu_lib, 16, d, d_i, "gelu", dtype, seed=29)
