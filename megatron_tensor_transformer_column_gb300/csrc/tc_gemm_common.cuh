@@ -253,13 +253,68 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
 // moves a warp's block in a few shared-memory wavefronts and one bulk copy.
 struct EpiStore {
   uint32_t buf;  // this warp's two blocks
-  uint32_t next;
+  uint32_t next; // the block the next store uses (every bulk group reads one block)
   int rows;      // rows of the current problem's outputs
   int sj, sy0;   // striped out0: the stripe of this warp's rows and its first row
 };
 
 template <int N>
 constexpr int epi_block_bytes() { return 32 * N * 2; }
+
+// The swizzled position of 16-byte piece g of row r in a staging block (the
+// output maps' 64- or 32-byte swizzle).
+template <int N>
+__device__ __forceinline__ uint32_t stage_off(int r, int g) {
+  const uint32_t sw = N == 32 ? (static_cast<uint32_t>(r) >> 1) & 3u : (static_cast<uint32_t>(r) >> 2) & 1u;
+  return static_cast<uint32_t>(r) * (2u * N) + ((static_cast<uint32_t>(g) ^ sw) << 4);
+}
+
+// Rows grow0 .. grow0 + 31 (valid_rows of them), columns x .. x + N - 1
+// (nvalid of them) of a row-major bf16 array into staging block blk,
+// coalesced: a warp instruction covers 32 / (N / 8) whole rows.
+template <int N>
+__device__ __forceinline__ void stage_rows(const void* src, int64_t ld, int64_t grow0, int valid_rows, int x,
+                                           int nvalid, uint32_t blk, int lane) {
+  constexpr int P = N / 8;
+  constexpr int RPI = 32 / P;
+  const int g = lane % P;
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    const int r = i * RPI + lane / P;
+    uint4 q = make_uint4(0, 0, 0, 0);
+    if (r < valid_rows && 8 * g < nvalid)
+      q = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(src) + (grow0 + r) * ld + x + 8 * g));
+    ptx::st_shared_v4(blk + stage_off<N>(r, g), q);
+  }
+}
+
+// This thread's row of a staging block as floats.
+template <int N>
+__device__ __forceinline__ void read_row(uint32_t blk, int lane, float (&v)[N]) {
+#pragma unroll
+  for (int g = 0; g < N / 8; ++g) {
+    const uint4 q = ptx::ld_shared_v4(blk + stage_off<N>(lane, g));
+    float2 f;
+    f = unpack_bf16x2(q.x); v[8 * g + 0] = f.x; v[8 * g + 1] = f.y;
+    f = unpack_bf16x2(q.y); v[8 * g + 2] = f.x; v[8 * g + 3] = f.y;
+    f = unpack_bf16x2(q.z); v[8 * g + 4] = f.x; v[8 * g + 5] = f.y;
+    f = unpack_bf16x2(q.w); v[8 * g + 6] = f.x; v[8 * g + 7] = f.y;
+  }
+}
+
+// This thread's row of a staging block from floats (bf16, swizzled).
+template <int N>
+__device__ __forceinline__ void write_row(uint32_t blk, int lane, const float (&v)[N]) {
+#pragma unroll
+  for (int g = 0; g < N / 8; ++g) {
+    uint4 o;
+    o.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
+    o.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
+    o.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
+    o.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
+    ptx::st_shared_v4(blk + stage_off<N>(lane, g), o);
+  }
+}
 
 // Output k (0..2) of problem P: columns x .. x + N - 1 (nvalid of them inside
 // the tensor) of this warp's rows y .. y + 31.
@@ -277,17 +332,7 @@ __device__ __forceinline__ void store_block(EpiStore& es, const GemmParams& p, c
   const uint32_t b = es.buf + es.next * epi_block_bytes<N>();
   if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last used block b has read it
   __syncwarp();
-  const uint32_t row = b + static_cast<uint32_t>(lane) * (2u * N);
-  const uint32_t sw = N == 32 ? (static_cast<uint32_t>(lane) >> 1) & 3u : (static_cast<uint32_t>(lane) >> 2) & 1u;
-#pragma unroll
-  for (int g = 0; g < N / 8; ++g) {
-    uint4 o;
-    o.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
-    o.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
-    o.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
-    o.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
-    ptx::st_shared_v4(row + ((static_cast<uint32_t>(g) ^ sw) << 4), o);
-  }
+  write_row<N>(b, lane, v);
   ptx::fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
@@ -298,37 +343,28 @@ __device__ __forceinline__ void store_block(EpiStore& es, const GemmParams& p, c
 }
 
 // Outputs k0 and k1 of the same chunk through both of the warp's blocks,
-// behind one async-proxy fence (the short-K configuration, N = 16: measured
-// on GB300, 3 % off the GPT-2-small column launch; with N = 32 on the larger
-// shapes it cost 1-2 %, the wait for both blocks outweighing the fence saved).
+// behind one async-proxy fence.  Measured on GB300: the GeLU forward's A and
+// H in the short-K configuration (N = 16), 3 % off the GPT-2-small column
+// launch, but 1-2 % slower with N = 32 on the larger shapes (the wait for both
+// blocks outweighing the fence saved); the SwiGLU backward's dG and dU, whose
+// chunks already wait on two loads, 1.1 % off C4's dgrad launch.
 template <int N>
 __device__ __forceinline__ void store_pair(EpiStore& es, const GemmParams& p, const Prob& P, int k0, int k1, int x,
                                            int y, const float (&v0)[N], const float (&v1)[N], int lane) {
   if (y >= es.rows) return;  // every row of this warp is past the end: no store starts out of range
-  const uint32_t sw = N == 32 ? (static_cast<uint32_t>(lane) >> 1) & 3u : (static_cast<uint32_t>(lane) >> 2) & 1u;
   if (lane == 0) ptx::bulk_wait_group_read<0>();  // both blocks have been read by their last stores
   __syncwarp();
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const float(&v)[N] = h ? v1 : v0;
-    const uint32_t row = es.buf + h * epi_block_bytes<N>() + static_cast<uint32_t>(lane) * (2u * N);
-#pragma unroll
-    for (int g = 0; g < N / 8; ++g) {
-      uint4 o;
-      o.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
-      o.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
-      o.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
-      o.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
-      ptx::st_shared_v4(row + ((static_cast<uint32_t>(g) ^ sw) << 4), o);
-    }
-  }
+  write_row<N>(es.buf, lane, v0);
+  write_row<N>(es.buf + epi_block_bytes<N>(), lane, v1);
   ptx::fence_proxy_async_smem();
   __syncwarp();
-  if (lane == 0) {
+  if (lane == 0) {  // one bulk group per block, block 1 last, as two single stores would leave them
     ptx::tma_store_2d(&p.maps[P.out_map[k0]], es.buf, x, y);
+    ptx::bulk_commit_group();
     ptx::tma_store_2d(&p.maps[P.out_map[k1]], es.buf + epi_block_bytes<N>(), x, y);
     ptx::bulk_commit_group();
   }
+  es.next = 0;
 }
 
 // N bf16 values of row `row` of a row-major array from column col on (the
@@ -391,6 +427,25 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& 
       break;
     }
     case EPI_GELU_BWD: {
+      if (N == 32 && !P.out1 && y < es.rows) {  // A staged through the output block, dA written over it
+        const uint32_t b = es.buf + es.next * epi_block_bytes<N>();
+        if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last used block b has read it
+        __syncwarp();
+        stage_rows<N>(P.aux0, P.ldo, grow - lane, es.rows - y, x, nvalid, b, lane);
+        __syncwarp();
+        float a[N];
+        read_row<N>(b, lane, a);
+        act::x2::gelu_bwd_xn<false>(acc, a, acc);
+        write_row<N>(b, lane, a);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&p.maps[P.out_map[0]], b, x, y);
+          ptx::bulk_commit_group();
+        }
+        es.next ^= 1u;
+        break;
+      }
       float a[N];
       load_row<N>(P.aux0, P.ldo, grow, x, nload, a);
       if (P.out1) {  // recompute H = GeLU(A) for the weight gradient of W2
@@ -404,6 +459,30 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& 
       break;
     }
     case EPI_SWIGLU_BWD: {
+      if (N == 32 && !P.out2 && y < es.rows) {  // G and U staged through both blocks, dG and dU written over them
+        if (lane == 0) ptx::bulk_wait_group_read<0>();
+        __syncwarp();
+        const uint32_t b0 = es.buf, b1 = es.buf + epi_block_bytes<N>();
+        stage_rows<N>(P.aux0, P.ldo, grow - lane, es.rows - y, x, nvalid, b0, lane);
+        stage_rows<N>(P.aux1, P.ldo, grow - lane, es.rows - y, x, nvalid, b1, lane);
+        __syncwarp();
+        float g[N], u[N];
+        read_row<N>(b0, lane, g);
+        read_row<N>(b1, lane, u);
+        act::x2::swiglu_bwd_xn<false>(acc, g, u, acc);
+        write_row<N>(b0, lane, g);
+        write_row<N>(b1, lane, u);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {  // one bulk group per block, as in store_pair
+          ptx::tma_store_2d(&p.maps[P.out_map[0]], b0, x, y);
+          ptx::bulk_commit_group();
+          ptx::tma_store_2d(&p.maps[P.out_map[1]], b1, x, y);
+          ptx::bulk_commit_group();
+        }
+        es.next = 0;
+        break;
+      }
       float g[N], u[N];
       load_row<N>(P.aux0, P.ldo, grow, x, nload, g);
       load_row<N>(P.aux1, P.ldo, grow, x, nload, u);
@@ -411,11 +490,12 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const Prob& 
         float h[N];
         act::x2::swiglu_bwd_xn<true>(acc, g, u, h);
         store_block<N>(es, p, P, 2, x, y, nvalid, h, lane);
-      } else {
+        store_block<N>(es, p, P, 0, x, y, nvalid, g, lane);
+        store_block<N>(es, p, P, 1, x, y, nvalid, u, lane);
+      } else {  // dG and dU behind one fence (C4's dgrad launch: -1.1 % on GB300)
         act::x2::swiglu_bwd_xn<false>(acc, g, u, acc);
+        store_pair<N>(es, p, P, 0, 1, x, y, g, u, lane);
       }
-      store_block<N>(es, p, P, 0, x, y, nvalid, g, lane);
-      store_block<N>(es, p, P, 1, x, y, nvalid, u, lane);
       break;
     }
     default:
