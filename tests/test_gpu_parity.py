@@ -136,6 +136,17 @@ def test_stream_k_deterministic_and_within_bound_of_round_robin(gpu_lib, act):
             assert rel_err(to_np(e), to_np(c)) <= 1e-2, k
 
 
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_deal_of_short_tiles(gpu_lib, act):
+    """A dgrad launch whose three K = T weight-gradient tiles (64 K blocks)
+    come first leaves, on 76 pairs, pairs 0-2 a long tile ahead; the planner
+    deals the first round of the 96 short tiles to pairs 3-75 (the Deal walk's
+    head phase).  Every output element against the oracle: a tile that the
+    walk skipped would show (that each tile is dealt exactly once is checked
+    on the host, test_deal_cpu)."""
+    _full_compare(gpu_lib, 8192, 256, (256, 256, 256), act, "bf16", seed=41)
+
+
 def test_config_C1_fp32(gpu_lib):
     w = si.WORKLOADS["C1"]
     _full_compare(gpu_lib, w.T, w.d, w.d_i, w.act, w.dtype)
