@@ -13,11 +13,12 @@
 //   * warp 1 (one lane, even CTA): allocates 512 TMEM columns in both CTAs,
 //     issues the MMAs into one of two 256-column accumulators and multicasts
 //     its commits (stage free, accumulator ready) to both CTAs;
-//   * warps 2..9 (or 2..17, see kEpiWarpsOf): drain the other accumulator
-//     through tcgen05.ld, apply the epilogue (store, GeLU / SwiGLU forward,
-//     GeLU' / SwiGLU' backward) and write bf16 rows to HBM; the two
-//     accumulators let the epilogue of one tile run under the main loop of
-//     the next.
+//   * warps 2..9 (or 2..17, see tc_epi_warps_for): drain the other
+//     accumulator through tcgen05.ld, apply the epilogue (store, GeLU /
+//     SwiGLU forward, GeLU' / SwiGLU' backward, whose saved pre-activations
+//     come in through the warp's staging blocks) and write bf16 rows to HBM
+//     with TMA stores from those blocks; the two accumulators let the
+//     epilogue of one tile run under the main loop of the next.
 // The MMAs of a stage are issued as straight-line code (issue_stage): on
 // GB300 a branch between two tcgen05.mma instructions cost about a third of
 // the tensor throughput.
